@@ -1,0 +1,261 @@
+"""Pins for the fp64 oracle, each independent of the oracle's own code.
+
+Product-Key Memory, "Factorising the key space": the factorised search is
+exact, so it must equal a brute-force top-k over every full key.  Memory
+Retrieval Mechanisms, top-k retrieval: softmax over the winners, weighted sum
+of their value rows.  Cases: brute force, hand-worked numbers, closed forms,
+exact integer ties, textbook special cases (k = 1 is an argmax, k = n_keys
+reaches every key), and the page's printed operation counts.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def rand_problem(rng, B, H, d_q, n, scale=1.0):
+    q = rng.standard_normal((B, H, d_q)).astype(np.float32)
+    C = (rng.standard_normal((H, 2, n, d_q // 2)) * scale).astype(np.float32)
+    return q, C
+
+
+def brute_python(q, C, k):
+    """Pure-Python exact brute force for integer-valued inputs (no rounding)."""
+    B, H, d_q = q.shape
+    n = C.shape[2]
+    hd = d_q // 2
+    res = np.empty((B, H, k), np.int64)
+    for b in range(B):
+        for h in range(H):
+            qq = [int(x) for x in q[b, h]]
+            keys = []
+            for a in range(n):
+                for c in range(n):
+                    key = [int(x) for x in C[h, 0, a]] + [int(x) for x in C[h, 1, c]]
+                    s = sum(x * y for x, y in zip(qq, key))
+                    keys.append((-s, a * n + c))
+            keys.sort()
+            res[b, h] = [f for _, f in keys[:k]]
+    return res
+
+
+def test_hand_worked_example():
+    # d_q = 2 (one element per half), n_keys = 3, k = 2.
+    # s1 = q1 * C1 = 2 * [1, 3, 2] = [2, 6, 4];  s2 = q2 * C2 = 1 * [0, -1, 5].
+    # Per-half top-2: half 1 -> a = 1 (6), a = 2 (4); half 2 -> b = 2 (5), b = 0 (0).
+    # Candidates: (1,2) 11 flat 5; (1,0) 6 flat 3; (2,2) 9 flat 8; (2,0) 4 flat 6.
+    # Top-2: flat 5 (11), flat 8 (9).  Softmax: 1/(1+e^-2), e^-2/(1+e^-2).
+    q = np.array([[[2.0, 1.0]]], np.float32)
+    C = np.array([[[[1.0], [3.0], [2.0]], [[0.0], [-1.0], [5.0]]]], np.float32)
+    r = oracle.lookup(q, C, 1, 1, 2, 3, 2)
+    assert r["idx"].tolist() == [[[5, 8]]]
+    assert r["score"].tolist() == [[[11.0, 9.0]]]
+    w0 = 1.0 / (1.0 + math.exp(-2.0))
+    assert r["w"][0, 0, 0] == pytest.approx(w0, abs=1e-15)
+    assert r["w"][0, 0, 1] == pytest.approx(1.0 - w0, abs=1e-15)
+    # value row r = [r, 1]: out = w0 * [5, 1] + (1 - w0) * [8, 1]
+    V = np.array([[float(r_), 1.0] for r_ in range(9)], np.float32)
+    out = oracle.gather(V, 9, 2, r["idx"], r["w"])
+    assert out[0, 0] == pytest.approx(5 * w0 + 8 * (1 - w0), abs=1e-14)
+    assert out[0, 1] == pytest.approx(1.0, abs=1e-15)
+
+
+def test_factorised_equals_brute_force_tiny():
+    cfg = synth.CONFIGS["tiny"]
+    q, C = synth.queries(cfg), synth.subkeys(cfg)
+    args = (cfg["B"], cfg["H"], cfg["d_q"], cfg["n_keys"])
+    for k in (1, 2, 8, 17, 32):
+        r = oracle.lookup(q, C, *args, k)
+        bi, bs = oracle.brute_topk(q, C, *args, k)
+        assert np.array_equal(r["idx"], bi), k
+        np.testing.assert_allclose(r["score"], bs, rtol=0, atol=1e-12)
+
+
+def test_factorised_equals_brute_force_multihead_random():
+    rng = np.random.default_rng(11)
+    q, C = rand_problem(rng, 6, 3, 10, 9)
+    r = oracle.lookup(q, C, 6, 3, 10, 9, 5)
+    bi, _ = oracle.brute_topk(q, C, 6, 3, 10, 9, 5)
+    assert np.array_equal(r["idx"], bi)
+
+
+def test_factorised_equals_brute_force_mid_sampled_bf16():
+    cfg = synth.CONFIGS["mid"]
+    rows = 3
+    q = synth.queries(cfg, rows=rows, row_offset=1000)
+    C = synth.subkeys(cfg)
+    args = (rows, cfg["H"], cfg["d_q"], cfg["n_keys"], cfg["k"])
+    r = oracle.lookup(q, C, *args, want_gaps=True)
+    bi, bs = oracle.brute_topk(q, C, *args)
+    # identical unless two keys are within fp64 rounding of each other
+    same = (r["idx"] == bi).all(axis=-1)
+    assert same.all() or (r["gap_in"][~same].min() < 1e-12)
+    np.testing.assert_allclose(r["score"], bs, rtol=1e-12, atol=1e-12)
+
+
+def test_integer_ties_exact():
+    # Small integers are exact in fp32 and fp64, so every score is exact and
+    # duplicated subkey rows force exact ties; the rule is lower flat index.
+    rng = np.random.default_rng(5)
+    B, H, d_q, n = 4, 2, 6, 7
+    q = rng.integers(-2, 3, (B, H, d_q)).astype(np.float32)
+    C = rng.integers(-2, 3, (H, 2, n, d_q // 2)).astype(np.float32)
+    C[:, 0, 4] = C[:, 0, 1]  # duplicate rows -> ties in half 1
+    C[:, 1, 6] = C[:, 1, 0]  # and in half 2
+    for k in (1, 3, 7):
+        r = oracle.lookup(q, C, B, H, d_q, n, k)
+        assert np.array_equal(r["idx"], brute_python(q, C, k)), k
+
+
+def test_all_equal_scores_pick_lowest_flat():
+    # Zero subkeys: every key scores 0, so the answer is flat 0..k-1, uniform w.
+    q = np.ones((2, 1, 8), np.float32)
+    C = np.zeros((1, 2, 5, 4), np.float32)
+    r = oracle.lookup(q, C, 2, 1, 8, 5, 4, want_gaps=True)
+    assert r["idx"].tolist() == [[[0, 1, 2, 3]]] * 2
+    np.testing.assert_allclose(r["w"], 0.25, rtol=0, atol=1e-15)
+    assert (r["gap_k"] == 0).all()
+
+
+def test_k1_is_argmax():
+    rng = np.random.default_rng(3)
+    B, H, d_q, n = 20, 2, 16, 11
+    q, C = rand_problem(rng, B, H, d_q, n)
+    r = oracle.lookup(q, C, B, H, d_q, n, 1)
+    qd, Cd = q.astype(np.float64), C.astype(np.float64)
+    s1 = np.einsum("bht,hat->bha", qd[..., : d_q // 2], Cd[:, 0])
+    s2 = np.einsum("bht,hat->bha", qd[..., d_q // 2:], Cd[:, 1])
+    expect = s1.argmax(-1) * n + s2.argmax(-1)
+    assert np.array_equal(r["idx"][..., 0], expect)
+    assert (r["w"] == 1.0).all()
+
+
+def test_k_equals_nkeys_reaches_every_key():
+    # k = n_keys: the k^2 candidate set is the whole key space.
+    rng = np.random.default_rng(8)
+    q, C = rand_problem(rng, 3, 1, 8, 6)
+    r = oracle.lookup(q, C, 3, 1, 8, 6, 6)
+    qd, Cd = q.astype(np.float64), C.astype(np.float64)
+    for b in range(3):
+        s1 = Cd[0, 0] @ qd[b, 0, :4]
+        s2 = Cd[0, 1] @ qd[b, 0, 4:]
+        full = (s1[:, None] + s2[None, :]).ravel()
+        order = sorted(range(36), key=lambda f: (-full[f], f))[:6]
+        assert r["idx"][b, 0].tolist() == order
+
+
+def test_softmax_invariants():
+    cfg = synth.CONFIGS["tiny"]
+    q, C = synth.queries(cfg), synth.subkeys(cfg)
+    r = oracle.lookup(q, C, 64, 1, 64, 32, 8)
+    np.testing.assert_allclose(r["w"].sum(-1), 1.0, rtol=0, atol=1e-12)
+    assert (np.diff(r["w"], axis=-1) <= 0).all()
+    assert (np.diff(r["score"], axis=-1) <= 0).all()
+    # closed form: w_j = exp(s_j) / sum exp(s_l)
+    e = np.exp(r["score"] - r["score"][..., :1])
+    np.testing.assert_allclose(r["w"], e / e.sum(-1, keepdims=True), rtol=1e-13)
+
+
+def test_gather_closed_forms():
+    rng = np.random.default_rng(1)
+    B, H, k, N, d = 5, 3, 4, 64, 64
+    idx = rng.integers(0, N, (B, H, k)).astype(np.int64)
+    w = rng.random((B, H, k))
+    w /= w.sum(-1, keepdims=True)
+    ones = np.ones((N, d), np.float32)
+    np.testing.assert_allclose(oracle.gather(ones, N, d, idx, w), float(H), atol=1e-14)
+    ramp = np.repeat(np.arange(N, dtype=np.float32)[:, None], d, 1)
+    expect = (w * idx).sum((1, 2))
+    np.testing.assert_allclose(oracle.gather(ramp, N, d, idx, w), expect[:, None] * np.ones(d),
+                               rtol=1e-14)
+    onehot = np.zeros((N, d), np.float32)
+    onehot[np.arange(N), np.arange(N) % d] = 1.0
+    scat = np.zeros((B, d))
+    for b in range(B):
+        for h in range(H):
+            for j in range(k):
+                scat[b, idx[b, h, j] % d] += w[b, h, j]
+    np.testing.assert_allclose(oracle.gather(onehot, N, d, idx, w), scat, atol=1e-15)
+    # bf16 bits widen exactly: 1.0 = 0x3F80
+    onesb = np.full((N, d), 0x3F80, np.uint16)
+    np.testing.assert_allclose(oracle.gather(onesb, N, d, idx, w), float(H), atol=1e-14)
+
+
+def test_gather_rejects_out_of_range_index():
+    V = np.ones((4, 2), np.float32)
+    with pytest.raises(ValueError):
+        oracle.gather(V, 4, 2, np.array([[[4]]], np.int64), np.array([[[1.0]]]))
+
+
+def test_forward_matches_torch_sketch_float64():
+    # The page's module forward, run op by op in float64 torch on continuous
+    # inputs (no ties): chunk, per-half matmul + topk, k^2 sums, flat index
+    # i1 * n + i2, topk, softmax, weighted sum of value rows; heads summed.
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(21)
+    B, H, d_q, n, d_v, k = 7, 2, 12, 9, 5, 4
+    q, C = rand_problem(rng, B, H, d_q, n)
+    V = rng.standard_normal((n * n, d_v)).astype(np.float32)
+    idx, w, out = oracle.forward(q, C, V, B, H, d_q, n, d_v, k)
+    tq, tC, tV = (torch.from_numpy(x).double() for x in (q, C, V))
+    tout = torch.zeros(B, d_v, dtype=torch.float64)
+    for h in range(H):
+        q1, q2 = tq[:, h].chunk(2, dim=-1)
+        s1, i1 = (q1 @ tC[h, 0].T).topk(k)
+        s2, i2 = (q2 @ tC[h, 1].T).topk(k)
+        scores = (s1[:, :, None] + s2[:, None, :]).flatten(1)
+        flat = (i1[:, :, None] * n + i2[:, None, :]).flatten(1)
+        top, pos = scores.topk(k)
+        sel = flat.gather(1, pos)
+        wt = top.softmax(-1)
+        assert np.array_equal(sel.numpy(), idx[:, h])
+        np.testing.assert_allclose(wt.numpy(), w[:, h], rtol=1e-12)
+        tout += (wt[:, :, None] * tV[sel]).sum(1)
+    np.testing.assert_allclose(out, tout.numpy(), rtol=1e-12, atol=1e-14)
+
+
+def test_page_operation_counts():
+    g = json.load(open(os.path.join(GOLDEN, "page_op_counts.json")))
+    n, k = g["n_keys"], g["k"]
+    rng = np.random.default_rng(2)
+    q, C = rand_problem(rng, 1, 1, 4, n)
+    r = oracle.lookup(q, C, 1, 1, 4, n, k)
+    assert r["counters"][0] == g["subkey_comparisons"]  # 2 sqrt(N) per query and head
+    assert r["counters"][1] == g["merge_candidates"] == k * k
+    # "instead of a million": the flat search scores every one of n^2 keys
+    assert abs(n * n - g["flat_comparisons_approx"]) / g["flat_comparisons_approx"] < 0.05
+    assert abs(g["value_params_N"] * g["value_params_d"] - g["value_params_approx"]) \
+        / g["value_params_approx"] < 0.05
+    # top-k retrieval: k / n_slots; 0.05% at k = 5 implies 10^4 slots
+    slots = 5 / (g["topk_fraction_k5_percent"] / 100)
+    assert round(slots / 5) == g["topk_reduction_k5"]
+    assert 100 * 100 / slots == g["topk_fraction_k100_percent"]
+
+
+def test_near_tie_report():
+    # Make the k-th and (k+1)-th full keys tie exactly: duplicate a half-2 subkey.
+    q = np.array([[[1.0, 0.0, 1.0, 0.0]]], np.float32)
+    C = np.zeros((1, 2, 4, 2), np.float32)
+    C[0, 0, :, 0] = [4.0, 3.0, 2.0, 1.0]
+    C[0, 1, :, 0] = [0.5, 0.25, 0.25, -9.0]
+    r = oracle.lookup(q, C, 1, 1, 4, 4, 2, want_gaps=True)
+    # best: (0,0)=4.5 flat 0; next (0,1) and (0,2) tie at 4.25 -> flat 1 wins
+    assert r["idx"].tolist() == [[[0, 1]]]
+    assert r["gap_k"][0, 0] == 0.0
+    assert r["gap_in"][0, 0] == pytest.approx(0.25 / 4.5)
+
+
+def test_rejects_bad_shapes():
+    q = np.zeros((1, 1, 4), np.float32)
+    C = np.zeros((1, 2, 3, 2), np.float32)
+    with pytest.raises(ValueError):
+        oracle.lookup(q, C, 1, 1, 4, 3, 4)  # k > n_keys
+    with pytest.raises(ValueError):
+        oracle.lookup(q, C, 1, 1, 3, 3, 1)  # odd d_q
