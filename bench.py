@@ -1,0 +1,345 @@
+"""Benchmark of the PKM lookup forward pass on GB300.
+
+One step = one full forward (scoring, per-half top-k, k^2 merge, softmax,
+weighted value read) over one batch of the page-scale workload: B = 16384
+queries, H = 4 heads, d_q = 1024, n_keys = 1024 (N = 2^20), d_v = 1024,
+k = 32, bf16 inputs, all resident in HBM.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload page|mid|skew|large|tiny]
+
+--impl reference times the fp64 CPU oracle on the host cores instead, on a
+bounded sample of the same workload.  Under torchrun (N > 1) each rank runs
+its own batch on its own GPU (weak scaling; no collective on the data path),
+the time is the max over ranks.
+"""
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "PKM lookups (queries×heads)/s; value-gather HBM GB/s and % of GB300 peak"
+UNIT = "lookups/s"
+L2_FLUSH_BYTES = 512 << 20
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sus=d["bf16_tflops_sustained"],
+                    src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=5)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(n_gpus):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def dist_max(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def workload(name, B=None):
+    c = dict(synth.CONFIGS[name])
+    if B is not None:
+        c["B"] = B
+    return c
+
+
+def cpu_inputs(c, sample, C=None, V=None):
+    """Inputs of the CPU oracle leg: the first `sample` queries, all tables."""
+    q = synth.queries(c, rows=sample, row_offset=0)
+    return q, (synth.subkeys(c) if C is None else C), (synth.values(c) if V is None else V)
+
+
+def cpu_oracle_time(c, inputs, sample, nthreads):
+    """Wall time of the fp64 oracle forward on `sample` queries of workload c."""
+    import oracle
+    q, C, V = inputs
+    t0 = time.perf_counter()
+    oracle.forward(q, C, V, sample, c["H"], c["d_q"], c["n_keys"], c["d_v"], c["k"],
+                   nthreads=nthreads)
+    return time.perf_counter() - t0
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    c = workload(args.workload)
+    nthreads = os.cpu_count() or 1
+    sample = min(args.cpu_sample, c["B"])
+    inputs = cpu_inputs(c, sample)
+    ts = []
+    for i in range(args.warmup + args.steps):
+        dt = cpu_oracle_time(c, inputs, sample, nthreads)
+        if i >= args.warmup:
+            ts.append(dt)
+    t = sum(ts) / len(ts)
+    value = sample * c["H"] / t
+    cpu = {"value": value, "unit": UNIT, "cores": nthreads, "kind": "oracle",
+           "sample": "%d of %d queries of the %s workload per step (fp64 oracle forward)"
+                     % (sample, c["B"], args.workload)}
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_json(c, args.workload),
+            "cpu_baseline": cpu,
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_json(c, name):
+    return {"workload": name, "B": c["B"], "H": c["H"], "d_q": c["d_q"], "n_keys": c["n_keys"],
+            "N": c["n_keys"] ** 2, "d_v": c["d_v"], "k": c["k"],
+            "inputs": "%s, seeded synthetic" % c["dtype"],
+            "l2": "flushed (512 MiB write) between timed steps; value table %.1f GiB"
+                  % (c["n_keys"] ** 2 * c["d_v"] * (2 if c["dtype"] == "bf16" else 4) / 2**30)}
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    import sparse_top_lookup_gb300 as pk
+
+    torch.cuda.set_device(local)
+    c = workload(args.workload)
+    B, H, d_q, n, d_v, k = (c[x] for x in ("B", "H", "d_q", "n_keys", "d_v", "k"))
+    bf16 = c["dtype"] == "bf16"
+    dt = pk.PKM_BF16 if bf16 else pk.PKM_F32
+    esz = 2 if bf16 else 4
+
+    # inputs: generated on the host from the seeded streams, copied to HBM once
+    def dev(a):
+        if bf16:
+            return torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16)
+        return torch.from_numpy(a).cuda()
+
+    q_np, C_np, V_np = synth.queries(c), synth.subkeys(c), synth.values(c)
+    dq, dC, dV = dev(q_np), dev(C_np), dev(V_np)
+    out = torch.empty(B, d_v, device="cuda")
+    idx = torch.empty(B, H, k, dtype=torch.int64, device="cuda")
+    w = torch.empty(B, H, k, device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    cfg = pk.make_config(d_q, d_v, B, H, n, k, q_dtype=dt, host_staging=1)
+    h = pk.pkm_create(cfg)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        pk.check(pk.pkm_lookup(h, dq, dC, B, H, n, k, idx, w, stream), "pkm_lookup")
+        pk.check(pk.pkm_gather(h, dV, B, H, n, k, idx, w, out, stream), "pkm_gather")
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    st = pk.pkm_get_status(h)
+    if st != pk.PKM_OK:
+        raise RuntimeError("device status after warm-up: %s" % pk.pkm_strerror(st))
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            pk.check(pk.pkm_lookup(h, dq, dC, B, H, n, k, idx, w, stream), "pkm_lookup")
+            ev[i][1].record(stream)
+            pk.check(pk.pkm_gather(h, dV, B, H, n, k, idx, w, out, stream), "pkm_gather")
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+        # keep sampling clocks long enough to see the load even for short runs
+        time.sleep(0.25)
+    dist_barrier(world)
+    st = pk.pkm_get_status(h)
+    if st != pk.PKM_OK:
+        raise RuntimeError("device status after timed steps: %s" % pk.pkm_strerror(st))
+    t_lookup = [e[0].elapsed_time(e[1]) for e in ev]
+    t_gather = [e[1].elapsed_time(e[2]) for e in ev]
+    ms_step_local = sum(a + b for a, b in zip(t_lookup, t_gather)) / args.steps
+    ms_step = dist_max(ms_step_local, world)
+    ms_lookup = sum(t_lookup) / args.steps
+    ms_gather = sum(t_gather) / args.steps
+
+    # end to end through the host-buffer entry point: H2D of q, D2H of out
+    q_host = torch.from_numpy(q_np.view(np.int16) if bf16 else q_np).pin_memory()
+    out_host = torch.empty(B, d_v).pin_memory()
+    for _ in range(2):
+        pk.check(pk.pkm_forward_host(h, q_host, dC, dV, B, H, n, k, out_host, None, None, stream),
+                 "pkm_forward_host")
+    e2e_steps = max(3, min(args.steps, 20))
+    dist_barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        pk.check(pk.pkm_forward_host(h, q_host, dC, dV, B, H, n, k, out_host, None, None, stream),
+                 "pkm_forward_host")
+    e2e_s = dist_max((time.perf_counter() - t0) / e2e_steps, world)
+    pk.pkm_destroy(h)
+
+    pk_ = peaks()
+    gather_bytes = B * H * k * d_v * esz + B * H * k * 12 + B * d_v * 4
+    achieved = gather_bytes / (ms_gather * 1e-3) / 1e9
+    flops = 2.0 * B * H * n * d_q
+    tflops = flops / (ms_lookup * 1e-3) / 1e12
+    value = world * B * H / (ms_step * 1e-3)
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "gather_traffic.json")
+    if os.path.exists(tpath):
+        tj = json.load(open(tpath))
+        if tj.get("workload") == args.workload and tj.get("kernel_rev") == GATHER_REV:
+            traffic = tj.get("bytes_per_launch")
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": c["dtype"], "data": "synthetic",
+        "config": config_json(c, args.workload),
+        "queries_per_s": world * B / (ms_step * 1e-3),
+        "stages_ms": {"lookup": ms_lookup, "gather": ms_gather},
+        "roofline": {"kernel": "gather_kernel (value read)", "bound": "hbm",
+                     "achieved": achieved, "peak": pk_["hbm"], "unit": "GB/s",
+                     "frac": achieved / pk_["hbm"], "traffic": traffic,
+                     "peak_source": pk_["src"]},
+        "scoring_roofline": {"kernel": "lookup_tc_kernel (scoring + selection)",
+                             "bound": "tensor", "achieved": tflops, "peak": pk_["bf16"],
+                             "unit": "TFLOP/s", "frac": tflops / pk_["bf16"],
+                             "peak_source": pk_["src"] + " bf16 burst"},
+        "e2e": {"value": world * B * H / e2e_s, "unit": UNIT,
+                "h2d_bytes_per_step": B * H * d_q * esz, "d2h_bytes_per_step": B * d_v * 4},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        nthreads = os.cpu_count() or 1
+        sample = min(args.cpu_sample, B)
+        t = cpu_oracle_time(c, cpu_inputs(c, sample, C=C_np, V=V_np), sample, nthreads)
+        line["cpu_baseline"] = {
+            "value": sample * H / t, "unit": UNIT, "cores": nthreads, "kind": "oracle",
+            "sample": "%d of %d queries (all %d heads) of the %s workload, fp64 oracle forward"
+                      % (sample, B, H, args.workload)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+GATHER_REV = "gather-v1"
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="page", choices=sorted(synth.CONFIGS))
+    ap.add_argument("--cpu-sample", type=int, default=1024)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, world, local = dist_setup(args.gpus)
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_ours(args, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,155 @@
+/*
+ * pkm.h - C ABI of the product-key memory (PKM) lookup forward pass on one
+ * NVIDIA GB300 GPU (sm_103a).
+ *
+ * The operation (Product-Key Memory, "Factorising the key space", and the
+ * forward method of the page's code listing; Memory Retrieval Mechanisms,
+ * the top-k retrieval equations):
+ *
+ *   for every query b and head h, with q = q[b,h,:] split into halves
+ *   q1 = q[0 : d_q/2] and q2 = q[d_q/2 : d_q]:
+ *     s1[a] = q1 . C[h,0,a,:]          s2[a] = q2 . C[h,1,a,:]      (a < n_keys)
+ *     A1 = top-k of s1, A2 = top-k of s2                  (per-half winners)
+ *     candidates (i, j) in A1 x A2: score s1[i] + s2[j], flat i*n_keys + j
+ *     idx[b,h,:] = the k best candidates, (score desc, flat asc)
+ *     w[b,h,:]   = softmax of their scores (no temperature)
+ *   out[b,:] = sum over h and j of w[b,h,j] * V[idx[b,h,j], :]
+ *
+ * The factorised search is exact: its result equals a top-k over all
+ * n_keys^2 full keys (q . concat(C[h,0,a], C[h,1,j])).  Ties are broken
+ * toward the lower subkey index within a half and the lower flat index
+ * overall.  Heads score their own subkeys with their own slice of q, share
+ * one value table, and their reads are summed.
+ *
+ * Layouts (all row-major, contiguous, device memory unless stated):
+ *   q        [B, H, d_q]            q_dtype
+ *   subkeys  [H, 2, n_keys, d_q/2]  key_dtype   (must equal q_dtype)
+ *   values   [n_keys^2, d_v]        value_dtype
+ *   out      [B, d_v]               fp32, overwritten
+ *   idx      [B, H, k]              int64 flat row indices
+ *   w        [B, H, k]              fp32 softmax weights aligned with idx
+ * bf16 arguments are raw IEEE bfloat16 bit patterns (uint16).
+ *
+ * Arithmetic: bf16 queries and subkeys are scored on the tensor cores with
+ * fp32 accumulation; fp32 queries and subkeys are scored with fp32 FMA on the
+ * CUDA cores.  Candidate sums, the softmax and the weighted row sum are fp32.
+ *
+ * Ownership: the caller owns every tensor pointer; nothing is retained after a
+ * call returns.  A handle owns only its scratch (device workspace for idx/w
+ * when the caller passes NULL, a device status word, and optional staging for
+ * pkm_forward_host).  pkm_create is the only call that allocates.
+ *
+ * Asynchrony: every call enqueues work on `stream` (a cudaStream_t; NULL is
+ * the legacy default stream) and returns without synchronising, except
+ * pkm_get_status and pkm_forward_host, which synchronise `stream`.  Results are
+ * valid once the stream has been synchronised.  Calls on one handle must not
+ * overlap on the GPU when they use the handle's scratch (idx/w == NULL).
+ *
+ * Errors: every call returns PKM_OK (0) or a negative code, checked on the
+ * host before anything is launched.  Device-side failures (an out-of-range
+ * index reaching the value read, a bounded wait that gave up) are recorded in
+ * the handle's status word and returned by pkm_get_status.
+ */
+#ifndef PKM_H
+#define PKM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PKM_ABI_VERSION 1
+
+/* element types */
+enum { PKM_F32 = 0, PKM_BF16 = 1 };
+
+/* return codes */
+enum {
+  PKM_OK = 0,
+  PKM_ERR_INVALID = -1,     /* NULL handle / tensor pointer, non-positive dims, odd d_q */
+  PKM_ERR_RANGE = -2,       /* B, H, n_keys or k outside the handle's config, k > n_keys */
+  PKM_ERR_UNSUPPORTED = -3, /* dtype combination, k above the path's limit (32 for bf16
+                               scoring, 64 for fp32), n_keys^2 >= 2^31, d_q or d_v layout */
+  PKM_ERR_ALIGN = -4,       /* a tensor pointer not 16-byte aligned */
+  PKM_ERR_CUDA = -5,        /* a CUDA runtime call or launch failed */
+  PKM_ERR_NOMEM = -6,       /* pkm_create could not allocate its scratch */
+  PKM_ERR_TIMEOUT = -7,     /* device: a bounded wait inside a kernel gave up */
+  PKM_ERR_BAD_INDEX = -8,   /* device: a row index outside [0, n_keys^2) reached the value read */
+  PKM_ERR_NO_STAGING = -9   /* pkm_forward_host on a handle created without host staging */
+};
+
+typedef struct pkm_handle *pkm_t;
+
+/*
+ * Fixed shape of a handle.  d_q: query width per head (even; a multiple of 16
+ * for bf16).  d_v: value row width (d_v * element size a multiple of 16
+ * bytes).  max_*: the largest B, H, n_keys and k any call will pass (sizes
+ * the scratch).  host_staging: nonzero to also allocate device staging for
+ * pkm_forward_host (max_B queries and outputs).
+ */
+typedef struct {
+  int d_q, d_v;
+  int max_B, max_H, max_n_keys, max_k;
+  int q_dtype, key_dtype, value_dtype;
+  int host_staging;
+} pkm_config;
+
+/* Allocate a handle on the current CUDA device.  *out is set only on success. */
+int pkm_create(pkm_t *out, const pkm_config *cfg);
+
+/* Free a handle and its scratch.  NULL is a no-op.  Synchronises the device work
+   that may still use the scratch (cudaFree semantics). */
+void pkm_destroy(pkm_t h);
+
+/*
+ * The whole forward pass: scoring, per-half top-k, k^2 merge, softmax and the
+ * weighted value read summed over heads.  idx and w may each be NULL, in which
+ * case the handle's scratch holds them.  B == 0 is a no-op returning PKM_OK.
+ */
+int pkm_forward(pkm_t h, const void *q, const void *subkeys, const void *values, int B, int H,
+                int n_keys, int k, float *out, int64_t *idx, float *w, void *stream);
+
+/* The lookup alone (scoring through softmax): writes idx and w, both required. */
+int pkm_lookup(pkm_t h, const void *q, const void *subkeys, int B, int H, int n_keys, int k,
+               int64_t *idx, float *w, void *stream);
+
+/*
+ * The value read alone: out[b,:] = sum_{h,j} w[b,h,j] * values[idx[b,h,j], :]
+ * (EmbeddingBag(mode="sum") with per-sample weights, bags of H*k rows).
+ * Rows with an index outside [0, n_keys^2) contribute nothing and set
+ * PKM_ERR_BAD_INDEX in the status word.
+ */
+int pkm_gather(pkm_t h, const void *values, int B, int H, int n_keys, int k, const int64_t *idx,
+               const float *w, float *out, void *stream);
+
+/*
+ * pkm_forward with the per-call tensors in HOST memory: q_host is copied to
+ * the handle's staging, the forward runs, and out_host (and idx_host / w_host
+ * when not NULL) are copied back; the call synchronises `stream` before it
+ * returns.  subkeys and values stay device pointers (they are parameters,
+ * resident on the GPU).  Host buffers should be pinned for full copy speed.
+ * Needs a handle created with host_staging != 0.
+ */
+int pkm_forward_host(pkm_t h, const void *q_host, const void *subkeys, const void *values, int B,
+                     int H, int n_keys, int k, float *out_host, int64_t *idx_host, float *w_host,
+                     void *stream);
+
+/* Synchronise `stream`, return the device status word (PKM_OK or a device error
+   code) and reset it to PKM_OK. */
+int pkm_get_status(pkm_t h, void *stream);
+
+/* Host-only argument check of a call against a config (no CUDA calls). */
+int pkm_check_args(const pkm_config *cfg, int B, int H, int n_keys, int k);
+
+/* Static description of a return code. */
+const char *pkm_strerror(int code);
+
+/* PKM_ABI_VERSION of the library. */
+int pkm_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKM_H */

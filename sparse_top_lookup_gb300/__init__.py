@@ -1,0 +1,159 @@
+"""Python binding of the PKM lookup C ABI (include/pkm.h).
+
+Argument marshalling only: every step of the lookup runs in the CUDA kernels
+of libpkm.so.  Tensor arguments may be torch tensors (their data_ptr is
+passed), numpy arrays (host memory, for pkm_forward_host), raw integer
+addresses, or None for optional outputs.  There is no CPU fallback: if
+libpkm.so has not been built, importing the library handle raises.
+"""
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpkm.so")
+INCLUDE = os.path.join(os.path.dirname(_HERE), "include", "pkm.h")
+
+PKM_F32, PKM_BF16 = 0, 1
+PKM_OK = 0
+PKM_ERR_INVALID, PKM_ERR_RANGE, PKM_ERR_UNSUPPORTED, PKM_ERR_ALIGN = -1, -2, -3, -4
+PKM_ERR_CUDA, PKM_ERR_NOMEM, PKM_ERR_TIMEOUT, PKM_ERR_BAD_INDEX = -5, -6, -7, -8
+PKM_ERR_NO_STAGING = -9
+
+EXPORTED = ["pkm_create", "pkm_destroy", "pkm_forward", "pkm_lookup", "pkm_gather",
+            "pkm_forward_host", "pkm_get_status", "pkm_check_args", "pkm_strerror",
+            "pkm_abi_version"]
+
+
+class pkm_config(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in
+                ("d_q", "d_v", "max_B", "max_H", "max_n_keys", "max_k", "q_dtype", "key_dtype",
+                 "value_dtype", "host_staging")]
+
+
+class PkmError(RuntimeError):
+    def __init__(self, code, where):
+        self.code = code
+        super().__init__("%s: %s (%d)" % (where, pkm_strerror(code), code))
+
+
+def build(force=False):
+    """Compile libpkm.so for sm_103a (nvcc)."""
+    from . import builder as _b
+    return _b.build(force=force)
+
+
+_lib = None
+
+
+def lib():
+    """The loaded libpkm.so; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError("libpkm.so is not built (run sparse_top_lookup_gb300.build())")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32 = ctypes.c_void_p, ctypes.c_int
+        cfgp = ctypes.POINTER(pkm_config)
+        L.pkm_create.argtypes = [ctypes.POINTER(vp), cfgp]
+        L.pkm_destroy.argtypes = [vp]
+        L.pkm_destroy.restype = None
+        L.pkm_forward.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp]
+        L.pkm_lookup.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp]
+        L.pkm_gather.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp]
+        L.pkm_forward_host.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp]
+        L.pkm_get_status.argtypes = [vp, vp]
+        L.pkm_check_args.argtypes = [cfgp, i32, i32, i32, i32]
+        L.pkm_strerror.argtypes = [i32]
+        L.pkm_strerror.restype = ctypes.c_char_p
+        L.pkm_abi_version.argtypes = []
+        for f in ("pkm_create", "pkm_forward", "pkm_lookup", "pkm_gather", "pkm_forward_host",
+                  "pkm_get_status", "pkm_check_args", "pkm_abi_version"):
+            getattr(L, f).restype = i32
+        _lib = L
+    return _lib
+
+
+def _addr(x):
+    """Device or host address of a tensor / array / int / None."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    if hasattr(x, "ctypes"):
+        return x.ctypes.data
+    raise TypeError("cannot take the address of %r" % type(x))
+
+
+def _stream(s):
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def make_config(d_q, d_v, max_B, max_H, max_n_keys, max_k, q_dtype=PKM_BF16, key_dtype=None,
+                value_dtype=None, host_staging=0):
+    key_dtype = q_dtype if key_dtype is None else key_dtype
+    value_dtype = q_dtype if value_dtype is None else value_dtype
+    return pkm_config(d_q, d_v, max_B, max_H, max_n_keys, max_k, q_dtype, key_dtype, value_dtype,
+                      int(bool(host_staging)))
+
+
+def pkm_strerror(code):
+    return lib().pkm_strerror(code).decode()
+
+
+def pkm_abi_version():
+    return lib().pkm_abi_version()
+
+
+def pkm_check_args(cfg, B, H, n_keys, k):
+    return lib().pkm_check_args(ctypes.byref(cfg), B, H, n_keys, k)
+
+
+def pkm_create(cfg):
+    h = ctypes.c_void_p()
+    rc = lib().pkm_create(ctypes.byref(h), ctypes.byref(cfg))
+    if rc != PKM_OK:
+        raise PkmError(rc, "pkm_create")
+    return h
+
+
+def pkm_destroy(h):
+    lib().pkm_destroy(h)
+
+
+def pkm_forward(h, q, subkeys, values, B, H, n_keys, k, out, idx=None, w=None, stream=None):
+    return lib().pkm_forward(h, _addr(q), _addr(subkeys), _addr(values), B, H, n_keys, k,
+                             _addr(out), _addr(idx), _addr(w), _stream(stream))
+
+
+def pkm_lookup(h, q, subkeys, B, H, n_keys, k, idx, w, stream=None):
+    return lib().pkm_lookup(h, _addr(q), _addr(subkeys), B, H, n_keys, k, _addr(idx), _addr(w),
+                            _stream(stream))
+
+
+def pkm_gather(h, values, B, H, n_keys, k, idx, w, out, stream=None):
+    return lib().pkm_gather(h, _addr(values), B, H, n_keys, k, _addr(idx), _addr(w), _addr(out),
+                            _stream(stream))
+
+
+def pkm_forward_host(h, q_host, subkeys, values, B, H, n_keys, k, out_host, idx_host=None,
+                     w_host=None, stream=None):
+    return lib().pkm_forward_host(h, _addr(q_host), _addr(subkeys), _addr(values), B, H, n_keys, k,
+                                  _addr(out_host), _addr(idx_host), _addr(w_host),
+                                  _stream(stream))
+
+
+def pkm_get_status(h, stream=None):
+    return lib().pkm_get_status(h, _stream(stream))
+
+
+def check(rc, where):
+    """Raise PkmError unless rc is PKM_OK."""
+    if rc != PKM_OK:
+        raise PkmError(rc, where)

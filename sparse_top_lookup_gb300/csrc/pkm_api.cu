@@ -1,0 +1,234 @@
+// The C ABI of include/pkm.h: argument checks, scratch ownership and launch
+// order.  No arithmetic of the lookup lives here.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdlib.h>
+
+#include "pkm_internal.cuh"
+
+struct pkm_handle {
+  pkm_config cfg;
+  int device;
+  int64_t* ws_idx;   // [max_B, max_H, max_k] when the caller passes idx == NULL
+  float* ws_w;       // [max_B, max_H, max_k] when the caller passes w == NULL
+  int* status;       // device status word
+  void* stage_q;     // pkm_forward_host staging (optional)
+  float* stage_out;
+  int64_t* stage_idx;
+  float* stage_w;
+};
+
+namespace {
+
+int elem_size(int dtype) { return dtype == PKM_BF16 ? 2 : 4; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_config(const pkm_config* c) {
+  if (!c) return PKM_ERR_INVALID;
+  if (c->d_q < 2 || (c->d_q & 1) || c->d_v < 1) return PKM_ERR_INVALID;
+  if (c->max_B < 0 || c->max_H < 1 || c->max_n_keys < 1 || c->max_k < 1) return PKM_ERR_INVALID;
+  for (int dt : {c->q_dtype, c->key_dtype, c->value_dtype})
+    if (dt != PKM_F32 && dt != PKM_BF16) return PKM_ERR_UNSUPPORTED;
+  if (c->q_dtype != c->key_dtype) return PKM_ERR_UNSUPPORTED;
+  if ((int64_t)c->d_v * elem_size(c->value_dtype) % 16) return PKM_ERR_UNSUPPORTED;
+  if ((int64_t)c->d_v * elem_size(c->value_dtype) / 16 > pkm::kGatherMaxVecPerRow)
+    return PKM_ERR_UNSUPPORTED;
+  if (c->q_dtype == PKM_BF16) {
+    if (c->d_q % 16) return PKM_ERR_UNSUPPORTED;  // TMA strides are multiples of 16 bytes
+    if (c->max_k > pkm::kTcMaxK) return PKM_ERR_UNSUPPORTED;
+  } else {
+    if (c->d_q > pkm::kSimtMaxDq || c->max_k > pkm::kSimtMaxK) return PKM_ERR_UNSUPPORTED;
+    if (c->max_n_keys > pkm::kSimtMaxNKeys) return PKM_ERR_UNSUPPORTED;
+  }
+  if ((int64_t)c->max_n_keys * c->max_n_keys > INT32_MAX) return PKM_ERR_UNSUPPORTED;
+  return PKM_OK;
+}
+
+int check_call(const pkm_config* c, int B, int H, int n, int k) {
+  int rc = check_config(c);
+  if (rc) return rc;
+  if (B < 0 || H < 1 || n < 1 || k < 1) return PKM_ERR_INVALID;
+  if (B > c->max_B || H > c->max_H || n > c->max_n_keys || k > c->max_k || k > n)
+    return PKM_ERR_RANGE;
+  if (B > 0 && (int64_t)B * H > INT32_MAX) return PKM_ERR_RANGE;
+  return PKM_OK;
+}
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? PKM_OK : PKM_ERR_CUDA; }
+
+int run_lookup(pkm_t h, const void* q, const void* subkeys, int B, int H, int n, int k,
+               int64_t* idx, float* w, cudaStream_t s) {
+  if (h->cfg.q_dtype == PKM_BF16)
+    return cuda_rc(pkm::launch_lookup_tc(static_cast<const uint16_t*>(q),
+                                         static_cast<const uint16_t*>(subkeys), B, H, h->cfg.d_q,
+                                         n, k, idx, w, h->status, s));
+  return cuda_rc(pkm::launch_lookup_simt(static_cast<const float*>(q),
+                                         static_cast<const float*>(subkeys), B, H, h->cfg.d_q, n,
+                                         k, idx, w, s));
+}
+
+int run_gather(pkm_t h, const void* values, int B, int H, int n, int k, const int64_t* idx,
+               const float* w, float* out, cudaStream_t s) {
+  return cuda_rc(pkm::launch_gather(values, h->cfg.value_dtype, (int64_t)n * n, h->cfg.d_v, B,
+                                    H * k, idx, w, out, h->status, s));
+}
+
+}  // namespace
+
+extern "C" {
+
+int pkm_abi_version(void) { return PKM_ABI_VERSION; }
+
+const char* pkm_strerror(int code) {
+  switch (code) {
+    case PKM_OK: return "ok";
+    case PKM_ERR_INVALID: return "invalid argument (NULL pointer, non-positive or odd dimension)";
+    case PKM_ERR_RANGE: return "size outside the handle's configuration or k > n_keys";
+    case PKM_ERR_UNSUPPORTED: return "unsupported dtype combination, k or layout";
+    case PKM_ERR_ALIGN: return "tensor pointer not 16-byte aligned";
+    case PKM_ERR_CUDA: return "CUDA runtime error";
+    case PKM_ERR_NOMEM: return "device allocation failed";
+    case PKM_ERR_TIMEOUT: return "a bounded wait inside a kernel gave up";
+    case PKM_ERR_BAD_INDEX: return "row index outside the value table";
+    case PKM_ERR_NO_STAGING: return "handle was created without host staging";
+    default: return "unknown error code";
+  }
+}
+
+int pkm_check_args(const pkm_config* cfg, int B, int H, int n_keys, int k) {
+  return check_call(cfg, B, H, n_keys, k);
+}
+
+void pkm_destroy(pkm_t h) {
+  if (!h) return;
+  cudaFree(h->ws_idx);
+  cudaFree(h->ws_w);
+  cudaFree(h->status);
+  cudaFree(h->stage_q);
+  cudaFree(h->stage_out);
+  cudaFree(h->stage_idx);
+  cudaFree(h->stage_w);
+  free(h);
+}
+
+int pkm_create(pkm_t* out, const pkm_config* cfg) {
+  if (!out) return PKM_ERR_INVALID;
+  int rc = check_config(cfg);
+  if (rc) return rc;
+  pkm_t h = static_cast<pkm_t>(calloc(1, sizeof(pkm_handle)));
+  if (!h) return PKM_ERR_NOMEM;
+  h->cfg = *cfg;
+  if (cudaGetDevice(&h->device) != cudaSuccess) {
+    free(h);
+    return PKM_ERR_CUDA;
+  }
+  const size_t sel = (size_t)cfg->max_B * cfg->max_H * cfg->max_k;
+  bool ok = cudaMalloc(&h->status, sizeof(int)) == cudaSuccess &&
+            cudaMemset(h->status, 0, sizeof(int)) == cudaSuccess;
+  if (ok && sel) {
+    ok = cudaMalloc(&h->ws_idx, sel * sizeof(int64_t)) == cudaSuccess &&
+         cudaMalloc(&h->ws_w, sel * sizeof(float)) == cudaSuccess;
+  }
+  if (ok && cfg->host_staging && cfg->max_B) {
+    const size_t qb = (size_t)cfg->max_B * cfg->max_H * cfg->d_q * elem_size(cfg->q_dtype);
+    ok = cudaMalloc(&h->stage_q, qb) == cudaSuccess &&
+         cudaMalloc(&h->stage_out, (size_t)cfg->max_B * cfg->d_v * sizeof(float)) == cudaSuccess &&
+         cudaMalloc(&h->stage_idx, sel * sizeof(int64_t)) == cudaSuccess &&
+         cudaMalloc(&h->stage_w, sel * sizeof(float)) == cudaSuccess;
+  }
+  if (!ok) {
+    cudaGetLastError();
+    pkm_destroy(h);
+    return PKM_ERR_NOMEM;
+  }
+  *out = h;
+  return PKM_OK;
+}
+
+int pkm_lookup(pkm_t h, const void* q, const void* subkeys, int B, int H, int n_keys, int k,
+               int64_t* idx, float* w, void* stream) {
+  if (!h) return PKM_ERR_INVALID;
+  int rc = check_call(&h->cfg, B, H, n_keys, k);
+  if (rc) return rc;
+  if (B == 0) return PKM_OK;
+  if (!q || !subkeys || !idx || !w) return PKM_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(subkeys) || !aligned16(idx) || !aligned16(w))
+    return PKM_ERR_ALIGN;
+  return run_lookup(h, q, subkeys, B, H, n_keys, k, idx, w, static_cast<cudaStream_t>(stream));
+}
+
+int pkm_gather(pkm_t h, const void* values, int B, int H, int n_keys, int k, const int64_t* idx,
+               const float* w, float* out, void* stream) {
+  if (!h) return PKM_ERR_INVALID;
+  int rc = check_call(&h->cfg, B, H, n_keys, k);
+  if (rc) return rc;
+  if (B == 0) return PKM_OK;
+  if (!values || !idx || !w || !out) return PKM_ERR_INVALID;
+  if (!aligned16(values) || !aligned16(idx) || !aligned16(w) || !aligned16(out))
+    return PKM_ERR_ALIGN;
+  return run_gather(h, values, B, H, n_keys, k, idx, w, out, static_cast<cudaStream_t>(stream));
+}
+
+int pkm_forward(pkm_t h, const void* q, const void* subkeys, const void* values, int B, int H,
+                int n_keys, int k, float* out, int64_t* idx, float* w, void* stream) {
+  if (!h) return PKM_ERR_INVALID;
+  int rc = check_call(&h->cfg, B, H, n_keys, k);
+  if (rc) return rc;
+  if (B == 0) return PKM_OK;
+  if (!q || !subkeys || !values || !out) return PKM_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(subkeys) || !aligned16(values) || !aligned16(out) ||
+      (idx && !aligned16(idx)) || (w && !aligned16(w)))
+    return PKM_ERR_ALIGN;
+  if (!idx) idx = h->ws_idx;
+  if (!w) w = h->ws_w;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  rc = run_lookup(h, q, subkeys, B, H, n_keys, k, idx, w, s);
+  if (rc) return rc;
+  return run_gather(h, values, B, H, n_keys, k, idx, w, out, s);
+}
+
+int pkm_forward_host(pkm_t h, const void* q_host, const void* subkeys, const void* values, int B,
+                     int H, int n_keys, int k, float* out_host, int64_t* idx_host, float* w_host,
+                     void* stream) {
+  if (!h) return PKM_ERR_INVALID;
+  int rc = check_call(&h->cfg, B, H, n_keys, k);
+  if (rc) return rc;
+  if (B == 0) return PKM_OK;
+  if (!h->stage_q) return PKM_ERR_NO_STAGING;
+  if (!q_host || !subkeys || !values || !out_host) return PKM_ERR_INVALID;
+  if (!aligned16(subkeys) || !aligned16(values)) return PKM_ERR_ALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t qb = (size_t)B * H * h->cfg.d_q * elem_size(h->cfg.q_dtype);
+  const size_t sel = (size_t)B * H * k;
+  if (cudaMemcpyAsync(h->stage_q, q_host, qb, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return PKM_ERR_CUDA;
+  rc = run_lookup(h, h->stage_q, subkeys, B, H, n_keys, k, h->stage_idx, h->stage_w, s);
+  if (rc) return rc;
+  rc = run_gather(h, values, B, H, n_keys, k, h->stage_idx, h->stage_w, h->stage_out, s);
+  if (rc) return rc;
+  if (cudaMemcpyAsync(out_host, h->stage_out, (size_t)B * h->cfg.d_v * sizeof(float),
+                      cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return PKM_ERR_CUDA;
+  if (idx_host && cudaMemcpyAsync(idx_host, h->stage_idx, sel * sizeof(int64_t),
+                                  cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return PKM_ERR_CUDA;
+  if (w_host &&
+      cudaMemcpyAsync(w_host, h->stage_w, sel * sizeof(float), cudaMemcpyDeviceToHost, s) !=
+          cudaSuccess)
+    return PKM_ERR_CUDA;
+  return cuda_rc(cudaStreamSynchronize(s));
+}
+
+int pkm_get_status(pkm_t h, void* stream) {
+  if (!h) return PKM_ERR_INVALID;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int v = 0;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return PKM_ERR_CUDA;
+  if (cudaMemcpy(&v, h->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return PKM_ERR_CUDA;
+  if (v != PKM_OK && cudaMemset(h->status, 0, sizeof(int)) != cudaSuccess) return PKM_ERR_CUDA;
+  return v;
+}
+
+}  // extern "C"

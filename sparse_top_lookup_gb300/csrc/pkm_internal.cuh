@@ -1,0 +1,36 @@
+// Internal interface between the C-ABI layer (pkm_api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pkm.h"
+
+namespace pkm {
+
+// Device status word values are the PKM_ERR_* codes of pkm.h.
+
+// Step a6 (value read).  values: [N, d_v] of value_dtype; idx/w: [B, H*k];
+// out: [B, d_v] fp32.  Returns a cudaError_t of the launch.
+cudaError_t launch_gather(const void* values, int value_dtype, int64_t N, int d_v, int B,
+                          int rows_per_bag, const int64_t* idx, const float* w, float* out,
+                          int* status, cudaStream_t stream);
+
+// Steps a1-a5 for fp32 queries/subkeys on the CUDA cores.
+cudaError_t launch_lookup_simt(const float* q, const float* subkeys, int B, int H, int d_q,
+                               int n_keys, int k, int64_t* idx, float* w, cudaStream_t stream);
+
+// Steps a1-a5 for bf16 queries/subkeys: tcgen05 scoring with the selection,
+// merge and softmax fused into the epilogue.
+cudaError_t launch_lookup_tc(const uint16_t* q, const uint16_t* subkeys, int B, int H, int d_q,
+                             int n_keys, int k, int64_t* idx, float* w, int* status,
+                             cudaStream_t stream);
+
+// Limits of each path (checked on the host before a launch).
+constexpr int kSimtMaxK = 64;
+constexpr int kSimtMaxNKeys = 4096;
+constexpr int kSimtMaxDq = 8192;
+constexpr int kTcMaxK = 32;
+constexpr int kGatherMaxVecPerRow = 1024;  // 16-byte vectors per value row
+
+}  // namespace pkm

@@ -1,0 +1,95 @@
+"""The C ABI on a machine without a GPU: the library loads, exports every
+function include/pkm.h declares, and rejects bad arguments on the host
+before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import sparse_top_lookup_gb300 as pk
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "pkm.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    pk.build()
+    return pk.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkm_\w+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert "pkm_forward" in names and "pkm_create" in names and "pkm_destroy" in names
+    for n in names:
+        assert hasattr(L, n), n
+    assert sorted(pk.EXPORTED) == names
+
+
+def test_abi_version_and_strerror(L):
+    assert pk.pkm_abi_version() == 1
+    for code in range(-9, 1):
+        assert pk.pkm_strerror(code) != "unknown error code"
+    assert pk.pkm_strerror(-100) == "unknown error code"
+
+
+def cfg(**kw):
+    base = dict(d_q=1024, d_v=1024, max_B=16384, max_H=4, max_n_keys=1024, max_k=32,
+                q_dtype=pk.PKM_BF16)
+    base.update(kw)
+    return pk.make_config(**base)
+
+
+def test_check_args(L):
+    c = cfg()
+    assert pk.pkm_check_args(c, 16384, 4, 1024, 32) == pk.PKM_OK
+    assert pk.pkm_check_args(c, 0, 4, 1024, 32) == pk.PKM_OK
+    assert pk.pkm_check_args(c, 16385, 4, 1024, 32) == pk.PKM_ERR_RANGE
+    assert pk.pkm_check_args(c, 1, 5, 1024, 32) == pk.PKM_ERR_RANGE
+    assert pk.pkm_check_args(c, 1, 4, 16, 32) == pk.PKM_ERR_RANGE       # k > n_keys
+    assert pk.pkm_check_args(c, -1, 4, 1024, 32) == pk.PKM_ERR_INVALID
+    assert pk.pkm_check_args(c, 1, 4, 1024, 0) == pk.PKM_ERR_INVALID
+    assert pk.pkm_check_args(cfg(d_q=1023), 1, 1, 4, 1) == pk.PKM_ERR_INVALID
+    assert pk.pkm_check_args(cfg(d_q=1000), 1, 1, 4, 1) == pk.PKM_ERR_UNSUPPORTED  # TMA stride
+    assert pk.pkm_check_args(cfg(max_k=33), 1, 1, 64, 1) == pk.PKM_ERR_UNSUPPORTED
+    assert pk.pkm_check_args(cfg(max_k=64, q_dtype=pk.PKM_F32, max_n_keys=1024), 1, 1, 64, 64) \
+        == pk.PKM_OK
+    assert pk.pkm_check_args(cfg(d_v=1001), 1, 1, 64, 1) == pk.PKM_ERR_UNSUPPORTED
+    assert pk.pkm_check_args(cfg(max_n_keys=46341), 1, 1, 64, 1) == pk.PKM_ERR_UNSUPPORTED
+    assert pk.pkm_check_args(cfg(key_dtype=pk.PKM_F32), 1, 1, 64, 1) == pk.PKM_ERR_UNSUPPORTED
+    c2 = cfg()
+    c2.value_dtype = 7
+    assert pk.pkm_check_args(c2, 1, 1, 64, 1) == pk.PKM_ERR_UNSUPPORTED
+    assert L.pkm_check_args(None, 1, 1, 1, 1) == pk.PKM_ERR_INVALID
+
+
+def test_null_handle_rejected_before_any_cuda_call(L):
+    vp = ctypes.c_void_p
+    assert L.pkm_forward(None, 16, 16, 16, 1, 1, 1, 1, 16, None, None, None) == pk.PKM_ERR_INVALID
+    assert L.pkm_lookup(None, 16, 16, 1, 1, 1, 1, 16, 16, None) == pk.PKM_ERR_INVALID
+    assert L.pkm_gather(None, 16, 1, 1, 1, 1, 16, 16, 16, None) == pk.PKM_ERR_INVALID
+    assert L.pkm_forward_host(None, 16, 16, 16, 1, 1, 1, 1, 16, None, None, None) \
+        == pk.PKM_ERR_INVALID
+    assert L.pkm_get_status(None, None) == pk.PKM_ERR_INVALID
+    L.pkm_destroy(None)
+    assert L.pkm_create(None, None) == pk.PKM_ERR_INVALID
+    h = vp()
+    assert L.pkm_create(ctypes.byref(h), None) == pk.PKM_ERR_INVALID
+    bad = cfg(d_q=3)
+    assert L.pkm_create(ctypes.byref(h), ctypes.byref(bad)) == pk.PKM_ERR_INVALID
+    assert h.value is None
+
+
+def test_product_path_refuses_without_library(monkeypatch, tmp_path):
+    # No CPU fallback: a missing libpkm.so is an import-time error.
+    monkeypatch.setattr(pk, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(pk, "_lib", None)
+    with pytest.raises(ImportError):
+        pk.lib()

@@ -1,0 +1,215 @@
+"""GPU parity against the fp64 oracle, through the C ABI.
+
+Workloads small enough for the oracle to check every output: the fp32 tiny
+problem (CUDA-core path), the bf16 mid problem (tensor-core path), and edge
+shapes: ragged batch tails, n_keys not a multiple of the chunk width, k = 1,
+k = n_keys, exact integer ties, B = 0, out-of-range indices.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from helpers import TOL, compare_lookup, compare_out, make_handle, to_device
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+pk = pytest.importorskip("sparse_top_lookup_gb300")
+
+
+def run_forward(cfgd, q, C, V, B=None):
+    B = cfgd["B"] if B is None else B
+    H, k, d_v = cfgd["H"], cfgd["k"], cfgd["d_v"]
+    h, _ = make_handle(dict(cfgd, B=max(B, 1)))
+    try:
+        dq, dC, dV = (to_device(x, cfgd["dtype"]) for x in (q, C, V))
+        out = torch.empty(B, d_v, device="cuda")
+        idx = torch.empty(B, H, k, dtype=torch.int64, device="cuda")
+        w = torch.empty(B, H, k, device="cuda")
+        pk.check(pk.pkm_forward(h, dq, dC, dV, B, H, cfgd["n_keys"], k, out, idx, w), "forward")
+        assert pk.pkm_get_status(h) == pk.PKM_OK
+        return out.cpu().numpy(), idx.cpu().numpy(), w.cpu().numpy()
+    finally:
+        pk.pkm_destroy(h)
+
+
+def check_against_oracle(cfgd, q, C, V, max_near_frac=0.01):
+    B, H, d_q, n, d_v, k = (cfgd[x] for x in ("B", "H", "d_q", "n_keys", "d_v", "k"))
+    out, idx, w = run_forward(cfgd, q, C, V)
+    ref = oracle.lookup(q, C, B, H, d_q, n, k)
+    rep = compare_lookup(idx, w, ref, q, C, cfgd["dtype"], H, d_q, n)
+    assert rep["failures"] == 0, rep
+    assert rep["near_ties"] <= max_near_frac * B * H, rep
+    assert rep["w_ok"], rep
+    ref_out = oracle.gather(V, n * n, d_v, ref["idx"], ref["w"])
+    err = compare_out(out, V, n * n, d_v, idx, ref["idx"], ref["w"], ref_out)
+    assert err <= TOL, err
+    np.testing.assert_allclose(w.sum(-1), 1.0, atol=1e-5)
+    return rep
+
+
+def cfg_inputs(name):
+    c = synth.CONFIGS[name]
+    return c, synth.queries(c), synth.subkeys(c), synth.values(c)
+
+
+def test_tiny_fp32_matches_oracle_and_brute_force():
+    c, q, C, V = cfg_inputs("tiny")
+    check_against_oracle(c, q, C, V)
+    _, idx, _ = run_forward(c, q, C, V)
+    bi, _ = oracle.brute_topk(q, C, c["B"], c["H"], c["d_q"], c["n_keys"], c["k"])
+    assert (idx == bi).all(-1).mean() > 0.99
+
+
+def test_mid_bf16_matches_oracle():
+    c, q, C, V = cfg_inputs("mid")
+    rep = check_against_oracle(c, q, C, V)
+    print("mid parity:", rep)
+
+
+def random_case(seed, B, H, d_q, n, d_v, k, dtype="bf16", kvar=None):
+    c = dict(B=B, H=H, d_q=d_q, n_keys=n, d_v=d_v, k=k, dtype=dtype)
+    kvar = kvar if kvar is not None else 2.0 / d_q
+    q = synth.normal(seed, 1, B * H * d_q, 1.0, dtype=dtype)
+    C = synth.normal(seed, 2, H * 2 * n * (d_q // 2), kvar, dtype=dtype)
+    V = synth.normal(seed, 3, n * n * d_v, 1.0 / d_v, dtype=dtype)
+    return c, q, C, V
+
+
+@pytest.mark.parametrize("shape", [
+    # B, H, d_q, n, d_v, k
+    (300, 2, 128, 256, 128, 16),    # ragged batch tail (300 = 2*128 + 44)
+    (130, 3, 192, 100, 64, 8),      # n_keys not a multiple of 32, d_q/2 not a multiple of 64
+    (257, 1, 64, 520, 256, 32),     # three chunks, the last one partial
+    (64, 2, 256, 48, 128, 1),       # k = 1: argmax per half
+    (40, 1, 32, 20, 64, 20),        # k = n_keys: every key is a candidate
+    (129, 2, 1024, 1024, 1024, 32),  # page-width rows, small batch
+])
+def test_bf16_shapes(shape):
+    c, q, C, V = random_case(sum(shape), *shape)
+    check_against_oracle(c, q, C, V)
+
+
+def test_fp32_shapes():
+    c, q, C, V = random_case(7, 33, 3, 48, 40, 32, 12, dtype="f32", kvar=1.0)
+    check_against_oracle(c, q, C, V)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_exact_integer_ties_bit_exact(dtype):
+    # Small integers are exact in bf16/fp32 and every partial sum stays exact
+    # in fp32, so GPU and oracle scores are identical: the tie rule (lower
+    # subkey index per half, lower flat index overall) must match bit for bit.
+    rng = np.random.default_rng(3)
+    B, H, d_q, n, d_v, k = 200, 2, 64, 64, 32, 16
+    qf = rng.integers(-3, 4, (B, H, d_q)).astype(np.float32)
+    Cf = rng.integers(-2, 3, (H, 2, n, d_q // 2)).astype(np.float32)
+    Cf[:, 0, 10:20] = Cf[:, 0, 0:10]   # duplicated rows force exact ties in half 1
+    Cf[:, 1, 40:60] = Cf[:, 1, 5][:, None, :]  # and many in half 2
+    Vf = rng.standard_normal((n * n, d_v)).astype(np.float32)
+    if dtype == "bf16":
+        q, C, V = synth.f32_to_bf16(qf), synth.f32_to_bf16(Cf), synth.f32_to_bf16(Vf)
+    else:
+        q, C, V = qf, Cf, Vf
+    c = dict(B=B, H=H, d_q=d_q, n_keys=n, d_v=d_v, k=k, dtype=dtype)
+    out, idx, w = run_forward(c, q.ravel(), C.ravel(), V.ravel())
+    ref = oracle.lookup(q.ravel(), C.ravel(), B, H, d_q, n, k)
+    assert np.array_equal(idx, ref["idx"])
+    assert (np.abs(w - ref["w"]) <= 1e-6 * (1 + ref["w"])).all()
+
+
+def test_gather_alone_fed_oracle_selection():
+    # Step a6 in isolation: oracle indices and weights in, fp64 read out.
+    for name in ("tiny", "mid"):
+        c, q, C, V = cfg_inputs(name)
+        B, H, d_q, n, d_v, k = (c[x] for x in ("B", "H", "d_q", "n_keys", "d_v", "k"))
+        ref = oracle.lookup(q, C, B, H, d_q, n, k)
+        w32 = ref["w"].astype(np.float32)
+        expect = oracle.gather(V, n * n, d_v, ref["idx"], w32.astype(np.float64))
+        h, _ = make_handle(c)
+        try:
+            out = torch.empty(B, d_v, device="cuda")
+            pk.check(pk.pkm_gather(h, to_device(V, c["dtype"]), B, H, n, k,
+                                   torch.from_numpy(ref["idx"]).cuda(),
+                                   torch.from_numpy(w32).cuda(), out), "gather")
+            assert pk.pkm_get_status(h) == pk.PKM_OK
+            got = out.cpu().numpy().astype(np.float64)
+        finally:
+            pk.pkm_destroy(h)
+        assert (np.abs(got - expect) <= 1e-5 * (1 + np.abs(expect))).all(), name
+
+
+def test_gather_closed_form_ones_and_bad_index():
+    B, H, k, n, d_v = 50, 3, 4, 16, 512
+    c = dict(B=B, H=H, d_q=32, n_keys=n, d_v=d_v, k=k, dtype="bf16")
+    h, _ = make_handle(c)
+    try:
+        V = torch.ones(n * n, d_v, dtype=torch.bfloat16, device="cuda")
+        idx = torch.randint(0, n * n, (B, H, k), device="cuda")
+        w = torch.full((B, H, k), 1.0 / k, device="cuda")
+        out = torch.empty(B, d_v, device="cuda")
+        pk.check(pk.pkm_gather(h, V, B, H, n, k, idx, w, out), "gather")
+        assert pk.pkm_get_status(h) == pk.PKM_OK
+        torch.testing.assert_close(out, torch.full_like(out, float(H)), rtol=1e-6, atol=1e-6)
+        idx[3, 1, 2] = n * n          # out of range: skipped and reported
+        idx[7, 0, 0] = -1
+        pk.check(pk.pkm_gather(h, V, B, H, n, k, idx, w, out), "gather")
+        assert pk.pkm_get_status(h) == pk.PKM_ERR_BAD_INDEX
+        assert pk.pkm_get_status(h) == pk.PKM_OK  # reading resets the word
+        assert abs(out[3, 0].item() - (H - 1.0 / k)) < 1e-6
+    finally:
+        pk.pkm_destroy(h)
+
+
+def test_empty_batch_and_argument_errors():
+    c = dict(B=8, H=1, d_q=64, n_keys=32, d_v=64, k=4, dtype="bf16")
+    h, cfg = make_handle(c)
+    try:
+        t = torch.zeros(1024, dtype=torch.bfloat16, device="cuda")
+        o = torch.zeros(64, dtype=torch.float32, device="cuda")
+        assert pk.pkm_forward(h, t, t, t, 0, 1, 32, 4, o) == pk.PKM_OK       # B = 0: no-op
+        assert pk.pkm_forward(h, t, t, t, 9, 1, 32, 4, o) == pk.PKM_ERR_RANGE  # B > max_B
+        assert pk.pkm_forward(h, t, t, t, 1, 1, 32, 33, o) == pk.PKM_ERR_RANGE
+        assert pk.pkm_forward(h, None, t, t, 1, 1, 32, 4, o) == pk.PKM_ERR_INVALID
+        assert pk.pkm_forward(h, t.data_ptr() + 2, t, t, 1, 1, 32, 4, o) == pk.PKM_ERR_ALIGN
+        assert pk.pkm_forward_host(h, np.zeros(64, np.uint16), t, t, 1, 1, 32, 4,
+                                   np.zeros(64, np.float32)) == pk.PKM_ERR_NO_STAGING
+        assert pk.pkm_get_status(h) == pk.PKM_OK
+    finally:
+        pk.pkm_destroy(h)
+
+
+def test_forward_host_matches_device_forward():
+    c, q, C, V = cfg_inputs("mid")
+    B = 1000
+    c = dict(c, B=B)
+    q = q[: B * c["H"] * c["d_q"]]
+    out_d, idx_d, w_d = run_forward(c, q, C, V)
+    h, _ = make_handle(c, staging=True)
+    try:
+        qh = torch.from_numpy(q.view(np.int16)).pin_memory()
+        oh = torch.empty(B, c["d_v"]).pin_memory()
+        ih = torch.empty(B, c["H"], c["k"], dtype=torch.int64).pin_memory()
+        wh = torch.empty(B, c["H"], c["k"]).pin_memory()
+        pk.check(pk.pkm_forward_host(h, qh, to_device(C, "bf16"), to_device(V, "bf16"), B, c["H"],
+                                     c["n_keys"], c["k"], oh, ih, wh), "forward_host")
+        assert np.array_equal(ih.numpy(), idx_d)
+        assert np.array_equal(wh.numpy(), w_d)
+        assert np.array_equal(oh.numpy(), out_d)
+    finally:
+        pk.pkm_destroy(h)
+
+
+def test_forward_with_scratch_selection_matches():
+    # idx/w == NULL: the handle's scratch holds the selection.
+    c, q, C, V = cfg_inputs("tiny")
+    out_a, _, _ = run_forward(c, q, C, V)
+    h, _ = make_handle(c)
+    try:
+        out = torch.empty(c["B"], c["d_v"], device="cuda")
+        pk.check(pk.pkm_forward(h, to_device(q, "f32"), to_device(C, "f32"), to_device(V, "f32"),
+                                c["B"], c["H"], c["n_keys"], c["k"], out), "forward")
+        assert np.array_equal(out.cpu().numpy(), out_a)
+    finally:
+        pk.pkm_destroy(h)
