@@ -76,7 +76,17 @@ enum {
   PKM_ERR_NOMEM = -6,       /* pkm_create could not allocate its scratch */
   PKM_ERR_TIMEOUT = -7,     /* device: a bounded wait inside a kernel gave up */
   PKM_ERR_BAD_INDEX = -8,   /* device: a row index outside [0, n_keys^2) reached the value read */
-  PKM_ERR_NO_STAGING = -9   /* pkm_forward_host on a handle created without host staging */
+  PKM_ERR_NO_STAGING = -9,  /* pkm_forward_host on a handle created without host staging */
+  PKM_ERR_OPTION = -10      /* pkm_set_option: unknown option or value */
+};
+
+/* options of pkm_set_option */
+enum {
+  /* bf16 path: the per-row selection threshold is mean + z * spread of the
+     row's first-chunk scores.  Any finite z gives exact results (a low z costs
+     more log compactions, a high z sends rows to the CUDA-core fallback);
+     NaN restores the automatic choice. */
+  PKM_OPT_HINT_Z = 1
 };
 
 typedef struct pkm_handle *pkm_t;
@@ -134,6 +144,14 @@ int pkm_gather(pkm_t h, const void *values, int B, int H, int n_keys, int k, con
 int pkm_forward_host(pkm_t h, const void *q_host, const void *subkeys, const void *values, int B,
                      int H, int n_keys, int k, float *out_host, int64_t *idx_host, float *w_host,
                      void *stream);
+
+/* Set a tuning option of a handle (PKM_OPT_*).  Affects later calls only. */
+int pkm_set_option(pkm_t h, int option, double value);
+
+/* Synchronise `stream` and report in *count how many (query, head) pairs the
+   last bf16 lookup on this handle recomputed on the CUDA cores because the
+   selection threshold hint was above their k-th score. */
+int pkm_get_fallback_count(pkm_t h, void *stream, int *count);
 
 /* Synchronise `stream`, return the device status word (PKM_OK or a device error
    code) and reset it to PKM_OK. */

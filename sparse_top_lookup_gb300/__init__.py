@@ -17,11 +17,12 @@ PKM_F32, PKM_BF16 = 0, 1
 PKM_OK = 0
 PKM_ERR_INVALID, PKM_ERR_RANGE, PKM_ERR_UNSUPPORTED, PKM_ERR_ALIGN = -1, -2, -3, -4
 PKM_ERR_CUDA, PKM_ERR_NOMEM, PKM_ERR_TIMEOUT, PKM_ERR_BAD_INDEX = -5, -6, -7, -8
-PKM_ERR_NO_STAGING = -9
+PKM_ERR_NO_STAGING, PKM_ERR_OPTION = -9, -10
+PKM_OPT_HINT_Z = 1
 
 EXPORTED = ["pkm_create", "pkm_destroy", "pkm_forward", "pkm_lookup", "pkm_gather",
             "pkm_forward_host", "pkm_get_status", "pkm_check_args", "pkm_strerror",
-            "pkm_abi_version"]
+            "pkm_abi_version", "pkm_set_option", "pkm_get_fallback_count"]
 
 
 class pkm_config(ctypes.Structure):
@@ -66,8 +67,11 @@ def lib():
         L.pkm_strerror.argtypes = [i32]
         L.pkm_strerror.restype = ctypes.c_char_p
         L.pkm_abi_version.argtypes = []
+        L.pkm_set_option.argtypes = [vp, i32, ctypes.c_double]
+        L.pkm_get_fallback_count.argtypes = [vp, vp, ctypes.POINTER(i32)]
         for f in ("pkm_create", "pkm_forward", "pkm_lookup", "pkm_gather", "pkm_forward_host",
-                  "pkm_get_status", "pkm_check_args", "pkm_abi_version"):
+                  "pkm_get_status", "pkm_check_args", "pkm_abi_version", "pkm_set_option",
+                  "pkm_get_fallback_count"):
             getattr(L, f).restype = i32
         _lib = L
     return _lib
@@ -147,6 +151,18 @@ def pkm_forward_host(h, q_host, subkeys, values, B, H, n_keys, k, out_host, idx_
     return lib().pkm_forward_host(h, _addr(q_host), _addr(subkeys), _addr(values), B, H, n_keys, k,
                                   _addr(out_host), _addr(idx_host), _addr(w_host),
                                   _stream(stream))
+
+
+def pkm_set_option(h, option, value):
+    return lib().pkm_set_option(h, option, float(value))
+
+
+def pkm_get_fallback_count(h, stream=None):
+    """Pairs the last bf16 lookup recomputed on the CUDA cores (synchronises)."""
+    c = ctypes.c_int()
+    check(lib().pkm_get_fallback_count(h, _stream(stream), ctypes.byref(c)),
+          "pkm_get_fallback_count")
+    return c.value
 
 
 def pkm_get_status(h, stream=None):

@@ -1,4 +1,6 @@
-// Steps a1-a5 for fp32 queries and subkeys, on the CUDA cores.
+// Steps a1-a5 on the CUDA cores: the path for fp32 queries and subkeys, and
+// the exact fallback of the tensor-core path for bf16 (rows whose selection
+// threshold hint turned out too high are listed and recomputed here).
 //
 // Product-Key Memory, "Factorising the key space": score each half of the
 // query against its own subkey set, keep the top-k of each half, form the k^2
@@ -7,7 +9,9 @@
 // problems (the tensor-core path takes bf16); it is plain and exact: one CTA
 // per (query, head), fp32 FMA dot products, and every selection done by
 // ranking, so ties follow the same total orders as everywhere else: (score
-// desc, subkey asc) within a half and (score desc, flat asc) overall.
+// desc, subkey asc) within a half and (score desc, flat asc) overall.  The
+// dot products are fp32 FMA; the order of the additions inside one dot
+// product is the lane-strided partial sums described at the scoring step.
 #include <float.h>
 #include <stdint.h>
 
@@ -16,12 +20,39 @@
 namespace pkm {
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;
 
-__global__ void __launch_bounds__(kThreads)
-lookup_simt_kernel(const float* __restrict__ q, const float* __restrict__ subkeys, int H, int d_q,
-                   int n, int k, int64_t* __restrict__ idx, float* __restrict__ w) {
-  extern __shared__ __align__(16) unsigned char smem[];
+__device__ __forceinline__ float load_elem(const float* p, int64_t i) { return p[i]; }
+__device__ __forceinline__ float load_elem(const uint16_t* p, int64_t i) {
+  return __uint_as_float((uint32_t)p[i] << 16);
+}
+
+// Products of one 16-byte vector of subkey elements with the matching query
+// elements, accumulated in element order.
+__device__ __forceinline__ float dot16(const uint4& u, const float* qv, const float*) {
+  float acc = 0.0f;
+  acc = fmaf(__uint_as_float(u.x), qv[0], acc);
+  acc = fmaf(__uint_as_float(u.y), qv[1], acc);
+  acc = fmaf(__uint_as_float(u.z), qv[2], acc);
+  acc = fmaf(__uint_as_float(u.w), qv[3], acc);
+  return acc;
+}
+__device__ __forceinline__ float dot16(const uint4& u, const float* qv, const uint16_t*) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+  float acc = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    acc = fmaf(__uint_as_float(w[i] << 16), qv[2 * i], acc);
+    acc = fmaf(__uint_as_float(w[i] & 0xffff0000u), qv[2 * i + 1], acc);
+  }
+  return acc;
+}
+
+// Steps a1-a5 for one (query, head) pair, by the whole CTA.
+template <typename TIn>
+__device__ void lookup_pair(const TIn* __restrict__ q, const TIn* __restrict__ subkeys, int H,
+                            int d_q, int n, int k, int64_t pair, int64_t* __restrict__ idx,
+                            float* __restrict__ w, unsigned char* smem) {
   const int hd = d_q / 2;
   float* s_q = reinterpret_cast<float*>(smem);         // [d_q]
   float* s_sc = s_q + d_q;                             // [2][n]
@@ -32,22 +63,40 @@ lookup_simt_kernel(const float* __restrict__ q, const float* __restrict__ subkey
   float* s_ov = reinterpret_cast<float*>(s_cf + k * k);  // [k] output scores
   int* s_of = reinterpret_cast<int*>(s_ov + k);          // [k] output flats
   float* s_z = reinterpret_cast<float*>(s_of + k);       // softmax denominator
-
-  const int64_t pair = blockIdx.x;  // b * H + h
-  const int h = (int)(pair % H);
   const int tid = threadIdx.x;
+  const int h = (int)(pair % H);
 
-  for (int t = tid; t < d_q; t += kThreads) s_q[t] = q[pair * d_q + t];
+  __syncthreads();  // shared data of a previous pair is no longer read
+  for (int t = tid; t < d_q; t += kThreads) s_q[t] = load_elem(q, pair * d_q + t);
   __syncthreads();
 
-  // a2: subkey scores of both halves.
-  for (int e = tid; e < 2 * n; e += kThreads) {
-    const int half = e / n, a = e - half * n;
-    const float* c = subkeys + (((int64_t)h * 2 + half) * n + a) * hd;
-    const float* qh = s_q + half * hd;
-    float acc = 0.0f;
-    for (int t = 0; t < hd; ++t) acc = fmaf(qh[t], c[t], acc);
-    s_sc[e] = acc;
+  // a2: subkey scores of both halves.  When a subkey row is a whole number
+  // of 16-byte vectors, one warp reads a row (coalesced), each lane takes every
+  // 32nd vector and the lanes' partial sums are added with shuffles.
+  constexpr int EPV = 16 / (int)sizeof(TIn);
+  if (hd % EPV == 0) {
+    const int warp = tid >> 5, lane = tid & 31;
+    const int nvec = hd / EPV;
+    for (int e = warp; e < 2 * n; e += kThreads / 32) {
+      const int half = e / n, a = e - half * n;
+      const uint4* row =
+          reinterpret_cast<const uint4*>(subkeys + (((int64_t)h * 2 + half) * n + a) * hd);
+      const float* qh = s_q + half * hd;
+      float acc = 0.0f;
+      for (int vi = lane; vi < nvec; vi += 32) acc += dot16(row[vi], qh + vi * EPV, subkeys);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      if (lane == 0) s_sc[e] = acc;
+    }
+  } else {
+    for (int e = tid; e < 2 * n; e += kThreads) {
+      const int half = e / n, a = e - half * n;
+      const int64_t c = (((int64_t)h * 2 + half) * n + a) * hd;
+      const float* qh = s_q + half * hd;
+      float acc = 0.0f;
+      for (int t = 0; t < hd; ++t) acc = fmaf(qh[t], load_elem(subkeys, c + t), acc);
+      s_sc[e] = acc;
+    }
   }
   __syncthreads();
 
@@ -99,21 +148,58 @@ lookup_simt_kernel(const float* __restrict__ q, const float* __restrict__ subkey
   }
 }
 
+// With pair_list == nullptr CTA b handles pair b; otherwise the CTAs walk
+// pair_list[0 .. *pair_count).
+template <typename TIn>
+__global__ void __launch_bounds__(kThreads)
+lookup_simt_kernel(const TIn* __restrict__ q, const TIn* __restrict__ subkeys, int H, int d_q,
+                   int n, int k, int64_t* __restrict__ idx, float* __restrict__ w,
+                   const int* __restrict__ pair_count, const int* __restrict__ pair_list) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  if (!pair_list) {
+    lookup_pair(q, subkeys, H, d_q, n, k, (int64_t)blockIdx.x, idx, w, smem);
+    return;
+  }
+  const int npairs = *pair_count;
+  for (int it = blockIdx.x; it < npairs; it += gridDim.x)
+    lookup_pair(q, subkeys, H, d_q, n, k, (int64_t)pair_list[it], idx, w, smem);
+}
+
+size_t simt_smem(int d_q, int n_keys, int k) {
+  return (size_t)d_q * 4 + (size_t)2 * n_keys * 4 + (size_t)4 * k * 4 + (size_t)2 * k * k * 4 +
+         (size_t)2 * k * 4 + 16;
+}
+
 }  // namespace
 
 cudaError_t launch_lookup_simt(const float* q, const float* subkeys, int B, int H, int d_q,
                                int n_keys, int k, int64_t* idx, float* w, cudaStream_t stream) {
   if (B == 0) return cudaSuccess;
-  const size_t smem = (size_t)d_q * 4 + (size_t)2 * n_keys * 4 + (size_t)4 * k * 4 +
-                      (size_t)2 * k * k * 4 + (size_t)2 * k * 4 + 16;
+  const size_t smem = simt_smem(d_q, n_keys, k);
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(lookup_simt_kernel,
+    cudaError_t e = cudaFuncSetAttribute(lookup_simt_kernel<float>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
   const int64_t pairs = (int64_t)B * H;
-  lookup_simt_kernel<<<(unsigned)pairs, kThreads, smem, stream>>>(q, subkeys, H, d_q, n_keys, k,
-                                                                  idx, w);
+  lookup_simt_kernel<float><<<(unsigned)pairs, kThreads, smem, stream>>>(
+      q, subkeys, H, d_q, n_keys, k, idx, w, nullptr, nullptr);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lookup_fallback(const uint16_t* q, const uint16_t* subkeys, int B, int H,
+                                   int d_q, int n_keys, int k, const int* pair_count,
+                                   const int* pair_list, int64_t* idx, float* w, int grid,
+                                   cudaStream_t stream) {
+  if (B == 0) return cudaSuccess;
+  const size_t smem = simt_smem(d_q, n_keys, k);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(lookup_simt_kernel<uint16_t>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  lookup_simt_kernel<uint16_t><<<grid, kThreads, smem, stream>>>(
+      q, subkeys, H, d_q, n_keys, k, idx, w, pair_count, pair_list);
   return cudaGetLastError();
 }
 

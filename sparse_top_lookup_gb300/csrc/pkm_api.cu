@@ -1,6 +1,7 @@
 // The C ABI of include/pkm.h: argument checks, scratch ownership and launch
 // order.  No arithmetic of the lookup lives here.
 #include <cuda_runtime.h>
+#include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 
@@ -12,6 +13,9 @@ struct pkm_handle {
   int64_t* ws_idx;   // [max_B, max_H, max_k] when the caller passes idx == NULL
   float* ws_w;       // [max_B, max_H, max_k] when the caller passes w == NULL
   int* status;       // device status word
+  int* fb_count;     // pairs recomputed by the fallback in the last bf16 lookup
+  int* fb_list;      // [max_B * max_H] their (query * H + head) indices
+  float hint_z;      // selection threshold hint override (NaN: automatic)
   void* stage_q;     // pkm_forward_host staging (optional)
   float* stage_out;
   int64_t* stage_idx;
@@ -59,10 +63,12 @@ int cuda_rc(cudaError_t e) { return e == cudaSuccess ? PKM_OK : PKM_ERR_CUDA; }
 
 int run_lookup(pkm_t h, const void* q, const void* subkeys, int B, int H, int n, int k,
                int64_t* idx, float* w, cudaStream_t s) {
-  if (h->cfg.q_dtype == PKM_BF16)
+  if (h->cfg.q_dtype == PKM_BF16) {
+    const float z = isnan(h->hint_z) ? pkm::default_hint_z(n, k) : h->hint_z;
     return cuda_rc(pkm::launch_lookup_tc(static_cast<const uint16_t*>(q),
                                          static_cast<const uint16_t*>(subkeys), B, H, h->cfg.d_q,
-                                         n, k, idx, w, h->status, s));
+                                         n, k, z, idx, w, h->status, h->fb_count, h->fb_list, s));
+  }
   return cuda_rc(pkm::launch_lookup_simt(static_cast<const float*>(q),
                                          static_cast<const float*>(subkeys), B, H, h->cfg.d_q, n,
                                          k, idx, w, s));
@@ -92,6 +98,7 @@ const char* pkm_strerror(int code) {
     case PKM_ERR_TIMEOUT: return "a bounded wait inside a kernel gave up";
     case PKM_ERR_BAD_INDEX: return "row index outside the value table";
     case PKM_ERR_NO_STAGING: return "handle was created without host staging";
+    case PKM_ERR_OPTION: return "unknown option or value";
     default: return "unknown error code";
   }
 }
@@ -105,6 +112,8 @@ void pkm_destroy(pkm_t h) {
   cudaFree(h->ws_idx);
   cudaFree(h->ws_w);
   cudaFree(h->status);
+  cudaFree(h->fb_count);
+  cudaFree(h->fb_list);
   cudaFree(h->stage_q);
   cudaFree(h->stage_out);
   cudaFree(h->stage_idx);
@@ -119,6 +128,7 @@ int pkm_create(pkm_t* out, const pkm_config* cfg) {
   pkm_t h = static_cast<pkm_t>(calloc(1, sizeof(pkm_handle)));
   if (!h) return PKM_ERR_NOMEM;
   h->cfg = *cfg;
+  h->hint_z = NAN;
   if (cudaGetDevice(&h->device) != cudaSuccess) {
     free(h);
     return PKM_ERR_CUDA;
@@ -129,6 +139,12 @@ int pkm_create(pkm_t* out, const pkm_config* cfg) {
   if (ok && sel) {
     ok = cudaMalloc(&h->ws_idx, sel * sizeof(int64_t)) == cudaSuccess &&
          cudaMalloc(&h->ws_w, sel * sizeof(float)) == cudaSuccess;
+  }
+  if (ok) {
+    const size_t pairs = (size_t)cfg->max_B * cfg->max_H;
+    ok = cudaMalloc(&h->fb_count, sizeof(int)) == cudaSuccess &&
+         cudaMemset(h->fb_count, 0, sizeof(int)) == cudaSuccess &&
+         cudaMalloc(&h->fb_list, (pairs ? pairs : 1) * sizeof(int)) == cudaSuccess;
   }
   if (ok && cfg->host_staging && cfg->max_B) {
     const size_t qb = (size_t)cfg->max_B * cfg->max_H * cfg->d_q * elem_size(cfg->q_dtype);
@@ -218,6 +234,26 @@ int pkm_forward_host(pkm_t h, const void* q_host, const void* subkeys, const voi
           cudaSuccess)
     return PKM_ERR_CUDA;
   return cuda_rc(cudaStreamSynchronize(s));
+}
+
+int pkm_set_option(pkm_t h, int option, double value) {
+  if (!h) return PKM_ERR_INVALID;
+  switch (option) {
+    case PKM_OPT_HINT_Z:
+      if (!isnan(value) && !isfinite(value)) return PKM_ERR_OPTION;
+      h->hint_z = (float)value;
+      return PKM_OK;
+    default:
+      return PKM_ERR_OPTION;
+  }
+}
+
+int pkm_get_fallback_count(pkm_t h, void* stream, int* count) {
+  if (!h || !count) return PKM_ERR_INVALID;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return PKM_ERR_CUDA;
+  if (cudaMemcpy(count, h->fb_count, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return PKM_ERR_CUDA;
+  return PKM_OK;
 }
 
 int pkm_get_status(pkm_t h, void* stream) {

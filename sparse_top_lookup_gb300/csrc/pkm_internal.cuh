@@ -21,10 +21,23 @@ cudaError_t launch_lookup_simt(const float* q, const float* subkeys, int B, int 
                                int n_keys, int k, int64_t* idx, float* w, cudaStream_t stream);
 
 // Steps a1-a5 for bf16 queries/subkeys: tcgen05 scoring with the selection,
-// merge and softmax fused into the epilogue.
+// merge and softmax fused into the epilogue.  hint_z sets the per-row
+// selection threshold (mean + hint_z * spread of a row's scores; any value
+// gives exact results).  fb_count / fb_list: device scratch (1 and B*H ints)
+// listing the (query, head) pairs recomputed by the CUDA-core fallback.
 cudaError_t launch_lookup_tc(const uint16_t* q, const uint16_t* subkeys, int B, int H, int d_q,
-                             int n_keys, int k, int64_t* idx, float* w, int* status,
-                             cudaStream_t stream);
+                             int n_keys, int k, float hint_z, int64_t* idx, float* w, int* status,
+                             int* fb_count, int* fb_list, cudaStream_t stream);
+
+// The hint_z launch_lookup_tc uses unless a handle overrides it.
+float default_hint_z(int n_keys, int k);
+
+// Exact recomputation of the listed (query, head) pairs, bf16 inputs, fp32
+// FMA on the CUDA cores; grid CTAs walk pair_list[0 .. *pair_count).
+cudaError_t launch_lookup_fallback(const uint16_t* q, const uint16_t* subkeys, int B, int H,
+                                   int d_q, int n_keys, int k, const int* pair_count,
+                                   const int* pair_list, int64_t* idx, float* w, int grid,
+                                   cudaStream_t stream);
 
 // Limits of each path (checked on the host before a launch).
 constexpr int kSimtMaxK = 64;

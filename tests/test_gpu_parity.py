@@ -18,25 +18,29 @@ torch = pytest.importorskip("torch")
 pk = pytest.importorskip("sparse_top_lookup_gb300")
 
 
-def run_forward(cfgd, q, C, V, B=None):
+def run_forward(cfgd, q, C, V, B=None, hint_z=None, report=None):
     B = cfgd["B"] if B is None else B
     H, k, d_v = cfgd["H"], cfgd["k"], cfgd["d_v"]
     h, _ = make_handle(dict(cfgd, B=max(B, 1)))
     try:
+        if hint_z is not None:
+            pk.check(pk.pkm_set_option(h, pk.PKM_OPT_HINT_Z, hint_z), "set_option")
         dq, dC, dV = (to_device(x, cfgd["dtype"]) for x in (q, C, V))
         out = torch.empty(B, d_v, device="cuda")
         idx = torch.empty(B, H, k, dtype=torch.int64, device="cuda")
         w = torch.empty(B, H, k, device="cuda")
         pk.check(pk.pkm_forward(h, dq, dC, dV, B, H, cfgd["n_keys"], k, out, idx, w), "forward")
         assert pk.pkm_get_status(h) == pk.PKM_OK
+        if report is not None and cfgd["dtype"] == "bf16":
+            report["fallback"] = pk.pkm_get_fallback_count(h)
         return out.cpu().numpy(), idx.cpu().numpy(), w.cpu().numpy()
     finally:
         pk.pkm_destroy(h)
 
 
-def check_against_oracle(cfgd, q, C, V, max_near_frac=0.01):
+def check_against_oracle(cfgd, q, C, V, max_near_frac=0.01, hint_z=None, report=None):
     B, H, d_q, n, d_v, k = (cfgd[x] for x in ("B", "H", "d_q", "n_keys", "d_v", "k"))
-    out, idx, w = run_forward(cfgd, q, C, V)
+    out, idx, w = run_forward(cfgd, q, C, V, hint_z=hint_z, report=report)
     ref = oracle.lookup(q, C, B, H, d_q, n, k)
     rep = compare_lookup(idx, w, ref, q, C, cfgd["dtype"], H, d_q, n)
     assert rep["failures"] == 0, rep
@@ -64,8 +68,11 @@ def test_tiny_fp32_matches_oracle_and_brute_force():
 
 def test_mid_bf16_matches_oracle():
     c, q, C, V = cfg_inputs("mid")
-    rep = check_against_oracle(c, q, C, V)
-    print("mid parity:", rep)
+    info = {}
+    rep = check_against_oracle(c, q, C, V, report=info)
+    print("mid parity:", rep, info)
+    # normally distributed scores: the automatic threshold hint never falls back
+    assert info["fallback"] == 0
 
 
 def random_case(seed, B, H, d_q, n, d_v, k, dtype="bf16", kvar=None):
@@ -89,6 +96,21 @@ def random_case(seed, B, H, d_q, n, d_v, k, dtype="bf16", kvar=None):
 def test_bf16_shapes(shape):
     c, q, C, V = random_case(sum(shape), *shape)
     check_against_oracle(c, q, C, V)
+
+
+@pytest.mark.parametrize("z", [1e30, -1e30, -1.0, 0.5, 2.5])
+def test_selection_exact_for_any_threshold_hint(z):
+    # The per-row threshold hint only steers cost.  A huge z leaves every row
+    # with too few logged scores, so every pair goes to the CUDA-core
+    # fallback; a very negative z logs every score and exercises repeated log
+    # compactions.  Either way the result is the oracle's.
+    c, q, C, V = random_case(99, 260, 2, 256, 512, 128, 32)
+    info = {}
+    check_against_oracle(c, q, C, V, hint_z=z, report=info)
+    if z == 1e30:
+        assert info["fallback"] == c["B"] * c["H"]
+    if z <= -1.0:
+        assert info["fallback"] == 0
 
 
 def test_fp32_shapes():
