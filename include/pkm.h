@@ -166,6 +166,36 @@ const char *pkm_strerror(int code);
 /* PKM_ABI_VERSION of the library. */
 int pkm_abi_version(void);
 
+/*
+ * No counterpart on the pages: a library-level addition for callers that
+ * cannot allocate device memory when they run a lookup (a serving process
+ * whose GPU memory is budgeted at start-up, a host framework that owns every
+ * device allocation through its own pool, a hot loop where cudaMalloc or
+ * cudaFree would synchronise the device).  pkm_create allocates, so this
+ * entry point takes no handle.
+ *
+ * pkm_lookup_static: the lookup alone (scoring through softmax) for bf16
+ * queries and subkeys, as pkm_lookup on a bf16 handle with d_q given here:
+ * idx and w [B, H, k] are written on `stream`.  It allocates nothing: its
+ * scratch (a status word and the list of (query, head) pairs recomputed on
+ * the CUDA cores, at most PKM_STATIC_MAX_PAIRS of them) is one fixed array of
+ * (PKM_STATIC_MAX_PAIRS + 2) * 4 bytes in the library's device memory, which
+ * every GPU that loads the library holds until the process exits.
+ *   - B * H above PKM_STATIC_MAX_PAIRS returns PKM_ERR_RANGE; other argument
+ *     errors are as for pkm_lookup.
+ *   - status: if not NULL, a device int that receives the call's device
+ *     status (PKM_OK or PKM_ERR_TIMEOUT) on `stream`.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) and caches it; make that first call before any
+ *     stream capture.
+ *   - All calls share the one array, and each call clears what must start at
+ *     zero.  Calls whose work overlaps on the GPU (other streams, other host
+ *     threads) race on it: serialise them.
+ */
+#define PKM_STATIC_MAX_PAIRS (1 << 20)
+int pkm_lookup_static(const void *q, const void *subkeys, int B, int H, int d_q, int n_keys, int k,
+                      int64_t *idx, float *w, int *status, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -22,7 +22,8 @@ PKM_OPT_HINT_Z = 1
 
 EXPORTED = ["pkm_create", "pkm_destroy", "pkm_forward", "pkm_lookup", "pkm_gather",
             "pkm_forward_host", "pkm_get_status", "pkm_check_args", "pkm_strerror",
-            "pkm_abi_version", "pkm_set_option", "pkm_get_fallback_count"]
+            "pkm_abi_version", "pkm_set_option", "pkm_get_fallback_count", "pkm_lookup_static"]
+PKM_STATIC_MAX_PAIRS = 1 << 20
 
 
 class pkm_config(ctypes.Structure):
@@ -68,10 +69,11 @@ def lib():
         L.pkm_strerror.restype = ctypes.c_char_p
         L.pkm_abi_version.argtypes = []
         L.pkm_set_option.argtypes = [vp, i32, ctypes.c_double]
+        L.pkm_lookup_static.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp]
         L.pkm_get_fallback_count.argtypes = [vp, vp, ctypes.POINTER(i32)]
         for f in ("pkm_create", "pkm_forward", "pkm_lookup", "pkm_gather", "pkm_forward_host",
                   "pkm_get_status", "pkm_check_args", "pkm_abi_version", "pkm_set_option",
-                  "pkm_get_fallback_count"):
+                  "pkm_get_fallback_count", "pkm_lookup_static"):
             getattr(L, f).restype = i32
         _lib = L
     return _lib
@@ -163,6 +165,12 @@ def pkm_get_fallback_count(h, stream=None):
     check(lib().pkm_get_fallback_count(h, _stream(stream), ctypes.byref(c)),
           "pkm_get_fallback_count")
     return c.value
+
+
+def pkm_lookup_static(q, subkeys, B, H, d_q, n_keys, k, idx, w, status=None, stream=None):
+    """The bf16 lookup without a handle or any device allocation (see include/pkm.h)."""
+    return lib().pkm_lookup_static(_addr(q), _addr(subkeys), B, H, d_q, n_keys, k, _addr(idx),
+                                   _addr(w), _addr(status), _stream(stream))
 
 
 def pkm_get_status(h, stream=None):

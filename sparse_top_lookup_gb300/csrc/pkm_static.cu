@@ -1,0 +1,79 @@
+// pkm_lookup_static: the bf16 lookup without a handle and without any
+// device allocation.
+//
+// Some callers cannot allocate device memory at the point where they run a
+// lookup: a serving process whose GPU memory budget is fixed when it starts,
+// a host framework that owns every device allocation through its own pool,
+// or a latency-critical loop where cudaMalloc / cudaFree would synchronise
+// the device.  pkm_create allocates the handle's scratch, so those callers
+// use this entry point instead.  Its scratch (a status word, the count and
+// the list of (query, head) pairs sent to the CUDA-core fallback) is one
+// fixed-size array in the library's device memory, present on every GPU that
+// loads the library until the process exits.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "pkm_internal.cuh"
+
+namespace {
+
+// [0] device status word, [1] fallback pair count, [2 ..] fallback pair list
+constexpr int kStaticWords = 2 + PKM_STATIC_MAX_PAIRS;
+static __device__ __align__(256) int g_static_scratch[kStaticWords];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_setup_mutex;
+int* g_scratch_addr[kMaxDevices] = {};  // device address of g_static_scratch, per device
+
+// Device address of the scratch array on the current device.  The first call
+// on a device looks it up (cudaGetSymbolAddress); later calls reuse it.
+int scratch_on_current_device(int** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PKM_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_setup_mutex);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) {
+      cudaGetLastError();
+      return PKM_ERR_CUDA;
+    }
+    g_scratch_addr[dev] = static_cast<int*>(p);
+  }
+  *out = g_scratch_addr[dev];
+  return PKM_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" int pkm_lookup_static(const void* q, const void* subkeys, int B, int H, int d_q,
+                                 int n_keys, int k, int64_t* idx, float* w, int* status,
+                                 void* stream) {
+  if (B < 0 || H < 1 || d_q < 2 || (d_q & 1) || n_keys < 1 || k < 1) return PKM_ERR_INVALID;
+  if (k > n_keys) return PKM_ERR_RANGE;
+  if (d_q % 16 || k > pkm::kTcMaxK || (int64_t)n_keys * n_keys > INT32_MAX)
+    return PKM_ERR_UNSUPPORTED;
+  if ((int64_t)B * H > PKM_STATIC_MAX_PAIRS) return PKM_ERR_RANGE;
+  if (B == 0) return PKM_OK;
+  if (!q || !subkeys || !idx || !w) return PKM_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(subkeys) || !aligned16(idx) || !aligned16(w))
+    return PKM_ERR_ALIGN;
+  int* scratch = nullptr;
+  int rc = scratch_on_current_device(&scratch);
+  if (rc) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the status word starts clear on every call (the fallback count is
+  // cleared by the lookup launch itself)
+  if (cudaMemsetAsync(scratch, 0, sizeof(int), s) != cudaSuccess) return PKM_ERR_CUDA;
+  cudaError_t e = pkm::launch_lookup_tc(
+      static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(subkeys), B, H, d_q, n_keys,
+      k, pkm::default_hint_z(n_keys, k), idx, w, scratch, scratch + 1, scratch + 2, s);
+  if (e != cudaSuccess) return PKM_ERR_CUDA;
+  if (status &&
+      cudaMemcpyAsync(status, scratch, sizeof(int), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+    return PKM_ERR_CUDA;
+  return PKM_OK;
+}

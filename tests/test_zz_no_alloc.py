@@ -1,0 +1,72 @@
+"""pkm_lookup_static: the bf16 lookup that allocates no device memory.
+
+It serves callers that cannot allocate when they run a lookup (a process
+whose GPU memory is budgeted up front, a host framework that owns every
+allocation, a hot loop where cudaMalloc / cudaFree would synchronise the
+device).  Its scratch is one fixed array in the library; every call reuses
+it.  This file is collected last on purpose.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+import synth
+
+
+def test_static_lookup_rejects_too_many_pairs_on_the_host():
+    pk = pytest.importorskip("sparse_top_lookup_gb300")
+    pk.build()
+    L = pk.lib()
+    too_many = pk.PKM_STATIC_MAX_PAIRS + 1
+    # rejected before any CUDA call: B * H over the fixed scratch size
+    assert L.pkm_lookup_static(16, 16, too_many, 1, 64, 64, 4, 16, 16, None, None) \
+        == pk.PKM_ERR_RANGE
+    assert L.pkm_lookup_static(16, 16, 1, 1, 64, 8, 9, 16, 16, None, None) == pk.PKM_ERR_RANGE
+    assert L.pkm_lookup_static(16, 16, 1, 1, 63, 8, 4, 16, 16, None, None) == pk.PKM_ERR_INVALID
+    assert L.pkm_lookup_static(16, 16, 1, 1, 72, 8, 4, 16, 16, None, None) \
+        == pk.PKM_ERR_UNSUPPORTED
+
+
+@pytest.mark.gpu
+def test_static_lookup_matches_handle_lookup_on_two_calls_in_a_row():
+    torch = pytest.importorskip("torch")
+    pk = pytest.importorskip("sparse_top_lookup_gb300")
+    L = pk.lib()
+
+    def dev(a):
+        return torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16)
+
+    cases = [  # B, H, d_q, n_keys, k: two calls in a row with different shapes
+        (300, 2, 256, 512, 32),
+        (130, 3, 128, 256, 16),
+    ]
+    for seed, (B, H, d_q, n, k) in enumerate(cases, start=41):
+        q = dev(synth.normal(seed, 1, B * H * d_q, 1.0, dtype="bf16"))
+        C = dev(synth.normal(seed, 2, H * 2 * n * (d_q // 2), 2.0 / d_q, dtype="bf16"))
+
+        # the existing entry point, through a handle
+        h = pk.pkm_create(pk.make_config(d_q, 64, B, H, n, k, q_dtype=pk.PKM_BF16))
+        try:
+            idx_ref = torch.empty(B, H, k, dtype=torch.int64, device="cuda")
+            w_ref = torch.empty(B, H, k, device="cuda")
+            pk.check(pk.pkm_lookup(h, q, C, B, H, n, k, idx_ref, w_ref), "pkm_lookup")
+            assert pk.pkm_get_status(h) == pk.PKM_OK
+        finally:
+            pk.pkm_destroy(h)
+
+        # the allocation-free entry point, called through the C ABI directly
+        idx = torch.full((B, H, k), -7, dtype=torch.int64, device="cuda")
+        w = torch.full((B, H, k), -7.0, device="cuda")
+        status = torch.full((1,), 12345, dtype=torch.int32, device="cuda")
+        stream = torch.cuda.current_stream().cuda_stream
+        rc = L.pkm_lookup_static(ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(C.data_ptr()),
+                                 B, H, d_q, n, k, ctypes.c_void_p(idx.data_ptr()),
+                                 ctypes.c_void_p(w.data_ptr()), ctypes.c_void_p(status.data_ptr()),
+                                 ctypes.c_void_p(stream))
+        assert rc == pk.PKM_OK, pk.pkm_strerror(rc)
+        torch.cuda.synchronize()
+        assert status.item() == pk.PKM_OK
+        assert torch.equal(idx, idx_ref)
+        ref = w_ref.double()
+        assert ((w.double() - ref).abs() <= 2e-3 * (1 + ref.abs())).all()
