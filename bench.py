@@ -159,7 +159,7 @@ def cpu_oracle_time(c, inputs, sample, nthreads):
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    c = workload(args.workload)
+    c = workload(args.workload, args.batch)
     nthreads = os.cpu_count() or 1
     sample = min(args.cpu_sample, c["B"])
     inputs = cpu_inputs(c, sample)
@@ -196,7 +196,7 @@ def run_ours(args, rank, world, local):
     import sparse_top_lookup_gb300 as pk
 
     torch.cuda.set_device(local)
-    c = workload(args.workload)
+    c = workload(args.workload, args.batch)
     B, H, d_q, n, d_v, k = (c[x] for x in ("B", "H", "d_q", "n_keys", "d_v", "k"))
     bf16 = c["dtype"] == "bf16"
     dt = pk.PKM_BF16 if bf16 else pk.PKM_F32
@@ -276,12 +276,7 @@ def run_ours(args, rank, world, local):
     flops = 2.0 * B * H * n * d_q
     tflops = flops / (ms_lookup * 1e-3) / 1e12
     value = world * B * H / (ms_step * 1e-3)
-    traffic = None
-    tpath = os.path.join(ROOT, "profiles", "gather_traffic.json")
-    if os.path.exists(tpath):
-        tj = json.load(open(tpath))
-        if tj.get("workload") == args.workload and tj.get("kernel_rev") == GATHER_REV:
-            traffic = tj.get("bytes_per_launch")
+    traffic = measured_traffic(args.workload, B)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
@@ -314,7 +309,28 @@ def run_ours(args, rank, world, local):
         print(json.dumps(line), flush=True)
 
 
-GATHER_REV = "gather-v1"
+def measured_traffic(workload_name, B):
+    """DRAM bytes (read + write) of one gather launch from the committed ncu
+    summary, if it was taken on this workload and the kernel source is
+    unchanged since (its sha256 prefix is recorded); else None."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "gather_kernel_%s.md" % workload_name)
+    src = os.path.join(ROOT, "sparse_top_lookup_gb300", "csrc", "gather.cu")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    for line in open(path):
+        if line.startswith("- ") and ": " in line:
+            key, val = line[2:].split(": ", 1)
+            fields[key.strip()] = val.strip().strip("`")
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    if fields.get("source sha256") != sha or fields.get("B") != str(B):
+        return None
+    try:
+        return int(fields["dram bytes read"]) + int(fields["dram bytes written"])
+    except (KeyError, ValueError):
+        return None
+
 
 
 def main():
@@ -325,6 +341,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="page", choices=sorted(synth.CONFIGS))
     ap.add_argument("--cpu-sample", type=int, default=1024)
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's query count B (profiling runs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -1,0 +1,88 @@
+"""Parity at the full workload sizes, in the benchmark's launch configuration.
+
+The whole batch runs through pkm_forward; the fp64 oracle recomputes a
+sample of queries (spread over the batch, first and last included), and
+properties that hold at any size are checked on every output: indices in
+range and distinct per (query, head), weights non-increasing and summing to 1.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from helpers import TOL, compare_lookup, compare_out
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+torch = pytest.importorskip("torch")
+pk = pytest.importorskip("sparse_top_lookup_gb300")
+
+SAMPLE = 48
+
+
+def run_workload(name):
+    c = synth.CONFIGS[name]
+    B, H, d_q, n, d_v, k = (c[x] for x in ("B", "H", "d_q", "n_keys", "d_v", "k"))
+    q, C, V = synth.queries(c), synth.subkeys(c), synth.values(c)
+
+    def dev(a):
+        return torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16)
+
+    cfg = pk.make_config(d_q, d_v, B, H, n, k, q_dtype=pk.PKM_BF16)
+    h = pk.pkm_create(cfg)
+    try:
+        dq, dC, dV = dev(q), dev(C), dev(V)
+        out = torch.empty(B, d_v, device="cuda")
+        idx = torch.empty(B, H, k, dtype=torch.int64, device="cuda")
+        w = torch.empty(B, H, k, device="cuda")
+        pk.check(pk.pkm_forward(h, dq, dC, dV, B, H, n, k, out, idx, w), "pkm_forward")
+        assert pk.pkm_get_status(h) == pk.PKM_OK
+        fallback = pk.pkm_get_fallback_count(h)
+        del dq, dC, dV
+        res = out.cpu().numpy(), idx.cpu().numpy(), w.cpu().numpy()
+    finally:
+        pk.pkm_destroy(h)
+        torch.cuda.empty_cache()
+    return c, q, C, V, res, fallback
+
+
+def check(name):
+    c, q, C, V, (out, idx, w), fallback = run_workload(name)
+    B, H, d_q, n, d_v, k = (c[x] for x in ("B", "H", "d_q", "n_keys", "d_v", "k"))
+    N = n * n
+
+    # properties of every output
+    assert idx.min() >= 0 and idx.max() < N
+    srt = np.sort(idx.reshape(-1, k), axis=1)
+    assert (np.diff(srt, axis=1) > 0).all(), "repeated index within a (query, head)"
+    np.testing.assert_allclose(w.sum(-1), 1.0, atol=1e-5)
+    assert (np.diff(w, axis=-1) <= 1e-7).all()
+
+    # oracle on a spread sample of queries
+    rng = np.random.default_rng(0)
+    rows = np.unique(np.concatenate([[0, B - 1], rng.choice(B, SAMPLE - 2, replace=False)]))
+    row_len = H * d_q
+    qs = q.reshape(B, row_len)[rows].reshape(-1)
+    ref = oracle.lookup(qs, C, len(rows), H, d_q, n, k)
+    rep = compare_lookup(idx[rows], w[rows], ref, qs, C, c["dtype"], H, d_q, n)
+    assert rep["failures"] == 0, rep
+    assert rep["w_ok"], rep
+    ref_out = oracle.gather(V, N, d_v, ref["idx"], ref["w"])
+    err = compare_out(out[rows], V, N, d_v, idx[rows], ref["idx"], ref["w"], ref_out)
+    assert err <= TOL, err
+    print("%s: sampled %d queries, %s, out err %.2e, fallback pairs %d of %d"
+          % (name, len(rows), rep, err, fallback, B * H))
+
+
+def test_page_scale_full_batch():
+    check("page")
+
+
+def test_skewed_usage_full_batch():
+    check("skew")
+
+
+def test_large_table_full_batch():
+    if torch.cuda.get_device_properties(0).total_memory < 40 * 2**30:
+        pytest.skip("needs ~20 GiB of device memory")
+    check("large")
