@@ -86,8 +86,13 @@ enum {
      row's first-chunk scores.  Any finite z gives exact results (a low z costs
      more log compactions, a high z sends rows to the CUDA-core fallback);
      NaN restores the automatic choice. */
-  PKM_OPT_HINT_Z = 1
+  PKM_OPT_HINT_Z = 1,
+  /* pkm_forward_host: number of batch slices (1 .. PKM_HOST_MAX_CHUNKS,
+     default 4) pipelined so the copy of slice i+1 in and of slice i-1 out
+     overlap the computation of slice i. */
+  PKM_OPT_HOST_CHUNKS = 2
 };
+#define PKM_HOST_MAX_CHUNKS 16
 
 typedef struct pkm_handle *pkm_t;
 
@@ -137,7 +142,9 @@ int pkm_gather(pkm_t h, const void *values, int B, int H, int n_keys, int k, con
  * pkm_forward with the per-call tensors in HOST memory: q_host is copied to
  * the handle's staging, the forward runs, and out_host (and idx_host / w_host
  * when not NULL) are copied back; the call synchronises `stream` before it
- * returns.  subkeys and values stay device pointers (they are parameters,
+ * returns.  The batch is cut into slices (PKM_OPT_HOST_CHUNKS) whose copies
+ * run on two streams of the handle, overlapping the computation, which stays
+ * on `stream`.  subkeys and values stay device pointers (they are parameters,
  * resident on the GPU).  Host buffers should be pinned for full copy speed.
  * Needs a handle created with host_staging != 0.
  */

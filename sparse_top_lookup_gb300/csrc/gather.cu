@@ -61,7 +61,8 @@ struct VecAcc<false> {
 };
 
 // grid: one CTA per bag.  block: vpr * groups threads.
-// dynamic smem: rows_per_bag * (8 + 4) bytes, plus blockDim * E * 4 when groups > 1.
+// dynamic smem: rows_per_bag * (4 + 4) bytes, plus blockDim * E * 4 when groups > 1
+// (kept small so these CTAs fit next to a running lookup kernel's CTA).
 template <bool kBf16>
 __global__ void gather_kernel(const uint4* __restrict__ values, int64_t N, int vpr, int groups,
                               int rows_per_bag, const int64_t* __restrict__ idx,
@@ -69,7 +70,7 @@ __global__ void gather_kernel(const uint4* __restrict__ values, int64_t N, int v
                               int* __restrict__ status) {
   constexpr int E = VecAcc<kBf16>::kElems;
   extern __shared__ __align__(16) unsigned char smem[];
-  int64_t* s_row = reinterpret_cast<int64_t*>(smem);
+  int* s_row = reinterpret_cast<int*>(smem);
   float* s_w = reinterpret_cast<float*>(s_row + rows_per_bag);
 
   const int64_t bag = blockIdx.x;
@@ -87,7 +88,7 @@ __global__ void gather_kernel(const uint4* __restrict__ values, int64_t N, int v
       row = 0;
       wt = 0.0f;
     }
-    s_row[r] = row * vpr;
+    s_row[r] = (int)row;
     s_w[r] = wt;
   }
   __syncthreads();
@@ -99,17 +100,18 @@ __global__ void gather_kernel(const uint4* __restrict__ values, int64_t N, int v
   for (int e = 0; e < E; ++e) acc[e] = 0.0f;
 
   const uint4* vbase = values + v;
+  const int64_t stride = vpr;  // 16-byte vectors per value row
   int r = g;
   const int step = groups * kUnroll;
   for (; r + (kUnroll - 1) * groups < rows_per_bag; r += step) {
     uint4 x[kUnroll];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) x[u] = ldg_stream(vbase + s_row[r + u * groups]);
+    for (int u = 0; u < kUnroll; ++u) x[u] = ldg_stream(vbase + s_row[r + u * groups] * stride);
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) VecAcc<kBf16>::fma(acc, s_w[r + u * groups], x[u]);
   }
   for (; r < rows_per_bag; r += groups) {
-    uint4 x = ldg_stream(vbase + s_row[r]);
+    uint4 x = ldg_stream(vbase + s_row[r] * stride);
     VecAcc<kBf16>::fma(acc, s_w[r], x);
   }
 
@@ -121,7 +123,7 @@ __global__ void gather_kernel(const uint4* __restrict__ values, int64_t N, int v
     return;
   }
   // Reduce the row groups: red[g][v][e].
-  float* red = reinterpret_cast<float*>(smem + ((size_t)rows_per_bag * 12 + 15) / 16 * 16);
+  float* red = reinterpret_cast<float*>(smem + ((size_t)rows_per_bag * 8 + 15) / 16 * 16);
 #pragma unroll
   for (int e = 0; e < E; ++e) red[(g * vpr + v) * E + e] = acc[e];
   __syncthreads();
@@ -147,13 +149,22 @@ cudaError_t launch_gather(const void* values, int value_dtype, int64_t N, int d_
   int groups = vpr >= 128 ? 1 : 128 / vpr;
   if (groups > rows_per_bag) groups = rows_per_bag > 0 ? rows_per_bag : 1;
   const int threads = vpr * groups;
-  const size_t staged = (size_t)rows_per_bag * 12;
+  const size_t staged = (size_t)rows_per_bag * 8;
   const size_t red_off = (staged + 15) / 16 * 16;
   const size_t smem = groups > 1 ? red_off + (size_t)threads * (bf16 ? 8 : 4) * 4 : staged;
   const void* fn = bf16 ? (const void*)gather_kernel<true> : (const void*)gather_kernel<false>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
+  }
+  // The loads bypass L1, so the SM can keep its maximum shared-memory split;
+  // CTAs of this kernel then fit next to a running lookup kernel's CTA.
+  static bool carveout_set[2] = {false, false};
+  if (!carveout_set[bf16]) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    carveout_set[bf16] = true;
   }
   if (bf16)
     gather_kernel<true><<<B, threads, smem, stream>>>(static_cast<const uint4*>(values), N, vpr,

@@ -20,6 +20,11 @@ struct pkm_handle {
   float* stage_out;
   int64_t* stage_idx;
   float* stage_w;
+  // pkm_forward_host pipeline: copies in / out on their own streams, so the
+  // copy engines move batch i+1 in and batch i-1 out while batch i computes
+  cudaStream_t s_in, s_out;
+  cudaEvent_t ev_start, ev_done, ev_in[PKM_HOST_MAX_CHUNKS], ev_comp[PKM_HOST_MAX_CHUNKS];
+  int host_chunks;
 };
 
 namespace {
@@ -118,6 +123,14 @@ void pkm_destroy(pkm_t h) {
   cudaFree(h->stage_out);
   cudaFree(h->stage_idx);
   cudaFree(h->stage_w);
+  if (h->s_in) cudaStreamDestroy(h->s_in);
+  if (h->s_out) cudaStreamDestroy(h->s_out);
+  if (h->ev_start) cudaEventDestroy(h->ev_start);
+  if (h->ev_done) cudaEventDestroy(h->ev_done);
+  for (int i = 0; i < PKM_HOST_MAX_CHUNKS; ++i) {
+    if (h->ev_in[i]) cudaEventDestroy(h->ev_in[i]);
+    if (h->ev_comp[i]) cudaEventDestroy(h->ev_comp[i]);
+  }
   free(h);
 }
 
@@ -152,6 +165,14 @@ int pkm_create(pkm_t* out, const pkm_config* cfg) {
          cudaMalloc(&h->stage_out, (size_t)cfg->max_B * cfg->d_v * sizeof(float)) == cudaSuccess &&
          cudaMalloc(&h->stage_idx, sel * sizeof(int64_t)) == cudaSuccess &&
          cudaMalloc(&h->stage_w, sel * sizeof(float)) == cudaSuccess;
+    ok = ok && cudaStreamCreateWithFlags(&h->s_in, cudaStreamNonBlocking) == cudaSuccess &&
+         cudaStreamCreateWithFlags(&h->s_out, cudaStreamNonBlocking) == cudaSuccess &&
+         cudaEventCreateWithFlags(&h->ev_start, cudaEventDisableTiming) == cudaSuccess &&
+         cudaEventCreateWithFlags(&h->ev_done, cudaEventDisableTiming) == cudaSuccess;
+    for (int i = 0; ok && i < PKM_HOST_MAX_CHUNKS; ++i)
+      ok = cudaEventCreateWithFlags(&h->ev_in[i], cudaEventDisableTiming) == cudaSuccess &&
+           cudaEventCreateWithFlags(&h->ev_comp[i], cudaEventDisableTiming) == cudaSuccess;
+    h->host_chunks = 4;
   }
   if (!ok) {
     cudaGetLastError();
@@ -215,23 +236,49 @@ int pkm_forward_host(pkm_t h, const void* q_host, const void* subkeys, const voi
   if (!q_host || !subkeys || !values || !out_host) return PKM_ERR_INVALID;
   if (!aligned16(subkeys) || !aligned16(values)) return PKM_ERR_ALIGN;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const size_t qb = (size_t)B * H * h->cfg.d_q * elem_size(h->cfg.q_dtype);
-  const size_t sel = (size_t)B * H * k;
-  if (cudaMemcpyAsync(h->stage_q, q_host, qb, cudaMemcpyHostToDevice, s) != cudaSuccess)
+  const size_t qrow = (size_t)H * h->cfg.d_q * elem_size(h->cfg.q_dtype);  // bytes per query
+  const size_t orow = (size_t)h->cfg.d_v * sizeof(float);
+  const size_t srow = (size_t)H * k;  // selections per query
+  // batch split: chunks of a multiple of 8 queries (keeps every device
+  // offset 16-byte aligned), at most host_chunks of them
+  int chunks = h->host_chunks < 1 ? 1 : h->host_chunks;
+  int per = (B + chunks - 1) / chunks;
+  per = (per + 7) / 8 * 8;
+  chunks = (B + per - 1) / per;
+  const char* qh = static_cast<const char*>(q_host);
+  char* qd = static_cast<char*>(h->stage_q);
+  if (cudaEventRecord(h->ev_start, s) != cudaSuccess ||
+      cudaStreamWaitEvent(h->s_in, h->ev_start, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(h->s_out, h->ev_start, 0) != cudaSuccess)
     return PKM_ERR_CUDA;
-  rc = run_lookup(h, h->stage_q, subkeys, B, H, n_keys, k, h->stage_idx, h->stage_w, s);
-  if (rc) return rc;
-  rc = run_gather(h, values, B, H, n_keys, k, h->stage_idx, h->stage_w, h->stage_out, s);
-  if (rc) return rc;
-  if (cudaMemcpyAsync(out_host, h->stage_out, (size_t)B * h->cfg.d_v * sizeof(float),
-                      cudaMemcpyDeviceToHost, s) != cudaSuccess)
-    return PKM_ERR_CUDA;
-  if (idx_host && cudaMemcpyAsync(idx_host, h->stage_idx, sel * sizeof(int64_t),
-                                  cudaMemcpyDeviceToHost, s) != cudaSuccess)
-    return PKM_ERR_CUDA;
-  if (w_host &&
-      cudaMemcpyAsync(w_host, h->stage_w, sel * sizeof(float), cudaMemcpyDeviceToHost, s) !=
-          cudaSuccess)
+  for (int c = 0; c < chunks; ++c) {
+    const int b0 = c * per, nb = (B - b0 < per) ? B - b0 : per;
+    if (cudaMemcpyAsync(qd + b0 * qrow, qh + b0 * qrow, nb * qrow, cudaMemcpyHostToDevice,
+                        h->s_in) != cudaSuccess ||
+        cudaEventRecord(h->ev_in[c], h->s_in) != cudaSuccess ||
+        cudaStreamWaitEvent(s, h->ev_in[c], 0) != cudaSuccess)
+      return PKM_ERR_CUDA;
+    int64_t* idx_d = h->stage_idx + b0 * srow;
+    float* w_d = h->stage_w + b0 * srow;
+    float* out_d = h->stage_out + (size_t)b0 * h->cfg.d_v;
+    rc = run_lookup(h, qd + b0 * qrow, subkeys, nb, H, n_keys, k, idx_d, w_d, s);
+    if (rc) return rc;
+    rc = run_gather(h, values, nb, H, n_keys, k, idx_d, w_d, out_d, s);
+    if (rc) return rc;
+    if (cudaEventRecord(h->ev_comp[c], s) != cudaSuccess ||
+        cudaStreamWaitEvent(h->s_out, h->ev_comp[c], 0) != cudaSuccess ||
+        cudaMemcpyAsync(out_host + (size_t)b0 * h->cfg.d_v, out_d, nb * orow,
+                        cudaMemcpyDeviceToHost, h->s_out) != cudaSuccess)
+      return PKM_ERR_CUDA;
+    if (idx_host && cudaMemcpyAsync(idx_host + b0 * srow, idx_d, nb * srow * sizeof(int64_t),
+                                    cudaMemcpyDeviceToHost, h->s_out) != cudaSuccess)
+      return PKM_ERR_CUDA;
+    if (w_host && cudaMemcpyAsync(w_host + b0 * srow, w_d, nb * srow * sizeof(float),
+                                  cudaMemcpyDeviceToHost, h->s_out) != cudaSuccess)
+      return PKM_ERR_CUDA;
+  }
+  if (cudaEventRecord(h->ev_done, h->s_out) != cudaSuccess ||
+      cudaStreamWaitEvent(s, h->ev_done, 0) != cudaSuccess)
     return PKM_ERR_CUDA;
   return cuda_rc(cudaStreamSynchronize(s));
 }
@@ -242,6 +289,11 @@ int pkm_set_option(pkm_t h, int option, double value) {
     case PKM_OPT_HINT_Z:
       if (!isnan(value) && !isfinite(value)) return PKM_ERR_OPTION;
       h->hint_z = (float)value;
+      return PKM_OK;
+    case PKM_OPT_HOST_CHUNKS:
+      if (!(value >= 1 && value <= PKM_HOST_MAX_CHUNKS) || value != (int)value)
+        return PKM_ERR_OPTION;
+      h->host_chunks = (int)value;
       return PKM_OK;
     default:
       return PKM_ERR_OPTION;

@@ -211,14 +211,20 @@ def test_forward_host_matches_device_forward():
     h, _ = make_handle(c, staging=True)
     try:
         qh = torch.from_numpy(q.view(np.int16)).pin_memory()
-        oh = torch.empty(B, c["d_v"]).pin_memory()
-        ih = torch.empty(B, c["H"], c["k"], dtype=torch.int64).pin_memory()
-        wh = torch.empty(B, c["H"], c["k"]).pin_memory()
-        pk.check(pk.pkm_forward_host(h, qh, to_device(C, "bf16"), to_device(V, "bf16"), B, c["H"],
-                                     c["n_keys"], c["k"], oh, ih, wh), "forward_host")
-        assert np.array_equal(ih.numpy(), idx_d)
-        assert np.array_equal(wh.numpy(), w_d)
-        assert np.array_equal(oh.numpy(), out_d)
+        dC, dV = to_device(C, "bf16"), to_device(V, "bf16")
+        for chunks in (None, 1, 3, 16):  # batch slices pipelined against the copies
+            if chunks is not None:
+                pk.check(pk.pkm_set_option(h, pk.PKM_OPT_HOST_CHUNKS, chunks), "set_option")
+            oh = torch.empty(B, c["d_v"]).pin_memory()
+            ih = torch.empty(B, c["H"], c["k"], dtype=torch.int64).pin_memory()
+            wh = torch.empty(B, c["H"], c["k"]).pin_memory()
+            pk.check(pk.pkm_forward_host(h, qh, dC, dV, B, c["H"], c["n_keys"], c["k"], oh, ih,
+                                         wh), "forward_host")
+            assert np.array_equal(ih.numpy(), idx_d), chunks
+            assert np.array_equal(wh.numpy(), w_d), chunks
+            assert np.array_equal(oh.numpy(), out_d), chunks
+        assert pk.pkm_set_option(h, pk.PKM_OPT_HOST_CHUNKS, 0) == pk.PKM_ERR_OPTION
+        assert pk.pkm_set_option(h, pk.PKM_OPT_HOST_CHUNKS, 17) == pk.PKM_ERR_OPTION
     finally:
         pk.pkm_destroy(h)
 
