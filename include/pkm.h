@@ -184,10 +184,11 @@ int pkm_abi_version(void);
  * pkm_lookup_static: the lookup alone (scoring through softmax) for bf16
  * queries and subkeys, as pkm_lookup on a bf16 handle with d_q given here:
  * idx and w [B, H, k] are written on `stream`.  It allocates nothing: its
- * scratch (a status word and the list of (query, head) pairs recomputed on
- * the CUDA cores, at most PKM_STATIC_MAX_PAIRS of them) is one fixed array of
- * (PKM_STATIC_MAX_PAIRS + 2) * 4 bytes in the library's device memory, which
- * every GPU that loads the library holds until the process exits.
+ * scratch (a status word, the list of (query, head) pairs recomputed on the
+ * CUDA cores and the per-half candidate lists, for at most
+ * PKM_STATIC_MAX_PAIRS pairs) is one fixed array of 256 + 388 *
+ * PKM_STATIC_MAX_PAIRS bytes (about 24 MiB) in the library's device memory,
+ * which every GPU that loads the library holds until the process exits.
  *   - B * H above PKM_STATIC_MAX_PAIRS returns PKM_ERR_RANGE; other argument
  *     errors are as for pkm_lookup.
  *   - status: if not NULL, a device int that receives the call's device
@@ -199,7 +200,7 @@ int pkm_abi_version(void);
  *     zero.  Calls whose work overlaps on the GPU (other streams, other host
  *     threads) race on it: serialise them.
  */
-#define PKM_STATIC_MAX_PAIRS (1 << 20)
+#define PKM_STATIC_MAX_PAIRS (1 << 16)
 int pkm_lookup_static(const void *q, const void *subkeys, int B, int H, int d_q, int n_keys, int k,
                       int64_t *idx, float *w, int *status, void *stream);
 

@@ -24,7 +24,7 @@ PKM_HOST_MAX_CHUNKS = 16
 EXPORTED = ["pkm_create", "pkm_destroy", "pkm_forward", "pkm_lookup", "pkm_gather",
             "pkm_forward_host", "pkm_get_status", "pkm_check_args", "pkm_strerror",
             "pkm_abi_version", "pkm_set_option", "pkm_get_fallback_count", "pkm_lookup_static"]
-PKM_STATIC_MAX_PAIRS = 1 << 20
+PKM_STATIC_MAX_PAIRS = 1 << 16
 
 
 class pkm_config(ctypes.Structure):

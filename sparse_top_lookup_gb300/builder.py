@@ -13,7 +13,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpkm.so")
-SOURCES = ["pkm_api.cu", "gather.cu", "lookup_simt.cu", "lookup_tc.cu", "pkm_static.cu"]
+SOURCES = ["pkm_api.cu", "gather.cu", "lookup_simt.cu", "lookup_tc.cu", "lookup_merge.cu",
+           "pkm_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -1,0 +1,199 @@
+// Steps a4-a5: the k^2 merge of the two per-half lists and the softmax.
+//
+// Product-Key Memory, "Factorising the key space": the global top-k lies
+// inside top_k(half 1) x top_k(half 2); code listing: k^2 sums
+// s1[i] + s2[j] with flat index i1 * n_keys + i2, their top-k, and a softmax
+// over the winners.  One thread owns one (query, head) pair, so many warps
+// per SM hide the latency of the per-pair work.
+//
+// The lists come from the selection kernel, each ordered by (score desc,
+// subkey asc).  Only pairs (i, j) with (i + 1)(j + 1) <= KL can reach the top
+// KL (every (i', j') with i' <= i, j' <= j scores at least as much).  Their
+// sums go through value-only sorting networks to the sorted KL best sums V;
+// when those are all distinct and no left-out pair ties the KL-th, each
+// surviving pair's output slot is the number of larger sums and its softmax
+// weight follows from V.  Exact ties take a frontier walk that orders equal
+// sums by flat index.  A list marked failed (subkey 0xffff in its first
+// slot) sends the pair to the CUDA-core fallback list instead.
+#include <math.h>
+#include <stdint.h>
+
+#include "pkm_internal.cuh"
+#include "select_net.cuh"
+
+namespace pkm {
+namespace {
+
+constexpr int kThreads = 128;
+
+template <int KL>
+__global__ void __launch_bounds__(kThreads)
+merge_kernel(const float* __restrict__ list_v, const unsigned short* __restrict__ list_c,
+             int pairs, int n, int k, int64_t* __restrict__ idx, float* __restrict__ w,
+             int* __restrict__ fb_count, int* __restrict__ fb_list) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  // per thread, [slot][thread] layouts: survivors' scores and (i*32+j), and
+  // the two lists' subkeys
+  float* sv = reinterpret_cast<float*>(smem);                                   // [KL][T]
+  unsigned short* sp = reinterpret_cast<unsigned short*>(sv + KL * kThreads);   // [KL][T]
+  unsigned short* sc = sp + KL * kThreads;                                      // [2KL][T]
+  const int t = threadIdx.x;
+  const int pair = blockIdx.x * kThreads + t;
+  if (pair >= pairs) return;
+
+  const float* v1 = list_v + (size_t)pair * 2 * KL;
+  const unsigned short* c1 = list_c + (size_t)pair * 2 * KL;
+  float s1v[KL], s2v[KL];
+  {
+    const float4* g = reinterpret_cast<const float4*>(v1);
+#pragma unroll
+    for (int i = 0; i < KL / 4; ++i) {
+      const float4 a = g[i], b = g[KL / 4 + i];
+      s1v[4 * i] = a.x; s1v[4 * i + 1] = a.y; s1v[4 * i + 2] = a.z; s1v[4 * i + 3] = a.w;
+      s2v[4 * i] = b.x; s2v[4 * i + 1] = b.y; s2v[4 * i + 2] = b.z; s2v[4 * i + 3] = b.w;
+    }
+    const uint4* gc = reinterpret_cast<const uint4*>(c1);
+#pragma unroll
+    for (int i = 0; i < 2 * KL / 8; ++i) {
+      const uint4 u = gc[i];
+      const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        sc[(8 * i + 2 * q) * kThreads + t] = (unsigned short)(wv[q] & 0xffffu);
+        sc[(8 * i + 2 * q + 1) * kThreads + t] = (unsigned short)(wv[q] >> 16);
+      }
+    }
+  }
+  if (sc[t] == 0xffffu || sc[KL * kThreads + t] == 0xffffu) {
+    fb_list[atomicAdd(fb_count, 1)] = pair;
+    return;
+  }
+  auto col1 = [&](int i) { return (int)sc[i * kThreads + t]; };
+  auto col2 = [&](int j) { return (int)sc[(KL + j) * kThreads + t]; };
+
+  constexpr MergePairs<KL> P{};
+  float V[KL];
+#pragma unroll
+  for (int i = 0; i < KL; ++i) V[i] = -INFINITY;
+#pragma unroll
+  for (int blk = 0; blk < P.kPadded / 32; ++blk) {
+    float Bv[32];
+#pragma unroll
+    for (int u = 0; u < 32; ++u) {
+      const int c = blk * 32 + u;
+      Bv[u] = P.i[c] >= 0 ? s1v[P.i[c]] + s2v[P.j[c]] : -INFINITY;
+    }
+    sort_desc<32>(Bv);
+    merge_top<KL>(V, Bv);
+  }
+  const float x = V[KL - 1];
+  bool tie = false;
+#pragma unroll
+  for (int i = 0; i + 1 < KL; ++i) tie |= V[i] == V[i + 1];
+  // survivors: pairs scoring >= x; more than KL of them means a tie at x
+  const uint32_t va0 = static_cast<uint32_t>(__cvta_generic_to_shared(sv + t));
+  const uint32_t va_end = va0 + KL * (kThreads * 4);
+  uint32_t va = va0, ca = static_cast<uint32_t>(__cvta_generic_to_shared(sp + t)), nsurv = 0;
+  const float below_x = nextafterf(x, -INFINITY);  // >= x  <=>  > below_x
+#pragma unroll
+  for (int c = 0; c < P.kCount; ++c) {
+    const float s = s1v[P.i[c]] + s2v[P.j[c]];
+    log_append_bounded<kThreads * 4, kThreads * 2>(va, ca, nsurv, va_end, s, below_x,
+                                                   (unsigned short)(P.i[c] * 32 + P.j[c]));
+  }
+  float z = 0.0f;
+#pragma unroll
+  for (int r = 0; r < KL; ++r)
+    if (r < k) z += expf(V[r] - V[0]);
+  int64_t* ip = idx + (size_t)pair * k;
+  float* wp = w + (size_t)pair * k;
+  if (!tie && nsurv == (uint32_t)KL) {
+#pragma unroll 2
+    for (int e = 0; e < KL; ++e) {
+      const float s = sv[e * kThreads + t];
+      const int pc = sp[e * kThreads + t];
+      int r4[4] = {0, 0, 0, 0};
+#pragma unroll
+      for (int i = 0; i < KL; ++i) r4[i & 3] += V[i] > s;
+      const int r = (r4[0] + r4[1]) + (r4[2] + r4[3]);
+      if (r < k) {
+        ip[r] = (int64_t)(col1(pc >> 5) * n + col2(pc & 31));
+        wp[r] = expf(s - V[0]) / z;
+      }
+    }
+    return;
+  }
+  // frontier walk (exact ties): row i of the candidate grid is sorted, the
+  // next winner is the best of the rows' heads, (score desc, flat asc)
+  float fv[KL];
+  int ff[KL], fp[KL];
+#pragma unroll
+  for (int i = 0; i < KL; ++i) {
+    fv[i] = s1v[i] + s2v[0];
+    ff[i] = col1(i) * n + col2(0);
+    fp[i] = 0;
+  }
+#pragma unroll 1
+  for (int r = 0; r < k; ++r) {
+    float bv = fv[0];
+    int bf = ff[0], bi = 0, bp = fp[0];
+#pragma unroll
+    for (int i = 1; i < KL; ++i) {
+      const bool better = fv[i] > bv || (fv[i] == bv && ff[i] < bf);
+      bv = better ? fv[i] : bv;
+      bf = better ? ff[i] : bf;
+      bi = better ? i : bi;
+      bp = better ? fp[i] : bp;
+    }
+    ip[r] = (int64_t)bf;
+    wp[r] = expf(bv - V[0]) / z;
+    const int np = bp + 1;
+    float nv = -INFINITY;
+    int nf = 0;
+    if (np < KL) {
+      nv = v1[bi] + v1[KL + np];
+      nf = col1(bi) * n + col2(np);
+    }
+#pragma unroll
+    for (int i = 0; i < KL; ++i) {
+      if (i == bi) {
+        fv[i] = nv;
+        ff[i] = nf;
+        fp[i] = np;
+      }
+    }
+  }
+}
+
+template <int KL>
+cudaError_t launch_merge_kl(const float* list_v, const unsigned short* list_c, int pairs, int n,
+                            int k, int64_t* idx, float* w, int* fb_count, int* fb_list,
+                            cudaStream_t stream) {
+  const size_t smem = (size_t)KL * kThreads * (4 + 2) + (size_t)2 * KL * kThreads * 2;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(merge_kernel<KL>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int grid = (pairs + kThreads - 1) / kThreads;
+  merge_kernel<KL><<<grid, kThreads, smem, stream>>>(list_v, list_c, pairs, n, k, idx, w,
+                                                      fb_count, fb_list);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_merge(const float* list_v, const unsigned short* list_c, int B, int H,
+                         int n_keys, int k, int64_t* idx, float* w, int* fb_count, int* fb_list,
+                         cudaStream_t stream) {
+  const int pairs = B * H;
+  if (pairs == 0) return cudaSuccess;
+  if (k <= 16)
+    return launch_merge_kl<16>(list_v, list_c, pairs, n_keys, k, idx, w, fb_count, fb_list,
+                               stream);
+  return launch_merge_kl<32>(list_v, list_c, pairs, n_keys, k, idx, w, fb_count, fb_list, stream);
+}
+
+}  // namespace pkm

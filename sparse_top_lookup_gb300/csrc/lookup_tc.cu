@@ -8,25 +8,28 @@
 // (forward): q.chunk(2) halves, per-half `q_i @ subkeys[i].T` then topk, k^2
 // sums with flat index i1 * n_keys + i2, topk, softmax.
 //
-// One CTA owns 128 queries x one head at a time (persistent over tiles):
+// This kernel does steps a1-a3: one work unit is 128 queries x one head x
+// one half; CTAs are persistent over units:
 //   warp 0      TMA producer: 128x64 query slabs and NCx64 subkey slabs
 //               (bf16, 128-byte swizzle) into a 3-stage shared-memory ring;
 //   warp 1      allocates 512 TMEM columns and issues tcgen05.mma
 //               (M=128, N=NC<=256, K=16, fp32 accumulate) into one of two
 //               TMEM buffers, so scoring chunk c+1 overlaps the epilogue of c;
 //   warps 2..5  epilogue, one thread per query row (= TMEM lane): reads its
-//               row's scores 32 columns at a time with tcgen05.ld and keeps
-//               an exact running top-KL list in registers (ties: lower subkey
-//               index first, since columns arrive in increasing order), then
-//               merges the two halves' lists and applies the softmax.
-// Scores never leave the SM.  Every mbarrier wait is bounded; on time-out
-// the kernel records PKM_ERR_TIMEOUT, stops issuing work, waits (bounded) for
-// its own copies and MMAs in flight, frees TMEM and returns.
+//               row's scores with tcgen05.ld and selects the half's exact
+//               top-KL (selection helpers below), then writes the half's list
+//               by (score desc, subkey asc) to global memory.
+// The k^2 merge and the softmax (a4, a5) run in lookup_merge.cu, one thread
+// per (query, head).  Scores never leave the SM.  Every mbarrier wait is
+// bounded; on time-out the kernel records PKM_ERR_TIMEOUT, stops issuing
+// work, waits (bounded) for its own copies and MMAs in flight, frees TMEM and
+// returns.
 #include <cuda.h>
 #include <math.h>
 #include <stdint.h>
 
 #include "pkm_internal.cuh"
+#include "select_net.cuh"
 
 namespace pkm {
 namespace {
@@ -209,113 +212,6 @@ __device__ __forceinline__ void wait_phase_drain(uint32_t bar, uint32_t parity) 
 
 constexpr int LOG_CAP = 96;  // log entries per row
 
-// Bitonic sort of N values, descending (compile-time network).
-template <int N>
-__device__ __forceinline__ void sort_desc(float (&a)[N]) {
-#pragma unroll
-  for (int size = 2; size <= N; size <<= 1)
-#pragma unroll
-    for (int stride = size >> 1; stride > 0; stride >>= 1)
-#pragma unroll
-      for (int i = 0; i < N; ++i) {
-        const int j = i ^ stride;
-        if (j > i) {
-          const float hi = fmaxf(a[i], a[j]), lo = fminf(a[i], a[j]);
-          if ((i & size) == 0) {
-            a[i] = hi;
-            a[j] = lo;
-          } else {
-            a[i] = lo;
-            a[j] = hi;
-          }
-        }
-      }
-}
-
-// V (descending, KL) <- the KL largest of V and B (descending, 32).
-template <int KL>
-__device__ __forceinline__ void merge_top(float (&V)[KL], const float (&B)[32]) {
-#pragma unroll
-  for (int i = 0; i < KL; ++i) V[i] = fmaxf(V[i], B[KL - 1 - i]);  // bitonic
-#pragma unroll
-  for (int stride = KL >> 1; stride > 0; stride >>= 1)
-#pragma unroll
-    for (int i = 0; i < KL; ++i) {
-      const int j = i ^ stride;
-      if (j > i) {
-        const float hi = fmaxf(V[i], V[j]), lo = fminf(V[i], V[j]);
-        V[i] = hi;
-        V[j] = lo;
-      }
-    }
-}
-
-// Append (v, col) at the log's end when v > thr, without a branch: the two
-// stores are predicated, and the shared-memory addresses of the next free
-// slot (va for the score, ca for the column) advance by one slot row when the
-// entry is taken.
-__device__ __forceinline__ void log_append(uint32_t& va, uint32_t& ca, float v, float thr,
-                                           unsigned short col) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.gt.f32 p, %2, %3;\n\t"
-      "@p st.shared.f32 [%0], %2;\n\t"
-      "@p st.shared.u16 [%1], %4;\n\t"
-      "@p add.u32 %0, %0, %5;\n\t"
-      "@p add.u32 %1, %1, %6;\n\t}"
-      : "+r"(va), "+r"(ca)
-      : "f"(v), "f"(thr), "h"(col), "n"(BM * 4), "n"(BM * 2)
-      : "memory");
-}
-
-// The candidate pairs (i, j) of the k^2 merge that can reach the top KL:
-// (i + 1)(j + 1) <= KL, since every (i', j') with i' <= i and j' <= j scores
-// at least as much.  Row-major, padded to a multiple of 32 with (-1, -1).
-template <int KL>
-struct MergePairs {
-  static constexpr int count() {
-    int c = 0;
-    for (int i = 0; i < KL; ++i)
-      for (int j = 0; (i + 1) * (j + 1) <= KL; ++j) ++c;
-    return c;
-  }
-  static constexpr int kCount = count();
-  static constexpr int kPadded = (kCount + 31) / 32 * 32;
-  int i[kPadded], j[kPadded];
-  constexpr MergePairs() : i(), j() {
-    int c = 0;
-    for (int a = 0; a < KL; ++a)
-      for (int b = 0; (a + 1) * (b + 1) <= KL; ++b) {
-        i[c] = a;
-        j[c] = b;
-        ++c;
-      }
-    for (; c < kPadded; ++c) {
-      i[c] = -1;
-      j[c] = -1;
-    }
-  }
-};
-
-// Count v > thr in `count`, and append (v, col) like log_append while the
-// score address is below va_end.
-__device__ __forceinline__ void log_append_bounded(uint32_t& va, uint32_t& ca, uint32_t& count,
-                                                   uint32_t va_end, float v, float thr,
-                                                   unsigned short col) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.gt.f32 p, %3, %4;\n\t"
-      "@p add.u32 %2, %2, 1;\n\t"
-      "setp.lt.and.u32 p, %0, %8, p;\n\t"
-      "@p st.shared.f32 [%0], %3;\n\t"
-      "@p st.shared.u16 [%1], %5;\n\t"
-      "@p add.u32 %0, %0, %6;\n\t"
-      "@p add.u32 %1, %1, %7;\n\t}"
-      : "+r"(va), "+r"(ca), "+r"(count)
-      : "f"(v), "f"(thr), "h"(col), "n"(BM * 4), "n"(BM * 2), "r"(va_end)
-      : "memory");
-}
-
 // Per-row log in shared memory, [slot][row] so a warp's 32 rows hit 32
 // different banks whatever their lengths.
 struct RowLog {
@@ -412,10 +308,10 @@ constexpr int SMEM_TOTAL = SMEM_TILES + LOG_BYTES + 1024;  // + alignment slack
 
 template <int KL>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-lookup_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_c,
-                 int B, int H, int n, int k, int NC, int nch, int kb_count, float hint_z,
-                 int64_t* __restrict__ idx, float* __restrict__ w, int* __restrict__ status,
-                 int* __restrict__ fb_count, int* __restrict__ fb_list) {
+select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_c,
+                 int B, int H, int n, int NC, int nch, int kb_count, float hint_z,
+                 float* __restrict__ list_v, unsigned short* __restrict__ list_c,
+                 int* __restrict__ status) {
   extern __shared__ unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t bars[2 * STAGES + 5];
   __shared__ uint32_t s_tmem_base;
@@ -424,8 +320,6 @@ lookup_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t tiles_u32 = smem_u32(smem);
-  // per-row log; at merge time its slots [0, KL) hold the half-2 list and
-  // [KL, 2 KL) the half-1 list
   float* log_v = reinterpret_cast<float*>(smem + SMEM_TILES);
   unsigned short* log_c = reinterpret_cast<unsigned short*>(smem + SMEM_TILES + LOG_CAP * BM * 4);
 
@@ -465,8 +359,9 @@ lookup_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
   const uint32_t tmem = s_tmem_base;
   const Ctl ctl{&s_abort, status};
 
+  // work unit u: tile u / 2 (row tile, head), half u % 2
   const int row_tiles = (B + BM - 1) / BM;
-  const int tiles = row_tiles * H;
+  const int units = row_tiles * H * 2;
 
   if (warp == 0) {
     // ---------------------------------------------------- TMA producer
@@ -474,22 +369,22 @@ lookup_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
       const uint32_t tx = (uint32_t)(A_BYTES + NC * BK * 2);
       uint32_t it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < tiles; tile += gridDim.x) {
-        const int rt = tile / H, h = tile - (tile / H) * H;
-        for (int half = 0; ok && half < 2; ++half)
-          for (int ch = 0; ok && ch < nch; ++ch)
-            for (int kb = 0; kb < kb_count; ++kb) {
-              const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-              if (!wait_phase(bar_empty(s), ph ^ 1u, ctl)) {
-                ok = false;
-                break;
-              }
-              mbar_expect_tx(bar_full(s), tx);
-              const uint32_t a_dst = tiles_u32 + s * STAGE_BYTES;
-              tma_load_4d(a_dst, &tmap_q, kb * BK, half, h, rt * BM, bar_full(s));
-              tma_load_3d(a_dst + A_BYTES, &tmap_c, kb * BK, ch * NC, h * 2 + half, bar_full(s));
-              ++it;
+      for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+        const int tile = u >> 1, half = u & 1;
+        const int rt = tile / H, h = tile - rt * H;
+        for (int ch = 0; ok && ch < nch; ++ch)
+          for (int kb = 0; kb < kb_count; ++kb) {
+            const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+            if (!wait_phase(bar_empty(s), ph ^ 1u, ctl)) {
+              ok = false;
+              break;
             }
+            mbar_expect_tx(bar_full(s), tx);
+            const uint32_t a_dst = tiles_u32 + s * STAGE_BYTES;
+            tma_load_4d(a_dst, &tmap_q, kb * BK, half, h, rt * BM, bar_full(s));
+            tma_load_3d(a_dst + A_BYTES, &tmap_c, kb * BK, ch * NC, h * 2 + half, bar_full(s));
+            ++it;
+          }
       }
       if (!ok) {  // let the copies already issued land before the CTA exits
         const uint32_t first = it > (uint32_t)STAGES ? it - STAGES : 0u;
@@ -502,33 +397,32 @@ lookup_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
       const uint32_t idesc = idesc_bf16(BM, NC);
       uint32_t it = 0, cc = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < tiles; tile += gridDim.x)
-        for (int half = 0; ok && half < 2; ++half)
-          for (int ch = 0; ok && ch < nch; ++ch, ++cc) {
-            const uint32_t buf = cc & 1u, use = cc >> 1;
-            if (!wait_phase(bar_tempty(buf), (use & 1u) ^ 1u, ctl)) {
+      for (int u = blockIdx.x; ok && u < units; u += gridDim.x)
+        for (int ch = 0; ok && ch < nch; ++ch, ++cc) {
+          const uint32_t buf = cc & 1u, use = cc >> 1;
+          if (!wait_phase(bar_tempty(buf), (use & 1u) ^ 1u, ctl)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem + buf * NCMAX;
+          for (int kb = 0; kb < kb_count; ++kb, ++it) {
+            const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+            if (!wait_phase(bar_full(s), ph, ctl)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint32_t d_tmem = tmem + buf * NCMAX;
-            for (int kb = 0; kb < kb_count; ++kb, ++it) {
-              const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-              if (!wait_phase(bar_full(s), ph, ctl)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              const uint64_t a_desc = sw128_desc(tiles_u32 + s * STAGE_BYTES);
-              const uint64_t b_desc = sw128_desc(tiles_u32 + s * STAGE_BYTES + A_BYTES);
+            const uint64_t a_desc = sw128_desc(tiles_u32 + s * STAGE_BYTES);
+            const uint64_t b_desc = sw128_desc(tiles_u32 + s * STAGE_BYTES + A_BYTES);
 #pragma unroll
-              for (int kk = 0; kk < BK / 16; ++kk)
-                tc_mma(d_tmem, a_desc + 2u * kk, b_desc + 2u * kk, idesc, (kb | kk) != 0);
-              tc_commit(bar_empty(s));  // frees the stage once these MMAs have read it
-            }
-            if (!ok) break;
-            tc_commit(bar_tfull(buf));  // chunk complete in TMEM
+            for (int kk = 0; kk < BK / 16; ++kk)
+              tc_mma(d_tmem, a_desc + 2u * kk, b_desc + 2u * kk, idesc, (kb | kk) != 0);
+            tc_commit(bar_empty(s));  // frees the stage once these MMAs have read it
           }
+          if (!ok) break;
+          tc_commit(bar_tfull(buf));  // chunk complete in TMEM
+        }
       // all issued MMAs complete before TMEM is released
       tc_commit(bar_done);
       wait_phase_drain(bar_done, 0);
@@ -544,210 +438,102 @@ lookup_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
     const int steps = nch * ngroups;  // 32-column groups of a half
     uint32_t cc = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < tiles; tile += gridDim.x) {
-      const int rt = tile / H, h = tile - (tile / H) * H;
-      bool failed = false;
-      float l1v[KL];  // the half-1 list, kept in registers while half 2 is selected
-      uint32_t l1c[KL / 2];  // its subkey indices, two 16-bit values per register
-      for (int half = 0; ok && half < 2; ++half) {
-        int len = 0, nsorted = 0;
-        float thr = -INFINITY;  // a score is logged when it is > thr
-        float V[KL];            // sorted values of the log's KL best (entries < nsorted)
+    for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+      const int tile = u >> 1, half = u & 1;
+      const int rt = tile / H, h = tile - rt * H;
+      int len = 0, nsorted = 0;
+      float thr = -INFINITY;  // a score is logged when it is > thr
+      float V[KL];            // sorted values of the log's KL best (entries < nsorted)
 #pragma unroll
-        for (int i = 0; i < KL; ++i) V[i] = -INFINITY;
-        uint32_t base = 0;
+      for (int i = 0; i < KL; ++i) V[i] = -INFINITY;
+      uint32_t base = 0;
 #pragma unroll 1
-        for (int st = 0; st <= steps; ++st) {
-          // room for 32 more entries in every lane's log; after the last
-          // group, everything is folded and the log cut to KL entries
-          const bool last = st == steps;
-          if (__any_sync(0xffffffffu, last || len > LOG_CAP - 32))
-            compact_log<KL>(L, len, nsorted, V, thr);
-          if (last) break;
-          const int ch = st / ngroups, g = st - ch * ngroups;
-          if (g == 0) {
-            const uint32_t buf = cc & 1u, use = cc >> 1;
-            // every lane observes the phase; the warp leaves together on failure
-            if (!__all_sync(0xffffffffu, wait_phase(bar_tfull(buf), use & 1u, ctl))) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            base = lane_addr + buf * NCMAX;
-            if (ch == 0 && n > LOG_CAP) {
-              // threshold hint: mean + z * spread of this chunk's scores
-              float a1[4] = {0.0f, 0.0f, 0.0f, 0.0f}, a2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      for (int st = 0; st <= steps; ++st) {
+        // room for 32 more entries in every lane's log; after the last
+        // group, everything is folded and the log cut to KL entries
+        const bool last = st == steps;
+        if (__any_sync(0xffffffffu, last || len > LOG_CAP - 32))
+          compact_log<KL>(L, len, nsorted, V, thr);
+        if (last) break;
+        const int ch = st / ngroups, g = st - ch * ngroups;
+        if (g == 0) {
+          const uint32_t buf = cc & 1u, use = cc >> 1;
+          // every lane observes the phase; the warp leaves together on failure
+          if (!__all_sync(0xffffffffu, wait_phase(bar_tfull(buf), use & 1u, ctl))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          base = lane_addr + buf * NCMAX;
+          if (ch == 0 && n > LOG_CAP) {
+            // threshold hint: mean + z * spread of this chunk's scores
+            float a1[4] = {0.0f, 0.0f, 0.0f, 0.0f}, a2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll 1
-              for (int gg = 0; gg < ngroups; ++gg) {
-                float v[32];
-                tmem_ld32(base + gg * 32, v);
+            for (int gg = 0; gg < ngroups; ++gg) {
+              float v[32];
+              tmem_ld32(base + gg * 32, v);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                  a1[j & 3] += v[j];
-                  a2[j & 3] = fmaf(v[j], v[j], a2[j & 3]);
-                }
+              for (int j = 0; j < 32; ++j) {
+                a1[j & 3] += v[j];
+                a2[j & 3] = fmaf(v[j], v[j], a2[j & 3]);
               }
-              const float s1 = (a1[0] + a1[1]) + (a1[2] + a1[3]);
-              const float s2 = (a2[0] + a2[1]) + (a2[2] + a2[3]);
-              // columns >= n score exactly 0 here (zero-filled subkeys)
-              const float m = (float)(n < NC ? n : NC);
-              const float mu = s1 / m;
-              const float sd = sqrtf(fmaxf(s2 / m - mu * mu, 0.0f));
-              thr = nextafterf(fmaf(hint_z, sd, mu), -INFINITY);  // v > thr <=> v >= hint
             }
-          }
-          float v[32];
-          tmem_ld32(base + g * 32, v);
-          const int col0 = ch * NC + g * 32;
-          if (col0 + 32 > n) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (col0 + j >= n) v[j] = -INFINITY;
-          }
-          {
-            const uint32_t va0 = smem_u32(L.v + row);
-            uint32_t va = va0 + (uint32_t)len * (BM * 4), ca = smem_u32(L.c + row) + (uint32_t)len * (BM * 2);
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              log_append(va, ca, v[j], thr, (unsigned short)(col0 + j));
-            len = (int)((va - va0) / (BM * 4));
-          }
-          if (g == ngroups - 1) {  // chunk consumed: hand the TMEM buffer back
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_tempty(cc & 1u));
-            ++cc;
+            const float s1 = (a1[0] + a1[1]) + (a1[2] + a1[3]);
+            const float s2 = (a2[0] + a2[1]) + (a2[2] + a2[3]);
+            // columns >= n score exactly 0 here (zero-filled subkeys)
+            const float m = (float)(n < NC ? n : NC);
+            const float mu = s1 / m;
+            const float sd = sqrtf(fmaxf(s2 / m - mu * mu, 0.0f));
+            thr = nextafterf(fmaf(hint_z, sd, mu), -INFINITY);  // v > thr <=> v >= hint
           }
         }
-        if (!ok) break;
-        failed |= len < need;
-        // the half's list by (score desc, column asc) into slots [2KL, 3KL)
-        sorted_list<KL>(L, len, V, 2 * KL);
-        if (half == 0) {
+        float v[32];
+        tmem_ld32(base + g * 32, v);
+        const int col0 = ch * NC + g * 32;
+        if (col0 + 32 > n) {
 #pragma unroll
-          for (int i = 0; i < KL; ++i) l1v[i] = L.val(2 * KL + i);
+          for (int j = 0; j < 32; ++j)
+            if (col0 + j >= n) v[j] = -INFINITY;
+        }
+        {
+          const uint32_t va0 = smem_u32(L.v + row);
+          uint32_t va = va0 + (uint32_t)len * (BM * 4),
+                   ca = smem_u32(L.c + row) + (uint32_t)len * (BM * 2);
 #pragma unroll
-          for (int i = 0; i < KL / 2; ++i)
-            l1c[i] = (uint32_t)L.col(2 * KL + 2 * i) | ((uint32_t)L.col(2 * KL + 2 * i + 1) << 16);
-        } else {
-#pragma unroll
-          for (int i = 0; i < KL; ++i) {  // list 1 to slots [KL, 2KL)
-            L.val(KL + i) = l1v[i];
-            L.col(KL + i) = (unsigned short)(l1c[i / 2] >> (16 * (i & 1)));
-          }
+          for (int j = 0; j < 32; ++j)
+            log_append<BM * 4, BM * 2>(va, ca, v[j], thr, (unsigned short)(col0 + j));
+          len = (int)((va - va0) / (BM * 4));
+        }
+        if (g == ngroups - 1) {  // chunk consumed: hand the TMEM buffer back
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_tempty(cc & 1u));
+          ++cc;
         }
       }
       if (!ok) break;
-
       const int b = rt * BM + row;
-      if (b >= B) continue;
-      if (failed) {  // a hint above the row's KL-th score: recomputed by the fallback kernel
-        fb_list[atomicAdd(fb_count, 1)] = b * H + h;
-        continue;
-      }
-      // a4: the k^2 merge.  List 1 is in slots [KL, 2KL), list 2 in
-      // [2KL, 3KL), each by (score desc, subkey asc).  The KL best sums are
-      // found with value-only networks over the candidate pairs; when they are
-      // all distinct and the KL-th is not shared with a left-out pair, each
-      // survivor's output position is the number of larger sums, and
-      // a5 (softmax) follows from the sorted sums.  Exact ties take the
-      // frontier walk below, which orders equal sums by flat index.
-      int64_t* ip = idx + ((int64_t)b * H + h) * k;
-      float* wp = w + ((int64_t)b * H + h) * k;
-      float s1v[KL], s2v[KL];
+      if (b < B) {
+        // the half's list by (score desc, subkey asc) into log slots [KL, 2KL),
+        // then to global memory; a list with fewer than `need` entries (the
+        // threshold hint was above the row's KL-th score) is marked by the
+        // subkey 0xffff in its first slot and recomputed by the fallback
+        sorted_list<KL>(L, len, V, KL);
+        const size_t off = (((size_t)b * H + h) * 2 + half) * KL;
+        float4* gv = reinterpret_cast<float4*>(list_v + off);
 #pragma unroll
-      for (int i = 0; i < KL; ++i) {
-        s1v[i] = L.val(KL + i);
-        s2v[i] = L.val(2 * KL + i);
-      }
-      constexpr MergePairs<KL> P{};
-      float V[KL];
+        for (int i = 0; i < KL; i += 4)
+          gv[i / 4] = make_float4(L.val(KL + i), L.val(KL + i + 1), L.val(KL + i + 2),
+                                  L.val(KL + i + 3));
+        uint4* gc = reinterpret_cast<uint4*>(list_c + off);
 #pragma unroll
-      for (int i = 0; i < KL; ++i) V[i] = -INFINITY;
+        for (int i = 0; i < KL; i += 8) {
+          uint32_t wv[4];
 #pragma unroll
-      for (int blk = 0; blk < P.kPadded / 32; ++blk) {
-        float Bv[32];
-#pragma unroll
-        for (int u = 0; u < 32; ++u) {
-          const int c = blk * 32 + u;
-          Bv[u] = P.i[c] >= 0 ? s1v[P.i[c]] + s2v[P.j[c]] : -INFINITY;
-        }
-        sort_desc<32>(Bv);
-        merge_top<KL>(V, Bv);
-      }
-      const float x = V[KL - 1];
-      bool tie = false;
-#pragma unroll
-      for (int i = 0; i + 1 < KL; ++i) tie |= V[i] == V[i + 1];
-      // survivors: the pairs scoring >= x, as (score, i * 32 + j) in slots
-      // [0, KL); more than KL of them means a tie at x
-      const uint32_t va0 = smem_u32(L.v + row), va_end = va0 + KL * (BM * 4);
-      uint32_t va = va0, ca = smem_u32(L.c + row), nsurv = 0;
-      const float below_x = nextafterf(x, -INFINITY);  // >= x  <=>  > below_x
-#pragma unroll
-      for (int c = 0; c < P.kCount; ++c) {
-        const float sc = s1v[P.i[c]] + s2v[P.j[c]];
-        log_append_bounded(va, ca, nsurv, va_end, sc, below_x,
-                           (unsigned short)(P.i[c] * 32 + P.j[c]));
-      }
-      float z = 0.0f;
-#pragma unroll
-      for (int t = 0; t < KL; ++t)
-        if (t < k) z += expf(V[t] - V[0]);
-      if (!tie && nsurv == (uint32_t)KL) {
-#pragma unroll 2
-        for (int e = 0; e < KL; ++e) {
-          const float sc = L.val(e);
-          const int pc = L.col(e);
-          int r4[4] = {0, 0, 0, 0};
-#pragma unroll
-          for (int i = 0; i < KL; ++i) r4[i & 3] += V[i] > sc;
-          const int r = (r4[0] + r4[1]) + (r4[2] + r4[3]);
-          if (r < k) {
-            ip[r] = (int64_t)((int)L.col(KL + (pc >> 5)) * n + (int)L.col(2 * KL + (pc & 31)));
-            wp[r] = expf(sc - V[0]) / z;
-          }
-        }
-        continue;
-      }
-      // frontier walk (exact ties): row i of the candidate grid is sorted, the
-      // next winner is the best of the rows' heads, (score desc, flat asc).
-      float fv[KL];
-      int ff[KL], fp[KL];
-#pragma unroll
-      for (int i = 0; i < KL; ++i) {
-        fv[i] = s1v[i] + s2v[0];
-        ff[i] = (int)L.col(KL + i) * n + (int)L.col(2 * KL);
-        fp[i] = 0;
-      }
-#pragma unroll 1
-      for (int t = 0; t < k; ++t) {
-        float bv = fv[0];
-        int bf = ff[0], bi = 0, bp = fp[0];
-#pragma unroll
-        for (int i = 1; i < KL; ++i) {
-          const bool better = fv[i] > bv || (fv[i] == bv && ff[i] < bf);
-          bv = better ? fv[i] : bv;
-          bf = better ? ff[i] : bf;
-          bi = better ? i : bi;
-          bp = better ? fp[i] : bp;
-        }
-        ip[t] = (int64_t)bf;
-        wp[t] = expf(bv - V[0]) / z;
-        const int np = bp + 1;
-        float nv = -INFINITY;
-        int nf = 0;
-        if (np < KL) {
-          nv = L.val(KL + bi) + L.val(2 * KL + np);
-          nf = (int)L.col(KL + bi) * n + (int)L.col(2 * KL + np);
-        }
-#pragma unroll
-        for (int i = 0; i < KL; ++i) {
-          if (i == bi) {
-            fv[i] = nv;
-            ff[i] = nf;
-            fp[i] = np;
-          }
+          for (int t = 0; t < 4; ++t)
+            wv[t] = (uint32_t)L.col(KL + i + 2 * t) | ((uint32_t)L.col(KL + i + 2 * t + 1) << 16);
+          if (i == 0 && len < need) wv[0] = (wv[0] & 0xffff0000u) | 0xffffu;
+          gc[i / 8] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
         }
       }
     }
@@ -790,20 +576,20 @@ int sm_count() {
 }
 
 template <int KL>
-cudaError_t launch_kl(const CUtensorMap& mq, const CUtensorMap& mc, int B, int H, int n, int k,
-                      int NC, int nch, int kbc, float hint_z, int64_t* idx, float* w, int* status,
-                      int* fb_count, int* fb_list, cudaStream_t stream) {
+cudaError_t launch_kl(const CUtensorMap& mq, const CUtensorMap& mc, int B, int H, int n, int NC,
+                      int nch, int kbc, float hint_z, float* list_v, unsigned short* list_c,
+                      int* status, cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(lookup_tc_kernel<KL>,
+    cudaError_t e = cudaFuncSetAttribute(select_tc_kernel<KL>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const int tiles = (B + BM - 1) / BM * H;
-  const int grid = tiles < sm_count() ? tiles : sm_count();
-  lookup_tc_kernel<KL><<<grid, NUM_THREADS, SMEM_TOTAL, stream>>>(
-      mq, mc, B, H, n, k, NC, nch, kbc, hint_z, idx, w, status, fb_count, fb_list);
+  const int units = (B + BM - 1) / BM * H * 2;
+  const int grid = units < sm_count() ? units : sm_count();
+  select_tc_kernel<KL><<<grid, NUM_THREADS, SMEM_TOTAL, stream>>>(
+      mq, mc, B, H, n, NC, nch, kbc, hint_z, list_v, list_c, status);
   return cudaGetLastError();
 }
 
@@ -832,9 +618,12 @@ float default_hint_z(int n_keys, int k) {
   return normal_upper_quantile(p);
 }
 
+int list_slots(int k) { return k <= 16 ? 16 : 32; }
+
 cudaError_t launch_lookup_tc(const uint16_t* q, const uint16_t* subkeys, int B, int H, int d_q,
                              int n_keys, int k, float hint_z, int64_t* idx, float* w, int* status,
-                             int* fb_count, int* fb_list, cudaStream_t stream) {
+                             int* fb_count, int* fb_list, float* list_v, unsigned short* list_c,
+                             cudaStream_t stream) {
   if (B == 0) return cudaSuccess;
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
@@ -867,14 +656,17 @@ cudaError_t launch_lookup_tc(const uint16_t* q, const uint16_t* subkeys, int B, 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  cudaError_t e = cudaMemsetAsync(fb_count, 0, sizeof(int), stream);
+  cudaError_t e = k <= 16 ? launch_kl<16>(mq, mc, B, H, n_keys, NC, nch, kbc, hint_z, list_v,
+                                          list_c, status, stream)
+                          : launch_kl<32>(mq, mc, B, H, n_keys, NC, nch, kbc, hint_z, list_v,
+                                          list_c, status, stream);
   if (e != cudaSuccess) return e;
-  e = k <= 16 ? launch_kl<16>(mq, mc, B, H, n_keys, k, NC, nch, kbc, hint_z, idx, w, status,
-                              fb_count, fb_list, stream)
-              : launch_kl<32>(mq, mc, B, H, n_keys, k, NC, nch, kbc, hint_z, idx, w, status,
-                              fb_count, fb_list, stream);
+  // a4, a5: the k^2 merge and softmax, one thread per (query, head)
+  e = cudaMemsetAsync(fb_count, 0, sizeof(int), stream);
   if (e != cudaSuccess) return e;
-  // rows whose threshold hint was too high: exact recomputation on the CUDA cores
+  e = launch_merge(list_v, list_c, B, H, n_keys, k, idx, w, fb_count, fb_list, stream);
+  if (e != cudaSuccess) return e;
+  // pairs whose threshold hint was too high: exact recomputation on the CUDA cores
   return launch_lookup_fallback(q, subkeys, B, H, d_q, n_keys, k, fb_count, fb_list, idx, w,
                                 2 * sm_count(), stream);
 }

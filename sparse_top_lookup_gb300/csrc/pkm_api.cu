@@ -15,6 +15,8 @@ struct pkm_handle {
   int* status;       // device status word
   int* fb_count;     // pairs recomputed by the fallback in the last bf16 lookup
   int* fb_list;      // [max_B * max_H] their (query * H + head) indices
+  float* list_v;     // [max_B * max_H * 2 * 32] per-half lists between the two bf16 kernels
+  unsigned short* list_c;
   float hint_z;      // selection threshold hint override (NaN: automatic)
   void* stage_q;     // pkm_forward_host staging (optional)
   float* stage_out;
@@ -72,7 +74,8 @@ int run_lookup(pkm_t h, const void* q, const void* subkeys, int B, int H, int n,
     const float z = isnan(h->hint_z) ? pkm::default_hint_z(n, k) : h->hint_z;
     return cuda_rc(pkm::launch_lookup_tc(static_cast<const uint16_t*>(q),
                                          static_cast<const uint16_t*>(subkeys), B, H, h->cfg.d_q,
-                                         n, k, z, idx, w, h->status, h->fb_count, h->fb_list, s));
+                                         n, k, z, idx, w, h->status, h->fb_count, h->fb_list,
+                                         h->list_v, h->list_c, s));
   }
   return cuda_rc(pkm::launch_lookup_simt(static_cast<const float*>(q),
                                          static_cast<const float*>(subkeys), B, H, h->cfg.d_q, n,
@@ -119,6 +122,8 @@ void pkm_destroy(pkm_t h) {
   cudaFree(h->status);
   cudaFree(h->fb_count);
   cudaFree(h->fb_list);
+  cudaFree(h->list_v);
+  cudaFree(h->list_c);
   cudaFree(h->stage_q);
   cudaFree(h->stage_out);
   cudaFree(h->stage_idx);
@@ -158,6 +163,11 @@ int pkm_create(pkm_t* out, const pkm_config* cfg) {
     ok = cudaMalloc(&h->fb_count, sizeof(int)) == cudaSuccess &&
          cudaMemset(h->fb_count, 0, sizeof(int)) == cudaSuccess &&
          cudaMalloc(&h->fb_list, (pairs ? pairs : 1) * sizeof(int)) == cudaSuccess;
+    if (ok && cfg->q_dtype == PKM_BF16 && pairs) {
+      const size_t slots = pairs * 2 * pkm::kListMaxSlots;
+      ok = cudaMalloc(&h->list_v, slots * sizeof(float)) == cudaSuccess &&
+           cudaMalloc(&h->list_c, slots * sizeof(unsigned short)) == cudaSuccess;
+    }
   }
   if (ok && cfg->host_staging && cfg->max_B) {
     const size_t qb = (size_t)cfg->max_B * cfg->max_H * cfg->d_q * elem_size(cfg->q_dtype);

@@ -20,14 +20,25 @@ cudaError_t launch_gather(const void* values, int value_dtype, int64_t N, int d_
 cudaError_t launch_lookup_simt(const float* q, const float* subkeys, int B, int H, int d_q,
                                int n_keys, int k, int64_t* idx, float* w, cudaStream_t stream);
 
-// Steps a1-a5 for bf16 queries/subkeys: tcgen05 scoring with the selection,
-// merge and softmax fused into the epilogue.  hint_z sets the per-row
-// selection threshold (mean + hint_z * spread of a row's scores; any value
-// gives exact results).  fb_count / fb_list: device scratch (1 and B*H ints)
-// listing the (query, head) pairs recomputed by the CUDA-core fallback.
+// Steps a1-a5 for bf16 queries/subkeys: tcgen05 scoring with the per-half
+// selection fused into its epilogue, then the k^2 merge and softmax kernel.
+// hint_z sets the per-row selection threshold (mean + hint_z * spread of a
+// row's scores; any value gives exact results).  Device scratch: fb_count /
+// fb_list (1 and B*H ints) list the (query, head) pairs recomputed by the
+// CUDA-core fallback; list_v / list_c (B*H*2*list_slots(k) floats and
+// 16-bit subkeys) hold the per-half lists between the two kernels.
 cudaError_t launch_lookup_tc(const uint16_t* q, const uint16_t* subkeys, int B, int H, int d_q,
                              int n_keys, int k, float hint_z, int64_t* idx, float* w, int* status,
-                             int* fb_count, int* fb_list, cudaStream_t stream);
+                             int* fb_count, int* fb_list, float* list_v, unsigned short* list_c,
+                             cudaStream_t stream);
+
+// Entries of one per-half list for a given k.
+int list_slots(int k);
+
+// Steps a4-a5 from the per-half lists (lookup_merge.cu).
+cudaError_t launch_merge(const float* list_v, const unsigned short* list_c, int B, int H,
+                         int n_keys, int k, int64_t* idx, float* w, int* fb_count, int* fb_list,
+                         cudaStream_t stream);
 
 // The hint_z launch_lookup_tc uses unless a handle overrides it.
 float default_hint_z(int n_keys, int k);
@@ -44,6 +55,7 @@ constexpr int kSimtMaxK = 64;
 constexpr int kSimtMaxNKeys = 4096;
 constexpr int kSimtMaxDq = 8192;
 constexpr int kTcMaxK = 32;
+constexpr int kListMaxSlots = 32;  // list_slots(k) for every supported k
 constexpr int kGatherMaxVecPerRow = 1024;  // 16-byte vectors per value row
 
 }  // namespace pkm

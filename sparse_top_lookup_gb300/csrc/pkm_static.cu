@@ -7,7 +7,8 @@
 // or a latency-critical loop where cudaMalloc / cudaFree would synchronise
 // the device.  pkm_create allocates the handle's scratch, so those callers
 // use this entry point instead.  Its scratch (a status word, the count and
-// the list of (query, head) pairs sent to the CUDA-core fallback) is one
+// the list of (query, head) pairs sent to the CUDA-core fallback, and the
+// per-half lists passed from the selection kernel to the merge kernel) is one
 // fixed-size array in the library's device memory, present on every GPU that
 // loads the library until the process exits.
 #include <cuda_runtime.h>
@@ -19,17 +20,21 @@
 
 namespace {
 
-// [0] device status word, [1] fallback pair count, [2 ..] fallback pair list
-constexpr int kStaticWords = 2 + PKM_STATIC_MAX_PAIRS;
-static __device__ __align__(256) int g_static_scratch[kStaticWords];
+// [0] device status word, [1] fallback pair count, then the fallback pair
+// list and the per-half lists of at most PKM_STATIC_MAX_PAIRS pairs
+constexpr size_t kHeader = 256;
+constexpr size_t kFbBytes = (size_t)PKM_STATIC_MAX_PAIRS * 4;
+constexpr size_t kListSlots = (size_t)PKM_STATIC_MAX_PAIRS * 2 * pkm::kListMaxSlots;
+constexpr size_t kStaticBytes = kHeader + kFbBytes + kListSlots * 4 + kListSlots * 2;
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticBytes];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
-int* g_scratch_addr[kMaxDevices] = {};  // device address of g_static_scratch, per device
+unsigned char* g_scratch_addr[kMaxDevices] = {};  // device address of g_static_scratch, per device
 
 // Device address of the scratch array on the current device.  The first call
 // on a device looks it up (cudaGetSymbolAddress); later calls reuse it.
-int scratch_on_current_device(int** out) {
+int scratch_on_current_device(unsigned char** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PKM_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_setup_mutex);
@@ -39,7 +44,7 @@ int scratch_on_current_device(int** out) {
       cudaGetLastError();
       return PKM_ERR_CUDA;
     }
-    g_scratch_addr[dev] = static_cast<int*>(p);
+    g_scratch_addr[dev] = static_cast<unsigned char*>(p);
   }
   *out = g_scratch_addr[dev];
   return PKM_OK;
@@ -61,16 +66,21 @@ extern "C" int pkm_lookup_static(const void* q, const void* subkeys, int B, int 
   if (!q || !subkeys || !idx || !w) return PKM_ERR_INVALID;
   if (!aligned16(q) || !aligned16(subkeys) || !aligned16(idx) || !aligned16(w))
     return PKM_ERR_ALIGN;
-  int* scratch = nullptr;
-  int rc = scratch_on_current_device(&scratch);
+  unsigned char* base = nullptr;
+  int rc = scratch_on_current_device(&base);
   if (rc) return rc;
+  int* scratch = reinterpret_cast<int*>(base);  // status, fallback count
+  int* fb_list = reinterpret_cast<int*>(base + kHeader);
+  float* list_v = reinterpret_cast<float*>(base + kHeader + kFbBytes);
+  unsigned short* list_c =
+      reinterpret_cast<unsigned short*>(base + kHeader + kFbBytes + kListSlots * 4);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // the status word starts clear on every call (the fallback count is
   // cleared by the lookup launch itself)
   if (cudaMemsetAsync(scratch, 0, sizeof(int), s) != cudaSuccess) return PKM_ERR_CUDA;
   cudaError_t e = pkm::launch_lookup_tc(
       static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(subkeys), B, H, d_q, n_keys,
-      k, pkm::default_hint_z(n_keys, k), idx, w, scratch, scratch + 1, scratch + 2, s);
+      k, pkm::default_hint_z(n_keys, k), idx, w, scratch, scratch + 1, fb_list, list_v, list_c, s);
   if (e != cudaSuccess) return PKM_ERR_CUDA;
   if (status &&
       cudaMemcpyAsync(status, scratch, sizeof(int), cudaMemcpyDeviceToDevice, s) != cudaSuccess)

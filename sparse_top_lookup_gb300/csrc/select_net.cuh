@@ -1,0 +1,119 @@
+// Selection building blocks shared by the lookup kernels: value-only
+// sorting networks, the candidate-pair table of the k^2 merge and
+// branch-free appends to per-row logs in shared memory.
+#pragma once
+
+#include <stdint.h>
+
+namespace pkm {
+
+// Bitonic sort of N values, descending (compile-time network).
+template <int N>
+__device__ __forceinline__ void sort_desc(float (&a)[N]) {
+#pragma unroll
+  for (int size = 2; size <= N; size <<= 1)
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1)
+#pragma unroll
+      for (int i = 0; i < N; ++i) {
+        const int j = i ^ stride;
+        if (j > i) {
+          const float hi = fmaxf(a[i], a[j]), lo = fminf(a[i], a[j]);
+          if ((i & size) == 0) {
+            a[i] = hi;
+            a[j] = lo;
+          } else {
+            a[i] = lo;
+            a[j] = hi;
+          }
+        }
+      }
+}
+
+// V (descending, KL) <- the KL largest of V and B (descending, 32).
+template <int KL>
+__device__ __forceinline__ void merge_top(float (&V)[KL], const float (&B)[32]) {
+#pragma unroll
+  for (int i = 0; i < KL; ++i) V[i] = fmaxf(V[i], B[KL - 1 - i]);  // bitonic
+#pragma unroll
+  for (int stride = KL >> 1; stride > 0; stride >>= 1)
+#pragma unroll
+    for (int i = 0; i < KL; ++i) {
+      const int j = i ^ stride;
+      if (j > i) {
+        const float hi = fmaxf(V[i], V[j]), lo = fminf(V[i], V[j]);
+        V[i] = hi;
+        V[j] = lo;
+      }
+    }
+}
+
+// The candidate pairs (i, j) of the k^2 merge that can reach the top KL:
+// (i + 1)(j + 1) <= KL, since every (i', j') with i' <= i and j' <= j scores
+// at least as much.  Row-major, padded to a multiple of 32 with (-1, -1).
+template <int KL>
+struct MergePairs {
+  static constexpr int count() {
+    int c = 0;
+    for (int i = 0; i < KL; ++i)
+      for (int j = 0; (i + 1) * (j + 1) <= KL; ++j) ++c;
+    return c;
+  }
+  static constexpr int kCount = count();
+  static constexpr int kPadded = (kCount + 31) / 32 * 32;
+  int i[kPadded], j[kPadded];
+  constexpr MergePairs() : i(), j() {
+    int c = 0;
+    for (int a = 0; a < KL; ++a)
+      for (int b = 0; (a + 1) * (b + 1) <= KL; ++b) {
+        i[c] = a;
+        j[c] = b;
+        ++c;
+      }
+    for (; c < kPadded; ++c) {
+      i[c] = -1;
+      j[c] = -1;
+    }
+  }
+};
+
+// Append (v, col) at a log's end when v > thr, without a branch: the two
+// stores are predicated, and the shared-memory addresses of the next free
+// slot (va for the score, ca for the column) advance by one slot row (VSTEP
+// and CSTEP bytes) when the entry is taken.
+template <int VSTEP, int CSTEP>
+__device__ __forceinline__ void log_append(uint32_t& va, uint32_t& ca, float v, float thr,
+                                           unsigned short col) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.gt.f32 p, %2, %3;\n\t"
+      "@p st.shared.f32 [%0], %2;\n\t"
+      "@p st.shared.u16 [%1], %4;\n\t"
+      "@p add.u32 %0, %0, %5;\n\t"
+      "@p add.u32 %1, %1, %6;\n\t}"
+      : "+r"(va), "+r"(ca)
+      : "f"(v), "f"(thr), "h"(col), "n"(VSTEP), "n"(CSTEP)
+      : "memory");
+}
+
+// Count v > thr in `count`, and append (v, col) like log_append while the
+// score address is below va_end.
+template <int VSTEP, int CSTEP>
+__device__ __forceinline__ void log_append_bounded(uint32_t& va, uint32_t& ca, uint32_t& count,
+                                                   uint32_t va_end, float v, float thr,
+                                                   unsigned short col) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.gt.f32 p, %3, %4;\n\t"
+      "@p add.u32 %2, %2, 1;\n\t"
+      "setp.lt.and.u32 p, %0, %8, p;\n\t"
+      "@p st.shared.f32 [%0], %3;\n\t"
+      "@p st.shared.u16 [%1], %5;\n\t"
+      "@p add.u32 %0, %0, %6;\n\t"
+      "@p add.u32 %1, %1, %7;\n\t}"
+      : "+r"(va), "+r"(ca), "+r"(count)
+      : "f"(v), "f"(thr), "h"(col), "n"(VSTEP), "n"(CSTEP), "r"(va_end)
+      : "memory");
+}
+
+}  // namespace pkm
