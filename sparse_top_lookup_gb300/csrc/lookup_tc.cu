@@ -36,13 +36,14 @@ namespace {
 
 constexpr int BM = 128;             // query rows per tile (MMA M)
 constexpr int BK = 64;              // bf16 elements per k-slab: one 128-byte swizzle row
-constexpr int NCMAX = 256;          // subkeys per chunk (MMA N)
+constexpr int NCMAX = 128;          // subkeys per chunk (MMA N)
 constexpr int STAGES = 3;
 constexpr int A_BYTES = BM * BK * 2;     // 16 KiB
-constexpr int B_BYTES = NCMAX * BK * 2;  // 32 KiB
+constexpr int B_BYTES = NCMAX * BK * 2;  // 16 KiB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int SMEM_TILES = STAGES * STAGE_BYTES;
-constexpr int NUM_THREADS = 192;
+constexpr int SETS = 2;                  // epilogue warp sets, each with 2 TMEM buffers
+constexpr int NUM_THREADS = 64 + SETS * 128;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;  // 2 s
 
@@ -123,6 +124,21 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_
       : "memory");
 }
 
+// 16 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 // 32 consecutive fp32 columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];
@@ -190,60 +206,72 @@ __device__ __forceinline__ void wait_phase_drain(uint32_t bar, uint32_t parity) 
 
 // ---------------------------------------------------- selection helpers
 //
-// Per-half selection in the epilogue, one thread per query row.  The ALU
-// pipe (compares, min/max, selects) is the scarce resource here, so the
-// exact top-KL is found without a per-candidate sorted insertion:
-//   1. a per-row threshold hint from the mean and spread of the first
-//      chunk's scores (FMA-pipe arithmetic), aimed at a few times KL of the
-//      row's n scores;
+// Per-half selection in the epilogue, one thread per query row.  Issue slots
+// and the half-rate ALU pipe (compares, min/max, selects) are the scarce
+// resources here, so the exact top-KL is found without a per-candidate
+// sorted insertion:
+//   1. a per-row threshold hint from the mean and spread of the first 256
+//      scores (FMA-pipe arithmetic), aimed at a few times KL of the row's n
+//      scores;
 //   2. every score above the threshold is appended, with its column, to a
-//      per-row log in shared memory (one compare and a predicated store);
+//      per-row log in shared memory: one compare and one predicated 8-byte
+//      store per score;
 //   3. when a log could overflow it is compacted: value-only sorting
-//      networks give its KL-th largest score x, entries below x (and ties at
-//      x beyond the ones the top-KL keeps, later columns first out) are
-//      dropped, and x becomes the new strict threshold.  x is a valid lower
-//      bound on the row's final KL-th score (KL logged scores are >= x), so
-//      everything that can still be selected is in the log: the result stays
-//      exact whatever the hint was;
-//   4. at the end of the half the log is compacted to exactly KL entries and
-//      sorted by (score desc, column asc).
+//      networks fold the new entries into V, the sorted values of the log's
+//      KL best; entries below the KL-th score x (and ties at x beyond the
+//      ones the top-KL keeps, later columns first out) are dropped, and x
+//      becomes the new strict threshold.  x is a valid lower bound on the
+//      row's final KL-th score (KL logged scores are >= x), so everything
+//      that can still be selected is in the log: the result stays exact
+//      whatever the hint was;
+//   4. at the end of the half the log is compacted to exactly KL entries;
+//      each entry's place in the (score desc, column asc) order comes from a
+//      binary search of its score in V.
 // A row whose hint was above its final KL-th score ends with fewer than KL
 // entries; it is reported and recomputed by the CUDA-core fallback kernel.
 
-constexpr int LOG_CAP = 96;  // log entries per row
+constexpr int LOG_CAP = 64;                 // log entries per row and epilogue set
+constexpr int SUB = 8;                      // scores appended between two overflow checks
+constexpr int LOG_STEP = BM * 8;            // bytes from one slot of a row to the next
+constexpr int LOG_BYTES = LOG_CAP * LOG_STEP;
 
-// Per-row log in shared memory, [slot][row] so a warp's 32 rows hit 32
-// different banks whatever their lengths.
+// Per-row log in shared memory: 8-byte entries (score bits, column),
+// [slot][row] so a warp's 32 rows touch distinct banks whatever their lengths.
 struct RowLog {
-  float* v;           // [LOG_CAP][BM]
-  unsigned short* c;  // [LOG_CAP][BM]
+  uint2* e;  // [LOG_CAP][BM]
   int row;
-  __device__ __forceinline__ float& val(int s) const { return v[s * BM + row]; }
-  __device__ __forceinline__ unsigned short& col(int s) const { return c[s * BM + row]; }
+  __device__ __forceinline__ uint2& at(int s) const { return e[s * BM + row]; }
+  __device__ __forceinline__ uint32_t addr(int s) const { return smem_u32(e + s * BM + row); }
 };
 
-// Fold the log entries [nsorted, len) into V, the sorted values of the whole
-// log's KL best; then, if the log holds more than KL entries, keep only
-// those KL (ties at the KL-th score: earliest columns) in column order and
-// raise the threshold to the KL-th score.  Warp-uniform: every lane runs the
-// networks, lanes without new entries fold -inf.
+// Fold the values of log entries [b0, b0 + NB) (those below len) into V.
+template <int KL, int NB>
+__device__ __forceinline__ void fold_block(const RowLog& L, int b0, int len, float (&V)[KL]) {
+  float Bv[NB];
+#pragma unroll
+  for (int j = 0; j < NB; ++j) {
+    const int e = b0 + j < LOG_CAP ? b0 + j : LOG_CAP - 1;  // in bounds, read unconditionally
+    const float x = __uint_as_float(L.at(e).x);
+    Bv[j] = (b0 + j < len) ? x : -INFINITY;
+  }
+  sort_desc<NB>(Bv);
+  merge_top<KL, NB>(V, Bv);
+}
+
+// Fold the log entries [nsorted, len) into V; then, if the log holds more
+// than KL entries, keep only those KL (ties at the KL-th score: earliest
+// columns) in column order and raise the threshold to the KL-th score.
+// Warp-uniform: every lane runs the networks, lanes without new entries fold
+// -inf.
 template <int KL>
 __device__ __forceinline__ void compact_log(const RowLog& L, int& len, int& nsorted,
                                             float (&V)[KL], float& thr) {
 #pragma unroll 1
-  for (int blk = 0; blk < LOG_CAP / 32; ++blk) {
-    const int b0 = nsorted + blk * 32;
-    if (__any_sync(0xffffffffu, len > b0)) {
-      float Bv[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int e = b0 + j < LOG_CAP ? b0 + j : LOG_CAP - 1;  // in bounds, read unconditionally
-        const float x = L.val(e);
-        Bv[j] = (b0 + j < len) ? x : -INFINITY;
-      }
-      sort_desc<32>(Bv);
-      merge_top<KL>(V, Bv);
-    }
+  for (int b0 = nsorted; __any_sync(0xffffffffu, len > b0); b0 += 32) {
+    if (__any_sync(0xffffffffu, len > b0 + 16))
+      fold_block<KL, 32>(L, b0, len, V);
+    else
+      fold_block<KL, 16>(L, b0, len, V);
   }
   nsorted = len;
   if (len <= KL) return;  // at most KL entries: all of them stay
@@ -252,60 +280,57 @@ __device__ __forceinline__ void compact_log(const RowLog& L, int& len, int& nsor
 #pragma unroll
   for (int i = 0; i < KL; ++i) gt += V[i] > x;
   int budget = KL - gt;  // ties at x that stay (earliest columns)
-  int w = 0;
+  const uint2* rp = &L.at(0);
+  uint2* wp = &L.at(0);
 #pragma unroll 4
-  for (int r = 0; r < len; ++r) {
+  for (int r = 0; r < len; ++r, rp += BM) {
     // slot w <= r was already read, so it can be written whether or not the
     // entry stays; w only advances past kept entries
-    const float v = L.val(r);
-    const unsigned short cc = L.col(r);
+    const uint2 t = *rp;
+    const float v = __uint_as_float(t.x);
     const bool eq = v == x;
     const bool keep = v > x || (eq && budget > 0);
     budget -= (eq && keep);
-    L.val(w) = v;
-    L.col(w) = cc;
-    w += keep;
+    *wp = t;
+    wp += keep ? BM : 0;
   }
-  len = w;  // == KL
-  nsorted = w;
+  len = KL;
+  nsorted = KL;
   thr = fmaxf(thr, x);
 }
 
 // Write the log's entries [0, len) (column order, values sorted in V) to
-// slots [dst, dst + KL) ordered by (score desc, column asc): an entry's slot
-// is the number of larger values, plus the number of earlier entries with
-// the same value.  Unused slots get -inf.
+// slots [KL, 2KL) ordered by (score desc, column asc): an entry's slot is
+// the number of larger values, plus the number of earlier entries with the
+// same value.  Unused slots get -inf.
 template <int KL>
 __device__ __forceinline__ void sorted_list(const RowLog& L, int len, const float (&V)[KL],
-                                            int dst) {
+                                            bool check_ties) {
   bool tie = false;
 #pragma unroll
   for (int i = 0; i + 1 < KL; ++i) tie |= (V[i] == V[i + 1]) && (V[i] > -INFINITY);
+  tie &= check_ties;
 #pragma unroll 2
   for (int e = 0; e < len; ++e) {
-    const float x = L.val(e);
-    const unsigned short c = L.col(e);
-    int r4[4] = {0, 0, 0, 0};
-#pragma unroll
-    for (int i = 0; i < KL; ++i) r4[i & 3] += V[i] > x;
-    int r = (r4[0] + r4[1]) + (r4[2] + r4[3]);
+    const uint2 t = L.at(e);
+    const float x = __uint_as_float(t.x);
+    int r = count_greater<KL>(V, x);
     if (tie)
-      for (int e2 = 0; e2 < e; ++e2) r += L.val(e2) == x;
-    L.val(dst + r) = x;
-    L.col(dst + r) = c;
+      for (int e2 = 0; e2 < e; ++e2) r += __uint_as_float(L.at(e2).x) == x;
+    L.at(KL + r) = t;
   }
 #pragma unroll 1
-  for (int r = len; r < KL; ++r) {
-    L.val(dst + r) = -INFINITY;
-    L.col(dst + r) = 0;
-  }
+  for (int r = len; r < KL; ++r) L.at(KL + r) = make_uint2(__float_as_uint(-INFINITY), 0u);
 }
 
 // ---------------------------------------------------------------- kernel
 
-constexpr int LOG_BYTES = LOG_CAP * BM * (4 + 2);
-constexpr int SMEM_TOTAL = SMEM_TILES + LOG_BYTES + 1024;  // + alignment slack
+constexpr int SMEM_TOTAL = SMEM_TILES + SETS * LOG_BYTES + 1024;  // + alignment slack
 
+// A CTA's units are u_i = blockIdx.x + i * gridDim.x; epilogue set i % 2
+// takes unit u_i.  The producer and the MMA walk the units two at a time,
+// chunk by chunk, alternating sets, so both sets are fed; set s's chunks go to
+// TMEM buffers 2s and 2s+1 in turn.
 template <int KL>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_c,
@@ -313,15 +338,13 @@ select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
                  float* __restrict__ list_v, unsigned short* __restrict__ list_c,
                  int* __restrict__ status) {
   extern __shared__ unsigned char smem_raw[];
-  __shared__ __align__(8) uint64_t bars[2 * STAGES + 5];
+  __shared__ __align__(8) uint64_t bars[2 * STAGES + 4 * SETS + 1];
   __shared__ uint32_t s_tmem_base;
   __shared__ int s_abort;
 
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t tiles_u32 = smem_u32(smem);
-  float* log_v = reinterpret_cast<float*>(smem + SMEM_TILES);
-  unsigned short* log_c = reinterpret_cast<unsigned short*>(smem + SMEM_TILES + LOG_CAP * BM * 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -329,17 +352,17 @@ select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
   auto bar_full = [&](uint32_t s) { return bar0 + 8u * s; };
   auto bar_empty = [&](uint32_t s) { return bar0 + 8u * (STAGES + s); };
   auto bar_tfull = [&](uint32_t b) { return bar0 + 8u * (2 * STAGES + b); };
-  auto bar_tempty = [&](uint32_t b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
-  const uint32_t bar_done = bar0 + 8u * (2 * STAGES + 4);
+  auto bar_tempty = [&](uint32_t b) { return bar0 + 8u * (2 * STAGES + 2 * SETS + b); };
+  const uint32_t bar_done = bar0 + 8u * (2 * STAGES + 4 * SETS);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar_full(s), 1);
       mbar_init(bar_empty(s), 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < 2 * SETS; ++b) {
       mbar_init(bar_tfull(b), 1);
-      mbar_init(bar_tempty(b), 4);  // one arrival per epilogue warp
+      mbar_init(bar_tempty(b), 4);  // one arrival per warp of the buffer's set
     }
     mbar_init(bar_done, 1);
     s_abort = 0;
@@ -362,6 +385,7 @@ select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
   // work unit u: tile u / 2 (row tile, head), half u % 2
   const int row_tiles = (B + BM - 1) / BM;
   const int units = row_tiles * H * 2;
+  const int mine = blockIdx.x < units ? (units - 1 - blockIdx.x) / gridDim.x + 1 : 0;
 
   if (warp == 0) {
     // ---------------------------------------------------- TMA producer
@@ -369,23 +393,25 @@ select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
       const uint32_t tx = (uint32_t)(A_BYTES + NC * BK * 2);
       uint32_t it = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
-        const int tile = u >> 1, half = u & 1;
-        const int rt = tile / H, h = tile - rt * H;
+      for (int i0 = 0; ok && i0 < mine; i0 += SETS)
         for (int ch = 0; ok && ch < nch; ++ch)
-          for (int kb = 0; kb < kb_count; ++kb) {
-            const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-            if (!wait_phase(bar_empty(s), ph ^ 1u, ctl)) {
-              ok = false;
-              break;
+          for (int st = 0; ok && st < SETS && i0 + st < mine; ++st) {
+            const int u = blockIdx.x + (i0 + st) * gridDim.x;
+            const int tile = u >> 1, half = u & 1;
+            const int rt = tile / H, h = tile - rt * H;
+            for (int kb = 0; kb < kb_count; ++kb) {
+              const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+              if (!wait_phase(bar_empty(s), ph ^ 1u, ctl)) {
+                ok = false;
+                break;
+              }
+              mbar_expect_tx(bar_full(s), tx);
+              const uint32_t a_dst = tiles_u32 + s * STAGE_BYTES;
+              tma_load_4d(a_dst, &tmap_q, kb * BK, half, h, rt * BM, bar_full(s));
+              tma_load_3d(a_dst + A_BYTES, &tmap_c, kb * BK, ch * NC, h * 2 + half, bar_full(s));
+              ++it;
             }
-            mbar_expect_tx(bar_full(s), tx);
-            const uint32_t a_dst = tiles_u32 + s * STAGE_BYTES;
-            tma_load_4d(a_dst, &tmap_q, kb * BK, half, h, rt * BM, bar_full(s));
-            tma_load_3d(a_dst + A_BYTES, &tmap_c, kb * BK, ch * NC, h * 2 + half, bar_full(s));
-            ++it;
           }
-      }
       if (!ok) {  // let the copies already issued land before the CTA exits
         const uint32_t first = it > (uint32_t)STAGES ? it - STAGES : 0u;
         for (uint32_t j = first; j < it; ++j) wait_phase_drain(bar_full(j % STAGES), (j / STAGES) & 1u);
@@ -395,145 +421,164 @@ select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
     // ---------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16(BM, NC);
-      uint32_t it = 0, cc = 0;
+      uint32_t it = 0, cnt[SETS] = {};
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < units; u += gridDim.x)
-        for (int ch = 0; ok && ch < nch; ++ch, ++cc) {
-          const uint32_t buf = cc & 1u, use = cc >> 1;
-          if (!wait_phase(bar_tempty(buf), (use & 1u) ^ 1u, ctl)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t d_tmem = tmem + buf * NCMAX;
-          for (int kb = 0; kb < kb_count; ++kb, ++it) {
-            const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-            if (!wait_phase(bar_full(s), ph, ctl)) {
+      for (int i0 = 0; ok && i0 < mine; i0 += SETS)
+        for (int ch = 0; ok && ch < nch; ++ch)
+          for (int st = 0; ok && st < SETS && i0 + st < mine; ++st) {
+            const uint32_t buf = 2 * st + (cnt[st] & 1u), use = cnt[st] >> 1;
+            ++cnt[st];
+            if (!wait_phase(bar_tempty(buf), (use & 1u) ^ 1u, ctl)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint64_t a_desc = sw128_desc(tiles_u32 + s * STAGE_BYTES);
-            const uint64_t b_desc = sw128_desc(tiles_u32 + s * STAGE_BYTES + A_BYTES);
+            const uint32_t d_tmem = tmem + buf * NCMAX;
+            for (int kb = 0; kb < kb_count; ++kb, ++it) {
+              const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+              if (!wait_phase(bar_full(s), ph, ctl)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint64_t a_desc = sw128_desc(tiles_u32 + s * STAGE_BYTES);
+              const uint64_t b_desc = sw128_desc(tiles_u32 + s * STAGE_BYTES + A_BYTES);
 #pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk)
-              tc_mma(d_tmem, a_desc + 2u * kk, b_desc + 2u * kk, idesc, (kb | kk) != 0);
-            tc_commit(bar_empty(s));  // frees the stage once these MMAs have read it
+              for (int kk = 0; kk < BK / 16; ++kk)
+                tc_mma(d_tmem, a_desc + 2u * kk, b_desc + 2u * kk, idesc, (kb | kk) != 0);
+              tc_commit(bar_empty(s));  // frees the stage once these MMAs have read it
+            }
+            if (!ok) break;
+            tc_commit(bar_tfull(buf));  // chunk complete in TMEM
           }
-          if (!ok) break;
-          tc_commit(bar_tfull(buf));  // chunk complete in TMEM
-        }
       // all issued MMAs complete before TMEM is released
       tc_commit(bar_done);
       wait_phase_drain(bar_done, 0);
     }
   } else {
-    // ---------------------------------------------------- epilogue
+    // ---------------------------------------------------- epilogue sets
+    const int set = (warp - 2) >> 2;
     const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
     const int row = quad * 32 + lane;
     const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16);
-    const RowLog L{log_v, log_c, row};
+    const RowLog L{reinterpret_cast<uint2*>(smem + SMEM_TILES + set * LOG_BYTES), row};
+    const uint32_t log0 = L.addr(0);
+    // a log at or below this address has room for SUB more entries
+    const uint32_t log_room = log0 + (uint32_t)(LOG_CAP - SUB) * LOG_STEP;
     const int need = KL < n ? KL : n;  // valid entries a full list holds
-    const int ngroups = NC / 32;
-    const int steps = nch * ngroups;  // 32-column groups of a half
-    uint32_t cc = 0;
+    uint32_t cnt = 0;                  // chunks of this set consumed so far
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+    for (int i = set; ok && i < mine; i += SETS) {
+      const int u = blockIdx.x + i * gridDim.x;
       const int tile = u >> 1, half = u & 1;
       const int rt = tile / H, h = tile - rt * H;
-      int len = 0, nsorted = 0;
+      int nsorted = 0;
       float thr = -INFINITY;  // a score is logged when it is > thr
       float V[KL];            // sorted values of the log's KL best (entries < nsorted)
 #pragma unroll
-      for (int i = 0; i < KL; ++i) V[i] = -INFINITY;
-      uint32_t base = 0;
+      for (int i2 = 0; i2 < KL; ++i2) V[i2] = -INFINITY;
+      uint32_t va = log0;  // next free slot of this row's log
 #pragma unroll 1
-      for (int st = 0; st <= steps; ++st) {
-        // room for 32 more entries in every lane's log; after the last
-        // group, everything is folded and the log cut to KL entries
-        const bool last = st == steps;
-        if (__any_sync(0xffffffffu, last || len > LOG_CAP - 32))
-          compact_log<KL>(L, len, nsorted, V, thr);
-        if (last) break;
-        const int ch = st / ngroups, g = st - ch * ngroups;
-        if (g == 0) {
-          const uint32_t buf = cc & 1u, use = cc >> 1;
-          // every lane observes the phase; the warp leaves together on failure
-          if (!__all_sync(0xffffffffu, wait_phase(bar_tfull(buf), use & 1u, ctl))) {
-            ok = false;
-            break;
+      for (int ch = 0; ch < nch; ++ch) {
+        // wait for this chunk; at the start of a unit also for the next one
+        // (the threshold hint uses the first two chunks' scores), which is
+        // then not waited for again
+        const int upto = (ch == 0 && nch > 1) ? 2 : 1;
+        if (ch != 1) {
+          for (int c = 0; c < upto && ok; ++c) {
+            const uint32_t cc = cnt + (uint32_t)c;
+            ok = __all_sync(0xffffffffu,
+                            wait_phase(bar_tfull(2 * set + (cc & 1u)), (cc >> 1) & 1u, ctl));
           }
-          tc_fence_after();
-          base = lane_addr + buf * NCMAX;
-          if (ch == 0 && n > LOG_CAP) {
-            // threshold hint: mean + z * spread of this chunk's scores
-            float a1[4] = {0.0f, 0.0f, 0.0f, 0.0f}, a2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        }
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t base = lane_addr + (2 * set + (cnt & 1u)) * NCMAX;
+        if (ch == 0 && n > LOG_CAP) {
+          // threshold hint: mean + z * spread of the first chunks' scores
+          float a1[4] = {0.0f, 0.0f, 0.0f, 0.0f}, a2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll 1
-            for (int gg = 0; gg < ngroups; ++gg) {
+          for (int c = 0; c < upto; ++c) {
+            const uint32_t cb = lane_addr + (2 * set + ((cnt + c) & 1u)) * NCMAX;
+#pragma unroll 1
+            for (int gg = 0; gg < NC; gg += 32) {
               float v[32];
-              tmem_ld32(base + gg * 32, v);
+              tmem_ld32(cb + gg, v);
 #pragma unroll
               for (int j = 0; j < 32; ++j) {
                 a1[j & 3] += v[j];
                 a2[j & 3] = fmaf(v[j], v[j], a2[j & 3]);
               }
             }
-            const float s1 = (a1[0] + a1[1]) + (a1[2] + a1[3]);
-            const float s2 = (a2[0] + a2[1]) + (a2[2] + a2[3]);
-            // columns >= n score exactly 0 here (zero-filled subkeys)
-            const float m = (float)(n < NC ? n : NC);
-            const float mu = s1 / m;
-            const float sd = sqrtf(fmaxf(s2 / m - mu * mu, 0.0f));
-            thr = nextafterf(fmaf(hint_z, sd, mu), -INFINITY);  // v > thr <=> v >= hint
+          }
+          const float s1 = (a1[0] + a1[1]) + (a1[2] + a1[3]);
+          const float s2 = (a2[0] + a2[1]) + (a2[2] + a2[3]);
+          // columns >= n score exactly 0 here (zero-filled subkeys)
+          const float m = (float)(n < upto * NC ? n : upto * NC);
+          const float mu = s1 / m;
+          const float sd = sqrtf(fmaxf(s2 / m - mu * mu, 0.0f));
+          thr = nextafterf(fmaf(hint_z, sd, mu), -INFINITY);  // v > thr <=> v >= hint
+        }
+        const int col_end = n - ch * NC;  // columns of this chunk below n (may exceed NC)
+#pragma unroll 1
+        for (int g = 0; g < NC; g += 16) {
+          float v[16];
+          tmem_ld16(base + g, v);
+          if (g + 16 > col_end) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (g + j >= col_end) v[j] = -INFINITY;
+          }
+          const uint32_t c0 = (uint32_t)(ch * NC + g);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) log_push<LOG_STEP>(va, v[j], thr, c0 + j);
+          if (__any_sync(0xffffffffu, va > log_room)) {
+            int len = (int)((va - log0) / LOG_STEP);
+            compact_log<KL>(L, len, nsorted, V, thr);
+            va = log0 + (uint32_t)len * LOG_STEP;
+          }
+#pragma unroll
+          for (int j = 8; j < 16; ++j) log_push<LOG_STEP>(va, v[j], thr, c0 + j);
+          if (__any_sync(0xffffffffu, va > log_room)) {
+            int len = (int)((va - log0) / LOG_STEP);
+            compact_log<KL>(L, len, nsorted, V, thr);
+            va = log0 + (uint32_t)len * LOG_STEP;
           }
         }
-        float v[32];
-        tmem_ld32(base + g * 32, v);
-        const int col0 = ch * NC + g * 32;
-        if (col0 + 32 > n) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (col0 + j >= n) v[j] = -INFINITY;
-        }
-        {
-          const uint32_t va0 = smem_u32(L.v + row);
-          uint32_t va = va0 + (uint32_t)len * (BM * 4),
-                   ca = smem_u32(L.c + row) + (uint32_t)len * (BM * 2);
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            log_append<BM * 4, BM * 2>(va, ca, v[j], thr, (unsigned short)(col0 + j));
-          len = (int)((va - va0) / (BM * 4));
-        }
-        if (g == ngroups - 1) {  // chunk consumed: hand the TMEM buffer back
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar_tempty(cc & 1u));
-          ++cc;
-        }
+        // chunk consumed: hand the TMEM buffer back
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_tempty(2 * set + (cnt & 1u)));
+        ++cnt;
       }
       if (!ok) break;
+      // everything folded and the log cut to KL entries
+      int len = (int)((va - log0) / LOG_STEP);
+      compact_log<KL>(L, len, nsorted, V, thr);
       const int b = rt * BM + row;
+      // the half's list by (score desc, subkey asc) into log slots [KL, 2KL),
+      // then to global memory; a list with fewer than `need` entries (the
+      // threshold hint was above the row's KL-th score) is marked by the
+      // subkey 0xffff in its first slot and recomputed by the fallback
+      sorted_list<KL>(L, len, V, b < B);
       if (b < B) {
-        // the half's list by (score desc, subkey asc) into log slots [KL, 2KL),
-        // then to global memory; a list with fewer than `need` entries (the
-        // threshold hint was above the row's KL-th score) is marked by the
-        // subkey 0xffff in its first slot and recomputed by the fallback
-        sorted_list<KL>(L, len, V, KL);
         const size_t off = (((size_t)b * H + h) * 2 + half) * KL;
         float4* gv = reinterpret_cast<float4*>(list_v + off);
-#pragma unroll
-        for (int i = 0; i < KL; i += 4)
-          gv[i / 4] = make_float4(L.val(KL + i), L.val(KL + i + 1), L.val(KL + i + 2),
-                                  L.val(KL + i + 3));
         uint4* gc = reinterpret_cast<uint4*>(list_c + off);
 #pragma unroll
-        for (int i = 0; i < KL; i += 8) {
+        for (int i2 = 0; i2 < KL; i2 += 8) {
+          uint2 t[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) t[q] = L.at(KL + i2 + q);
+          gv[i2 / 4] = make_float4(__uint_as_float(t[0].x), __uint_as_float(t[1].x),
+                                   __uint_as_float(t[2].x), __uint_as_float(t[3].x));
+          gv[i2 / 4 + 1] = make_float4(__uint_as_float(t[4].x), __uint_as_float(t[5].x),
+                                       __uint_as_float(t[6].x), __uint_as_float(t[7].x));
           uint32_t wv[4];
 #pragma unroll
-          for (int t = 0; t < 4; ++t)
-            wv[t] = (uint32_t)L.col(KL + i + 2 * t) | ((uint32_t)L.col(KL + i + 2 * t + 1) << 16);
-          if (i == 0 && len < need) wv[0] = (wv[0] & 0xffff0000u) | 0xffffu;
-          gc[i / 8] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+          for (int q = 0; q < 4; ++q) wv[q] = (t[2 * q].y & 0xffffu) | (t[2 * q + 1].y << 16);
+          if (i2 == 0 && len < need) wv[0] = (wv[0] & 0xffff0000u) | 0xffffu;
+          gc[i2 / 8] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
         }
       }
     }
@@ -587,7 +632,7 @@ cudaError_t launch_kl(const CUtensorMap& mq, const CUtensorMap& mc, int B, int H
     attr_set = true;
   }
   const int units = (B + BM - 1) / BM * H * 2;
-  const int grid = units < sm_count() ? units : sm_count();
+  const int grid = units < sm_count() ? units : sm_count();  // persistent: one CTA per SM
   select_tc_kernel<KL><<<grid, NUM_THREADS, SMEM_TOTAL, stream>>>(
       mq, mc, B, H, n, NC, nch, kbc, hint_z, list_v, list_c, status);
   return cudaGetLastError();

@@ -30,11 +30,18 @@ __device__ __forceinline__ void sort_desc(float (&a)[N]) {
       }
 }
 
-// V (descending, KL) <- the KL largest of V and B (descending, 32).
-template <int KL>
-__device__ __forceinline__ void merge_top(float (&V)[KL], const float (&B)[32]) {
+// V (descending, KL) <- the KL largest of V and B (descending, NB).  The
+// elementwise max of V and B reversed (B padded with -inf) holds the KL
+// largest of both and is bitonic; a bitonic merge sorts it.
+template <int KL, int NB>
+__device__ __forceinline__ void merge_top(float (&V)[KL], const float (&B)[NB]) {
+  if (NB >= KL) {
 #pragma unroll
-  for (int i = 0; i < KL; ++i) V[i] = fmaxf(V[i], B[KL - 1 - i]);  // bitonic
+    for (int i = 0; i < KL; ++i) V[i] = fmaxf(V[i], B[KL - 1 - i]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < NB; ++i) V[KL - NB + i] = fmaxf(V[KL - NB + i], B[NB - 1 - i]);
+  }
 #pragma unroll
   for (int stride = KL >> 1; stride > 0; stride >>= 1)
 #pragma unroll
@@ -46,6 +53,27 @@ __device__ __forceinline__ void merge_top(float (&V)[KL], const float (&B)[32]) 
         V[j] = lo;
       }
     }
+}
+
+// Number of entries of V (descending) greater than x: a binary search whose
+// probes are taken from registers by selects (no dynamic indexing).  P holds
+// the current window of V, halved at every step.
+template <int KL>
+__device__ __forceinline__ int count_greater(const float (&V)[KL], float x) {
+  float P[KL];
+#pragma unroll
+  for (int i = 0; i < KL; ++i) P[i] = V[i];
+  int r = 0;
+#pragma unroll
+  for (int s = KL / 2; s >= 1; s >>= 1) {
+    const bool gt = P[s - 1] > x;  // the whole lower half of the window is > x
+    r += gt ? s : 0;
+    if (s > 1) {
+#pragma unroll
+      for (int i = 0; i < s; ++i) P[i] = gt ? P[s + i] : P[i];
+    }
+  }
+  return r;
 }
 
 // The candidate pairs (i, j) of the k^2 merge that can reach the top KL:
@@ -93,6 +121,21 @@ __device__ __forceinline__ void log_append(uint32_t& va, uint32_t& ca, float v, 
       "@p add.u32 %1, %1, %6;\n\t}"
       : "+r"(va), "+r"(ca)
       : "f"(v), "f"(thr), "h"(col), "n"(VSTEP), "n"(CSTEP)
+      : "memory");
+}
+
+// Append the 8-byte entry (v, col) at a log's end when v > thr, without a
+// branch: one predicated store, and the shared-memory address of the next
+// free slot advances by STEP bytes when the entry is taken.
+template <int STEP>
+__device__ __forceinline__ void log_push(uint32_t& a, float v, float thr, uint32_t col) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.gt.f32 p, %1, %2;\n\t"
+      "@p st.shared.v2.b32 [%0], {%1, %3};\n\t"
+      "@p add.u32 %0, %0, %4;\n\t}"
+      : "+r"(a)
+      : "f"(v), "f"(thr), "r"(col), "n"(STEP)
       : "memory");
 }
 
