@@ -27,22 +27,39 @@ namespace {
 constexpr int kThreads = 128;
 
 template <int KL>
+struct MergeLayout {
+  static constexpr MergePairs<KL> P{};
+  static constexpr int kRow01 = KL + KL / 2;         // candidates of rows 0 and 1 (table is row-major)
+  static constexpr int kRest = P.kCount - kRow01;    // candidates of rows >= 2
+  // region A, 4-byte slots in [slot][thread] order: the rows >= 2 scores
+  // staged for folding (slots [0, kRest)), later the survivors' scores
+  // (slots [0, KL)) and pair codes (slots [KL, 2KL)).  Every use keeps a
+  // thread inside its own column, so warps in different phases never touch
+  // each other's slots.
+  static constexpr int kRegionA = (kRest > 2 * KL ? kRest : 2 * KL) * 4 * kThreads;
+  static constexpr int kBytes = kRegionA + 2 * KL * 2 * kThreads;  // + the lists' subkeys
+};
+
+template <int KL>
 __global__ void __launch_bounds__(kThreads)
 merge_kernel(const float* __restrict__ list_v, const unsigned short* __restrict__ list_c,
              int pairs, int n, int k, int64_t* __restrict__ idx, float* __restrict__ w,
              int* __restrict__ fb_count, int* __restrict__ fb_list) {
+  using Lay = MergeLayout<KL>;
+  constexpr MergePairs<KL> P{};
   extern __shared__ __align__(16) unsigned char smem[];
-  // per thread, [slot][thread] layouts: survivors' scores and (i*32+j), and
-  // the two lists' subkeys
+  float* stg = reinterpret_cast<float*>(smem);                                  // [kRest][T]
   float* sv = reinterpret_cast<float*>(smem);                                   // [KL][T]
-  unsigned short* sp = reinterpret_cast<unsigned short*>(sv + KL * kThreads);   // [KL][T]
-  unsigned short* sc = sp + KL * kThreads;                                      // [2KL][T]
+  uint32_t* sp = reinterpret_cast<uint32_t*>(sv + KL * kThreads);               // [KL][T]
+  unsigned short* sc = reinterpret_cast<unsigned short*>(smem + Lay::kRegionA); // [2KL][T]
   const int t = threadIdx.x;
   const int pair = blockIdx.x * kThreads + t;
-  if (pair >= pairs) return;
+  // every lane stays to the end (warp votes below); lanes without a pair of
+  // their own work on zeros and store nothing
+  bool valid = pair < pairs;
 
-  const float* v1 = list_v + (size_t)pair * 2 * KL;
-  const unsigned short* c1 = list_c + (size_t)pair * 2 * KL;
+  const float* v1 = list_v + (size_t)(valid ? pair : 0) * 2 * KL;
+  const unsigned short* c1 = list_c + (size_t)(valid ? pair : 0) * 2 * KL;
   float s1v[KL], s2v[KL];
   {
     const float4* g = reinterpret_cast<const float4*>(v1);
@@ -64,43 +81,80 @@ merge_kernel(const float* __restrict__ list_v, const unsigned short* __restrict_
       }
     }
   }
-  if (sc[t] == 0xffffu || sc[KL * kThreads + t] == 0xffffu) {
+  if (valid && (sc[t] == 0xffffu || sc[KL * kThreads + t] == 0xffffu)) {
     fb_list[atomicAdd(fb_count, 1)] = pair;
-    return;
+    valid = false;
+  }
+  if (!valid) {
+#pragma unroll
+    for (int i = 0; i < KL; ++i) s1v[i] = s2v[i] = 0.0f;
   }
   auto col1 = [&](int i) { return (int)sc[i * kThreads + t]; };
   auto col2 = [&](int j) { return (int)sc[(KL + j) * kThreads + t]; };
 
-  constexpr MergePairs<KL> P{};
+  // V: the sorted KL best sums.  Row 0 of the candidate grid is already in
+  // descending order; row 1 is too, and one bitonic merge takes it in.
   float V[KL];
 #pragma unroll
-  for (int i = 0; i < KL; ++i) V[i] = -INFINITY;
+  for (int j = 0; j < KL; ++j) V[j] = s1v[0] + s2v[j];
+  {
+    float R[KL / 2];
 #pragma unroll
-  for (int blk = 0; blk < P.kPadded / 32; ++blk) {
-    float Bv[32];
+    for (int j = 0; j < KL / 2; ++j) R[j] = s1v[1] + s2v[j];
+    merge_top<KL, KL / 2>(V, R);
+  }
+  // rows >= 2: only sums above V's KL-th can change V; they are staged in
+  // shared memory and folded in blocks
+  {
+    const float x1 = V[KL - 1];
+    const uint32_t a0 = static_cast<uint32_t>(__cvta_generic_to_shared(stg + t));
+    uint32_t a = a0;
 #pragma unroll
-    for (int u = 0; u < 32; ++u) {
-      const int c = blk * 32 + u;
-      Bv[u] = P.i[c] >= 0 ? s1v[P.i[c]] + s2v[P.j[c]] : -INFINITY;
+    for (int c = Lay::kRow01; c < P.kCount; ++c)
+      stage_push<kThreads * 4>(a, s1v[P.i[c]] + s2v[P.j[c]], x1);
+    const int m = (int)((a - a0) / (kThreads * 4));
+#pragma unroll 1
+    for (int b0 = 0; __any_sync(0xffffffffu, m > b0); b0 += 32) {
+      if (__any_sync(0xffffffffu, m > b0 + 16)) {
+        float Bv[32];
+#pragma unroll
+        for (int u = 0; u < 32; ++u) {
+          const int e = b0 + u < Lay::kRest ? b0 + u : Lay::kRest - 1;
+          const float x = stg[e * kThreads + t];
+          Bv[u] = b0 + u < m ? x : -INFINITY;
+        }
+        sort_desc<32>(Bv);
+        merge_top<KL, 32>(V, Bv);
+      } else {
+        float Bv[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          const int e = b0 + u < Lay::kRest ? b0 + u : Lay::kRest - 1;
+          const float x = stg[e * kThreads + t];
+          Bv[u] = b0 + u < m ? x : -INFINITY;
+        }
+        sort_desc<16>(Bv);
+        merge_top<KL, 16>(V, Bv);
+      }
     }
-    sort_desc<32>(Bv);
-    merge_top<KL>(V, Bv);
   }
   const float x = V[KL - 1];
   bool tie = false;
 #pragma unroll
   for (int i = 0; i + 1 < KL; ++i) tie |= V[i] == V[i + 1];
   // survivors: pairs scoring >= x; more than KL of them means a tie at x
+  // (region A is free again: the staged scores were all folded)
   const uint32_t va0 = static_cast<uint32_t>(__cvta_generic_to_shared(sv + t));
   const uint32_t va_end = va0 + KL * (kThreads * 4);
-  uint32_t va = va0, ca = static_cast<uint32_t>(__cvta_generic_to_shared(sp + t)), nsurv = 0;
+  uint32_t va = va0, nsurv = 0;
   const float below_x = nextafterf(x, -INFINITY);  // >= x  <=>  > below_x
 #pragma unroll
   for (int c = 0; c < P.kCount; ++c) {
     const float s = s1v[P.i[c]] + s2v[P.j[c]];
-    log_append_bounded<kThreads * 4, kThreads * 2>(va, ca, nsurv, va_end, s, below_x,
-                                                   (unsigned short)(P.i[c] * 32 + P.j[c]));
+    surv_push<kThreads * 4, KL * kThreads * 4>(va, nsurv, va_end, s, below_x,
+                                               (uint32_t)(P.i[c] * 32 + P.j[c]));
   }
+  if (!valid) return;
   float z = 0.0f;
 #pragma unroll
   for (int r = 0; r < KL; ++r)
@@ -111,11 +165,8 @@ merge_kernel(const float* __restrict__ list_v, const unsigned short* __restrict_
 #pragma unroll 2
     for (int e = 0; e < KL; ++e) {
       const float s = sv[e * kThreads + t];
-      const int pc = sp[e * kThreads + t];
-      int r4[4] = {0, 0, 0, 0};
-#pragma unroll
-      for (int i = 0; i < KL; ++i) r4[i & 3] += V[i] > s;
-      const int r = (r4[0] + r4[1]) + (r4[2] + r4[3]);
+      const int pc = (int)sp[e * kThreads + t];
+      const int r = count_greater<KL>(V, s);
       if (r < k) {
         ip[r] = (int64_t)(col1(pc >> 5) * n + col2(pc & 31));
         wp[r] = expf(s - V[0]) / z;
@@ -169,7 +220,7 @@ template <int KL>
 cudaError_t launch_merge_kl(const float* list_v, const unsigned short* list_c, int pairs, int n,
                             int k, int64_t* idx, float* w, int* fb_count, int* fb_list,
                             cudaStream_t stream) {
-  const size_t smem = (size_t)KL * kThreads * (4 + 2) + (size_t)2 * KL * kThreads * 2;
+  const size_t smem = MergeLayout<KL>::kBytes;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(merge_kernel<KL>,

@@ -1,6 +1,6 @@
 // Selection building blocks shared by the lookup kernels: value-only
-// sorting networks, the candidate-pair table of the k^2 merge and
-// branch-free appends to per-row logs in shared memory.
+// sorting networks, a register binary search, the candidate-pair table of
+// the k^2 merge and branch-free appends to per-thread logs in shared memory.
 #pragma once
 
 #include <stdint.h>
@@ -35,7 +35,7 @@ __device__ __forceinline__ void sort_desc(float (&a)[N]) {
 // largest of both and is bitonic; a bitonic merge sorts it.
 template <int KL, int NB>
 __device__ __forceinline__ void merge_top(float (&V)[KL], const float (&B)[NB]) {
-  if (NB >= KL) {
+  if constexpr (NB >= KL) {
 #pragma unroll
     for (int i = 0; i < KL; ++i) V[i] = fmaxf(V[i], B[KL - 1 - i]);
   } else {
@@ -105,25 +105,6 @@ struct MergePairs {
   }
 };
 
-// Append (v, col) at a log's end when v > thr, without a branch: the two
-// stores are predicated, and the shared-memory addresses of the next free
-// slot (va for the score, ca for the column) advance by one slot row (VSTEP
-// and CSTEP bytes) when the entry is taken.
-template <int VSTEP, int CSTEP>
-__device__ __forceinline__ void log_append(uint32_t& va, uint32_t& ca, float v, float thr,
-                                           unsigned short col) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.gt.f32 p, %2, %3;\n\t"
-      "@p st.shared.f32 [%0], %2;\n\t"
-      "@p st.shared.u16 [%1], %4;\n\t"
-      "@p add.u32 %0, %0, %5;\n\t"
-      "@p add.u32 %1, %1, %6;\n\t}"
-      : "+r"(va), "+r"(ca)
-      : "f"(v), "f"(thr), "h"(col), "n"(VSTEP), "n"(CSTEP)
-      : "memory");
-}
-
 // Append the 8-byte entry (v, col) at a log's end when v > thr, without a
 // branch: one predicated store, and the shared-memory address of the next
 // free slot advances by STEP bytes when the entry is taken.
@@ -139,23 +120,38 @@ __device__ __forceinline__ void log_push(uint32_t& a, float v, float thr, uint32
       : "memory");
 }
 
-// Count v > thr in `count`, and append (v, col) like log_append while the
-// score address is below va_end.
-template <int VSTEP, int CSTEP>
-__device__ __forceinline__ void log_append_bounded(uint32_t& va, uint32_t& ca, uint32_t& count,
-                                                   uint32_t va_end, float v, float thr,
-                                                   unsigned short col) {
+// Append the score v at a stage's end when v > thr (predicated store; the
+// address advances by STEP bytes when the score is taken).
+template <int STEP>
+__device__ __forceinline__ void stage_push(uint32_t& a, float v, float thr) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "setp.gt.f32 p, %3, %4;\n\t"
-      "@p add.u32 %2, %2, 1;\n\t"
-      "setp.lt.and.u32 p, %0, %8, p;\n\t"
-      "@p st.shared.f32 [%0], %3;\n\t"
-      "@p st.shared.u16 [%1], %5;\n\t"
-      "@p add.u32 %0, %0, %6;\n\t"
-      "@p add.u32 %1, %1, %7;\n\t}"
-      : "+r"(va), "+r"(ca), "+r"(count)
-      : "f"(v), "f"(thr), "h"(col), "n"(VSTEP), "n"(CSTEP), "r"(va_end)
+      "setp.gt.f32 p, %1, %2;\n\t"
+      "@p st.shared.f32 [%0], %1;\n\t"
+      "@p add.u32 %0, %0, %3;\n\t}"
+      : "+r"(a)
+      : "f"(v), "f"(thr), "n"(STEP)
+      : "memory");
+}
+
+// Count v > thr in `count`; while the score address is below va_end, also
+// store v at the score address and the 32-bit code OFF bytes after it
+// (predicated stores, no branch), and advance the address by STEP.  Both
+// outputs are written after every input has been read, so the compiler may
+// place an input in an output's register.
+template <int STEP, int OFF>
+__device__ __forceinline__ void surv_push(uint32_t& va, uint32_t& count, uint32_t va_end, float v,
+                                          float thr, uint32_t code) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.gt.f32 p, %2, %3;\n\t"
+      "setp.lt.and.u32 q, %0, %5, p;\n\t"
+      "@q st.shared.f32 [%0], %2;\n\t"
+      "@q st.shared.b32 [%0+%7], %4;\n\t"
+      "@q add.u32 %0, %0, %6;\n\t"
+      "@p add.u32 %1, %1, 1;\n\t}"
+      : "+r"(va), "+r"(count)
+      : "f"(v), "f"(thr), "r"(code), "r"(va_end), "n"(STEP), "n"(OFF)
       : "memory");
 }
 
