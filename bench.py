@@ -288,13 +288,15 @@ def run_ours(args, rank, world, local):
                      "achieved": achieved, "peak": pk_["hbm"], "unit": "GB/s",
                      "frac": achieved / pk_["hbm"], "traffic": traffic,
                      "peak_source": pk_["src"]},
-        "scoring_roofline": {"kernel": "lookup_tc_kernel (scoring + selection)",
+        "scoring_roofline": {"kernel": "select_tc_kernel + merge_kernel (a1-a5, one lookup call)",
                              "bound": "tensor", "achieved": tflops, "peak": pk_["bf16"],
                              "unit": "TFLOP/s", "frac": tflops / pk_["bf16"],
                              "peak_source": pk_["src"] + " bf16 burst"},
         "e2e": {"value": world * B * H / e2e_s, "unit": UNIT,
                 "h2d_bytes_per_step": B * H * d_q * esz, "d2h_bytes_per_step": B * d_v * 4},
-        "gpu_launches": 2 * args.steps,
+        # per step: select_tc_kernel, merge_kernel, the (usually empty) fallback
+        # kernel and gather_kernel (fp32 inputs: lookup_simt_kernel and gather_kernel)
+        "gpu_launches": (4 if bf16 else 2) * args.steps,
         "clocks": clk.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

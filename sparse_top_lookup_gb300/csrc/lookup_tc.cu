@@ -244,9 +244,11 @@ struct RowLog {
   __device__ __forceinline__ uint32_t addr(int s) const { return smem_u32(e + s * BM + row); }
 };
 
-// Fold the values of log entries [b0, b0 + NB) (those below len) into V.
+// Fold the values of log entries [b0, b0 + NB) (those below len) into V;
+// when V holds nothing yet (first fold of a half), the sorted block is V.
 template <int KL, int NB>
-__device__ __forceinline__ void fold_block(const RowLog& L, int b0, int len, float (&V)[KL]) {
+__device__ __forceinline__ void fold_block(const RowLog& L, int b0, int len, float (&V)[KL],
+                                           bool v_empty) {
   float Bv[NB];
 #pragma unroll
   for (int j = 0; j < NB; ++j) {
@@ -255,7 +257,12 @@ __device__ __forceinline__ void fold_block(const RowLog& L, int b0, int len, flo
     Bv[j] = (b0 + j < len) ? x : -INFINITY;
   }
   sort_desc<NB>(Bv);
-  merge_top<KL, NB>(V, Bv);
+  if (v_empty) {
+#pragma unroll
+    for (int i = 0; i < KL; ++i) V[i] = i < NB ? Bv[i] : -INFINITY;
+  } else {
+    merge_top<KL, NB>(V, Bv);
+  }
 }
 
 // Fold the log entries [nsorted, len) into V; then, if the log holds more
@@ -265,13 +272,14 @@ __device__ __forceinline__ void fold_block(const RowLog& L, int b0, int len, flo
 // -inf.
 template <int KL>
 __device__ __forceinline__ void compact_log(const RowLog& L, int& len, int& nsorted,
-                                            float (&V)[KL], float& thr) {
+                                            float (&V)[KL], float& thr, bool& v_empty) {
 #pragma unroll 1
   for (int b0 = nsorted; __any_sync(0xffffffffu, len > b0); b0 += 32) {
     if (__any_sync(0xffffffffu, len > b0 + 16))
-      fold_block<KL, 32>(L, b0, len, V);
+      fold_block<KL, 32>(L, b0, len, V, v_empty);
     else
-      fold_block<KL, 16>(L, b0, len, V);
+      fold_block<KL, 16>(L, b0, len, V, v_empty);
+    v_empty = false;
   }
   nsorted = len;
   if (len <= KL) return;  // at most KL entries: all of them stay
@@ -473,6 +481,7 @@ select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
       const int tile = u >> 1, half = u & 1;
       const int rt = tile / H, h = tile - rt * H;
       int nsorted = 0;
+      bool v_empty = true;    // warp-uniform: nothing folded into V yet
       float thr = -INFINITY;  // a score is logged when it is > thr
       float V[KL];            // sorted values of the log's KL best (entries < nsorted)
 #pragma unroll
@@ -534,14 +543,14 @@ select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
           for (int j = 0; j < 8; ++j) log_push<LOG_STEP>(va, v[j], thr, c0 + j);
           if (__any_sync(0xffffffffu, va > log_room)) {
             int len = (int)((va - log0) / LOG_STEP);
-            compact_log<KL>(L, len, nsorted, V, thr);
+            compact_log<KL>(L, len, nsorted, V, thr, v_empty);
             va = log0 + (uint32_t)len * LOG_STEP;
           }
 #pragma unroll
           for (int j = 8; j < 16; ++j) log_push<LOG_STEP>(va, v[j], thr, c0 + j);
           if (__any_sync(0xffffffffu, va > log_room)) {
             int len = (int)((va - log0) / LOG_STEP);
-            compact_log<KL>(L, len, nsorted, V, thr);
+            compact_log<KL>(L, len, nsorted, V, thr, v_empty);
             va = log0 + (uint32_t)len * LOG_STEP;
           }
         }
@@ -554,7 +563,7 @@ select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
       if (!ok) break;
       // everything folded and the log cut to KL entries
       int len = (int)((va - log0) / LOG_STEP);
-      compact_log<KL>(L, len, nsorted, V, thr);
+      compact_log<KL>(L, len, nsorted, V, thr, v_empty);
       const int b = rt * BM + row;
       // the half's list by (score desc, subkey asc) into log slots [KL, 2KL),
       // then to global memory; a list with fewer than `need` entries (the

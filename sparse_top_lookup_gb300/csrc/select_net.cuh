@@ -7,27 +7,46 @@
 
 namespace pkm {
 
-// Bitonic sort of N values, descending (compile-time network).
+// Batcher's odd-even merge sort network on N (a power of two) inputs, as a
+// compile-time list of compare-exchanges (hi, lo): 19, 63 and 191 of them
+// for N = 8, 16 and 32, against 24, 80 and 240 for the bitonic sorter.
+template <int N>
+struct OddEvenMergeNet {
+  template <typename F>
+  static constexpr void visit(F f) {
+    for (int p = 1; p < N; p <<= 1)
+      for (int k = p; k >= 1; k >>= 1)
+        for (int j = k % p; j + k < N; j += 2 * k)
+          for (int i = 0; i < k && i < N - j - k; ++i)
+            if ((i + j) / (2 * p) == (i + j + k) / (2 * p)) f(i + j, i + j + k);
+  }
+  static constexpr int count() {
+    int c = 0;
+    visit([&c](int, int) { ++c; });
+    return c;
+  }
+  static constexpr int kCount = count();
+  int hi[kCount], lo[kCount];
+  constexpr OddEvenMergeNet() : hi(), lo() {
+    int c = 0;
+    visit([this, &c](int a, int b) {
+      hi[c] = a;
+      lo[c] = b;
+      ++c;
+    });
+  }
+};
+
+// Sort of N values, descending, through the odd-even merge network.
 template <int N>
 __device__ __forceinline__ void sort_desc(float (&a)[N]) {
+  constexpr OddEvenMergeNet<N> net{};
 #pragma unroll
-  for (int size = 2; size <= N; size <<= 1)
-#pragma unroll
-    for (int stride = size >> 1; stride > 0; stride >>= 1)
-#pragma unroll
-      for (int i = 0; i < N; ++i) {
-        const int j = i ^ stride;
-        if (j > i) {
-          const float hi = fmaxf(a[i], a[j]), lo = fminf(a[i], a[j]);
-          if ((i & size) == 0) {
-            a[i] = hi;
-            a[j] = lo;
-          } else {
-            a[i] = lo;
-            a[j] = hi;
-          }
-        }
-      }
+  for (int c = 0; c < net.kCount; ++c) {
+    const float x = a[net.hi[c]], y = a[net.lo[c]];
+    a[net.hi[c]] = fmaxf(x, y);
+    a[net.lo[c]] = fminf(x, y);
+  }
 }
 
 // V (descending, KL) <- the KL largest of V and B (descending, NB).  The
