@@ -44,8 +44,14 @@ def lib():
         L.oracle_forward.argtypes = [vp, i32, vp, i32, vp, i32, i32, i32, i32, i32, i32, i32, vp,
                                      vp, vp, i32]
         L.oracle_brute_topk.argtypes = [vp, i32, vp, i32, i32, i32, i32, i32, i32, vp, vp, i32]
+        L.oracle_quantize_fp8.argtypes = [vp, i32, i64, i32, vp, vp, i32]
+        L.oracle_gather_fp8.argtypes = [vp, vp, i64, i32, i32, i32, i32, vp, vp, vp, i32]
+        L.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+        L.oracle_e4m3_value.restype = ctypes.c_double
+        L.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+        L.oracle_e4m3_encode.restype = ctypes.c_uint8
         for f in (L.oracle_lookup, L.oracle_gather, L.oracle_forward, L.oracle_brute_topk,
-                  L.oracle_num_threads):
+                  L.oracle_num_threads, L.oracle_quantize_fp8, L.oracle_gather_fp8):
             f.restype = i32
         _lib = L
     return _lib
@@ -129,3 +135,40 @@ def brute_topk(q, subkeys, B, H, d_q, n_keys, k, nthreads=0):
     if rc != 0:
         raise ValueError("oracle_brute_topk rejected the shape")
     return idx, score
+
+
+def e4m3_value(code):
+    """The value of one fp8 e4m3 code (format definition)."""
+    return lib().oracle_e4m3_value(int(code))
+
+
+def e4m3_encode(x):
+    """The e4m3 code nearest to the float32 x (ties to even, saturated)."""
+    return int(lib().oracle_e4m3_encode(float(np.float32(x))))
+
+
+def quantize_fp8(values, N, d_v, nthreads=0):
+    """Per-row fp8 e4m3 quantisation.  Returns (codes uint8 [N, d_v], scales float32 [N])."""
+    values = _c(values)
+    codes = np.empty((N, d_v), np.uint8)
+    scales = np.empty(N, np.float32)
+    rc = lib().oracle_quantize_fp8(_p(values), _dt(values), N, d_v, _p(codes), _p(scales),
+                                   nthreads)
+    if rc != 0:
+        raise ValueError("oracle_quantize_fp8: bad shape")
+    return codes, scales
+
+
+def gather_fp8(codes, scales, N, d_v, idx, w, nthreads=0):
+    """out[b] = sum_{h,j} w[b,h,j] * scale[r] * value(codes[r]) in double, r = idx[b,h,j]."""
+    codes = np.ascontiguousarray(codes, np.uint8)
+    scales = np.ascontiguousarray(scales, np.float32)
+    idx = np.ascontiguousarray(idx, np.int64)
+    w = np.ascontiguousarray(w, np.float64)
+    B, H, k = idx.shape
+    out = np.empty((B, d_v), np.float64)
+    rc = lib().oracle_gather_fp8(_p(codes), _p(scales), N, d_v, B, H, k, _p(idx), _p(w), _p(out),
+                                 nthreads)
+    if rc != 0:
+        raise ValueError("oracle_gather_fp8: bad shape or index out of range")
+    return out

@@ -21,6 +21,17 @@
 //   softmax temperature; several heads each score their own subkeys with their
 //   own query slice, share one value table, and their reads are summed.
 //
+// Low-precision value table (the note after the code listing calls the
+// value table "a good candidate for keeping in a lower precision"): rows of
+// fp8 e4m3 codes with one fp32 scale per row.  e4m3 as defined by the OCP 8-bit
+// floating point format: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa
+// bits; exponent field 0 is subnormal (2^-6 * m/8); the all-ones pattern
+// S.1111.111 is NaN and there are no infinities (largest finite 448).  The
+// quantiser (a reading: the page fixes no recipe) takes per row
+// scale = max(amax / 448, FLT_MIN) in fp32, amax = the row's largest |x|, and
+// code = the e4m3 value nearest to x / scale (fp32 division), ties to the even
+// mantissa, saturated to +-448.  The fp8 read dequantises exactly in double.
+//
 // Arithmetic: inputs are widened exactly to double (bf16 and fp32 are both
 // subsets of double); every dot product is one sequential loop in double;
 // the softmax uses std::exp after subtracting the largest selected score.
@@ -30,6 +41,7 @@
 // n_keys^2 keys, closed forms, hand-worked cases); none is "parity unpinned".
 
 #include <algorithm>
+#include <cfloat>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -221,6 +233,93 @@ int oracle_forward(const void* q, int qdt, const void* subkeys, int cdt, const v
                          nullptr, nullptr, nthreads);
   if (rc) return rc;
   return oracle_gather(values, vdt, (int64_t)n * n, d_v, B, H, k, idx, w, out, nthreads);
+}
+
+// ---------------------------------------------------------- fp8 value table
+
+// The value of an e4m3 code, from the format's definition.
+double oracle_e4m3_value(uint8_t code) {
+  const int s = code >> 7, e = (code >> 3) & 0xF, m = code & 7;
+  if (e == 15 && m == 7) return std::nan("");
+  const double mag = e == 0 ? std::ldexp(m / 8.0, -6) : std::ldexp(1.0 + m / 8.0, e - 7);
+  return s ? -mag : mag;
+}
+
+// The e4m3 code nearest to x (ties to the even mantissa), saturated to the
+// largest finite magnitude; NaN -> 0x7F.  Binary search over the 127
+// non-negative finite codes, whose values increase with the code.
+uint8_t oracle_e4m3_encode(float x) {
+  if (std::isnan(x)) return 0x7F;
+  const uint8_t sign = std::signbit(x) ? 0x80 : 0x00;
+  const double a = std::fabs((double)x);
+  if (a >= 448.0) return sign | 0x7E;
+  int lo = 0, hi = 0x7E;  // value(lo) <= a < value(hi) after the search
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) / 2;
+    if (oracle_e4m3_value((uint8_t)mid) <= a) lo = mid; else hi = mid;
+  }
+  if (oracle_e4m3_value((uint8_t)hi) <= a) lo = hi;  // only when a == 448 exactly (handled above)
+  const double vlo = oracle_e4m3_value((uint8_t)lo);
+  if (vlo == a || lo == 0x7E) return sign | (uint8_t)lo;
+  const double vhi = oracle_e4m3_value((uint8_t)(lo + 1));
+  const double dlo = a - vlo, dhi = vhi - a;
+  int c = lo;
+  if (dhi < dlo || (dhi == dlo && ((lo + 1) & 1) == 0)) c = lo + 1;
+  return sign | (uint8_t)c;
+}
+
+// Per-row quantisation of values [N, d_v] (fp32 or bf16 bits) into e4m3
+// codes [N, d_v] and fp32 scales [N] (recipe in the header comment).
+int oracle_quantize_fp8(const void* values, int vdt, int64_t N, int d_v, uint8_t* codes,
+                        float* scales, int nthreads) {
+  if (N < 1 || d_v < 1) return -1;
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(static)
+#endif
+  for (int64_t r = 0; r < N; ++r) {
+    float amax = 0.0f;
+    for (int t = 0; t < d_v; ++t) {
+      const float x = (float)widen(values, vdt, r * d_v + t);  // exact: every input is a float
+      amax = std::max(amax, std::fabs(x));
+    }
+    float scale = amax / 448.0f;
+    if (!(scale >= FLT_MIN)) scale = FLT_MIN;
+    scales[r] = scale;
+    for (int t = 0; t < d_v; ++t) {
+      const float x = (float)widen(values, vdt, r * d_v + t);
+      codes[r * d_v + t] = oracle_e4m3_encode(x / scale);
+    }
+  }
+  return 0;
+}
+
+// Value read from the fp8 table: out[b, :] = sum_h sum_j w[b,h,j] * scale[r] *
+// value(code[r, :]) with r = idx[b,h,j], in double (each product is exact).
+int oracle_gather_fp8(const uint8_t* codes, const float* scales, int64_t N, int d_v, int B, int H,
+                      int k, const int64_t* idx, const double* w, double* out, int nthreads) {
+  if (B < 0 || H < 1 || k < 1 || d_v < 1 || N < 1) return -1;
+  int bad = 0;
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(static) reduction(| : bad)
+#endif
+  for (int64_t b = 0; b < B; ++b) {
+    double* o = out + b * d_v;
+    for (int t = 0; t < d_v; ++t) o[t] = 0.0;
+    for (int h = 0; h < H; ++h)
+      for (int j = 0; j < k; ++j) {
+        const int64_t e = (b * H + h) * k + j;
+        const int64_t r = idx[e];
+        if (r < 0 || r >= N) {
+          bad = 1;
+          continue;
+        }
+        const double ws = w[e] * (double)scales[r];
+        for (int t = 0; t < d_v; ++t) o[t] += ws * oracle_e4m3_value(codes[r * d_v + t]);
+      }
+  }
+  return bad ? -1 : 0;
 }
 
 // Brute force over every full key: score(a, b') is ONE d_q-long dot product

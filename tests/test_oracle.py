@@ -259,3 +259,126 @@ def test_rejects_bad_shapes():
         oracle.lookup(q, C, 1, 1, 4, 3, 4)  # k > n_keys
     with pytest.raises(ValueError):
         oracle.lookup(q, C, 1, 1, 3, 3, 1)  # odd d_q
+
+
+# ------------------------------------------------------------------ fp8 table
+#
+# Product-Key Memory, note after the code listing: the value table is "a good
+# candidate for keeping in a lower precision".  The fp8 e4m3 format (OCP 8-bit
+# floating point: bias 7, 3 mantissa bits, subnormals, S.1111.111 = NaN, no
+# infinities) is pinned against torch's float8_e4m3fn and against brute force
+# over its finite values; the quantiser and the fp8 read against closed forms.
+
+def _finite_e4m3():
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], np.uint8)
+    return codes, np.array([oracle.e4m3_value(c) for c in codes])
+
+
+def test_e4m3_values_match_torch_for_every_code():
+    torch = pytest.importorskip("torch")
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+    mine = np.array([oracle.e4m3_value(c) for c in codes])
+    assert (np.isnan(ref) == np.isnan(mine)).all()
+    fin = ~np.isnan(ref)
+    assert (ref[fin] == mine[fin]).all()
+    # a few values from the definition itself
+    assert oracle.e4m3_value(0x01) == 2.0 ** -9 and oracle.e4m3_value(0x08) == 2.0 ** -6
+    assert oracle.e4m3_value(0x38) == 1.0 and oracle.e4m3_value(0x7E) == 448.0
+    assert oracle.e4m3_value(0xFE) == -448.0
+
+
+def test_e4m3_encode_is_nearest_with_ties_to_even():
+    torch = pytest.importorskip("torch")
+    codes, vals = _finite_e4m3()
+    rng = np.random.default_rng(5)
+    x = (rng.standard_normal(4000) * rng.choice([1e-3, 0.05, 1.0, 40.0, 300.0], 4000))
+    x = x.astype(np.float32)
+    # exact midpoints between neighbours, both signs
+    pos = np.sort(vals[vals > 0])
+    mids = ((pos[:-1] + pos[1:]) / 2).astype(np.float32)
+    x = np.concatenate([x, mids, -mids, np.float32([0.0, -0.0, 2.0 ** -10, 447.0])])
+    x = x[np.abs(x) < 448]
+    got = np.array([oracle.e4m3_encode(v) for v in x], np.uint8)
+    # brute force: nearest finite value, ties to the even code (even mantissa)
+    for v, g in zip(x[:1500], got[:1500]):
+        d = np.abs(vals - float(v))
+        best = d.min()
+        cand = [c for c, dd in zip(codes, d) if dd == best]
+        same_sign = [c for c in cand if (c >> 7) == (1 if np.signbit(v) else 0)]
+        cand = same_sign or cand
+        want = [c for c in cand if (c & 1) == 0] if len(cand) > 1 else cand
+        assert g == want[0], (v, g, cand)
+    # and torch's round-to-nearest-even cast agrees on every in-range value
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert (got == ref).all()
+
+
+def test_e4m3_encode_saturates():
+    for v in (448.0, 460.0, 464.0, 470.0, 1e6, float("inf")):
+        assert oracle.e4m3_encode(v) == 0x7E
+        assert oracle.e4m3_encode(-v) == 0xFE
+    assert oracle.e4m3_encode(float("nan")) == 0x7F
+
+
+def test_quantize_fp8_scales_and_error_bound():
+    rng = np.random.default_rng(6)
+    N, d_v = 300, 48
+    V = (rng.standard_normal((N, d_v)) * rng.choice([1e-30, 1e-4, 1.0, 1e4], (N, 1)))
+    V = V.astype(np.float32)
+    V[7] = 0.0                      # an all-zero row
+    V[8, :] = 0.0
+    V[8, 3] = -2.5                  # a single non-zero element
+    codes, scales = oracle.quantize_fp8(V, N, d_v)
+    amax = np.abs(V).max(axis=1)
+    want_scale = np.maximum(amax / np.float32(448.0), np.finfo(np.float32).tiny)
+    assert (scales == want_scale.astype(np.float32)).all()
+    dq = np.vectorize(oracle.e4m3_value)(codes) * scales[:, None].astype(np.float64)
+    # e4m3: relative spacing 2^-3 for normals -> half a step = 2^-4 of the value;
+    # below 2^-6 the step is 2^-9 (absolute, in units of the scale)
+    bound = np.maximum(np.abs(V) * 2.0 ** -4, 2.0 ** -10 * scales[:, None])
+    assert (np.abs(dq - V) <= bound * (1 + 1e-12)).all()
+    assert (codes[7] == 0).all() and (dq[7] == 0).all()
+    # the row's only value maps to -448; the scale 2.5 / 448 is rounded to fp32
+    assert codes[8, 3] == 0xFE and abs(dq[8, 3] + 2.5) <= 2.5 * 2.0 ** -24
+    # every non-zero row's largest magnitude lands on +-448
+    for r in range(N):
+        if amax[r] > 0:
+            c = codes[r, np.argmax(np.abs(V[r]))]
+            assert c & 0x7F == 0x7E
+
+
+def test_quantize_fp8_bf16_input_matches_fp32_input():
+    rng = np.random.default_rng(7)
+    V = synth.normal(3, 3, 64 * 32, 0.5, dtype="bf16").reshape(64, 32)
+    V32 = (V.astype(np.uint32) << 16).view(np.float32)
+    a = oracle.quantize_fp8(V, 64, 32)
+    b = oracle.quantize_fp8(V32, 64, 32)
+    assert (a[0] == b[0]).all() and (a[1] == b[1]).all()
+
+
+def test_gather_fp8_closed_forms():
+    rng = np.random.default_rng(8)
+    B, H, k, d_v, N = 5, 3, 4, 32, 96
+    idx = rng.integers(0, N, (B, H, k)).astype(np.int64)
+    w = rng.random((B, H, k))
+    w /= w.sum(-1, keepdims=True)
+    # every code 1.0 with scale 1 -> out = H everywhere
+    out = oracle.gather_fp8(np.full((N, d_v), 0x38, np.uint8), np.ones(N, np.float32), N, d_v,
+                            idx, w)
+    np.testing.assert_allclose(out, H, rtol=0, atol=1e-12)
+    # one-hot rows: row r holds 1.0 at column r mod d_v, scaled by s_r
+    codes = np.zeros((N, d_v), np.uint8)
+    codes[np.arange(N), np.arange(N) % d_v] = 0x38
+    s = (1.0 + np.arange(N) / 8).astype(np.float32)
+    out = oracle.gather_fp8(codes, s, N, d_v, idx, w)
+    want = np.zeros((B, d_v))
+    for b in range(B):
+        for h in range(H):
+            for j in range(k):
+                want[b, idx[b, h, j] % d_v] += w[b, h, j] * float(s[idx[b, h, j]])
+    np.testing.assert_allclose(out, want, rtol=1e-14, atol=0)
+    with pytest.raises(ValueError):
+        bad = idx.copy()
+        bad[0, 0, 0] = N
+        oracle.gather_fp8(codes, s, N, d_v, bad, w)
