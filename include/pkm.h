@@ -24,11 +24,20 @@
  * Layouts (all row-major, contiguous, device memory unless stated):
  *   q        [B, H, d_q]            q_dtype
  *   subkeys  [H, 2, n_keys, d_q/2]  key_dtype   (must equal q_dtype)
- *   values   [n_keys^2, d_v]        value_dtype
+ *   values   [n_keys^2, d_v]        value_dtype (PKM_FP8_E4M3: see below)
  *   out      [B, d_v]               fp32, overwritten
  *   idx      [B, H, k]              int64 flat row indices
  *   w        [B, H, k]              fp32 softmax weights aligned with idx
  * bf16 arguments are raw IEEE bfloat16 bit patterns (uint16).
+ *
+ * Low-precision value table (Product-Key Memory, note after the code listing:
+ * the value table is "a good candidate for keeping in a lower precision"):
+ * with value_dtype = PKM_FP8_E4M3, `values` is one buffer holding the
+ * N = n_keys^2 rows of d_v fp8 e4m3 codes (N * d_v bytes, row-major) followed
+ * directly by N fp32 row scales; row r reads as V[r, c] = e4m3(code[r, c]) *
+ * scale[r].  e4m3 is the OCP 8-bit floating-point format (bias 7, 3 mantissa
+ * bits, subnormals, no infinities, largest finite 448).
+ * pkm_quantize_values_fp8 writes such a buffer from an fp32 or bf16 table.
  *
  * Arithmetic: bf16 queries and subkeys are scored on the tensor cores with
  * fp32 accumulation; fp32 queries and subkeys are scored with fp32 FMA on the
@@ -59,10 +68,10 @@
 extern "C" {
 #endif
 
-#define PKM_ABI_VERSION 1
+#define PKM_ABI_VERSION 2
 
-/* element types */
-enum { PKM_F32 = 0, PKM_BF16 = 1 };
+/* element types (PKM_FP8_E4M3: value tables only) */
+enum { PKM_F32 = 0, PKM_BF16 = 1, PKM_FP8_E4M3 = 2 };
 
 /* return codes */
 enum {
@@ -99,8 +108,8 @@ typedef struct pkm_handle *pkm_t;
 /*
  * Fixed shape of a handle.  d_q: query width per head (even; a multiple of 16
  * for bf16).  d_v: value row width (d_v * element size a multiple of 16
- * bytes).  max_*: the largest B, H, n_keys and k any call will pass (sizes
- * the scratch).  host_staging: nonzero to also allocate device staging for
+ * bytes; a multiple of 16 for PKM_FP8_E4M3).  max_*: the largest B, H,
+ * n_keys and k any call will pass (sizes the scratch).  host_staging: nonzero to also allocate device staging for
  * pkm_forward_host (max_B queries and outputs).
  */
 typedef struct {
@@ -203,6 +212,20 @@ int pkm_abi_version(void);
 #define PKM_STATIC_MAX_PAIRS (1 << 16)
 int pkm_lookup_static(const void *q, const void *subkeys, int B, int H, int d_q, int n_keys, int k,
                       int64_t *idx, float *w, int *status, void *stream);
+
+/*
+ * Quantise a value table to the PKM_FP8_E4M3 layout above.  values: [N, d_v]
+ * of value_dtype (PKM_F32 or PKM_BF16), device memory.  out: device buffer of
+ * N * d_v + 4 * N bytes, 16-byte aligned, overwritten (codes, then scales).
+ * Per row r, with amax = max_c |V[r, c]| (a recipe of this library; the page
+ * fixes none): scale[r] = max(amax / 448, FLT_MIN) in fp32, and code[r, c] =
+ * the e4m3 value nearest to V[r, c] / scale[r] (fp32 division, ties to the
+ * even mantissa, saturated to +-448).  Enqueued on `stream`.  Errors:
+ * PKM_ERR_INVALID (NULL pointer, N < 1, d_v < 1), PKM_ERR_UNSUPPORTED
+ * (value_dtype, d_v not a multiple of 16), PKM_ERR_ALIGN, PKM_ERR_CUDA.
+ */
+int pkm_quantize_values_fp8(const void *values, int value_dtype, int64_t N, int d_v, void *out,
+                            void *stream);
 
 #ifdef __cplusplus
 }

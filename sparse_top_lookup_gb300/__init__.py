@@ -13,7 +13,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libpkm.so")
 INCLUDE = os.path.join(os.path.dirname(_HERE), "include", "pkm.h")
 
-PKM_F32, PKM_BF16 = 0, 1
+PKM_F32, PKM_BF16, PKM_FP8_E4M3 = 0, 1, 2
 PKM_OK = 0
 PKM_ERR_INVALID, PKM_ERR_RANGE, PKM_ERR_UNSUPPORTED, PKM_ERR_ALIGN = -1, -2, -3, -4
 PKM_ERR_CUDA, PKM_ERR_NOMEM, PKM_ERR_TIMEOUT, PKM_ERR_BAD_INDEX = -5, -6, -7, -8
@@ -23,7 +23,8 @@ PKM_HOST_MAX_CHUNKS = 16
 
 EXPORTED = ["pkm_create", "pkm_destroy", "pkm_forward", "pkm_lookup", "pkm_gather",
             "pkm_forward_host", "pkm_get_status", "pkm_check_args", "pkm_strerror",
-            "pkm_abi_version", "pkm_set_option", "pkm_get_fallback_count", "pkm_lookup_static"]
+            "pkm_abi_version", "pkm_set_option", "pkm_get_fallback_count", "pkm_lookup_static",
+            "pkm_quantize_values_fp8"]
 PKM_STATIC_MAX_PAIRS = 1 << 16
 
 
@@ -72,9 +73,10 @@ def lib():
         L.pkm_set_option.argtypes = [vp, i32, ctypes.c_double]
         L.pkm_lookup_static.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp]
         L.pkm_get_fallback_count.argtypes = [vp, vp, ctypes.POINTER(i32)]
+        L.pkm_quantize_values_fp8.argtypes = [vp, i32, ctypes.c_int64, i32, vp, vp]
         for f in ("pkm_create", "pkm_forward", "pkm_lookup", "pkm_gather", "pkm_forward_host",
                   "pkm_get_status", "pkm_check_args", "pkm_abi_version", "pkm_set_option",
-                  "pkm_get_fallback_count", "pkm_lookup_static"):
+                  "pkm_get_fallback_count", "pkm_lookup_static", "pkm_quantize_values_fp8"):
             getattr(L, f).restype = i32
         _lib = L
     return _lib
@@ -172,6 +174,17 @@ def pkm_lookup_static(q, subkeys, B, H, d_q, n_keys, k, idx, w, status=None, str
     """The bf16 lookup without a handle or any device allocation (see include/pkm.h)."""
     return lib().pkm_lookup_static(_addr(q), _addr(subkeys), B, H, d_q, n_keys, k, _addr(idx),
                                    _addr(w), _addr(status), _stream(stream))
+
+
+def pkm_quantize_values_fp8(values, value_dtype, N, d_v, out, stream=None):
+    """Write the fp8 e4m3 table (N*d_v codes, then N fp32 scales) of an fp32/bf16 table."""
+    return lib().pkm_quantize_values_fp8(_addr(values), value_dtype, N, d_v, _addr(out),
+                                         _stream(stream))
+
+
+def fp8_table_bytes(N, d_v):
+    """Size of the PKM_FP8_E4M3 value buffer: codes then row scales."""
+    return N * d_v + 4 * N
 
 
 def pkm_get_status(h, stream=None):

@@ -15,6 +15,14 @@
 // every G-th row and are reduced through shared memory at the end.  Loads are
 // 16-byte non-coherent loads that bypass L1 (each row is used once per bag),
 // unrolled eight rows deep so a thread keeps 128 bytes in flight.
+//
+// fp8 table (the note after the code listing: the value table is "a good
+// candidate for keeping in a lower precision"): rows of e4m3 codes, one fp32
+// scale per row stored after the codes.  A 16-byte vector then holds 16
+// elements; the row's scale is folded into its staged weight, the codes are
+// widened exactly (e4m3 -> f16 -> f32) and accumulated in fp32.
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <stdint.h>
 
 #include "pkm_internal.cuh"
@@ -32,12 +40,32 @@ __device__ __forceinline__ uint4 ldg_stream(const uint4* p) {
   return r;
 }
 
-// Accumulate one 16-byte vector: 8 bf16 or 4 fp32 elements.
-template <bool kBf16>
+// Accumulate one 16-byte vector: 4 fp32, 8 bf16 or 16 fp8 e4m3 elements.
+template <int VT>
 struct VecAcc;
 
 template <>
-struct VecAcc<true> {
+struct VecAcc<PKM_FP8_E4M3> {
+  static constexpr int kElems = 16;
+  __device__ __forceinline__ static void fma(float (&acc)[16], float wt, const uint4& v) {
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+      for (int hlf = 0; hlf < 2; ++hlf) {
+        // two codes -> two exact halves -> two floats (byte order = element order)
+        const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(
+            (__nv_fp8x2_storage_t)((u[i] >> (16 * hlf)) & 0xffffu), __NV_E4M3);
+        const float2 f = __half22float2(__half2(hr));
+        acc[4 * i + 2 * hlf] = fmaf(wt, f.x, acc[4 * i + 2 * hlf]);
+        acc[4 * i + 2 * hlf + 1] = fmaf(wt, f.y, acc[4 * i + 2 * hlf + 1]);
+      }
+    }
+  }
+};
+
+template <>
+struct VecAcc<PKM_BF16> {
   static constexpr int kElems = 8;
   __device__ __forceinline__ static void fma(float (&acc)[8], float wt, const uint4& v) {
     const uint32_t u[4] = {v.x, v.y, v.z, v.w};
@@ -50,7 +78,7 @@ struct VecAcc<true> {
 };
 
 template <>
-struct VecAcc<false> {
+struct VecAcc<PKM_F32> {
   static constexpr int kElems = 4;
   __device__ __forceinline__ static void fma(float (&acc)[4], float wt, const uint4& v) {
     acc[0] = fmaf(wt, __uint_as_float(v.x), acc[0]);
@@ -63,12 +91,13 @@ struct VecAcc<false> {
 // grid: one CTA per bag.  block: vpr * groups threads.
 // dynamic smem: rows_per_bag * (4 + 4) bytes, plus blockDim * E * 4 when groups > 1
 // (kept small so these CTAs fit next to a running lookup kernel's CTA).
-template <bool kBf16>
-__global__ void gather_kernel(const uint4* __restrict__ values, int64_t N, int vpr, int groups,
-                              int rows_per_bag, const int64_t* __restrict__ idx,
-                              const float* __restrict__ w, float* __restrict__ out,
-                              int* __restrict__ status) {
-  constexpr int E = VecAcc<kBf16>::kElems;
+// scales: the fp8 table's row scales (null for fp32 / bf16 tables).
+template <int VT>
+__global__ void gather_kernel(const uint4* __restrict__ values, const float* __restrict__ scales,
+                              int64_t N, int vpr, int groups, int rows_per_bag,
+                              const int64_t* __restrict__ idx, const float* __restrict__ w,
+                              float* __restrict__ out, int* __restrict__ status) {
+  constexpr int E = VecAcc<VT>::kElems;
   extern __shared__ __align__(16) unsigned char smem[];
   int* s_row = reinterpret_cast<int*>(smem);
   float* s_w = reinterpret_cast<float*>(s_row + rows_per_bag);
@@ -88,6 +117,7 @@ __global__ void gather_kernel(const uint4* __restrict__ values, int64_t N, int v
       row = 0;
       wt = 0.0f;
     }
+    if (VT == PKM_FP8_E4M3) wt *= scales[row];
     s_row[r] = (int)row;
     s_w[r] = wt;
   }
@@ -108,11 +138,11 @@ __global__ void gather_kernel(const uint4* __restrict__ values, int64_t N, int v
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) x[u] = ldg_stream(vbase + s_row[r + u * groups] * stride);
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) VecAcc<kBf16>::fma(acc, s_w[r + u * groups], x[u]);
+    for (int u = 0; u < kUnroll; ++u) VecAcc<VT>::fma(acc, s_w[r + u * groups], x[u]);
   }
   for (; r < rows_per_bag; r += groups) {
     uint4 x = ldg_stream(vbase + s_row[r] * stride);
-    VecAcc<kBf16>::fma(acc, s_w[r], x);
+    VecAcc<VT>::fma(acc, s_w[r], x);
   }
 
   float* orow = out + bag * (int64_t)vpr * E;
@@ -137,42 +167,56 @@ __global__ void gather_kernel(const uint4* __restrict__ values, int64_t N, int v
   }
 }
 
+template <int VT>
+cudaError_t launch_gather_vt(const void* values, int64_t N, int d_v, int B, int rows_per_bag,
+                             const int64_t* idx, const float* w, float* out, int* status,
+                             cudaStream_t stream) {
+  constexpr int E = VecAcc<VT>::kElems;
+  const int vpr = d_v / E;  // 16-byte vectors per row
+  int groups = vpr >= 128 ? 1 : 128 / vpr;
+  if (groups > rows_per_bag) groups = rows_per_bag > 0 ? rows_per_bag : 1;
+  const int threads = vpr * groups;
+  const size_t staged = (size_t)rows_per_bag * 8;
+  const size_t red_off = (staged + 15) / 16 * 16;
+  const size_t smem = groups > 1 ? red_off + (size_t)threads * E * 4 : staged;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(gather_kernel<VT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  // The loads bypass L1, so the SM can keep its maximum shared-memory split;
+  // CTAs of this kernel then fit next to a running lookup kernel's CTA.
+  static bool carveout_set = false;
+  if (!carveout_set) {
+    cudaError_t e = cudaFuncSetAttribute(gather_kernel<VT>,
+                                         cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    carveout_set = true;
+  }
+  // an fp8 table's row scales follow its N * d_v code bytes
+  const float* scales =
+      VT == PKM_FP8_E4M3
+          ? reinterpret_cast<const float*>(static_cast<const unsigned char*>(values) + N * d_v)
+          : nullptr;
+  gather_kernel<VT><<<B, threads, smem, stream>>>(static_cast<const uint4*>(values), scales, N,
+                                                  vpr, groups, rows_per_bag, idx, w, out, status);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_gather(const void* values, int value_dtype, int64_t N, int d_v, int B,
                           int rows_per_bag, const int64_t* idx, const float* w, float* out,
                           int* status, cudaStream_t stream) {
   if (B == 0) return cudaSuccess;
-  const bool bf16 = value_dtype == PKM_BF16;
-  const int elem = bf16 ? 2 : 4;
-  const int vpr = d_v * elem / 16;
-  int groups = vpr >= 128 ? 1 : 128 / vpr;
-  if (groups > rows_per_bag) groups = rows_per_bag > 0 ? rows_per_bag : 1;
-  const int threads = vpr * groups;
-  const size_t staged = (size_t)rows_per_bag * 8;
-  const size_t red_off = (staged + 15) / 16 * 16;
-  const size_t smem = groups > 1 ? red_off + (size_t)threads * (bf16 ? 8 : 4) * 4 : staged;
-  const void* fn = bf16 ? (const void*)gather_kernel<true> : (const void*)gather_kernel<false>;
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-  }
-  // The loads bypass L1, so the SM can keep its maximum shared-memory split;
-  // CTAs of this kernel then fit next to a running lookup kernel's CTA.
-  static bool carveout_set[2] = {false, false};
-  if (!carveout_set[bf16]) {
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                         cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess) return e;
-    carveout_set[bf16] = true;
-  }
-  if (bf16)
-    gather_kernel<true><<<B, threads, smem, stream>>>(static_cast<const uint4*>(values), N, vpr,
-                                                      groups, rows_per_bag, idx, w, out, status);
-  else
-    gather_kernel<false><<<B, threads, smem, stream>>>(static_cast<const uint4*>(values), N, vpr,
-                                                       groups, rows_per_bag, idx, w, out, status);
-  return cudaGetLastError();
+  if (value_dtype == PKM_FP8_E4M3)
+    return launch_gather_vt<PKM_FP8_E4M3>(values, N, d_v, B, rows_per_bag, idx, w, out, status,
+                                          stream);
+  if (value_dtype == PKM_BF16)
+    return launch_gather_vt<PKM_BF16>(values, N, d_v, B, rows_per_bag, idx, w, out, status,
+                                      stream);
+  return launch_gather_vt<PKM_F32>(values, N, d_v, B, rows_per_bag, idx, w, out, status, stream);
 }
 
 }  // namespace pkm

@@ -31,7 +31,7 @@ struct pkm_handle {
 
 namespace {
 
-int elem_size(int dtype) { return dtype == PKM_BF16 ? 2 : 4; }
+int elem_size(int dtype) { return dtype == PKM_FP8_E4M3 ? 1 : dtype == PKM_BF16 ? 2 : 4; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -39,8 +39,10 @@ int check_config(const pkm_config* c) {
   if (!c) return PKM_ERR_INVALID;
   if (c->d_q < 2 || (c->d_q & 1) || c->d_v < 1) return PKM_ERR_INVALID;
   if (c->max_B < 0 || c->max_H < 1 || c->max_n_keys < 1 || c->max_k < 1) return PKM_ERR_INVALID;
-  for (int dt : {c->q_dtype, c->key_dtype, c->value_dtype})
+  for (int dt : {c->q_dtype, c->key_dtype})
     if (dt != PKM_F32 && dt != PKM_BF16) return PKM_ERR_UNSUPPORTED;
+  if (c->value_dtype != PKM_F32 && c->value_dtype != PKM_BF16 && c->value_dtype != PKM_FP8_E4M3)
+    return PKM_ERR_UNSUPPORTED;
   if (c->q_dtype != c->key_dtype) return PKM_ERR_UNSUPPORTED;
   if ((int64_t)c->d_v * elem_size(c->value_dtype) % 16) return PKM_ERR_UNSUPPORTED;
   if ((int64_t)c->d_v * elem_size(c->value_dtype) / 16 > pkm::kGatherMaxVecPerRow)

@@ -10,6 +10,10 @@ namespace pkm {
 
 // Device status word values are the PKM_ERR_* codes of pkm.h.
 
+// The fp8 value table: codes [N, d_v] then fp32 scales [N] in `out`.
+cudaError_t launch_quantize_fp8(const void* values, int value_dtype, int64_t N, int d_v, void* out,
+                                cudaStream_t stream);
+
 // Step a6 (value read).  values: [N, d_v] of value_dtype; idx/w: [B, H*k];
 // out: [B, d_v] fp32.  Returns a cudaError_t of the launch.
 cudaError_t launch_gather(const void* values, int value_dtype, int64_t N, int d_v, int B,

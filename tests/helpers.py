@@ -62,13 +62,17 @@ def compare_lookup(gidx, gw, ref, q=None, C=None, dtype=None, H=None, d_q=None, 
                 max_w_err=float(werr.max()) if werr.size else 0.0, w_ok=bool((werr <= TOL).all()))
 
 
-def compare_out(gout, values, N, d_v, gidx, ref_idx, ref_w, ref_out):
+def compare_out(gout, values, N, d_v, gidx, ref_idx, ref_w, ref_out, regather=None):
     """Output parity; queries whose selection was a near-tie swap are judged
-    against the fp64 read of the GPU's rows with the oracle's weights."""
+    against the fp64 read of the GPU's rows with the oracle's weights
+    (`regather(idx, w)` replaces the plain read, e.g. for an fp8 table)."""
     ref = ref_out.copy()
     swapped = ~(gidx == ref_idx).all(-1).all(-1)
     if swapped.any():
-        ref[swapped] = oracle.gather(values, N, d_v, gidx[swapped], ref_w[swapped])
+        if regather is None:
+            ref[swapped] = oracle.gather(values, N, d_v, gidx[swapped], ref_w[swapped])
+        else:
+            ref[swapped] = regather(gidx[swapped], ref_w[swapped])
     err = np.abs(gout.astype(np.float64) - ref) / (1 + np.abs(ref))
     return float(err.max()) if err.size else 0.0
 

@@ -34,7 +34,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_abi_version_and_strerror(L):
-    assert pk.pkm_abi_version() == 1
+    assert pk.pkm_abi_version() == 2
     for code in range(-10, 1):
         assert pk.pkm_strerror(code) != "unknown error code"
     assert pk.pkm_strerror(-100) == "unknown error code"
@@ -64,6 +64,11 @@ def test_check_args(L):
     assert pk.pkm_check_args(cfg(d_v=1001), 1, 1, 64, 1) == pk.PKM_ERR_UNSUPPORTED
     assert pk.pkm_check_args(cfg(max_n_keys=46341), 1, 1, 64, 1) == pk.PKM_ERR_UNSUPPORTED
     assert pk.pkm_check_args(cfg(key_dtype=pk.PKM_F32), 1, 1, 64, 1) == pk.PKM_ERR_UNSUPPORTED
+    # fp8 e4m3 is a value-table type only; its rows must be whole 16-byte vectors
+    assert pk.pkm_check_args(cfg(value_dtype=pk.PKM_FP8_E4M3), 1, 1, 64, 1) == pk.PKM_OK
+    assert pk.pkm_check_args(cfg(value_dtype=pk.PKM_FP8_E4M3, d_v=1000), 1, 1, 64, 1) \
+        == pk.PKM_ERR_UNSUPPORTED
+    assert pk.pkm_check_args(cfg(q_dtype=pk.PKM_FP8_E4M3), 1, 1, 64, 1) == pk.PKM_ERR_UNSUPPORTED
     c2 = cfg()
     c2.value_dtype = 7
     assert pk.pkm_check_args(c2, 1, 1, 64, 1) == pk.PKM_ERR_UNSUPPORTED
@@ -85,6 +90,17 @@ def test_null_handle_rejected_before_any_cuda_call(L):
     bad = cfg(d_q=3)
     assert L.pkm_create(ctypes.byref(h), ctypes.byref(bad)) == pk.PKM_ERR_INVALID
     assert h.value is None
+
+
+def test_fp8_quantiser_rejects_bad_arguments_before_any_cuda_call(L):
+    Q = L.pkm_quantize_values_fp8
+    assert Q(None, pk.PKM_BF16, 4, 16, 16, None) == pk.PKM_ERR_INVALID
+    assert Q(16, pk.PKM_BF16, 0, 16, 16, None) == pk.PKM_ERR_INVALID
+    assert Q(16, pk.PKM_BF16, 4, 0, 16, None) == pk.PKM_ERR_INVALID
+    assert Q(16, pk.PKM_FP8_E4M3, 4, 16, 16, None) == pk.PKM_ERR_UNSUPPORTED
+    assert Q(16, pk.PKM_F32, 4, 24, 16, None) == pk.PKM_ERR_UNSUPPORTED
+    assert Q(8, pk.PKM_F32, 4, 16, 16, None) == pk.PKM_ERR_ALIGN
+    assert pk.fp8_table_bytes(1 << 20, 1024) == (1 << 30) + (1 << 22)
 
 
 def test_product_path_refuses_without_library(monkeypatch, tmp_path):
