@@ -140,19 +140,32 @@ def workload(name, B=None):
     return c
 
 
+def is_fp8(c):
+    return c.get("value_format") == "fp8_e4m3"
+
+
 def cpu_inputs(c, sample, C=None, V=None):
-    """Inputs of the CPU oracle leg: the first `sample` queries, all tables."""
+    """Inputs of the CPU oracle leg: the first `sample` queries, all tables
+    (an fp8 table quantised by the oracle's own quantiser: codes, scales)."""
+    import oracle
     q = synth.queries(c, rows=sample, row_offset=0)
-    return q, (synth.subkeys(c) if C is None else C), (synth.values(c) if V is None else V)
+    V = synth.values(c) if V is None else V
+    if is_fp8(c):
+        V = oracle.quantize_fp8(V, c["n_keys"] ** 2, c["d_v"])
+    return q, (synth.subkeys(c) if C is None else C), V
 
 
 def cpu_oracle_time(c, inputs, sample, nthreads):
     """Wall time of the fp64 oracle forward on `sample` queries of workload c."""
     import oracle
     q, C, V = inputs
+    H, d_q, n, d_v, k = c["H"], c["d_q"], c["n_keys"], c["d_v"], c["k"]
     t0 = time.perf_counter()
-    oracle.forward(q, C, V, sample, c["H"], c["d_q"], c["n_keys"], c["d_v"], c["k"],
-                   nthreads=nthreads)
+    if is_fp8(c):
+        ref = oracle.lookup(q, C, sample, H, d_q, n, k, nthreads=nthreads)
+        oracle.gather_fp8(V[0], V[1], n * n, d_v, ref["idx"], ref["w"], nthreads=nthreads)
+    else:
+        oracle.forward(q, C, V, sample, H, d_q, n, d_v, k, nthreads=nthreads)
     return time.perf_counter() - t0
 
 
@@ -183,12 +196,22 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def value_row_bytes(c):
+    """Bytes of one value row as stored (an fp8 row carries its 4-byte scale)."""
+    if is_fp8(c):
+        return c["d_v"] + 4
+    return c["d_v"] * (2 if c["dtype"] == "bf16" else 4)
+
+
 def config_json(c, name):
+    inputs = "%s, seeded synthetic" % c["dtype"]
+    if is_fp8(c):
+        inputs = ("bf16 queries and subkeys, seeded synthetic; value table fp8 e4m3 codes with "
+                  "per-row fp32 scales, quantised on the GPU from the seeded bf16 table")
     return {"workload": name, "B": c["B"], "H": c["H"], "d_q": c["d_q"], "n_keys": c["n_keys"],
-            "N": c["n_keys"] ** 2, "d_v": c["d_v"], "k": c["k"],
-            "inputs": "%s, seeded synthetic" % c["dtype"],
+            "N": c["n_keys"] ** 2, "d_v": c["d_v"], "k": c["k"], "inputs": inputs,
             "l2": "flushed (512 MiB write) between timed steps; value table %.1f GiB"
-                  % (c["n_keys"] ** 2 * c["d_v"] * (2 if c["dtype"] == "bf16" else 4) / 2**30)}
+                  % (c["n_keys"] ** 2 * value_row_bytes(c) / 2**30)}
 
 
 def run_ours(args, rank, world, local):
@@ -210,11 +233,18 @@ def run_ours(args, rank, world, local):
 
     q_np, C_np, V_np = synth.queries(c), synth.subkeys(c), synth.values(c)
     dq, dC, dV = dev(q_np), dev(C_np), dev(V_np)
+    vdt = dt
+    if is_fp8(c):
+        # the table as stored for the fp8 read: codes then row scales
+        dV8 = torch.empty(pk.fp8_table_bytes(n * n, d_v), dtype=torch.uint8, device="cuda")
+        pk.check(pk.pkm_quantize_values_fp8(dV, pk.PKM_BF16, n * n, d_v, dV8), "quantize")
+        torch.cuda.synchronize()
+        dV, vdt = dV8, pk.PKM_FP8_E4M3
     out = torch.empty(B, d_v, device="cuda")
     idx = torch.empty(B, H, k, dtype=torch.int64, device="cuda")
     w = torch.empty(B, H, k, device="cuda")
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
-    cfg = pk.make_config(d_q, d_v, B, H, n, k, q_dtype=dt, host_staging=1)
+    cfg = pk.make_config(d_q, d_v, B, H, n, k, q_dtype=dt, value_dtype=vdt, host_staging=1)
     h = pk.pkm_create(cfg)
     stream = torch.cuda.current_stream()
 
@@ -271,7 +301,7 @@ def run_ours(args, rank, world, local):
     pk.pkm_destroy(h)
 
     pk_ = peaks()
-    gather_bytes = B * H * k * d_v * esz + B * H * k * 12 + B * d_v * 4
+    gather_bytes = B * H * k * value_row_bytes(c) + B * H * k * 12 + B * d_v * 4
     achieved = gather_bytes / (ms_gather * 1e-3) / 1e9
     flops = 2.0 * B * H * n * d_q
     tflops = flops / (ms_lookup * 1e-3) / 1e12

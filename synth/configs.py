@@ -31,6 +31,11 @@ CONFIGS = {
     "skew": dict(cfg_id=3, B=65536, H=8, d_q=1024, n_keys=1024, d_v=1024, k=32, dtype="bf16",
                  q_var=1.0, key_var=1.0 / 512, value_var=1.0 / 1024, q_kind="mixture",
                  mix_components=64, mix_zipf_s=1.1, mix_sd=0.1),
+    # the page workload's inputs (same seed), its value table kept as fp8 e4m3
+    # codes with per-row scales (quantised from the bf16 table).
+    "page_fp8": dict(cfg_id=2, B=16384, H=4, d_q=1024, n_keys=1024, d_v=1024, k=32,
+                     dtype="bf16", value_format="fp8_e4m3", q_var=1.0, key_var=1.0 / 512,
+                     value_var=1.0 / 1024, q_kind="normal"),
     # 16 GiB value table.
     "large": dict(cfg_id=4, B=32768, H=4, d_q=2048, n_keys=2048, d_v=2048, k=32, dtype="bf16",
                   q_var=1.0, key_var=1.0 / 1024, value_var=1.0 / 2048, q_kind="normal"),

@@ -24,14 +24,22 @@ def run_workload(name):
     c = synth.CONFIGS[name]
     B, H, d_q, n, d_v, k = (c[x] for x in ("B", "H", "d_q", "n_keys", "d_v", "k"))
     q, C, V = synth.queries(c), synth.subkeys(c), synth.values(c)
+    fp8 = c.get("value_format") == "fp8_e4m3"
+    if fp8:  # the oracle quantises the table; the GPU reads the oracle's codes
+        V = oracle.quantize_fp8(V, n * n, d_v)
 
     def dev(a):
         return torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16)
 
-    cfg = pk.make_config(d_q, d_v, B, H, n, k, q_dtype=pk.PKM_BF16)
+    cfg = pk.make_config(d_q, d_v, B, H, n, k, q_dtype=pk.PKM_BF16,
+                         value_dtype=pk.PKM_FP8_E4M3 if fp8 else pk.PKM_BF16)
     h = pk.pkm_create(cfg)
     try:
-        dq, dC, dV = dev(q), dev(C), dev(V)
+        if fp8:
+            dV = torch.from_numpy(np.concatenate([V[0].reshape(-1), V[1].view(np.uint8)])).cuda()
+        else:
+            dV = dev(V)
+        dq, dC = dev(q), dev(C)
         out = torch.empty(B, d_v, device="cuda")
         idx = torch.empty(B, H, k, dtype=torch.int64, device="cuda")
         w = torch.empty(B, H, k, device="cuda")
@@ -67,8 +75,15 @@ def check(name):
     rep = compare_lookup(idx[rows], w[rows], ref, qs, C, c["dtype"], H, d_q, n)
     assert rep["failures"] == 0, rep
     assert rep["w_ok"], rep
-    ref_out = oracle.gather(V, N, d_v, ref["idx"], ref["w"])
-    err = compare_out(out[rows], V, N, d_v, idx[rows], ref["idx"], ref["w"], ref_out)
+    if isinstance(V, tuple):  # fp8 table: (codes, scales)
+        def read(i, ww):
+            return oracle.gather_fp8(V[0], V[1], N, d_v, i, ww)
+        ref_out = read(ref["idx"], ref["w"])
+        err = compare_out(out[rows], None, N, d_v, idx[rows], ref["idx"], ref["w"], ref_out,
+                          regather=read)
+    else:
+        ref_out = oracle.gather(V, N, d_v, ref["idx"], ref["w"])
+        err = compare_out(out[rows], V, N, d_v, idx[rows], ref["idx"], ref["w"], ref_out)
     assert err <= TOL, err
     print("%s: sampled %d queries, %s, out err %.2e, fallback pairs %d of %d"
           % (name, len(rows), rep, err, fallback, B * H))
@@ -76,6 +91,10 @@ def check(name):
 
 def test_page_scale_full_batch():
     check("page")
+
+
+def test_page_scale_fp8_table_full_batch():
+    check("page_fp8")
 
 
 def test_skewed_usage_full_batch():
