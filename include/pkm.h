@@ -92,9 +92,10 @@ enum {
 /* options of pkm_set_option */
 enum {
   /* bf16 path: the per-row selection threshold is mean + z * spread of the
-     row's first-chunk scores.  Any finite z gives exact results (a low z costs
-     more log compactions, a high z sends rows to the CUDA-core fallback);
-     NaN restores the automatic choice. */
+     row's first 256 scores.  Any finite z gives exact results (a low z costs
+     more log compactions; a high z makes more rows miss their k-th score, and
+     their row tiles are selected again without the hint); NaN restores the
+     automatic choice. */
   PKM_OPT_HINT_Z = 1,
   /* pkm_forward_host: number of batch slices (1 .. PKM_HOST_MAX_CHUNKS,
      default 4) pipelined so the copy of slice i+1 in and of slice i-1 out
@@ -164,9 +165,10 @@ int pkm_forward_host(pkm_t h, const void *q_host, const void *subkeys, const voi
 /* Set a tuning option of a handle (PKM_OPT_*).  Affects later calls only. */
 int pkm_set_option(pkm_t h, int option, double value);
 
-/* Synchronise `stream` and report in *count how many (query, head) pairs the
-   last bf16 lookup on this handle recomputed on the CUDA cores because the
-   selection threshold hint was above their k-th score. */
+/* Synchronise `stream` and report in *count how many (query, head) pairs of
+   the last bf16 lookup on this handle had a per-half selection threshold hint
+   above their k-th score; their row tiles were scored and selected again
+   without the hint (exact), in the same call. */
 int pkm_get_fallback_count(pkm_t h, void *stream, int *count);
 
 /* Synchronise `stream`, return the device status word (PKM_OK or a device error

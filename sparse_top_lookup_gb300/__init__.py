@@ -163,7 +163,7 @@ def pkm_set_option(h, option, value):
 
 
 def pkm_get_fallback_count(h, stream=None):
-    """Pairs the last bf16 lookup recomputed on the CUDA cores (synchronises)."""
+    """Pairs of the last bf16 lookup whose threshold hint missed (re-selected; synchronises)."""
     c = ctypes.c_int()
     check(lib().pkm_get_fallback_count(h, _stream(stream), ctypes.byref(c)),
           "pkm_get_fallback_count")

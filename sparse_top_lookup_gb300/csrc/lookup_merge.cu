@@ -14,7 +14,9 @@
 // surviving pair's output slot is the number of larger sums and its softmax
 // weight follows from V.  Exact ties take a frontier walk that orders equal
 // sums by flat index.  A list marked failed (subkey 0xffff in its first
-// slot) sends the pair to the CUDA-core fallback list instead.
+// slot: the selection threshold hint was above the row's KL-th score) lists
+// its work unit for the retry pass, which selects that unit again without
+// the hint and then merges the unit's pairs in this kernel's retry mode.
 #include <math.h>
 #include <stdint.h>
 
@@ -40,11 +42,13 @@ struct MergeLayout {
   static constexpr int kBytes = kRegionA + 2 * KL * 2 * kThreads;  // + the lists' subkeys
 };
 
+// Pairs: first pass, pair = blockIdx.x * 128 + thread; retry pass, CTA c takes
+// listed unit c (if c < the listed count) and thread t its row tile's query t.
 template <int KL>
 __global__ void __launch_bounds__(kThreads)
-merge_kernel(const float* __restrict__ list_v, const unsigned short* __restrict__ list_c,
-             int pairs, int n, int k, int64_t* __restrict__ idx, float* __restrict__ w,
-             int* __restrict__ fb_count, int* __restrict__ fb_list) {
+merge_kernel(const float* __restrict__ list_v, const unsigned short* __restrict__ list_c, int B,
+             int H, int n, int k, int64_t* __restrict__ idx, float* __restrict__ w,
+             RetryScratch retry, bool retry_pass) {
   using Lay = MergeLayout<KL>;
   constexpr MergePairs<KL> P{};
   extern __shared__ __align__(16) unsigned char smem[];
@@ -53,10 +57,21 @@ merge_kernel(const float* __restrict__ list_v, const unsigned short* __restrict_
   uint32_t* sp = reinterpret_cast<uint32_t*>(sv + KL * kThreads);               // [KL][T]
   unsigned short* sc = reinterpret_cast<unsigned short*>(smem + Lay::kRegionA); // [2KL][T]
   const int t = threadIdx.x;
-  const int pair = blockIdx.x * kThreads + t;
+  int pair;
   // every lane stays to the end (warp votes below); lanes without a pair of
   // their own work on zeros and store nothing
-  bool valid = pair < pairs;
+  bool valid;
+  if (retry_pass) {
+    if ((int)blockIdx.x >= retry.counts[1]) return;  // the whole CTA: no unit listed here
+    const int tile = retry.unit_list[blockIdx.x] >> 1;
+    const int rt = tile / H, h = tile - (tile / H) * H;
+    const int b = rt * kThreads + t;  // row tiles hold 128 queries, one per thread
+    valid = b < B;
+    pair = valid ? b * H + h : 0;
+  } else {
+    pair = blockIdx.x * kThreads + t;
+    valid = pair < B * H;
+  }
 
   const float* v1 = list_v + (size_t)(valid ? pair : 0) * 2 * KL;
   const unsigned short* c1 = list_c + (size_t)(valid ? pair : 0) * 2 * KL;
@@ -81,8 +96,14 @@ merge_kernel(const float* __restrict__ list_v, const unsigned short* __restrict_
       }
     }
   }
-  if (valid && (sc[t] == 0xffffu || sc[KL * kThreads + t] == 0xffffu)) {
-    fb_list[atomicAdd(fb_count, 1)] = pair;
+  const bool bad1 = sc[t] == 0xffffu, bad2 = sc[KL * kThreads + t] == 0xffffu;
+  if (valid && (bad1 || bad2) && !retry_pass) {  // without the hint every list is complete
+    atomicAdd(&retry.counts[0], 1);
+    const int b = pair / H, h = pair - (pair / H) * H;
+    const int unit0 = ((b / kThreads) * H + h) << 1;
+    for (int hf = 0; hf < 2; ++hf)
+      if ((hf ? bad2 : bad1) && atomicExch(&retry.unit_flag[unit0 | hf], 1) == 0)
+        retry.unit_list[atomicAdd(&retry.counts[1], 1)] = unit0 | hf;
     valid = false;
   }
   if (!valid) {
@@ -217,9 +238,9 @@ merge_kernel(const float* __restrict__ list_v, const unsigned short* __restrict_
 }
 
 template <int KL>
-cudaError_t launch_merge_kl(const float* list_v, const unsigned short* list_c, int pairs, int n,
-                            int k, int64_t* idx, float* w, int* fb_count, int* fb_list,
-                            cudaStream_t stream) {
+cudaError_t launch_merge_kl(const float* list_v, const unsigned short* list_c, int B, int H, int n,
+                            int k, int64_t* idx, float* w, const RetryScratch& retry,
+                            bool retry_pass, cudaStream_t stream) {
   const size_t smem = MergeLayout<KL>::kBytes;
   static bool attr_set = false;
   if (!attr_set) {
@@ -228,23 +249,25 @@ cudaError_t launch_merge_kl(const float* list_v, const unsigned short* list_c, i
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const int grid = (pairs + kThreads - 1) / kThreads;
-  merge_kernel<KL><<<grid, kThreads, smem, stream>>>(list_v, list_c, pairs, n, k, idx, w,
-                                                      fb_count, fb_list);
+  const int64_t grid =
+      retry_pass ? retry_units(B, H) : ((int64_t)B * H + kThreads - 1) / kThreads;
+  merge_kernel<KL><<<(unsigned)grid, kThreads, smem, stream>>>(list_v, list_c, B, H, n, k, idx, w,
+                                                                retry, retry_pass);
   return cudaGetLastError();
 }
 
 }  // namespace
 
+int64_t retry_units(int64_t B, int64_t H) { return (B + kThreads - 1) / kThreads * H * 2; }
+
 cudaError_t launch_merge(const float* list_v, const unsigned short* list_c, int B, int H,
-                         int n_keys, int k, int64_t* idx, float* w, int* fb_count, int* fb_list,
-                         cudaStream_t stream) {
-  const int pairs = B * H;
-  if (pairs == 0) return cudaSuccess;
+                         int n_keys, int k, int64_t* idx, float* w, const RetryScratch& retry,
+                         bool retry_pass, cudaStream_t stream) {
+  if ((int64_t)B * H == 0) return cudaSuccess;
   if (k <= 16)
-    return launch_merge_kl<16>(list_v, list_c, pairs, n_keys, k, idx, w, fb_count, fb_list,
+    return launch_merge_kl<16>(list_v, list_c, B, H, n_keys, k, idx, w, retry, retry_pass,
                                stream);
-  return launch_merge_kl<32>(list_v, list_c, pairs, n_keys, k, idx, w, fb_count, fb_list, stream);
+  return launch_merge_kl<32>(list_v, list_c, B, H, n_keys, k, idx, w, retry, retry_pass, stream);
 }
 
 }  // namespace pkm

@@ -1,6 +1,4 @@
-// Steps a1-a5 on the CUDA cores: the path for fp32 queries and subkeys, and
-// the exact fallback of the tensor-core path for bf16 (rows whose selection
-// threshold hint turned out too high are listed and recomputed here).
+// Steps a1-a5 on the CUDA cores: the path for fp32 queries and subkeys.
 //
 // Product-Key Memory, "Factorising the key space": score each half of the
 // query against its own subkey set, keep the top-k of each half, form the k^2
@@ -23,9 +21,6 @@ namespace {
 constexpr int kThreads = 256;
 
 __device__ __forceinline__ float load_elem(const float* p, int64_t i) { return p[i]; }
-__device__ __forceinline__ float load_elem(const uint16_t* p, int64_t i) {
-  return __uint_as_float((uint32_t)p[i] << 16);
-}
 
 // Products of one 16-byte vector of subkey elements with the matching query
 // elements, accumulated in element order.
@@ -37,17 +32,6 @@ __device__ __forceinline__ float dot16(const uint4& u, const float* qv, const fl
   acc = fmaf(__uint_as_float(u.w), qv[3], acc);
   return acc;
 }
-__device__ __forceinline__ float dot16(const uint4& u, const float* qv, const uint16_t*) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-  float acc = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    acc = fmaf(__uint_as_float(w[i] << 16), qv[2 * i], acc);
-    acc = fmaf(__uint_as_float(w[i] & 0xffff0000u), qv[2 * i + 1], acc);
-  }
-  return acc;
-}
-
 // Steps a1-a5 for one (query, head) pair, by the whole CTA.
 template <typename TIn>
 __device__ void lookup_pair(const TIn* __restrict__ q, const TIn* __restrict__ subkeys, int H,
@@ -72,21 +56,41 @@ __device__ void lookup_pair(const TIn* __restrict__ q, const TIn* __restrict__ s
 
   // a2: subkey scores of both halves.  When a subkey row is a whole number
   // of 16-byte vectors, one warp reads a row (coalesced), each lane takes every
-  // 32nd vector and the lanes' partial sums are added with shuffles.
+  // 32nd vector and the lanes' partial sums are added with shuffles.  A warp
+  // takes 8 rows at a time so their loads are in flight together.
   constexpr int EPV = 16 / (int)sizeof(TIn);
   if (hd % EPV == 0) {
+    constexpr int R = 8;
     const int warp = tid >> 5, lane = tid & 31;
     const int nvec = hd / EPV;
-    for (int e = warp; e < 2 * n; e += kThreads / 32) {
-      const int half = e / n, a = e - half * n;
-      const uint4* row =
-          reinterpret_cast<const uint4*>(subkeys + (((int64_t)h * 2 + half) * n + a) * hd);
-      const float* qh = s_q + half * hd;
-      float acc = 0.0f;
-      for (int vi = lane; vi < nvec; vi += 32) acc += dot16(row[vi], qh + vi * EPV, subkeys);
+    const int nwarps = kThreads / 32;
+    for (int e0 = warp * R; e0 < 2 * n; e0 += nwarps * R) {
+      float acc[R];
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-      if (lane == 0) s_sc[e] = acc;
+      for (int u = 0; u < R; ++u) acc[u] = 0.0f;
+      for (int vi = lane; vi < nvec; vi += 32) {
+        uint4 x[R];
+#pragma unroll
+        for (int u = 0; u < R; ++u) {
+          const int e = e0 + u < 2 * n ? e0 + u : 2 * n - 1;  // in bounds, unused past the end
+          const int half = e / n, a = e - half * n;
+          x[u] = reinterpret_cast<const uint4*>(subkeys +
+                                                (((int64_t)h * 2 + half) * n + a) * hd)[vi];
+        }
+#pragma unroll
+        for (int u = 0; u < R; ++u) {
+          const int e = e0 + u < 2 * n ? e0 + u : 2 * n - 1;
+          acc[u] += dot16(x[u], s_q + (e / n) * hd + vi * EPV, subkeys);
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+        for (int u = 0; u < R; ++u) acc[u] += __shfl_xor_sync(0xffffffffu, acc[u], off);
+      if (lane == 0)
+#pragma unroll
+        for (int u = 0; u < R; ++u)
+          if (e0 + u < 2 * n) s_sc[e0 + u] = acc[u];
     }
   } else {
     for (int e = tid; e < 2 * n; e += kThreads) {
@@ -148,21 +152,13 @@ __device__ void lookup_pair(const TIn* __restrict__ q, const TIn* __restrict__ s
   }
 }
 
-// With pair_list == nullptr CTA b handles pair b; otherwise the CTAs walk
-// pair_list[0 .. *pair_count).
+// CTA b handles the (query, head) pair b.
 template <typename TIn>
 __global__ void __launch_bounds__(kThreads)
 lookup_simt_kernel(const TIn* __restrict__ q, const TIn* __restrict__ subkeys, int H, int d_q,
-                   int n, int k, int64_t* __restrict__ idx, float* __restrict__ w,
-                   const int* __restrict__ pair_count, const int* __restrict__ pair_list) {
+                   int n, int k, int64_t* __restrict__ idx, float* __restrict__ w) {
   extern __shared__ __align__(16) unsigned char smem[];
-  if (!pair_list) {
-    lookup_pair(q, subkeys, H, d_q, n, k, (int64_t)blockIdx.x, idx, w, smem);
-    return;
-  }
-  const int npairs = *pair_count;
-  for (int it = blockIdx.x; it < npairs; it += gridDim.x)
-    lookup_pair(q, subkeys, H, d_q, n, k, (int64_t)pair_list[it], idx, w, smem);
+  lookup_pair(q, subkeys, H, d_q, n, k, (int64_t)blockIdx.x, idx, w, smem);
 }
 
 size_t simt_smem(int d_q, int n_keys, int k) {
@@ -183,23 +179,7 @@ cudaError_t launch_lookup_simt(const float* q, const float* subkeys, int B, int 
   }
   const int64_t pairs = (int64_t)B * H;
   lookup_simt_kernel<float><<<(unsigned)pairs, kThreads, smem, stream>>>(
-      q, subkeys, H, d_q, n_keys, k, idx, w, nullptr, nullptr);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_lookup_fallback(const uint16_t* q, const uint16_t* subkeys, int B, int H,
-                                   int d_q, int n_keys, int k, const int* pair_count,
-                                   const int* pair_list, int64_t* idx, float* w, int grid,
-                                   cudaStream_t stream) {
-  if (B == 0) return cudaSuccess;
-  const size_t smem = simt_smem(d_q, n_keys, k);
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(lookup_simt_kernel<uint16_t>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-  }
-  lookup_simt_kernel<uint16_t><<<grid, kThreads, smem, stream>>>(
-      q, subkeys, H, d_q, n_keys, k, idx, w, pair_count, pair_list);
+      q, subkeys, H, d_q, n_keys, k, idx, w);
   return cudaGetLastError();
 }
 

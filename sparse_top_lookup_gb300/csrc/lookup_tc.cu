@@ -13,14 +13,17 @@
 //   warp 0      TMA producer: 128x64 query slabs and NCx64 subkey slabs
 //               (bf16, 128-byte swizzle) into a 3-stage shared-memory ring;
 //   warp 1      allocates 512 TMEM columns and issues tcgen05.mma
-//               (M=128, N=NC<=256, K=16, fp32 accumulate) into one of two
-//               TMEM buffers, so scoring chunk c+1 overlaps the epilogue of c;
-//   warps 2..5  epilogue, one thread per query row (= TMEM lane): reads its
-//               row's scores with tcgen05.ld and selects the half's exact
-//               top-KL (selection helpers below), then writes the half's list
-//               by (score desc, subkey asc) to global memory.
+//               (M=128, N=NC<=128, K=16, fp32 accumulate) into four TMEM
+//               buffers, two per epilogue set, so scoring overlaps selection;
+//   warps 2..9  two epilogue sets of four warps, each set on every other
+//               unit; one thread per query row (= TMEM lane) reads its row's
+//               scores with tcgen05.ld and selects the half's exact top-KL
+//               (selection helpers below), then writes the half's list by
+//               (score desc, subkey asc) to global memory.
 // The k^2 merge and the softmax (a4, a5) run in lookup_merge.cu, one thread
-// per (query, head).  Scores never leave the SM.  Every mbarrier wait is
+// per (query, head).  A retry launch of this kernel re-selects, without the
+// threshold hint, the units listed in a device array.  Scores never leave
+// the SM.  Every mbarrier wait is
 // bounded; on time-out the kernel records PKM_ERR_TIMEOUT, stops issuing
 // work, waits (bounded) for its own copies and MMAs in flight, frees TMEM and
 // returns.
@@ -228,7 +231,8 @@ __device__ __forceinline__ void wait_phase_drain(uint32_t bar, uint32_t parity) 
 //      each entry's place in the (score desc, column asc) order comes from a
 //      binary search of its score in V.
 // A row whose hint was above its final KL-th score ends with fewer than KL
-// entries; it is reported and recomputed by the CUDA-core fallback kernel.
+// entries; its list is marked, and the retry pass selects its unit again
+// without the hint.
 
 constexpr int LOG_CAP = 64;                 // log entries per row and epilogue set
 constexpr int SUB = 8;                      // scores appended between two overflow checks
@@ -344,11 +348,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_c,
                  int B, int H, int n, int NC, int nch, int kb_count, float hint_z,
                  float* __restrict__ list_v, unsigned short* __restrict__ list_c,
-                 int* __restrict__ status) {
+                 int* __restrict__ status, const int* __restrict__ unit_list,
+                 const int* __restrict__ unit_count) {
   extern __shared__ unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t bars[2 * STAGES + 4 * SETS + 1];
   __shared__ uint32_t s_tmem_base;
   __shared__ int s_abort;
+
+  // work unit u: tile u / 2 (row tile, head), half u % 2.  The CTA's i-th
+  // unit is entry blockIdx.x + i * gridDim.x of all units, or of unit_list
+  // when one is given (a retry launch).  A CTA without units returns at once.
+  const int row_tiles = (B + BM - 1) / BM;
+  const int units = unit_list ? *unit_count : row_tiles * H * 2;
+  const int mine = (int)blockIdx.x < units ? (units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  if (mine == 0) return;
+  auto unit_at = [&](int i) {
+    const int e = blockIdx.x + i * gridDim.x;
+    return unit_list ? unit_list[e] : e;
+  };
 
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -390,10 +407,6 @@ select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
   const uint32_t tmem = s_tmem_base;
   const Ctl ctl{&s_abort, status};
 
-  // work unit u: tile u / 2 (row tile, head), half u % 2
-  const int row_tiles = (B + BM - 1) / BM;
-  const int units = row_tiles * H * 2;
-  const int mine = blockIdx.x < units ? (units - 1 - blockIdx.x) / gridDim.x + 1 : 0;
 
   if (warp == 0) {
     // ---------------------------------------------------- TMA producer
@@ -404,7 +417,7 @@ select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
       for (int i0 = 0; ok && i0 < mine; i0 += SETS)
         for (int ch = 0; ok && ch < nch; ++ch)
           for (int st = 0; ok && st < SETS && i0 + st < mine; ++st) {
-            const int u = blockIdx.x + (i0 + st) * gridDim.x;
+            const int u = unit_at(i0 + st);
             const int tile = u >> 1, half = u & 1;
             const int rt = tile / H, h = tile - rt * H;
             for (int kb = 0; kb < kb_count; ++kb) {
@@ -477,7 +490,7 @@ select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
     uint32_t cnt = 0;                  // chunks of this set consumed so far
     bool ok = true;
     for (int i = set; ok && i < mine; i += SETS) {
-      const int u = blockIdx.x + i * gridDim.x;
+      const int u = unit_at(i);
       const int tile = u >> 1, half = u & 1;
       const int rt = tile / H, h = tile - rt * H;
       int nsorted = 0;
@@ -503,7 +516,7 @@ select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
         if (!ok) break;
         tc_fence_after();
         const uint32_t base = lane_addr + (2 * set + (cnt & 1u)) * NCMAX;
-        if (ch == 0 && n > LOG_CAP) {
+        if (ch == 0 && n > LOG_CAP && hint_z > -INFINITY) {
           // threshold hint: mean + z * spread of the first chunks' scores
           float a1[4] = {0.0f, 0.0f, 0.0f, 0.0f}, a2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll 1
@@ -568,7 +581,7 @@ select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
       // the half's list by (score desc, subkey asc) into log slots [KL, 2KL),
       // then to global memory; a list with fewer than `need` entries (the
       // threshold hint was above the row's KL-th score) is marked by the
-      // subkey 0xffff in its first slot and recomputed by the fallback
+      // subkey 0xffff in its first slot and selected again by the retry pass
       sorted_list<KL>(L, len, V, b < B);
       if (b < B) {
         const size_t off = (((size_t)b * H + h) * 2 + half) * KL;
@@ -632,7 +645,8 @@ int sm_count() {
 template <int KL>
 cudaError_t launch_kl(const CUtensorMap& mq, const CUtensorMap& mc, int B, int H, int n, int NC,
                       int nch, int kbc, float hint_z, float* list_v, unsigned short* list_c,
-                      int* status, cudaStream_t stream) {
+                      int* status, const int* unit_list, const int* unit_count,
+                      cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(select_tc_kernel<KL>,
@@ -640,10 +654,10 @@ cudaError_t launch_kl(const CUtensorMap& mq, const CUtensorMap& mc, int B, int H
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const int units = (B + BM - 1) / BM * H * 2;
+  const int units = (B + BM - 1) / BM * H * 2;  // also the most a retry can list
   const int grid = units < sm_count() ? units : sm_count();  // persistent: one CTA per SM
   select_tc_kernel<KL><<<grid, NUM_THREADS, SMEM_TOTAL, stream>>>(
-      mq, mc, B, H, n, NC, nch, kbc, hint_z, list_v, list_c, status);
+      mq, mc, B, H, n, NC, nch, kbc, hint_z, list_v, list_c, status, unit_list, unit_count);
   return cudaGetLastError();
 }
 
@@ -676,7 +690,7 @@ int list_slots(int k) { return k <= 16 ? 16 : 32; }
 
 cudaError_t launch_lookup_tc(const uint16_t* q, const uint16_t* subkeys, int B, int H, int d_q,
                              int n_keys, int k, float hint_z, int64_t* idx, float* w, int* status,
-                             int* fb_count, int* fb_list, float* list_v, unsigned short* list_c,
+                             const RetryScratch& retry, float* list_v, unsigned short* list_c,
                              cudaStream_t stream) {
   if (B == 0) return cudaSuccess;
   EncodeTiledFn enc = encode_fn();
@@ -710,19 +724,26 @@ cudaError_t launch_lookup_tc(const uint16_t* q, const uint16_t* subkeys, int B, 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  cudaError_t e = k <= 16 ? launch_kl<16>(mq, mc, B, H, n_keys, NC, nch, kbc, hint_z, list_v,
-                                          list_c, status, stream)
-                          : launch_kl<32>(mq, mc, B, H, n_keys, NC, nch, kbc, hint_z, list_v,
-                                          list_c, status, stream);
-  if (e != cudaSuccess) return e;
-  // a4, a5: the k^2 merge and softmax, one thread per (query, head)
-  e = cudaMemsetAsync(fb_count, 0, sizeof(int), stream);
-  if (e != cudaSuccess) return e;
-  e = launch_merge(list_v, list_c, B, H, n_keys, k, idx, w, fb_count, fb_list, stream);
-  if (e != cudaSuccess) return e;
-  // pairs whose threshold hint was too high: exact recomputation on the CUDA cores
-  return launch_lookup_fallback(q, subkeys, B, H, d_q, n_keys, k, fb_count, fb_list, idx, w,
-                                2 * sm_count(), stream);
+  auto select = [&](float z, const int* list, const int* count) {
+    return k <= 16 ? launch_kl<16>(mq, mc, B, H, n_keys, NC, nch, kbc, z, list_v, list_c, status,
+                                   list, count, stream)
+                   : launch_kl<32>(mq, mc, B, H, n_keys, NC, nch, kbc, z, list_v, list_c, status,
+                                   list, count, stream);
+  };
+  // the retry bookkeeping starts clear: counts and the per-unit flags (one buffer)
+  cudaError_t e =
+      cudaMemsetAsync(retry.counts, 0, (2 + (size_t)retry_units(B, H)) * sizeof(int), stream);
+  if (e == cudaSuccess) e = select(hint_z, nullptr, nullptr);
+  // a4, a5: the k^2 merge and softmax, one thread per (query, head); lists
+  // the units whose threshold hint was above a row's KL-th score
+  if (e == cudaSuccess)
+    e = launch_merge(list_v, list_c, B, H, n_keys, k, idx, w, retry, false, stream);
+  // retry: those units again without the hint (exact), then their pairs;
+  // both launches return at once when nothing is listed
+  if (e == cudaSuccess) e = select(-INFINITY, retry.unit_list, retry.counts + 1);
+  if (e == cudaSuccess)
+    e = launch_merge(list_v, list_c, B, H, n_keys, k, idx, w, retry, true, stream);
+  return e;
 }
 
 }  // namespace pkm

@@ -13,8 +13,9 @@ struct pkm_handle {
   int64_t* ws_idx;   // [max_B, max_H, max_k] when the caller passes idx == NULL
   float* ws_w;       // [max_B, max_H, max_k] when the caller passes w == NULL
   int* status;       // device status word
-  int* fb_count;     // pairs recomputed by the fallback in the last bf16 lookup
-  int* fb_list;      // [max_B * max_H] their (query * H + head) indices
+  int* retry_counts;  // [2 + units]: pairs of the last bf16 lookup that needed the retry,
+                      // units retried, then the per-unit flags (units = retry_units(max_B, max_H))
+  int* unit_list;     // [units]
   float* list_v;     // [max_B * max_H * 2 * 32] per-half lists between the two bf16 kernels
   unsigned short* list_c;
   float hint_z;      // selection threshold hint override (NaN: automatic)
@@ -76,7 +77,8 @@ int run_lookup(pkm_t h, const void* q, const void* subkeys, int B, int H, int n,
     const float z = isnan(h->hint_z) ? pkm::default_hint_z(n, k) : h->hint_z;
     return cuda_rc(pkm::launch_lookup_tc(static_cast<const uint16_t*>(q),
                                          static_cast<const uint16_t*>(subkeys), B, H, h->cfg.d_q,
-                                         n, k, z, idx, w, h->status, h->fb_count, h->fb_list,
+                                         n, k, z, idx, w, h->status,
+                                         {h->retry_counts, h->retry_counts + 2, h->unit_list},
                                          h->list_v, h->list_c, s));
   }
   return cuda_rc(pkm::launch_lookup_simt(static_cast<const float*>(q),
@@ -122,8 +124,8 @@ void pkm_destroy(pkm_t h) {
   cudaFree(h->ws_idx);
   cudaFree(h->ws_w);
   cudaFree(h->status);
-  cudaFree(h->fb_count);
-  cudaFree(h->fb_list);
+  cudaFree(h->retry_counts);
+  cudaFree(h->unit_list);
   cudaFree(h->list_v);
   cudaFree(h->list_c);
   cudaFree(h->stage_q);
@@ -162,9 +164,11 @@ int pkm_create(pkm_t* out, const pkm_config* cfg) {
   }
   if (ok) {
     const size_t pairs = (size_t)cfg->max_B * cfg->max_H;
-    ok = cudaMalloc(&h->fb_count, sizeof(int)) == cudaSuccess &&
-         cudaMemset(h->fb_count, 0, sizeof(int)) == cudaSuccess &&
-         cudaMalloc(&h->fb_list, (pairs ? pairs : 1) * sizeof(int)) == cudaSuccess;
+    const size_t units =
+        cfg->q_dtype == PKM_BF16 ? (size_t)pkm::retry_units(cfg->max_B, cfg->max_H) : 0;
+    ok = cudaMalloc(&h->retry_counts, (2 + units) * sizeof(int)) == cudaSuccess &&
+         cudaMemset(h->retry_counts, 0, (2 + units) * sizeof(int)) == cudaSuccess &&
+         cudaMalloc(&h->unit_list, (units ? units : 1) * sizeof(int)) == cudaSuccess;
     if (ok && cfg->q_dtype == PKM_BF16 && pairs) {
       const size_t slots = pairs * 2 * pkm::kListMaxSlots;
       ok = cudaMalloc(&h->list_v, slots * sizeof(float)) == cudaSuccess &&
@@ -315,7 +319,7 @@ int pkm_set_option(pkm_t h, int option, double value) {
 int pkm_get_fallback_count(pkm_t h, void* stream, int* count) {
   if (!h || !count) return PKM_ERR_INVALID;
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return PKM_ERR_CUDA;
-  if (cudaMemcpy(count, h->fb_count, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+  if (cudaMemcpy(count, h->retry_counts, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
     return PKM_ERR_CUDA;
   return PKM_OK;
 }

@@ -24,35 +24,46 @@ cudaError_t launch_gather(const void* values, int value_dtype, int64_t N, int d_
 cudaError_t launch_lookup_simt(const float* q, const float* subkeys, int B, int H, int d_q,
                                int n_keys, int k, int64_t* idx, float* w, cudaStream_t stream);
 
+// Device scratch of the bf16 lookup's retry pass.  A per-half list whose
+// selection threshold hint was above the row's KL-th score is marked by the
+// selection kernel; the merge then lists that list's work unit (128 queries x
+// one head x one half; unit index ((row tile * H + head) << 1) | half), and
+// the listed units are scored and selected again without the hint, which is
+// exact by construction, and their pairs merged again.
+// counts and unit_flag are one buffer (unit_flag == counts + 2), cleared by
+// one memset per call.
+struct RetryScratch {
+  int* counts;     // [0] pairs that had a marked list, [1] units listed for the retry
+  int* unit_flag;  // [retry_units(B, H)]: nonzero once a unit is listed
+  int* unit_list;  // [retry_units(B, H)]
+};
+int64_t retry_units(int64_t B, int64_t H);
+
 // Steps a1-a5 for bf16 queries/subkeys: tcgen05 scoring with the per-half
-// selection fused into its epilogue, then the k^2 merge and softmax kernel.
-// hint_z sets the per-row selection threshold (mean + hint_z * spread of a
-// row's scores; any value gives exact results).  Device scratch: fb_count /
-// fb_list (1 and B*H ints) list the (query, head) pairs recomputed by the
-// CUDA-core fallback; list_v / list_c (B*H*2*list_slots(k) floats and
-// 16-bit subkeys) hold the per-half lists between the two kernels.
+// selection fused into its epilogue, then the k^2 merge and softmax kernel,
+// then the retry pass (it returns at once when no unit is listed).  hint_z
+// sets the per-row selection threshold (mean + hint_z * spread of a row's
+// first scores; any value gives exact results).  list_v / list_c
+// (B*H*2*list_slots(k) floats and 16-bit subkeys) hold the per-half lists
+// between the kernels.
 cudaError_t launch_lookup_tc(const uint16_t* q, const uint16_t* subkeys, int B, int H, int d_q,
                              int n_keys, int k, float hint_z, int64_t* idx, float* w, int* status,
-                             int* fb_count, int* fb_list, float* list_v, unsigned short* list_c,
+                             const RetryScratch& retry, float* list_v, unsigned short* list_c,
                              cudaStream_t stream);
 
 // Entries of one per-half list for a given k.
 int list_slots(int k);
 
-// Steps a4-a5 from the per-half lists (lookup_merge.cu).
+// Steps a4-a5 from the per-half lists (lookup_merge.cu).  First pass: every
+// pair; pairs with a marked list are counted in retry.counts[0] and their
+// units listed.  Retry pass: the pairs of the units in
+// retry.unit_list[0 .. retry.counts[1]), one CTA per listed unit.
 cudaError_t launch_merge(const float* list_v, const unsigned short* list_c, int B, int H,
-                         int n_keys, int k, int64_t* idx, float* w, int* fb_count, int* fb_list,
-                         cudaStream_t stream);
+                         int n_keys, int k, int64_t* idx, float* w, const RetryScratch& retry,
+                         bool retry_pass, cudaStream_t stream);
 
 // The hint_z launch_lookup_tc uses unless a handle overrides it.
 float default_hint_z(int n_keys, int k);
-
-// Exact recomputation of the listed (query, head) pairs, bf16 inputs, fp32
-// FMA on the CUDA cores; grid CTAs walk pair_list[0 .. *pair_count).
-cudaError_t launch_lookup_fallback(const uint16_t* q, const uint16_t* subkeys, int B, int H,
-                                   int d_q, int n_keys, int k, const int* pair_count,
-                                   const int* pair_list, int64_t* idx, float* w, int grid,
-                                   cudaStream_t stream);
 
 // Limits of each path (checked on the host before a launch).
 constexpr int kSimtMaxK = 64;

@@ -6,11 +6,11 @@
 // a host framework that owns every device allocation through its own pool,
 // or a latency-critical loop where cudaMalloc / cudaFree would synchronise
 // the device.  pkm_create allocates the handle's scratch, so those callers
-// use this entry point instead.  Its scratch (a status word, the count and
-// the list of (query, head) pairs sent to the CUDA-core fallback, and the
-// per-half lists passed from the selection kernel to the merge kernel) is one
-// fixed-size array in the library's device memory, present on every GPU that
-// loads the library until the process exits.
+// use this entry point instead.  Its scratch (a status word, the retry
+// pass's counts, per-unit flags and unit list, and the per-half lists passed
+// from the selection kernel to the merge kernel) is one fixed-size array in
+// the library's device memory, present on every GPU that loads the library
+// until the process exits.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -20,10 +20,13 @@
 
 namespace {
 
-// [0] device status word, [1] fallback pair count, then the fallback pair
-// list and the per-half lists of at most PKM_STATIC_MAX_PAIRS pairs
-constexpr size_t kHeader = 256;
-constexpr size_t kFbBytes = (size_t)PKM_STATIC_MAX_PAIRS * 4;
+// [0] device status word, [1..2] retry counts and from [3] the per-unit
+// flags, then the retry pass's unit list and the per-half lists of at most
+// PKM_STATIC_MAX_PAIRS pairs.  Work units number
+// ceil(B / 128) * H * 2 <= 2 * (B*H / 128 + H).
+constexpr size_t kMaxUnits = 2 * ((size_t)PKM_STATIC_MAX_PAIRS / 128 + PKM_STATIC_MAX_PAIRS);
+constexpr size_t kHeader = (3 + kMaxUnits) * 4 / 256 * 256 + 256;
+constexpr size_t kFbBytes = kMaxUnits * 4;
 constexpr size_t kListSlots = (size_t)PKM_STATIC_MAX_PAIRS * 2 * pkm::kListMaxSlots;
 constexpr size_t kStaticBytes = kHeader + kFbBytes + kListSlots * 4 + kListSlots * 2;
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticBytes];
@@ -69,18 +72,19 @@ extern "C" int pkm_lookup_static(const void* q, const void* subkeys, int B, int 
   unsigned char* base = nullptr;
   int rc = scratch_on_current_device(&base);
   if (rc) return rc;
-  int* scratch = reinterpret_cast<int*>(base);  // status, fallback count
-  int* fb_list = reinterpret_cast<int*>(base + kHeader);
+  int* scratch = reinterpret_cast<int*>(base);  // status, retry counts, unit flags
+  int* unit_list = reinterpret_cast<int*>(base + kHeader);
   float* list_v = reinterpret_cast<float*>(base + kHeader + kFbBytes);
   unsigned short* list_c =
       reinterpret_cast<unsigned short*>(base + kHeader + kFbBytes + kListSlots * 4);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // the status word starts clear on every call (the fallback count is
+  // the status word starts clear on every call (the retry bookkeeping is
   // cleared by the lookup launch itself)
   if (cudaMemsetAsync(scratch, 0, sizeof(int), s) != cudaSuccess) return PKM_ERR_CUDA;
   cudaError_t e = pkm::launch_lookup_tc(
       static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(subkeys), B, H, d_q, n_keys,
-      k, pkm::default_hint_z(n_keys, k), idx, w, scratch, scratch + 1, fb_list, list_v, list_c, s);
+      k, pkm::default_hint_z(n_keys, k), idx, w, scratch, {scratch + 1, scratch + 3, unit_list},
+      list_v, list_c, s);
   if (e != cudaSuccess) return PKM_ERR_CUDA;
   if (status &&
       cudaMemcpyAsync(status, scratch, sizeof(int), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
