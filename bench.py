@@ -324,9 +324,10 @@ def run_ours(args, rank, world, local):
                              "peak_source": pk_["src"] + " bf16 burst"},
         "e2e": {"value": world * B * H / e2e_s, "unit": UNIT,
                 "h2d_bytes_per_step": B * H * d_q * esz, "d2h_bytes_per_step": B * d_v * 4},
-        # per step: select_tc_kernel, merge_kernel, the (usually empty) fallback
-        # kernel and gather_kernel (fp32 inputs: lookup_simt_kernel and gather_kernel)
-        "gpu_launches": (4 if bf16 else 2) * args.steps,
+        # per step: select_tc_kernel and merge_kernel, their retry launches
+        # (return at once when no row missed its threshold hint) and
+        # gather_kernel (fp32 inputs: lookup_simt_kernel and gather_kernel)
+        "gpu_launches": (5 if bf16 else 2) * args.steps,
         "clocks": clk.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -195,11 +195,10 @@ int pkm_abi_version(void);
  * pkm_lookup_static: the lookup alone (scoring through softmax) for bf16
  * queries and subkeys, as pkm_lookup on a bf16 handle with d_q given here:
  * idx and w [B, H, k] are written on `stream`.  It allocates nothing: its
- * scratch (a status word, the list of (query, head) pairs recomputed on the
- * CUDA cores and the per-half candidate lists, for at most
- * PKM_STATIC_MAX_PAIRS pairs) is one fixed array of 256 + 388 *
- * PKM_STATIC_MAX_PAIRS bytes (about 24 MiB) in the library's device memory,
- * which every GPU that loads the library holds until the process exits.
+ * scratch (a status word, the retry pass's counts, unit flags and unit list,
+ * and the per-half candidate lists, for at most PKM_STATIC_MAX_PAIRS pairs)
+ * is one fixed array of about 25 MiB in the library's device memory, which
+ * every GPU that loads the library holds until the process exits.
  *   - B * H above PKM_STATIC_MAX_PAIRS returns PKM_ERR_RANGE; other argument
  *     errors are as for pkm_lookup.
  *   - status: if not NULL, a device int that receives the call's device
