@@ -45,13 +45,16 @@ def lib():
                                      vp, vp, i32]
         L.oracle_brute_topk.argtypes = [vp, i32, vp, i32, i32, i32, i32, i32, i32, vp, vp, i32]
         L.oracle_quantize_fp8.argtypes = [vp, i32, i64, i32, vp, vp, i32]
+        L.oracle_query_net.argtypes = [vp, i32, vp, i32, i32, i32, i32, vp, vp, vp, vp,
+                                       ctypes.c_double, vp, i32]
         L.oracle_gather_fp8.argtypes = [vp, vp, i64, i32, i32, i32, i32, vp, vp, vp, i32]
         L.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
         L.oracle_e4m3_value.restype = ctypes.c_double
         L.oracle_e4m3_encode.argtypes = [ctypes.c_float]
         L.oracle_e4m3_encode.restype = ctypes.c_uint8
         for f in (L.oracle_lookup, L.oracle_gather, L.oracle_forward, L.oracle_brute_topk,
-                  L.oracle_num_threads, L.oracle_quantize_fp8, L.oracle_gather_fp8):
+                  L.oracle_num_threads, L.oracle_quantize_fp8, L.oracle_gather_fp8,
+                  L.oracle_query_net):
             f.restype = i32
         _lib = L
     return _lib
@@ -172,3 +175,15 @@ def gather_fp8(codes, scales, N, d_v, idx, w, nthreads=0):
     if rc != 0:
         raise ValueError("oracle_gather_fp8: bad shape or index out of range")
     return out
+
+
+def query_net(x, weight, B, dim, F, gamma, beta, mean, var, eps, nthreads=0):
+    """q = BatchNorm1d(x W^T) with running statistics, in double.  Returns [B, F]."""
+    x, weight = _c(x), _c(weight)
+    params = [np.ascontiguousarray(a, np.float32) for a in (gamma, beta, mean, var)]
+    q = np.empty((B, F), np.float64)
+    rc = lib().oracle_query_net(_p(x), _dt(x), _p(weight), _dt(weight), B, dim, F,
+                                *[_p(a) for a in params], float(eps), _p(q), nthreads)
+    if rc != 0:
+        raise ValueError("oracle_query_net: bad shape")
+    return q

@@ -322,6 +322,33 @@ int oracle_gather_fp8(const uint8_t* codes, const float* scales, int64_t N, int 
   return bad ? -1 : 0;
 }
 
+// ----------------------------------------------------------- query network
+
+// Product-Key Memory, code listing: q = qnorm(query(x)) with query an
+// nn.Linear(dim, F, bias=False) (weight [F, dim]) and qnorm an
+// nn.BatchNorm1d(F), here in its inference form with running statistics:
+//   z[b, f] = sum_t x[b, t] * W[f, t]                      (one sequential loop)
+//   q[b, f] = (z[b, f] - mean[f]) / sqrt(var[f] + eps) * gamma[f] + beta[f]
+// in double; x and W fp32 or bf16 bits.
+int oracle_query_net(const void* x, int xdt, const void* w, int wdt, int B, int dim, int F,
+                     const float* gamma, const float* beta, const float* mean, const float* var,
+                     double eps, double* q, int nthreads) {
+  if (B < 0 || dim < 1 || F < 1) return -1;
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(static)
+#endif
+  for (int64_t b = 0; b < B; ++b)
+    for (int f = 0; f < F; ++f) {
+      double z = 0.0;
+      for (int t = 0; t < dim; ++t)
+        z += widen(x, xdt, b * dim + t) * widen(w, wdt, (int64_t)f * dim + t);
+      q[b * F + f] = (z - (double)mean[f]) / std::sqrt((double)var[f] + eps) * (double)gamma[f] +
+                     (double)beta[f];
+    }
+  return 0;
+}
+
 // Brute force over every full key: score(a, b') is ONE d_q-long dot product
 // of q[b,h] with concat(C[h,0,a], C[h,1,b']); all n^2 keys sorted by
 // (score desc, flat asc); first k kept.  Independent of the factorisation.

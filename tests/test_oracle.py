@@ -382,3 +382,53 @@ def test_gather_fp8_closed_forms():
         bad = idx.copy()
         bad[0, 0, 0] = N
         oracle.gather_fp8(codes, s, N, d_v, bad, w)
+
+
+# ----------------------------------------------------------- query network
+#
+# Product-Key Memory, code listing: q = BatchNorm1d(Linear(dim, F, bias=False)(x)),
+# the BatchNorm in its inference form (running statistics).
+
+def test_query_net_matches_torch_float64():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(31)
+    B, dim, F, eps = 37, 48, 96, 1e-5
+    x = rng.standard_normal((B, dim)).astype(np.float32)
+    W = (rng.standard_normal((F, dim)) / np.sqrt(dim)).astype(np.float32)
+    gamma = (1 + 0.2 * rng.standard_normal(F)).astype(np.float32)
+    beta = (0.3 * rng.standard_normal(F)).astype(np.float32)
+    mean = (0.1 * rng.standard_normal(F)).astype(np.float32)
+    var = (0.5 + rng.random(F)).astype(np.float32)
+    q = oracle.query_net(x, W, B, dim, F, gamma, beta, mean, var, eps)
+    lin = torch.nn.Linear(dim, F, bias=False).double()
+    bn = torch.nn.BatchNorm1d(F, eps=eps).double().eval()
+    with torch.no_grad():
+        lin.weight.copy_(torch.from_numpy(W.astype(np.float64)))
+        bn.weight.copy_(torch.from_numpy(gamma.astype(np.float64)))
+        bn.bias.copy_(torch.from_numpy(beta.astype(np.float64)))
+        bn.running_mean.copy_(torch.from_numpy(mean.astype(np.float64)))
+        bn.running_var.copy_(torch.from_numpy(var.astype(np.float64)))
+        ref = bn(lin(torch.from_numpy(x.astype(np.float64)))).numpy()
+    np.testing.assert_allclose(q, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_query_net_closed_forms():
+    rng = np.random.default_rng(32)
+    B, dim = 9, 32
+    x = rng.standard_normal((B, dim)).astype(np.float32)
+    eye = np.eye(dim, dtype=np.float32)
+    one, zero = np.ones(dim, np.float32), np.zeros(dim, np.float32)
+    # identity weight, neutral normalisation (var + eps = 1): q = x
+    q = oracle.query_net(x, eye, B, dim, dim, one, zero, zero, np.full(dim, 0.75, np.float32), 0.25)
+    assert (q == x.astype(np.float64)).all()
+    # identity weight: q = (x - mean) / sqrt(var + eps) * gamma + beta, column by column
+    g, bt, m, v = (rng.random(dim).astype(np.float32) + 0.5 for _ in range(4))
+    q = oracle.query_net(x, eye, B, dim, dim, g, bt, m, v, 1e-3)
+    want = (x.astype(np.float64) - m) / np.sqrt(v.astype(np.float64) + 1e-3) * g + bt
+    np.testing.assert_allclose(q, want, rtol=1e-14)
+    # a bf16 input gives the same result as its exact fp32 widening
+    xb = synth.normal(5, 6, B * dim, 1.0, dtype="bf16").reshape(B, dim)
+    xf = (xb.astype(np.uint32) << 16).view(np.float32)
+    a = oracle.query_net(xb, eye, B, dim, dim, g, bt, m, v, 1e-3)
+    b = oracle.query_net(xf, eye, B, dim, dim, g, bt, m, v, 1e-3)
+    assert (a == b).all()
