@@ -228,6 +228,31 @@ int pkm_lookup_static(const void *q, const void *subkeys, int B, int H, int d_q,
 int pkm_quantize_values_fp8(const void *values, int value_dtype, int64_t N, int d_v, void *out,
                             void *stream);
 
+/*
+ * The query network ahead of the lookup (Product-Key Memory, code listing:
+ * q = BatchNorm1d(Linear(dim, dim, bias=False)(x)); with H heads of width d_q
+ * the Linear maps dim -> F = H * d_q features and q is the [B, H, d_q] query
+ * of pkm_forward).  The BatchNorm is taken in its inference form, with
+ * running statistics (the listing does not fix the mode).
+ *
+ * pkm_bn_fold: scale[f] = gamma[f] / sqrt(var[f] + eps), shift[f] = beta[f] -
+ * mean[f] * scale[f], fp32, f < F (device arrays; enqueued on `stream`).
+ *
+ * pkm_query_net: q[b, f] = bf16_rn((sum_t x[b, t] * W[f, t]) * scale[f] +
+ * shift[f]), x [B, dim] bf16, W [F, dim] bf16 (nn.Linear's weight layout),
+ * scale / shift [F] fp32, q [B, F] bf16; tensor cores, fp32 accumulation.
+ * dim a multiple of 16, F a multiple of 32, pointers 16-byte aligned.
+ * status: NULL, or a device int that receives PKM_ERR_TIMEOUT if a bounded
+ * wait inside the kernel gives up (it is not cleared).  Errors:
+ * PKM_ERR_INVALID (NULL pointer, B < 0, dim < 1, F < 1), PKM_ERR_UNSUPPORTED
+ * (dim or F layout), PKM_ERR_ALIGN, PKM_ERR_CUDA.  B == 0 is a no-op.
+ */
+int pkm_bn_fold(const float *gamma, const float *beta, const float *running_mean,
+                const float *running_var, float eps, int F, float *scale, float *shift,
+                void *stream);
+int pkm_query_net(const void *x, const void *weight, int B, int dim, int F, const float *scale,
+                  const float *shift, void *q, int *status, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -24,7 +24,7 @@ PKM_HOST_MAX_CHUNKS = 16
 EXPORTED = ["pkm_create", "pkm_destroy", "pkm_forward", "pkm_lookup", "pkm_gather",
             "pkm_forward_host", "pkm_get_status", "pkm_check_args", "pkm_strerror",
             "pkm_abi_version", "pkm_set_option", "pkm_get_fallback_count", "pkm_lookup_static",
-            "pkm_quantize_values_fp8"]
+            "pkm_quantize_values_fp8", "pkm_bn_fold", "pkm_query_net"]
 PKM_STATIC_MAX_PAIRS = 1 << 16
 
 
@@ -74,9 +74,12 @@ def lib():
         L.pkm_lookup_static.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp]
         L.pkm_get_fallback_count.argtypes = [vp, vp, ctypes.POINTER(i32)]
         L.pkm_quantize_values_fp8.argtypes = [vp, i32, ctypes.c_int64, i32, vp, vp]
+        L.pkm_bn_fold.argtypes = [vp, vp, vp, vp, ctypes.c_float, i32, vp, vp, vp]
+        L.pkm_query_net.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp, vp, vp]
         for f in ("pkm_create", "pkm_forward", "pkm_lookup", "pkm_gather", "pkm_forward_host",
                   "pkm_get_status", "pkm_check_args", "pkm_abi_version", "pkm_set_option",
-                  "pkm_get_fallback_count", "pkm_lookup_static", "pkm_quantize_values_fp8"):
+                  "pkm_get_fallback_count", "pkm_lookup_static", "pkm_quantize_values_fp8",
+                  "pkm_bn_fold", "pkm_query_net"):
             getattr(L, f).restype = i32
         _lib = L
     return _lib
@@ -180,6 +183,18 @@ def pkm_quantize_values_fp8(values, value_dtype, N, d_v, out, stream=None):
     """Write the fp8 e4m3 table (N*d_v codes, then N fp32 scales) of an fp32/bf16 table."""
     return lib().pkm_quantize_values_fp8(_addr(values), value_dtype, N, d_v, _addr(out),
                                          _stream(stream))
+
+
+def pkm_bn_fold(gamma, beta, running_mean, running_var, eps, F, scale, shift, stream=None):
+    """Per-feature scale / shift of an eval-mode BatchNorm1d (device arrays)."""
+    return lib().pkm_bn_fold(_addr(gamma), _addr(beta), _addr(running_mean), _addr(running_var),
+                             float(eps), F, _addr(scale), _addr(shift), _stream(stream))
+
+
+def pkm_query_net(x, weight, B, dim, F, scale, shift, q, status=None, stream=None):
+    """q = (x W^T) * scale + shift in bf16: the query network ahead of the lookup."""
+    return lib().pkm_query_net(_addr(x), _addr(weight), B, dim, F, _addr(scale), _addr(shift),
+                               _addr(q), _addr(status), _stream(stream))
 
 
 def fp8_table_bytes(N, d_v):

@@ -14,6 +14,15 @@ namespace pkm {
 cudaError_t launch_quantize_fp8(const void* values, int value_dtype, int64_t N, int d_v, void* out,
                                 cudaStream_t stream);
 
+// The query network (qnet.cu): per-feature scale / shift of an eval-mode
+// BatchNorm1d, and q = (x W^T) * scale + shift in bf16 on the tensor cores.
+cudaError_t launch_bn_fold(const float* gamma, const float* beta, const float* mean,
+                           const float* var, float eps, int F, float* scale, float* shift,
+                           cudaStream_t stream);
+cudaError_t launch_qnet(const uint16_t* x, const uint16_t* w, int B, int dim, int F,
+                        const float* scale, const float* shift, uint16_t* q, int* status,
+                        cudaStream_t stream);
+
 // Step a6 (value read).  values: [N, d_v] of value_dtype; idx/w: [B, H*k];
 // out: [B, d_v] fp32.  Returns a cudaError_t of the launch.
 cudaError_t launch_gather(const void* values, int value_dtype, int64_t N, int d_v, int B,

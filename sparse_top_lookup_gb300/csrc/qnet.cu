@@ -1,0 +1,315 @@
+// The query network ahead of the lookup: q = BatchNorm1d(x W^T), eval mode.
+//
+// Product-Key Memory, code listing (module setup and forward): the query is
+// an nn.Linear(dim, dim, bias=False) of the layer input followed by an
+// nn.BatchNorm1d, a global constraint on the query distribution.  With H
+// heads of width d_q the Linear maps dim -> F = H * d_q features (one head
+// in the listing).  The listing leaves the BatchNorm mode open; this is the
+// inference form: per feature f, q = (z - mean[f]) / sqrt(var[f] + eps) *
+// gamma[f] + beta[f] with the running statistics, folded into
+// q = z * scale[f] + shift[f] (bn_fold_kernel).
+//
+// GEMM z = x W^T on the tcgen05 tensor cores, bf16 in, fp32 accumulate, one
+// persistent CTA per SM over 128 x 256 output tiles:
+//   warp 0      TMA producer: 128x64 slabs of x and 256x64 slabs of W
+//               (128-byte swizzle) into a 4-stage ring of 48 KB stages;
+//   warp 1      allocates 512 TMEM columns and issues tcgen05.mma
+//               (M=128, N=256, K=16) into one of two 256-column accumulators,
+//               so tile t+1 is multiplied while tile t is written out;
+//   warps 2..5  epilogue, one thread per output row (its TMEM lane): fp32
+//               accumulators -> z * scale + shift -> bf16 (nearest even) ->
+//               64-byte row segments in global memory.
+// Every mbarrier wait is bounded like the lookup kernel's.
+#include <cuda_bf16.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "pkm_internal.cuh"
+#include "tc_common.cuh"
+
+namespace pkm {
+namespace {
+
+using namespace tc;
+
+constexpr int QM = 128;   // rows per tile (MMA M)
+constexpr int QN = 256;   // features per tile (MMA N)
+constexpr int QK = 64;    // bf16 per k-slab: one 128-byte swizzle row
+constexpr int QSTAGES = 4;
+constexpr int QA_BYTES = QM * QK * 2;  // 16 KiB
+constexpr int QB_BYTES = QN * QK * 2;  // 32 KiB
+constexpr int QSTAGE_BYTES = QA_BYTES + QB_BYTES;
+constexpr int QSMEM = QSTAGES * QSTAGE_BYTES + 1024;  // + alignment slack
+constexpr int QTHREADS = 192;
+
+__global__ void bn_fold_kernel(const float* __restrict__ gamma, const float* __restrict__ beta,
+                               const float* __restrict__ mean, const float* __restrict__ var,
+                               float eps, int F, float* __restrict__ scale,
+                               float* __restrict__ shift) {
+  const int f = blockIdx.x * blockDim.x + threadIdx.x;
+  if (f >= F) return;
+  const float s = __fdiv_rn(gamma[f], __fsqrt_rn(var[f] + eps));
+  scale[f] = s;
+  shift[f] = fmaf(-mean[f], s, beta[f]);
+}
+
+__global__ void __launch_bounds__(QTHREADS, 1)
+qnet_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
+            int B, int F, int dim, const float* __restrict__ scale,
+            const float* __restrict__ shift, __nv_bfloat16* __restrict__ q,
+            int* __restrict__ status) {
+  extern __shared__ unsigned char smem_raw[];
+  __shared__ __align__(8) uint64_t bars[2 * QSTAGES + 4 + 1];
+  __shared__ uint32_t s_tmem_base;
+  __shared__ int s_abort;
+
+  const int tm_count = (B + QM - 1) / QM, tn_count = (F + QN - 1) / QN;
+  const int tiles = tm_count * tn_count;
+  const int mine = (int)blockIdx.x < tiles ? (tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  if (mine == 0) return;
+  const int kb_count = (dim + QK - 1) / QK;
+
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t tiles_u32 = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t bar0 = smem_u32(&bars[0]);
+  auto bar_full = [&](uint32_t s) { return bar0 + 8u * s; };
+  auto bar_empty = [&](uint32_t s) { return bar0 + 8u * (QSTAGES + s); };
+  auto bar_tfull = [&](uint32_t b) { return bar0 + 8u * (2 * QSTAGES + b); };
+  auto bar_tempty = [&](uint32_t b) { return bar0 + 8u * (2 * QSTAGES + 2 + b); };
+  const uint32_t bar_done = bar0 + 8u * (2 * QSTAGES + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < QSTAGES; ++s) {
+      mbar_init(bar_full(s), 1);
+      mbar_init(bar_empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_tfull(b), 1);
+      mbar_init(bar_tempty(b), 4);  // one arrival per epilogue warp
+    }
+    mbar_init(bar_done, 1);
+    s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&s_tmem_base)),
+                 "r"(512)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem_base;
+  const Ctl ctl{&s_abort, status};
+  auto tile_of = [&](int i, int& tm, int& tn) {
+    const int t = blockIdx.x + i * gridDim.x;
+    tm = t / tn_count;
+    tn = t - tm * tn_count;
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int i = 0; ok && i < mine; ++i) {
+        int tm, tn;
+        tile_of(i, tm, tn);
+        for (int kb = 0; kb < kb_count; ++kb, ++it) {
+          const uint32_t s = it % QSTAGES, ph = (it / QSTAGES) & 1u;
+          if (!wait_phase(bar_empty(s), ph ^ 1u, ctl)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(bar_full(s), QSTAGE_BYTES);
+          const uint32_t dst = tiles_u32 + s * QSTAGE_BYTES;
+          tma_load_2d(dst, &tmap_x, kb * QK, tm * QM, bar_full(s));
+          tma_load_2d(dst + QA_BYTES, &tmap_w, kb * QK, tn * QN, bar_full(s));
+        }
+      }
+      if (!ok) {  // let the copies already issued land before the CTA exits
+        const uint32_t first = it > (uint32_t)QSTAGES ? it - QSTAGES : 0u;
+        for (uint32_t j = first; j < it; ++j) wait_phase_drain(bar_full(j % QSTAGES), (j / QSTAGES) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(QM, QN);
+      uint32_t it = 0;
+      bool ok = true;
+      for (int i = 0; ok && i < mine; ++i) {
+        const uint32_t buf = i & 1u, use = i >> 1;
+        if (!wait_phase(bar_tempty(buf), (use & 1u) ^ 1u, ctl)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + buf * QN;
+        for (int kb = 0; kb < kb_count; ++kb, ++it) {
+          const uint32_t s = it % QSTAGES, ph = (it / QSTAGES) & 1u;
+          if (!wait_phase(bar_full(s), ph, ctl)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t a_desc = sw128_desc(tiles_u32 + s * QSTAGE_BYTES);
+          const uint64_t b_desc = sw128_desc(tiles_u32 + s * QSTAGE_BYTES + QA_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < QK / 16; ++kk)
+            tc_mma(d_tmem, a_desc + 2u * kk, b_desc + 2u * kk, idesc, (kb | kk) != 0);
+          tc_commit(bar_empty(s));
+        }
+        if (!ok) break;
+        tc_commit(bar_tfull(buf));
+      }
+      tc_commit(bar_done);
+      wait_phase_drain(bar_done, 0);
+    }
+  } else {
+    // ------------------------------------------------ epilogue
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16);
+    for (int i = 0; i < mine; ++i) {
+      int tm, tn;
+      tile_of(i, tm, tn);
+      const uint32_t buf = i & 1u, use = i >> 1;
+      if (!__all_sync(0xffffffffu, wait_phase(bar_tfull(buf), use & 1u, ctl))) break;
+      tc_fence_after();
+      const int b = tm * QM + row;
+      for (int g = 0; g < QN; g += 32) {
+        const int c0 = tn * QN + g;
+        if (c0 >= F) break;  // F is a multiple of 32: a group is all in or all out
+        float v[32];
+        tmem_ld32(lane_addr + buf * QN + g, v);
+        const float4* sc4 = reinterpret_cast<const float4*>(scale + c0);
+        const float4* sh4 = reinterpret_cast<const float4*>(shift + c0);
+        uint32_t packed[16];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float4 a = sc4[j], t = sh4[j];
+          const __nv_bfloat162 lo =
+              __floats2bfloat162_rn(fmaf(v[4 * j], a.x, t.x), fmaf(v[4 * j + 1], a.y, t.y));
+          const __nv_bfloat162 hi =
+              __floats2bfloat162_rn(fmaf(v[4 * j + 2], a.z, t.z), fmaf(v[4 * j + 3], a.w, t.w));
+          packed[2 * j] = *reinterpret_cast<const uint32_t*>(&lo);
+          packed[2 * j + 1] = *reinterpret_cast<const uint32_t*>(&hi);
+        }
+        if (b < B) {
+          uint4* dst = reinterpret_cast<uint4*>(q + (size_t)b * F + c0);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            dst[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_tempty(buf));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512)
+                 : "memory");
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_bn_fold(const float* gamma, const float* beta, const float* mean,
+                           const float* var, float eps, int F, float* scale, float* shift,
+                           cudaStream_t stream) {
+  bn_fold_kernel<<<(F + 255) / 256, 256, 0, stream>>>(gamma, beta, mean, var, eps, F, scale,
+                                                      shift);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_qnet(const uint16_t* x, const uint16_t* w, int B, int dim, int F,
+                        const float* scale, const float* shift, uint16_t* q, int* status,
+                        cudaStream_t stream) {
+  if (B == 0) return cudaSuccess;
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  CUtensorMap mx, mw;
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)dim, (cuuint64_t)B};
+    const cuuint64_t strides[1] = {(cuuint64_t)dim * 2};
+    const cuuint32_t box[2] = {QK, QM};
+    const cuuint32_t es[2] = {1, 1};
+    if (enc(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)dim, (cuuint64_t)F};
+    const cuuint64_t strides[1] = {(cuuint64_t)dim * 2};
+    const cuuint32_t box[2] = {QK, QN};
+    const cuuint32_t es[2] = {1, 1};
+    if (enc(&mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(w), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e =
+        cudaFuncSetAttribute(qnet_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, QSMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int tiles = (B + QM - 1) / QM * ((F + QN - 1) / QN);
+  const int grid = tiles < sm_count() ? tiles : sm_count();
+  qnet_kernel<<<grid, QTHREADS, QSMEM, stream>>>(mx, mw, B, F, dim, scale, shift,
+                                                 reinterpret_cast<__nv_bfloat16*>(q), status);
+  return cudaGetLastError();
+}
+
+}  // namespace pkm
+
+namespace {
+// device status word for pkm_query_net calls that pass none
+__device__ int g_qnet_status;
+
+bool qnet_aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+}  // namespace
+
+extern "C" int pkm_bn_fold(const float* gamma, const float* beta, const float* running_mean,
+                           const float* running_var, float eps, int F, float* scale, float* shift,
+                           void* stream) {
+  if (!gamma || !beta || !running_mean || !running_var || !scale || !shift || F < 1)
+    return PKM_ERR_INVALID;
+  return pkm::launch_bn_fold(gamma, beta, running_mean, running_var, eps, F, scale, shift,
+                             static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PKM_OK
+             : PKM_ERR_CUDA;
+}
+
+extern "C" int pkm_query_net(const void* x, const void* weight, int B, int dim, int F,
+                             const float* scale, const float* shift, void* q, int* status,
+                             void* stream) {
+  if (B < 0 || dim < 1 || F < 1) return PKM_ERR_INVALID;
+  if (dim % 16 || F % 32) return PKM_ERR_UNSUPPORTED;
+  if (B == 0) return PKM_OK;
+  if (!x || !weight || !scale || !shift || !q) return PKM_ERR_INVALID;
+  if (!qnet_aligned16(x) || !qnet_aligned16(weight) || !qnet_aligned16(scale) ||
+      !qnet_aligned16(shift) || !qnet_aligned16(q))
+    return PKM_ERR_ALIGN;
+  int* st = status;
+  if (!st) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_qnet_status) != cudaSuccess) return PKM_ERR_CUDA;
+    st = static_cast<int*>(p);
+  }
+  return pkm::launch_qnet(static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(weight), B,
+                          dim, F, scale, shift, static_cast<uint16_t*>(q), st,
+                          static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PKM_OK
+             : PKM_ERR_CUDA;
+}

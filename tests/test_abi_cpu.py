@@ -103,6 +103,19 @@ def test_fp8_quantiser_rejects_bad_arguments_before_any_cuda_call(L):
     assert pk.fp8_table_bytes(1 << 20, 1024) == (1 << 30) + (1 << 22)
 
 
+def test_query_net_rejects_bad_arguments_before_any_cuda_call(L):
+    Q = L.pkm_query_net
+    assert Q(16, 16, -1, 64, 64, 16, 16, 16, None, None) == pk.PKM_ERR_INVALID
+    assert Q(16, 16, 4, 0, 64, 16, 16, 16, None, None) == pk.PKM_ERR_INVALID
+    assert Q(16, 16, 4, 72, 64, 16, 16, 16, None, None) == pk.PKM_ERR_UNSUPPORTED  # dim % 16
+    assert Q(16, 16, 4, 64, 48, 16, 16, 16, None, None) == pk.PKM_ERR_UNSUPPORTED  # F % 32
+    assert Q(16, 16, 0, 64, 64, 16, 16, 16, None, None) == pk.PKM_OK               # B == 0
+    assert Q(None, 16, 4, 64, 64, 16, 16, 16, None, None) == pk.PKM_ERR_INVALID
+    assert Q(8, 16, 4, 64, 64, 16, 16, 16, None, None) == pk.PKM_ERR_ALIGN
+    assert L.pkm_bn_fold(None, 16, 16, 16, 1e-5, 4, 16, 16, None) == pk.PKM_ERR_INVALID
+    assert L.pkm_bn_fold(16, 16, 16, 16, 1e-5, 0, 16, 16, None) == pk.PKM_ERR_INVALID
+
+
 def test_product_path_refuses_without_library(monkeypatch, tmp_path):
     # No CPU fallback: a missing libpkm.so is an import-time error.
     monkeypatch.setattr(pk, "LIB_PATH", str(tmp_path / "missing.so"))
