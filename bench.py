@@ -144,11 +144,20 @@ def is_fp8(c):
     return c.get("value_format") == "fp8_e4m3"
 
 
+def is_layer(c):
+    """A layer workload starts from the layer input x and runs the query network."""
+    return "qnet_dim" in c
+
+
 def cpu_inputs(c, sample, C=None, V=None):
-    """Inputs of the CPU oracle leg: the first `sample` queries, all tables
-    (an fp8 table quantised by the oracle's own quantiser: codes, scales)."""
+    """Inputs of the CPU oracle leg: the first `sample` queries (or layer
+    inputs), all tables (an fp8 table quantised by the oracle's own
+    quantiser: codes, scales)."""
     import oracle
-    q = synth.queries(c, rows=sample, row_offset=0)
+    if is_layer(c):
+        q = synth.query_net_inputs(c, rows=sample)
+    else:
+        q = synth.queries(c, rows=sample, row_offset=0)
     V = synth.values(c) if V is None else V
     if is_fp8(c):
         V = oracle.quantize_fp8(V, c["n_keys"] ** 2, c["d_v"])
@@ -161,6 +170,11 @@ def cpu_oracle_time(c, inputs, sample, nthreads):
     q, C, V = inputs
     H, d_q, n, d_v, k = c["H"], c["d_q"], c["n_keys"], c["d_v"], c["k"]
     t0 = time.perf_counter()
+    if is_layer(c):
+        x, W, gamma, beta, mean, var = q
+        qf = oracle.query_net(x, W, sample, c["qnet_dim"], H * d_q, gamma, beta, mean, var,
+                              c["bn_eps"], nthreads=nthreads)
+        q = synth.f32_to_bf16(qf.astype(np.float32))
     if is_fp8(c):
         ref = oracle.lookup(q, C, sample, H, d_q, n, k, nthreads=nthreads)
         oracle.gather_fp8(V[0], V[1], n * n, d_v, ref["idx"], ref["w"], nthreads=nthreads)
@@ -208,6 +222,10 @@ def config_json(c, name):
     if is_fp8(c):
         inputs = ("bf16 queries and subkeys, seeded synthetic; value table fp8 e4m3 codes with "
                   "per-row fp32 scales, quantised on the GPU from the seeded bf16 table")
+    if is_layer(c):
+        inputs = ("layer input x [B, %d] bf16 N(0,1); query network weight [H*d_q, %d] bf16 "
+                  "N(0,1/%d) and BatchNorm running statistics; subkeys and values as page; "
+                  "seeded synthetic" % (c["qnet_dim"], c["qnet_dim"], c["qnet_dim"]))
     return {"workload": name, "B": c["B"], "H": c["H"], "d_q": c["d_q"], "n_keys": c["n_keys"],
             "N": c["n_keys"] ** 2, "d_v": c["d_v"], "k": c["k"], "inputs": inputs,
             "l2": "flushed (512 MiB write) between timed steps; value table %.1f GiB"
@@ -231,8 +249,21 @@ def run_ours(args, rank, world, local):
             return torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16)
         return torch.from_numpy(a).cuda()
 
-    q_np, C_np, V_np = synth.queries(c), synth.subkeys(c), synth.values(c)
-    dq, dC, dV = dev(q_np), dev(C_np), dev(V_np)
+    layer = is_layer(c)
+    C_np, V_np = synth.subkeys(c), synth.values(c)
+    dC, dV = dev(C_np), dev(V_np)
+    if layer:
+        # the layer input and the query network; its BatchNorm is folded once
+        dim, F = c["qnet_dim"], H * d_q
+        x_np, W_np, *bn = synth.query_net_inputs(c)
+        dx, dW = dev(x_np), dev(W_np)
+        bn_d = [torch.from_numpy(a).cuda() for a in bn]
+        scale, shift = torch.empty(F, device="cuda"), torch.empty(F, device="cuda")
+        pk.check(pk.pkm_bn_fold(*bn_d, c["bn_eps"], F, scale, shift), "pkm_bn_fold")
+        dq = torch.empty(B, H, d_q, dtype=torch.bfloat16, device="cuda")
+    else:
+        q_np = synth.queries(c)
+        dq = dev(q_np)
     vdt = dt
     if is_fp8(c):
         # the table as stored for the fp8 read: codes then row scales
@@ -248,7 +279,13 @@ def run_ours(args, rank, world, local):
     h = pk.pkm_create(cfg)
     stream = torch.cuda.current_stream()
 
+    def qnet():
+        if layer:
+            pk.check(pk.pkm_query_net(dx, dW, B, dim, F, scale, shift, dq, None, stream),
+                     "pkm_query_net")
+
     def step():
+        qnet()
         pk.check(pk.pkm_lookup(h, dq, dC, B, H, n, k, idx, w, stream), "pkm_lookup")
         pk.check(pk.pkm_gather(h, dV, B, H, n, k, idx, w, out, stream), "pkm_gather")
 
@@ -260,17 +297,19 @@ def run_ours(args, rank, world, local):
     if st != pk.PKM_OK:
         raise RuntimeError("device status after warm-up: %s" % pk.pkm_strerror(st))
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     dist_barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(torch.cuda.current_device()) as clk:
         for i in range(args.steps):
             flush.zero_()
             ev[i][0].record(stream)
-            pk.check(pk.pkm_lookup(h, dq, dC, B, H, n, k, idx, w, stream), "pkm_lookup")
+            qnet()
             ev[i][1].record(stream)
-            pk.check(pk.pkm_gather(h, dV, B, H, n, k, idx, w, out, stream), "pkm_gather")
+            pk.check(pk.pkm_lookup(h, dq, dC, B, H, n, k, idx, w, stream), "pkm_lookup")
             ev[i][2].record(stream)
+            pk.check(pk.pkm_gather(h, dV, B, H, n, k, idx, w, out, stream), "pkm_gather")
+            ev[i][3].record(stream)
         torch.cuda.synchronize()
         # keep sampling clocks long enough to see the load even for short runs
         time.sleep(0.25)
@@ -278,25 +317,45 @@ def run_ours(args, rank, world, local):
     st = pk.pkm_get_status(h)
     if st != pk.PKM_OK:
         raise RuntimeError("device status after timed steps: %s" % pk.pkm_strerror(st))
-    t_lookup = [e[0].elapsed_time(e[1]) for e in ev]
-    t_gather = [e[1].elapsed_time(e[2]) for e in ev]
-    ms_step_local = sum(a + b for a, b in zip(t_lookup, t_gather)) / args.steps
+    t_qnet = [e[0].elapsed_time(e[1]) for e in ev]
+    t_lookup = [e[1].elapsed_time(e[2]) for e in ev]
+    t_gather = [e[2].elapsed_time(e[3]) for e in ev]
+    ms_step_local = sum(e[0].elapsed_time(e[3]) for e in ev) / args.steps
     ms_step = dist_max(ms_step_local, world)
+    ms_qnet = sum(t_qnet) / args.steps
     ms_lookup = sum(t_lookup) / args.steps
     ms_gather = sum(t_gather) / args.steps
 
-    # end to end through the host-buffer entry point: H2D of q, D2H of out
-    q_host = torch.from_numpy(q_np.view(np.int16) if bf16 else q_np).pin_memory()
     out_host = torch.empty(B, d_v).pin_memory()
-    for _ in range(2):
-        pk.check(pk.pkm_forward_host(h, q_host, dC, dV, B, H, n, k, out_host, None, None, stream),
-                 "pkm_forward_host")
     e2e_steps = max(3, min(args.steps, 20))
+    if layer:
+        # end to end through the public calls: x in from pinned host memory,
+        # query network, forward, out back to pinned host memory
+        x_host = torch.from_numpy(x_np.view(np.int16)).pin_memory()
+
+        def e2e_call():
+            dx.view(torch.int16).view(-1).copy_(x_host, non_blocking=True)
+            pk.check(pk.pkm_query_net(dx, dW, B, dim, F, scale, shift, dq, None, stream),
+                     "pkm_query_net")
+            pk.check(pk.pkm_forward(h, dq, dC, dV, B, H, n, k, out, None, None, stream),
+                     "pkm_forward")
+            out_host.copy_(out, non_blocking=True)
+            stream.synchronize()
+        h2d = B * dim * 2
+    else:
+        # end to end through the host-buffer entry point: H2D of q, D2H of out
+        q_host = torch.from_numpy(q_np.view(np.int16) if bf16 else q_np).pin_memory()
+
+        def e2e_call():
+            pk.check(pk.pkm_forward_host(h, q_host, dC, dV, B, H, n, k, out_host, None, None,
+                                         stream), "pkm_forward_host")
+        h2d = B * H * d_q * esz
+    for _ in range(2):
+        e2e_call()
     dist_barrier(world)
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
-        pk.check(pk.pkm_forward_host(h, q_host, dC, dV, B, H, n, k, out_host, None, None, stream),
-                 "pkm_forward_host")
+        e2e_call()
     e2e_s = dist_max((time.perf_counter() - t0) / e2e_steps, world)
     pk.pkm_destroy(h)
 
@@ -313,7 +372,8 @@ def run_ours(args, rank, world, local):
         "scaling": "weak", "vs_baseline": None, "dtype": c["dtype"], "data": "synthetic",
         "config": config_json(c, args.workload),
         "queries_per_s": world * B / (ms_step * 1e-3),
-        "stages_ms": {"lookup": ms_lookup, "gather": ms_gather},
+        "stages_ms": ({"query_net": ms_qnet} if layer else {}) | {"lookup": ms_lookup,
+                                                                  "gather": ms_gather},
         "roofline": {"kernel": "gather_kernel (value read)", "bound": "hbm",
                      "achieved": achieved, "peak": pk_["hbm"], "unit": "GB/s",
                      "frac": achieved / pk_["hbm"], "traffic": traffic,
@@ -323,13 +383,20 @@ def run_ours(args, rank, world, local):
                              "unit": "TFLOP/s", "frac": tflops / pk_["bf16"],
                              "peak_source": pk_["src"] + " bf16 burst"},
         "e2e": {"value": world * B * H / e2e_s, "unit": UNIT,
-                "h2d_bytes_per_step": B * H * d_q * esz, "d2h_bytes_per_step": B * d_v * 4},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": B * d_v * 4},
         # per step: select_tc_kernel and merge_kernel, their retry launches
         # (return at once when no row missed its threshold hint) and
         # gather_kernel (fp32 inputs: lookup_simt_kernel and gather_kernel)
-        "gpu_launches": (5 if bf16 else 2) * args.steps,
+        "gpu_launches": ((5 if bf16 else 2) + (1 if layer else 0)) * args.steps,
         "clocks": clk.summary(),
     }
+    if layer:
+        qflops = 2.0 * B * dim * F
+        line["query_net_roofline"] = {
+            "kernel": "qnet_kernel (x W^T + BatchNorm, tcgen05)", "bound": "tensor",
+            "achieved": qflops / (ms_qnet * 1e-3) / 1e12, "peak": pk_["bf16"], "unit": "TFLOP/s",
+            "frac": qflops / (ms_qnet * 1e-3) / 1e12 / pk_["bf16"],
+            "peak_source": pk_["src"] + " bf16 burst"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         nthreads = os.cpu_count() or 1
         sample = min(args.cpu_sample, B)

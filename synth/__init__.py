@@ -11,8 +11,8 @@ import subprocess
 
 import numpy as np
 
-from .configs import (CONFIGS, TID_KEYS, TID_MIX_MEAN, TID_MIX_PICK, TID_Q, TID_VALUES,
-                      n_rows, seed_of)
+from .configs import (CONFIGS, TID_BN, TID_KEYS, TID_MIX_MEAN, TID_MIX_PICK, TID_Q, TID_QW,
+                      TID_VALUES, TID_X, n_rows, seed_of)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gen.c")
@@ -143,5 +143,24 @@ def value_rows(cfg, rows):
     return out
 
 
+def query_net_inputs(cfg, rows=None, row_offset=0):
+    """Query-network inputs of a layer workload: x [rows, dim] bf16 bits,
+    W [H*d_q, dim] bf16 bits, and the BatchNorm's gamma ~ 1 + N(0, 0.01),
+    beta ~ N(0, 0.01), running mean ~ N(0, 0.0025), running var ~ 1 + |N(0, 0.01)|
+    (fp32, one per feature)."""
+    if isinstance(cfg, str):
+        cfg = CONFIGS[cfg]
+    rows = cfg["B"] if rows is None else rows
+    dim, F, s = cfg["qnet_dim"], cfg["H"] * cfg["d_q"], seed_of(cfg)
+    x = normal(s, TID_X, rows * dim, 1.0, dtype="bf16", offset=row_offset * dim)
+    W = normal(s, TID_QW, F * dim, 1.0 / dim, dtype="bf16")
+    gamma = normal(s, TID_BN, F, 0.01, mean=1.0)
+    beta = normal(s, TID_BN + 1, F, 0.01)
+    mean = normal(s, TID_BN + 2, F, 0.0025)
+    var = (1.0 + np.abs(normal(s, TID_BN + 3, F, 0.01))).astype(np.float32)
+    return x, W, gamma, beta, mean, var
+
+
 __all__ = ["CONFIGS", "build", "normal", "uniform", "mixture_bf16", "f32_to_bf16",
-           "bf16_to_f32", "queries", "subkeys", "values", "value_rows", "seed_of", "n_rows"]
+           "bf16_to_f32", "queries", "subkeys", "values", "value_rows", "seed_of", "n_rows",
+           "query_net_inputs"]

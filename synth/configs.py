@@ -15,6 +15,9 @@ TID_KEYS = 2
 TID_VALUES = 3
 TID_MIX_MEAN = 4
 TID_MIX_PICK = 5
+TID_X = 6            # layer input of the query network
+TID_QW = 7           # query network weight
+TID_BN = 8           # BatchNorm gamma, beta, running mean, running var: 8, 9, 10, 11
 
 CONFIGS = {
     # fp32 everywhere; small enough for brute force over all n_keys**2 keys.
@@ -36,6 +39,12 @@ CONFIGS = {
     "page_fp8": dict(cfg_id=2, B=16384, H=4, d_q=1024, n_keys=1024, d_v=1024, k=32,
                      dtype="bf16", value_format="fp8_e4m3", q_var=1.0, key_var=1.0 / 512,
                      value_var=1.0 / 1024, q_kind="normal"),
+    # the whole layer on page shapes: layer input x [B, dim] -> query network
+    # (Linear dim -> H*d_q, BatchNorm with running statistics) -> lookup -> read.
+    # x ~ N(0, 1), W ~ N(0, 1/dim), so the queries are about N(0, 1) as in page.
+    "page_layer": dict(cfg_id=2, B=16384, H=4, d_q=1024, n_keys=1024, d_v=1024, k=32,
+                       dtype="bf16", q_var=1.0, key_var=1.0 / 512, value_var=1.0 / 1024,
+                       q_kind="normal", qnet_dim=1024, bn_eps=1e-5),
     # 16 GiB value table.
     "large": dict(cfg_id=4, B=32768, H=4, d_q=2048, n_keys=2048, d_v=2048, k=32, dtype="bf16",
                   q_var=1.0, key_var=1.0 / 1024, value_var=1.0 / 2048, q_kind="normal"),
