@@ -45,6 +45,8 @@ def lib():
                                      vp, vp, i32]
         L.oracle_brute_topk.argtypes = [vp, i32, vp, i32, i32, i32, i32, i32, i32, vp, vp, i32]
         L.oracle_quantize_fp8.argtypes = [vp, i32, i64, i32, vp, vp, i32]
+        L.oracle_backward.argtypes = [vp, i32, vp, i32, vp, i32, i32, i32, i32, i32, i32, i32,
+                                      vp, vp, vp, vp, vp, vp, vp]
         L.oracle_query_net.argtypes = [vp, i32, vp, i32, i32, i32, i32, vp, vp, vp, vp,
                                        ctypes.c_double, vp, i32]
         L.oracle_gather_fp8.argtypes = [vp, vp, i64, i32, i32, i32, i32, vp, vp, vp, i32]
@@ -54,7 +56,7 @@ def lib():
         L.oracle_e4m3_encode.restype = ctypes.c_uint8
         for f in (L.oracle_lookup, L.oracle_gather, L.oracle_forward, L.oracle_brute_topk,
                   L.oracle_num_threads, L.oracle_quantize_fp8, L.oracle_gather_fp8,
-                  L.oracle_query_net):
+                  L.oracle_query_net, L.oracle_backward):
             f.restype = i32
         _lib = L
     return _lib
@@ -187,3 +189,22 @@ def query_net(x, weight, B, dim, F, gamma, beta, mean, var, eps, nthreads=0):
     if rc != 0:
         raise ValueError("oracle_query_net: bad shape")
     return q
+
+
+def backward(q, subkeys, values, B, H, d_q, n_keys, d_v, k, idx, w, dout):
+    """Gradients for a fixed selection.  Returns dict(dw, dq, dsubkeys, dvalues)
+    (dvalues dense [n_keys**2, d_v]: small problems only)."""
+    q, subkeys, values = _c(q), _c(subkeys), _c(values)
+    idx = np.ascontiguousarray(idx, np.int64)
+    w = np.ascontiguousarray(w, np.float64)
+    dout = np.ascontiguousarray(dout, np.float64)
+    dw = np.empty((B, H, k), np.float64)
+    dq = np.empty((B, H, d_q), np.float64)
+    dC = np.zeros((H, 2, n_keys, d_q // 2), np.float64)
+    dV = np.zeros((n_keys * n_keys, d_v), np.float64)
+    rc = lib().oracle_backward(_p(q), _dt(q), _p(subkeys), _dt(subkeys), _p(values), _dt(values),
+                               B, H, d_q, n_keys, d_v, k, _p(idx), _p(w), _p(dout), _p(dw),
+                               _p(dq), _p(dC), _p(dV))
+    if rc != 0:
+        raise ValueError("oracle_backward: bad shape or index")
+    return dict(dw=dw, dq=dq, dsubkeys=dC, dvalues=dV)

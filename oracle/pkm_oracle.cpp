@@ -322,6 +322,58 @@ int oracle_gather_fp8(const uint8_t* codes, const float* scales, int64_t N, int 
   return bad ? -1 : 0;
 }
 
+// ---------------------------------------------------------------- backward
+
+// Gradients of the forward pass for a fixed selection (the top-k choices are
+// not differentiated; only the selected scores and rows carry gradient, as
+// in the code listing's autograd through topk, the softmax and the
+// EmbeddingBag read).  Given dout [B, d_v]:
+//   dV[r, :]   += sum over (b,h,j) with idx = r of w[b,h,j] * dout[b, :]
+//   dw[b,h,j]   = dout[b, :] . V[idx[b,h,j], :]
+//   ds[b,h,j]   = w[b,h,j] * (dw[b,h,j] - sum_l w[b,h,l] * dw[b,h,l])      (softmax)
+//   each winner's score is s1[a1] + s2[a2] with a1 = idx / n, a2 = idx % n:
+//   dq[b,h,0:D/2]   += ds * C[h,0,a1,:]      dC[h,0,a1,:] += ds * q[b,h,0:D/2]
+//   dq[b,h,D/2:D]   += ds * C[h,1,a2,:]      dC[h,1,a2,:] += ds * q[b,h,D/2:D]
+// in double.  dq [B,H,d_q] and dw [B,H,k] are overwritten; dC [H,2,n,d_q/2]
+// and dV [n^2, d_v] are added to.  Sequential over queries (the scatters).
+int oracle_backward(const void* q, int qdt, const void* subkeys, int cdt, const void* values,
+                    int vdt, int B, int H, int d_q, int n, int d_v, int k, const int64_t* idx,
+                    const double* w, const double* dout, double* dw, double* dq, double* dC,
+                    double* dV) {
+  if (B < 0 || H < 1 || d_q < 2 || (d_q & 1) || n < 1 || k < 1 || d_v < 1) return -1;
+  const int hd = d_q / 2;
+  const int64_t N = (int64_t)n * n;
+  std::vector<double> ds(k);
+  for (int64_t b = 0; b < B; ++b)
+    for (int h = 0; h < H; ++h) {
+      const int64_t e0 = (b * H + h) * k;
+      double sw = 0.0;
+      for (int j = 0; j < k; ++j) {
+        const int64_t r = idx[e0 + j];
+        if (r < 0 || r >= N) return -1;
+        double acc = 0.0;
+        for (int t = 0; t < d_v; ++t) acc += dout[b * d_v + t] * widen(values, vdt, r * d_v + t);
+        dw[e0 + j] = acc;
+        sw += w[e0 + j] * acc;
+        for (int t = 0; t < d_v; ++t) dV[r * d_v + t] += w[e0 + j] * dout[b * d_v + t];
+      }
+      for (int j = 0; j < k; ++j) ds[j] = w[e0 + j] * (dw[e0 + j] - sw);
+      double* dqb = dq + (b * H + h) * d_q;
+      for (int t = 0; t < d_q; ++t) dqb[t] = 0.0;
+      for (int j = 0; j < k; ++j) {
+        const int64_t a[2] = {idx[e0 + j] / n, idx[e0 + j] % n};
+        for (int half = 0; half < 2; ++half) {
+          const int64_t crow = (((int64_t)h * 2 + half) * n + a[half]) * hd;
+          for (int t = 0; t < hd; ++t) {
+            dqb[half * hd + t] += ds[j] * widen(subkeys, cdt, crow + t);
+            dC[crow + t] += ds[j] * widen(q, qdt, (b * H + h) * d_q + half * hd + t);
+          }
+        }
+      }
+    }
+  return 0;
+}
+
 // ----------------------------------------------------------- query network
 
 // Product-Key Memory, code listing: q = qnorm(query(x)) with query an

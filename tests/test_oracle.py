@@ -432,3 +432,70 @@ def test_query_net_closed_forms():
     a = oracle.query_net(xb, eye, B, dim, dim, g, bt, m, v, 1e-3)
     b = oracle.query_net(xf, eye, B, dim, dim, g, bt, m, v, 1e-3)
     assert (a == b).all()
+
+
+# ------------------------------------------------------------------ backward
+#
+# The forward pass is differentiable for a fixed selection (the code listing's
+# autograd runs through the selected scores, the softmax and the EmbeddingBag
+# read).  The oracle's gradients are pinned by central finite differences of
+# L = sum(dout * out) computed with the oracle's own forward on perturbed
+# inputs, in fp32-exact problems whose selection does not change.
+
+def _loss(q, C, V, B, H, d_q, n, d_v, k, dout):
+    _, _, out = oracle.forward(q, C, V, B, H, d_q, n, d_v, k)
+    return float((out * dout).sum())
+
+
+def test_backward_matches_finite_differences():
+    rng = np.random.default_rng(41)
+    B, H, d_q, n, d_v, k = 3, 2, 8, 6, 5, 4
+    q = rng.standard_normal((B, H, d_q)).astype(np.float32)
+    C = rng.standard_normal((H, 2, n, d_q // 2)).astype(np.float32)
+    V = rng.standard_normal((n * n, d_v)).astype(np.float32)
+    dout = rng.standard_normal((B, d_v))
+    ref = oracle.lookup(q, C, B, H, d_q, n, k, want_gaps=True)
+    assert ref["gap_k"].min() > 1e-3  # the selection is stable under small steps
+    g = oracle.backward(q, C, V, B, H, d_q, n, d_v, k, ref["idx"], ref["w"], dout)
+    eps = 1e-3
+
+    def numeric(arr, pos, fn):
+        a = arr.copy(); a[pos] += eps
+        b = arr.copy(); b[pos] -= eps
+        return (fn(a) - fn(b)) / (2 * eps)
+
+    for pos in [(0, 0, 1), (1, 1, 7), (2, 0, 4)]:
+        num = numeric(q, pos, lambda a: _loss(a, C, V, B, H, d_q, n, d_v, k, dout))
+        assert abs(num - g["dq"][pos]) <= 1e-4 * (1 + abs(num)), (pos, num, g["dq"][pos])
+    used = np.unique(ref["idx"])
+    for r in used[:3]:
+        pos = (int(r), 2)
+        num = numeric(V, pos, lambda a: _loss(q, C, a, B, H, d_q, n, d_v, k, dout))
+        assert abs(num - g["dvalues"][pos]) <= 1e-4 * (1 + abs(num))
+    a1 = int(ref["idx"][0, 0, 0] // n)
+    for pos in [(0, 0, a1, 1), (0, 0, a1, 3)]:
+        num = numeric(C, pos, lambda a: _loss(q, a, V, B, H, d_q, n, d_v, k, dout))
+        assert abs(num - g["dsubkeys"][pos]) <= 1e-4 * (1 + abs(num)), (pos, num)
+    # unselected rows and subkeys get nothing
+    untouched = np.setdiff1d(np.arange(n * n), used)
+    assert (g["dvalues"][untouched] == 0).all()
+
+
+def test_backward_closed_forms():
+    # one selected row (k = 1): w = 1, so ds = 0 and only the read carries
+    # gradient: dV[idx] = dout, dq = 0, dsubkeys = 0, dw = dout . V[idx]
+    rng = np.random.default_rng(42)
+    B, H, d_q, n, d_v = 4, 1, 6, 5, 3
+    q = rng.standard_normal((B, H, d_q)).astype(np.float32)
+    C = rng.standard_normal((H, 2, n, d_q // 2)).astype(np.float32)
+    V = rng.standard_normal((n * n, d_v)).astype(np.float32)
+    dout = rng.standard_normal((B, d_v))
+    ref = oracle.lookup(q, C, B, H, d_q, n, 1)
+    g = oracle.backward(q, C, V, B, H, d_q, n, d_v, 1, ref["idx"], ref["w"], dout)
+    want = np.zeros((n * n, d_v))
+    for b in range(B):
+        want[ref["idx"][b, 0, 0]] += dout[b]
+    np.testing.assert_allclose(g["dvalues"], want, rtol=1e-15)
+    assert (g["dq"] == 0).all() and (g["dsubkeys"] == 0).all()
+    np.testing.assert_allclose(g["dw"][:, 0, 0],
+                               (dout * V[ref["idx"][:, 0, 0]].astype(np.float64)).sum(-1))
