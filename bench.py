@@ -133,15 +133,22 @@ def dist_barrier(world):
         dist.barrier()
 
 
-def workload(name, B=None):
+def workload(name, B=None, n_keys=None):
     c = dict(synth.CONFIGS[name])
     if B is not None:
         c["B"] = B
+    if n_keys is not None:
+        c["n_keys"] = n_keys
     return c
 
 
 def is_fp8(c):
     return c.get("value_format") == "fp8_e4m3"
+
+
+def is_train(c):
+    """A training workload times the forward and the backward pass."""
+    return bool(c.get("train"))
 
 
 def is_layer(c):
@@ -178,6 +185,13 @@ def cpu_oracle_time(c, inputs, sample, nthreads):
     if is_fp8(c):
         ref = oracle.lookup(q, C, sample, H, d_q, n, k, nthreads=nthreads)
         oracle.gather_fp8(V[0], V[1], n * n, d_v, ref["idx"], ref["w"], nthreads=nthreads)
+    elif is_train(c):
+        # forward, then the backward pass for its selection (dvalues formed
+        # for the selected rows only)
+        idx, w, _ = oracle.forward(q, C, V, sample, H, d_q, n, d_v, k, nthreads=nthreads)
+        dout = synth.output_grads(c, rows=sample).astype(np.float64)
+        oracle.backward(q, C, V, sample, H, d_q, n, d_v, k, idx, w, dout,
+                        dvalue_rows=np.unique(idx))
     else:
         oracle.forward(q, C, V, sample, H, d_q, n, d_v, k, nthreads=nthreads)
     return time.perf_counter() - t0
@@ -186,7 +200,7 @@ def cpu_oracle_time(c, inputs, sample, nthreads):
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    c = workload(args.workload, args.batch)
+    c = workload(args.workload, args.batch, args.n_keys)
     nthreads = os.cpu_count() or 1
     sample = min(args.cpu_sample, c["B"])
     inputs = cpu_inputs(c, sample)
@@ -198,8 +212,9 @@ def run_reference(args, rank, world):
     t = sum(ts) / len(ts)
     value = sample * c["H"] / t
     cpu = {"value": value, "unit": UNIT, "cores": nthreads, "kind": "oracle",
-           "sample": "%d of %d queries of the %s workload per step (fp64 oracle forward)"
-                     % (sample, c["B"], args.workload)}
+           "sample": "%d of %d queries of the %s workload per step (fp64 oracle %s)"
+                     % (sample, c["B"], args.workload,
+                        "forward + backward" if is_train(c) else "forward")}
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -222,6 +237,9 @@ def config_json(c, name):
     if is_fp8(c):
         inputs = ("bf16 queries and subkeys, seeded synthetic; value table fp8 e4m3 codes with "
                   "per-row fp32 scales, quantised on the GPU from the seeded bf16 table")
+    if is_train(c):
+        inputs = ("page inputs, seeded synthetic; output gradient dout [B, d_v] fp32 N(0,1); "
+                  "step = forward + backward (dq; dsubkeys and dvalues accumulated in fp32)")
     if is_layer(c):
         inputs = ("layer input x [B, %d] bf16 N(0,1); query network weight [H*d_q, %d] bf16 "
                   "N(0,1/%d) and BatchNorm running statistics; subkeys and values as page; "
@@ -237,7 +255,7 @@ def run_ours(args, rank, world, local):
     import sparse_top_lookup_gb300 as pk
 
     torch.cuda.set_device(local)
-    c = workload(args.workload, args.batch)
+    c = workload(args.workload, args.batch, args.n_keys)
     B, H, d_q, n, d_v, k = (c[x] for x in ("B", "H", "d_q", "n_keys", "d_v", "k"))
     bf16 = c["dtype"] == "bf16"
     dt = pk.PKM_BF16 if bf16 else pk.PKM_F32
@@ -250,6 +268,7 @@ def run_ours(args, rank, world, local):
         return torch.from_numpy(a).cuda()
 
     layer = is_layer(c)
+    train = is_train(c)
     C_np, V_np = synth.subkeys(c), synth.values(c)
     dC, dV = dev(C_np), dev(V_np)
     if layer:
@@ -275,9 +294,29 @@ def run_ours(args, rank, world, local):
     idx = torch.empty(B, H, k, dtype=torch.int64, device="cuda")
     w = torch.empty(B, H, k, device="cuda")
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
-    cfg = pk.make_config(d_q, d_v, B, H, n, k, q_dtype=dt, value_dtype=vdt, host_staging=1)
+    cfg = pk.make_config(d_q, d_v, B, H, n, k, q_dtype=dt, value_dtype=vdt, host_staging=1,
+                         with_backward=int(train))
     h = pk.pkm_create(cfg)
     stream = torch.cuda.current_stream()
+    if train:
+        # the backward pass's buffers: dout in, dw between its two calls,
+        # gradients out (dsubkeys and dvalues accumulate over the steps)
+        dout_np = synth.output_grads(c)
+        g_dout = torch.from_numpy(dout_np).cuda()
+        g_dw = torch.empty(B, H, k, device="cuda")
+        g_q = torch.empty(B, H, d_q, device="cuda")
+        g_C = torch.zeros(H, 2, n, d_q // 2, device="cuda")
+        g_V = torch.zeros(n * n, d_v, device="cuda")
+
+    def backward_read():
+        if train:
+            pk.check(pk.pkm_backward_read(h, dV, B, H, n, k, idx, w, g_dout, g_dw, g_V, stream),
+                     "pkm_backward_read")
+
+    def backward_scores():
+        if train:
+            pk.check(pk.pkm_backward_scores(h, dq, dC, B, H, n, k, idx, w, g_dw, g_q, g_C,
+                                            stream), "pkm_backward_scores")
 
     def qnet():
         if layer:
@@ -288,6 +327,8 @@ def run_ours(args, rank, world, local):
         qnet()
         pk.check(pk.pkm_lookup(h, dq, dC, B, H, n, k, idx, w, stream), "pkm_lookup")
         pk.check(pk.pkm_gather(h, dV, B, H, n, k, idx, w, out, stream), "pkm_gather")
+        backward_read()
+        backward_scores()
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -297,7 +338,7 @@ def run_ours(args, rank, world, local):
     if st != pk.PKM_OK:
         raise RuntimeError("device status after warm-up: %s" % pk.pkm_strerror(st))
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
     dist_barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(torch.cuda.current_device()) as clk:
@@ -310,6 +351,10 @@ def run_ours(args, rank, world, local):
             ev[i][2].record(stream)
             pk.check(pk.pkm_gather(h, dV, B, H, n, k, idx, w, out, stream), "pkm_gather")
             ev[i][3].record(stream)
+            backward_read()
+            ev[i][4].record(stream)
+            backward_scores()
+            ev[i][5].record(stream)
         torch.cuda.synchronize()
         # keep sampling clocks long enough to see the load even for short runs
         time.sleep(0.25)
@@ -320,7 +365,9 @@ def run_ours(args, rank, world, local):
     t_qnet = [e[0].elapsed_time(e[1]) for e in ev]
     t_lookup = [e[1].elapsed_time(e[2]) for e in ev]
     t_gather = [e[2].elapsed_time(e[3]) for e in ev]
-    ms_step_local = sum(e[0].elapsed_time(e[3]) for e in ev) / args.steps
+    ms_bread = sum(e[3].elapsed_time(e[4]) for e in ev) / args.steps
+    ms_bscores = sum(e[4].elapsed_time(e[5]) for e in ev) / args.steps
+    ms_step_local = sum(e[0].elapsed_time(e[5]) for e in ev) / args.steps
     ms_step = dist_max(ms_step_local, world)
     ms_qnet = sum(t_qnet) / args.steps
     ms_lookup = sum(t_lookup) / args.steps
@@ -328,7 +375,23 @@ def run_ours(args, rank, world, local):
 
     out_host = torch.empty(B, d_v).pin_memory()
     e2e_steps = max(3, min(args.steps, 20))
-    if layer:
+    if train:
+        # end to end through the public calls: q and dout in from pinned host
+        # memory, forward, out back, backward (the gradients stay on the device)
+        q_host = torch.from_numpy(q_np.view(np.int16)).pin_memory()
+        dout_host = torch.from_numpy(dout_np).pin_memory()
+
+        def e2e_call():
+            dq.view(torch.int16).view(-1).copy_(q_host.view(-1), non_blocking=True)
+            pk.check(pk.pkm_forward(h, dq, dC, dV, B, H, n, k, out, idx, w, stream),
+                     "pkm_forward")
+            out_host.copy_(out, non_blocking=True)
+            g_dout.copy_(dout_host, non_blocking=True)
+            pk.check(pk.pkm_backward(h, dq, dC, dV, B, H, n, k, idx, w, g_dout, g_q, g_C, g_V,
+                                     stream), "pkm_backward")
+            stream.synchronize()
+        h2d = B * H * d_q * 2 + B * d_v * 4
+    elif layer:
         # end to end through the public calls: x in from pinned host memory,
         # query network, forward, out back to pinned host memory
         x_host = torch.from_numpy(x_np.view(np.int16)).pin_memory()
@@ -366,18 +429,34 @@ def run_ours(args, rank, world, local):
     tflops = flops / (ms_lookup * 1e-3) / 1e12
     value = world * B * H / (ms_step * 1e-3)
     traffic = measured_traffic(args.workload, B)
+    roof = {"kernel": "gather_kernel (value read)", "bound": "hbm",
+            "achieved": achieved, "peak": pk_["hbm"], "unit": "GB/s",
+            "frac": achieved / pk_["hbm"], "traffic": traffic, "peak_source": pk_["src"]}
+    if train:
+        # per distinct selected row: the value row read once and its dvalues
+        # row read and written once (fp32); per selection: idx, w and dw; per
+        # query: dout.  The time is the whole pkm_backward_read call (bucket
+        # count, scan and scatter, then row_grad_kernel).
+        rows_touched = int(torch.unique(idx).numel())
+        bread_bytes = (rows_touched * (value_row_bytes(c) + 8 * d_v) + B * H * k * 16
+                       + B * d_v * 4)
+        bread = bread_bytes / (ms_bread * 1e-3) / 1e9
+        broof = {"kernel": "pkm_backward_read (bucket sort + row_grad_kernel)", "bound": "hbm",
+                 "achieved": bread, "peak": pk_["hbm"], "unit": "GB/s",
+                 "frac": bread / pk_["hbm"], "traffic": None, "peak_source": pk_["src"],
+                 "rows_touched": rows_touched}
+        forward_roof, roof = roof, broof
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": c["dtype"], "data": "synthetic",
         "config": config_json(c, args.workload),
         "queries_per_s": world * B / (ms_step * 1e-3),
-        "stages_ms": ({"query_net": ms_qnet} if layer else {}) | {"lookup": ms_lookup,
-                                                                  "gather": ms_gather},
-        "roofline": {"kernel": "gather_kernel (value read)", "bound": "hbm",
-                     "achieved": achieved, "peak": pk_["hbm"], "unit": "GB/s",
-                     "frac": achieved / pk_["hbm"], "traffic": traffic,
-                     "peak_source": pk_["src"]},
+        "stages_ms": (({"query_net": ms_qnet} if layer else {}) |
+                      {"lookup": ms_lookup, "gather": ms_gather} |
+                      ({"backward_read": ms_bread, "backward_scores": ms_bscores}
+                       if train else {})),
+        "roofline": roof,
         "scoring_roofline": {"kernel": "select_tc_kernel + merge_kernel (a1-a5, one lookup call)",
                              "bound": "tensor", "achieved": tflops, "peak": pk_["bf16"],
                              "unit": "TFLOP/s", "frac": tflops / pk_["bf16"],
@@ -387,9 +466,14 @@ def run_ours(args, rank, world, local):
         # per step: select_tc_kernel and merge_kernel, their retry launches
         # (return at once when no row missed its threshold hint) and
         # gather_kernel (fp32 inputs: lookup_simt_kernel and gather_kernel)
-        "gpu_launches": ((5 if bf16 else 2) + (1 if layer else 0)) * args.steps,
+        # (training: bucket_count, bucket_scan, bucket_scatter, row_grad and
+        # ds_rows kernels too, besides a memset and two cuBLAS GEMM launches)
+        "gpu_launches": ((5 if bf16 else 2) + (1 if layer else 0) + (5 if train else 0))
+        * args.steps,
         "clocks": clk.summary(),
     }
+    if train:
+        line["forward_roofline"] = forward_roof
     if layer:
         qflops = 2.0 * B * dim * F
         line["query_net_roofline"] = {
@@ -403,8 +487,9 @@ def run_ours(args, rank, world, local):
         t = cpu_oracle_time(c, cpu_inputs(c, sample, C=C_np, V=V_np), sample, nthreads)
         line["cpu_baseline"] = {
             "value": sample * H / t, "unit": UNIT, "cores": nthreads, "kind": "oracle",
-            "sample": "%d of %d queries (all %d heads) of the %s workload, fp64 oracle forward"
-                      % (sample, B, H, args.workload)}
+            "sample": "%d of %d queries (all %d heads) of the %s workload, fp64 oracle %s"
+                      % (sample, B, H, args.workload,
+                         "forward + backward" if train else "forward")}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -443,6 +528,8 @@ def main():
     ap.add_argument("--cpu-sample", type=int, default=1024)
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's query count B (profiling runs)")
+    ap.add_argument("--n-keys", type=int, default=None,
+                    help="override the workload's n_keys (small profiling captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

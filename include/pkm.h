@@ -45,14 +45,16 @@
  *
  * Ownership: the caller owns every tensor pointer; nothing is retained after a
  * call returns.  A handle owns only its scratch (device workspace for idx/w
- * when the caller passes NULL, a device status word, and optional staging for
- * pkm_forward_host).  pkm_create is the only call that allocates.
+ * when the caller passes NULL, a device status word, optional staging for
+ * pkm_forward_host, and for pkm_backward a cuBLAS handle and gradient
+ * scratch).  pkm_create is the only call that allocates.
  *
  * Asynchrony: every call enqueues work on `stream` (a cudaStream_t; NULL is
  * the legacy default stream) and returns without synchronising, except
  * pkm_get_status and pkm_forward_host, which synchronise `stream`.  Results are
  * valid once the stream has been synchronised.  Calls on one handle must not
- * overlap on the GPU when they use the handle's scratch (idx/w == NULL).
+ * overlap on the GPU when they use the handle's scratch (idx/w == NULL, and
+ * every pkm_backward).
  *
  * Errors: every call returns PKM_OK (0) or a negative code, checked on the
  * host before anything is launched.  Device-side failures (an out-of-range
@@ -68,7 +70,7 @@
 extern "C" {
 #endif
 
-#define PKM_ABI_VERSION 2
+#define PKM_ABI_VERSION 3
 
 /* element types (PKM_FP8_E4M3: value tables only) */
 enum { PKM_F32 = 0, PKM_BF16 = 1, PKM_FP8_E4M3 = 2 };
@@ -82,11 +84,12 @@ enum {
                                scoring, 64 for fp32), n_keys^2 >= 2^31, d_q or d_v layout */
   PKM_ERR_ALIGN = -4,       /* a tensor pointer not 16-byte aligned */
   PKM_ERR_CUDA = -5,        /* a CUDA runtime call or launch failed */
-  PKM_ERR_NOMEM = -6,       /* pkm_create could not allocate its scratch */
+  PKM_ERR_NOMEM = -6,       /* pkm_create could not allocate its scratch (or cuBLAS handle) */
   PKM_ERR_TIMEOUT = -7,     /* device: a bounded wait inside a kernel gave up */
   PKM_ERR_BAD_INDEX = -8,   /* device: a row index outside [0, n_keys^2) reached the value read */
   PKM_ERR_NO_STAGING = -9,  /* pkm_forward_host on a handle created without host staging */
-  PKM_ERR_OPTION = -10      /* pkm_set_option: unknown option or value */
+  PKM_ERR_OPTION = -10,     /* pkm_set_option: unknown option or value */
+  PKM_ERR_NO_BACKWARD = -11 /* pkm_backward on a handle created without with_backward */
 };
 
 /* options of pkm_set_option */
@@ -110,14 +113,21 @@ typedef struct pkm_handle *pkm_t;
  * Fixed shape of a handle.  d_q: query width per head (even; a multiple of 16
  * for bf16).  d_v: value row width (d_v * element size a multiple of 16
  * bytes; a multiple of 16 for PKM_FP8_E4M3).  max_*: the largest B, H,
- * n_keys and k any call will pass (sizes the scratch).  host_staging: nonzero to also allocate device staging for
- * pkm_forward_host (max_B queries and outputs).
+ * n_keys and k any call will pass (sizes the scratch).  host_staging:
+ * nonzero to also allocate device staging for pkm_forward_host (max_B
+ * queries and outputs).  with_backward: nonzero to also allocate what
+ * pkm_backward needs (bf16 queries and subkeys, bf16 or fp32 values): a
+ * cuBLAS handle with a 32 MiB workspace and scratch for the gradients
+ * (about 4 * max_B * max_H * (max_k + max_n_keys) bytes, or 24 * max_B *
+ * max_H * max_k + max_n_keys^2 / 32 if larger); max_B * max_H * max_k and
+ * max_B * d_v / 4 must stay below 2^31.
  */
 typedef struct {
   int d_q, d_v;
   int max_B, max_H, max_n_keys, max_k;
   int q_dtype, key_dtype, value_dtype;
   int host_staging;
+  int with_backward;
 } pkm_config;
 
 /* Allocate a handle on the current CUDA device.  *out is set only on success. */
@@ -213,6 +223,50 @@ int pkm_abi_version(void);
 #define PKM_STATIC_MAX_PAIRS (1 << 16)
 int pkm_lookup_static(const void *q, const void *subkeys, int B, int H, int d_q, int n_keys, int k,
                       int64_t *idx, float *w, int *status, void *stream);
+
+/*
+ * Backward pass of pkm_forward for the selection it made (the top-k choices
+ * are not differentiated: gradient flows through the selected scores, the
+ * softmax and the weighted read, as autograd does through the page's code
+ * listing).  Inputs: the forward's q, subkeys and values (bf16 queries and
+ * subkeys; bf16 or fp32 values), its idx and w, and dout [B, d_v] fp32 (the
+ * gradient of out).  Outputs, fp32 device arrays:
+ *   dq        [B, H, d_q]              overwritten;
+ *   dsubkeys  [H, 2, n_keys, d_q/2]    added to (zero it first, or accumulate);
+ *   dvalues   [n_keys^2, d_v]          added to (only the selected rows change).
+ * With dw = dout . V[idx] and ds = w * (dw - sum(w * dw)): dvalues[idx] +=
+ * w * dout; dq and dsubkeys take ds through each winner's two subkeys.  The
+ * per-subkey score gradients are rounded to bf16 for the two tensor-core
+ * products (cuBLAS) that form dq and dsubkeys; dvalues and dw are fp32.
+ * Requires a handle created with with_backward (else PKM_ERR_NO_BACKWARD).
+ * Enqueued on `stream`; an index outside [0, n_keys^2) sets
+ * PKM_ERR_BAD_INDEX in the status word and contributes nothing.
+ * pkm_backward = pkm_backward_read then pkm_backward_scores, with dw kept in
+ * the handle's scratch.
+ */
+int pkm_backward(pkm_t h, const void *q, const void *subkeys, const void *values, int B, int H,
+                 int n_keys, int k, const int64_t *idx, const float *w, const float *dout,
+                 float *dq, float *dsubkeys, float *dvalues, void *stream);
+
+/*
+ * The read's part of the backward pass: dw [B, H, k] fp32 = dout[b] . V[idx]
+ * (overwritten; the gradient of the softmax weights) and dvalues[idx] +=
+ * w * dout[b].  The selections are grouped by value row first, so each
+ * selected row of values and dvalues is read (and written) once; a row's
+ * additions are fp32 and their order may vary between runs.  Requires
+ * with_backward (its scratch).
+ */
+int pkm_backward_read(pkm_t h, const void *values, int B, int H, int n_keys, int k,
+                      const int64_t *idx, const float *w, const float *dout, float *dw,
+                      float *dvalues, void *stream);
+
+/*
+ * The scores' part of the backward pass, from w and dw: dq overwritten,
+ * dsubkeys added to, as in pkm_backward.  Requires with_backward.
+ */
+int pkm_backward_scores(pkm_t h, const void *q, const void *subkeys, int B, int H, int n_keys,
+                        int k, const int64_t *idx, const float *w, const float *dw, float *dq,
+                        float *dsubkeys, void *stream);
 
 /*
  * Quantise a value table to the PKM_FP8_E4M3 layout above.  values: [N, d_v]

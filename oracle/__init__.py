@@ -46,7 +46,7 @@ def lib():
         L.oracle_brute_topk.argtypes = [vp, i32, vp, i32, i32, i32, i32, i32, i32, vp, vp, i32]
         L.oracle_quantize_fp8.argtypes = [vp, i32, i64, i32, vp, vp, i32]
         L.oracle_backward.argtypes = [vp, i32, vp, i32, vp, i32, i32, i32, i32, i32, i32, i32,
-                                      vp, vp, vp, vp, vp, vp, vp]
+                                      vp, vp, vp, vp, vp, vp, vp, vp]
         L.oracle_query_net.argtypes = [vp, i32, vp, i32, i32, i32, i32, vp, vp, vp, vp,
                                        ctypes.c_double, vp, i32]
         L.oracle_gather_fp8.argtypes = [vp, vp, i64, i32, i32, i32, i32, vp, vp, vp, i32]
@@ -191,9 +191,11 @@ def query_net(x, weight, B, dim, F, gamma, beta, mean, var, eps, nthreads=0):
     return q
 
 
-def backward(q, subkeys, values, B, H, d_q, n_keys, d_v, k, idx, w, dout):
-    """Gradients for a fixed selection.  Returns dict(dw, dq, dsubkeys, dvalues)
-    (dvalues dense [n_keys**2, d_v]: small problems only)."""
+def backward(q, subkeys, values, B, H, d_q, n_keys, d_v, k, idx, w, dout, dvalue_rows=None):
+    """Gradients for a fixed selection.  Returns dict(dw, dq, dsubkeys, dvalues):
+    dvalues dense [n_keys**2, d_v] (small problems only), or, with
+    dvalue_rows (a list of distinct table rows), [len(dvalue_rows), d_v]
+    holding those rows' sums."""
     q, subkeys, values = _c(q), _c(subkeys), _c(values)
     idx = np.ascontiguousarray(idx, np.int64)
     w = np.ascontiguousarray(w, np.float64)
@@ -201,10 +203,17 @@ def backward(q, subkeys, values, B, H, d_q, n_keys, d_v, k, idx, w, dout):
     dw = np.empty((B, H, k), np.float64)
     dq = np.empty((B, H, d_q), np.float64)
     dC = np.zeros((H, 2, n_keys, d_q // 2), np.float64)
-    dV = np.zeros((n_keys * n_keys, d_v), np.float64)
+    slot = None
+    if dvalue_rows is None:
+        dV = np.zeros((n_keys * n_keys, d_v), np.float64)
+    else:
+        rows = np.asarray(dvalue_rows, np.int64)
+        slot = np.full(n_keys * n_keys, -1, np.int64)
+        slot[rows] = np.arange(len(rows))
+        dV = np.zeros((len(rows), d_v), np.float64)
     rc = lib().oracle_backward(_p(q), _dt(q), _p(subkeys), _dt(subkeys), _p(values), _dt(values),
                                B, H, d_q, n_keys, d_v, k, _p(idx), _p(w), _p(dout), _p(dw),
-                               _p(dq), _p(dC), _p(dV))
+                               _p(dq), _p(dC), _p(dV), None if slot is None else _p(slot))
     if rc != 0:
         raise ValueError("oracle_backward: bad shape or index")
     return dict(dw=dw, dq=dq, dsubkeys=dC, dvalues=dV)

@@ -335,11 +335,13 @@ int oracle_gather_fp8(const uint8_t* codes, const float* scales, int64_t N, int 
 //   dq[b,h,0:D/2]   += ds * C[h,0,a1,:]      dC[h,0,a1,:] += ds * q[b,h,0:D/2]
 //   dq[b,h,D/2:D]   += ds * C[h,1,a2,:]      dC[h,1,a2,:] += ds * q[b,h,D/2:D]
 // in double.  dq [B,H,d_q] and dw [B,H,k] are overwritten; dC [H,2,n,d_q/2]
-// and dV [n^2, d_v] are added to.  Sequential over queries (the scatters).
+// and dV are added to: dV is [n^2, d_v], or with dv_slot given, one row per
+// table row r whose dv_slot[r] >= 0 (at that row; other rows' sums are not
+// formed).  Sequential over queries (the scatters).
 int oracle_backward(const void* q, int qdt, const void* subkeys, int cdt, const void* values,
                     int vdt, int B, int H, int d_q, int n, int d_v, int k, const int64_t* idx,
                     const double* w, const double* dout, double* dw, double* dq, double* dC,
-                    double* dV) {
+                    double* dV, const int64_t* dv_slot) {
   if (B < 0 || H < 1 || d_q < 2 || (d_q & 1) || n < 1 || k < 1 || d_v < 1) return -1;
   const int hd = d_q / 2;
   const int64_t N = (int64_t)n * n;
@@ -355,7 +357,10 @@ int oracle_backward(const void* q, int qdt, const void* subkeys, int cdt, const 
         for (int t = 0; t < d_v; ++t) acc += dout[b * d_v + t] * widen(values, vdt, r * d_v + t);
         dw[e0 + j] = acc;
         sw += w[e0 + j] * acc;
-        for (int t = 0; t < d_v; ++t) dV[r * d_v + t] += w[e0 + j] * dout[b * d_v + t];
+        // dv_slot (optional): the dV row each table row accumulates into, -1 for none
+        const int64_t slot = dv_slot ? dv_slot[r] : r;
+        if (slot >= 0)
+          for (int t = 0; t < d_v; ++t) dV[slot * d_v + t] += w[e0 + j] * dout[b * d_v + t];
       }
       for (int j = 0; j < k; ++j) ds[j] = w[e0 + j] * (dw[e0 + j] - sw);
       double* dqb = dq + (b * H + h) * d_q;

@@ -17,21 +17,22 @@ PKM_F32, PKM_BF16, PKM_FP8_E4M3 = 0, 1, 2
 PKM_OK = 0
 PKM_ERR_INVALID, PKM_ERR_RANGE, PKM_ERR_UNSUPPORTED, PKM_ERR_ALIGN = -1, -2, -3, -4
 PKM_ERR_CUDA, PKM_ERR_NOMEM, PKM_ERR_TIMEOUT, PKM_ERR_BAD_INDEX = -5, -6, -7, -8
-PKM_ERR_NO_STAGING, PKM_ERR_OPTION = -9, -10
+PKM_ERR_NO_STAGING, PKM_ERR_OPTION, PKM_ERR_NO_BACKWARD = -9, -10, -11
 PKM_OPT_HINT_Z, PKM_OPT_HOST_CHUNKS = 1, 2
 PKM_HOST_MAX_CHUNKS = 16
 
 EXPORTED = ["pkm_create", "pkm_destroy", "pkm_forward", "pkm_lookup", "pkm_gather",
             "pkm_forward_host", "pkm_get_status", "pkm_check_args", "pkm_strerror",
             "pkm_abi_version", "pkm_set_option", "pkm_get_fallback_count", "pkm_lookup_static",
-            "pkm_quantize_values_fp8", "pkm_bn_fold", "pkm_query_net"]
+            "pkm_quantize_values_fp8", "pkm_bn_fold", "pkm_query_net", "pkm_backward", "pkm_backward_read",
+            "pkm_backward_scores"]
 PKM_STATIC_MAX_PAIRS = 1 << 16
 
 
 class pkm_config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in
                 ("d_q", "d_v", "max_B", "max_H", "max_n_keys", "max_k", "q_dtype", "key_dtype",
-                 "value_dtype", "host_staging")]
+                 "value_dtype", "host_staging", "with_backward")]
 
 
 class PkmError(RuntimeError):
@@ -76,10 +77,14 @@ def lib():
         L.pkm_quantize_values_fp8.argtypes = [vp, i32, ctypes.c_int64, i32, vp, vp]
         L.pkm_bn_fold.argtypes = [vp, vp, vp, vp, ctypes.c_float, i32, vp, vp, vp]
         L.pkm_query_net.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp, vp, vp]
+        L.pkm_backward.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]
+        L.pkm_backward_read.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
+        L.pkm_backward_scores.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
         for f in ("pkm_create", "pkm_forward", "pkm_lookup", "pkm_gather", "pkm_forward_host",
                   "pkm_get_status", "pkm_check_args", "pkm_abi_version", "pkm_set_option",
                   "pkm_get_fallback_count", "pkm_lookup_static", "pkm_quantize_values_fp8",
-                  "pkm_bn_fold", "pkm_query_net"):
+                  "pkm_bn_fold", "pkm_query_net", "pkm_backward", "pkm_backward_read",
+                  "pkm_backward_scores"):
             getattr(L, f).restype = i32
         _lib = L
     return _lib
@@ -108,11 +113,11 @@ def _stream(s):
 
 
 def make_config(d_q, d_v, max_B, max_H, max_n_keys, max_k, q_dtype=PKM_BF16, key_dtype=None,
-                value_dtype=None, host_staging=0):
+                value_dtype=None, host_staging=0, with_backward=0):
     key_dtype = q_dtype if key_dtype is None else key_dtype
     value_dtype = q_dtype if value_dtype is None else value_dtype
     return pkm_config(d_q, d_v, max_B, max_H, max_n_keys, max_k, q_dtype, key_dtype, value_dtype,
-                      int(bool(host_staging)))
+                      int(bool(host_staging)), int(bool(with_backward)))
 
 
 def pkm_strerror(code):
@@ -152,6 +157,27 @@ def pkm_lookup(h, q, subkeys, B, H, n_keys, k, idx, w, stream=None):
 def pkm_gather(h, values, B, H, n_keys, k, idx, w, out, stream=None):
     return lib().pkm_gather(h, _addr(values), B, H, n_keys, k, _addr(idx), _addr(w), _addr(out),
                             _stream(stream))
+
+
+def pkm_backward(h, q, subkeys, values, B, H, n_keys, k, idx, w, dout, dq, dsubkeys, dvalues,
+                 stream=None):
+    """Gradients of pkm_forward for its selection: dq overwritten, dsubkeys and dvalues added to."""
+    return lib().pkm_backward(h, _addr(q), _addr(subkeys), _addr(values), B, H, n_keys, k,
+                              _addr(idx), _addr(w), _addr(dout), _addr(dq), _addr(dsubkeys),
+                              _addr(dvalues), _stream(stream))
+
+
+def pkm_backward_read(h, values, B, H, n_keys, k, idx, w, dout, dw, dvalues, stream=None):
+    """dw = dout . V[idx] (overwritten) and dvalues[idx] += w * dout."""
+    return lib().pkm_backward_read(h, _addr(values), B, H, n_keys, k, _addr(idx), _addr(w),
+                                   _addr(dout), _addr(dw), _addr(dvalues), _stream(stream))
+
+
+def pkm_backward_scores(h, q, subkeys, B, H, n_keys, k, idx, w, dw, dq, dsubkeys, stream=None):
+    """dq (overwritten) and dsubkeys (added to) from the weights and their gradient dw."""
+    return lib().pkm_backward_scores(h, _addr(q), _addr(subkeys), B, H, n_keys, k, _addr(idx),
+                                     _addr(w), _addr(dw), _addr(dq), _addr(dsubkeys),
+                                     _stream(stream))
 
 
 def pkm_forward_host(h, q_host, subkeys, values, B, H, n_keys, k, out_host, idx_host=None,

@@ -14,7 +14,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpkm.so")
 SOURCES = ["pkm_api.cu", "gather.cu", "lookup_simt.cu", "lookup_tc.cu", "lookup_merge.cu",
-           "pkm_static.cu", "values_fp8.cu", "qnet.cu"]
+           "pkm_static.cu", "values_fp8.cu", "qnet.cu", "backward.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -64,7 +64,7 @@ def build(force=False, verbose=False, ptxas_info=False):
                 sys.stderr.write(err)
     tmp = LIB + ".tmp%d" % os.getpid()
     cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + [o for o, _ in results] + [
-        "-cudart", "shared", "-Xlinker", "-rpath," + _cuda_lib_dir()]
+        "-cudart", "shared", "-lcublas", "-Xlinker", "-rpath," + _cuda_lib_dir()]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s\n%s" % (r.stdout, r.stderr))

@@ -16,6 +16,9 @@ struct pkm_handle {
   int* retry_counts;  // [2 + units]: pairs of the last bf16 lookup that needed the retry,
                       // units retried, then the per-unit flags (units = retry_units(max_B, max_H))
   int* unit_list;     // [units]
+  cublasHandle_t blas;  // with_backward: dq / dsubkeys products
+  void* blas_ws;        // its workspace
+  void* bwd_ws;         // with_backward: dw and score-gradient rows
   float* list_v;     // [max_B * max_H * 2 * 32] per-half lists between the two bf16 kernels
   unsigned short* list_c;
   float hint_z;      // selection threshold hint override (NaN: automatic)
@@ -32,6 +35,8 @@ struct pkm_handle {
 
 namespace {
 
+constexpr size_t kBlasWorkspace = 32u << 20;  // cuBLAS workspace of a with_backward handle
+
 int elem_size(int dtype) { return dtype == PKM_FP8_E4M3 ? 1 : dtype == PKM_BF16 ? 2 : 4; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -45,6 +50,10 @@ int check_config(const pkm_config* c) {
   if (c->value_dtype != PKM_F32 && c->value_dtype != PKM_BF16 && c->value_dtype != PKM_FP8_E4M3)
     return PKM_ERR_UNSUPPORTED;
   if (c->q_dtype != c->key_dtype) return PKM_ERR_UNSUPPORTED;
+  if (c->with_backward && (c->q_dtype != PKM_BF16 || c->value_dtype == PKM_FP8_E4M3 ||
+                          (int64_t)c->max_B * c->max_H * c->max_k > INT32_MAX ||
+                          (int64_t)c->max_B * c->d_v / 4 > INT32_MAX))
+    return PKM_ERR_UNSUPPORTED;
   if ((int64_t)c->d_v * elem_size(c->value_dtype) % 16) return PKM_ERR_UNSUPPORTED;
   if ((int64_t)c->d_v * elem_size(c->value_dtype) / 16 > pkm::kGatherMaxVecPerRow)
     return PKM_ERR_UNSUPPORTED;
@@ -111,6 +120,7 @@ const char* pkm_strerror(int code) {
     case PKM_ERR_BAD_INDEX: return "row index outside the value table";
     case PKM_ERR_NO_STAGING: return "handle was created without host staging";
     case PKM_ERR_OPTION: return "unknown option or value";
+    case PKM_ERR_NO_BACKWARD: return "handle was created without with_backward";
     default: return "unknown error code";
   }
 }
@@ -128,6 +138,9 @@ void pkm_destroy(pkm_t h) {
   cudaFree(h->unit_list);
   cudaFree(h->list_v);
   cudaFree(h->list_c);
+  if (h->blas) cublasDestroy(h->blas);
+  cudaFree(h->blas_ws);
+  cudaFree(h->bwd_ws);
   cudaFree(h->stage_q);
   cudaFree(h->stage_out);
   cudaFree(h->stage_idx);
@@ -190,6 +203,14 @@ int pkm_create(pkm_t* out, const pkm_config* cfg) {
            cudaEventCreateWithFlags(&h->ev_comp[i], cudaEventDisableTiming) == cudaSuccess;
     h->host_chunks = 4;
   }
+  if (ok && cfg->with_backward) {
+    const size_t ws = pkm::backward_workspace_bytes(cfg->max_B, cfg->max_H, cfg->max_n_keys,
+                                                    cfg->max_k);
+    ok = cudaMalloc(&h->bwd_ws, ws ? ws : 256) == cudaSuccess &&
+         cudaMalloc(&h->blas_ws, kBlasWorkspace) == cudaSuccess &&
+         cublasCreate(&h->blas) == CUBLAS_STATUS_SUCCESS &&
+         cublasSetWorkspace(h->blas, h->blas_ws, kBlasWorkspace) == CUBLAS_STATUS_SUCCESS;
+  }
   if (!ok) {
     cudaGetLastError();
     pkm_destroy(h);
@@ -239,6 +260,65 @@ int pkm_forward(pkm_t h, const void* q, const void* subkeys, const void* values,
   rc = run_lookup(h, q, subkeys, B, H, n_keys, k, idx, w, s);
   if (rc) return rc;
   return run_gather(h, values, B, H, n_keys, k, idx, w, out, s);
+}
+
+// The part of a handle's backward scratch the read and score parts take in turn.
+static void* backward_region(pkm_t h) {
+  return static_cast<unsigned char*>(h->bwd_ws) +
+         pkm::backward_dw_bytes(h->cfg.max_B, h->cfg.max_H, h->cfg.max_k);
+}
+
+int pkm_backward_read(pkm_t h, const void* values, int B, int H, int n_keys, int k,
+                      const int64_t* idx, const float* w, const float* dout, float* dw,
+                      float* dvalues, void* stream) {
+  if (!h) return PKM_ERR_INVALID;
+  int rc = check_call(&h->cfg, B, H, n_keys, k);
+  if (rc) return rc;
+  if (!h->cfg.with_backward) return PKM_ERR_NO_BACKWARD;
+  if (B == 0) return PKM_OK;
+  if (!values || !idx || !w || !dout || !dw || !dvalues) return PKM_ERR_INVALID;
+  for (const void* p : {values, (const void*)idx, (const void*)w, (const void*)dout,
+                        (const void*)dw, (const void*)dvalues})
+    if (!aligned16(p)) return PKM_ERR_ALIGN;
+  return cuda_rc(pkm::launch_backward_read(values, h->cfg.value_dtype, B, H, n_keys,
+                                           h->cfg.d_v, k, idx, w, dout, dw, dvalues,
+                                           backward_region(h), h->status,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
+int pkm_backward_scores(pkm_t h, const void* q, const void* subkeys, int B, int H, int n_keys,
+                        int k, const int64_t* idx, const float* w, const float* dw, float* dq,
+                        float* dsubkeys, void* stream) {
+  if (!h) return PKM_ERR_INVALID;
+  int rc = check_call(&h->cfg, B, H, n_keys, k);
+  if (rc) return rc;
+  if (!h->cfg.with_backward) return PKM_ERR_NO_BACKWARD;
+  if (B == 0) return PKM_OK;
+  if (!q || !subkeys || !idx || !w || !dw || !dq || !dsubkeys) return PKM_ERR_INVALID;
+  for (const void* p : {q, subkeys, (const void*)idx, (const void*)w, (const void*)dw,
+                        (const void*)dq, (const void*)dsubkeys})
+    if (!aligned16(p)) return PKM_ERR_ALIGN;
+  return cuda_rc(pkm::launch_backward_scores(
+      h->blas, static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(subkeys), B, H,
+      h->cfg.d_q, n_keys, k, idx, w, dw, dq, dsubkeys, backward_region(h), h->blas_ws,
+      kBlasWorkspace,
+      static_cast<cudaStream_t>(stream)));
+}
+
+int pkm_backward(pkm_t h, const void* q, const void* subkeys, const void* values, int B, int H,
+                 int n_keys, int k, const int64_t* idx, const float* w, const float* dout,
+                 float* dq, float* dsubkeys, float* dvalues, void* stream) {
+  if (!h) return PKM_ERR_INVALID;
+  int rc = check_call(&h->cfg, B, H, n_keys, k);
+  if (rc) return rc;
+  if (!h->cfg.with_backward) return PKM_ERR_NO_BACKWARD;
+  if (B == 0) return PKM_OK;
+  if (!q || !subkeys || !values || !idx || !w || !dout || !dq || !dsubkeys || !dvalues)
+    return PKM_ERR_INVALID;
+  float* dw = static_cast<float*>(h->bwd_ws);
+  rc = pkm_backward_read(h, values, B, H, n_keys, k, idx, w, dout, dw, dvalues, stream);
+  if (rc) return rc;
+  return pkm_backward_scores(h, q, subkeys, B, H, n_keys, k, idx, w, dw, dq, dsubkeys, stream);
 }
 
 int pkm_forward_host(pkm_t h, const void* q_host, const void* subkeys, const void* values, int B,

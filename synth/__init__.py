@@ -12,7 +12,7 @@ import subprocess
 import numpy as np
 
 from .configs import (CONFIGS, TID_BN, TID_KEYS, TID_MIX_MEAN, TID_MIX_PICK, TID_Q, TID_QW,
-                      TID_VALUES, TID_X, n_rows, seed_of)
+                      TID_SEL, TID_VALUES, TID_X, n_rows, seed_of)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gen.c")
@@ -161,6 +161,40 @@ def query_net_inputs(cfg, rows=None, row_offset=0):
     return x, W, gamma, beta, mean, var
 
 
+def selections(cfg, rows=None, row_offset=0):
+    """A stand-in selection for backward-pass inputs, shaped like a lookup's:
+    per (query, head), S = ceil(sqrt(2k)) subkeys drawn uniformly for each
+    half, then k winners, each a uniform pick of one subkey from each half's
+    list (so winners share subkeys, as selected keys do; a winner may repeat,
+    which a lookup never gives but the gradient sums alike), and positive weights
+    summing to 1 (exponential draws, normalised; flat Dirichlet).  Returns
+    (a1, a2, w): [rows, H, k] int64 subkey numbers and float32 weights."""
+    if isinstance(cfg, str):
+        cfg = CONFIGS[cfg]
+    rows = cfg["B"] if rows is None else rows
+    H, n, k, s = cfg["H"], cfg["n_keys"], cfg["k"], seed_of(cfg)
+    S = min(n, int(math.ceil(math.sqrt(2 * k))))
+    P = rows * H
+    lists = uniform(s, TID_SEL, P * 2 * S, offset=row_offset * H * 2 * S).reshape(P, 2, S)
+    lists = np.minimum((lists * n).astype(np.int64), n - 1)
+    pick = uniform(s, TID_SEL + 1, P * 2 * k, offset=row_offset * H * 2 * k).reshape(P, 2, k)
+    pick = np.minimum((pick * S).astype(np.int64), S - 1)
+    a1 = np.take_along_axis(lists[:, 0], pick[:, 0], axis=1)
+    a2 = np.take_along_axis(lists[:, 1], pick[:, 1], axis=1)
+    e = -np.log1p(-uniform(s, TID_SEL + 2, P * k, offset=row_offset * H * k)).reshape(P, k)
+    w = (e / e.sum(1, keepdims=True)).astype(np.float32)
+    return a1.reshape(rows, H, k), a2.reshape(rows, H, k), w.reshape(rows, H, k)
+
+
+def output_grads(cfg, rows=None, row_offset=0):
+    """dout [rows, d_v] float32 ~ N(0, 1): the gradient arriving at the read's output."""
+    if isinstance(cfg, str):
+        cfg = CONFIGS[cfg]
+    rows = cfg["B"] if rows is None else rows
+    d = cfg["d_v"]
+    return normal(seed_of(cfg), TID_SEL + 3, rows * d, 1.0, offset=row_offset * d).reshape(rows, d)
+
+
 __all__ = ["CONFIGS", "build", "normal", "uniform", "mixture_bf16", "f32_to_bf16",
            "bf16_to_f32", "queries", "subkeys", "values", "value_rows", "seed_of", "n_rows",
-           "query_net_inputs"]
+           "query_net_inputs", "selections", "output_grads"]

@@ -18,6 +18,7 @@ TID_MIX_PICK = 5
 TID_X = 6            # layer input of the query network
 TID_QW = 7           # query network weight
 TID_BN = 8           # BatchNorm gamma, beta, running mean, running var: 8, 9, 10, 11
+TID_SEL = 12         # backward inputs: per-half subkey lists, picks, weights, dout: 12 .. 15
 
 CONFIGS = {
     # fp32 everywhere; small enough for brute force over all n_keys**2 keys.
@@ -45,6 +46,12 @@ CONFIGS = {
     "page_layer": dict(cfg_id=2, B=16384, H=4, d_q=1024, n_keys=1024, d_v=1024, k=32,
                        dtype="bf16", q_var=1.0, key_var=1.0 / 512, value_var=1.0 / 1024,
                        q_kind="normal", qnet_dim=1024, bn_eps=1e-5),
+    # a training step on page shapes: the forward pass, then the backward
+    # pass for its selection with a seeded output gradient dout ~ N(0, 1)
+    # (dq; dsubkeys and dvalues accumulated in fp32).
+    "page_train": dict(cfg_id=2, B=16384, H=4, d_q=1024, n_keys=1024, d_v=1024, k=32,
+                       dtype="bf16", q_var=1.0, key_var=1.0 / 512, value_var=1.0 / 1024,
+                       q_kind="normal", train=True),
     # 16 GiB value table.
     "large": dict(cfg_id=4, B=32768, H=4, d_q=2048, n_keys=2048, d_v=2048, k=32, dtype="bf16",
                   q_var=1.0, key_var=1.0 / 1024, value_var=1.0 / 2048, q_kind="normal"),

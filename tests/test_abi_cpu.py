@@ -34,8 +34,8 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_abi_version_and_strerror(L):
-    assert pk.pkm_abi_version() == 2
-    for code in range(-10, 1):
+    assert pk.pkm_abi_version() == 3
+    for code in range(-11, 1):
         assert pk.pkm_strerror(code) != "unknown error code"
     assert pk.pkm_strerror(-100) == "unknown error code"
 
@@ -73,6 +73,14 @@ def test_check_args(L):
     c2.value_dtype = 7
     assert pk.pkm_check_args(c2, 1, 1, 64, 1) == pk.PKM_ERR_UNSUPPORTED
     assert L.pkm_check_args(None, 1, 1, 1, 1) == pk.PKM_ERR_INVALID
+    # the backward pass is on the bf16 path, with bf16 or fp32 values
+    assert pk.pkm_check_args(cfg(with_backward=1), 1, 1, 64, 1) == pk.PKM_OK
+    assert pk.pkm_check_args(cfg(with_backward=1, value_dtype=pk.PKM_F32), 1, 1, 64, 1) \
+        == pk.PKM_OK
+    assert pk.pkm_check_args(cfg(with_backward=1, value_dtype=pk.PKM_FP8_E4M3), 1, 1, 64, 1) \
+        == pk.PKM_ERR_UNSUPPORTED
+    assert pk.pkm_check_args(cfg(with_backward=1, q_dtype=pk.PKM_F32), 1, 1, 64, 1) \
+        == pk.PKM_ERR_UNSUPPORTED
 
 
 def test_null_handle_rejected_before_any_cuda_call(L):
@@ -83,6 +91,12 @@ def test_null_handle_rejected_before_any_cuda_call(L):
     assert L.pkm_forward_host(None, 16, 16, 16, 1, 1, 1, 1, 16, None, None, None) \
         == pk.PKM_ERR_INVALID
     assert L.pkm_get_status(None, None) == pk.PKM_ERR_INVALID
+    assert L.pkm_backward(None, 16, 16, 16, 1, 1, 1, 1, 16, 16, 16, 16, 16, 16, None) \
+        == pk.PKM_ERR_INVALID
+    assert L.pkm_backward_read(None, 16, 1, 1, 1, 1, 16, 16, 16, 16, 16, None) \
+        == pk.PKM_ERR_INVALID
+    assert L.pkm_backward_scores(None, 16, 16, 1, 1, 1, 1, 16, 16, 16, 16, 16, None) \
+        == pk.PKM_ERR_INVALID
     L.pkm_destroy(None)
     assert L.pkm_create(None, None) == pk.PKM_ERR_INVALID
     h = vp()

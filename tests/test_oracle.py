@@ -499,3 +499,9 @@ def test_backward_closed_forms():
     assert (g["dq"] == 0).all() and (g["dsubkeys"] == 0).all()
     np.testing.assert_allclose(g["dw"][:, 0, 0],
                                (dout * V[ref["idx"][:, 0, 0]].astype(np.float64)).sum(-1))
+    # the row-subset form of dvalues returns the same rows (in the order asked)
+    rows = [int(ref["idx"][2, 0, 0]), 0, int(ref["idx"][0, 0, 0])]
+    rows = list(dict.fromkeys(rows))
+    g2 = oracle.backward(q, C, V, B, H, d_q, n, d_v, 1, ref["idx"], ref["w"], dout,
+                         dvalue_rows=rows)
+    np.testing.assert_array_equal(g2["dvalues"], want[rows])
