@@ -20,14 +20,21 @@
 //                          list cut into chunks of at most kChunk selections;
 //   bucket_scatter_kernel  selection numbers into their bucket's list;
 //   bucket_sort_kernel     one CTA per item: a counting sort of the chunk by
-//                          row in shared memory, written back in place, and
-//                          the chunk's pieces (up to kPiece selections of one
-//                          row) appended to a global piece list;
-//   row_grad_kernel        persistent, a warp per piece: the value row is read
-//                          once for every dw of the piece and the dV row
-//                          updated once: plain read-modify-write when the row
-//                          has one piece in one item, vector atomic adds
-//                          otherwise.
+//                          row in shared memory, cut into pieces (up to
+//                          kPiece selections of one row), each appended to a
+//                          global list as a 64-byte record (row, count,
+//                          whether the row is shared, and per selection its
+//                          number, dout row and weight);
+//   row_grad_kernel        persistent, 16 warps per SM; each warp walks its
+//                          pieces in segments of kSegW columns through a
+//                          private ring of kRgStages shared-memory stages,
+//                          every lane prefetching (cp.async) and then using
+//                          only its own 4 columns of the value row, of the dV
+//                          row (unless the row is shared) and of the
+//                          selections' dout rows.  The value segment serves
+//                          every dw of the piece, and the dV segment is
+//                          written back once: a plain store when the row has
+//                          one piece in one item, vector atomic adds otherwise.
 // Score part:
 //   ds_rows_kernel         one warp per (query, head, half): softmax backward
 //                          and the dense bf16 DS row (duplicates summed in
@@ -48,34 +55,28 @@ namespace {
 
 constexpr int kRowsPerBucket = 256;  // a row's place in its bucket fits a byte
 constexpr int kChunk = 2048;         // selections one CTA sorts in shared memory
-constexpr int kPiece = 8;            // selections of one row in one warp pass
-constexpr int kReadWarps = 8;
+constexpr int kPiece = 4;            // selections of one row in one warp pass
+constexpr int kReadWarps = 8;        // warps of bucket_sort_kernel
+constexpr int kSegW = 128;           // value-row columns per stage (4 per lane)
+constexpr int kRgWarps = 8;          // warps per CTA of row_grad_kernel (two CTAs per SM)
+constexpr int kRgStages = 4;         // stages per warp
+// a stage: value, dV and kPiece dout regions of [lane][16 bytes]
+constexpr int kStageBytes = 512 * (2 + kPiece);
+
+// One piece of a row's selections (64 bytes): row; m | shared << 8; then per
+// selection g < m its number e, its dout row b and its weight w.
+struct alignas(16) PieceRec {
+  int row, mf, pad0, pad1;
+  int e[kPiece];
+  int b[kPiece];
+  float w[kPiece];
+};
+static_assert(sizeof(PieceRec) == 64 && kPiece == 4, "piece record layout");
 
 __device__ __forceinline__ void red_add4(float* p, float a, float b, float c, float d) {
   asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a),
                "f"(b), "f"(c), "f"(d)
                : "memory");
-}
-
-// Elements 4u .. 4u+3 of value row `row`, widened to fp32.
-template <bool kBf16>
-__device__ __forceinline__ void load4(const void* values, int64_t row, int d_v, int u,
-                                      float (&x)[4]) {
-  if (kBf16) {
-    const uint2 v = __ldg(reinterpret_cast<const uint2*>(
-                              static_cast<const uint16_t*>(values) + row * d_v) + u);
-    x[0] = __uint_as_float(v.x << 16);
-    x[1] = __uint_as_float(v.x & 0xffff0000u);
-    x[2] = __uint_as_float(v.y << 16);
-    x[3] = __uint_as_float(v.y & 0xffff0000u);
-  } else {
-    const float4 v =
-        __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(values) + row * d_v) + u);
-    x[0] = v.x;
-    x[1] = v.y;
-    x[2] = v.z;
-    x[3] = v.w;
-  }
 }
 
 __global__ void bucket_count_kernel(const int64_t* __restrict__ idx, int E, int64_t N,
@@ -163,14 +164,16 @@ __global__ void bucket_scatter_kernel(const int64_t* __restrict__ idx, int E, in
 }
 
 // One CTA per item: the item's selections sorted by row (counting sort in
-// shared memory) and written back in place; each row's run cut into pieces of
-// at most kPiece, appended to the piece list as (row, first, m, atomic).
+// shared memory); each row's run cut into pieces of at most kPiece, each
+// appended to the piece list as a PieceRec.
 __global__ void __launch_bounds__(kReadWarps * 32)
-bucket_sort_kernel(const int64_t* __restrict__ idx, const int4* __restrict__ items,
-                   const int* __restrict__ n_items, int* __restrict__ list,
-                   int4* __restrict__ pieces, int* __restrict__ n_pieces) {
+bucket_sort_kernel(const int64_t* __restrict__ idx, const float* __restrict__ w, int HK,
+                   const int4* __restrict__ items, const int* __restrict__ n_items,
+                   const int* __restrict__ list, PieceRec* __restrict__ pieces,
+                   int* __restrict__ n_pieces) {
   constexpr int R = kRowsPerBucket;
   __shared__ int s_e[kChunk];
+  __shared__ int s_sorted[kChunk];
   __shared__ unsigned char s_r[kChunk];
   __shared__ int s_cnt[R];
   __shared__ int s_start[R + 1];
@@ -227,82 +230,254 @@ bucket_sort_kernel(const int64_t* __restrict__ idx, const int4* __restrict__ ite
     }
   }
   __syncthreads();
-  for (int i = tid; i < len; i += nt) list[it.x + atomicAdd(&s_cnt[s_r[i]], 1)] = s_e[i];
-  for (int r = tid; r < R; r += nt) {
-    const int c = s_start[r + 1] - s_start[r];
-    const int np = s_pstart[r + 1] - s_pstart[r];
-    for (int q = 0; q < np; ++q)
-      pieces[s_base + s_pstart[r] + q] =
-          make_int4((int)(row0 + r), it.x + s_start[r] + q * kPiece, min(kPiece, c - q * kPiece),
-                    !excl || np > 1);
+  for (int i = tid; i < len; i += nt) s_sorted[atomicAdd(&s_cnt[s_r[i]], 1)] = s_e[i];
+  __syncthreads();
+  const int npieces = s_pstart[R];
+  for (int q = tid; q < npieces; q += nt) {
+    int lo = 0, hi = R;  // row of piece q: s_pstart[lo] <= q < s_pstart[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_pstart[mid] <= q)
+        lo = mid;
+      else
+        hi = mid;
+    }
+    const int first = s_start[lo] + (q - s_pstart[lo]) * kPiece;
+    const int m = min(kPiece, s_start[lo + 1] - first);
+    const bool shared = !excl || s_pstart[lo + 1] - s_pstart[lo] > 1;
+    int e[kPiece], b[kPiece];
+    float wt[kPiece];
+#pragma unroll
+    for (int g = 0; g < kPiece; ++g) {
+      e[g] = g < m ? s_sorted[first + g] : 0;
+      b[g] = e[g] / HK;
+      wt[g] = g < m ? __ldg(w + e[g]) : 0.0f;
+    }
+    int4* out = reinterpret_cast<int4*>(pieces + s_base + q);
+    out[0] = make_int4((int)(row0 + lo), m | (shared ? 1 << 8 : 0), 0, 0);
+    out[1] = make_int4(e[0], e[1], e[2], e[3]);
+    out[2] = make_int4(b[0], b[1], b[2], b[3]);
+    out[3] = make_int4(__float_as_int(wt[0]), __float_as_int(wt[1]), __float_as_int(wt[2]),
+                       __float_as_int(wt[3]));
   }
 }
 
-// Persistent; a warp per piece (row, first, m, atomic): the m <= kPiece
-// selections list[first .. first+m) of one value row.  One pass over the
-// row's 4-element units reads the value row once for all m dot products dw
-// and adds sum_g w_g * dout[b_g] into the dV row, by plain read-modify-write
-// (the warp owns the row) or by vector atomic adds.
-template <bool kBf16>
-__global__ void __launch_bounds__(kReadWarps * 32, 4)
-row_grad_kernel(const void* __restrict__ values, int d_v, int HK, const float* __restrict__ w,
-                const float* __restrict__ dout, const int* __restrict__ list,
-                const int4* __restrict__ pieces, const int* __restrict__ n_pieces,
-                float* __restrict__ dw, float* __restrict__ dvalues) {
-  const int lane = threadIdx.x & 31;
-  const int total = *n_pieces;
-  const int nu = d_v >> 2;
-  for (int p = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5); p < total;
-       p += (int)((gridDim.x * blockDim.x) >> 5)) {
-    const int4 pc = pieces[p];
-    const int64_t row = pc.x;
-    const int m = pc.z;
-    const bool atomic = pc.w != 0;
-    const int my_e = lane < m ? list[pc.y + lane] : 0;
-    float wt[kPiece], part[kPiece];
-    int doff[kPiece];  // dout row of each selection, in 16-byte units
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Per stage, written by lane 0 when the stage is issued: the piece's row,
+// m | shared << 8, the segment's first column, whether it is the piece's
+// last segment, and per selection its number and weight.
+struct alignas(16) StageMeta {
+  int row, mf, c0, last;
+  int e[kPiece];
+  float w[kPiece];
+  int pad[4];
+};
+
+// One lane's 4 columns of one segment for a piece of M selections: dot
+// products into part, sum_g w_g * dout[b_g] added to the dV columns (read
+// from the stage, or 0 for atomic adds).
+template <int M, bool kBf16>
+__device__ __forceinline__ void seg_compute(const unsigned char* st, int lane,
+                                            const float (&wt)[kPiece], float (&part)[kPiece],
+                                            bool shared, float* drow) {
+  float x[4];
+  if (kBf16) {
+    const uint2 v = *reinterpret_cast<const uint2*>(st + lane * 16);
+    x[0] = __uint_as_float(v.x << 16);
+    x[1] = __uint_as_float(v.x & 0xffff0000u);
+    x[2] = __uint_as_float(v.y << 16);
+    x[3] = __uint_as_float(v.y & 0xffff0000u);
+  } else {
+    const float4 v = *reinterpret_cast<const float4*>(st + lane * 16);
+    x[0] = v.x;
+    x[1] = v.y;
+    x[2] = v.z;
+    x[3] = v.w;
+  }
+  float4 acc = shared ? make_float4(0.0f, 0.0f, 0.0f, 0.0f)
+                      : *reinterpret_cast<const float4*>(st + 512 + lane * 16);
 #pragma unroll
-    for (int g = 0; g < kPiece; ++g) {
-      const int e = __shfl_sync(0xffffffffu, my_e, g);
-      wt[g] = g < m ? __ldg(w + e) : 0.0f;
-      doff[g] = (e / HK) * nu;
-      part[g] = 0.0f;
+  for (int g = 0; g < M; ++g) {
+    const float4 d = *reinterpret_cast<const float4*>(st + 512 * (2 + g) + lane * 16);
+    part[g] = fmaf(d.x, x[0], part[g]);
+    part[g] = fmaf(d.y, x[1], part[g]);
+    part[g] = fmaf(d.z, x[2], part[g]);
+    part[g] = fmaf(d.w, x[3], part[g]);
+    acc.x = fmaf(wt[g], d.x, acc.x);
+    acc.y = fmaf(wt[g], d.y, acc.y);
+    acc.z = fmaf(wt[g], d.z, acc.z);
+    acc.w = fmaf(wt[g], d.w, acc.w);
+  }
+  if (shared)
+    red_add4(drow, acc.x, acc.y, acc.z, acc.w);
+  else
+    *reinterpret_cast<float4*>(drow) = acc;
+}
+
+// The copies of one lane's 4 columns (column col of row `row`) of a segment
+// into the stage at shared address dst.
+template <int M, bool kBf16>
+__device__ __forceinline__ void seg_issue(uint32_t dst, const void* values, const float* dvalues,
+                                          const float* dout, int64_t row, int d_v, int col,
+                                          const int (&b)[kPiece], bool shared) {
+  const int64_t off = row * d_v + col;
+  if (kBf16)
+    cp_async8(dst, static_cast<const uint16_t*>(values) + off);
+  else
+    cp_async16(dst, static_cast<const float*>(values) + off);
+  if (!shared) cp_async16(dst + 512, dvalues + off);
+#pragma unroll
+  for (int g = 0; g < M; ++g) cp_async16(dst + 512 * (2 + g), dout + (int64_t)b[g] * d_v + col);
+}
+
+// Persistent, kRgWarps warps per CTA, two CTAs per SM.  Warp gw of GW takes
+// pieces gw, gw + GW, ...; each piece is walked in segments of kSegW
+// columns, one stage each, kRgStages - 1 stages ahead of the one computed.
+// Records are fetched 32 at a time (one per lane) and broadcast by shuffles.
+// Lane l copies and uses columns c0 + 4l .. c0 + 4l + 3 of the segment only,
+// so a lane waits for its own copies (cp.async groups) and no data crosses
+// lanes except the dw sums.
+template <bool kBf16>
+__global__ void __launch_bounds__(kRgWarps * 32, 2)
+row_grad_kernel(const void* __restrict__ values, int d_v, const float* __restrict__ dout,
+                const PieceRec* __restrict__ pieces, const int* __restrict__ n_pieces,
+                float* __restrict__ dw, float* __restrict__ dvalues) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  constexpr int S = kRgStages;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned char* ring = smem + warp * S * kStageBytes;
+  StageMeta* meta = reinterpret_cast<StageMeta*>(smem + kRgWarps * S * kStageBytes) + warp * S;
+  const uint32_t ring_s = tc::smem_u32(ring);
+  const int total = *n_pieces;
+  const int GW = gridDim.x * kRgWarps, gw = blockIdx.x * kRgWarps + warp;
+  const int np = gw < total ? (total - gw + GW - 1) / GW : 0;
+  const int nseg = (d_v + kSegW - 1) / kSegW;
+  const int ntask = np * nseg;
+
+  int4 r0 = make_int4(0, 0, 0, 0), r1 = r0, r2 = r0, r3 = r0;  // this lane's record
+  int win = -32;                                                // first piece of the window
+  int pj = -1, ps = 0;                                          // task being issued
+  int irow = 0, im = 0, ishared = 0, ib[kPiece] = {0, 0, 0, 0};
+  int issued = 0;
+
+  auto issue = [&]() {
+    if (issued < ntask) {
+      if (ps == 0) {  // a new piece: its record from the lane that holds it
+        ++pj;
+        if (pj >= win + 32) {
+          win = pj;
+          if (win + lane < np) {
+            const int4* rp =
+                reinterpret_cast<const int4*>(pieces + gw + (int64_t)GW * (win + lane));
+            r0 = rp[0];
+            r1 = rp[1];
+            r2 = rp[2];
+            r3 = rp[3];
+          }
+        }
+        const int hl = pj - win;
+        irow = __shfl_sync(0xffffffffu, r0.x, hl);
+        const int mf = __shfl_sync(0xffffffffu, r0.y, hl);
+        im = mf & 0xff;
+        ishared = mf >> 8;
+        ib[0] = __shfl_sync(0xffffffffu, r2.x, hl);
+        ib[1] = __shfl_sync(0xffffffffu, r2.y, hl);
+        ib[2] = __shfl_sync(0xffffffffu, r2.z, hl);
+        ib[3] = __shfl_sync(0xffffffffu, r2.w, hl);
+        const int e0 = __shfl_sync(0xffffffffu, r1.x, hl), e1 = __shfl_sync(0xffffffffu, r1.y, hl);
+        const int e2 = __shfl_sync(0xffffffffu, r1.z, hl), e3 = __shfl_sync(0xffffffffu, r1.w, hl);
+        const int w0 = __shfl_sync(0xffffffffu, r3.x, hl), w1 = __shfl_sync(0xffffffffu, r3.y, hl);
+        const int w2 = __shfl_sync(0xffffffffu, r3.z, hl), w3 = __shfl_sync(0xffffffffu, r3.w, hl);
+        if (lane == 0) {  // the piece's selections, for every stage of the piece
+          int4* ep = reinterpret_cast<int4*>(meta + issued % S);
+          ep[1] = make_int4(e0, e1, e2, e3);
+          ep[2] = make_int4(w0, w1, w2, w3);
+        }
+      } else if (lane == 0) {
+        const int4* prev = reinterpret_cast<const int4*>(meta + (issued + S - 1) % S);
+        int4* ep = reinterpret_cast<int4*>(meta + issued % S);
+        ep[1] = prev[1];
+        ep[2] = prev[2];
+      }
+      const int st = issued % S;
+      const int c0 = ps * kSegW;
+      if (lane == 0)
+        reinterpret_cast<int4*>(meta + st)[0] =
+            make_int4(irow, im | (ishared << 8), c0, ps == nseg - 1);
+      const int col = c0 + 4 * lane;
+      if (col < d_v) {
+        const uint32_t dst = ring_s + st * kStageBytes + lane * 16;
+        switch (im) {
+          case 1: seg_issue<1, kBf16>(dst, values, dvalues, dout, irow, d_v, col, ib, ishared);
+            break;
+          case 2: seg_issue<2, kBf16>(dst, values, dvalues, dout, irow, d_v, col, ib, ishared);
+            break;
+          case 3: seg_issue<3, kBf16>(dst, values, dvalues, dout, irow, d_v, col, ib, ishared);
+            break;
+          default: seg_issue<4, kBf16>(dst, values, dvalues, dout, irow, d_v, col, ib, ishared);
+            break;
+        }
+      }
+      if (++ps == nseg) ps = 0;
+      ++issued;
     }
-    const float4* d4 = reinterpret_cast<const float4*>(dout);
-    float4* dv = reinterpret_cast<float4*>(dvalues + row * d_v);
-    for (int u = lane; u < nu; u += 32) {
-      float x[4];
-      load4<kBf16>(values, row, d_v, u, x);
-      float4 acc = atomic ? make_float4(0.0f, 0.0f, 0.0f, 0.0f) : dv[u];
+    cp_async_commit();  // one group per slot of the ring, empty ones included
+    __syncwarp();
+  };
+
+  float part[kPiece] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+  for (int i = 0; i < S - 1; ++i) issue();
+  for (int t = 0; t < ntask; ++t) {
+    issue();
+    cp_async_wait<S - 1>();  // this lane's copies of task t have landed
+    const int st = t % S;
+    const int4 h = reinterpret_cast<const int4*>(meta + st)[0];
+    const int m = h.y & 0xff;
+    const bool shared = (h.y >> 8) != 0;
+    const int col = h.z + 4 * lane;
+    if (col < d_v) {
+      const float4 wv = reinterpret_cast<const float4*>(meta + st)[2];
+      const float wt[kPiece] = {wv.x, wv.y, wv.z, wv.w};
+      const unsigned char* base = ring + st * kStageBytes;
+      float* drow = dvalues + (int64_t)h.x * d_v + col;
+      switch (m) {
+        case 1: seg_compute<1, kBf16>(base, lane, wt, part, shared, drow); break;
+        case 2: seg_compute<2, kBf16>(base, lane, wt, part, shared, drow); break;
+        case 3: seg_compute<3, kBf16>(base, lane, wt, part, shared, drow); break;
+        default: seg_compute<4, kBf16>(base, lane, wt, part, shared, drow); break;
+      }
+    }
+    if (h.w) {  // the piece's last segment: its dw
+      const int4 ev = reinterpret_cast<const int4*>(meta + st)[1];
+      const int es[kPiece] = {ev.x, ev.y, ev.z, ev.w};
 #pragma unroll
       for (int g = 0; g < kPiece; ++g) {
         if (g < m) {
-          const float4 d = __ldg(d4 + doff[g] + u);
-          part[g] = fmaf(d.x, x[0], part[g]);
-          part[g] = fmaf(d.y, x[1], part[g]);
-          part[g] = fmaf(d.z, x[2], part[g]);
-          part[g] = fmaf(d.w, x[3], part[g]);
-          acc.x = fmaf(wt[g], d.x, acc.x);
-          acc.y = fmaf(wt[g], d.y, acc.y);
-          acc.z = fmaf(wt[g], d.z, acc.z);
-          acc.w = fmaf(wt[g], d.w, acc.w);
+          float v = part[g];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+          if (lane == g) dw[es[g]] = v;
         }
-      }
-      if (atomic)
-        red_add4(&dv[u].x, acc.x, acc.y, acc.z, acc.w);
-      else
-        dv[u] = acc;
-    }
-#pragma unroll
-    for (int g = 0; g < kPiece; ++g) {
-      if (g < m) {
-        float v = part[g];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == g) dw[my_e] = v;
+        part[g] = 0.0f;
       }
     }
+    __syncwarp();  // the stage's metadata is read before it is reissued
   }
+  cp_async_wait<0>();
 }
 
 // One warp per (query, head, half): ds_j = w_j (dw_j - sum_l w_l dw_l), then
@@ -353,7 +528,7 @@ static size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 // The read part's scratch, each array 256-byte aligned: the item and piece
 // counts and the bucket sizes [nb] (cleared per call, one memset), scatter
 // cursors [nb], the items [max_items], the bucketed selection numbers [E] and
-// the pieces [E].
+// the piece records [E].
 static void read_layout(int64_t N, int64_t E, size_t* off, int64_t* nb_out, int64_t* items_out) {
   const int64_t nb = (N + kRowsPerBucket - 1) / kRowsPerBucket;
   const int64_t items = std::min(nb, E) + E / kChunk + 1;
@@ -363,7 +538,7 @@ static void read_layout(int64_t N, int64_t E, size_t* off, int64_t* nb_out, int6
   off[3] = off[2] + align256(nb * 4);           // items
   off[4] = off[3] + align256(items * 16);       // list
   off[5] = off[4] + align256(E * 4);            // pieces
-  off[6] = off[5] + align256(E * 16);           // end
+  off[6] = off[5] + align256(E * sizeof(PieceRec));  // end
   *nb_out = nb;
   *items_out = items;
 }
@@ -404,7 +579,7 @@ cudaError_t launch_backward_read(const void* values, int value_dtype, int B, int
   int* cursor = reinterpret_cast<int*>(ws + off[2]);
   int4* items = reinterpret_cast<int4*>(ws + off[3]);
   int* list = reinterpret_cast<int*>(ws + off[4]);
-  int4* pieces = reinterpret_cast<int4*>(ws + off[5]);
+  PieceRec* pieces = reinterpret_cast<PieceRec*>(ws + off[5]);
   cudaError_t e = cudaMemsetAsync(ws, 0, off[2], stream);
   if (e != cudaSuccess) return e;
   const int sms = tc::sm_count();
@@ -412,18 +587,22 @@ cudaError_t launch_backward_read(const void* values, int value_dtype, int B, int
   bucket_count_kernel<<<grid, 256, 0, stream>>>(idx, (int)E, N, bcount, dw, status);
   bucket_scan_kernel<<<1, 1024, 0, stream>>>(bcount, (int)nb, cursor, items, n_items);
   bucket_scatter_kernel<<<grid, 256, 0, stream>>>(idx, (int)E, N, cursor, list);
-  bucket_sort_kernel<<<(unsigned)max_items, kReadWarps * 32, 0, stream>>>(idx, items, n_items,
-                                                                           list, pieces, n_pieces);
-  // persistent: 4 CTAs of 8 warps per SM (64 registers a thread), a warp per piece
-  const int grid2 = (int)std::min<int64_t>((E + kReadWarps - 1) / kReadWarps, (int64_t)sms * 4);
-  if (value_dtype == PKM_BF16)
-    row_grad_kernel<true><<<grid2, kReadWarps * 32, 0, stream>>>(values, d_v, H * k, w, dout,
-                                                                 list, pieces, n_pieces, dw,
-                                                                 dvalues);
-  else
-    row_grad_kernel<false><<<grid2, kReadWarps * 32, 0, stream>>>(values, d_v, H * k, w, dout,
-                                                                  list, pieces, n_pieces, dw,
-                                                                  dvalues);
+  bucket_sort_kernel<<<(unsigned)max_items, kReadWarps * 32, 0, stream>>>(
+      idx, w, H * k, items, n_items, list, pieces, n_pieces);
+  const size_t sm = (size_t)kRgWarps * kRgStages * (kStageBytes + sizeof(StageMeta));
+  if (value_dtype == PKM_BF16) {
+    e = cudaFuncSetAttribute(row_grad_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sm);
+    if (e != cudaSuccess) return e;
+    row_grad_kernel<true><<<2 * sms, kRgWarps * 32, sm, stream>>>(values, d_v, dout, pieces,
+                                                                  n_pieces, dw, dvalues);
+  } else {
+    e = cudaFuncSetAttribute(row_grad_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sm);
+    if (e != cudaSuccess) return e;
+    row_grad_kernel<false><<<2 * sms, kRgWarps * 32, sm, stream>>>(values, d_v, dout, pieces,
+                                                                   n_pieces, dw, dvalues);
+  }
   return cudaGetLastError();
 }
 

@@ -54,7 +54,7 @@ def test_reference_arm_runs_on_rank_zero_only(capsys):
     import bench
 
     class A:
-        workload, batch, cpu_sample, steps, warmup = "tiny", None, 8, 1, 0
+        workload, batch, n_keys, cpu_sample, steps, warmup = "tiny", None, None, 8, 1, 0
 
     bench.run_reference(A, rank=1, world=2)
     assert capsys.readouterr().out == ""

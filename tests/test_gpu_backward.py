@@ -68,7 +68,7 @@ def gpu_error_bounds(q64, C64, Vsel, idx, w, dout, dw, n, k, B_gemm):
 
 def dvalue_bound(idx, w, dout, rows):
     """|gpu - exact| bound for dvalues rows of m selections: fused multiply-adds
-    of w * dout into fp32 partial sums of up to 8 selections, each added onto
+    of w * dout into fp32 partial sums of up to 4 selections, each added onto
     the row (at most 2m + 1 roundings, in any order)."""
     slot = {int(r): i for i, r in enumerate(rows)}
     absum = np.zeros((len(rows), dout.shape[1]))
