@@ -46,6 +46,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "pkm_internal.cuh"
 #include "tc_common.cuh"
@@ -55,10 +56,12 @@ namespace {
 
 constexpr int kRowsPerBucket = 256;  // a row's place in its bucket fits a byte
 constexpr int kChunk = 2048;         // selections one CTA sorts in shared memory
-constexpr int kPiece = 4;            // selections of one row in one warp pass
+constexpr int kRec = 4;              // selections a piece record can hold
+constexpr int kPiece = 4;            // selections of one row in one warp pass (<= kRec)
 constexpr int kReadWarps = 8;        // warps of bucket_sort_kernel
 constexpr int kSegW = 128;           // value-row columns per stage (4 per lane)
-constexpr int kRgWarps = 8;          // warps per CTA of row_grad_kernel (two CTAs per SM)
+constexpr int kRgWarps = 8;          // warps per CTA of row_grad_kernel
+constexpr int kRgCtas = 2;           // CTAs of row_grad_kernel per SM
 constexpr int kRgStages = 4;         // stages per warp
 // a stage: value, dV and kPiece dout regions of [lane][16 bytes]
 constexpr int kStageBytes = 512 * (2 + kPiece);
@@ -67,11 +70,24 @@ constexpr int kStageBytes = 512 * (2 + kPiece);
 // selection g < m its number e, its dout row b and its weight w.
 struct alignas(16) PieceRec {
   int row, mf, pad0, pad1;
-  int e[kPiece];
-  int b[kPiece];
-  float w[kPiece];
+  int e[kRec];
+  int b[kRec];
+  float w[kRec];
 };
-static_assert(sizeof(PieceRec) == 64 && kPiece == 4, "piece record layout");
+static_assert(sizeof(PieceRec) == 64 && kRec == 4 && kPiece <= kRec, "piece record layout");
+
+// f(std::integral_constant<int, m>) for the piece size m in 1 .. kPiece.
+template <int M = 1, typename F>
+__device__ __forceinline__ void with_piece_size(int m, F&& f) {
+  if constexpr (M == kPiece) {
+    f(std::integral_constant<int, M>{});
+  } else {
+    if (m == M)
+      f(std::integral_constant<int, M>{});
+    else
+      with_piece_size<M + 1>(m, f);
+  }
+}
 
 __device__ __forceinline__ void red_add4(float* p, float a, float b, float c, float d) {
   asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a),
@@ -245,10 +261,10 @@ bucket_sort_kernel(const int64_t* __restrict__ idx, const float* __restrict__ w,
     const int first = s_start[lo] + (q - s_pstart[lo]) * kPiece;
     const int m = min(kPiece, s_start[lo + 1] - first);
     const bool shared = !excl || s_pstart[lo + 1] - s_pstart[lo] > 1;
-    int e[kPiece], b[kPiece];
-    float wt[kPiece];
+    int e[kRec], b[kRec];
+    float wt[kRec];
 #pragma unroll
-    for (int g = 0; g < kPiece; ++g) {
+    for (int g = 0; g < kRec; ++g) {
       e[g] = g < m ? s_sorted[first + g] : 0;
       b[g] = e[g] / HK;
       wt[g] = g < m ? __ldg(w + e[g]) : 0.0f;
@@ -262,11 +278,33 @@ bucket_sort_kernel(const int64_t* __restrict__ idx, const float* __restrict__ w,
   }
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+// Asynchronous copies global -> shared with an L2 cache policy (createpolicy):
+// the streamed value and dV rows are marked evict-first, the dout rows (re-read
+// for every selection) evict-last, so that dout stays in L2.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint64_t pol) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "l"(pol)
+               : "memory");
 }
-__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src, uint64_t pol) {
+  asm volatile("cp.async.ca.shared.global.L2::cache_hint [%0], [%1], 8, %2;" ::"r"(dst), "l"(src),
+               "l"(pol)
+               : "memory");
+}
+__device__ __forceinline__ void st_global_stream(float* p, float4 v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "f"(v.x),
+               "f"(v.y), "f"(v.z), "f"(v.w), "l"(pol)
+               : "memory");
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
 }
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
@@ -281,8 +319,8 @@ __device__ __forceinline__ void cp_async_wait() {
 // last segment, and per selection its number and weight.
 struct alignas(16) StageMeta {
   int row, mf, c0, last;
-  int e[kPiece];
-  float w[kPiece];
+  int e[kRec];
+  float w[kRec];
   int pad[4];
 };
 
@@ -291,8 +329,8 @@ struct alignas(16) StageMeta {
 // from the stage, or 0 for atomic adds).
 template <int M, bool kBf16>
 __device__ __forceinline__ void seg_compute(const unsigned char* st, int lane,
-                                            const float (&wt)[kPiece], float (&part)[kPiece],
-                                            bool shared, float* drow) {
+                                            const float (&wt)[kRec], float (&part)[kRec],
+                                            bool shared, float* drow, uint64_t pol_stream) {
   float x[4];
   if (kBf16) {
     const uint2 v = *reinterpret_cast<const uint2*>(st + lane * 16);
@@ -324,7 +362,7 @@ __device__ __forceinline__ void seg_compute(const unsigned char* st, int lane,
   if (shared)
     red_add4(drow, acc.x, acc.y, acc.z, acc.w);
   else
-    *reinterpret_cast<float4*>(drow) = acc;
+    st_global_stream(drow, acc, pol_stream);
 }
 
 // The copies of one lane's 4 columns (column col of row `row`) of a segment
@@ -332,18 +370,20 @@ __device__ __forceinline__ void seg_compute(const unsigned char* st, int lane,
 template <int M, bool kBf16>
 __device__ __forceinline__ void seg_issue(uint32_t dst, const void* values, const float* dvalues,
                                           const float* dout, int64_t row, int d_v, int col,
-                                          const int (&b)[kPiece], bool shared) {
+                                          const int (&b)[kRec], bool shared,
+                                          uint64_t pol_stream, uint64_t pol_keep) {
   const int64_t off = row * d_v + col;
   if (kBf16)
-    cp_async8(dst, static_cast<const uint16_t*>(values) + off);
+    cp_async8(dst, static_cast<const uint16_t*>(values) + off, pol_stream);
   else
-    cp_async16(dst, static_cast<const float*>(values) + off);
-  if (!shared) cp_async16(dst + 512, dvalues + off);
+    cp_async16(dst, static_cast<const float*>(values) + off, pol_stream);
+  if (!shared) cp_async16(dst + 512, dvalues + off, pol_stream);
 #pragma unroll
-  for (int g = 0; g < M; ++g) cp_async16(dst + 512 * (2 + g), dout + (int64_t)b[g] * d_v + col);
+  for (int g = 0; g < M; ++g)
+    cp_async16(dst + 512 * (2 + g), dout + (int64_t)b[g] * d_v + col, pol_keep);
 }
 
-// Persistent, kRgWarps warps per CTA, two CTAs per SM.  Warp gw of GW takes
+// Persistent, kRgWarps warps per CTA, kRgCtas CTAs per SM.  Warp gw of GW takes
 // pieces gw, gw + GW, ...; each piece is walked in segments of kSegW
 // columns, one stage each, kRgStages - 1 stages ahead of the one computed.
 // Records are fetched 32 at a time (one per lane) and broadcast by shuffles.
@@ -351,7 +391,7 @@ __device__ __forceinline__ void seg_issue(uint32_t dst, const void* values, cons
 // so a lane waits for its own copies (cp.async groups) and no data crosses
 // lanes except the dw sums.
 template <bool kBf16>
-__global__ void __launch_bounds__(kRgWarps * 32, 2)
+__global__ void __launch_bounds__(kRgWarps * 32, kRgCtas)
 row_grad_kernel(const void* __restrict__ values, int d_v, const float* __restrict__ dout,
                 const PieceRec* __restrict__ pieces, const int* __restrict__ n_pieces,
                 float* __restrict__ dw, float* __restrict__ dvalues) {
@@ -366,11 +406,12 @@ row_grad_kernel(const void* __restrict__ values, int d_v, const float* __restric
   const int np = gw < total ? (total - gw + GW - 1) / GW : 0;
   const int nseg = (d_v + kSegW - 1) / kSegW;
   const int ntask = np * nseg;
+  const uint64_t pol_stream = policy_evict_first(), pol_keep = policy_evict_last();
 
   int4 r0 = make_int4(0, 0, 0, 0), r1 = r0, r2 = r0, r3 = r0;  // this lane's record
   int win = -32;                                                // first piece of the window
   int pj = -1, ps = 0;                                          // task being issued
-  int irow = 0, im = 0, ishared = 0, ib[kPiece] = {0, 0, 0, 0};
+  int irow = 0, im = 0, ishared = 0, ib[kRec] = {0, 0, 0, 0};
   int issued = 0;
 
   auto issue = [&]() {
@@ -420,16 +461,10 @@ row_grad_kernel(const void* __restrict__ values, int d_v, const float* __restric
       const int col = c0 + 4 * lane;
       if (col < d_v) {
         const uint32_t dst = ring_s + st * kStageBytes + lane * 16;
-        switch (im) {
-          case 1: seg_issue<1, kBf16>(dst, values, dvalues, dout, irow, d_v, col, ib, ishared);
-            break;
-          case 2: seg_issue<2, kBf16>(dst, values, dvalues, dout, irow, d_v, col, ib, ishared);
-            break;
-          case 3: seg_issue<3, kBf16>(dst, values, dvalues, dout, irow, d_v, col, ib, ishared);
-            break;
-          default: seg_issue<4, kBf16>(dst, values, dvalues, dout, irow, d_v, col, ib, ishared);
-            break;
-        }
+        with_piece_size(im, [&](auto mc) {
+          seg_issue<decltype(mc)::value, kBf16>(dst, values, dvalues, dout, irow, d_v, col, ib,
+                                                ishared, pol_stream, pol_keep);
+        });
       }
       if (++ps == nseg) ps = 0;
       ++issued;
@@ -438,7 +473,7 @@ row_grad_kernel(const void* __restrict__ values, int d_v, const float* __restric
     __syncwarp();
   };
 
-  float part[kPiece] = {0.0f, 0.0f, 0.0f, 0.0f};
+  float part[kRec] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
   for (int i = 0; i < S - 1; ++i) issue();
   for (int t = 0; t < ntask; ++t) {
@@ -451,19 +486,16 @@ row_grad_kernel(const void* __restrict__ values, int d_v, const float* __restric
     const int col = h.z + 4 * lane;
     if (col < d_v) {
       const float4 wv = reinterpret_cast<const float4*>(meta + st)[2];
-      const float wt[kPiece] = {wv.x, wv.y, wv.z, wv.w};
+      const float wt[kRec] = {wv.x, wv.y, wv.z, wv.w};
       const unsigned char* base = ring + st * kStageBytes;
       float* drow = dvalues + (int64_t)h.x * d_v + col;
-      switch (m) {
-        case 1: seg_compute<1, kBf16>(base, lane, wt, part, shared, drow); break;
-        case 2: seg_compute<2, kBf16>(base, lane, wt, part, shared, drow); break;
-        case 3: seg_compute<3, kBf16>(base, lane, wt, part, shared, drow); break;
-        default: seg_compute<4, kBf16>(base, lane, wt, part, shared, drow); break;
-      }
+      with_piece_size(m, [&](auto mc) {
+        seg_compute<decltype(mc)::value, kBf16>(base, lane, wt, part, shared, drow, pol_stream);
+      });
     }
     if (h.w) {  // the piece's last segment: its dw
       const int4 ev = reinterpret_cast<const int4*>(meta + st)[1];
-      const int es[kPiece] = {ev.x, ev.y, ev.z, ev.w};
+      const int es[kRec] = {ev.x, ev.y, ev.z, ev.w};
 #pragma unroll
       for (int g = 0; g < kPiece; ++g) {
         if (g < m) {
@@ -594,13 +626,13 @@ cudaError_t launch_backward_read(const void* values, int value_dtype, int B, int
     e = cudaFuncSetAttribute(row_grad_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)sm);
     if (e != cudaSuccess) return e;
-    row_grad_kernel<true><<<2 * sms, kRgWarps * 32, sm, stream>>>(values, d_v, dout, pieces,
+    row_grad_kernel<true><<<kRgCtas * sms, kRgWarps * 32, sm, stream>>>(values, d_v, dout, pieces,
                                                                   n_pieces, dw, dvalues);
   } else {
     e = cudaFuncSetAttribute(row_grad_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)sm);
     if (e != cudaSuccess) return e;
-    row_grad_kernel<false><<<2 * sms, kRgWarps * 32, sm, stream>>>(values, d_v, dout, pieces,
+    row_grad_kernel<false><<<kRgCtas * sms, kRgWarps * 32, sm, stream>>>(values, d_v, dout, pieces,
                                                                    n_pieces, dw, dvalues);
   }
   return cudaGetLastError();
