@@ -183,6 +183,27 @@ def test_backward_split_calls():
     assert (np.abs(got[4] - ref["dw"]) <= (d_v / 32 + 6) * U * A).all()
 
 
+@pytest.mark.parametrize("vdt", ["bf16", "f32"])
+def test_backward_concentrated_selection(vdt):
+    # usage collapse ("Keeping the memory in use"): 9,600 selections on 300
+    # rows of a 4,096-row table, so one 256-row bucket holds more than one
+    # chunk of selections (rows shared between CTAs, vector atomic adds) and
+    # most rows more than one piece; plus one row every query selects
+    B, H, d_q, n, d_v, k = 300, 2, 64, 64, 128, 16
+    s = synth.seed_of(dict(cfg_id=140))
+    q = synth.normal(s, 1, B * H * d_q, 1.0, dtype="bf16")
+    C = synth.normal(s, 2, H * 2 * n * (d_q // 2), 2.0 / d_q, dtype="bf16")
+    V = synth.normal(s, 3, n * n * d_v, 1.0 / d_v, dtype=vdt)
+    dout = synth.normal(s, 15, B * d_v, 1.0).reshape(B, d_v).astype(np.float64)
+    u = synth.uniform(s, 12, B * H * k).reshape(B, H, k)
+    idx = np.minimum((u * 300).astype(np.int64), 299)
+    idx[:, 0, 0] = 4000  # a hot row in another bucket
+    e = -np.log1p(-synth.uniform(s, 14, B * H * k)).reshape(B, H, k)
+    w = (e / e.sum(-1, keepdims=True)).astype(np.float32)
+    got = run_backward(q, C, V, vdt, B, H, d_q, n, d_v, k, idx, w, dout)
+    check_against_oracle(q, C, V, vdt, B, H, d_q, n, d_v, k, idx, w, dout, got)
+
+
 def test_backward_single_winner_closed_form():
     # k = 1: w = 1, so ds = 0: dq is exactly 0, dsubkeys unchanged, and
     # dvalues[idx] gains the dout of every query that selected it
