@@ -443,7 +443,9 @@ def run_ours(args, rank, world, local):
         bread = bread_bytes / (ms_bread * 1e-3) / 1e9
         broof = {"kernel": "pkm_backward_read (bucket sort + row_grad_kernel)", "bound": "hbm",
                  "achieved": bread, "peak": pk_["hbm"], "unit": "GB/s",
-                 "frac": bread / pk_["hbm"], "traffic": None, "peak_source": pk_["src"],
+                 "frac": bread / pk_["hbm"],
+                 "traffic": measured_traffic(args.workload, B, "row_grad_kernel", "backward.cu"),
+                 "peak_source": pk_["src"],
                  "rows_touched": rows_touched}
         forward_roof, roof = roof, broof
     line = {
@@ -494,13 +496,14 @@ def run_ours(args, rank, world, local):
         print(json.dumps(line), flush=True)
 
 
-def measured_traffic(workload_name, B):
-    """DRAM bytes (read + write) of one gather launch from the committed ncu
-    summary, if it was taken on this workload and the kernel source is
-    unchanged since (its sha256 prefix is recorded); else None."""
+def measured_traffic(workload_name, B, kernel="gather_kernel", source="gather.cu"):
+    """DRAM bytes (read + write) of one launch (or call) from the committed ncu
+    summary profiles/<kernel>_<workload>.md, if it was taken on this workload
+    and the kernel source is unchanged since (its sha256 prefix is recorded);
+    else None."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", "gather_kernel_%s.md" % workload_name)
-    src = os.path.join(ROOT, "sparse_top_lookup_gb300", "csrc", "gather.cu")
+    path = os.path.join(ROOT, "profiles", "%s_%s.md" % (kernel, workload_name))
+    src = os.path.join(ROOT, "sparse_top_lookup_gb300", "csrc", source)
     if not os.path.exists(path):
         return None
     fields = {}
