@@ -101,8 +101,9 @@ enum {
      automatic choice. */
   PKM_OPT_HINT_Z = 1,
   /* pkm_forward_host: number of batch slices (1 .. PKM_HOST_MAX_CHUNKS,
-     default 4) pipelined so the copy of slice i+1 in and of slice i-1 out
-     overlap the computation of slice i. */
+     default 3) pipelined so the copy of slice i+1 in and of slice i-1 out
+     overlap the computation of slice i; the first and last slices are half
+     the size of the others (shorter pipeline fill and drain). */
   PKM_OPT_HOST_CHUNKS = 2
 };
 #define PKM_HOST_MAX_CHUNKS 16

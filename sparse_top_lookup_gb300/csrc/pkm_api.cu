@@ -201,7 +201,7 @@ int pkm_create(pkm_t* out, const pkm_config* cfg) {
     for (int i = 0; ok && i < PKM_HOST_MAX_CHUNKS; ++i)
       ok = cudaEventCreateWithFlags(&h->ev_in[i], cudaEventDisableTiming) == cudaSuccess &&
            cudaEventCreateWithFlags(&h->ev_comp[i], cudaEventDisableTiming) == cudaSuccess;
-    h->host_chunks = 4;
+    h->host_chunks = 3;
   }
   if (ok && cfg->with_backward) {
     const size_t ws = pkm::backward_workspace_bytes(cfg->max_B, cfg->max_H, cfg->max_n_keys,
@@ -335,12 +335,20 @@ int pkm_forward_host(pkm_t h, const void* q_host, const void* subkeys, const voi
   const size_t qrow = (size_t)H * h->cfg.d_q * elem_size(h->cfg.q_dtype);  // bytes per query
   const size_t orow = (size_t)h->cfg.d_v * sizeof(float);
   const size_t srow = (size_t)H * k;  // selections per query
-  // batch split: chunks of a multiple of 8 queries (keeps every device
-  // offset 16-byte aligned), at most host_chunks of them
-  int chunks = h->host_chunks < 1 ? 1 : h->host_chunks;
-  int per = (B + chunks - 1) / chunks;
-  per = (per + 7) / 8 * 8;
-  chunks = (B + per - 1) / per;
+  // batch split into at most host_chunks slices, each a multiple of 8
+  // queries (keeps every device offset 16-byte aligned); the first and the
+  // last slice are half the size of the others, which shortens the pipeline's
+  // fill (the first slice's copy in) and drain (the last slice's copy out):
+  // slice i covers [cut(i), cut(i+1)) with cut(i) = B * (i - 1/2) / (chunks - 1)
+  const int want = h->host_chunks < 1 ? 1 : h->host_chunks;
+  int cut[PKM_HOST_MAX_CHUNKS + 1];
+  int chunks = 0;
+  cut[0] = 0;
+  for (int i = 1; i <= want; ++i) {
+    int64_t c = i == want ? B : ((int64_t)B * (2 * i - 1) / (2 * (want - 1)) + 7) / 8 * 8;
+    if (c > B) c = B;
+    if (c > cut[chunks]) cut[++chunks] = (int)c;
+  }
   const char* qh = static_cast<const char*>(q_host);
   char* qd = static_cast<char*>(h->stage_q);
   if (cudaEventRecord(h->ev_start, s) != cudaSuccess ||
@@ -348,7 +356,7 @@ int pkm_forward_host(pkm_t h, const void* q_host, const void* subkeys, const voi
       cudaStreamWaitEvent(h->s_out, h->ev_start, 0) != cudaSuccess)
     return PKM_ERR_CUDA;
   for (int c = 0; c < chunks; ++c) {
-    const int b0 = c * per, nb = (B - b0 < per) ? B - b0 : per;
+    const int b0 = cut[c], nb = cut[c + 1] - cut[c];
     if (cudaMemcpyAsync(qd + b0 * qrow, qh + b0 * qrow, nb * qrow, cudaMemcpyHostToDevice,
                         h->s_in) != cudaSuccess ||
         cudaEventRecord(h->ev_in[c], h->s_in) != cudaSuccess ||

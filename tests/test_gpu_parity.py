@@ -214,7 +214,7 @@ def test_forward_host_matches_device_forward():
     try:
         qh = torch.from_numpy(q.view(np.int16)).pin_memory()
         dC, dV = to_device(C, "bf16"), to_device(V, "bf16")
-        for chunks in (None, 1, 3, 16):  # batch slices pipelined against the copies
+        for chunks in (None, 1, 2, 3, 4, 16):  # batch slices pipelined against the copies
             if chunks is not None:
                 pk.check(pk.pkm_set_option(h, pk.PKM_OPT_HOST_CHUNKS, chunks), "set_option")
             oh = torch.empty(B, c["d_v"]).pin_memory()
