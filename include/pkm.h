@@ -51,7 +51,8 @@
  *
  * Asynchrony: every call enqueues work on `stream` (a cudaStream_t; NULL is
  * the legacy default stream) and returns without synchronising, except
- * pkm_get_status and pkm_forward_host, which synchronise `stream`.  Results are
+ * pkm_get_status and pkm_forward_host, which synchronise `stream`
+ * (pkm_forward_host_async signals an event instead).  Results are
  * valid once the stream has been synchronised.  Calls on one handle must not
  * overlap on the GPU when they use the handle's scratch (idx/w == NULL, and
  * every pkm_backward).
@@ -115,8 +116,8 @@ typedef struct pkm_handle *pkm_t;
  * for bf16).  d_v: value row width (d_v * element size a multiple of 16
  * bytes; a multiple of 16 for PKM_FP8_E4M3).  max_*: the largest B, H,
  * n_keys and k any call will pass (sizes the scratch).  host_staging:
- * nonzero to also allocate device staging for pkm_forward_host (max_B
- * queries and outputs).  with_backward: nonzero to also allocate what
+ * nonzero to also allocate device staging for pkm_forward_host (two slots of
+ * max_B queries and outputs).  with_backward: nonzero to also allocate what
  * pkm_backward needs (bf16 queries and subkeys, bf16 or fp32 values): a
  * cuBLAS handle with a 32 MiB workspace and scratch for the gradients
  * (about 4 * max_B * max_H * (max_k + max_n_keys) bytes, or 24 * max_B *
@@ -172,6 +173,22 @@ int pkm_gather(pkm_t h, const void *values, int B, int H, int n_keys, int k, con
 int pkm_forward_host(pkm_t h, const void *q_host, const void *subkeys, const void *values, int B,
                      int H, int n_keys, int k, float *out_host, int64_t *idx_host, float *w_host,
                      void *stream);
+
+/*
+ * pkm_forward_host without the final synchronisation, for callers that keep
+ * several batches in flight: the call enqueues the copies and the forward and
+ * returns; done_event (a cudaEvent_t, required) is recorded after the last
+ * copy back, and out_host / idx_host / w_host are valid once it has
+ * completed.  q_host must stay unchanged and the host buffers valid until
+ * then.  The handle keeps two staging slots used in turn, so the copies in of
+ * one call run while the previous call computes; a third call's copies wait
+ * (on the device) until the first call's results are copied back.  The batch
+ * is one slice unless PKM_OPT_HOST_CHUNKS was set on the handle (the call in
+ * flight beside it already hides the copies).
+ */
+int pkm_forward_host_async(pkm_t h, const void *q_host, const void *subkeys, const void *values,
+                           int B, int H, int n_keys, int k, float *out_host, int64_t *idx_host,
+                           float *w_host, void *stream, void *done_event);
 
 /* Set a tuning option of a handle (PKM_OPT_*).  Affects later calls only. */
 int pkm_set_option(pkm_t h, int option, double value);

@@ -25,7 +25,7 @@ EXPORTED = ["pkm_create", "pkm_destroy", "pkm_forward", "pkm_lookup", "pkm_gathe
             "pkm_forward_host", "pkm_get_status", "pkm_check_args", "pkm_strerror",
             "pkm_abi_version", "pkm_set_option", "pkm_get_fallback_count", "pkm_lookup_static",
             "pkm_quantize_values_fp8", "pkm_bn_fold", "pkm_query_net", "pkm_backward", "pkm_backward_read",
-            "pkm_backward_scores"]
+            "pkm_backward_scores", "pkm_forward_host_async"]
 PKM_STATIC_MAX_PAIRS = 1 << 16
 
 
@@ -66,6 +66,8 @@ def lib():
         L.pkm_lookup.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp]
         L.pkm_gather.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp]
         L.pkm_forward_host.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp]
+        L.pkm_forward_host_async.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp,
+                                             vp]
         L.pkm_get_status.argtypes = [vp, vp]
         L.pkm_check_args.argtypes = [cfgp, i32, i32, i32, i32]
         L.pkm_strerror.argtypes = [i32]
@@ -84,7 +86,7 @@ def lib():
                   "pkm_get_status", "pkm_check_args", "pkm_abi_version", "pkm_set_option",
                   "pkm_get_fallback_count", "pkm_lookup_static", "pkm_quantize_values_fp8",
                   "pkm_bn_fold", "pkm_query_net", "pkm_backward", "pkm_backward_read",
-                  "pkm_backward_scores"):
+                  "pkm_backward_scores", "pkm_forward_host_async"):
             getattr(L, f).restype = i32
         _lib = L
     return _lib
@@ -185,6 +187,22 @@ def pkm_forward_host(h, q_host, subkeys, values, B, H, n_keys, k, out_host, idx_
     return lib().pkm_forward_host(h, _addr(q_host), _addr(subkeys), _addr(values), B, H, n_keys, k,
                                   _addr(out_host), _addr(idx_host), _addr(w_host),
                                   _stream(stream))
+
+
+def pkm_forward_host_async(h, q_host, subkeys, values, B, H, n_keys, k, out_host, done_event,
+                           idx_host=None, w_host=None, stream=None):
+    """pkm_forward_host without the final synchronisation; done_event (a
+    torch.cuda.Event or a raw cudaEvent_t) completes when the results are
+    back in the host buffers."""
+    if hasattr(done_event, "cuda_event"):
+        if not done_event.cuda_event:  # torch creates its events when first recorded
+            done_event.record()
+        ev = done_event.cuda_event
+    else:
+        ev = done_event
+    return lib().pkm_forward_host_async(h, _addr(q_host), _addr(subkeys), _addr(values), B, H,
+                                        n_keys, k, _addr(out_host), _addr(idx_host),
+                                        _addr(w_host), _stream(stream), ev)
 
 
 def pkm_set_option(h, option, value):

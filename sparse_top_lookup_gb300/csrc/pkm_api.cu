@@ -22,15 +22,20 @@ struct pkm_handle {
   float* list_v;     // [max_B * max_H * 2 * 32] per-half lists between the two bf16 kernels
   unsigned short* list_c;
   float hint_z;      // selection threshold hint override (NaN: automatic)
-  void* stage_q;     // pkm_forward_host staging (optional)
-  float* stage_out;
-  int64_t* stage_idx;
-  float* stage_w;
+  // pkm_forward_host staging (optional), two slots used by turns, so one
+  // call's copies in can run while the previous call computes
+  void* stage_q[2];
+  float* stage_out[2];
+  int64_t* stage_idx[2];
+  float* stage_w[2];
+  int next_slot;
   // pkm_forward_host pipeline: copies in / out on their own streams, so the
-  // copy engines move batch i+1 in and batch i-1 out while batch i computes
+  // copy engines move batch i+1 in and batch i-1 out while batch i computes;
+  // ev_done[s]: the last copy out of the call that used slot s
   cudaStream_t s_in, s_out;
-  cudaEvent_t ev_start, ev_done, ev_in[PKM_HOST_MAX_CHUNKS], ev_comp[PKM_HOST_MAX_CHUNKS];
+  cudaEvent_t ev_done[2], ev_in[PKM_HOST_MAX_CHUNKS], ev_comp[PKM_HOST_MAX_CHUNKS];
   int host_chunks;
+  bool host_chunks_set;  // PKM_OPT_HOST_CHUNKS given by the caller
 };
 
 namespace {
@@ -141,14 +146,15 @@ void pkm_destroy(pkm_t h) {
   if (h->blas) cublasDestroy(h->blas);
   cudaFree(h->blas_ws);
   cudaFree(h->bwd_ws);
-  cudaFree(h->stage_q);
-  cudaFree(h->stage_out);
-  cudaFree(h->stage_idx);
-  cudaFree(h->stage_w);
+  for (int s = 0; s < 2; ++s) {
+    cudaFree(h->stage_q[s]);
+    cudaFree(h->stage_out[s]);
+    cudaFree(h->stage_idx[s]);
+    cudaFree(h->stage_w[s]);
+    if (h->ev_done[s]) cudaEventDestroy(h->ev_done[s]);
+  }
   if (h->s_in) cudaStreamDestroy(h->s_in);
   if (h->s_out) cudaStreamDestroy(h->s_out);
-  if (h->ev_start) cudaEventDestroy(h->ev_start);
-  if (h->ev_done) cudaEventDestroy(h->ev_done);
   for (int i = 0; i < PKM_HOST_MAX_CHUNKS; ++i) {
     if (h->ev_in[i]) cudaEventDestroy(h->ev_in[i]);
     if (h->ev_comp[i]) cudaEventDestroy(h->ev_comp[i]);
@@ -190,14 +196,15 @@ int pkm_create(pkm_t* out, const pkm_config* cfg) {
   }
   if (ok && cfg->host_staging && cfg->max_B) {
     const size_t qb = (size_t)cfg->max_B * cfg->max_H * cfg->d_q * elem_size(cfg->q_dtype);
-    ok = cudaMalloc(&h->stage_q, qb) == cudaSuccess &&
-         cudaMalloc(&h->stage_out, (size_t)cfg->max_B * cfg->d_v * sizeof(float)) == cudaSuccess &&
-         cudaMalloc(&h->stage_idx, sel * sizeof(int64_t)) == cudaSuccess &&
-         cudaMalloc(&h->stage_w, sel * sizeof(float)) == cudaSuccess;
+    for (int st = 0; ok && st < 2; ++st)
+      ok = cudaMalloc(&h->stage_q[st], qb) == cudaSuccess &&
+           cudaMalloc(&h->stage_out[st], (size_t)cfg->max_B * cfg->d_v * sizeof(float)) ==
+               cudaSuccess &&
+           cudaMalloc(&h->stage_idx[st], sel * sizeof(int64_t)) == cudaSuccess &&
+           cudaMalloc(&h->stage_w[st], sel * sizeof(float)) == cudaSuccess &&
+           cudaEventCreateWithFlags(&h->ev_done[st], cudaEventDisableTiming) == cudaSuccess;
     ok = ok && cudaStreamCreateWithFlags(&h->s_in, cudaStreamNonBlocking) == cudaSuccess &&
-         cudaStreamCreateWithFlags(&h->s_out, cudaStreamNonBlocking) == cudaSuccess &&
-         cudaEventCreateWithFlags(&h->ev_start, cudaEventDisableTiming) == cudaSuccess &&
-         cudaEventCreateWithFlags(&h->ev_done, cudaEventDisableTiming) == cudaSuccess;
+         cudaStreamCreateWithFlags(&h->s_out, cudaStreamNonBlocking) == cudaSuccess;
     for (int i = 0; ok && i < PKM_HOST_MAX_CHUNKS; ++i)
       ok = cudaEventCreateWithFlags(&h->ev_in[i], cudaEventDisableTiming) == cudaSuccess &&
            cudaEventCreateWithFlags(&h->ev_comp[i], cudaEventDisableTiming) == cudaSuccess;
@@ -321,17 +328,24 @@ int pkm_backward(pkm_t h, const void* q, const void* subkeys, const void* values
   return pkm_backward_scores(h, q, subkeys, B, H, n_keys, k, idx, w, dw, dq, dsubkeys, stream);
 }
 
-int pkm_forward_host(pkm_t h, const void* q_host, const void* subkeys, const void* values, int B,
-                     int H, int n_keys, int k, float* out_host, int64_t* idx_host, float* w_host,
-                     void* stream) {
+// The host-buffer forward: the batch in slices, each slice's copy in on s_in,
+// its lookup and read on `stream`, its copies out on s_out.  The call takes
+// the next of the two staging slots; its copies in first wait (on the
+// device) for the last copy out of the call that used the slot before, so
+// two calls can be in flight.  sync: wait for the copies out; else record
+// `done` on s_out after them.
+static int forward_host(pkm_t h, const void* q_host, const void* subkeys, const void* values,
+                        int B, int H, int n_keys, int k, float* out_host, int64_t* idx_host,
+                        float* w_host, cudaStream_t s, bool sync, cudaEvent_t done) {
   if (!h) return PKM_ERR_INVALID;
   int rc = check_call(&h->cfg, B, H, n_keys, k);
   if (rc) return rc;
-  if (B == 0) return PKM_OK;
-  if (!h->stage_q) return PKM_ERR_NO_STAGING;
+  if (B == 0) return sync ? PKM_OK : cuda_rc(cudaEventRecord(done, h->s_out));
+  if (!h->stage_q[0]) return PKM_ERR_NO_STAGING;
   if (!q_host || !subkeys || !values || !out_host) return PKM_ERR_INVALID;
   if (!aligned16(subkeys) || !aligned16(values)) return PKM_ERR_ALIGN;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int slot = h->next_slot;
+  h->next_slot ^= 1;
   const size_t qrow = (size_t)H * h->cfg.d_q * elem_size(h->cfg.q_dtype);  // bytes per query
   const size_t orow = (size_t)h->cfg.d_v * sizeof(float);
   const size_t srow = (size_t)H * k;  // selections per query
@@ -340,7 +354,9 @@ int pkm_forward_host(pkm_t h, const void* q_host, const void* subkeys, const voi
   // last slice are half the size of the others, which shortens the pipeline's
   // fill (the first slice's copy in) and drain (the last slice's copy out):
   // slice i covers [cut(i), cut(i+1)) with cut(i) = B * (i - 1/2) / (chunks - 1)
-  const int want = h->host_chunks < 1 ? 1 : h->host_chunks;
+  // (pkm_forward_host_async: one slice unless the caller chose the count;
+  // the call in flight beside it already hides its copies)
+  const int want = !sync && !h->host_chunks_set ? 1 : h->host_chunks < 1 ? 1 : h->host_chunks;
   int cut[PKM_HOST_MAX_CHUNKS + 1];
   int chunks = 0;
   cut[0] = 0;
@@ -350,11 +366,11 @@ int pkm_forward_host(pkm_t h, const void* q_host, const void* subkeys, const voi
     if (c > cut[chunks]) cut[++chunks] = (int)c;
   }
   const char* qh = static_cast<const char*>(q_host);
-  char* qd = static_cast<char*>(h->stage_q);
-  if (cudaEventRecord(h->ev_start, s) != cudaSuccess ||
-      cudaStreamWaitEvent(h->s_in, h->ev_start, 0) != cudaSuccess ||
-      cudaStreamWaitEvent(h->s_out, h->ev_start, 0) != cudaSuccess)
-    return PKM_ERR_CUDA;
+  char* qd = static_cast<char*>(h->stage_q[slot]);
+  // copies in wait for the slot's previous user to have copied its results
+  // out (copies out follow each slice's computation, itself after the
+  // caller's earlier work on `stream`)
+  if (cudaStreamWaitEvent(h->s_in, h->ev_done[slot], 0) != cudaSuccess) return PKM_ERR_CUDA;
   for (int c = 0; c < chunks; ++c) {
     const int b0 = cut[c], nb = cut[c + 1] - cut[c];
     if (cudaMemcpyAsync(qd + b0 * qrow, qh + b0 * qrow, nb * qrow, cudaMemcpyHostToDevice,
@@ -362,9 +378,9 @@ int pkm_forward_host(pkm_t h, const void* q_host, const void* subkeys, const voi
         cudaEventRecord(h->ev_in[c], h->s_in) != cudaSuccess ||
         cudaStreamWaitEvent(s, h->ev_in[c], 0) != cudaSuccess)
       return PKM_ERR_CUDA;
-    int64_t* idx_d = h->stage_idx + b0 * srow;
-    float* w_d = h->stage_w + b0 * srow;
-    float* out_d = h->stage_out + (size_t)b0 * h->cfg.d_v;
+    int64_t* idx_d = h->stage_idx[slot] + b0 * srow;
+    float* w_d = h->stage_w[slot] + b0 * srow;
+    float* out_d = h->stage_out[slot] + (size_t)b0 * h->cfg.d_v;
     rc = run_lookup(h, qd + b0 * qrow, subkeys, nb, H, n_keys, k, idx_d, w_d, s);
     if (rc) return rc;
     rc = run_gather(h, values, nb, H, n_keys, k, idx_d, w_d, out_d, s);
@@ -381,10 +397,26 @@ int pkm_forward_host(pkm_t h, const void* q_host, const void* subkeys, const voi
                                   cudaMemcpyDeviceToHost, h->s_out) != cudaSuccess)
       return PKM_ERR_CUDA;
   }
-  if (cudaEventRecord(h->ev_done, h->s_out) != cudaSuccess ||
-      cudaStreamWaitEvent(s, h->ev_done, 0) != cudaSuccess)
-    return PKM_ERR_CUDA;
+  if (cudaEventRecord(h->ev_done[slot], h->s_out) != cudaSuccess) return PKM_ERR_CUDA;
+  if (!sync) return cuda_rc(cudaEventRecord(done, h->s_out));
+  if (cudaStreamWaitEvent(s, h->ev_done[slot], 0) != cudaSuccess) return PKM_ERR_CUDA;
   return cuda_rc(cudaStreamSynchronize(s));
+}
+
+int pkm_forward_host(pkm_t h, const void* q_host, const void* subkeys, const void* values, int B,
+                     int H, int n_keys, int k, float* out_host, int64_t* idx_host, float* w_host,
+                     void* stream) {
+  return forward_host(h, q_host, subkeys, values, B, H, n_keys, k, out_host, idx_host, w_host,
+                      static_cast<cudaStream_t>(stream), true, nullptr);
+}
+
+int pkm_forward_host_async(pkm_t h, const void* q_host, const void* subkeys, const void* values,
+                           int B, int H, int n_keys, int k, float* out_host, int64_t* idx_host,
+                           float* w_host, void* stream, void* done_event) {
+  if (!done_event) return PKM_ERR_INVALID;
+  return forward_host(h, q_host, subkeys, values, B, H, n_keys, k, out_host, idx_host, w_host,
+                      static_cast<cudaStream_t>(stream), false,
+                      static_cast<cudaEvent_t>(done_event));
 }
 
 int pkm_set_option(pkm_t h, int option, double value) {
@@ -398,6 +430,7 @@ int pkm_set_option(pkm_t h, int option, double value) {
       if (!(value >= 1 && value <= PKM_HOST_MAX_CHUNKS) || value != (int)value)
         return PKM_ERR_OPTION;
       h->host_chunks = (int)value;
+      h->host_chunks_set = true;
       return PKM_OK;
     default:
       return PKM_ERR_OPTION;

@@ -88,6 +88,8 @@ def test_null_handle_rejected_before_any_cuda_call(L):
     assert L.pkm_forward(None, 16, 16, 16, 1, 1, 1, 1, 16, None, None, None) == pk.PKM_ERR_INVALID
     assert L.pkm_lookup(None, 16, 16, 1, 1, 1, 1, 16, 16, None) == pk.PKM_ERR_INVALID
     assert L.pkm_gather(None, 16, 1, 1, 1, 1, 16, 16, 16, None) == pk.PKM_ERR_INVALID
+    assert L.pkm_forward_host_async(None, 16, 16, 16, 1, 1, 1, 1, 16, None, None, None, 16) \
+        == pk.PKM_ERR_INVALID
     assert L.pkm_forward_host(None, 16, 16, 16, 1, 1, 1, 1, 16, None, None, None) \
         == pk.PKM_ERR_INVALID
     assert L.pkm_get_status(None, None) == pk.PKM_ERR_INVALID

@@ -225,6 +225,31 @@ def test_forward_host_matches_device_forward():
             assert np.array_equal(ih.numpy(), idx_d), chunks
             assert np.array_equal(wh.numpy(), w_d), chunks
             assert np.array_equal(oh.numpy(), out_d), chunks
+        # several calls in flight (the handle's two staging slots in turn, and
+        # a third call waiting for the first's copies back), alternating two
+        # query batches and their own output buffers
+        q2 = synth.queries(c, rows=B, row_offset=B)
+        out_d2, idx_d2, w_d2 = run_forward(c, q2, C, V)
+        qh2 = torch.from_numpy(q2.view(np.int16)).pin_memory()
+        pk.check(pk.pkm_set_option(h, pk.PKM_OPT_HOST_CHUNKS, 3), "set_option")
+        h_default, _ = make_handle(c, staging=True)  # async default: one slice
+        calls = []
+        for i in range(6):
+            hh = h if i < 3 else h_default
+            oh = torch.empty(B, c["d_v"]).pin_memory()
+            ih = torch.empty(B, c["H"], c["k"], dtype=torch.int64).pin_memory()
+            ev = torch.cuda.Event()
+            pk.check(pk.pkm_forward_host_async(hh, qh if i % 2 == 0 else qh2, dC, dV, B, c["H"],
+                                               c["n_keys"], c["k"], oh, ev, ih), "async")
+            calls.append((i, oh, ih, ev))
+        for i, oh, ih, ev in calls:
+            ev.synchronize()
+            want_o, want_i = (out_d, idx_d) if i % 2 == 0 else (out_d2, idx_d2)
+            assert np.array_equal(ih.numpy(), want_i), i
+            assert np.array_equal(oh.numpy(), want_o), i
+        pk.pkm_destroy(h_default)
+        assert pk.pkm_forward_host_async(h, qh, dC, dV, B, c["H"], c["n_keys"], c["k"], oh,
+                                         0) == pk.PKM_ERR_INVALID
         assert pk.pkm_set_option(h, pk.PKM_OPT_HOST_CHUNKS, 0) == pk.PKM_ERR_OPTION
         assert pk.pkm_set_option(h, pk.PKM_OPT_HOST_CHUNKS, 17) == pk.PKM_ERR_OPTION
     finally:
