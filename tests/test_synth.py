@@ -77,3 +77,22 @@ def test_value_rows_match_full_table():
     assert np.array_equal(synth.value_rows(cfg, rows), V[rows])
     q = synth.queries(cfg).reshape(cfg["B"], -1)
     assert np.array_equal(synth.queries(cfg, rows=3, row_offset=10).reshape(3, -1), q[10:13])
+
+
+def test_backward_stand_ins():
+    # the stand-in selection: subkeys in range, a few per half and head
+    # shared between the winners, weights positive and summing to 1;
+    # slices of the batch agree with the whole; dout ~ N(0, 1)
+    cfg = CONFIGS["page_train"]
+    n, k = cfg["n_keys"], cfg["k"]
+    a1, a2, w = synth.selections(cfg, rows=64)
+    assert a1.shape == (64, cfg["H"], k) and w.dtype == np.float32
+    assert a1.min() >= 0 and a1.max() < n and a2.min() >= 0 and a2.max() < n
+    per_head = [len(np.unique(a1[b, h])) for b in range(64) for h in range(cfg["H"])]
+    assert max(per_head) <= 8 and np.mean(per_head) > 4
+    assert (w > 0).all() and np.allclose(w.sum(-1), 1, atol=1e-6)
+    b1, b2, w2 = synth.selections(cfg, rows=16, row_offset=40)
+    assert (b1 == a1[40:56]).all() and (b2 == a2[40:56]).all() and (w2 == w[40:56]).all()
+    d = synth.output_grads(cfg, rows=512)
+    assert d.shape == (512, cfg["d_v"]) and abs(d.std() - 1) < 0.01
+    assert (synth.output_grads(cfg, rows=2, row_offset=7) == d[7:9]).all()
