@@ -98,7 +98,8 @@ __device__ __forceinline__ void red_add4(float* p, float a, float b, float c, fl
 __global__ void bucket_count_kernel(const int64_t* __restrict__ idx, int E, int64_t N,
                                     int* __restrict__ bcount, float* __restrict__ dw,
                                     int* __restrict__ status) {
-  for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < E; e += gridDim.x * blockDim.x) {
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < E;
+       e += (int64_t)gridDim.x * blockDim.x) {
     const int64_t r = idx[e];
     if (r < 0 || r >= N) {  // recorded; the selection contributes nothing
       atomicExch(status, PKM_ERR_BAD_INDEX);
@@ -172,10 +173,11 @@ bucket_scan_kernel(const int* __restrict__ bcount, int nb, int* __restrict__ cur
 
 __global__ void bucket_scatter_kernel(const int64_t* __restrict__ idx, int E, int64_t N,
                                       int* __restrict__ cursor, int* __restrict__ list) {
-  for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < E; e += gridDim.x * blockDim.x) {
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < E;
+       e += (int64_t)gridDim.x * blockDim.x) {
     const int64_t r = idx[e];
     if (r < 0 || r >= N) continue;
-    list[atomicAdd(&cursor[r / kRowsPerBucket], 1)] = e;
+    list[atomicAdd(&cursor[r / kRowsPerBucket], 1)] = (int)e;
   }
 }
 
