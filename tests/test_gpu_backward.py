@@ -163,6 +163,8 @@ def lookup_case(seed, B, H, d_q, n, d_v, k, vdt="bf16"):
     (300, 2, 128, 64, 256, 16, "bf16"),     # ragged batch, two heads
     (130, 3, 64, 33, 64, 8, "f32"),         # odd n_keys (unpaired bf16 stores), fp32 table
     (64, 1, 1024, 1024, 1024, 32, "bf16"),  # the page's d, n_keys and k
+    (1, 4, 32, 100, 32, 7, "bf16"),          # one query, odd k, small d_q, n_keys not 2^p
+    (257, 1, 16, 40, 16, 1, "f32"),          # k = 1, the smallest d_q and d_v
 ])
 def test_backward_matches_oracle(shape):
     B, H, d_q, n, d_v, k, vdt = shape
