@@ -239,7 +239,9 @@ def config_json(c, name):
                   "per-row fp32 scales, quantised on the GPU from the seeded bf16 table")
     if is_train(c):
         inputs = ("page inputs, seeded synthetic; output gradient dout [B, d_v] fp32 N(0,1); "
-                  "step = forward + backward (dq; dsubkeys and dvalues accumulated in fp32)")
+                  "step = forward + backward (dq; dsubkeys accumulated in fp32; dvalues %s)"
+                  % ("as distinct rows and their fp32 gradient rows" if c.get("sparse_grad")
+                     else "accumulated into the dense fp32 table"))
     if is_layer(c):
         inputs = ("layer input x [B, %d] bf16 N(0,1); query network weight [H*d_q, %d] bf16 "
                   "N(0,1/%d) and BatchNorm running statistics; subkeys and values as page; "
@@ -298,18 +300,29 @@ def run_ours(args, rank, world, local):
                          with_backward=int(train))
     h = pk.pkm_create(cfg)
     stream = torch.cuda.current_stream()
+    sparse = bool(c.get("sparse_grad"))
     if train:
         # the backward pass's buffers: dout in, dw between its two calls,
-        # gradients out (dsubkeys and dvalues accumulate over the steps)
+        # gradients out (dsubkeys and a dense dvalues accumulate over the
+        # steps; the sparse form rewrites its rows and gradient rows)
         dout_np = synth.output_grads(c)
         g_dout = torch.from_numpy(dout_np).cuda()
         g_dw = torch.empty(B, H, k, device="cuda")
         g_q = torch.empty(B, H, d_q, device="cuda")
         g_C = torch.zeros(H, 2, n, d_q // 2, device="cuda")
-        g_V = torch.zeros(n * n, d_v, device="cuda")
+        if sparse:
+            g_rows = torch.empty(B * H * k, dtype=torch.int64, device="cuda")
+            g_grad = torch.empty(B * H * k, d_v, device="cuda")
+            g_nrows = torch.zeros(1, dtype=torch.int32, device="cuda")
+        else:
+            g_V = torch.zeros(n * n, d_v, device="cuda")
 
     def backward_read():
-        if train:
+        if train and sparse:
+            pk.check(pk.pkm_backward_read_sparse(h, dV, B, H, n, k, idx, w, g_dout, g_dw, g_rows,
+                                                 g_grad, g_nrows, stream),
+                     "pkm_backward_read_sparse")
+        elif train:
             pk.check(pk.pkm_backward_read(h, dV, B, H, n, k, idx, w, g_dout, g_dw, g_V, stream),
                      "pkm_backward_read")
 
@@ -387,8 +400,13 @@ def run_ours(args, rank, world, local):
                      "pkm_forward")
             out_host.copy_(out, non_blocking=True)
             g_dout.copy_(dout_host, non_blocking=True)
-            pk.check(pk.pkm_backward(h, dq, dC, dV, B, H, n, k, idx, w, g_dout, g_q, g_C, g_V,
-                                     stream), "pkm_backward")
+            if sparse:
+                pk.check(pk.pkm_backward_sparse(h, dq, dC, dV, B, H, n, k, idx, w, g_dout, g_q,
+                                                g_C, g_rows, g_grad, g_nrows, stream),
+                         "pkm_backward_sparse")
+            else:
+                pk.check(pk.pkm_backward(h, dq, dC, dV, B, H, n, k, idx, w, g_dout, g_q, g_C,
+                                         g_V, stream), "pkm_backward")
             stream.synchronize()
         h2d = B * H * d_q * 2 + B * d_v * 4
     elif layer:
@@ -456,14 +474,16 @@ def run_ours(args, rank, world, local):
             "frac": achieved / pk_["hbm"], "traffic": traffic, "peak_source": pk_["src"]}
     if train:
         # per distinct selected row: the value row read once and its dvalues
-        # row read and written once (fp32); per selection: idx, w and dw; per
-        # query: dout.  The time is the whole pkm_backward_read call (bucket
-        # count, scan and scatter, then row_grad_kernel).
+        # row read and written once (fp32; the sparse form writes its gradient
+        # row and row number once); per selection: idx, w and dw; per query:
+        # dout.  The time is the whole read call (bucket count, scan and
+        # scatter, sort, then row_grad_kernel).
         rows_touched = int(torch.unique(idx).numel())
-        bread_bytes = (rows_touched * (value_row_bytes(c) + 8 * d_v) + B * H * k * 16
-                       + B * d_v * 4)
+        per_row = value_row_bytes(c) + (4 * d_v + 8 if sparse else 8 * d_v)
+        bread_bytes = rows_touched * per_row + B * H * k * 16 + B * d_v * 4
         bread = bread_bytes / (ms_bread * 1e-3) / 1e9
-        broof = {"kernel": "pkm_backward_read (bucket sort + row_grad_kernel)", "bound": "hbm",
+        broof = {"kernel": "pkm_backward_read%s (bucket sort + row_grad_kernel)"
+                 % ("_sparse" if sparse else ""), "bound": "hbm",
                  "achieved": bread, "peak": pk_["hbm"], "unit": "GB/s",
                  "frac": bread / pk_["hbm"],
                  "traffic": measured_traffic(args.workload, B, "row_grad_kernel", "backward.cu"),

@@ -279,6 +279,27 @@ int pkm_backward_read(pkm_t h, const void *values, int B, int H, int n_keys, int
                       float *dvalues, void *stream);
 
 /*
+ * pkm_backward with the value-table gradient in sparse form, the way a
+ * sparse optimiser consumes it (EmbeddingBag with sparse gradients): the
+ * distinct selected rows, ascending, in rows[0 .. *n_rows) and each row's
+ * gradient sum(w * dout) over its selections in grad_rows[i, :] (overwritten;
+ * fp32, d_v wide).  n_rows is a device int written by the call; rows and
+ * grad_rows must hold B * H * k entries (the case of no repeated row).  The
+ * dense dvalues table is neither read nor written.  Same requirements and
+ * status reporting as pkm_backward; an index outside [0, n_keys^2) is not
+ * listed.
+ */
+int pkm_backward_sparse(pkm_t h, const void *q, const void *subkeys, const void *values, int B,
+                        int H, int n_keys, int k, const int64_t *idx, const float *w,
+                        const float *dout, float *dq, float *dsubkeys, int64_t *rows,
+                        float *grad_rows, int *n_rows, void *stream);
+
+/* The read's part of pkm_backward_sparse: dw and the sparse value-table gradient. */
+int pkm_backward_read_sparse(pkm_t h, const void *values, int B, int H, int n_keys, int k,
+                             const int64_t *idx, const float *w, const float *dout, float *dw,
+                             int64_t *rows, float *grad_rows, int *n_rows, void *stream);
+
+/*
  * The scores' part of the backward pass, from w and dw: dq overwritten,
  * dsubkeys added to, as in pkm_backward.  Requires with_backward.
  */

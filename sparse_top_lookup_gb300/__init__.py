@@ -25,7 +25,8 @@ EXPORTED = ["pkm_create", "pkm_destroy", "pkm_forward", "pkm_lookup", "pkm_gathe
             "pkm_forward_host", "pkm_get_status", "pkm_check_args", "pkm_strerror",
             "pkm_abi_version", "pkm_set_option", "pkm_get_fallback_count", "pkm_lookup_static",
             "pkm_quantize_values_fp8", "pkm_bn_fold", "pkm_query_net", "pkm_backward", "pkm_backward_read",
-            "pkm_backward_scores", "pkm_forward_host_async"]
+            "pkm_backward_scores", "pkm_forward_host_async", "pkm_backward_sparse",
+            "pkm_backward_read_sparse"]
 PKM_STATIC_MAX_PAIRS = 1 << 16
 
 
@@ -82,11 +83,16 @@ def lib():
         L.pkm_backward.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]
         L.pkm_backward_read.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
         L.pkm_backward_scores.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
+        L.pkm_backward_sparse.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp,
+                                          vp, vp, vp, vp]
+        L.pkm_backward_read_sparse.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp,
+                                               vp, vp, vp]
         for f in ("pkm_create", "pkm_forward", "pkm_lookup", "pkm_gather", "pkm_forward_host",
                   "pkm_get_status", "pkm_check_args", "pkm_abi_version", "pkm_set_option",
                   "pkm_get_fallback_count", "pkm_lookup_static", "pkm_quantize_values_fp8",
                   "pkm_bn_fold", "pkm_query_net", "pkm_backward", "pkm_backward_read",
-                  "pkm_backward_scores", "pkm_forward_host_async"):
+                  "pkm_backward_scores", "pkm_forward_host_async", "pkm_backward_sparse",
+                  "pkm_backward_read_sparse"):
             getattr(L, f).restype = i32
         _lib = L
     return _lib
@@ -167,6 +173,24 @@ def pkm_backward(h, q, subkeys, values, B, H, n_keys, k, idx, w, dout, dq, dsubk
     return lib().pkm_backward(h, _addr(q), _addr(subkeys), _addr(values), B, H, n_keys, k,
                               _addr(idx), _addr(w), _addr(dout), _addr(dq), _addr(dsubkeys),
                               _addr(dvalues), _stream(stream))
+
+
+def pkm_backward_sparse(h, q, subkeys, values, B, H, n_keys, k, idx, w, dout, dq, dsubkeys, rows,
+                        grad_rows, n_rows, stream=None):
+    """Gradients with the value-table part sparse: rows[:n_rows] (distinct, ascending) and
+    grad_rows[:n_rows]; n_rows is a device int32."""
+    return lib().pkm_backward_sparse(h, _addr(q), _addr(subkeys), _addr(values), B, H, n_keys, k,
+                                     _addr(idx), _addr(w), _addr(dout), _addr(dq),
+                                     _addr(dsubkeys), _addr(rows), _addr(grad_rows),
+                                     _addr(n_rows), _stream(stream))
+
+
+def pkm_backward_read_sparse(h, values, B, H, n_keys, k, idx, w, dout, dw, rows, grad_rows, n_rows,
+                             stream=None):
+    """dw and the sparse value-table gradient (see pkm_backward_sparse)."""
+    return lib().pkm_backward_read_sparse(h, _addr(values), B, H, n_keys, k, _addr(idx), _addr(w),
+                                          _addr(dout), _addr(dw), _addr(rows), _addr(grad_rows),
+                                          _addr(n_rows), _stream(stream))
 
 
 def pkm_backward_read(h, values, B, H, n_keys, k, idx, w, dout, dw, dvalues, stream=None):

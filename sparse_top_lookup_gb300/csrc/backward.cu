@@ -66,10 +66,11 @@ constexpr int kRgStages = 4;         // stages per warp
 // a stage: value, dV and kPiece dout regions of [lane][16 bytes]
 constexpr int kStageBytes = 512 * (2 + kPiece);
 
-// One piece of a row's selections (64 bytes): row; m | shared << 8; then per
-// selection g < m its number e, its dout row b and its weight w.
+// One piece of a row's selections (64 bytes): row; m | shared << 8; the
+// row's slot in the sparse output; then per selection g < m its number e,
+// its dout row b and its weight w.
 struct alignas(16) PieceRec {
-  int row, mf, pad0, pad1;
+  int row, mf, slot, pad;
   int e[kRec];
   int b[kRec];
   float w[kRec];
@@ -95,9 +96,11 @@ __device__ __forceinline__ void red_add4(float* p, float a, float b, float c, fl
                : "memory");
 }
 
+// Selections per bucket; with `bitmap` (the sparse output) also one bit per
+// selected row.
 __global__ void bucket_count_kernel(const int64_t* __restrict__ idx, int E, int64_t N,
-                                    int* __restrict__ bcount, float* __restrict__ dw,
-                                    int* __restrict__ status) {
+                                    int* __restrict__ bcount, uint32_t* __restrict__ bitmap,
+                                    float* __restrict__ dw, int* __restrict__ status) {
   for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < E;
        e += (int64_t)gridDim.x * blockDim.x) {
     const int64_t r = idx[e];
@@ -107,68 +110,84 @@ __global__ void bucket_count_kernel(const int64_t* __restrict__ idx, int E, int6
       continue;
     }
     atomicAdd(&bcount[r / kRowsPerBucket], 1);
+    if (bitmap) atomicOr(&bitmap[r >> 5], 1u << (r & 31));
   }
 }
 
 // One CTA of 1024 threads: exclusive scans of the bucket sizes (list
-// offsets, the scatter's cursors) and of their chunk counts (item numbers);
+// offsets, the scatter's cursors), of their chunk counts (item numbers) and,
+// with `bitmap`, of their distinct selected rows (each bucket's first slot
+// in the sparse output; the total goes to *n_rows);
 // item = (list start, length, bucket, bucket has a single item).
 __global__ void __launch_bounds__(1024)
 bucket_scan_kernel(const int* __restrict__ bcount, int nb, int* __restrict__ cursor,
-                   int4* __restrict__ items, int* __restrict__ n_items) {
-  __shared__ int s_w0[32], s_w1[32];
-  __shared__ int s_carry0, s_carry1;
+                   int4* __restrict__ items, int* __restrict__ n_items,
+                   const uint32_t* __restrict__ bitmap, int* __restrict__ rowoff,
+                   int* __restrict__ n_rows) {
+  constexpr int Q = 3;
+  __shared__ int s_w[Q][32];
+  __shared__ int s_carry[Q];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (threadIdx.x == 0) s_carry0 = s_carry1 = 0;
+  if (threadIdx.x < Q) s_carry[threadIdx.x] = 0;
   __syncthreads();
   for (int base = 0; base < nb; base += 1024) {
     const int i = base + threadIdx.x;
-    const int c = i < nb ? bcount[i] : 0;
-    const int nc = (c + kChunk - 1) / kChunk;
-    int x0 = c, x1 = nc;
+    int v[Q];
+    v[0] = i < nb ? bcount[i] : 0;
+    v[1] = (v[0] + kChunk - 1) / kChunk;
+    v[2] = 0;
+    if (bitmap && i < nb) {
+#pragma unroll
+      for (int j = 0; j < kRowsPerBucket / 32; ++j)
+        v[2] += __popc(bitmap[(int64_t)i * (kRowsPerBucket / 32) + j]);
+    }
+    int x[Q];
+#pragma unroll
+    for (int q = 0; q < Q; ++q) x[q] = v[q];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int y0 = __shfl_up_sync(0xffffffffu, x0, o), y1 = __shfl_up_sync(0xffffffffu, x1, o);
-      if (lane >= o) {
-        x0 += y0;
-        x1 += y1;
+#pragma unroll
+      for (int q = 0; q < Q; ++q) {
+        const int y = __shfl_up_sync(0xffffffffu, x[q], o);
+        if (lane >= o) x[q] += y;
       }
     }
     if (lane == 31) {
-      s_w0[warp] = x0;
-      s_w1[warp] = x1;
+#pragma unroll
+      for (int q = 0; q < Q; ++q) s_w[q][warp] = x[q];
     }
     __syncthreads();
     if (warp == 0) {
-      int a0 = s_w0[lane], a1 = s_w1[lane];
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y0 = __shfl_up_sync(0xffffffffu, a0, o),
-                  y1 = __shfl_up_sync(0xffffffffu, a1, o);
-        if (lane >= o) {
-          a0 += y0;
-          a1 += y1;
+      for (int q = 0; q < Q; ++q) {
+        int a = s_w[q][lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, a, o);
+          if (lane >= o) a += y;
         }
+        s_w[q][lane] = a;
       }
-      s_w0[lane] = a0;
-      s_w1[lane] = a1;
     }
     __syncthreads();
-    const int off0 = s_carry0 + (warp ? s_w0[warp - 1] : 0) + x0 - c;
-    const int off1 = s_carry1 + (warp ? s_w1[warp - 1] : 0) + x1 - nc;
+    int off[Q];
+#pragma unroll
+    for (int q = 0; q < Q; ++q) off[q] = s_carry[q] + (warp ? s_w[q][warp - 1] : 0) + x[q] - v[q];
     if (i < nb) {
-      cursor[i] = off0;
-      for (int j = 0; j < nc; ++j)
-        items[off1 + j] = make_int4(off0 + j * kChunk, min(kChunk, c - j * kChunk), i, nc == 1);
+      cursor[i] = off[0];
+      if (bitmap) rowoff[i] = off[2];
+      for (int j = 0; j < v[1]; ++j)
+        items[off[1] + j] =
+            make_int4(off[0] + j * kChunk, min(kChunk, v[0] - j * kChunk), i, v[1] == 1);
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-      s_carry0 += s_w0[31];
-      s_carry1 += s_w1[31];
-    }
+    if (threadIdx.x < Q) s_carry[threadIdx.x] += s_w[threadIdx.x][31];
     __syncthreads();
   }
-  if (threadIdx.x == 0) *n_items = s_carry1;
+  if (threadIdx.x == 0) {
+    *n_items = s_carry[1];
+    if (bitmap) *n_rows = s_carry[2];
+  }
 }
 
 __global__ void bucket_scatter_kernel(const int64_t* __restrict__ idx, int E, int64_t N,
@@ -188,7 +207,9 @@ __global__ void __launch_bounds__(kReadWarps * 32)
 bucket_sort_kernel(const int64_t* __restrict__ idx, const float* __restrict__ w, int HK,
                    const int4* __restrict__ items, const int* __restrict__ n_items,
                    const int* __restrict__ list, PieceRec* __restrict__ pieces,
-                   int* __restrict__ n_pieces) {
+                   int* __restrict__ n_pieces, const uint32_t* __restrict__ bitmap,
+                   const int* __restrict__ rowoff, int64_t* __restrict__ rows_out,
+                   int* __restrict__ zero_list, int* __restrict__ n_zero) {
   constexpr int R = kRowsPerBucket;
   __shared__ int s_e[kChunk];
   __shared__ int s_sorted[kChunk];
@@ -271,12 +292,40 @@ bucket_sort_kernel(const int64_t* __restrict__ idx, const float* __restrict__ w,
       b[g] = e[g] / HK;
       wt[g] = g < m ? __ldg(w + e[g]) : 0.0f;
     }
+    // the sparse output: the row's slot is the bucket's first slot plus the
+    // selected rows below it in the bucket (bitmap); the row's first piece in
+    // this item lists it, and a shared row's slot is cleared before any
+    // piece adds to it
+    int slot = 0;
+    if (bitmap) {
+      const uint32_t* bw = bitmap + (int64_t)it.z * (R / 32);
+      slot = rowoff[it.z];
+      for (int j = 0; j < (lo >> 5); ++j) slot += __popc(bw[j]);
+      slot += __popc(bw[lo >> 5] & ((1u << (lo & 31)) - 1u));
+      if (q == s_pstart[lo]) {
+        rows_out[slot] = row0 + lo;
+        if (shared) zero_list[atomicAdd(n_zero, 1)] = slot;
+      }
+    }
     int4* out = reinterpret_cast<int4*>(pieces + s_base + q);
-    out[0] = make_int4((int)(row0 + lo), m | (shared ? 1 << 8 : 0), 0, 0);
+    out[0] = make_int4((int)(row0 + lo), m | (shared ? 1 << 8 : 0), slot, 0);
     out[1] = make_int4(e[0], e[1], e[2], e[3]);
     out[2] = make_int4(b[0], b[1], b[2], b[3]);
     out[3] = make_int4(__float_as_int(wt[0]), __float_as_int(wt[1]), __float_as_int(wt[2]),
                        __float_as_int(wt[3]));
+  }
+}
+
+// Sparse output: the slots of shared rows (several pieces add to them) are
+// cleared first; a slot listed twice is cleared twice.
+__global__ void zero_rows_kernel(const int* __restrict__ zero_list, const int* __restrict__ n_zero,
+                                 int d_v, float* __restrict__ grad_rows) {
+  const int nz = *n_zero;
+  const int nu = d_v >> 2;
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < (int64_t)nz * nu;
+       t += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t slot = zero_list[t / nu];
+    reinterpret_cast<float4*>(grad_rows + slot * d_v)[t % nu] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
 }
 
@@ -332,7 +381,8 @@ struct alignas(16) StageMeta {
 template <int M, bool kBf16>
 __device__ __forceinline__ void seg_compute(const unsigned char* st, int lane,
                                             const float (&wt)[kRec], float (&part)[kRec],
-                                            bool shared, float* drow, uint64_t pol_stream) {
+                                            bool copied, bool shared, float* drow,
+                                            uint64_t pol_stream) {
   float x[4];
   if (kBf16) {
     const uint2 v = *reinterpret_cast<const uint2*>(st + lane * 16);
@@ -347,8 +397,8 @@ __device__ __forceinline__ void seg_compute(const unsigned char* st, int lane,
     x[2] = v.z;
     x[3] = v.w;
   }
-  float4 acc = shared ? make_float4(0.0f, 0.0f, 0.0f, 0.0f)
-                      : *reinterpret_cast<const float4*>(st + 512 + lane * 16);
+  float4 acc = copied ? *reinterpret_cast<const float4*>(st + 512 + lane * 16)
+                      : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll
   for (int g = 0; g < M; ++g) {
     const float4 d = *reinterpret_cast<const float4*>(st + 512 * (2 + g) + lane * 16);
@@ -370,16 +420,16 @@ __device__ __forceinline__ void seg_compute(const unsigned char* st, int lane,
 // The copies of one lane's 4 columns (column col of row `row`) of a segment
 // into the stage at shared address dst.
 template <int M, bool kBf16>
-__device__ __forceinline__ void seg_issue(uint32_t dst, const void* values, const float* dvalues,
-                                          const float* dout, int64_t row, int d_v, int col,
-                                          const int (&b)[kRec], bool shared,
+__device__ __forceinline__ void seg_issue(uint32_t dst, const void* values, const float* out_rows,
+                                          const float* dout, int64_t row, int64_t dst_row,
+                                          int d_v, int col, const int (&b)[kRec], bool copy_dv,
                                           uint64_t pol_stream, uint64_t pol_keep) {
   const int64_t off = row * d_v + col;
   if (kBf16)
     cp_async8(dst, static_cast<const uint16_t*>(values) + off, pol_stream);
   else
     cp_async16(dst, static_cast<const float*>(values) + off, pol_stream);
-  if (!shared) cp_async16(dst + 512, dvalues + off, pol_stream);
+  if (copy_dv) cp_async16(dst + 512, out_rows + dst_row * d_v + col, pol_stream);
 #pragma unroll
   for (int g = 0; g < M; ++g)
     cp_async16(dst + 512 * (2 + g), dout + (int64_t)b[g] * d_v + col, pol_keep);
@@ -396,7 +446,7 @@ template <bool kBf16>
 __global__ void __launch_bounds__(kRgWarps * 32, kRgCtas)
 row_grad_kernel(const void* __restrict__ values, int d_v, const float* __restrict__ dout,
                 const PieceRec* __restrict__ pieces, const int* __restrict__ n_pieces,
-                float* __restrict__ dw, float* __restrict__ dvalues) {
+                float* __restrict__ dw, float* __restrict__ out_rows, bool sparse) {
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int S = kRgStages;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -413,7 +463,9 @@ row_grad_kernel(const void* __restrict__ values, int d_v, const float* __restric
   int4 r0 = make_int4(0, 0, 0, 0), r1 = r0, r2 = r0, r3 = r0;  // this lane's record
   int win = -32;                                                // first piece of the window
   int pj = -1, ps = 0;                                          // task being issued
-  int irow = 0, im = 0, ishared = 0, ib[kRec] = {0, 0, 0, 0};
+  // the piece being issued: its value row, its output row (the value row
+  // itself, or its slot in the sparse output), size, flags and dout rows
+  int irow = 0, idst = 0, im = 0, ishared = 0, ib[kRec] = {0, 0, 0, 0};
   int issued = 0;
 
   auto issue = [&]() {
@@ -433,6 +485,7 @@ row_grad_kernel(const void* __restrict__ values, int d_v, const float* __restric
         }
         const int hl = pj - win;
         irow = __shfl_sync(0xffffffffu, r0.x, hl);
+        idst = sparse ? __shfl_sync(0xffffffffu, r0.z, hl) : irow;
         const int mf = __shfl_sync(0xffffffffu, r0.y, hl);
         im = mf & 0xff;
         ishared = mf >> 8;
@@ -457,15 +510,18 @@ row_grad_kernel(const void* __restrict__ values, int d_v, const float* __restric
       }
       const int st = issued % S;
       const int c0 = ps * kSegW;
+      // the dV segment is read (and rewritten) only for an owned row of the
+      // dense output; shared rows and the sparse output start from zero
+      const bool copy_dv = !sparse && !ishared;
       if (lane == 0)
         reinterpret_cast<int4*>(meta + st)[0] =
-            make_int4(irow, im | (ishared << 8), c0, ps == nseg - 1);
+            make_int4(idst, im | (ishared << 8) | (copy_dv ? 1 << 9 : 0), c0, ps == nseg - 1);
       const int col = c0 + 4 * lane;
       if (col < d_v) {
         const uint32_t dst = ring_s + st * kStageBytes + lane * 16;
         with_piece_size(im, [&](auto mc) {
-          seg_issue<decltype(mc)::value, kBf16>(dst, values, dvalues, dout, irow, d_v, col, ib,
-                                                ishared, pol_stream, pol_keep);
+          seg_issue<decltype(mc)::value, kBf16>(dst, values, out_rows, dout, irow, idst, d_v,
+                                                col, ib, copy_dv, pol_stream, pol_keep);
         });
       }
       if (++ps == nseg) ps = 0;
@@ -484,15 +540,16 @@ row_grad_kernel(const void* __restrict__ values, int d_v, const float* __restric
     const int st = t % S;
     const int4 h = reinterpret_cast<const int4*>(meta + st)[0];
     const int m = h.y & 0xff;
-    const bool shared = (h.y >> 8) != 0;
+    const bool shared = ((h.y >> 8) & 1) != 0, copied = ((h.y >> 9) & 1) != 0;
     const int col = h.z + 4 * lane;
     if (col < d_v) {
       const float4 wv = reinterpret_cast<const float4*>(meta + st)[2];
       const float wt[kRec] = {wv.x, wv.y, wv.z, wv.w};
       const unsigned char* base = ring + st * kStageBytes;
-      float* drow = dvalues + (int64_t)h.x * d_v + col;
+      float* drow = out_rows + (int64_t)h.x * d_v + col;
       with_piece_size(m, [&](auto mc) {
-        seg_compute<decltype(mc)::value, kBf16>(base, lane, wt, part, shared, drow, pol_stream);
+        seg_compute<decltype(mc)::value, kBf16>(base, lane, wt, part, copied, shared, drow,
+                                                pol_stream);
       });
     }
     if (h.w) {  // the piece's last segment: its dw
@@ -559,29 +616,36 @@ __global__ void ds_rows_kernel(const int64_t* __restrict__ idx, const float* __r
 
 static size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
-// The read part's scratch, each array 256-byte aligned: the item and piece
-// counts and the bucket sizes [nb] (cleared per call, one memset), scatter
-// cursors [nb], the items [max_items], the bucketed selection numbers [E] and
-// the piece records [E].
+// The read part's scratch, each array 256-byte aligned: the item, piece and
+// zero-list counts, the bucket sizes [nb] and the selected-row bitmap
+// [nb * 8 words] (these three cleared per call, one memset), the scatter
+// cursors [nb], the buckets' first sparse-output slots [nb], the items
+// [max_items], the bucketed selection numbers [E], the piece records [E] and
+// the sparse output's slots to clear [E].
+enum { kOffHead, kOffCount, kOffBitmap, kOffCursor, kOffRowOff, kOffItems, kOffList, kOffPieces,
+       kOffZero, kOffEnd };
 static void read_layout(int64_t N, int64_t E, size_t* off, int64_t* nb_out, int64_t* items_out) {
   const int64_t nb = (N + kRowsPerBucket - 1) / kRowsPerBucket;
   const int64_t items = std::min(nb, E) + E / kChunk + 1;
-  off[0] = 0;                                   // n_items, n_pieces
-  off[1] = off[0] + 256;                        // bcount
-  off[2] = off[1] + align256(nb * 4);           // cursor
-  off[3] = off[2] + align256(nb * 4);           // items
-  off[4] = off[3] + align256(items * 16);       // list
-  off[5] = off[4] + align256(E * 4);            // pieces
-  off[6] = off[5] + align256(E * sizeof(PieceRec));  // end
+  off[kOffHead] = 0;
+  off[kOffCount] = off[kOffHead] + 256;
+  off[kOffBitmap] = off[kOffCount] + align256(nb * 4);
+  off[kOffCursor] = off[kOffBitmap] + align256(nb * (kRowsPerBucket / 32) * 4);
+  off[kOffRowOff] = off[kOffCursor] + align256(nb * 4);
+  off[kOffItems] = off[kOffRowOff] + align256(nb * 4);
+  off[kOffList] = off[kOffItems] + align256(items * 16);
+  off[kOffPieces] = off[kOffList] + align256(E * 4);
+  off[kOffZero] = off[kOffPieces] + align256(E * sizeof(PieceRec));
+  off[kOffEnd] = off[kOffZero] + align256(E * 4);
   *nb_out = nb;
   *items_out = items;
 }
 
 size_t backward_read_workspace_bytes(int B, int H, int n_keys, int k) {
-  size_t off[7];
+  size_t off[kOffEnd + 1];
   int64_t nb, items;
   read_layout((int64_t)n_keys * n_keys, (int64_t)B * H * k, off, &nb, &items);
-  return off[6];
+  return off[kOffEnd];
 }
 
 size_t backward_scores_workspace_bytes(int B, int H, int n_keys) {
@@ -597,45 +661,61 @@ size_t backward_workspace_bytes(int B, int H, int n_keys, int k) {
 
 cudaError_t launch_backward_read(const void* values, int value_dtype, int B, int H, int n_keys,
                                  int d_v, int k, const int64_t* idx, const float* w,
-                                 const float* dout, float* dw, float* dvalues, void* workspace,
-                                 int* status, cudaStream_t stream) {
-  if (B == 0) return cudaSuccess;
+                                 const float* dout, float* dw, float* dvalues, int64_t* rows_out,
+                                 float* grad_rows, int* n_rows, void* workspace, int* status,
+                                 cudaStream_t stream) {
+  const bool sparse = rows_out != nullptr;
   const int64_t N = (int64_t)n_keys * n_keys, E = (int64_t)B * H * k;
   if (E > INT32_MAX || (int64_t)B * d_v / 4 > INT32_MAX) return cudaErrorInvalidValue;
-  size_t off[7];
+  size_t off[kOffEnd + 1];
   int64_t nb, max_items;
   read_layout(N, E, off, &nb, &max_items);
   if (nb > INT32_MAX || max_items > INT32_MAX) return cudaErrorInvalidValue;
   unsigned char* ws = static_cast<unsigned char*>(workspace);
-  int* n_items = reinterpret_cast<int*>(ws + off[0]);
+  int* n_items = reinterpret_cast<int*>(ws + off[kOffHead]);
   int* n_pieces = n_items + 1;
-  int* bcount = reinterpret_cast<int*>(ws + off[1]);
-  int* cursor = reinterpret_cast<int*>(ws + off[2]);
-  int4* items = reinterpret_cast<int4*>(ws + off[3]);
-  int* list = reinterpret_cast<int*>(ws + off[4]);
-  PieceRec* pieces = reinterpret_cast<PieceRec*>(ws + off[5]);
-  cudaError_t e = cudaMemsetAsync(ws, 0, off[2], stream);
+  int* n_zero = n_items + 2;
+  int* bcount = reinterpret_cast<int*>(ws + off[kOffCount]);
+  uint32_t* bitmap = sparse ? reinterpret_cast<uint32_t*>(ws + off[kOffBitmap]) : nullptr;
+  int* cursor = reinterpret_cast<int*>(ws + off[kOffCursor]);
+  int* rowoff = reinterpret_cast<int*>(ws + off[kOffRowOff]);
+  int4* items = reinterpret_cast<int4*>(ws + off[kOffItems]);
+  int* list = reinterpret_cast<int*>(ws + off[kOffList]);
+  PieceRec* pieces = reinterpret_cast<PieceRec*>(ws + off[kOffPieces]);
+  int* zero_list = reinterpret_cast<int*>(ws + off[kOffZero]);
+  cudaError_t e =
+      cudaMemsetAsync(ws, 0, sparse ? off[kOffCursor] : off[kOffBitmap], stream);
   if (e != cudaSuccess) return e;
+  if (sparse) {  // no row selected yet
+    e = cudaMemsetAsync(n_rows, 0, sizeof(int), stream);
+    if (e != cudaSuccess) return e;
+  }
+  if (B == 0) return cudaSuccess;
   const int sms = tc::sm_count();
   const int grid = (int)std::min<int64_t>((E + 255) / 256, (int64_t)sms * 8);
-  bucket_count_kernel<<<grid, 256, 0, stream>>>(idx, (int)E, N, bcount, dw, status);
-  bucket_scan_kernel<<<1, 1024, 0, stream>>>(bcount, (int)nb, cursor, items, n_items);
+  bucket_count_kernel<<<grid, 256, 0, stream>>>(idx, (int)E, N, bcount, bitmap, dw, status);
+  bucket_scan_kernel<<<1, 1024, 0, stream>>>(bcount, (int)nb, cursor, items, n_items, bitmap,
+                                             rowoff, n_rows);
   bucket_scatter_kernel<<<grid, 256, 0, stream>>>(idx, (int)E, N, cursor, list);
   bucket_sort_kernel<<<(unsigned)max_items, kReadWarps * 32, 0, stream>>>(
-      idx, w, H * k, items, n_items, list, pieces, n_pieces);
+      idx, w, H * k, items, n_items, list, pieces, n_pieces, bitmap, rowoff, rows_out, zero_list,
+      n_zero);
+  if (sparse)
+    zero_rows_kernel<<<sms * 4, 256, 0, stream>>>(zero_list, n_zero, d_v, grad_rows);
+  float* out_rows = sparse ? grad_rows : dvalues;
   const size_t sm = (size_t)kRgWarps * kRgStages * (kStageBytes + sizeof(StageMeta));
   if (value_dtype == PKM_BF16) {
     e = cudaFuncSetAttribute(row_grad_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)sm);
     if (e != cudaSuccess) return e;
-    row_grad_kernel<true><<<kRgCtas * sms, kRgWarps * 32, sm, stream>>>(values, d_v, dout, pieces,
-                                                                  n_pieces, dw, dvalues);
+    row_grad_kernel<true><<<kRgCtas * sms, kRgWarps * 32, sm, stream>>>(
+        values, d_v, dout, pieces, n_pieces, dw, out_rows, sparse);
   } else {
     e = cudaFuncSetAttribute(row_grad_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)sm);
     if (e != cudaSuccess) return e;
-    row_grad_kernel<false><<<kRgCtas * sms, kRgWarps * 32, sm, stream>>>(values, d_v, dout, pieces,
-                                                                   n_pieces, dw, dvalues);
+    row_grad_kernel<false><<<kRgCtas * sms, kRgWarps * 32, sm, stream>>>(
+        values, d_v, dout, pieces, n_pieces, dw, out_rows, sparse);
   }
   return cudaGetLastError();
 }

@@ -275,22 +275,44 @@ static void* backward_region(pkm_t h) {
          pkm::backward_dw_bytes(h->cfg.max_B, h->cfg.max_H, h->cfg.max_k);
 }
 
-int pkm_backward_read(pkm_t h, const void* values, int B, int H, int n_keys, int k,
-                      const int64_t* idx, const float* w, const float* dout, float* dw,
-                      float* dvalues, void* stream) {
+// The read part, dense (rows == NULL: dvalues added to) or sparse.
+static int backward_read(pkm_t h, const void* values, int B, int H, int n_keys, int k,
+                         const int64_t* idx, const float* w, const float* dout, float* dw,
+                         float* dvalues, int64_t* rows, float* grad_rows, int* n_rows,
+                         void* stream) {
   if (!h) return PKM_ERR_INVALID;
   int rc = check_call(&h->cfg, B, H, n_keys, k);
   if (rc) return rc;
   if (!h->cfg.with_backward) return PKM_ERR_NO_BACKWARD;
-  if (B == 0) return PKM_OK;
-  if (!values || !idx || !w || !dout || !dw || !dvalues) return PKM_ERR_INVALID;
+  const bool sparse = rows != nullptr || grad_rows != nullptr || n_rows != nullptr;
+  if (sparse && (!rows || !grad_rows || !n_rows)) return PKM_ERR_INVALID;
+  if (!sparse && B == 0) return PKM_OK;
+  if (B > 0 && (!values || !idx || !w || !dout || !dw || (!sparse && !dvalues)))
+    return PKM_ERR_INVALID;
   for (const void* p : {values, (const void*)idx, (const void*)w, (const void*)dout,
-                        (const void*)dw, (const void*)dvalues})
-    if (!aligned16(p)) return PKM_ERR_ALIGN;
+                        (const void*)dw, (const void*)dvalues, (const void*)rows,
+                        (const void*)grad_rows})
+    if (p && !aligned16(p)) return PKM_ERR_ALIGN;
   return cuda_rc(pkm::launch_backward_read(values, h->cfg.value_dtype, B, H, n_keys,
-                                           h->cfg.d_v, k, idx, w, dout, dw, dvalues,
-                                           backward_region(h), h->status,
+                                           h->cfg.d_v, k, idx, w, dout, dw, dvalues, rows,
+                                           grad_rows, n_rows, backward_region(h), h->status,
                                            static_cast<cudaStream_t>(stream)));
+}
+
+int pkm_backward_read(pkm_t h, const void* values, int B, int H, int n_keys, int k,
+                      const int64_t* idx, const float* w, const float* dout, float* dw,
+                      float* dvalues, void* stream) {
+  if (!dvalues && B > 0) return PKM_ERR_INVALID;
+  return backward_read(h, values, B, H, n_keys, k, idx, w, dout, dw, dvalues, nullptr, nullptr,
+                       nullptr, stream);
+}
+
+int pkm_backward_read_sparse(pkm_t h, const void* values, int B, int H, int n_keys, int k,
+                             const int64_t* idx, const float* w, const float* dout, float* dw,
+                             int64_t* rows, float* grad_rows, int* n_rows, void* stream) {
+  if (!rows || !grad_rows || !n_rows) return PKM_ERR_INVALID;
+  return backward_read(h, values, B, H, n_keys, k, idx, w, dout, dw, nullptr, rows, grad_rows,
+                       n_rows, stream);
 }
 
 int pkm_backward_scores(pkm_t h, const void* q, const void* subkeys, int B, int H, int n_keys,
@@ -312,20 +334,37 @@ int pkm_backward_scores(pkm_t h, const void* q, const void* subkeys, int B, int 
       static_cast<cudaStream_t>(stream)));
 }
 
-int pkm_backward(pkm_t h, const void* q, const void* subkeys, const void* values, int B, int H,
-                 int n_keys, int k, const int64_t* idx, const float* w, const float* dout,
-                 float* dq, float* dsubkeys, float* dvalues, void* stream) {
+static int backward_all(pkm_t h, const void* q, const void* subkeys, const void* values, int B,
+                        int H, int n_keys, int k, const int64_t* idx, const float* w,
+                        const float* dout, float* dq, float* dsubkeys, float* dvalues,
+                        int64_t* rows, float* grad_rows, int* n_rows, void* stream) {
   if (!h) return PKM_ERR_INVALID;
   int rc = check_call(&h->cfg, B, H, n_keys, k);
   if (rc) return rc;
   if (!h->cfg.with_backward) return PKM_ERR_NO_BACKWARD;
-  if (B == 0) return PKM_OK;
-  if (!q || !subkeys || !values || !idx || !w || !dout || !dq || !dsubkeys || !dvalues)
-    return PKM_ERR_INVALID;
+  if (B > 0 && (!q || !subkeys || !dq || !dsubkeys)) return PKM_ERR_INVALID;
   float* dw = static_cast<float*>(h->bwd_ws);
-  rc = pkm_backward_read(h, values, B, H, n_keys, k, idx, w, dout, dw, dvalues, stream);
-  if (rc) return rc;
+  rc = backward_read(h, values, B, H, n_keys, k, idx, w, dout, dw, dvalues, rows, grad_rows,
+                     n_rows, stream);
+  if (rc || B == 0) return rc;
   return pkm_backward_scores(h, q, subkeys, B, H, n_keys, k, idx, w, dw, dq, dsubkeys, stream);
+}
+
+int pkm_backward(pkm_t h, const void* q, const void* subkeys, const void* values, int B, int H,
+                 int n_keys, int k, const int64_t* idx, const float* w, const float* dout,
+                 float* dq, float* dsubkeys, float* dvalues, void* stream) {
+  if (!dvalues && B > 0) return PKM_ERR_INVALID;
+  return backward_all(h, q, subkeys, values, B, H, n_keys, k, idx, w, dout, dq, dsubkeys, dvalues,
+                      nullptr, nullptr, nullptr, stream);
+}
+
+int pkm_backward_sparse(pkm_t h, const void* q, const void* subkeys, const void* values, int B,
+                        int H, int n_keys, int k, const int64_t* idx, const float* w,
+                        const float* dout, float* dq, float* dsubkeys, int64_t* rows,
+                        float* grad_rows, int* n_rows, void* stream) {
+  if (!rows || !grad_rows || !n_rows) return PKM_ERR_INVALID;
+  return backward_all(h, q, subkeys, values, B, H, n_keys, k, idx, w, dout, dq, dsubkeys, nullptr,
+                      rows, grad_rows, n_rows, stream);
 }
 
 // The host-buffer forward: the batch in slices, each slice's copy in on s_in,

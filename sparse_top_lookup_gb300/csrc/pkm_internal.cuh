@@ -25,23 +25,26 @@ cudaError_t launch_qnet(const uint16_t* x, const uint16_t* w, int B, int dim, in
                         cudaStream_t stream);
 
 // Backward pass for a fixed selection (backward.cu), in two parts.
-// Read part: dw = dout . V[idx] (overwritten), dvalues[idx] += w * dout;
-// bf16 or fp32 values; B*H*k < 2^31; workspace:
-// backward_read_workspace_bytes.  Score part: dq overwritten and dsubkeys
-// added to, from w, dw and the selection; bf16 queries/subkeys, k <= 32;
-// workspace: backward_scores_workspace_bytes (the dense bf16 per-subkey
-// score-gradient rows [2H][B][n_keys]); blas_workspace: the cuBLAS handle's
-// workspace (re-attached after its stream is set).  A handle's backward
-// scratch is backward_workspace_bytes: dw (backward_dw_bytes), then one
-// region the two parts take in turn.
+// Read part: dw = dout . V[idx] (overwritten) and the value-table gradient,
+// either added to the dense dvalues (rows_out == NULL) or written sparse:
+// the distinct selected rows ascending in rows_out[0 .. *n_rows) and their
+// gradients in grad_rows [*n_rows, d_v]; bf16 or fp32 values; B*H*k < 2^31;
+// workspace: backward_read_workspace_bytes.  Score part: dq overwritten and
+// dsubkeys added to, from w, dw and the selection; bf16 queries/subkeys,
+// k <= 32; workspace: backward_scores_workspace_bytes (the dense bf16
+// per-subkey score-gradient rows [2H][B][n_keys]); blas_workspace: the
+// cuBLAS handle's workspace (re-attached after its stream is set).  A
+// handle's backward scratch is backward_workspace_bytes: dw
+// (backward_dw_bytes), then one region the two parts take in turn.
 size_t backward_workspace_bytes(int B, int H, int n_keys, int k);
 size_t backward_dw_bytes(int B, int H, int k);
 size_t backward_read_workspace_bytes(int B, int H, int n_keys, int k);
 size_t backward_scores_workspace_bytes(int B, int H, int n_keys);
 cudaError_t launch_backward_read(const void* values, int value_dtype, int B, int H, int n_keys,
                                  int d_v, int k, const int64_t* idx, const float* w,
-                                 const float* dout, float* dw, float* dvalues, void* workspace,
-                                 int* status, cudaStream_t stream);
+                                 const float* dout, float* dw, float* dvalues, int64_t* rows_out,
+                                 float* grad_rows, int* n_rows, void* workspace, int* status,
+                                 cudaStream_t stream);
 cudaError_t launch_backward_scores(cublasHandle_t blas, const uint16_t* q,
                                    const uint16_t* subkeys, int B, int H, int d_q, int n_keys,
                                    int k, const int64_t* idx, const float* w, const float* dw,

@@ -52,6 +52,12 @@ CONFIGS = {
     "page_train": dict(cfg_id=2, B=16384, H=4, d_q=1024, n_keys=1024, d_v=1024, k=32,
                        dtype="bf16", q_var=1.0, key_var=1.0 / 512, value_var=1.0 / 1024,
                        q_kind="normal", train=True),
+    # the same training step with the value-table gradient in sparse form
+    # (distinct selected rows and their gradient rows) instead of added to a
+    # dense fp32 table.
+    "page_train_sparse": dict(cfg_id=2, B=16384, H=4, d_q=1024, n_keys=1024, d_v=1024, k=32,
+                              dtype="bf16", q_var=1.0, key_var=1.0 / 512, value_var=1.0 / 1024,
+                              q_kind="normal", train=True, sparse_grad=True),
     # 16 GiB value table.
     "large": dict(cfg_id=4, B=32768, H=4, d_q=2048, n_keys=2048, d_v=2048, k=32, dtype="bf16",
                   q_var=1.0, key_var=1.0 / 1024, value_var=1.0 / 2048, q_kind="normal"),

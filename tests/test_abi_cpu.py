@@ -99,6 +99,10 @@ def test_null_handle_rejected_before_any_cuda_call(L):
         == pk.PKM_ERR_INVALID
     assert L.pkm_backward_scores(None, 16, 16, 1, 1, 1, 1, 16, 16, 16, 16, 16, None) \
         == pk.PKM_ERR_INVALID
+    assert L.pkm_backward_sparse(None, 16, 16, 16, 1, 1, 1, 1, 16, 16, 16, 16, 16, 16, 16, 16,
+                                 None) == pk.PKM_ERR_INVALID
+    assert L.pkm_backward_read_sparse(None, 16, 1, 1, 1, 1, 16, 16, 16, 16, 16, 16, 16, None) \
+        == pk.PKM_ERR_INVALID
     L.pkm_destroy(None)
     assert L.pkm_create(None, None) == pk.PKM_ERR_INVALID
     h = vp()

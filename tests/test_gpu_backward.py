@@ -206,6 +206,83 @@ def test_backward_concentrated_selection(vdt):
     check_against_oracle(q, C, V, vdt, B, H, d_q, n, d_v, k, idx, w, dout, got)
 
 
+def run_backward_sparse(q, C, V, vdt, B, H, d_q, n, d_v, k, idx, w, dout):
+    """pkm_backward_sparse; returns (dq, dC, rows, grad_rows, status)."""
+    cfg = pk.make_config(d_q, d_v, B, H, n, k, q_dtype=pk.PKM_BF16,
+                         value_dtype=pk.PKM_F32 if vdt == "f32" else pk.PKM_BF16,
+                         with_backward=1)
+    h = pk.pkm_create(cfg)
+    try:
+        E = B * H * k
+        tq, tC, tV = to_device(q, "bf16"), to_device(C, "bf16"), to_device(V, vdt)
+        tidx = torch.from_numpy(np.ascontiguousarray(idx, np.int64)).cuda()
+        tw = torch.from_numpy(np.ascontiguousarray(w, np.float32)).cuda()
+        tdout = torch.from_numpy(np.ascontiguousarray(dout, np.float32)).cuda()
+        dq = torch.full((B, H, d_q), float("nan"), device="cuda")
+        dC = torch.zeros(H, 2, n, d_q // 2, device="cuda")
+        rows = torch.full((E,), -7, dtype=torch.int64, device="cuda")
+        grad = torch.full((E, d_v), float("nan"), device="cuda")
+        nr = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+        pk.check(pk.pkm_backward_sparse(h, tq, tC, tV, B, H, n, k, tidx, tw, tdout, dq, dC, rows,
+                                        grad, nr), "pkm_backward_sparse")
+        status = pk.pkm_get_status(h)
+        m = int(nr.item())
+        return (dq.cpu().numpy(), dC.cpu().numpy(), rows[:m].cpu().numpy(),
+                grad[:m].cpu().numpy(), status)
+    finally:
+        pk.pkm_destroy(h)
+
+
+def concentrated_case(vdt):
+    B, H, d_q, n, d_v, k = 300, 2, 64, 64, 128, 16
+    s = synth.seed_of(dict(cfg_id=140))
+    q = synth.normal(s, 1, B * H * d_q, 1.0, dtype="bf16")
+    C = synth.normal(s, 2, H * 2 * n * (d_q // 2), 2.0 / d_q, dtype="bf16")
+    V = synth.normal(s, 3, n * n * d_v, 1.0 / d_v, dtype=vdt)
+    dout = synth.normal(s, 15, B * d_v, 1.0).reshape(B, d_v).astype(np.float64)
+    u = synth.uniform(s, 12, B * H * k).reshape(B, H, k)
+    idx = np.minimum((u * 300).astype(np.int64), 299)
+    idx[:, 0, 0] = 4000
+    e = -np.log1p(-synth.uniform(s, 14, B * H * k)).reshape(B, H, k)
+    w = (e / e.sum(-1, keepdims=True)).astype(np.float32)
+    return (B, H, d_q, n, d_v, k), q, C, V, idx, w, dout
+
+
+@pytest.mark.parametrize("case", ["lookup", "concentrated_bf16", "concentrated_f32", "bad_index"])
+def test_backward_sparse_matches_oracle(case):
+    # the sparse value-table gradient: the distinct selected rows (ascending,
+    # exact) and their gradients (fp32 bound); dq and dsubkeys as the dense form
+    if case.startswith("concentrated"):
+        vdt = case.split("_")[1]
+        (B, H, d_q, n, d_v, k), q, C, V, idx, w, dout = concentrated_case(vdt)
+    else:
+        vdt = "bf16"
+        B, H, d_q, n, d_v, k = 200, 2, 128, 64, 256, 16
+        q, C, V, idx, w, dout = lookup_case(21, B, H, d_q, n, d_v, k)
+    gidx = idx.copy()
+    if case == "bad_index":
+        gidx[3, 1, 5] = -1  # left out of the rows, recorded in the status
+    gdq, gdC, rows, grad, status = run_backward_sparse(q, C, V, vdt, B, H, d_q, n, d_v, k, gidx, w,
+                                                       dout)
+    assert status == (pk.PKM_ERR_BAD_INDEX if case == "bad_index" else pk.PKM_OK)
+    valid = gidx[gidx >= 0]
+    want_rows = np.unique(valid)
+    assert np.array_equal(rows, want_rows)
+    if case == "bad_index":
+        return
+    ref = oracle.backward(q, C, V, B, H, d_q, n, d_v, k, idx, w.astype(np.float64), dout,
+                          dvalue_rows=rows)
+    w64 = w.astype(np.float64)
+    # (the bound counts a starting value DV0 the sparse rows do not have: looser by that term)
+    assert (np.abs(grad - ref["dvalues"]) <= dvalue_bound(idx, w64, dout, rows)).all()
+    q64 = widen(q, "bf16").reshape(B, H, d_q)
+    C64 = widen(C, "bf16").reshape(H, 2, n, d_q // 2)
+    Vsel = widen(V.reshape(n * n, d_v)[idx.ravel()], vdt).reshape(B, H, k, d_v)
+    tol_dq, tol_dC, _ = gpu_error_bounds(q64, C64, Vsel, idx, w64, dout, ref["dw"], n, k, B)
+    assert (np.abs(gdq - ref["dq"]) <= tol_dq).all()
+    assert (np.abs(gdC - ref["dsubkeys"]) <= tol_dC).all()
+
+
 def test_backward_single_winner_closed_form():
     # k = 1: w = 1, so ds = 0: dq is exactly 0, dsubkeys unchanged, and
     # dvalues[idx] gains the dout of every query that selected it
