@@ -184,7 +184,8 @@ int pkm_forward_host(pkm_t h, const void *q_host, const void *subkeys, const voi
  * one call run while the previous call computes; a third call's copies wait
  * (on the device) until the first call's results are copied back.  The batch
  * is one slice unless PKM_OPT_HOST_CHUNKS was set on the handle (the call in
- * flight beside it already hides the copies).
+ * flight beside it already hides the copies).  Calls in flight on one handle
+ * share its lookup scratch, so they must be enqueued on the same stream.
  */
 int pkm_forward_host_async(pkm_t h, const void *q_host, const void *subkeys, const void *values,
                            int B, int H, int n_keys, int k, float *out_host, int64_t *idx_host,
