@@ -70,3 +70,58 @@ def test_static_lookup_matches_handle_lookup_on_two_calls_in_a_row():
         assert torch.equal(idx, idx_ref)
         ref = w_ref.double()
         assert ((w.double() - ref).abs() <= 2e-3 * (1 + ref.abs())).all()
+
+
+@pytest.mark.gpu
+def test_handle_calls_do_not_allocate_after_warm_up():
+    # pkm_create is the only call that allocates: after one warm-up call of
+    # each entry point (which may load kernels), repeated calls leave the
+    # device's free memory unchanged
+    torch = pytest.importorskip("torch")
+    pk = pytest.importorskip("sparse_top_lookup_gb300")
+    B, H, d_q, n, d_v, k = 256, 2, 128, 128, 128, 16
+    s = 55
+
+    def dev(a):
+        return torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16)
+
+    q_np = synth.normal(s, 1, B * H * d_q, 1.0, dtype="bf16")
+    q, C = dev(q_np), dev(synth.normal(s, 2, H * 2 * n * (d_q // 2), 2.0 / d_q, dtype="bf16"))
+    V = dev(synth.normal(s, 3, n * n * d_v, 1.0 / d_v, dtype="bf16"))
+    cfg = pk.make_config(d_q, d_v, B, H, n, k, q_dtype=pk.PKM_BF16, host_staging=1,
+                         with_backward=1)
+    h = pk.pkm_create(cfg)
+    try:
+        out = torch.empty(B, d_v, device="cuda")
+        idx = torch.empty(B, H, k, dtype=torch.int64, device="cuda")
+        w = torch.empty(B, H, k, device="cuda")
+        dout = torch.randn(B, d_v, device="cuda", generator=torch.Generator("cuda").manual_seed(1))
+        dq = torch.empty(B, H, d_q, device="cuda")
+        dC = torch.zeros(H, 2, n, d_q // 2, device="cuda")
+        dVt = torch.zeros(n * n, d_v, device="cuda")
+        rows = torch.empty(B * H * k, dtype=torch.int64, device="cuda")
+        grad = torch.empty(B * H * k, d_v, device="cuda")
+        nr = torch.zeros(1, dtype=torch.int32, device="cuda")
+        qh = torch.from_numpy(q_np.view(np.int16)).pin_memory()
+        oh = torch.empty(B, d_v).pin_memory()
+        ev = torch.cuda.Event()
+
+        def round_of_calls():
+            pk.check(pk.pkm_forward(h, q, C, V, B, H, n, k, out, idx, w), "forward")
+            pk.check(pk.pkm_backward(h, q, C, V, B, H, n, k, idx, w, dout, dq, dC, dVt),
+                     "backward")
+            pk.check(pk.pkm_backward_sparse(h, q, C, V, B, H, n, k, idx, w, dout, dq, dC, rows,
+                                            grad, nr), "backward_sparse")
+            pk.check(pk.pkm_forward_host(h, qh, C, V, B, H, n, k, oh), "forward_host")
+            pk.check(pk.pkm_forward_host_async(h, qh, C, V, B, H, n, k, oh, ev), "async")
+            ev.synchronize()
+            torch.cuda.synchronize()
+
+        round_of_calls()
+        free0 = torch.cuda.mem_get_info()[0]
+        for _ in range(3):
+            round_of_calls()
+        assert torch.cuda.mem_get_info()[0] == free0
+        assert pk.pkm_get_status(h) == pk.PKM_OK
+    finally:
+        pk.pkm_destroy(h)
