@@ -92,6 +92,8 @@ def random_case(seed, B, H, d_q, n, d_v, k, dtype="bf16", kvar=None):
     (64, 2, 256, 48, 128, 1),       # k = 1: argmax per half
     (40, 1, 32, 20, 64, 20),        # k = n_keys: every key is a candidate
     (129, 2, 1024, 1024, 1024, 32),  # page-width rows, small batch
+    (64, 8, 256, 256, 128, 32),     # eight heads (the skewed workload's H)
+    (70, 1, 128, 2048, 64, 32),     # 16 chunks per half (the large workload's n_keys)
 ])
 def test_bf16_shapes(shape):
     c, q, C, V = random_case(sum(shape), *shape)
