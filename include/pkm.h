@@ -1,6 +1,11 @@
 /*
- * pkm.h - C ABI of the product-key memory (PKM) lookup forward pass on one
- * NVIDIA GB300 GPU (sm_103a).
+ * pkm.h - C ABI of the product-key memory (PKM) lookup on one NVIDIA GB300
+ * GPU (sm_103a): the forward pass (pkm_forward; its two stages pkm_lookup and
+ * pkm_gather; pkm_forward_host / pkm_forward_host_async with host buffers;
+ * the allocation-free pkm_lookup_static), its backward pass for the selection
+ * it made (pkm_backward, pkm_backward_sparse and their two parts), the query
+ * network ahead of it (pkm_bn_fold, pkm_query_net) and the fp8 value-table
+ * quantiser (pkm_quantize_values_fp8).
  *
  * The operation (Product-Key Memory, "Factorising the key space", and the
  * forward method of the page's code listing; Memory Retrieval Mechanisms,
@@ -54,8 +59,8 @@
  * pkm_get_status and pkm_forward_host, which synchronise `stream`
  * (pkm_forward_host_async signals an event instead).  Results are
  * valid once the stream has been synchronised.  Calls on one handle must not
- * overlap on the GPU when they use the handle's scratch (idx/w == NULL, and
- * every pkm_backward).
+ * overlap on the GPU when they use the handle's scratch (idx/w == NULL, every
+ * backward call, every host-buffer call).
  *
  * Errors: every call returns PKM_OK (0) or a negative code, checked on the
  * host before anything is launched.  Device-side failures (an out-of-range
