@@ -110,7 +110,13 @@ enum {
      default 3) pipelined so the copy of slice i+1 in and of slice i-1 out
      overlap the computation of slice i; the first and last slices are half
      the size of the others (shorter pipeline fill and drain). */
-  PKM_OPT_HOST_CHUNKS = 2
+  PKM_OPT_HOST_CHUNKS = 2,
+  /* Tests of failure reporting only (1 on, 0 off): while on, the bf16
+     lookups of this handle run their selection kernel with its loads held
+     back, so the kernel's bounded pipeline wait runs out (about 2 s), it
+     records PKM_ERR_TIMEOUT in the status word and returns; results of such
+     calls are not meaningful.  The GPU context stays usable. */
+  PKM_OPT_TEST_STALL = 3
 };
 #define PKM_HOST_MAX_CHUNKS 16
 

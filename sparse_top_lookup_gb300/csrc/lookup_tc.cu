@@ -194,7 +194,7 @@ select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
                  int B, int H, int n, int NC, int nch, int kb_count, float hint_z,
                  float* __restrict__ list_v, unsigned short* __restrict__ list_c,
                  int* __restrict__ status, const int* __restrict__ unit_list,
-                 const int* __restrict__ unit_count) {
+                 const int* __restrict__ unit_count, int stall) {
   extern __shared__ unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t bars[2 * STAGES + 4 * SETS + 1];
   __shared__ uint32_t s_tmem_base;
@@ -255,7 +255,10 @@ select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
 
   if (warp == 0) {
     // ---------------------------------------------------- TMA producer
-    if (lane == 0) {
+    // (stall: a test of the bounded waits; nothing is loaded, so the MMA
+    // warp's first wait runs out, the kernel records PKM_ERR_TIMEOUT and every
+    // warp returns; no copy is ever in flight)
+    if (lane == 0 && !stall) {
       const uint32_t tx = (uint32_t)(A_BYTES + NC * BK * 2);
       uint32_t it = 0;
       bool ok = true;
@@ -465,7 +468,7 @@ select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
 template <int KL>
 cudaError_t launch_kl(const CUtensorMap& mq, const CUtensorMap& mc, int B, int H, int n, int NC,
                       int nch, int kbc, float hint_z, float* list_v, unsigned short* list_c,
-                      int* status, const int* unit_list, const int* unit_count,
+                      int* status, const int* unit_list, const int* unit_count, int stall,
                       cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
@@ -477,7 +480,8 @@ cudaError_t launch_kl(const CUtensorMap& mq, const CUtensorMap& mc, int B, int H
   const int units = (B + BM - 1) / BM * H * 2;  // also the most a retry can list
   const int grid = units < sm_count() ? units : sm_count();  // persistent: one CTA per SM
   select_tc_kernel<KL><<<grid, NUM_THREADS, SMEM_TOTAL, stream>>>(
-      mq, mc, B, H, n, NC, nch, kbc, hint_z, list_v, list_c, status, unit_list, unit_count);
+      mq, mc, B, H, n, NC, nch, kbc, hint_z, list_v, list_c, status, unit_list, unit_count,
+      stall);
   return cudaGetLastError();
 }
 
@@ -511,7 +515,7 @@ int list_slots(int k) { return k <= 16 ? 16 : 32; }
 cudaError_t launch_lookup_tc(const uint16_t* q, const uint16_t* subkeys, int B, int H, int d_q,
                              int n_keys, int k, float hint_z, int64_t* idx, float* w, int* status,
                              const RetryScratch& retry, float* list_v, unsigned short* list_c,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, bool stall) {
   if (B == 0) return cudaSuccess;
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
@@ -544,23 +548,23 @@ cudaError_t launch_lookup_tc(const uint16_t* q, const uint16_t* subkeys, int B, 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  auto select = [&](float z, const int* list, const int* count) {
+  auto select = [&](float z, const int* list, const int* count, int st) {
     return k <= 16 ? launch_kl<16>(mq, mc, B, H, n_keys, NC, nch, kbc, z, list_v, list_c, status,
-                                   list, count, stream)
+                                   list, count, st, stream)
                    : launch_kl<32>(mq, mc, B, H, n_keys, NC, nch, kbc, z, list_v, list_c, status,
-                                   list, count, stream);
+                                   list, count, st, stream);
   };
   // the retry bookkeeping starts clear: counts and the per-unit flags (one buffer)
   cudaError_t e =
       cudaMemsetAsync(retry.counts, 0, (2 + (size_t)retry_units(B, H)) * sizeof(int), stream);
-  if (e == cudaSuccess) e = select(hint_z, nullptr, nullptr);
+  if (e == cudaSuccess) e = select(hint_z, nullptr, nullptr, stall ? 1 : 0);
   // a4, a5: the k^2 merge and softmax, one thread per (query, head); lists
   // the units whose threshold hint was above a row's KL-th score
   if (e == cudaSuccess)
     e = launch_merge(list_v, list_c, B, H, n_keys, k, idx, w, retry, false, stream);
   // retry: those units again without the hint (exact), then their pairs;
   // both launches return at once when nothing is listed
-  if (e == cudaSuccess) e = select(-INFINITY, retry.unit_list, retry.counts + 1);
+  if (e == cudaSuccess) e = select(-INFINITY, retry.unit_list, retry.counts + 1, 0);
   if (e == cudaSuccess)
     e = launch_merge(list_v, list_c, B, H, n_keys, k, idx, w, retry, true, stream);
   return e;

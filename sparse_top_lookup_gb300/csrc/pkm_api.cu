@@ -36,6 +36,7 @@ struct pkm_handle {
   cudaEvent_t ev_done[2], ev_in[PKM_HOST_MAX_CHUNKS], ev_comp[PKM_HOST_MAX_CHUNKS];
   int host_chunks;
   bool host_chunks_set;  // PKM_OPT_HOST_CHUNKS given by the caller
+  int test_stall;        // PKM_OPT_TEST_STALL: the bf16 lookups stall their selection kernel
 };
 
 namespace {
@@ -93,7 +94,7 @@ int run_lookup(pkm_t h, const void* q, const void* subkeys, int B, int H, int n,
                                          static_cast<const uint16_t*>(subkeys), B, H, h->cfg.d_q,
                                          n, k, z, idx, w, h->status,
                                          {h->retry_counts, h->retry_counts + 2, h->unit_list},
-                                         h->list_v, h->list_c, s));
+                                         h->list_v, h->list_c, s, h->test_stall != 0));
   }
   return cuda_rc(pkm::launch_lookup_simt(static_cast<const float*>(q),
                                          static_cast<const float*>(subkeys), B, H, h->cfg.d_q, n,
@@ -470,6 +471,10 @@ int pkm_set_option(pkm_t h, int option, double value) {
         return PKM_ERR_OPTION;
       h->host_chunks = (int)value;
       h->host_chunks_set = true;
+      return PKM_OK;
+    case PKM_OPT_TEST_STALL:
+      if (value != 0 && value != 1) return PKM_ERR_OPTION;
+      h->test_stall = (int)value;
       return PKM_OK;
     default:
       return PKM_ERR_OPTION;

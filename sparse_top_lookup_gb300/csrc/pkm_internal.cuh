@@ -84,10 +84,13 @@ int64_t retry_units(int64_t B, int64_t H);
 // first scores; any value gives exact results).  list_v / list_c
 // (B*H*2*list_slots(k) floats and 16-bit subkeys) hold the per-half lists
 // between the kernels.
+// stall (tests of the bounded waits only): the first selection launch loads
+// nothing, so its pipeline wait runs out (about 2 s) and it records
+// PKM_ERR_TIMEOUT; the lists it leaves are not meaningful.
 cudaError_t launch_lookup_tc(const uint16_t* q, const uint16_t* subkeys, int B, int H, int d_q,
                              int n_keys, int k, float hint_z, int64_t* idx, float* w, int* status,
                              const RetryScratch& retry, float* list_v, unsigned short* list_c,
-                             cudaStream_t stream);
+                             cudaStream_t stream, bool stall = false);
 
 // Entries of one per-half list for a given k.
 int list_slots(int k);

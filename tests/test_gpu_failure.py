@@ -1,0 +1,46 @@
+"""Failure reporting on the GPU without a fault: a bounded wait that runs out.
+
+PKM_OPT_TEST_STALL holds back the selection kernel's loads, so the MMA
+warp's wait for its first stage runs out (about 2 s).  The kernel records
+PKM_ERR_TIMEOUT in the status word and every warp returns; the test then
+checks that the status is reported once and that the same context computes
+correct results afterwards.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from helpers import compare_lookup, to_device
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+pk = pytest.importorskip("sparse_top_lookup_gb300")
+
+
+def test_bounded_wait_runs_out_is_reported_and_context_stays_usable():
+    B, H, d_q, n, d_v, k = 256, 1, 128, 256, 64, 16
+    s = synth.seed_of(dict(cfg_id=160))
+    q = synth.normal(s, 1, B * H * d_q, 1.0, dtype="bf16")
+    C = synth.normal(s, 2, H * 2 * n * (d_q // 2), 2.0 / d_q, dtype="bf16")
+    h = pk.pkm_create(pk.make_config(d_q, d_v, B, H, n, k, q_dtype=pk.PKM_BF16))
+    try:
+        tq, tC = to_device(q, "bf16"), to_device(C, "bf16")
+        idx = torch.empty(B, H, k, dtype=torch.int64, device="cuda")
+        w = torch.empty(B, H, k, device="cuda")
+        assert pk.pkm_set_option(h, pk.PKM_OPT_TEST_STALL, 2) == pk.PKM_ERR_OPTION
+        pk.check(pk.pkm_set_option(h, pk.PKM_OPT_TEST_STALL, 1), "set_option")
+        pk.check(pk.pkm_lookup(h, tq, tC, B, H, n, k, idx, w), "pkm_lookup")
+        assert pk.pkm_get_status(h) == pk.PKM_ERR_TIMEOUT
+        assert pk.pkm_get_status(h) == pk.PKM_OK  # reported once, then cleared
+        # the same context, the stall off: exact results again
+        pk.check(pk.pkm_set_option(h, pk.PKM_OPT_TEST_STALL, 0), "set_option")
+        pk.check(pk.pkm_lookup(h, tq, tC, B, H, n, k, idx, w), "pkm_lookup")
+        assert pk.pkm_get_status(h) == pk.PKM_OK
+        ref = oracle.lookup(q, C, B, H, d_q, n, k)
+        res = compare_lookup(idx.cpu().numpy(), w.cpu().numpy(), ref, q, C, "bf16", H, d_q, n)
+        assert res["failures"] == 0 and res["w_ok"], res
+    finally:
+        pk.pkm_destroy(h)
+    torch.cuda.synchronize()
