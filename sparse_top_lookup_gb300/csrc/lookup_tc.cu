@@ -188,9 +188,16 @@ constexpr int SMEM_TOTAL = SMEM_TILES + SETS * LOG_BYTES + 1024;  // + alignment
 // takes unit u_i.  The producer and the MMA walk the units two at a time,
 // chunk by chunk, alternating sets, so both sets are fed; set s's chunks go to
 // TMEM buffers 2s and 2s+1 in turn.
-template <int KL>
+// kPair: clusters of two CTAs on neighbouring row tiles (2j, 2j+1) of the same
+// (head, half), in lockstep, so each subkey slab crosses from L2 once for the
+// pair: CTA rank r loads rows [r NC/2, (r+1) NC/2) of it (tmap_c_half) and
+// multicasts them to both.  A stage is then free only when both CTAs' MMAs
+// have read it: each MMA's release commit arrives on both CTAs' empty
+// barriers.  The pair's units are p_i = cluster + i * clusters.
+template <int KL, bool kPair>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_c,
+                 const __grid_constant__ CUtensorMap tmap_c_half,
                  int B, int H, int n, int NC, int nch, int kb_count, float hint_z,
                  float* __restrict__ list_v, unsigned short* __restrict__ list_c,
                  int* __restrict__ status, const int* __restrict__ unit_list,
@@ -204,11 +211,21 @@ select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
   // unit is entry blockIdx.x + i * gridDim.x of all units, or of unit_list
   // when one is given (a retry launch).  A CTA without units returns at once.
   const int row_tiles = (B + BM - 1) / BM;
-  const int units = unit_list ? *unit_count : row_tiles * H * 2;
-  const int mine = (int)blockIdx.x < units ? (units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-  if (mine == 0) return;
+  // pair mode: the cluster's work item (pair unit) index and count, and this
+  // CTA's rank in it; otherwise the CTA's own
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+  const int slot = kPair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int slots = kPair ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  const int units = kPair ? (row_tiles + 1) / 2 * H * 2
+                          : (unit_list ? *unit_count : row_tiles * H * 2);
+  const int mine = slot < units ? (units - 1 - slot) / slots + 1 : 0;
+  if (mine == 0) return;  // (pair mode: both CTAs of the cluster alike)
   auto unit_at = [&](int i) {
-    const int e = blockIdx.x + i * gridDim.x;
+    const int e = slot + i * slots;
+    if (kPair) {  // pair unit (pair tile, head, half) -> this CTA's row tile of it
+      const int pt = (e >> 1) / H, h = (e >> 1) - ((e >> 1) / H) * H;
+      return ((((2 * pt + (int)rank) * H) + h) << 1) | (e & 1);
+    }
     return unit_list ? unit_list[e] : e;
   };
 
@@ -228,7 +245,7 @@ select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar_full(s), 1);
-      mbar_init(bar_empty(s), 1);
+      mbar_init(bar_empty(s), kPair ? 2 : 1);  // pair: both CTAs' MMAs release it
     }
     for (int b = 0; b < 2 * SETS; ++b) {
       mbar_init(bar_tfull(b), 1);
@@ -249,6 +266,7 @@ select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (kPair) cluster_sync();  // the peer's barriers exist before any multicast reaches them
   const uint32_t tmem = s_tmem_base;
   const Ctl ctl{&s_abort, status};
 
@@ -277,7 +295,12 @@ select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
               mbar_expect_tx(bar_full(s), tx);
               const uint32_t a_dst = tiles_u32 + s * STAGE_BYTES;
               tma_load_4d(a_dst, &tmap_q, kb * BK, half, h, rt * BM, bar_full(s));
-              tma_load_3d(a_dst + A_BYTES, &tmap_c, kb * BK, ch * NC, h * 2 + half, bar_full(s));
+              if (kPair)  // this CTA's half of the subkey slab, to both CTAs
+                tma_load_3d_mc(a_dst + A_BYTES + rank * (NC / 2) * 128, &tmap_c_half, kb * BK,
+                               ch * NC + (int)rank * (NC / 2), h * 2 + half, bar_full(s), 3);
+              else
+                tma_load_3d(a_dst + A_BYTES, &tmap_c, kb * BK, ch * NC, h * 2 + half,
+                            bar_full(s));
               ++it;
             }
           }
@@ -315,7 +338,12 @@ select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
 #pragma unroll
               for (int kk = 0; kk < BK / 16; ++kk)
                 tc_mma(d_tmem, a_desc + 2u * kk, b_desc + 2u * kk, idesc, (kb | kk) != 0);
-              tc_commit(bar_empty(s));  // frees the stage once these MMAs have read it
+              // frees the stage once these MMAs have read it (pair: in both CTAs,
+              // whose halves of the subkey slab it holds)
+              if (kPair)
+                tc_commit_mc(bar_empty(s), 3);
+              else
+                tc_commit(bar_empty(s));
             }
             if (!ok) break;
             tc_commit(bar_tfull(buf));  // chunk complete in TMEM
@@ -461,28 +489,56 @@ select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS)
                  : "memory");
   }
+  // pair: neither CTA leaves while the other may still load into its shared
+  // memory or arrive on its barriers
+  if (kPair) cluster_sync();
 }
 
 // ------------------------------------------------------------------ host
 
-template <int KL>
-cudaError_t launch_kl(const CUtensorMap& mq, const CUtensorMap& mc, int B, int H, int n, int NC,
-                      int nch, int kbc, float hint_z, float* list_v, unsigned short* list_c,
-                      int* status, const int* unit_list, const int* unit_count, int stall,
-                      cudaStream_t stream) {
+// One selection launch.  pair: the main pass over all units, as clusters of
+// two CTAs sharing each subkey slab (see select_tc_kernel); as many clusters
+// as can be resident at once, so the grid stays persistent.
+template <int KL, bool kPair>
+cudaError_t launch_kl(const CUtensorMap& mq, const CUtensorMap& mc, const CUtensorMap& mch,
+                      int B, int H, int n, int NC, int nch, int kbc, float hint_z,
+                      float* list_v, unsigned short* list_c, int* status, const int* unit_list,
+                      const int* unit_count, int stall, cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(select_tc_kernel<KL>,
+    cudaError_t e = cudaFuncSetAttribute(select_tc_kernel<KL, kPair>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const int units = (B + BM - 1) / BM * H * 2;  // also the most a retry can list
-  const int grid = units < sm_count() ? units : sm_count();  // persistent: one CTA per SM
-  select_tc_kernel<KL><<<grid, NUM_THREADS, SMEM_TOTAL, stream>>>(
-      mq, mc, B, H, n, NC, nch, kbc, hint_z, list_v, list_c, status, unit_list, unit_count,
-      stall);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = SMEM_TOTAL;
+  cfg.stream = stream;
+  if (kPair) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    static int max_clusters = 0;
+    if (!max_clusters) {
+      cfg.gridDim = dim3(2 * sm_count() / 2);
+      cudaError_t e = cudaOccupancyMaxActiveClusters(&max_clusters, select_tc_kernel<KL, kPair>,
+                                                     &cfg);
+      if (e != cudaSuccess) return e;
+      if (max_clusters < 1) return cudaErrorInvalidConfiguration;
+    }
+    const int pair_units = ((B + BM - 1) / BM + 1) / 2 * H * 2;
+    cfg.gridDim = dim3(2 * (pair_units < max_clusters ? pair_units : max_clusters));
+  } else {
+    const int units = (B + BM - 1) / BM * H * 2;  // also the most a retry can list
+    cfg.gridDim = dim3(units < sm_count() ? units : sm_count());  // one CTA per SM
+  }
+  return cudaLaunchKernelEx(&cfg, select_tc_kernel<KL, kPair>, mq, mc, mch, B, H, n, NC, nch,
+                            kbc, hint_z, list_v, list_c, status, unit_list, unit_count, stall);
 }
 
 // z with P(N(0,1) > z) = p, by bisection on the normal tail (host, once per call).
@@ -524,7 +580,7 @@ cudaError_t launch_lookup_tc(const uint16_t* q, const uint16_t* subkeys, int B, 
   const int nch = (n_keys + NC - 1) / NC;
   const int kbc = (hd + BK - 1) / BK;
 
-  CUtensorMap mq, mc;
+  CUtensorMap mq, mc, mch;
   {
     // q viewed as [B][H][2][hd]: innermost first.
     const cuuint64_t dims[4] = {(cuuint64_t)hd, 2, (cuuint64_t)H, (cuuint64_t)B};
@@ -547,12 +603,32 @@ cudaError_t launch_lookup_tc(const uint16_t* q, const uint16_t* subkeys, int B, 
             strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
+    // the same view in half-chunk boxes (NC/2 subkeys): each CTA of a pair
+    // loads one half and multicasts it
+    const cuuint32_t hbox[3] = {BK, (cuuint32_t)NC / 2, 1};
+    if (enc(&mch, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(subkeys), dims,
+            strides, hbox, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
   }
+  // the main pass as CTA pairs sharing each subkey slab when there are at
+  // least two row tiles and the half-query is at most 512 wide (8 k-slabs);
+  // the retry pass (listed units) one CTA per unit.  Measured on GB300
+  // (lookup call): page 0.318 -> 0.308 ms and the skewed workload 2.03 ->
+  // 1.77 ms with pairs, where the selection work dominates; the large
+  // workload (16 k-slabs, pipeline-latency-bound with three stages) 1.25 ->
+  // 1.35 ms, since each stage of a pair waits for the slower of its two CTAs
+  const bool pair = (B + BM - 1) / BM >= 2 && kbc <= 8;
   auto select = [&](float z, const int* list, const int* count, int st) {
-    return k <= 16 ? launch_kl<16>(mq, mc, B, H, n_keys, NC, nch, kbc, z, list_v, list_c, status,
-                                   list, count, st, stream)
-                   : launch_kl<32>(mq, mc, B, H, n_keys, NC, nch, kbc, z, list_v, list_c, status,
-                                   list, count, st, stream);
+    if (pair && !list)
+      return k <= 16 ? launch_kl<16, true>(mq, mc, mch, B, H, n_keys, NC, nch, kbc, z, list_v,
+                                           list_c, status, list, count, st, stream)
+                     : launch_kl<32, true>(mq, mc, mch, B, H, n_keys, NC, nch, kbc, z, list_v,
+                                           list_c, status, list, count, st, stream);
+    return k <= 16 ? launch_kl<16, false>(mq, mc, mch, B, H, n_keys, NC, nch, kbc, z, list_v,
+                                          list_c, status, list, count, st, stream)
+                   : launch_kl<32, false>(mq, mc, mch, B, H, n_keys, NC, nch, kbc, z, list_v,
+                                          list_c, status, list, count, st, stream);
   };
   // the retry bookkeeping starts clear: counts and the per-unit flags (one buffer)
   cudaError_t e =
