@@ -116,7 +116,13 @@ enum {
      back, so the kernel's bounded pipeline wait runs out (about 2 s), it
      records PKM_ERR_TIMEOUT in the status word and returns; results of such
      calls are not meaningful.  The GPU context stays usable. */
-  PKM_OPT_TEST_STALL = 3
+  PKM_OPT_TEST_STALL = 3,
+  /* SMs of the value read (pkm_gather, pkm_forward, pkm_forward_host); 0
+     (default): all of them.  Value rows of 512-byte multiples (up to 8 KB)
+     stream through shared memory as whole-row bulk copies, one persistent CTA
+     per SM; other row widths are read with one CTA per query on every SM
+     whatever this option says. */
+  PKM_OPT_READ_SMS = 4
 };
 #define PKM_HOST_MAX_CHUNKS 16
 

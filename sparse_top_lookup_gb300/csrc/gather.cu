@@ -26,6 +26,7 @@
 #include <stdint.h>
 
 #include "pkm_internal.cuh"
+#include "tc_common.cuh"
 
 namespace pkm {
 namespace {
@@ -167,12 +168,254 @@ __global__ void gather_kernel(const uint4* __restrict__ values, const float* __r
   }
 }
 
+// Bulk-copy form (one persistent CTA per SM): value rows stream into a
+// shared-memory ring as whole-row bulk copies (cp.async.bulk, the SM's copy
+// engine), up to ~200 KB in flight per SM.  The CTA holds `teams` teams;
+// team t is an independent pipeline over bags (g * gridDim.x + blockIdx.x) *
+// teams + t, g = 0, 1, ...:
+//   producer  warp t: stages its bags' indices and weights (and, for an fp8
+//             table, the selected rows' scales) in shared memory by cp.async
+//             ahead of use; for each batch of kBatch rows, lane j waits for
+//             the team's next batch slot to be free, stores row j's weight
+//             beside its ring slot and issues one bulk copy of the row; the
+//             batch completes on one barrier;
+//   consumers vpr threads (whole warps), one 16-byte column of the rows each:
+//             per batch one wait, then weight * row accumulated in fp32 over
+//             the batch's rows, in row order; each warp then frees the slot.
+// Every wait is bounded (2 s); on time-out the kernel records
+// PKM_ERR_TIMEOUT, stops, and waits (bounded) for the copies in flight
+// before it returns.
+constexpr int kBatch = 8;            // rows per batch (one barrier)
+constexpr int kBulkMaxTeams = 8;
+constexpr int kBulkConsumers = 512;  // consumer threads per CTA at most
+constexpr int kBulkThreads = 768;    // producer warps + consumers per CTA at most
+
+template <int VT>
+__global__ void __launch_bounds__(kBulkThreads, 1)
+gather_bulk_kernel(const unsigned char* __restrict__ values, const float* __restrict__ scales,
+                   int64_t N, int row_bytes, int rows_per_bag, int B, int teams, int nbs,
+                   const int64_t* __restrict__ idx, const float* __restrict__ w,
+                   float* __restrict__ out, int* __restrict__ status) {
+  using namespace tc;
+  constexpr int E = VecAcc<VT>::kElems;
+  constexpr bool kFp8 = VT == PKM_FP8_E4M3;
+  extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ int s_abort;
+  const int vpr = row_bytes / 16;
+  const int cpb = (rows_per_bag + kBatch - 1) / kBatch;  // batches per bag
+  const int bslots = teams * nbs;                         // batch slots, nbs per team
+  const int rpb = rows_per_bag;
+  // ring [bslots * kBatch][row_bytes]; then 8-byte items: full and empty
+  // barriers per batch slot, staged indices [teams][3][rpb]; then 4-byte
+  // items: row weights [bslots * kBatch], batch slot uses [bslots], staged
+  // weights [teams][3][rpb], staged fp8 scales [teams][2][rpb]
+  unsigned char* ring = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ring + (size_t)bslots * kBatch * row_bytes);
+  int64_t* st_idx = reinterpret_cast<int64_t*>(bars + 2 * bslots);
+  float* slot_w = reinterpret_cast<float*>(st_idx + (size_t)teams * 3 * rpb);
+  int* last_use = reinterpret_cast<int*>(slot_w + bslots * kBatch);
+  float* st_w = reinterpret_cast<float*>(last_use + bslots);
+  float* st_sc = st_w + (size_t)teams * 3 * rpb;
+  const uint32_t bar_full0 = smem_u32(bars), bar_empty0 = smem_u32(bars + bslots);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < bslots; ++i) {
+      mbar_init(bar_full0 + 8u * i, kBatch);                 // one arrival per producer lane
+      mbar_init(bar_empty0 + 8u * i, (uint32_t)(vpr / 32));  // one per consumer warp
+      last_use[i] = -1;
+    }
+    s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  const Ctl ctl{&s_abort, status};
+  auto bag_of = [&](int64_t g, int t) { return (g * gridDim.x + blockIdx.x) * (int64_t)teams + t; };
+
+  if (warp < teams) {
+    // ------------------------------------------------------------ producer
+    const int t = warp;
+    int64_t* my_idx = st_idx + (size_t)t * 3 * rpb;  // [3][rpb], bag g in buffer g % 3
+    float* my_w = st_w + (size_t)t * 3 * rpb;
+    float* my_sc = st_sc + (size_t)t * 2 * rpb;       // [2][rpb], bag g in buffer g % 2
+    auto stage_rows = [&](int64_t g) {               // indices and weights of bag g
+      const int64_t bag = bag_of(g, t);
+      if (bag >= B) return;
+      const int buf = (int)(g % 3);
+      for (int j = lane; j < rpb; j += 32) {
+        cp_async8(smem_u32(my_idx + buf * rpb + j), idx + bag * rpb + j);
+        cp_async4(smem_u32(my_w + buf * rpb + j), w + bag * rpb + j);
+      }
+    };
+    auto stage_scales = [&](int64_t g) {  // fp8 row scales of bag g (its indices have landed)
+      if constexpr (kFp8) {
+        if (bag_of(g, t) >= B) return;
+        for (int j = lane; j < rpb; j += 32) {
+          const int64_t r = my_idx[(g % 3) * rpb + j];
+          cp_async4(smem_u32(my_sc + (g & 1) * rpb + j), scales + (r >= 0 && r < N ? r : 0));
+        }
+      }
+    };
+    stage_rows(0);
+    stage_rows(1);
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncwarp();
+    stage_scales(0);
+    cp_async_commit();
+    bool ok = true;
+    uint32_t bq = 0, ph = 0;  // the team's next batch slot and its use parity
+    for (int64_t g = 0; ok && bag_of(g, t) < B; ++g) {
+      // what was staged one bag ago has landed: bag g's scales, bag g+1's rows
+      cp_async_wait<0>();
+      __syncwarp();
+      stage_rows(g + 2);
+      stage_scales(g + 1);
+      cp_async_commit();
+      const int rb = (int)(g % 3) * rpb, sb = (int)(g & 1) * rpb;
+      for (int c = 0; ok && c < cpb; ++c) {
+        const uint32_t bb = (uint32_t)t * nbs + bq;
+        const uint32_t full = bar_full0 + 8u * bb;
+        if (lane < kBatch) {
+          // slot bb's previous use was this team's batch nbs batches ago,
+          // issued earlier, so the team's consumers free it
+          if (!wait_phase(bar_empty0 + 8u * bb, ph ^ 1u, ctl)) {
+            ok = false;
+          } else {
+            const int j = c * kBatch + lane;
+            if (lane == 0) last_use[bb] = (int)ph;
+            if (j < rpb) {
+              int64_t row = my_idx[rb + j];
+              float wt = my_w[rb + j];
+              if (row < 0 || row >= N) {
+                atomicExch(status, PKM_ERR_BAD_INDEX);
+                row = 0;
+                wt = 0.0f;
+              } else if (kFp8) {
+                wt *= my_sc[sb + j];
+              }
+              const uint32_t rs = bb * kBatch + lane;  // ring slot of the row
+              slot_w[rs] = wt;
+              mbar_expect_tx(full, (uint32_t)row_bytes);
+              bulk_load(smem_u32(ring + (size_t)rs * row_bytes), values + row * row_bytes,
+                        (uint32_t)row_bytes, full);
+            } else {
+              mbar_arrive(full);  // past the bag's end: arrival only
+            }
+          }
+        }
+        ok = __all_sync(0xffffffffu, ok);
+        if (++bq == (uint32_t)nbs) {
+          bq = 0;
+          ph ^= 1u;
+        }
+      }
+    }
+    cp_async_wait<0>();  // no staging copy outlives the CTA
+    if (!ok) {
+      // only a batch slot's last use can still be in flight (each use waits
+      // for the previous one to be consumed): let those copies land
+      __syncwarp();
+      for (int i = t * nbs + lane; i < (t + 1) * nbs; i += 32)
+        if (last_use[i] >= 0) wait_phase_drain(bar_full0 + 8u * i, (uint32_t)last_use[i] & 1u);
+    }
+  } else {
+    // ------------------------------------------------------------ consumers
+    const int ct = threadIdx.x - 32 * teams;
+    const int t = ct / vpr, v = ct - (ct / vpr) * vpr;
+    bool ok = true;
+    uint32_t bq = 0, ph = 0;
+    for (int64_t g = 0; ok && bag_of(g, t) < B; ++g) {
+      const int64_t bag = bag_of(g, t);
+      float acc[E];
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] = 0.0f;
+      for (int c = 0; c < cpb; ++c) {
+        const uint32_t bb = (uint32_t)t * nbs + bq;
+        if (!__all_sync(0xffffffffu, wait_phase(bar_full0 + 8u * bb, ph, ctl))) {
+          ok = false;
+          break;
+        }
+        const int nr = rpb - c * kBatch < kBatch ? rpb - c * kBatch : kBatch;
+        const unsigned char* base = ring + (size_t)bb * kBatch * row_bytes + v * 16;
+        const float* wb = slot_w + bb * kBatch;
+        uint4 x[kBatch];
+        float wt[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          if (u < nr) {
+            x[u] = *reinterpret_cast<const uint4*>(base + (size_t)u * row_bytes);
+            wt[u] = wb[u];
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u)
+          if (u < nr) VecAcc<VT>::fma(acc, wt[u], x[u]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_empty0 + 8u * bb);
+        if (++bq == (uint32_t)nbs) {
+          bq = 0;
+          ph ^= 1u;
+        }
+      }
+      if (!ok) break;
+      float4* o4 = reinterpret_cast<float4*>(out + bag * (int64_t)vpr * E + v * E);
+#pragma unroll
+      for (int e = 0; e < E; e += 4)
+        o4[e / 4] = make_float4(acc[e], acc[e + 1], acc[e + 2], acc[e + 3]);
+    }
+  }
+  __syncthreads();
+}
+
+// Shape of the bulk form for a row of vpr 16-byte vectors: the most teams
+// (a power of two) whose staging and two batch slots each fit, or false when
+// the row does not suit it (teams must be whole warps).
+bool bulk_shape(int vpr, int rows_per_bag, int& teams, int& nbs, size_t& smem) {
+  if (vpr % 32 || vpr > kBulkConsumers || rows_per_bag < 1) return false;
+  const size_t budget = 220u * 1024u;
+  const size_t per_batch = kBatch * ((size_t)vpr * 16 + 4) + 8 * 2 + 4;
+  int tm = 1;
+  while (tm * 2 <= kBulkMaxTeams && tm * 2 * vpr <= kBulkConsumers &&
+         tm * 2 * (32 + vpr) <= kBulkThreads)
+    tm *= 2;
+  for (teams = tm; teams >= 1; teams /= 2) {
+    const size_t staging = (size_t)teams * rows_per_bag * (3 * (8 + 4) + 2 * 4);
+    if (staging + 2 * per_batch * teams > budget) continue;
+    nbs = (int)((budget - staging) / (per_batch * teams));
+    smem = per_batch * teams * nbs + staging;
+    return true;
+  }
+  return false;
+}
+
 template <int VT>
 cudaError_t launch_gather_vt(const void* values, int64_t N, int d_v, int B, int rows_per_bag,
                              const int64_t* idx, const float* w, float* out, int* status,
-                             cudaStream_t stream) {
+                             int ctas, cudaStream_t stream) {
   constexpr int E = VecAcc<VT>::kElems;
   const int vpr = d_v / E;  // 16-byte vectors per row
+  // an fp8 table's row scales follow its N * d_v code bytes
+  const float* scales =
+      VT == PKM_FP8_E4M3
+          ? reinterpret_cast<const float*>(static_cast<const unsigned char*>(values) + N * d_v)
+          : nullptr;
+  int teams = 0, nbs = 0;
+  size_t bulk_smem = 0;
+  if (ctas > 0 && bulk_shape(vpr, rows_per_bag, teams, nbs, bulk_smem)) {
+    static size_t smem_set = 0;
+    if (bulk_smem > smem_set) {
+      cudaError_t e = cudaFuncSetAttribute(
+          gather_bulk_kernel<VT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bulk_smem);
+      if (e != cudaSuccess) return e;
+      smem_set = bulk_smem;
+    }
+    const int64_t want = ((int64_t)B + teams - 1) / teams;
+    const int grid = want < ctas ? (int)want : ctas;
+    gather_bulk_kernel<VT><<<grid, teams * (32 + vpr), bulk_smem, stream>>>(
+        static_cast<const unsigned char*>(values), scales, N, vpr * 16, rows_per_bag, B, teams,
+        nbs, idx, w, out, status);
+    return cudaGetLastError();
+  }
   int groups = vpr >= 128 ? 1 : 128 / vpr;
   if (groups > rows_per_bag) groups = rows_per_bag > 0 ? rows_per_bag : 1;
   const int threads = vpr * groups;
@@ -194,11 +437,6 @@ cudaError_t launch_gather_vt(const void* values, int64_t N, int d_v, int B, int 
     if (e != cudaSuccess) return e;
     carveout_set = true;
   }
-  // an fp8 table's row scales follow its N * d_v code bytes
-  const float* scales =
-      VT == PKM_FP8_E4M3
-          ? reinterpret_cast<const float*>(static_cast<const unsigned char*>(values) + N * d_v)
-          : nullptr;
   gather_kernel<VT><<<B, threads, smem, stream>>>(static_cast<const uint4*>(values), scales, N,
                                                   vpr, groups, rows_per_bag, idx, w, out, status);
   return cudaGetLastError();
@@ -206,17 +444,25 @@ cudaError_t launch_gather_vt(const void* values, int64_t N, int d_v, int B, int 
 
 }  // namespace
 
+bool gather_bulk_ok(int value_dtype, int d_v, int rows_per_bag) {
+  const int esz = value_dtype == PKM_FP8_E4M3 ? 1 : value_dtype == PKM_BF16 ? 2 : 4;
+  int teams, ns;
+  size_t smem;
+  return (int64_t)d_v * esz % 16 == 0 && bulk_shape(d_v * esz / 16, rows_per_bag, teams, ns, smem);
+}
+
 cudaError_t launch_gather(const void* values, int value_dtype, int64_t N, int d_v, int B,
                           int rows_per_bag, const int64_t* idx, const float* w, float* out,
-                          int* status, cudaStream_t stream) {
+                          int* status, cudaStream_t stream, int ctas) {
   if (B == 0) return cudaSuccess;
   if (value_dtype == PKM_FP8_E4M3)
     return launch_gather_vt<PKM_FP8_E4M3>(values, N, d_v, B, rows_per_bag, idx, w, out, status,
-                                          stream);
+                                          ctas, stream);
   if (value_dtype == PKM_BF16)
-    return launch_gather_vt<PKM_BF16>(values, N, d_v, B, rows_per_bag, idx, w, out, status,
+    return launch_gather_vt<PKM_BF16>(values, N, d_v, B, rows_per_bag, idx, w, out, status, ctas,
                                       stream);
-  return launch_gather_vt<PKM_F32>(values, N, d_v, B, rows_per_bag, idx, w, out, status, stream);
+  return launch_gather_vt<PKM_F32>(values, N, d_v, B, rows_per_bag, idx, w, out, status, ctas,
+                                   stream);
 }
 
 }  // namespace pkm

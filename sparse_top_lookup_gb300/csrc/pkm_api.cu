@@ -37,6 +37,8 @@ struct pkm_handle {
   int host_chunks;
   bool host_chunks_set;  // PKM_OPT_HOST_CHUNKS given by the caller
   int test_stall;        // PKM_OPT_TEST_STALL: the bf16 lookups stall their selection kernel
+  int sms;               // SMs of the device
+  int read_sms;          // PKM_OPT_READ_SMS: SMs of the value read (0: all)
 };
 
 namespace {
@@ -101,10 +103,13 @@ int run_lookup(pkm_t h, const void* q, const void* subkeys, int B, int H, int n,
                                          k, idx, w, s));
 }
 
+// ctas: SMs of the read (bulk-copy form where the row shape suits it); 0:
+// the handle's PKM_OPT_READ_SMS, whose 0 means every SM
 int run_gather(pkm_t h, const void* values, int B, int H, int n, int k, const int64_t* idx,
-               const float* w, float* out, cudaStream_t s) {
+               const float* w, float* out, cudaStream_t s, int ctas = 0) {
+  if (ctas <= 0) ctas = h->read_sms > 0 ? h->read_sms : h->sms;
   return cuda_rc(pkm::launch_gather(values, h->cfg.value_dtype, (int64_t)n * n, h->cfg.d_v, B,
-                                    H * k, idx, w, out, h->status, s));
+                                    H * k, idx, w, out, h->status, s, ctas));
 }
 
 }  // namespace
@@ -176,7 +181,9 @@ int pkm_create(pkm_t* out, const pkm_config* cfg) {
     return PKM_ERR_CUDA;
   }
   const size_t sel = (size_t)cfg->max_B * cfg->max_H * cfg->max_k;
-  bool ok = cudaMalloc(&h->status, sizeof(int)) == cudaSuccess &&
+  bool ok = cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, h->device) ==
+                cudaSuccess &&
+            cudaMalloc(&h->status, sizeof(int)) == cudaSuccess &&
             cudaMemset(h->status, 0, sizeof(int)) == cudaSuccess;
   if (ok && sel) {
     ok = cudaMalloc(&h->ws_idx, sel * sizeof(int64_t)) == cudaSuccess &&
@@ -475,6 +482,10 @@ int pkm_set_option(pkm_t h, int option, double value) {
     case PKM_OPT_TEST_STALL:
       if (value != 0 && value != 1) return PKM_ERR_OPTION;
       h->test_stall = (int)value;
+      return PKM_OK;
+    case PKM_OPT_READ_SMS:
+      if (!(value >= 0 && value <= h->sms) || value != (int)value) return PKM_ERR_OPTION;
+      h->read_sms = (int)value;
       return PKM_OK;
     default:
       return PKM_ERR_OPTION;

@@ -53,10 +53,14 @@ cudaError_t launch_backward_scores(cublasHandle_t blas, const uint16_t* q,
                                    cudaStream_t stream);
 
 // Step a6 (value read).  values: [N, d_v] of value_dtype; idx/w: [B, H*k];
-// out: [B, d_v] fp32.  Returns a cudaError_t of the launch.
+// out: [B, d_v] fp32.  ctas > 0 and a row shape that gather_bulk_ok accepts:
+// a persistent grid of at most ctas CTAs (one per SM) streaming whole rows
+// with bulk copies; otherwise one CTA per bag on every SM.  Returns a
+// cudaError_t of the launch.
 cudaError_t launch_gather(const void* values, int value_dtype, int64_t N, int d_v, int B,
                           int rows_per_bag, const int64_t* idx, const float* w, float* out,
-                          int* status, cudaStream_t stream);
+                          int* status, cudaStream_t stream, int ctas = 0);
+bool gather_bulk_ok(int value_dtype, int d_v, int rows_per_bag);
 
 // Steps a1-a5 for fp32 queries/subkeys on the CUDA cores.
 cudaError_t launch_lookup_simt(const float* q, const float* subkeys, int B, int H, int d_q,
