@@ -27,7 +27,7 @@
 //                          number, dout row and weight);
 //   row_grad_kernel        persistent, 16 warps per SM; each warp walks its
 //                          pieces in segments of kSegW columns through a
-//                          private ring of kRgStages shared-memory stages,
+//                          private ring of shared-memory stages (4 to 6),
 //                          every lane prefetching (cp.async) and then using
 //                          only its own 4 columns of the value row, of the dV
 //                          row (unless the row is shared) and of the
@@ -62,9 +62,9 @@ constexpr int kReadWarps = 8;        // warps of bucket_sort_kernel
 constexpr int kSegW = 128;           // value-row columns per stage (4 per lane)
 constexpr int kRgWarps = 8;          // warps per CTA of row_grad_kernel
 constexpr int kRgCtas = 2;           // CTAs of row_grad_kernel per SM
-constexpr int kRgStages = 4;         // stages per warp
-// a stage: value, dV and kPiece dout regions of [lane][16 bytes]
-constexpr int kStageBytes = 512 * (2 + kPiece);
+// shared memory per warp (ring + metadata): two CTAs of 8 warps and their
+// 1 KB reserves within an SM's 228 KB
+constexpr int kRgWarpBytes = 113 * 1024 / kRgWarps;
 
 // One piece of a row's selections (64 bytes): row; m | shared << 8; the
 // row's slot in the sparse output; then per selection g < m its number e,
@@ -375,17 +375,34 @@ struct alignas(16) StageMeta {
   int pad[4];
 };
 
+// A stage of row_grad_kernel: the value segment ([lane][8 bytes] for bf16,
+// [lane][16 bytes] for fp32), the dV segment ([lane][16 bytes]; the dense
+// output only) and kPiece dout segments ([lane][16 bytes]); as many stages
+// per warp as its share of shared memory holds (more for the sparse output,
+// which reads no dV segment, so more copies are in flight).
+template <bool kBf16, bool kSparse>
+struct RgLayout {
+  static constexpr int kVStride = kBf16 ? 8 : 16;
+  static constexpr int kDvOff = 32 * kVStride;
+  static constexpr int kDoutOff = kDvOff + (kSparse ? 0 : 512);
+  static constexpr int kStage = kDoutOff + 512 * kPiece;
+  static constexpr int kS0 = kRgWarpBytes / (kStage + (int)sizeof(StageMeta));
+  static constexpr int kStages = kS0 > 8 ? 8 : kS0;
+  static_assert(kStages >= 3, "row_grad ring too shallow");
+};
+
 // One lane's 4 columns of one segment for a piece of M selections: dot
 // products into part, sum_g w_g * dout[b_g] added to the dV columns (read
 // from the stage, or 0 for atomic adds).
-template <int M, bool kBf16>
+template <int M, bool kBf16, bool kSparse>
 __device__ __forceinline__ void seg_compute(const unsigned char* st, int lane,
                                             const float (&wt)[kRec], float (&part)[kRec],
                                             bool copied, bool shared, float* drow,
                                             uint64_t pol_stream) {
+  using Lay = RgLayout<kBf16, kSparse>;
   float x[4];
   if (kBf16) {
-    const uint2 v = *reinterpret_cast<const uint2*>(st + lane * 16);
+    const uint2 v = *reinterpret_cast<const uint2*>(st + lane * Lay::kVStride);
     x[0] = __uint_as_float(v.x << 16);
     x[1] = __uint_as_float(v.x & 0xffff0000u);
     x[2] = __uint_as_float(v.y << 16);
@@ -397,11 +414,12 @@ __device__ __forceinline__ void seg_compute(const unsigned char* st, int lane,
     x[2] = v.z;
     x[3] = v.w;
   }
-  float4 acc = copied ? *reinterpret_cast<const float4*>(st + 512 + lane * 16)
-                      : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  float4 acc = !kSparse && copied ? *reinterpret_cast<const float4*>(st + Lay::kDvOff + lane * 16)
+                                  : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll
   for (int g = 0; g < M; ++g) {
-    const float4 d = *reinterpret_cast<const float4*>(st + 512 * (2 + g) + lane * 16);
+    const float4 d =
+        *reinterpret_cast<const float4*>(st + Lay::kDoutOff + 512 * g + lane * 16);
     part[g] = fmaf(d.x, x[0], part[g]);
     part[g] = fmaf(d.y, x[1], part[g]);
     part[g] = fmaf(d.z, x[2], part[g]);
@@ -418,37 +436,43 @@ __device__ __forceinline__ void seg_compute(const unsigned char* st, int lane,
 }
 
 // The copies of one lane's 4 columns (column col of row `row`) of a segment
-// into the stage at shared address dst.
-template <int M, bool kBf16>
-__device__ __forceinline__ void seg_issue(uint32_t dst, const void* values, const float* out_rows,
-                                          const float* dout, int64_t row, int64_t dst_row,
-                                          int d_v, int col, const int (&b)[kRec], bool copy_dv,
-                                          uint64_t pol_stream, uint64_t pol_keep) {
+// into the stage at shared address st (the stage's first byte).
+template <int M, bool kBf16, bool kSparse>
+__device__ __forceinline__ void seg_issue(uint32_t st, int lane, const void* values,
+                                          const float* out_rows, const float* dout, int64_t row,
+                                          int64_t dst_row, int d_v, int col, const int (&b)[kRec],
+                                          bool copy_dv, uint64_t pol_stream, uint64_t pol_keep) {
+  using Lay = RgLayout<kBf16, kSparse>;
   const int64_t off = row * d_v + col;
   if (kBf16)
-    cp_async8(dst, static_cast<const uint16_t*>(values) + off, pol_stream);
+    cp_async8(st + lane * Lay::kVStride, static_cast<const uint16_t*>(values) + off, pol_stream);
   else
-    cp_async16(dst, static_cast<const float*>(values) + off, pol_stream);
-  if (copy_dv) cp_async16(dst + 512, out_rows + dst_row * d_v + col, pol_stream);
+    cp_async16(st + lane * Lay::kVStride, static_cast<const float*>(values) + off, pol_stream);
+  if (!kSparse && copy_dv)
+    cp_async16(st + Lay::kDvOff + lane * 16, out_rows + dst_row * d_v + col, pol_stream);
 #pragma unroll
   for (int g = 0; g < M; ++g)
-    cp_async16(dst + 512 * (2 + g), dout + (int64_t)b[g] * d_v + col, pol_keep);
+    cp_async16(st + Lay::kDoutOff + 512 * g + lane * 16, dout + (int64_t)b[g] * d_v + col,
+               pol_keep);
 }
 
 // Persistent, kRgWarps warps per CTA, kRgCtas CTAs per SM.  Warp gw of GW takes
 // pieces gw, gw + GW, ...; each piece is walked in segments of kSegW
-// columns, one stage each, kRgStages - 1 stages ahead of the one computed.
+// columns, one stage each, S - 1 stages ahead of the one computed.
 // Records are fetched 32 at a time (one per lane) and broadcast by shuffles.
 // Lane l copies and uses columns c0 + 4l .. c0 + 4l + 3 of the segment only,
 // so a lane waits for its own copies (cp.async groups) and no data crosses
 // lanes except the dw sums.
-template <bool kBf16>
+template <bool kBf16, bool kSparse>
 __global__ void __launch_bounds__(kRgWarps * 32, kRgCtas)
 row_grad_kernel(const void* __restrict__ values, int d_v, const float* __restrict__ dout,
                 const PieceRec* __restrict__ pieces, const int* __restrict__ n_pieces,
-                float* __restrict__ dw, float* __restrict__ out_rows, bool sparse) {
+                float* __restrict__ dw, float* __restrict__ out_rows) {
   extern __shared__ __align__(128) unsigned char smem[];
-  constexpr int S = kRgStages;
+  using Lay = RgLayout<kBf16, kSparse>;
+  constexpr int S = Lay::kStages;
+  constexpr int kStageBytes = Lay::kStage;
+  constexpr bool sparse = kSparse;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   unsigned char* ring = smem + warp * S * kStageBytes;
   StageMeta* meta = reinterpret_cast<StageMeta*>(smem + kRgWarps * S * kStageBytes) + warp * S;
@@ -518,10 +542,11 @@ row_grad_kernel(const void* __restrict__ values, int d_v, const float* __restric
             make_int4(idst, im | (ishared << 8) | (copy_dv ? 1 << 9 : 0), c0, ps == nseg - 1);
       const int col = c0 + 4 * lane;
       if (col < d_v) {
-        const uint32_t dst = ring_s + st * kStageBytes + lane * 16;
+        const uint32_t dst = ring_s + st * kStageBytes;
         with_piece_size(im, [&](auto mc) {
-          seg_issue<decltype(mc)::value, kBf16>(dst, values, out_rows, dout, irow, idst, d_v,
-                                                col, ib, copy_dv, pol_stream, pol_keep);
+          seg_issue<decltype(mc)::value, kBf16, kSparse>(dst, lane, values, out_rows, dout, irow,
+                                                         idst, d_v, col, ib, copy_dv, pol_stream,
+                                                         pol_keep);
         });
       }
       if (++ps == nseg) ps = 0;
@@ -548,8 +573,8 @@ row_grad_kernel(const void* __restrict__ values, int d_v, const float* __restric
       const unsigned char* base = ring + st * kStageBytes;
       float* drow = out_rows + (int64_t)h.x * d_v + col;
       with_piece_size(m, [&](auto mc) {
-        seg_compute<decltype(mc)::value, kBf16>(base, lane, wt, part, copied, shared, drow,
-                                                pol_stream);
+        seg_compute<decltype(mc)::value, kBf16, kSparse>(base, lane, wt, part, copied, shared,
+                                                         drow, pol_stream);
       });
     }
     if (h.w) {  // the piece's last segment: its dw
@@ -703,20 +728,30 @@ cudaError_t launch_backward_read(const void* values, int value_dtype, int B, int
   if (sparse)
     zero_rows_kernel<<<sms * 4, 256, 0, stream>>>(zero_list, n_zero, d_v, grad_rows);
   float* out_rows = sparse ? grad_rows : dvalues;
-  const size_t sm = (size_t)kRgWarps * kRgStages * (kStageBytes + sizeof(StageMeta));
-  if (value_dtype == PKM_BF16) {
-    e = cudaFuncSetAttribute(row_grad_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)sm);
-    if (e != cudaSuccess) return e;
-    row_grad_kernel<true><<<kRgCtas * sms, kRgWarps * 32, sm, stream>>>(
-        values, d_v, dout, pieces, n_pieces, dw, out_rows, sparse);
-  } else {
-    e = cudaFuncSetAttribute(row_grad_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)sm);
-    if (e != cudaSuccess) return e;
-    row_grad_kernel<false><<<kRgCtas * sms, kRgWarps * 32, sm, stream>>>(
-        values, d_v, dout, pieces, n_pieces, dw, out_rows, sparse);
-  }
+  auto launch = [&](auto kernel, int stages, int stage_bytes) {
+    const size_t sm = (size_t)kRgWarps * stages * (stage_bytes + sizeof(StageMeta));
+    // two CTAs per SM need the whole shared-memory carveout
+    cudaError_t e2 = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)sm);
+    if (e2 == cudaSuccess)
+      e2 = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                cudaSharedmemCarveoutMaxShared);
+    if (e2 != cudaSuccess) return e2;
+    kernel<<<kRgCtas * sms, kRgWarps * 32, sm, stream>>>(values, d_v, dout, pieces, n_pieces, dw,
+                                                         out_rows);
+    return cudaSuccess;
+  };
+  if (value_dtype == PKM_BF16)
+    e = sparse ? launch(row_grad_kernel<true, true>, RgLayout<true, true>::kStages,
+                        RgLayout<true, true>::kStage)
+               : launch(row_grad_kernel<true, false>, RgLayout<true, false>::kStages,
+                        RgLayout<true, false>::kStage);
+  else
+    e = sparse ? launch(row_grad_kernel<false, true>, RgLayout<false, true>::kStages,
+                        RgLayout<false, true>::kStage)
+               : launch(row_grad_kernel<false, false>, RgLayout<false, false>::kStages,
+                        RgLayout<false, false>::kStage);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
