@@ -33,6 +33,10 @@ import synth  # noqa: E402
 METRIC = "PKM lookups (queries×heads)/s; value-gather HBM GB/s and % of GB300 peak"
 UNIT = "lookups/s"
 L2_FLUSH_BYTES = 512 << 20
+# host-buffer calls the pipelined end-to-end measurement keeps in flight: the
+# forward workloads use the handle's three staging slots, the layer and
+# training workloads two sets of their own device buffers
+IN_FLIGHT = 3
 
 
 def peaks():
@@ -464,10 +468,11 @@ def run_ours(args, rank, world, local):
     else:
         # end to end through the host-buffer entry points: every call copies
         # its q in from pinned host memory and its out back; the pipelined
-        # form keeps two calls in flight (pkm_forward_host_async, two output
-        # buffers in turn), the synchronous form one
+        # form keeps three calls in flight (pkm_forward_host_async, one per
+        # staging slot of the handle, three output buffers in turn), the
+        # synchronous form one
         q_host = torch.from_numpy(q_np.view(np.int16) if bf16 else q_np).pin_memory()
-        out_hosts = [out_host, torch.empty(B, d_v).pin_memory()]
+        out_hosts = [out_host] + [torch.empty(B, d_v).pin_memory() for _ in range(2)]
 
         def e2e_call():
             pk.check(pk.pkm_forward_host(h, q_host, dC, dV, B, H, n, k, out_host, None, None,
@@ -476,12 +481,13 @@ def run_ours(args, rank, world, local):
         def e2e_pipelined(calls):
             evs = [torch.cuda.Event() for _ in range(calls)]
             for i in range(calls):
-                if i >= 2:
-                    evs[i - 2].synchronize()  # its output buffer is reused now
+                if i >= IN_FLIGHT:
+                    evs[i - IN_FLIGHT].synchronize()  # its output buffer is reused now
                 pk.check(pk.pkm_forward_host_async(h, q_host, dC, dV, B, H, n, k,
-                                                   out_hosts[i % 2], evs[i], stream=stream),
+                                                   out_hosts[i % IN_FLIGHT], evs[i],
+                                                   stream=stream),
                          "pkm_forward_host_async")
-            for ev in evs[-2:]:
+            for ev in evs[-IN_FLIGHT:]:
                 ev.synchronize()
         h2d = B * H * d_q * esz
     for _ in range(2):
@@ -549,7 +555,7 @@ def run_ours(args, rank, world, local):
                              "peak_source": pk_["src"] + " bf16 burst"},
         "e2e": {"value": world * B * H / e2e_s, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": B * d_v * 4,
-                "calls_in_flight": 2,
+                "calls_in_flight": 2 if (train or layer) else IN_FLIGHT,
                 "value_one_call_in_flight": world * B * H / e2e_sync_s},
         # per step: select_tc_kernel and merge_kernel, their retry launches
         # (return at once when no row missed its threshold hint) and the

@@ -133,7 +133,7 @@ typedef struct pkm_handle *pkm_t;
  * for bf16).  d_v: value row width (d_v * element size a multiple of 16
  * bytes; a multiple of 16 for PKM_FP8_E4M3).  max_*: the largest B, H,
  * n_keys and k any call will pass (sizes the scratch).  host_staging:
- * nonzero to also allocate device staging for pkm_forward_host (two slots of
+ * nonzero to also allocate device staging for pkm_forward_host (three slots of
  * max_B queries and outputs).  with_backward: nonzero to also allocate what
  * pkm_backward needs (bf16 queries and subkeys, bf16 or fp32 values): a
  * cuBLAS handle with a 32 MiB workspace and scratch for the gradients
@@ -197,11 +197,11 @@ int pkm_forward_host(pkm_t h, const void *q_host, const void *subkeys, const voi
  * returns; done_event (a cudaEvent_t, required) is recorded after the last
  * copy back, and out_host / idx_host / w_host are valid once it has
  * completed.  q_host must stay unchanged and the host buffers valid until
- * then.  The handle keeps two staging slots used in turn, so the copies in of
- * one call run while the previous call computes; a third call's copies wait
- * (on the device) until the first call's results are copied back.  The batch
- * is one slice unless PKM_OPT_HOST_CHUNKS was set on the handle (the call in
- * flight beside it already hides the copies).  Calls in flight on one handle
+ * then.  The handle keeps three staging slots used in turn, so the copies in
+ * of one call run while the two calls before it compute and copy out; a
+ * fourth call's copies wait (on the device) until the first call's results
+ * are copied back.  The batch is one slice unless PKM_OPT_HOST_CHUNKS was set
+ * on the handle (the calls in flight beside it already hide the copies).  Calls in flight on one handle
  * share its lookup scratch, so they must be enqueued on the same stream.
  */
 int pkm_forward_host_async(pkm_t h, const void *q_host, const void *subkeys, const void *values,

@@ -7,6 +7,10 @@
 
 #include "pkm_internal.cuh"
 
+// pkm_forward_host staging slots: a call's copies in can start while the two
+// calls before it still compute or copy out
+constexpr int kHostSlots = 3;
+
 struct pkm_handle {
   pkm_config cfg;
   int device;
@@ -22,18 +26,18 @@ struct pkm_handle {
   float* list_v;     // [max_B * max_H * 2 * 32] per-half lists between the two bf16 kernels
   unsigned short* list_c;
   float hint_z;      // selection threshold hint override (NaN: automatic)
-  // pkm_forward_host staging (optional), two slots used by turns, so one
+  // pkm_forward_host staging (optional), kHostSlots slots used by turns, so
   // call's copies in can run while the previous call computes
-  void* stage_q[2];
-  float* stage_out[2];
-  int64_t* stage_idx[2];
-  float* stage_w[2];
+  void* stage_q[kHostSlots];
+  float* stage_out[kHostSlots];
+  int64_t* stage_idx[kHostSlots];
+  float* stage_w[kHostSlots];
   int next_slot;
   // pkm_forward_host pipeline: copies in / out on their own streams, so the
   // copy engines move batch i+1 in and batch i-1 out while batch i computes;
   // ev_done[s]: the last copy out of the call that used slot s
   cudaStream_t s_in, s_out;
-  cudaEvent_t ev_done[2], ev_in[PKM_HOST_MAX_CHUNKS], ev_comp[PKM_HOST_MAX_CHUNKS];
+  cudaEvent_t ev_done[kHostSlots], ev_in[PKM_HOST_MAX_CHUNKS], ev_comp[PKM_HOST_MAX_CHUNKS];
   int host_chunks;
   bool host_chunks_set;  // PKM_OPT_HOST_CHUNKS given by the caller
   int test_stall;        // PKM_OPT_TEST_STALL: the bf16 lookups stall their selection kernel
@@ -152,7 +156,7 @@ void pkm_destroy(pkm_t h) {
   if (h->blas) cublasDestroy(h->blas);
   cudaFree(h->blas_ws);
   cudaFree(h->bwd_ws);
-  for (int s = 0; s < 2; ++s) {
+  for (int s = 0; s < kHostSlots; ++s) {
     cudaFree(h->stage_q[s]);
     cudaFree(h->stage_out[s]);
     cudaFree(h->stage_idx[s]);
@@ -204,7 +208,7 @@ int pkm_create(pkm_t* out, const pkm_config* cfg) {
   }
   if (ok && cfg->host_staging && cfg->max_B) {
     const size_t qb = (size_t)cfg->max_B * cfg->max_H * cfg->d_q * elem_size(cfg->q_dtype);
-    for (int st = 0; ok && st < 2; ++st)
+    for (int st = 0; ok && st < kHostSlots; ++st)
       ok = cudaMalloc(&h->stage_q[st], qb) == cudaSuccess &&
            cudaMalloc(&h->stage_out[st], (size_t)cfg->max_B * cfg->d_v * sizeof(float)) ==
                cudaSuccess &&
@@ -377,9 +381,9 @@ int pkm_backward_sparse(pkm_t h, const void* q, const void* subkeys, const void*
 
 // The host-buffer forward: the batch in slices, each slice's copy in on s_in,
 // its lookup and read on `stream`, its copies out on s_out.  The call takes
-// the next of the two staging slots; its copies in first wait (on the
+// the next of the kHostSlots staging slots; its copies in first wait (on the
 // device) for the last copy out of the call that used the slot before, so
-// two calls can be in flight.  sync: wait for the copies out; else record
+// kHostSlots calls can be in flight.  sync: wait for the copies out; else record
 // `done` on s_out after them.
 static int forward_host(pkm_t h, const void* q_host, const void* subkeys, const void* values,
                         int B, int H, int n_keys, int k, float* out_host, int64_t* idx_host,
@@ -392,7 +396,7 @@ static int forward_host(pkm_t h, const void* q_host, const void* subkeys, const 
   if (!q_host || !subkeys || !values || !out_host) return PKM_ERR_INVALID;
   if (!aligned16(subkeys) || !aligned16(values)) return PKM_ERR_ALIGN;
   const int slot = h->next_slot;
-  h->next_slot ^= 1;
+  h->next_slot = (slot + 1) % kHostSlots;
   const size_t qrow = (size_t)H * h->cfg.d_q * elem_size(h->cfg.q_dtype);  // bytes per query
   const size_t orow = (size_t)h->cfg.d_v * sizeof(float);
   const size_t srow = (size_t)H * k;  // selections per query

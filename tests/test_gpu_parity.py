@@ -227,17 +227,18 @@ def test_forward_host_matches_device_forward():
             assert np.array_equal(ih.numpy(), idx_d), chunks
             assert np.array_equal(wh.numpy(), w_d), chunks
             assert np.array_equal(oh.numpy(), out_d), chunks
-        # several calls in flight (the handle's two staging slots in turn, and
-        # a third call waiting for the first's copies back), alternating two
-        # query batches and their own output buffers
+        # several calls in flight (the handle's three staging slots in turn,
+        # and the fourth and fifth calls waiting for the first and second
+        # calls' copies back), alternating two query batches and their own
+        # output buffers
         q2 = synth.queries(c, rows=B, row_offset=B)
         out_d2, idx_d2, w_d2 = run_forward(c, q2, C, V)
         qh2 = torch.from_numpy(q2.view(np.int16)).pin_memory()
         pk.check(pk.pkm_set_option(h, pk.PKM_OPT_HOST_CHUNKS, 3), "set_option")
         h_default, _ = make_handle(c, staging=True)  # async default: one slice
         calls = []
-        for i in range(6):
-            hh = h if i < 3 else h_default
+        for i in range(8):
+            hh = h if i < 5 else h_default
             oh = torch.empty(B, c["d_v"]).pin_memory()
             ih = torch.empty(B, c["H"], c["k"], dtype=torch.int64).pin_memory()
             ev = torch.cuda.Event()
