@@ -86,8 +86,11 @@ enum {
   PKM_OK = 0,
   PKM_ERR_INVALID = -1,     /* NULL handle / tensor pointer, non-positive dims, odd d_q */
   PKM_ERR_RANGE = -2,       /* B, H, n_keys or k outside the handle's config, k > n_keys */
-  PKM_ERR_UNSUPPORTED = -3, /* dtype combination, k above the path's limit (32 for bf16
-                               scoring, 64 for fp32), n_keys^2 >= 2^31, d_q or d_v layout */
+  PKM_ERR_UNSUPPORTED = -3, /* dtype combination, k above 64 (bf16 lookups with k <= 32
+                               score on the tensor cores, those with 32 < k <= 64 and
+                               fp32 ones on the CUDA cores, which also bound d_q <= 8192
+                               and n_keys <= 4096; a with_backward handle takes k <= 32),
+                               n_keys^2 >= 2^31, d_q or d_v layout */
   PKM_ERR_ALIGN = -4,       /* a tensor pointer not 16-byte aligned */
   PKM_ERR_CUDA = -5,        /* a CUDA runtime call or launch failed */
   PKM_ERR_NOMEM = -6,       /* pkm_create could not allocate its scratch (or cuBLAS handle) */

@@ -3,8 +3,9 @@
 // Product-Key Memory, "Factorising the key space": score each half of the
 // query against its own subkey set, keep the top-k of each half, form the k^2
 // separable sums s1 + s2 with flat index a1 * n_keys + a2, keep their top-k,
-// and (code listing) softmax the winners.  This path serves small fp32
-// problems (the tensor-core path takes bf16); it is plain and exact: one CTA
+// and (code listing) softmax the winners.  This path serves fp32 problems
+// and bf16 ones with 32 < k <= 64 (the tensor-core path keeps lists of at most
+// 32 per half); bf16 inputs are widened exactly.  It is plain and exact: one CTA
 // per (query, head), fp32 FMA dot products, and every selection done by
 // ranking, so ties follow the same total orders as everywhere else: (score
 // desc, subkey asc) within a half and (score desc, flat asc) overall.  The
@@ -21,6 +22,10 @@ namespace {
 constexpr int kThreads = 256;
 
 __device__ __forceinline__ float load_elem(const float* p, int64_t i) { return p[i]; }
+// bf16 (raw bits) widened exactly to fp32
+__device__ __forceinline__ float load_elem(const uint16_t* p, int64_t i) {
+  return __uint_as_float((uint32_t)p[i] << 16);
+}
 
 // Products of one 16-byte vector of subkey elements with the matching query
 // elements, accumulated in element order.
@@ -30,6 +35,16 @@ __device__ __forceinline__ float dot16(const uint4& u, const float* qv, const fl
   acc = fmaf(__uint_as_float(u.y), qv[1], acc);
   acc = fmaf(__uint_as_float(u.z), qv[2], acc);
   acc = fmaf(__uint_as_float(u.w), qv[3], acc);
+  return acc;
+}
+__device__ __forceinline__ float dot16(const uint4& u, const float* qv, const uint16_t*) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+  float acc = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    acc = fmaf(__uint_as_float(w[i] << 16), qv[2 * i], acc);
+    acc = fmaf(__uint_as_float(w[i] & 0xffff0000u), qv[2 * i + 1], acc);
+  }
   return acc;
 }
 // Steps a1-a5 for one (query, head) pair, by the whole CTA.
@@ -168,19 +183,31 @@ size_t simt_smem(int d_q, int n_keys, int k) {
 
 }  // namespace
 
-cudaError_t launch_lookup_simt(const float* q, const float* subkeys, int B, int H, int d_q,
-                               int n_keys, int k, int64_t* idx, float* w, cudaStream_t stream) {
+template <typename TIn>
+cudaError_t launch_simt(const TIn* q, const TIn* subkeys, int B, int H, int d_q, int n_keys,
+                        int k, int64_t* idx, float* w, cudaStream_t stream) {
   if (B == 0) return cudaSuccess;
   const size_t smem = simt_smem(d_q, n_keys, k);
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(lookup_simt_kernel<float>,
+    cudaError_t e = cudaFuncSetAttribute(lookup_simt_kernel<TIn>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
   const int64_t pairs = (int64_t)B * H;
-  lookup_simt_kernel<float><<<(unsigned)pairs, kThreads, smem, stream>>>(
-      q, subkeys, H, d_q, n_keys, k, idx, w);
+  lookup_simt_kernel<TIn><<<(unsigned)pairs, kThreads, smem, stream>>>(q, subkeys, H, d_q,
+                                                                       n_keys, k, idx, w);
   return cudaGetLastError();
+}
+
+cudaError_t launch_lookup_simt(const float* q, const float* subkeys, int B, int H, int d_q,
+                               int n_keys, int k, int64_t* idx, float* w, cudaStream_t stream) {
+  return launch_simt(q, subkeys, B, H, d_q, n_keys, k, idx, w, stream);
+}
+
+cudaError_t launch_lookup_simt_bf16(const uint16_t* q, const uint16_t* subkeys, int B, int H,
+                                    int d_q, int n_keys, int k, int64_t* idx, float* w,
+                                    cudaStream_t stream) {
+  return launch_simt(q, subkeys, B, H, d_q, n_keys, k, idx, w, stream);
 }
 
 }  // namespace pkm

@@ -71,7 +71,11 @@ int check_config(const pkm_config* c) {
     return PKM_ERR_UNSUPPORTED;
   if (c->q_dtype == PKM_BF16) {
     if (c->d_q % 16) return PKM_ERR_UNSUPPORTED;  // TMA strides are multiples of 16 bytes
-    if (c->max_k > pkm::kTcMaxK) return PKM_ERR_UNSUPPORTED;
+    // k above the tensor-core path's lists: the CUDA-core path (forward only)
+    if (c->max_k > pkm::kTcMaxK &&
+        (c->max_k > pkm::kSimtMaxK || c->d_q > pkm::kSimtMaxDq ||
+         c->max_n_keys > pkm::kSimtMaxNKeys || c->with_backward))
+      return PKM_ERR_UNSUPPORTED;
   } else {
     if (c->d_q > pkm::kSimtMaxDq || c->max_k > pkm::kSimtMaxK) return PKM_ERR_UNSUPPORTED;
     if (c->max_n_keys > pkm::kSimtMaxNKeys) return PKM_ERR_UNSUPPORTED;
@@ -94,6 +98,13 @@ int cuda_rc(cudaError_t e) { return e == cudaSuccess ? PKM_OK : PKM_ERR_CUDA; }
 
 int run_lookup(pkm_t h, const void* q, const void* subkeys, int B, int H, int n, int k,
                int64_t* idx, float* w, cudaStream_t s) {
+  if (h->cfg.q_dtype == PKM_BF16 && k > pkm::kTcMaxK) {
+    // exact without a threshold hint: nothing to retry (the count reads 0)
+    if (cudaMemsetAsync(h->retry_counts, 0, sizeof(int), s) != cudaSuccess) return PKM_ERR_CUDA;
+    return cuda_rc(pkm::launch_lookup_simt_bf16(static_cast<const uint16_t*>(q),
+                                                static_cast<const uint16_t*>(subkeys), B, H,
+                                                h->cfg.d_q, n, k, idx, w, s));
+  }
   if (h->cfg.q_dtype == PKM_BF16) {
     const float z = isnan(h->hint_z) ? pkm::default_hint_z(n, k) : h->hint_z;
     return cuda_rc(pkm::launch_lookup_tc(static_cast<const uint16_t*>(q),

@@ -62,9 +62,13 @@ cudaError_t launch_gather(const void* values, int value_dtype, int64_t N, int d_
                           int* status, cudaStream_t stream, int ctas = 0);
 bool gather_bulk_ok(int value_dtype, int d_v, int rows_per_bag);
 
-// Steps a1-a5 for fp32 queries/subkeys on the CUDA cores.
+// Steps a1-a5 on the CUDA cores: fp32 queries/subkeys, and bf16 ones with a
+// k above the tensor-core path's kTcMaxK (inputs widened exactly).
 cudaError_t launch_lookup_simt(const float* q, const float* subkeys, int B, int H, int d_q,
                                int n_keys, int k, int64_t* idx, float* w, cudaStream_t stream);
+cudaError_t launch_lookup_simt_bf16(const uint16_t* q, const uint16_t* subkeys, int B, int H,
+                                    int d_q, int n_keys, int k, int64_t* idx, float* w,
+                                    cudaStream_t stream);
 
 // Device scratch of the bf16 lookup's retry pass.  A per-half list whose
 // selection threshold hint was above the row's KL-th score is marked by the

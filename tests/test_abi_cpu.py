@@ -58,7 +58,15 @@ def test_check_args(L):
     assert pk.pkm_check_args(c, 1, 4, 1024, 0) == pk.PKM_ERR_INVALID
     assert pk.pkm_check_args(cfg(d_q=1023), 1, 1, 4, 1) == pk.PKM_ERR_INVALID
     assert pk.pkm_check_args(cfg(d_q=1000), 1, 1, 4, 1) == pk.PKM_ERR_UNSUPPORTED  # TMA stride
-    assert pk.pkm_check_args(cfg(max_k=33), 1, 1, 64, 1) == pk.PKM_ERR_UNSUPPORTED
+    # bf16 with 32 < k <= 64: the CUDA-core path, forward only and within its limits
+    assert pk.pkm_check_args(cfg(max_k=64), 1, 1, 64, 48) == pk.PKM_OK
+    assert pk.pkm_check_args(cfg(max_k=65), 1, 1, 128, 1) == pk.PKM_ERR_UNSUPPORTED
+    assert pk.pkm_check_args(cfg(max_k=33, with_backward=1), 1, 1, 64, 1) \
+        == pk.PKM_ERR_UNSUPPORTED
+    assert pk.pkm_check_args(cfg(max_k=33, max_n_keys=4097), 1, 1, 64, 1) \
+        == pk.PKM_ERR_UNSUPPORTED
+    assert pk.pkm_check_args(cfg(max_k=33, d_q=8208), 1, 1, 64, 1) == pk.PKM_ERR_UNSUPPORTED
+    assert pk.pkm_check_args(cfg(max_k=32, with_backward=1), 1, 1, 64, 32) == pk.PKM_OK
     assert pk.pkm_check_args(cfg(max_k=64, q_dtype=pk.PKM_F32, max_n_keys=1024), 1, 1, 64, 64) \
         == pk.PKM_OK
     assert pk.pkm_check_args(cfg(d_v=1001), 1, 1, 64, 1) == pk.PKM_ERR_UNSUPPORTED

@@ -100,6 +100,34 @@ def test_bf16_shapes(shape):
     check_against_oracle(c, q, C, V)
 
 
+@pytest.mark.parametrize("shape", [
+    # B, H, d_q, n, d_v, k: bf16 lookups with 32 < k <= 64 run on the CUDA cores
+    (70, 2, 128, 256, 128, 48),     # ragged batch, k^2 = 2304 candidates
+    (33, 1, 64, 100, 64, 64),       # k = 64 of 100 subkeys per half
+    (20, 4, 1024, 1024, 1024, 40),  # page-width rows
+])
+def test_bf16_large_k(shape):
+    c, q, C, V = random_case(sum(shape) + 1, *shape)
+    check_against_oracle(c, q, C, V)
+
+
+def test_bf16_large_k_exact_ties():
+    # integer-valued bf16 inputs: exact fp32 scores, so the CUDA-core path's
+    # tie orders must reproduce the oracle's bit for bit at k = 40
+    rng = np.random.default_rng(8)
+    B, H, d_q, n, d_v, k = 50, 2, 64, 64, 32, 40
+    qf = rng.integers(-3, 4, (B, H, d_q)).astype(np.float32)
+    Cf = rng.integers(-2, 3, (H, 2, n, d_q // 2)).astype(np.float32)
+    Cf[:, 0, 10:20] = Cf[:, 0, 0:10]
+    Vf = rng.standard_normal((n * n, d_v)).astype(np.float32)
+    q, C, V = synth.f32_to_bf16(qf), synth.f32_to_bf16(Cf), synth.f32_to_bf16(Vf)
+    c = dict(B=B, H=H, d_q=d_q, n_keys=n, d_v=d_v, k=k, dtype="bf16")
+    out, idx, w = run_forward(c, q.ravel(), C.ravel(), V.ravel())
+    ref = oracle.lookup(q.ravel(), C.ravel(), B, H, d_q, n, k)
+    assert np.array_equal(idx, ref["idx"])
+    assert (np.abs(w - ref["w"]) <= 1e-6 * (1 + ref["w"])).all()
+
+
 @pytest.mark.parametrize("z", [1e30, -1e30, -1.0, 0.5, 1.53, 2.5])
 def test_selection_exact_for_any_threshold_hint(z):
     # The per-row threshold hint only steers cost.  A huge z leaves every row
