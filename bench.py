@@ -519,14 +519,19 @@ def run_ours(args, rank, world, local):
     traffic = measured_traffic(args.workload, B, gather_name)
     roof = {"kernel": "%s (value read)" % gather_name, "bound": "hbm",
             "achieved": achieved, "peak": pk_["hbm"], "unit": "GB/s",
-            "frac": achieved / pk_["hbm"], "traffic": traffic, "peak_source": pk_["src"]}
+            "frac": achieved / pk_["hbm"], "traffic": traffic, "peak_source": pk_["src"],
+            # distinct value rows the step selected (each crosses HBM at most
+            # once per launch if L2 keeps it), and the DRAM rate of the
+            # measured traffic when a profile of this source and batch exists
+            "distinct_rows": int(torch.unique(idx).numel()),
+            "dram_gbs": traffic / (ms_gather * 1e-3) / 1e9 if traffic else None}
     if train:
         # per distinct selected row: the value row read once and its dvalues
         # row read and written once (fp32; the sparse form writes its gradient
         # row and row number once); per selection: idx, w and dw; per query:
         # dout.  The time is the whole read call (bucket count, scan and
         # scatter, sort, then row_grad_kernel).
-        rows_touched = int(torch.unique(idx).numel())
+        rows_touched = roof["distinct_rows"]
         per_row = value_row_bytes(c) + (4 * d_v + 8 if sparse else 8 * d_v)
         bread_bytes = rows_touched * per_row + B * H * k * 16 + B * d_v * 4
         bread = bread_bytes / (ms_bread * 1e-3) / 1e9
@@ -578,12 +583,22 @@ def run_ours(args, rank, world, local):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         nthreads = os.cpu_count() or 1
         sample = min(args.cpu_sample, B)
-        t = cpu_oracle_time(c, cpu_inputs(c, sample, C=C_np, V=V_np), sample, nthreads)
+        inputs = cpu_inputs(c, sample, C=C_np, V=V_np)
+        t = cpu_oracle_time(c, inputs, sample, nthreads)
+        # the same oracle on one thread, on the first quarter of the sample
+        s1 = max(1, sample // 4)
+        q_in = inputs[0]
+        if is_layer(c):
+            q1 = (q_in[0][: s1 * c["qnet_dim"]],) + tuple(q_in[1:])
+        else:
+            q1 = q_in[: s1 * H * d_q]
+        t1 = cpu_oracle_time(c, (q1,) + tuple(inputs[1:]), s1, 1)
         line["cpu_baseline"] = {
             "value": sample * H / t, "unit": UNIT, "cores": nthreads, "kind": "oracle",
             "sample": "%d of %d queries (all %d heads) of the %s workload, fp64 oracle %s"
                       % (sample, B, H, args.workload,
-                         "forward + backward" if train else "forward")}
+                         "forward + backward" if train else "forward"),
+            "value_1_thread": s1 * H / t1, "sample_1_thread": "the first %d of them" % s1}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
