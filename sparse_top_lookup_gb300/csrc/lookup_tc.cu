@@ -43,14 +43,11 @@ using namespace tc;
 constexpr int BM = 128;             // query rows per tile (MMA M)
 constexpr int BK = 64;              // bf16 elements per k-slab: one 128-byte swizzle row
 constexpr int NCMAX = 128;          // subkeys per chunk (MMA N)
-constexpr int STAGES = 3;
 constexpr int A_BYTES = BM * BK * 2;     // 16 KiB
 constexpr int B_BYTES = NCMAX * BK * 2;  // 16 KiB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int SMEM_TILES = STAGES * STAGE_BYTES;
-constexpr int SETS = 2;                  // epilogue warp sets, each with 2 TMEM buffers
-constexpr int NUM_THREADS = 64 + SETS * 128;
-constexpr uint32_t TMEM_COLS = 512;
+constexpr int TBUFS = 4;                 // 128-column TMEM score buffers
+constexpr uint32_t TMEM_COLS = TBUFS * NCMAX;
 
 // ---------------------------------------------------- selection helpers
 //
@@ -182,28 +179,43 @@ __device__ __forceinline__ void sorted_list(const RowLog& L, int len, const floa
 
 // ---------------------------------------------------------------- kernel
 
-constexpr int SMEM_TOTAL = SMEM_TILES + SETS * LOG_BYTES + 1024;  // + alignment slack
+// Shape of a launch by its number of epilogue warp sets: two sets (each
+// with 2 TMEM buffers, 3 tile stages) where the selection work dominates, or
+// one set (4 TMEM buffers, 5 tile stages: 160 KB of tiles in flight instead of
+// 96 KB) where the tile pipeline does (wide half-queries).
+template <int kSets>
+struct SelShape {
+  static constexpr int kStages = kSets == 1 ? 5 : 3;
+  static constexpr int kBufs = TBUFS / kSets;  // TMEM buffers per set
+  static constexpr int kThreads = 64 + kSets * 128;
+  static constexpr int kTiles = kStages * STAGE_BYTES;
+  static constexpr int kSmem = kTiles + kSets * LOG_BYTES + 1024;  // + alignment slack
+  static_assert(kSmem <= 227 * 1024, "selection kernel shared memory");
+};
 
-// A CTA's units are u_i = blockIdx.x + i * gridDim.x; epilogue set i % 2
-// takes unit u_i.  The producer and the MMA walk the units two at a time,
-// chunk by chunk, alternating sets, so both sets are fed; set s's chunks go to
-// TMEM buffers 2s and 2s+1 in turn.
+// A CTA's units are u_i = blockIdx.x + i * gridDim.x; epilogue set i % kSets
+// takes unit u_i.  The producer and the MMA walk the units kSets at a time,
+// chunk by chunk, alternating sets, so every set is fed; set s's chunks go to
+// its kBufs TMEM buffers in turn.
 // kPair: clusters of two CTAs on neighbouring row tiles (2j, 2j+1) of the same
 // (head, half), in lockstep, so each subkey slab crosses from L2 once for the
 // pair: CTA rank r loads rows [r NC/2, (r+1) NC/2) of it (tmap_c_half) and
 // multicasts them to both.  A stage is then free only when both CTAs' MMAs
 // have read it: each MMA's release commit arrives on both CTAs' empty
 // barriers.  The pair's units are p_i = cluster + i * clusters.
-template <int KL, bool kPair>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+template <int KL, bool kPair, int kSets>
+__global__ void __launch_bounds__(SelShape<kSets>::kThreads, 1)
 select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_c,
                  const __grid_constant__ CUtensorMap tmap_c_half,
                  int B, int H, int n, int NC, int nch, int kb_count, float hint_z,
                  float* __restrict__ list_v, unsigned short* __restrict__ list_c,
                  int* __restrict__ status, const int* __restrict__ unit_list,
                  const int* __restrict__ unit_count, int stall) {
+  using Shape = SelShape<kSets>;
+  constexpr int STAGES = Shape::kStages, SETS = kSets, BUFS = Shape::kBufs;
+  constexpr int SMEM_TILES = Shape::kTiles;
   extern __shared__ unsigned char smem_raw[];
-  __shared__ __align__(8) uint64_t bars[2 * STAGES + 4 * SETS + 1];
+  __shared__ __align__(8) uint64_t bars[2 * STAGES + 2 * TBUFS + 1];
   __shared__ uint32_t s_tmem_base;
   __shared__ int s_abort;
 
@@ -239,15 +251,15 @@ select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
   auto bar_full = [&](uint32_t s) { return bar0 + 8u * s; };
   auto bar_empty = [&](uint32_t s) { return bar0 + 8u * (STAGES + s); };
   auto bar_tfull = [&](uint32_t b) { return bar0 + 8u * (2 * STAGES + b); };
-  auto bar_tempty = [&](uint32_t b) { return bar0 + 8u * (2 * STAGES + 2 * SETS + b); };
-  const uint32_t bar_done = bar0 + 8u * (2 * STAGES + 4 * SETS);
+  auto bar_tempty = [&](uint32_t b) { return bar0 + 8u * (2 * STAGES + TBUFS + b); };
+  const uint32_t bar_done = bar0 + 8u * (2 * STAGES + 2 * TBUFS);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar_full(s), 1);
       mbar_init(bar_empty(s), kPair ? 2 : 1);  // pair: both CTAs' MMAs release it
     }
-    for (int b = 0; b < 2 * SETS; ++b) {
+    for (int b = 0; b < TBUFS; ++b) {
       mbar_init(bar_tfull(b), 1);
       mbar_init(bar_tempty(b), 4);  // one arrival per warp of the buffer's set
     }
@@ -318,7 +330,7 @@ select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
       for (int i0 = 0; ok && i0 < mine; i0 += SETS)
         for (int ch = 0; ok && ch < nch; ++ch)
           for (int st = 0; ok && st < SETS && i0 + st < mine; ++st) {
-            const uint32_t buf = 2 * st + (cnt[st] & 1u), use = cnt[st] >> 1;
+            const uint32_t buf = st * BUFS + cnt[st] % BUFS, use = cnt[st] / BUFS;
             ++cnt[st];
             if (!wait_phase(bar_tempty(buf), (use & 1u) ^ 1u, ctl)) {
               ok = false;
@@ -386,18 +398,18 @@ select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
           for (int c = 0; c < upto && ok; ++c) {
             const uint32_t cc = cnt + (uint32_t)c;
             ok = __all_sync(0xffffffffu,
-                            wait_phase(bar_tfull(2 * set + (cc & 1u)), (cc >> 1) & 1u, ctl));
+                            wait_phase(bar_tfull(set * BUFS + cc % BUFS), (cc / BUFS) & 1u, ctl));
           }
         }
         if (!ok) break;
         tc_fence_after();
-        const uint32_t base = lane_addr + (2 * set + (cnt & 1u)) * NCMAX;
+        const uint32_t base = lane_addr + (set * BUFS + cnt % BUFS) * NCMAX;
         if (ch == 0 && n > LOG_CAP && hint_z > -INFINITY) {
           // threshold hint: mean + z * spread of the first chunks' scores
           float a1[4] = {0.0f, 0.0f, 0.0f, 0.0f}, a2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll 1
           for (int c = 0; c < upto; ++c) {
-            const uint32_t cb = lane_addr + (2 * set + ((cnt + c) & 1u)) * NCMAX;
+            const uint32_t cb = lane_addr + (set * BUFS + (cnt + c) % BUFS) * NCMAX;
 #pragma unroll 1
             for (int gg = 0; gg < NC; gg += 32) {
               float v[32];
@@ -446,7 +458,7 @@ select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
         // chunk consumed: hand the TMEM buffer back
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_tempty(2 * set + (cnt & 1u)));
+        if (lane == 0) mbar_arrive(bar_tempty(set * BUFS + cnt % BUFS));
         ++cnt;
       }
       if (!ok) break;
@@ -499,22 +511,24 @@ select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
 // One selection launch.  pair: the main pass over all units, as clusters of
 // two CTAs sharing each subkey slab (see select_tc_kernel); as many clusters
 // as can be resident at once, so the grid stays persistent.
-template <int KL, bool kPair>
+template <int KL, bool kPair, int kSets>
 cudaError_t launch_kl(const CUtensorMap& mq, const CUtensorMap& mc, const CUtensorMap& mch,
                       int B, int H, int n, int NC, int nch, int kbc, float hint_z,
                       float* list_v, unsigned short* list_c, int* status, const int* unit_list,
                       const int* unit_count, int stall, cudaStream_t stream) {
+  using Shape = SelShape<kSets>;
+  auto kernel = select_tc_kernel<KL, kPair, kSets>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(select_tc_kernel<KL, kPair>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
+    cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Shape::kSmem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(NUM_THREADS);
-  cfg.dynamicSmemBytes = SMEM_TOTAL;
+  cfg.blockDim = dim3(Shape::kThreads);
+  cfg.dynamicSmemBytes = Shape::kSmem;
   cfg.stream = stream;
   if (kPair) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -526,8 +540,7 @@ cudaError_t launch_kl(const CUtensorMap& mq, const CUtensorMap& mc, const CUtens
     static int max_clusters = 0;
     if (!max_clusters) {
       cfg.gridDim = dim3(2 * sm_count() / 2);
-      cudaError_t e = cudaOccupancyMaxActiveClusters(&max_clusters, select_tc_kernel<KL, kPair>,
-                                                     &cfg);
+      cudaError_t e = cudaOccupancyMaxActiveClusters(&max_clusters, kernel, &cfg);
       if (e != cudaSuccess) return e;
       if (max_clusters < 1) return cudaErrorInvalidConfiguration;
     }
@@ -537,8 +550,8 @@ cudaError_t launch_kl(const CUtensorMap& mq, const CUtensorMap& mc, const CUtens
     const int units = (B + BM - 1) / BM * H * 2;  // also the most a retry can list
     cfg.gridDim = dim3(units < sm_count() ? units : sm_count());  // one CTA per SM
   }
-  return cudaLaunchKernelEx(&cfg, select_tc_kernel<KL, kPair>, mq, mc, mch, B, H, n, NC, nch,
-                            kbc, hint_z, list_v, list_c, status, unit_list, unit_count, stall);
+  return cudaLaunchKernelEx(&cfg, kernel, mq, mc, mch, B, H, n, NC, nch, kbc, hint_z, list_v,
+                            list_c, status, unit_list, unit_count, stall);
 }
 
 // z with P(N(0,1) > z) = p, by bisection on the normal tail (host, once per call).
@@ -619,16 +632,18 @@ cudaError_t launch_lookup_tc(const uint16_t* q, const uint16_t* subkeys, int B, 
   // workload (16 k-slabs, pipeline-latency-bound with three stages) 1.25 ->
   // 1.35 ms, since each stage of a pair waits for the slower of its two CTAs
   const bool pair = (B + BM - 1) / BM >= 2 && kbc <= 8;
+  // wide half-queries (more than 8 k-slabs per chunk) are bound by the tile
+  // pipeline, not by the selection: their main pass runs one epilogue set per
+  // CTA with 5 tile stages in flight
+  const bool deep = kbc > 8;
   auto select = [&](float z, const int* list, const int* count, int st) {
-    if (pair && !list)
-      return k <= 16 ? launch_kl<16, true>(mq, mc, mch, B, H, n_keys, NC, nch, kbc, z, list_v,
-                                           list_c, status, list, count, st, stream)
-                     : launch_kl<32, true>(mq, mc, mch, B, H, n_keys, NC, nch, kbc, z, list_v,
-                                           list_c, status, list, count, st, stream);
-    return k <= 16 ? launch_kl<16, false>(mq, mc, mch, B, H, n_keys, NC, nch, kbc, z, list_v,
-                                          list_c, status, list, count, st, stream)
-                   : launch_kl<32, false>(mq, mc, mch, B, H, n_keys, NC, nch, kbc, z, list_v,
-                                          list_c, status, list, count, st, stream);
+#define PKM_SELECT(KLv, PAIRv, SETSv)                                                          \
+  launch_kl<KLv, PAIRv, SETSv>(mq, mc, mch, B, H, n_keys, NC, nch, kbc, z, list_v, list_c, \
+                               status, list, count, st, stream)
+    if (pair && !list) return k <= 16 ? PKM_SELECT(16, true, 2) : PKM_SELECT(32, true, 2);
+    if (deep && !list) return k <= 16 ? PKM_SELECT(16, false, 1) : PKM_SELECT(32, false, 1);
+    return k <= 16 ? PKM_SELECT(16, false, 2) : PKM_SELECT(32, false, 2);
+#undef PKM_SELECT
   };
   // the retry bookkeeping starts clear: counts and the per-unit flags (one buffer)
   cudaError_t e =

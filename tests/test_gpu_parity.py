@@ -94,6 +94,8 @@ def random_case(seed, B, H, d_q, n, d_v, k, dtype="bf16", kvar=None):
     (129, 2, 1024, 1024, 1024, 32),  # page-width rows, small batch
     (64, 8, 256, 256, 128, 32),     # eight heads (the skewed workload's H)
     (70, 1, 128, 2048, 64, 32),     # 16 chunks per half (the large workload's n_keys)
+    (130, 2, 2048, 256, 128, 32),   # 16 k-slabs per chunk: one epilogue set, 5 tile stages
+    (200, 1, 1152, 300, 64, 16),    # 9 k-slabs (the narrowest one-set shape), ragged chunks
 ])
 def test_bf16_shapes(shape):
     c, q, C, V = random_case(sum(shape), *shape)
@@ -142,6 +144,19 @@ def test_selection_exact_for_any_threshold_hint(z):
     if z == 1e30:
         assert info["fallback"] == c["B"] * c["H"]
     if z <= -1.0:
+        assert info["fallback"] == 0
+
+
+@pytest.mark.parametrize("z", [1e30, 1.53, -1e30])
+def test_one_set_selection_exact_for_any_threshold_hint(z):
+    # the one-set form (wide half-queries) with every row retried (huge z),
+    # about half of them (z = 1.53), or none and every score logged
+    c, q, C, V = random_case(77, 260, 2, 2048, 512, 128, 32)
+    info = {}
+    check_against_oracle(c, q, C, V, hint_z=z, report=info)
+    if z == 1e30:
+        assert info["fallback"] == c["B"] * c["H"]
+    if z < 0:
         assert info["fallback"] == 0
 
 
