@@ -379,6 +379,9 @@ def run_ours(args, rank, world, local):
     st = pk.pkm_get_status(h)
     if st != pk.PKM_OK:
         raise RuntimeError("device status after timed steps: %s" % pk.pkm_strerror(st))
+    # (query, head) pairs of the last timed lookup whose threshold hint missed
+    # (their row tiles were selected again without it, inside the step)
+    retried = pk.pkm_get_fallback_count(h) if bf16 else 0
     t_qnet = [e[0].elapsed_time(e[1]) for e in ev]
     t_lookup = [e[1].elapsed_time(e[2]) for e in ev]
     t_gather = [e[2].elapsed_time(e[3]) for e in ev]
@@ -554,6 +557,7 @@ def run_ours(args, rank, world, local):
                       ({"backward_read": ms_bread, "backward_scores": ms_bscores}
                        if train else {})),
         "roofline": roof,
+        "retried_pairs": retried,
         "scoring_roofline": {"kernel": "select_tc_kernel + merge_kernel (a1-a5, one lookup call)",
                              "bound": "tensor", "achieved": tflops, "peak": pk_["bf16"],
                              "unit": "TFLOP/s", "frac": tflops / pk_["bf16"],
