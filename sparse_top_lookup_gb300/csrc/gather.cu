@@ -7,14 +7,21 @@
 // retrieval): r = sum_j alpha_j v_{i_j}.  Here one bag holds the H*k rows a
 // query selected over all its heads, so the per-head reads are summed.
 //
-// The kernel is HBM-bound: every byte of a selected row is read once, the
-// arithmetic is one FMA per element.  One CTA owns one query (bag).  Each
-// value row is split into 16-byte vectors and one thread owns one vector
-// column, so a warp reads 512 contiguous bytes of a row; when a row has fewer
-// vectors than the CTA has threads, the threads form row groups that take
-// every G-th row and are reduced through shared memory at the end.  Loads are
-// 16-byte non-coherent loads that bypass L1 (each row is used once per bag),
-// unrolled eight rows deep so a thread keeps 128 bytes in flight.
+// The read is HBM-bound: every byte of a selected row is read once, the
+// arithmetic is one FMA per element.  Two forms:
+//   gather_bulk_kernel (rows of 512-byte multiples up to 8 KB): one
+//     persistent CTA per SM streams whole rows into a shared-memory ring by
+//     bulk copies (described above the kernel); an SM keeps far more bytes in
+//     flight this way than with per-thread loads, whose misses in flight
+//     hold an SM near 45 GB/s;
+//   gather_kernel (other widths): one CTA owns one query (bag).  Each value
+//     row is split into 16-byte vectors and one thread owns one vector
+//     column, so a warp reads 512 contiguous bytes of a row; when a row has
+//     fewer vectors than the CTA has threads, the threads form row groups
+//     that take every G-th row and are reduced through shared memory at the
+//     end.  Loads are 16-byte non-coherent loads that bypass L1 (each row is
+//     used once per bag), unrolled eight rows deep.
+// Both accumulate in fp32 (the bulk form in row order within a bag).
 //
 // fp8 table (the note after the code listing: the value table is "a good
 // candidate for keeping in a lower precision"): rows of e4m3 codes, one fp32
@@ -91,7 +98,7 @@ struct VecAcc<PKM_F32> {
 
 // grid: one CTA per bag.  block: vpr * groups threads.
 // dynamic smem: rows_per_bag * (4 + 4) bytes, plus blockDim * E * 4 when groups > 1
-// (kept small so these CTAs fit next to a running lookup kernel's CTA).
+// (kept small, so many CTAs fit on an SM).
 // scales: the fp8 table's row scales (null for fp32 / bf16 tables).
 template <int VT>
 __global__ void gather_kernel(const uint4* __restrict__ values, const float* __restrict__ scales,
@@ -427,8 +434,7 @@ cudaError_t launch_gather_vt(const void* values, int64_t N, int d_v, int B, int 
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  // The loads bypass L1, so the SM can keep its maximum shared-memory split;
-  // CTAs of this kernel then fit next to a running lookup kernel's CTA.
+  // The loads bypass L1, so the SM can keep its maximum shared-memory split.
   static bool carveout_set = false;
   if (!carveout_set) {
     cudaError_t e = cudaFuncSetAttribute(gather_kernel<VT>,
