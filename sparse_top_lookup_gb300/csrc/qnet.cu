@@ -53,20 +53,33 @@ __global__ void bn_fold_kernel(const float* __restrict__ gamma, const float* __r
   shift[f] = fmaf(-mean[f], s, beta[f]);
 }
 
+// kPair: clusters of two CTAs on row tiles 2p and 2p+1 of the same feature
+// tile, in lockstep: each CTA loads its own x slab and half (128 rows) of the
+// W slab, multicast to both, so a W slab crosses from L2 once for the pair
+// (32 KB of L2 reads per stage and CTA instead of 48 KB).  A stage is free
+// once both CTAs' MMAs have read it (each MMA's release commit arrives on
+// both CTAs' empty barriers).  A CTA whose row tile is past the batch loads
+// zero-filled x rows for its partner's sake and stores nothing.
+template <bool kPair>
 __global__ void __launch_bounds__(QTHREADS, 1)
 qnet_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
-            int B, int F, int dim, const float* __restrict__ scale,
-            const float* __restrict__ shift, __nv_bfloat16* __restrict__ q,
-            int* __restrict__ status) {
+            const __grid_constant__ CUtensorMap tmap_w_half, int B, int F, int dim,
+            const float* __restrict__ scale, const float* __restrict__ shift,
+            __nv_bfloat16* __restrict__ q, int* __restrict__ status) {
   extern __shared__ unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t bars[2 * QSTAGES + 4 + 1];
   __shared__ uint32_t s_tmem_base;
   __shared__ int s_abort;
 
   const int tm_count = (B + QM - 1) / QM, tn_count = (F + QN - 1) / QN;
-  const int tiles = tm_count * tn_count;
-  const int mine = (int)blockIdx.x < tiles ? (tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-  if (mine == 0) return;
+  // pair mode: the cluster's work items (pair tiles: two row tiles, one
+  // feature tile) and this CTA's rank in it; otherwise the CTA's own tiles
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+  const int slot = kPair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int slots = kPair ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  const int tiles = (kPair ? (tm_count + 1) / 2 : tm_count) * tn_count;
+  const int mine = slot < tiles ? (tiles - 1 - slot) / slots + 1 : 0;
+  if (mine == 0) return;  // (pair mode: both CTAs of the cluster alike)
   const int kb_count = (dim + QK - 1) / QK;
 
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -83,7 +96,7 @@ qnet_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
   if (threadIdx.x == 0) {
     for (int s = 0; s < QSTAGES; ++s) {
       mbar_init(bar_full(s), 1);
-      mbar_init(bar_empty(s), 1);
+      mbar_init(bar_empty(s), kPair ? 2 : 1);  // pair: both CTAs' MMAs release it
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar_tfull(b), 1);
@@ -104,12 +117,14 @@ qnet_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (kPair) cluster_sync();  // the peer's barriers exist before any multicast reaches them
   const uint32_t tmem = s_tmem_base;
   const Ctl ctl{&s_abort, status};
   auto tile_of = [&](int i, int& tm, int& tn) {
-    const int t = blockIdx.x + i * gridDim.x;
+    const int t = slot + i * slots;
     tm = t / tn_count;
     tn = t - tm * tn_count;
+    if (kPair) tm = 2 * tm + (int)rank;
   };
 
   if (warp == 0) {
@@ -129,7 +144,11 @@ qnet_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
           mbar_expect_tx(bar_full(s), QSTAGE_BYTES);
           const uint32_t dst = tiles_u32 + s * QSTAGE_BYTES;
           tma_load_2d(dst, &tmap_x, kb * QK, tm * QM, bar_full(s));
-          tma_load_2d(dst + QA_BYTES, &tmap_w, kb * QK, tn * QN, bar_full(s));
+          if (kPair)  // this CTA's half of the W slab, to both CTAs
+            tma_load_2d_mc(dst + QA_BYTES + rank * (QN / 2) * 128, &tmap_w_half, kb * QK,
+                           tn * QN + (int)rank * (QN / 2), bar_full(s), 3);
+          else
+            tma_load_2d(dst + QA_BYTES, &tmap_w, kb * QK, tn * QN, bar_full(s));
         }
       }
       if (!ok) {  // let the copies already issued land before the CTA exits
@@ -160,7 +179,10 @@ qnet_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
 #pragma unroll
           for (int kk = 0; kk < QK / 16; ++kk)
             tc_mma(d_tmem, a_desc + 2u * kk, b_desc + 2u * kk, idesc, (kb | kk) != 0);
-          tc_commit(bar_empty(s));
+          if (kPair)
+            tc_commit_mc(bar_empty(s), 3);
+          else
+            tc_commit(bar_empty(s));
         }
         if (!ok) break;
         tc_commit(bar_tfull(buf));
@@ -218,6 +240,9 @@ qnet_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512)
                  : "memory");
   }
+  // pair: neither CTA leaves while the other may still load into its shared
+  // memory or arrive on its barriers
+  if (kPair) cluster_sync();
 }
 
 }  // namespace
@@ -236,7 +261,7 @@ cudaError_t launch_qnet(const uint16_t* x, const uint16_t* w, int B, int dim, in
   if (B == 0) return cudaSuccess;
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
-  CUtensorMap mx, mw;
+  CUtensorMap mx, mw, mwh;
   {
     const cuuint64_t dims[2] = {(cuuint64_t)dim, (cuuint64_t)B};
     const cuuint64_t strides[1] = {(cuuint64_t)dim * 2};
@@ -256,18 +281,59 @@ cudaError_t launch_qnet(const uint16_t* x, const uint16_t* w, int B, int dim, in
             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
+    // the same view in half-slab boxes (128 rows): each CTA of a pair loads
+    // one half and multicasts it
+    const cuuint32_t hbox[2] = {QK, QN / 2};
+    if (enc(&mwh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(w), dims, strides,
+            hbox, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
   }
-  static bool attr_set = false;
-  if (!attr_set) {
+  const int tm_count = (B + QM - 1) / QM, tn_count = (F + QN - 1) / QN;
+  auto q16 = reinterpret_cast<__nv_bfloat16*>(q);
+  // pairs of row tiles share each W slab when there are at least two
+  if (tm_count >= 2) {
+    static bool attr_set = false;
+    if (!attr_set) {
+      cudaError_t e = cudaFuncSetAttribute(qnet_kernel<true>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, QSMEM);
+      if (e != cudaSuccess) return e;
+      attr_set = true;
+    }
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(QTHREADS);
+    cfg.dynamicSmemBytes = QSMEM;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    static int max_clusters = 0;
+    if (!max_clusters) {
+      cfg.gridDim = dim3(2 * (sm_count() / 2));
+      cudaError_t e = cudaOccupancyMaxActiveClusters(&max_clusters, qnet_kernel<true>, &cfg);
+      if (e != cudaSuccess) return e;
+      if (max_clusters < 1) return cudaErrorInvalidConfiguration;
+    }
+    const int pair_tiles = (tm_count + 1) / 2 * tn_count;
+    cfg.gridDim = dim3(2 * (pair_tiles < max_clusters ? pair_tiles : max_clusters));
+    return cudaLaunchKernelEx(&cfg, qnet_kernel<true>, mx, mw, mwh, B, F, dim, scale, shift, q16,
+                              status);
+  }
+  static bool attr_set1 = false;
+  if (!attr_set1) {
     cudaError_t e =
-        cudaFuncSetAttribute(qnet_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, QSMEM);
+        cudaFuncSetAttribute(qnet_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, QSMEM);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_set1 = true;
   }
-  const int tiles = (B + QM - 1) / QM * ((F + QN - 1) / QN);
+  const int tiles = tm_count * tn_count;
   const int grid = tiles < sm_count() ? tiles : sm_count();
-  qnet_kernel<<<grid, QTHREADS, QSMEM, stream>>>(mx, mw, B, F, dim, scale, shift,
-                                                 reinterpret_cast<__nv_bfloat16*>(q), status);
+  qnet_kernel<false><<<grid, QTHREADS, QSMEM, stream>>>(mx, mw, mwh, B, F, dim, scale, shift, q16,
+                                                        status);
   return cudaGetLastError();
 }
 

@@ -114,6 +114,17 @@ __device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const CUtensorMap* 
       : "memory");
 }
 
+// 2-D tile load multicast to the CTAs of this cluster in `mask` (same
+// shared-memory and mbarrier offsets in each).
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, int c0,
+                                               int c1, uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "h"(mask)
+      : "memory");
+}
+
 // tcgen05.commit that arrives on the mbarrier at this offset in every CTA of
 // the cluster in `mask`.
 __device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
