@@ -183,12 +183,17 @@ __device__ __forceinline__ void sorted_list(const RowLog& L, int len, const floa
 // with 2 TMEM buffers, 3 tile stages) where the selection work dominates, or
 // one set (4 TMEM buffers, 5 tile stages: 160 KB of tiles in flight instead of
 // 96 KB) where the tile pipeline does (wide half-queries).
+// The one-set form also loads each query slab once for two key chunks (a
+// stage holds the query slab and both chunks' subkey slabs, and two MMAs read
+// it), so a chunk pair streams 384 KB into the SM instead of 512 KB.
 template <int kSets>
 struct SelShape {
-  static constexpr int kStages = kSets == 1 ? 5 : 3;
+  static constexpr int kCps = kSets == 1 ? 2 : 1;  // key chunks per stage
+  static constexpr int kStageBytes = A_BYTES + kCps * B_BYTES;
+  static constexpr int kStages = 3;
   static constexpr int kBufs = TBUFS / kSets;  // TMEM buffers per set
   static constexpr int kThreads = 64 + kSets * 128;
-  static constexpr int kTiles = kStages * STAGE_BYTES;
+  static constexpr int kTiles = kStages * kStageBytes;
   static constexpr int kSmem = kTiles + kSets * LOG_BYTES + 1024;  // + alignment slack
   static_assert(kSmem <= 227 * 1024, "selection kernel shared memory");
 };
@@ -212,8 +217,9 @@ select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
                  int* __restrict__ status, const int* __restrict__ unit_list,
                  const int* __restrict__ unit_count, int stall) {
   using Shape = SelShape<kSets>;
-  constexpr int STAGES = Shape::kStages, SETS = kSets, BUFS = Shape::kBufs;
-  constexpr int SMEM_TILES = Shape::kTiles;
+  constexpr int STAGES = Shape::kStages, SETS = kSets, BUFS = Shape::kBufs, CPS = Shape::kCps;
+  constexpr int SMEM_TILES = Shape::kTiles, STAGE_BYTES = Shape::kStageBytes;
+  static_assert(!kPair || CPS == 1, "pairs multicast one subkey slab per stage");
   extern __shared__ unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t bars[2 * STAGES + 2 * TBUFS + 1];
   __shared__ uint32_t s_tmem_base;
@@ -289,15 +295,16 @@ select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
     // warp's first wait runs out, the kernel records PKM_ERR_TIMEOUT and every
     // warp returns; no copy is ever in flight)
     if (lane == 0 && !stall) {
-      const uint32_t tx = (uint32_t)(A_BYTES + NC * BK * 2);
       uint32_t it = 0;
       bool ok = true;
       for (int i0 = 0; ok && i0 < mine; i0 += SETS)
-        for (int ch = 0; ok && ch < nch; ++ch)
+        for (int ch = 0; ok && ch < nch; ch += CPS)
           for (int st = 0; ok && st < SETS && i0 + st < mine; ++st) {
             const int u = unit_at(i0 + st);
             const int tile = u >> 1, half = u & 1;
             const int rt = tile / H, h = tile - rt * H;
+            const int nc = CPS == 2 && ch + 1 < nch ? 2 : 1;  // key chunks in these stages
+            const uint32_t tx = (uint32_t)(A_BYTES + nc * NC * BK * 2);
             for (int kb = 0; kb < kb_count; ++kb) {
               const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
               if (!wait_phase(bar_empty(s), ph ^ 1u, ctl)) {
@@ -311,8 +318,9 @@ select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
                 tma_load_3d_mc(a_dst + A_BYTES + rank * (NC / 2) * 128, &tmap_c_half, kb * BK,
                                ch * NC + (int)rank * (NC / 2), h * 2 + half, bar_full(s), 3);
               else
-                tma_load_3d(a_dst + A_BYTES, &tmap_c, kb * BK, ch * NC, h * 2 + half,
-                            bar_full(s));
+                for (int c = 0; c < nc; ++c)
+                  tma_load_3d(a_dst + A_BYTES + c * B_BYTES, &tmap_c, kb * BK, (ch + c) * NC,
+                              h * 2 + half, bar_full(s));
               ++it;
             }
           }
@@ -328,16 +336,18 @@ select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
       uint32_t it = 0, cnt[SETS] = {};
       bool ok = true;
       for (int i0 = 0; ok && i0 < mine; i0 += SETS)
-        for (int ch = 0; ok && ch < nch; ++ch)
+        for (int ch = 0; ok && ch < nch; ch += CPS)
           for (int st = 0; ok && st < SETS && i0 + st < mine; ++st) {
-            const uint32_t buf = st * BUFS + cnt[st] % BUFS, use = cnt[st] / BUFS;
-            ++cnt[st];
-            if (!wait_phase(bar_tempty(buf), (use & 1u) ^ 1u, ctl)) {
-              ok = false;
-              break;
+            const int nc = CPS == 2 && ch + 1 < nch ? 2 : 1;  // key chunks in these stages
+            uint32_t buf[CPS];
+            for (int c = 0; ok && c < nc; ++c) {
+              buf[c] = st * BUFS + cnt[st] % BUFS;
+              const uint32_t use = cnt[st] / BUFS;
+              ++cnt[st];
+              if (!wait_phase(bar_tempty(buf[c]), (use & 1u) ^ 1u, ctl)) ok = false;
             }
+            if (!ok) break;
             tc_fence_after();
-            const uint32_t d_tmem = tmem + buf * NCMAX;
             for (int kb = 0; kb < kb_count; ++kb, ++it) {
               const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
               if (!wait_phase(bar_full(s), ph, ctl)) {
@@ -346,10 +356,14 @@ select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
               }
               tc_fence_after();
               const uint64_t a_desc = sw128_desc(tiles_u32 + s * STAGE_BYTES);
-              const uint64_t b_desc = sw128_desc(tiles_u32 + s * STAGE_BYTES + A_BYTES);
+              for (int c = 0; c < nc; ++c) {
+                const uint32_t d_tmem = tmem + buf[c] * NCMAX;
+                const uint64_t b_desc =
+                    sw128_desc(tiles_u32 + s * STAGE_BYTES + A_BYTES + c * B_BYTES);
 #pragma unroll
-              for (int kk = 0; kk < BK / 16; ++kk)
-                tc_mma(d_tmem, a_desc + 2u * kk, b_desc + 2u * kk, idesc, (kb | kk) != 0);
+                for (int kk = 0; kk < BK / 16; ++kk)
+                  tc_mma(d_tmem, a_desc + 2u * kk, b_desc + 2u * kk, idesc, (kb | kk) != 0);
+              }
               // frees the stage once these MMAs have read it (pair: in both CTAs,
               // whose halves of the subkey slab it holds)
               if (kPair)
@@ -358,7 +372,7 @@ select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
                 tc_commit(bar_empty(s));
             }
             if (!ok) break;
-            tc_commit(bar_tfull(buf));  // chunk complete in TMEM
+            for (int c = 0; c < nc; ++c) tc_commit(bar_tfull(buf[c]));  // chunks complete in TMEM
           }
       // all issued MMAs complete before TMEM is released
       tc_commit(bar_done);
