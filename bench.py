@@ -500,13 +500,29 @@ def run_ours(args, rank, world, local):
     for _ in range(e2e_steps):
         e2e_call()
     e2e_sync_s = dist_max((time.perf_counter() - t0) / e2e_steps, world)
-    # two steps (calls) in flight
+    # several steps (calls) in flight
     e2e_pipelined(4)
     dist_barrier(world)
     t0 = time.perf_counter()
     e2e_pipelined(e2e_steps)
     e2e_s = dist_max((time.perf_counter() - t0) / e2e_steps, world)
     pk.pkm_destroy(h)
+
+    # this host's copy rates on the same pinned buffers (one copy each way,
+    # alone), to read the end-to-end figures against
+    def copy_gbs(dst, src):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        dst.copy_(src, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        return src.numel() * src.element_size() / (a.elapsed_time(b) * 1e-3) / 1e9
+    h_in = in_host if (train or layer) else q_host
+    d_tmp = torch.empty_like(h_in, device="cuda")
+    copy_gbs(d_tmp, h_in)
+    h2d_gbs = copy_gbs(d_tmp, h_in)
+    d2h_gbs = copy_gbs(out_host, out)
+    del d_tmp
 
     pk_ = peaks()
     gather_bytes = B * H * k * value_row_bytes(c) + B * H * k * 12 + B * d_v * 4
@@ -565,6 +581,7 @@ def run_ours(args, rank, world, local):
         "e2e": {"value": world * B * H / e2e_s, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": B * d_v * 4,
                 "calls_in_flight": 2 if (train or layer) else IN_FLIGHT,
+                "copy_gbs": {"h2d": h2d_gbs, "d2h": d2h_gbs},
                 "value_one_call_in_flight": world * B * H / e2e_sync_s},
         # per step: select_tc_kernel and merge_kernel, their retry launches
         # (return at once when no row missed its threshold hint) and the
