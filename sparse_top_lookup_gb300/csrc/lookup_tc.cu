@@ -14,12 +14,19 @@
 //               (bf16, 128-byte swizzle) into a 3-stage shared-memory ring;
 //   warp 1      allocates 512 TMEM columns and issues tcgen05.mma
 //               (M=128, N=NC<=128, K=16, fp32 accumulate) into four TMEM
-//               buffers, two per epilogue set, so scoring overlaps selection;
-//   warps 2..9  two epilogue sets of four warps, each set on every other
-//               unit; one thread per query row (= TMEM lane) reads its row's
-//               scores with tcgen05.ld and selects the half's exact top-KL
-//               (selection helpers below), then writes the half's list by
-//               (score desc, subkey asc) to global memory.
+//               buffers, shared out among the epilogue sets, so scoring
+//               overlaps selection;
+//   warps 2..   the epilogue sets of four warps, each set on every other
+//               unit (or one set on every unit); one thread per query row
+//               (= TMEM lane) reads its row's scores with tcgen05.ld and
+//               selects the half's exact top-KL (selection helpers below),
+//               then writes the half's list by (score desc, subkey asc) to
+//               global memory.
+// Forms (template arguments, chosen per call by the host): two sets per CTA
+// in clusters of two CTAs that share each subkey slab by multicast
+// (kPair); two sets per CTA alone (the retry pass); one set per CTA whose
+// stages each hold a query slab and two key chunks' subkey slabs (wide
+// half-queries, where the tile bytes an SM receives bound the kernel).
 // The k^2 merge and the softmax (a4, a5) run in lookup_merge.cu, one thread
 // per (query, head).  A retry launch of this kernel re-selects, without the
 // threshold hint, the units listed in a device array.  Scores never leave
