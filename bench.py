@@ -586,10 +586,11 @@ def run_ours(args, rank, world, local):
         # per step: select_tc_kernel and merge_kernel, their retry launches
         # (return at once when no row missed its threshold hint) and the
         # value read (fp32 inputs: lookup_simt_kernel and the value read)
-        # (training: bucket_count, bucket_scan, bucket_scatter, row_grad and
-        # ds_rows kernels too, besides a memset and two cuBLAS GEMM launches)
-        "gpu_launches": ((5 if bf16 else 2) + (1 if layer else 0) + (5 if train else 0))
-        * args.steps,
+        # (training: bucket_count, bucket_scan, bucket_scatter, bucket_sort,
+        # row_grad and ds_rows kernels too, and zero_rows for the sparse
+        # gradient, besides memsets and two cuBLAS GEMM launches)
+        "gpu_launches": ((5 if bf16 else 2) + (1 if layer else 0)
+                         + ((7 if sparse else 6) if train else 0)) * args.steps,
         "clocks": clk.summary(),
     }
     if train:
