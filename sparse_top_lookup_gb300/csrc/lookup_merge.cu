@@ -39,7 +39,9 @@ struct MergeLayout {
   // thread inside its own column, so warps in different phases never touch
   // each other's slots.
   static constexpr int kRegionA = (kRest > 2 * KL ? kRest : 2 * KL) * 4 * kThreads;
-  static constexpr int kBytes = kRegionA + 2 * KL * 2 * kThreads;  // + the lists' subkeys
+  static constexpr int kRegionC = kRegionA + 2 * KL * 2 * kThreads;  // after the lists' subkeys
+  // region C, [place][thread]: the survivors' pair codes by output place
+  static constexpr int kBytes = kRegionC + KL * 4 * kThreads;
 };
 
 // Pairs: first pass, pair = blockIdx.x * 128 + thread; retry pass, CTA c takes
@@ -56,6 +58,7 @@ merge_kernel(const float* __restrict__ list_v, const unsigned short* __restrict_
   float* sv = reinterpret_cast<float*>(smem);                                   // [KL][T]
   uint32_t* sp = reinterpret_cast<uint32_t*>(sv + KL * kThreads);               // [KL][T]
   unsigned short* sc = reinterpret_cast<unsigned short*>(smem + Lay::kRegionA); // [2KL][T]
+  uint32_t* so = reinterpret_cast<uint32_t*>(smem + Lay::kRegionC);             // [KL][T]
   const int t = threadIdx.x;
   int pair;
   // every lane stays to the end (warp votes below); lanes without a pair of
@@ -183,14 +186,36 @@ merge_kernel(const float* __restrict__ list_v, const unsigned short* __restrict_
   int64_t* ip = idx + (size_t)pair * k;
   float* wp = w + (size_t)pair * k;
   if (!tie && nsurv == (uint32_t)KL) {
+    // each survivor's output place is the number of larger sums; its pair
+    // code goes to that place's slot of this thread's column
 #pragma unroll 2
     for (int e = 0; e < KL; ++e) {
       const float s = sv[e * kThreads + t];
-      const int pc = (int)sp[e * kThreads + t];
-      const int r = count_greater<KL>(V, s);
-      if (r < k) {
-        ip[r] = (int64_t)(col1(pc >> 5) * n + col2(pc & 31));
-        wp[r] = expf(s - V[0]) / z;
+      so[count_greater<KL>(V, s) * kThreads + t] = sp[e * kThreads + t];
+    }
+    // then the places in order: flat index and softmax weight (the place's
+    // sum is V[r]), written as whole vectors when the row holds KL
+    const float inv_z = 1.0f / z;
+    auto flat = [&](int r) {
+      const int pc = (int)so[r * kThreads + t];
+      return (int64_t)(col1(pc >> 5) * n + col2(pc & 31));
+    };
+    if (k == KL) {
+#pragma unroll
+      for (int r = 0; r < KL; r += 4) {
+        reinterpret_cast<longlong2*>(ip + r)[0] = make_longlong2(flat(r), flat(r + 1));
+        reinterpret_cast<longlong2*>(ip + r)[1] = make_longlong2(flat(r + 2), flat(r + 3));
+        reinterpret_cast<float4*>(wp + r)[0] =
+            make_float4(expf(V[r] - V[0]) * inv_z, expf(V[r + 1] - V[0]) * inv_z,
+                        expf(V[r + 2] - V[0]) * inv_z, expf(V[r + 3] - V[0]) * inv_z);
+      }
+    } else {
+#pragma unroll
+      for (int r = 0; r < KL; ++r) {
+        if (r < k) {
+          ip[r] = flat(r);
+          wp[r] = expf(V[r] - V[0]) * inv_z;
+        }
       }
     }
     return;
