@@ -114,11 +114,12 @@ enum {
      overlap the computation of slice i; the first and last slices are half
      the size of the others (shorter pipeline fill and drain). */
   PKM_OPT_HOST_CHUNKS = 2,
-  /* Tests of failure reporting only (1 on, 0 off): while on, the bf16
+  /* Tests of failure reporting only (a bit mask, 0 off): with bit 0 the bf16
      lookups of this handle run their selection kernel with its loads held
-     back, so the kernel's bounded pipeline wait runs out (about 2 s), it
-     records PKM_ERR_TIMEOUT in the status word and returns; results of such
-     calls are not meaningful.  The GPU context stays usable. */
+     back, with bit 1 the bulk-copy value read issues no copy; the kernel's
+     bounded waits run out (about 2 s), it records PKM_ERR_TIMEOUT in the
+     status word and returns; results of such calls are not meaningful.  The
+     GPU context stays usable. */
   PKM_OPT_TEST_STALL = 3,
   /* SMs of the value read (pkm_gather, pkm_forward, pkm_forward_host); 0
      (default): all of them.  Value rows of 512-byte multiples (up to 8 KB)

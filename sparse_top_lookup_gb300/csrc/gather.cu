@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
 gather_bulk_kernel(const unsigned char* __restrict__ values, const float* __restrict__ scales,
                    int64_t N, int row_bytes, int rows_per_bag, int B, int teams, int nbs,
                    const int64_t* __restrict__ idx, const float* __restrict__ w,
-                   float* __restrict__ out, int* __restrict__ status) {
+                   float* __restrict__ out, int* __restrict__ status, int stall) {
   using namespace tc;
   constexpr int E = VecAcc<VT>::kElems;
   constexpr bool kFp8 = VT == PKM_FP8_E4M3;
@@ -238,7 +238,11 @@ gather_bulk_kernel(const unsigned char* __restrict__ values, const float* __rest
   const Ctl ctl{&s_abort, status};
   auto bag_of = [&](int64_t g, int t) { return (g * gridDim.x + blockIdx.x) * (int64_t)teams + t; };
 
-  if (warp < teams) {
+  if (warp < teams && stall) {
+    // (stall: a test of the bounded waits; no copy is issued, so every
+    // consumer's first wait runs out, the kernel records PKM_ERR_TIMEOUT and
+    // every warp returns)
+  } else if (warp < teams) {
     // ------------------------------------------------------------ producer
     const int t = warp;
     int64_t* my_idx = st_idx + (size_t)t * 3 * rpb;  // [3][rpb], bag g in buffer g % 3
@@ -398,7 +402,7 @@ bool bulk_shape(int vpr, int rows_per_bag, int& teams, int& nbs, size_t& smem) {
 template <int VT>
 cudaError_t launch_gather_vt(const void* values, int64_t N, int d_v, int B, int rows_per_bag,
                              const int64_t* idx, const float* w, float* out, int* status,
-                             int ctas, cudaStream_t stream) {
+                             int ctas, bool stall, cudaStream_t stream) {
   constexpr int E = VecAcc<VT>::kElems;
   const int vpr = d_v / E;  // 16-byte vectors per row
   // an fp8 table's row scales follow its N * d_v code bytes
@@ -420,7 +424,7 @@ cudaError_t launch_gather_vt(const void* values, int64_t N, int d_v, int B, int 
     const int grid = want < ctas ? (int)want : ctas;
     gather_bulk_kernel<VT><<<grid, teams * (32 + vpr), bulk_smem, stream>>>(
         static_cast<const unsigned char*>(values), scales, N, vpr * 16, rows_per_bag, B, teams,
-        nbs, idx, w, out, status);
+        nbs, idx, w, out, status, stall ? 1 : 0);
     return cudaGetLastError();
   }
   int groups = vpr >= 128 ? 1 : 128 / vpr;
@@ -459,16 +463,16 @@ bool gather_bulk_ok(int value_dtype, int d_v, int rows_per_bag) {
 
 cudaError_t launch_gather(const void* values, int value_dtype, int64_t N, int d_v, int B,
                           int rows_per_bag, const int64_t* idx, const float* w, float* out,
-                          int* status, cudaStream_t stream, int ctas) {
+                          int* status, cudaStream_t stream, int ctas, bool stall) {
   if (B == 0) return cudaSuccess;
   if (value_dtype == PKM_FP8_E4M3)
     return launch_gather_vt<PKM_FP8_E4M3>(values, N, d_v, B, rows_per_bag, idx, w, out, status,
-                                          ctas, stream);
+                                          ctas, stall, stream);
   if (value_dtype == PKM_BF16)
     return launch_gather_vt<PKM_BF16>(values, N, d_v, B, rows_per_bag, idx, w, out, status, ctas,
-                                      stream);
+                                      stall, stream);
   return launch_gather_vt<PKM_F32>(values, N, d_v, B, rows_per_bag, idx, w, out, status, ctas,
-                                   stream);
+                                   stall, stream);
 }
 
 }  // namespace pkm

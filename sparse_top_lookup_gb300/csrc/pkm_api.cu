@@ -40,7 +40,7 @@ struct pkm_handle {
   cudaEvent_t ev_done[kHostSlots], ev_in[PKM_HOST_MAX_CHUNKS], ev_comp[PKM_HOST_MAX_CHUNKS];
   int host_chunks;
   bool host_chunks_set;  // PKM_OPT_HOST_CHUNKS given by the caller
-  int test_stall;        // PKM_OPT_TEST_STALL: the bf16 lookups stall their selection kernel
+  int test_stall;        // PKM_OPT_TEST_STALL: 1 stalls the selection kernel, 2 the bulk read
   int sms;               // SMs of the device
   int read_sms;          // PKM_OPT_READ_SMS: SMs of the value read (0: all)
 };
@@ -111,7 +111,7 @@ int run_lookup(pkm_t h, const void* q, const void* subkeys, int B, int H, int n,
                                          static_cast<const uint16_t*>(subkeys), B, H, h->cfg.d_q,
                                          n, k, z, idx, w, h->status,
                                          {h->retry_counts, h->retry_counts + 2, h->unit_list},
-                                         h->list_v, h->list_c, s, h->test_stall != 0));
+                                         h->list_v, h->list_c, s, (h->test_stall & 1) != 0));
   }
   return cuda_rc(pkm::launch_lookup_simt(static_cast<const float*>(q),
                                          static_cast<const float*>(subkeys), B, H, h->cfg.d_q, n,
@@ -124,7 +124,8 @@ int run_gather(pkm_t h, const void* values, int B, int H, int n, int k, const in
                const float* w, float* out, cudaStream_t s, int ctas = 0) {
   if (ctas <= 0) ctas = h->read_sms > 0 ? h->read_sms : h->sms;
   return cuda_rc(pkm::launch_gather(values, h->cfg.value_dtype, (int64_t)n * n, h->cfg.d_v, B,
-                                    H * k, idx, w, out, h->status, s, ctas));
+                                    H * k, idx, w, out, h->status, s, ctas,
+                                    (h->test_stall & 2) != 0));
 }
 
 }  // namespace
@@ -495,7 +496,7 @@ int pkm_set_option(pkm_t h, int option, double value) {
       h->host_chunks_set = true;
       return PKM_OK;
     case PKM_OPT_TEST_STALL:
-      if (value != 0 && value != 1) return PKM_ERR_OPTION;
+      if (!(value >= 0 && value <= 3) || value != (int)value) return PKM_ERR_OPTION;
       h->test_stall = (int)value;
       return PKM_OK;
     case PKM_OPT_READ_SMS:

@@ -56,10 +56,12 @@ cudaError_t launch_backward_scores(cublasHandle_t blas, const uint16_t* q,
 // out: [B, d_v] fp32.  ctas > 0 and a row shape that gather_bulk_ok accepts:
 // a persistent grid of at most ctas CTAs (one per SM) streaming whole rows
 // with bulk copies; otherwise one CTA per bag on every SM.  Returns a
-// cudaError_t of the launch.
+// cudaError_t of the launch.  stall (tests of the bounded waits only): the
+// bulk-copy form issues no copy, so its consumers' waits run out (about 2 s)
+// and it records PKM_ERR_TIMEOUT; the output is not meaningful.
 cudaError_t launch_gather(const void* values, int value_dtype, int64_t N, int d_v, int B,
                           int rows_per_bag, const int64_t* idx, const float* w, float* out,
-                          int* status, cudaStream_t stream, int ctas = 0);
+                          int* status, cudaStream_t stream, int ctas = 0, bool stall = false);
 bool gather_bulk_ok(int value_dtype, int d_v, int rows_per_bag);
 
 // Steps a1-a5 on the CUDA cores: fp32 queries/subkeys, and bf16 ones with a
