@@ -303,6 +303,8 @@ def run_ours(args, rank, world, local):
     cfg = pk.make_config(d_q, d_v, B, H, n, k, q_dtype=dt, value_dtype=vdt, host_staging=1,
                          with_backward=int(train))
     h = pk.pkm_create(cfg)
+    if args.select_form is not None:
+        pk.check(pk.pkm_set_option(h, pk.PKM_OPT_SELECT_FORM, args.select_form), "set_option")
     stream = torch.cuda.current_stream()
     sparse = bool(c.get("sparse_grad"))
     if train:
@@ -575,7 +577,7 @@ def run_ours(args, rank, world, local):
                        if train else {})),
         "roofline": roof,
         "retried_pairs": retried,
-        "scoring_roofline": {"kernel": "select_tc_kernel + merge_kernel (a1-a5, one lookup call)",
+        "scoring_roofline": {"kernel": "select_2sm_kernel + merge_kernel (a1-a5, one lookup call)",
                              "bound": "tensor", "achieved": tflops, "peak": pk_["bf16"],
                              "unit": "TFLOP/s", "frac": tflops / pk_["bf16"],
                              "peak_source": pk_["src"] + " bf16 burst"},
@@ -664,6 +666,9 @@ def main():
     ap.add_argument("--n-keys", type=int, default=None,
                     help="override the workload's n_keys (small profiling captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--select-form", type=int, default=None, choices=[0, 1, 2],
+                    help="selection kernel form of the bf16 lookup (0 automatic, 1 one-SM, "
+                         "2 two-SM)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -126,7 +126,13 @@ enum {
      stream through shared memory as whole-row bulk copies, one persistent CTA
      per SM; other row widths are read with one CTA per query on every SM
      whatever this option says. */
-  PKM_OPT_READ_SMS = 4
+  PKM_OPT_READ_SMS = 4,
+  /* bf16 lookups with k <= 32: the form of the selection kernel's main pass.
+     0 (default): automatic; 1: one-SM forms (tcgen05 MMAs of 128 query rows
+     per SM); 2: the two-SM form (MMAs of 256 query rows spanning the two
+     CTAs of a cluster, each loading half of every subkey slab).  Results are
+     the same in every form. */
+  PKM_OPT_SELECT_FORM = 5
 };
 #define PKM_HOST_MAX_CHUNKS 16
 

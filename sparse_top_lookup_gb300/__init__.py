@@ -20,6 +20,7 @@ PKM_ERR_CUDA, PKM_ERR_NOMEM, PKM_ERR_TIMEOUT, PKM_ERR_BAD_INDEX = -5, -6, -7, -8
 PKM_ERR_NO_STAGING, PKM_ERR_OPTION, PKM_ERR_NO_BACKWARD = -9, -10, -11
 PKM_OPT_HINT_Z, PKM_OPT_HOST_CHUNKS, PKM_OPT_TEST_STALL = 1, 2, 3
 PKM_OPT_READ_SMS = 4
+PKM_OPT_SELECT_FORM = 5
 PKM_HOST_MAX_CHUNKS = 16
 
 EXPORTED = ["pkm_create", "pkm_destroy", "pkm_forward", "pkm_lookup", "pkm_gather",

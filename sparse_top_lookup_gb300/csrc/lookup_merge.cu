@@ -28,6 +28,13 @@ namespace {
 
 constexpr int kThreads = 128;
 
+int tc_sms() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
 template <int KL>
 struct MergeLayout {
   static constexpr MergePairs<KL> P{};
@@ -44,13 +51,14 @@ struct MergeLayout {
   static constexpr int kBytes = kRegionC + KL * 4 * kThreads;
 };
 
-// Pairs: first pass, pair = blockIdx.x * 128 + thread; retry pass, CTA c takes
-// listed unit c (if c < the listed count) and thread t its row tile's query t.
+// One CTA's pairs: first pass, pair = cta * 128 + thread; retry pass, listed
+// unit `cta` and thread t its row tile's query t.
 template <int KL>
-__global__ void __launch_bounds__(kThreads)
-merge_kernel(const float* __restrict__ list_v, const unsigned short* __restrict__ list_c, int B,
-             int H, int n, int k, int64_t* __restrict__ idx, float* __restrict__ w,
-             RetryScratch retry, bool retry_pass) {
+__device__ __forceinline__ void merge_cta(const float* __restrict__ list_v,
+                                          const unsigned short* __restrict__ list_c, int B, int H,
+                                          int n, int k, int64_t* __restrict__ idx,
+                                          float* __restrict__ w, const RetryScratch& retry,
+                                          bool retry_pass, int cta) {
   using Lay = MergeLayout<KL>;
   constexpr MergePairs<KL> P{};
   extern __shared__ __align__(16) unsigned char smem[];
@@ -65,14 +73,13 @@ merge_kernel(const float* __restrict__ list_v, const unsigned short* __restrict_
   // their own work on zeros and store nothing
   bool valid;
   if (retry_pass) {
-    if ((int)blockIdx.x >= retry.counts[1]) return;  // the whole CTA: no unit listed here
-    const int tile = retry.unit_list[blockIdx.x] >> 1;
+    const int tile = retry.unit_list[cta] >> 1;
     const int rt = tile / H, h = tile - (tile / H) * H;
     const int b = rt * kThreads + t;  // row tiles hold 128 queries, one per thread
     valid = b < B;
     pair = valid ? b * H + h : 0;
   } else {
-    pair = blockIdx.x * kThreads + t;
+    pair = cta * kThreads + t;
     valid = pair < B * H;
   }
 
@@ -262,6 +269,25 @@ merge_kernel(const float* __restrict__ list_v, const unsigned short* __restrict_
   }
 }
 
+// First pass: CTA c merges pairs [128c, 128c + 128).  Retry pass: a
+// persistent grid walks the listed units (none listed: every CTA returns at
+// once).
+template <int KL>
+__global__ void __launch_bounds__(kThreads)
+merge_kernel(const float* __restrict__ list_v, const unsigned short* __restrict__ list_c, int B,
+             int H, int n, int k, int64_t* __restrict__ idx, float* __restrict__ w,
+             RetryScratch retry, bool retry_pass) {
+  if (!retry_pass) {
+    merge_cta<KL>(list_v, list_c, B, H, n, k, idx, w, retry, false, (int)blockIdx.x);
+    return;
+  }
+  const int listed = retry.counts[1];
+  for (int u = (int)blockIdx.x; u < listed; u += (int)gridDim.x) {
+    merge_cta<KL>(list_v, list_c, B, H, n, k, idx, w, retry, true, u);
+    __syncthreads();  // the CTA's shared-memory columns are reused by its next unit
+  }
+}
+
 template <int KL>
 cudaError_t launch_merge_kl(const float* list_v, const unsigned short* list_c, int B, int H, int n,
                             int k, int64_t* idx, float* w, const RetryScratch& retry,
@@ -274,8 +300,9 @@ cudaError_t launch_merge_kl(const float* list_v, const unsigned short* list_c, i
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const int64_t grid =
-      retry_pass ? retry_units(B, H) : ((int64_t)B * H + kThreads - 1) / kThreads;
+  const int64_t units = retry_units(B, H);
+  const int64_t grid = retry_pass ? (units < 2 * tc_sms() ? units : 2 * tc_sms())
+                                  : ((int64_t)B * H + kThreads - 1) / kThreads;
   merge_kernel<KL><<<(unsigned)grid, kThreads, smem, stream>>>(list_v, list_c, B, H, n, k, idx, w,
                                                                 retry, retry_pass);
   return cudaGetLastError();

@@ -605,7 +605,7 @@ int list_slots(int k) { return k <= 16 ? 16 : 32; }
 cudaError_t launch_lookup_tc(const uint16_t* q, const uint16_t* subkeys, int B, int H, int d_q,
                              int n_keys, int k, float hint_z, int64_t* idx, float* w, int* status,
                              const RetryScratch& retry, float* list_v, unsigned short* list_c,
-                             cudaStream_t stream, bool stall) {
+                             cudaStream_t stream, bool stall, int form) {
   if (B == 0) return cudaSuccess;
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
@@ -614,7 +614,7 @@ cudaError_t launch_lookup_tc(const uint16_t* q, const uint16_t* subkeys, int B, 
   const int nch = (n_keys + NC - 1) / NC;
   const int kbc = (hd + BK - 1) / BK;
 
-  CUtensorMap mq, mc, mch;
+  CUtensorMap mq, mc, mch, m2;
   {
     // q viewed as [B][H][2][hd]: innermost first.
     const cuuint64_t dims[4] = {(cuuint64_t)hd, 2, (cuuint64_t)H, (cuuint64_t)B};
@@ -644,6 +644,12 @@ cudaError_t launch_lookup_tc(const uint16_t* q, const uint16_t* subkeys, int B, 
             strides, hbox, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
+    // the two-SM form: each CTA loads 128 subkeys (half of a 256-key chunk)
+    const cuuint32_t box2[3] = {BK, 128, 1};
+    if (enc(&m2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(subkeys), dims,
+            strides, box2, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
   }
   // the main pass as CTA pairs sharing each subkey slab when there are at
   // least two row tiles and the half-query is at most 512 wide (8 k-slabs);
@@ -657,7 +663,13 @@ cudaError_t launch_lookup_tc(const uint16_t* q, const uint16_t* subkeys, int B, 
   // pipeline, not by the selection: their main pass runs one epilogue set per
   // CTA with 5 tile stages in flight
   const bool deep = kbc > 8;
+  // the two-SM form (MMAs of 256 query rows over a CTA pair, each CTA
+  // receiving half of every subkey slab) for the main pass
+  const bool two_sm = form == 2 || (form == 0 && B >= 2 * BM);
   auto select = [&](float z, const int* list, const int* count, int st) {
+    if (two_sm && !list)
+      return launch_select_2sm(mq, m2, B, H, d_q, n_keys, k, z, list_v, list_c, status, st != 0,
+                               stream);
 #define PKM_SELECT(KLv, PAIRv, SETSv)                                                          \
   launch_kl<KLv, PAIRv, SETSv>(mq, mc, mch, B, H, n_keys, NC, nch, kbc, z, list_v, list_c, \
                                status, list, count, st, stream)

@@ -43,6 +43,7 @@ struct pkm_handle {
   int test_stall;        // PKM_OPT_TEST_STALL: 1 stalls the selection kernel, 2 the bulk read
   int sms;               // SMs of the device
   int read_sms;          // PKM_OPT_READ_SMS: SMs of the value read (0: all)
+  int select_form;       // PKM_OPT_SELECT_FORM
 };
 
 namespace {
@@ -111,7 +112,8 @@ int run_lookup(pkm_t h, const void* q, const void* subkeys, int B, int H, int n,
                                          static_cast<const uint16_t*>(subkeys), B, H, h->cfg.d_q,
                                          n, k, z, idx, w, h->status,
                                          {h->retry_counts, h->retry_counts + 2, h->unit_list},
-                                         h->list_v, h->list_c, s, (h->test_stall & 1) != 0));
+                                         h->list_v, h->list_c, s, (h->test_stall & 1) != 0,
+                                         h->select_form));
   }
   return cuda_rc(pkm::launch_lookup_simt(static_cast<const float*>(q),
                                          static_cast<const float*>(subkeys), B, H, h->cfg.d_q, n,
@@ -498,6 +500,10 @@ int pkm_set_option(pkm_t h, int option, double value) {
     case PKM_OPT_TEST_STALL:
       if (!(value >= 0 && value <= 3) || value != (int)value) return PKM_ERR_OPTION;
       h->test_stall = (int)value;
+      return PKM_OK;
+    case PKM_OPT_SELECT_FORM:
+      if (!(value >= 0 && value <= 2) || value != (int)value) return PKM_ERR_OPTION;
+      h->select_form = (int)value;
       return PKM_OK;
     case PKM_OPT_READ_SMS:
       if (!(value >= 0 && value <= h->sms) || value != (int)value) return PKM_ERR_OPTION;

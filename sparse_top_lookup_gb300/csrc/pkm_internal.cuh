@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cublas_v2.h>
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -97,10 +98,22 @@ int64_t retry_units(int64_t B, int64_t H);
 // stall (tests of the bounded waits only): the first selection launch loads
 // nothing, so its pipeline wait runs out (about 2 s) and it records
 // PKM_ERR_TIMEOUT; the lists it leaves are not meaningful.
+// form: the selection kernel's main pass (PKM_OPT_SELECT_FORM: 0 automatic,
+// 1 one-SM forms, 2 the two-SM form).
 cudaError_t launch_lookup_tc(const uint16_t* q, const uint16_t* subkeys, int B, int H, int d_q,
                              int n_keys, int k, float hint_z, int64_t* idx, float* w, int* status,
                              const RetryScratch& retry, float* list_v, unsigned short* list_c,
-                             cudaStream_t stream, bool stall = false);
+                             cudaStream_t stream, bool stall = false, int form = 0);
+
+// The two-SM selection kernel (lookup_2sm.cu), the main pass of a bf16
+// lookup: per-half lists of every (query, head) in list_v / list_c.
+// tmap_q: q viewed as [B][H][2][d_q/2] in 128x64 boxes; tmap_c_half: the
+// subkeys viewed as [2H][n_keys][d_q/2] in 128x64 boxes; both 128-byte
+// swizzled.  sets: epilogue warp sets per CTA (1 or 2).
+cudaError_t launch_select_2sm(const CUtensorMap& tmap_q, const CUtensorMap& tmap_c_half, int B,
+                              int H, int d_q, int n_keys, int k, float hint_z, float* list_v,
+                              unsigned short* list_c, int* status, bool stall,
+                              cudaStream_t stream, int sets = 2);
 
 // Entries of one per-half list for a given k.
 int list_slots(int k);

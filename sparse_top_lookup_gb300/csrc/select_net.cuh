@@ -1,6 +1,7 @@
-// Selection building blocks shared by the lookup kernels: value-only
-// sorting networks, a register binary search, the candidate-pair table of
-// the k^2 merge and branch-free appends to per-thread logs in shared memory.
+// Selection building blocks shared by the lookup kernels: sorting networks
+// on values (alone, or carrying a 32-bit payload that orders equal values),
+// a register binary search, the candidate-pair table of the k^2 merge and
+// branch-free appends to per-thread logs in shared memory.
 #pragma once
 
 #include <stdint.h>
@@ -139,6 +140,22 @@ __device__ __forceinline__ void log_push(uint32_t& a, float v, float thr, uint32
       : "memory");
 }
 
+// As log_push for a log filled from its top slot downwards: the address of
+// the next free slot falls by STEP bytes when the entry is taken.  Two such
+// logs, one growing up and one down in the same slots, give two
+// independent address chains.
+template <int STEP>
+__device__ __forceinline__ void log_push_down(uint32_t& a, float v, float thr, uint32_t col) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.gt.f32 p, %1, %2;\n\t"
+      "@p st.shared.v2.b32 [%0], {%1, %3};\n\t"
+      "@p sub.u32 %0, %0, %4;\n\t}"
+      : "+r"(a)
+      : "f"(v), "f"(thr), "r"(col), "n"(STEP)
+      : "memory");
+}
+
 // Append the score v at a stage's end when v > thr (predicated store; the
 // address advances by STEP bytes when the score is taken).
 template <int STEP>
@@ -172,6 +189,80 @@ __device__ __forceinline__ void surv_push(uint32_t& va, uint32_t& count, uint32_
       : "+r"(va), "+r"(count)
       : "f"(v), "f"(thr), "r"(code), "r"(va_end), "n"(STEP), "n"(OFF)
       : "memory");
+}
+
+// ----------------------------------------------- networks with a payload
+//
+// Lists in (value desc, payload asc) order: value-only compare-exchanges,
+// then equal neighbours put in payload order (rows that hold none skip it).
+
+// Compare-exchange (value desc) carrying a 32-bit payload.
+__device__ __forceinline__ void cx_payload(float& a, float& b, uint32_t& ca, uint32_t& cb) {
+  const bool sw = b > a;
+  const float x = a, y = b;
+  const uint32_t cx = ca, cy = cb;
+  a = sw ? y : x;
+  b = sw ? x : y;
+  ca = sw ? cy : cx;
+  cb = sw ? cx : cy;
+}
+
+template <int N>
+__device__ __forceinline__ void sort_desc_payload(float (&a)[N], uint32_t (&c)[N]) {
+  constexpr OddEvenMergeNet<N> net{};
+#pragma unroll
+  for (int q = 0; q < net.kCount; ++q) cx_payload(a[net.hi[q]], a[net.lo[q]], c[net.hi[q]], c[net.lo[q]]);
+}
+
+// Put equal neighbours of a (value desc) sorted list in payload order:
+// odd-even transposition passes over the equal pairs, until a pass changes
+// nothing.  Rows without equal finite neighbours skip it (the order of -inf
+// padding does not matter).
+template <int N>
+__device__ __forceinline__ void order_ties(float (&a)[N], uint32_t (&c)[N]) {
+  bool eq = false;
+#pragma unroll
+  for (int i = 0; i + 1 < N; ++i) eq |= a[i] == a[i + 1] && a[i] > -INFINITY;
+  if (!eq) return;
+#pragma unroll 1
+  for (int pass = 0; pass < N; ++pass) {
+    bool moved = false;
+#pragma unroll
+    for (int i = 0; i + 1 < N; ++i) {
+      if ((i & 1) != (pass & 1)) continue;
+      const bool sw = a[i] == a[i + 1] && c[i] > c[i + 1];
+      const uint32_t x = c[i], y = c[i + 1];
+      c[i] = sw ? y : x;
+      c[i + 1] = sw ? x : y;
+      moved |= sw;
+    }
+    if (!moved && pass > 0) break;
+  }
+}
+
+// V / C (KL) <- the KL best of V and B (NB <= KL), both in (value desc,
+// payload asc) order, payloads alongside: the first step pairs V's last NB
+// with B reversed and keeps the better of each pair (a bitonic split, exact
+// under that order), the rest is a bitonic merge by value.
+template <int KL, int NB>
+__device__ __forceinline__ void merge_top_payload(float (&V)[KL], uint32_t (&C)[KL],
+                                                  const float (&Bv)[NB], const uint32_t (&Bc)[NB]) {
+#pragma unroll
+  for (int i = 0; i < NB; ++i) {
+    const float a = V[KL - NB + i], b = Bv[NB - 1 - i];
+    const uint32_t ca = C[KL - NB + i], cb = Bc[NB - 1 - i];
+    const bool take = b > a || (b == a && cb < ca);
+    V[KL - NB + i] = take ? b : a;
+    C[KL - NB + i] = take ? cb : ca;
+  }
+#pragma unroll
+  for (int stride = KL >> 1; stride > 0; stride >>= 1)
+#pragma unroll
+    for (int i = 0; i < KL; ++i) {
+      const int j = i ^ stride;
+      if (j > i) cx_payload(V[i], V[j], C[i], C[j]);
+    }
+  order_ties<KL>(V, C);
 }
 
 }  // namespace pkm

@@ -135,6 +135,80 @@ __device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
       : "memory");
 }
 
+// ---------------------------------------------- two-SM (CTA pair) forms
+//
+// tcgen05 with .cta_group::2: one MMA spans the two CTAs of a cluster pair.
+// A (M = 256) is split by rows, 128 in each CTA's shared memory; B (N keys)
+// by its N rows, N/2 in each CTA's shared memory, both at the same offsets;
+// each CTA's TMEM receives its own 128 rows x N columns.  The MMAs, their
+// commits and the TMEM allocation all use .cta_group::2 in such a kernel.
+
+// Shared-memory address of the same variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+// Tile loads into this CTA's shared memory whose completion is signalled on
+// an mbarrier that may sit in either CTA of the pair (bar: a shared::cluster
+// address, e.g. from mapa_shared).
+__device__ __forceinline__ void tma_load_4d_cg2(uint32_t dst, const CUtensorMap* map, int c0,
+                                                int c1, int c2, int c3, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_cg2(uint32_t dst, const CUtensorMap* map, int c0,
+                                                int c1, int c2, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_mma_cg2(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrives on the mbarrier at this offset in every CTA of `mask` once the
+// pair MMAs issued so far by this thread have completed.
+__device__ __forceinline__ void tc_commit_cg2_mc(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
+
+// Arrival (release at cluster scope) on an mbarrier given by its
+// shared::cluster address, in this CTA or its peer.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -233,6 +307,22 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const 
   const unsigned long long t0 = globaltimer();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
+    if (*ctl.abort) return false;
+    if (globaltimer() - t0 > WAIT_LIMIT_NS) {
+      *ctl.abort = 1;
+      atomicExch(ctl.status, PKM_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// As wait_phase, acquiring at cluster scope: for barriers that the peer CTA
+// of a pair arrives on (directly, or through a TMA or MMA completion).
+__device__ __forceinline__ bool wait_phase_cluster(uint32_t bar, uint32_t parity, const Ctl& ctl) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  while (true) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
     if (*ctl.abort) return false;
     if (globaltimer() - t0 > WAIT_LIMIT_NS) {
       *ctl.abort = 1;

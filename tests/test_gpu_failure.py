@@ -20,7 +20,11 @@ torch = pytest.importorskip("torch")
 pk = pytest.importorskip("sparse_top_lookup_gb300")
 
 
-def test_bounded_wait_runs_out_is_reported_and_context_stays_usable():
+@pytest.mark.parametrize("form", [1, 2])
+def test_bounded_wait_runs_out_is_reported_and_context_stays_usable(form):
+    # form 1: the one-SM selection kernel; form 2: the two-SM one, whose two
+    # CTAs both run out (each on its own waits) and meet at the final cluster
+    # barrier
     B, H, d_q, n, d_v, k = 256, 1, 128, 256, 64, 16
     s = synth.seed_of(dict(cfg_id=160))
     q = synth.normal(s, 1, B * H * d_q, 1.0, dtype="bf16")
@@ -30,6 +34,7 @@ def test_bounded_wait_runs_out_is_reported_and_context_stays_usable():
         tq, tC = to_device(q, "bf16"), to_device(C, "bf16")
         idx = torch.empty(B, H, k, dtype=torch.int64, device="cuda")
         w = torch.empty(B, H, k, device="cuda")
+        pk.check(pk.pkm_set_option(h, pk.PKM_OPT_SELECT_FORM, form), "set_option")
         assert pk.pkm_set_option(h, pk.PKM_OPT_TEST_STALL, 4) == pk.PKM_ERR_OPTION
         pk.check(pk.pkm_set_option(h, pk.PKM_OPT_TEST_STALL, 1), "set_option")
         pk.check(pk.pkm_lookup(h, tq, tC, B, H, n, k, idx, w), "pkm_lookup")

@@ -18,13 +18,15 @@ torch = pytest.importorskip("torch")
 pk = pytest.importorskip("sparse_top_lookup_gb300")
 
 
-def run_forward(cfgd, q, C, V, B=None, hint_z=None, report=None):
+def run_forward(cfgd, q, C, V, B=None, hint_z=None, report=None, form=None):
     B = cfgd["B"] if B is None else B
     H, k, d_v = cfgd["H"], cfgd["k"], cfgd["d_v"]
     h, _ = make_handle(dict(cfgd, B=max(B, 1)))
     try:
         if hint_z is not None:
             pk.check(pk.pkm_set_option(h, pk.PKM_OPT_HINT_Z, hint_z), "set_option")
+        if form is not None:
+            pk.check(pk.pkm_set_option(h, pk.PKM_OPT_SELECT_FORM, form), "set_option")
         dq, dC, dV = (to_device(x, cfgd["dtype"]) for x in (q, C, V))
         out = torch.empty(B, d_v, device="cuda")
         idx = torch.empty(B, H, k, dtype=torch.int64, device="cuda")
@@ -38,9 +40,10 @@ def run_forward(cfgd, q, C, V, B=None, hint_z=None, report=None):
         pk.pkm_destroy(h)
 
 
-def check_against_oracle(cfgd, q, C, V, max_near_frac=0.01, hint_z=None, report=None):
+def check_against_oracle(cfgd, q, C, V, max_near_frac=0.01, hint_z=None, report=None,
+                         form=None):
     B, H, d_q, n, d_v, k = (cfgd[x] for x in ("B", "H", "d_q", "n_keys", "d_v", "k"))
-    out, idx, w = run_forward(cfgd, q, C, V, hint_z=hint_z, report=report)
+    out, idx, w = run_forward(cfgd, q, C, V, hint_z=hint_z, report=report, form=form)
     ref = oracle.lookup(q, C, B, H, d_q, n, k)
     rep = compare_lookup(idx, w, ref, q, C, cfgd["dtype"], H, d_q, n)
     assert rep["failures"] == 0, rep
@@ -100,6 +103,49 @@ def random_case(seed, B, H, d_q, n, d_v, k, dtype="bf16", kvar=None):
 def test_bf16_shapes(shape):
     c, q, C, V = random_case(sum(shape), *shape)
     check_against_oracle(c, q, C, V)
+
+
+@pytest.mark.parametrize("shape", [
+    # B, H, d_q, n, d_v, k: the two-SM selection form forced
+    (100, 1, 128, 256, 64, 16),     # one pair tile: the second CTA's rows all out of range
+    (300, 2, 128, 256, 128, 16),    # second pair tile ragged (300 = 256 + 44)
+    (257, 1, 64, 520, 256, 32),     # three 256-key chunks, the last one holding 8 keys
+    (130, 3, 192, 100, 64, 8),      # n below one CTA's 128-key half; 3 k-slabs, the last partial
+    (64, 2, 256, 48, 128, 1),       # k = 1
+    (40, 1, 32, 20, 64, 20),        # k = n_keys, one k-slab of 16 columns
+    (520, 2, 1024, 1024, 1024, 32),  # page-width rows: 4 chunks of 8 k-slabs
+    (300, 8, 256, 256, 128, 32),    # eight heads
+    (129, 1, 128, 2048, 64, 32),    # 8 chunks per half (the large workload's n_keys)
+    (260, 2, 2048, 512, 128, 32),   # 16 k-slabs per chunk (the large workload's width)
+])
+def test_two_sm_form_shapes(shape):
+    c, q, C, V = random_case(sum(shape) + 5, *shape)
+    check_against_oracle(c, q, C, V, form=2)
+
+
+@pytest.mark.parametrize("z", [1e30, 1.53, -1e30])
+def test_two_sm_form_exact_for_any_threshold_hint(z):
+    # every row retried (huge z: the lists are marked and the retry pass
+    # selects their 128-row units with the one-SM kernel), about half of them,
+    # or none with every score logged (repeated compactions from both log ends)
+    c, q, C, V = random_case(99, 520, 2, 256, 1024, 128, 32)
+    info = {}
+    check_against_oracle(c, q, C, V, hint_z=z, report=info, form=2)
+    if z == 1e30:
+        assert info["fallback"] == c["B"] * c["H"]
+    if z < 0:
+        assert info["fallback"] == 0
+
+
+@pytest.mark.parametrize("form", [1, 2])
+def test_forms_agree_bit_for_bit(form):
+    # the mid workload through each selection form gives the same indices,
+    # weights and outputs as the automatic choice
+    c, q, C, V = cfg_inputs("mid")
+    want = run_forward(c, q, C, V)
+    got = run_forward(c, q, C, V, form=form)
+    for a, b in zip(got, want):
+        assert np.array_equal(a, b)
 
 
 @pytest.mark.parametrize("shape", [
@@ -165,8 +211,8 @@ def test_fp32_shapes():
     check_against_oracle(c, q, C, V)
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
-def test_exact_integer_ties_bit_exact(dtype):
+@pytest.mark.parametrize("dtype,form", [("bf16", 1), ("bf16", 2), ("f32", None)])
+def test_exact_integer_ties_bit_exact(dtype, form):
     # Small integers are exact in bf16/fp32 and every partial sum stays exact
     # in fp32, so GPU and oracle scores are identical: the tie rule (lower
     # subkey index per half, lower flat index overall) must match bit for bit.
@@ -182,10 +228,32 @@ def test_exact_integer_ties_bit_exact(dtype):
     else:
         q, C, V = qf, Cf, Vf
     c = dict(B=B, H=H, d_q=d_q, n_keys=n, d_v=d_v, k=k, dtype=dtype)
-    out, idx, w = run_forward(c, q.ravel(), C.ravel(), V.ravel())
+    out, idx, w = run_forward(c, q.ravel(), C.ravel(), V.ravel(), form=form)
     ref = oracle.lookup(q.ravel(), C.ravel(), B, H, d_q, n, k)
     assert np.array_equal(idx, ref["idx"])
     assert (np.abs(w - ref["w"]) <= 1e-6 * (1 + ref["w"])).all()
+
+
+@pytest.mark.parametrize("form", [1, 2])
+def test_exact_integer_ties_many_chunks(form):
+    # exact ties across chunks and at the KL-th score of long rows: integer
+    # scores over 520 subkeys (three 256-key chunks) with runs of duplicated
+    # subkey rows, k = 32; every row logs far more than its KL entries, so
+    # compactions cut through tied scores
+    rng = np.random.default_rng(11)
+    B, H, d_q, n, d_v, k = 300, 1, 64, 520, 32, 32
+    qf = rng.integers(-2, 3, (B, H, d_q)).astype(np.float32)
+    Cf = rng.integers(-1, 2, (H, 2, n, d_q // 2)).astype(np.float32)
+    Cf[:, 0, 300:400] = Cf[:, 0, 0:100]
+    Cf[:, 1, 256:512] = Cf[:, 1, 0:256]
+    Vf = rng.standard_normal((n * n, d_v)).astype(np.float32)
+    q, C, V = synth.f32_to_bf16(qf), synth.f32_to_bf16(Cf), synth.f32_to_bf16(Vf)
+    c = dict(B=B, H=H, d_q=d_q, n_keys=n, d_v=d_v, k=k, dtype="bf16")
+    for z in (None, -1e30):
+        _, idx, w = run_forward(c, q.ravel(), C.ravel(), V.ravel(), form=form, hint_z=z)
+        ref = oracle.lookup(q.ravel(), C.ravel(), B, H, d_q, n, k)
+        assert np.array_equal(idx, ref["idx"]), z
+        assert (np.abs(w - ref["w"]) <= 1e-6 * (1 + ref["w"])).all(), z
 
 
 def test_gather_alone_fed_oracle_selection():
