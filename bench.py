@@ -9,9 +9,9 @@ k = 32, bf16 inputs, all resident in HBM.  Prints one JSON line.
                   [--workload page|mid|skew|large|tiny]
 
 --impl reference times the fp64 CPU oracle on the host cores instead, on a
-bounded sample of the same workload.  Under torchrun (N > 1) each rank runs
-its own batch on its own GPU (weak scaling; no collective on the data path),
-the time is the max over ranks.
+bounded sample of the same workload.  This build runs on one GPU: under
+torchrun (N > 1) rank 0 prints an "unavailable" line for this arm and no GPU
+work is done; the reference arm runs on rank 0 alone.
 """
 import argparse
 import json
@@ -257,6 +257,15 @@ def config_json(c, name):
 
 
 def run_ours(args, rank, world, local):
+    if world > 1:
+        # every call of this library runs on one GPU; queries would shard
+        # across GPUs as independent replicas, which this build does not run
+        # (its tile loads shared by CTA pairs stay on one GPU's memory)
+        if rank == 0:
+            print(json.dumps({"impl": "ours", "metric": METRIC, "unit": UNIT, "n_gpus": world,
+                              "unavailable": "one-GPU build: no multi-GPU path (replicas only, "
+                                            "not run)"}), flush=True)
+        return
     import torch
     import sparse_top_lookup_gb300 as pk
 
@@ -666,9 +675,8 @@ def main():
     ap.add_argument("--n-keys", type=int, default=None,
                     help="override the workload's n_keys (small profiling captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--select-form", type=int, default=None, choices=[0, 1, 2],
-                    help="selection kernel form of the bf16 lookup (0 automatic, 1 one-SM, "
-                         "2 two-SM)")
+    ap.add_argument("--select-form", type=int, default=None, choices=[0, 1, 2, 3],
+                    help="selection kernel form of the bf16 lookup (PKM_OPT_SELECT_FORM)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -130,8 +130,9 @@ enum {
   /* bf16 lookups with k <= 32: the form of the selection kernel's main pass.
      0 (default): automatic; 1: one-SM forms (tcgen05 MMAs of 128 query rows
      per SM); 2: the two-SM form (MMAs of 256 query rows spanning the two
-     CTAs of a cluster, each loading half of every subkey slab).  Results are
-     the same in every form. */
+     CTAs of a cluster, each loading half of every subkey slab) with two
+     epilogue warp sets on alternate work units; 3: the two-SM form with one
+     epilogue warp set.  Results are the same in every form. */
   PKM_OPT_SELECT_FORM = 5
 };
 #define PKM_HOST_MAX_CHUNKS 16
@@ -241,6 +242,16 @@ const char *pkm_strerror(int code);
 int pkm_abi_version(void);
 
 /*
+ * 1 if every one of the `count` pointers is device memory of the current
+ * device, else 0 (also on any CUDA error, or with no device).  The lookup's
+ * one-SM selection form and the query network load tiles once for two CTAs
+ * of a cluster (TMA multicast) only when their operands pass this test;
+ * other operands (host, managed or another GPU's memory) take the one-CTA
+ * forms.  Host-side only; nothing is launched.
+ */
+int pkm_multicast_ok(const void *const *ptrs, int count);
+
+/*
  * No counterpart on the pages: a library-level addition for callers that
  * cannot allocate device memory when they run a lookup (a serving process
  * whose GPU memory is budgeted at start-up, a host framework that owns every
@@ -249,7 +260,8 @@ int pkm_abi_version(void);
  * entry point takes no handle.
  *
  * pkm_lookup_static: the lookup alone (scoring through softmax) for bf16
- * queries and subkeys, as pkm_lookup on a bf16 handle with d_q given here:
+ * queries and subkeys and k <= 32 (the tensor-core path; a larger k returns
+ * PKM_ERR_UNSUPPORTED), as pkm_lookup on a bf16 handle with d_q given here:
  * idx and w [B, H, k] are written on `stream`.  It allocates nothing: its
  * scratch (a status word, the retry pass's counts, unit flags and unit list,
  * and the per-half candidate lists, for at most PKM_STATIC_MAX_PAIRS pairs)
@@ -260,8 +272,9 @@ int pkm_abi_version(void);
  *   - status: if not NULL, a device int that receives the call's device
  *     status (PKM_OK or PKM_ERR_TIMEOUT) on `stream`.
  *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress) and caches it; make that first call before any
- *     stream capture.
+ *     (cudaGetSymbolAddress) and caches it with the device's current
+ *     context; make that first call before any stream capture.  A call in a
+ *     new context of the device (after cudaDeviceReset) looks it up again.
  *   - All calls share the one array, and each call clears what must start at
  *     zero.  Calls whose work overlaps on the GPU (other streams, other host
  *     threads) race on it: serialise them.

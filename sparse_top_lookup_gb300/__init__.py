@@ -28,7 +28,7 @@ EXPORTED = ["pkm_create", "pkm_destroy", "pkm_forward", "pkm_lookup", "pkm_gathe
             "pkm_abi_version", "pkm_set_option", "pkm_get_fallback_count", "pkm_lookup_static",
             "pkm_quantize_values_fp8", "pkm_bn_fold", "pkm_query_net", "pkm_backward", "pkm_backward_read",
             "pkm_backward_scores", "pkm_forward_host_async", "pkm_backward_sparse",
-            "pkm_backward_read_sparse"]
+            "pkm_backward_read_sparse", "pkm_multicast_ok"]
 PKM_STATIC_MAX_PAIRS = 1 << 16
 
 

@@ -62,13 +62,17 @@ constexpr int LOG_CAP = 64;                 // log slots per row
 constexpr int LOG_STEP = BM * 8;            // bytes from one slot of a row to the next
 constexpr int LOG_BYTES = LOG_CAP * LOG_STEP;
 
-// Shape by the number of epilogue warp sets.  One set: both TMEM buffers are
-// its (the MMA fills one while the set reads the other), 5 tile stages.  Two
-// sets: each set owns one buffer and takes every other unit, so two sets'
-// selection work overlaps; 3 tile stages leave room for the second log.
-template <int kSets>
+// Epilogue forms.  kEpiOneSet: four warps read both TMEM buffers in turn
+// (the MMA fills one while they read the other), 5 tile stages.
+// kEpiTwoSets: two sets of four warps own one buffer each and take every
+// other unit, so two units' selection work overlaps; 3 tile stages leave
+// room for the second log.
+constexpr int kEpiOneSet = 1, kEpiTwoSets = 2;
+
+template <int kEpi>
 struct Shape2 {
-  static constexpr int kStages = kSets == 1 ? 5 : 3;
+  static constexpr int kStages = kEpi == kEpiTwoSets ? 3 : 5;
+  static constexpr int kSets = kEpi == kEpiTwoSets ? 2 : 1;  // epilogue warp sets
   static constexpr int kThreads = 64 + kSets * 128;
   static constexpr int kTiles = kStages * STAGE_BYTES;
   static constexpr int kSmem = kTiles + kSets * LOG_BYTES + 1024;  // + alignment slack
@@ -95,7 +99,7 @@ struct Shape2 {
 // equal scores too, so the cut is exact.
 
 struct RowLog {
-  uint2* e;  // [LOG_CAP][BM]
+  uint2* e;  // [capacity][BM]
   int row;
   __device__ __forceinline__ uint2& at(int s) const { return e[s * BM + row]; }
 };
@@ -135,12 +139,12 @@ __device__ __forceinline__ void append8(uint32_t lrow, uint32_t& oA, uint32_t& o
 // sorted and merged in.  Raises the threshold to the KL-th value and counts
 // the values held (nv, at most KL).  Warp-uniform loop; lanes without
 // entries fold -inf.
-template <int KL>
+template <int KL, int CAP = LOG_CAP>
 __device__ __forceinline__ void fold_log(const RowLog& L, uint32_t& oA, uint32_t& oB,
                                          float (&V)[KL], uint32_t (&C)[KL], float& thr, int& nv) {
   const int nA = (int)(oA / LOG_STEP);
   const int tB = (int)(oB / LOG_STEP) + 1;
-  const int cnt = nA + (LOG_CAP - tB);
+  const int cnt = nA + (CAP - tB);
 #pragma unroll 1
   for (int b0 = 0; __any_sync(0xffffffffu, cnt > b0); b0 += 16) {
     float Bv[16];
@@ -160,7 +164,7 @@ __device__ __forceinline__ void fold_log(const RowLog& L, uint32_t& oA, uint32_t
   nv = min(KL, nv + cnt);
   if (V[KL - 1] > -INFINITY) thr = fmaxf(thr, V[KL - 1]);
   oA = 0;
-  oB = (uint32_t)(LOG_CAP - 1) * LOG_STEP;
+  oB = (uint32_t)(CAP - 1) * LOG_STEP;
 }
 
 // 16 TMEM columns of this thread's lane into registers; the empty asm after
@@ -187,14 +191,14 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 // Cluster c (CTAs 2c, 2c+1; rank 0 leads) takes pair units c + i * clusters.
 // Pair unit u: half u & 1, pair tile (u >> 1) / H, head (u >> 1) % H; CTA
 // rank r holds query rows 256 * tile + 128 * r + [0, 128).
-template <int KL, int kSets>
-__global__ void __launch_bounds__(Shape2<kSets>::kThreads, 1)
+template <int KL, int kEpi>
+__global__ void __launch_bounds__(Shape2<kEpi>::kThreads, 1)
 select_2sm_kernel(const __grid_constant__ CUtensorMap tmap_q,
                   const __grid_constant__ CUtensorMap tmap_c, int B, int H, int n, int nch,
                   int kb_count, float hint_z, float* __restrict__ list_v,
                   unsigned short* __restrict__ list_c, int* __restrict__ status, int stall) {
-  constexpr int STAGES = Shape2<kSets>::kStages, SETS = kSets;
-  constexpr int SMEM_TILES = Shape2<kSets>::kTiles;
+  constexpr int STAGES = Shape2<kEpi>::kStages, SETS = Shape2<kEpi>::kSets;
+  constexpr int SMEM_TILES = Shape2<kEpi>::kTiles;
   extern __shared__ unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t bars[2 * STAGES + 2 * TBUFS + 1];
   __shared__ uint32_t s_tmem_base;
@@ -219,7 +223,6 @@ select_2sm_kernel(const __grid_constant__ CUtensorMap tmap_q,
   auto bar_tfull = [&](uint32_t b) { return bar0 + 8u * (2 * STAGES + b); };
   auto bar_tempty = [&](uint32_t b) { return bar0 + 8u * (2 * STAGES + TBUFS + b); };
   const uint32_t bar_done = bar0 + 8u * (2 * STAGES + 2 * TBUFS);
-
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar_full(s), 1);   // leader: its producer's expect_tx (both CTAs' bytes)
@@ -359,7 +362,7 @@ select_2sm_kernel(const __grid_constant__ CUtensorMap tmap_q,
       for (int st = 0; st <= steps; ++st) {
         // before each group, room for 16 more entries (8 per end)
         if (__any_sync(0xffffffffu, st == steps || oB < oA + 15u * LOG_STEP))
-          fold_log<KL>(L, oA, oB, V, C, thr, nv);
+          fold_log<KL, LOG_CAP>(L, oA, oB, V, C, thr, nv);
         if (st == steps) break;
         const int ch = st / kGroups, g = (st - ch * kGroups) * 16;
         if (g == 0) {
@@ -450,12 +453,12 @@ select_2sm_kernel(const __grid_constant__ CUtensorMap tmap_q,
 
 // ------------------------------------------------------------------ host
 
-template <int KL, int kSets>
+template <int KL, int kEpi>
 cudaError_t launch_kl(const CUtensorMap& mq, const CUtensorMap& mc, int B, int H, int n, int nch,
                       int kbc, float hint_z, float* list_v, unsigned short* list_c, int* status,
                       int stall, cudaStream_t stream) {
-  auto kernel = select_2sm_kernel<KL, kSets>;
-  constexpr int SMEM_BYTES = Shape2<kSets>::kSmem;
+  auto kernel = select_2sm_kernel<KL, kEpi>;
+  constexpr int SMEM_BYTES = Shape2<kEpi>::kSmem;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e =
@@ -469,7 +472,7 @@ cudaError_t launch_kl(const CUtensorMap& mq, const CUtensorMap& mc, int B, int H
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(Shape2<kSets>::kThreads);
+  cfg.blockDim = dim3(Shape2<kEpi>::kThreads);
   cfg.dynamicSmemBytes = SMEM_BYTES;
   cfg.stream = stream;
   cfg.attrs = attr;
@@ -492,16 +495,16 @@ cudaError_t launch_kl(const CUtensorMap& mq, const CUtensorMap& mc, int B, int H
 cudaError_t launch_select_2sm(const CUtensorMap& tmap_q, const CUtensorMap& tmap_c_half, int B,
                               int H, int d_q, int n_keys, int k, float hint_z, float* list_v,
                               unsigned short* list_c, int* status, bool stall,
-                              cudaStream_t stream, int sets) {
+                              cudaStream_t stream, int epi) {
   if (B == 0) return cudaSuccess;
   const int nch = (n_keys + NP - 1) / NP;
   const int kbc = (d_q / 2 + BK - 1) / BK;
   const int st = stall ? 1 : 0;
-#define PKM_SEL2(KLv, SETSv)                                                                  \
-  launch_kl<KLv, SETSv>(tmap_q, tmap_c_half, B, H, n_keys, nch, kbc, hint_z, list_v, list_c, \
-                        status, st, stream)
-  if (sets == 1) return k <= 16 ? PKM_SEL2(16, 1) : PKM_SEL2(32, 1);
-  return k <= 16 ? PKM_SEL2(16, 2) : PKM_SEL2(32, 2);
+#define PKM_SEL2(KLv, EPIv)                                                                   \
+  launch_kl<KLv, EPIv>(tmap_q, tmap_c_half, B, H, n_keys, nch, kbc, hint_z, list_v, list_c, \
+                       status, st, stream)
+  if (epi == kEpiOneSet) return k <= 16 ? PKM_SEL2(16, kEpiOneSet) : PKM_SEL2(32, kEpiOneSet);
+  return k <= 16 ? PKM_SEL2(16, kEpiTwoSets) : PKM_SEL2(32, kEpiTwoSets);
 #undef PKM_SEL2
 }
 

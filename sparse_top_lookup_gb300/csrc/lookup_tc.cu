@@ -658,18 +658,23 @@ cudaError_t launch_lookup_tc(const uint16_t* q, const uint16_t* subkeys, int B, 
   // 1.77 ms with pairs, where the selection work dominates; the large
   // workload (16 k-slabs, pipeline-latency-bound with three stages) 1.25 ->
   // 1.35 ms, since each stage of a pair waits for the slower of its two CTAs
-  const bool pair = (B + BM - 1) / BM >= 2 && kbc <= 8;
+  const bool pair_shape = (B + BM - 1) / BM >= 2 && kbc <= 8;
   // wide half-queries (more than 8 k-slabs per chunk) are bound by the tile
   // pipeline, not by the selection: their main pass runs one epilogue set per
   // CTA with 5 tile stages in flight
   const bool deep = kbc > 8;
   // the two-SM form (MMAs of 256 query rows over a CTA pair, each CTA
   // receiving half of every subkey slab) for the main pass
-  const bool two_sm = form == 2 || (form == 0 && B >= 2 * BM);
+  const bool two_sm = form >= 2 || (form == 0 && B >= 2 * BM);
+  // the one-SM pair form multicasts subkey slabs: only with this device's
+  // own memory
+  const void* const operands[2] = {q, subkeys};
+  const bool pair = !two_sm && pair_shape && tc::buffers_on_this_device(operands, 2);
+  const int epi = form == 3 ? 1 : 2;  // the two-SM kernel's epilogue form
   auto select = [&](float z, const int* list, const int* count, int st) {
     if (two_sm && !list)
       return launch_select_2sm(mq, m2, B, H, d_q, n_keys, k, z, list_v, list_c, status, st != 0,
-                               stream);
+                               stream, epi);
 #define PKM_SELECT(KLv, PAIRv, SETSv)                                                          \
   launch_kl<KLv, PAIRv, SETSv>(mq, mc, mch, B, H, n_keys, NC, nch, kbc, z, list_v, list_c, \
                                status, list, count, st, stream)

@@ -6,6 +6,7 @@
 #include <stdlib.h>
 
 #include "pkm_internal.cuh"
+#include "tc_common.cuh"
 
 // pkm_forward_host staging slots: a call's copies in can start while the two
 // calls before it still compute or copy out
@@ -502,7 +503,7 @@ int pkm_set_option(pkm_t h, int option, double value) {
       h->test_stall = (int)value;
       return PKM_OK;
     case PKM_OPT_SELECT_FORM:
-      if (!(value >= 0 && value <= 2) || value != (int)value) return PKM_ERR_OPTION;
+      if (!(value >= 0 && value <= 3) || value != (int)value) return PKM_ERR_OPTION;
       h->select_form = (int)value;
       return PKM_OK;
     case PKM_OPT_READ_SMS:
@@ -512,6 +513,11 @@ int pkm_set_option(pkm_t h, int option, double value) {
     default:
       return PKM_ERR_OPTION;
   }
+}
+
+int pkm_multicast_ok(const void* const* ptrs, int count) {
+  if (!ptrs || count < 0) return 0;
+  return pkm::tc::buffers_on_this_device(ptrs, count) ? 1 : 0;
 }
 
 int pkm_get_fallback_count(pkm_t h, void* stream, int* count) {

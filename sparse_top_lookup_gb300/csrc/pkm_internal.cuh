@@ -109,11 +109,12 @@ cudaError_t launch_lookup_tc(const uint16_t* q, const uint16_t* subkeys, int B, 
 // lookup: per-half lists of every (query, head) in list_v / list_c.
 // tmap_q: q viewed as [B][H][2][d_q/2] in 128x64 boxes; tmap_c_half: the
 // subkeys viewed as [2H][n_keys][d_q/2] in 128x64 boxes; both 128-byte
-// swizzled.  sets: epilogue warp sets per CTA (1 or 2).
+// swizzled.  epi: the epilogue form (1: one set of epilogue warps, 2: two
+// sets on alternate work units).
 cudaError_t launch_select_2sm(const CUtensorMap& tmap_q, const CUtensorMap& tmap_c_half, int B,
                               int H, int d_q, int n_keys, int k, float hint_z, float* list_v,
                               unsigned short* list_c, int* status, bool stall,
-                              cudaStream_t stream, int sets = 2);
+                              cudaStream_t stream, int epi = 2);
 
 // Entries of one per-half list for a given k.
 int list_slots(int k);

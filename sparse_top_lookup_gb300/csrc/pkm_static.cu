@@ -11,6 +11,7 @@
 // from the selection kernel to the merge kernel) is one fixed-size array in
 // the library's device memory, present on every GPU that loads the library
 // until the process exits.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -34,20 +35,46 @@ static __device__ __align__(256) unsigned char g_static_scratch[kStaticBytes];
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
 unsigned char* g_scratch_addr[kMaxDevices] = {};  // device address of g_static_scratch, per device
+CUcontext g_scratch_ctx[kMaxDevices] = {};        // the context the address was found in
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+// The device's current context (cuCtxGetCurrent through the runtime's
+// driver entry point), or NULL when it cannot be found.
+CUcontext current_context() {
+  static CtxGetCurrentFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  }
+  CUcontext c = nullptr;
+  if (fn && fn(&c) != CUDA_SUCCESS) c = nullptr;
+  return c;
+}
 
 // Device address of the scratch array on the current device.  The first call
-// on a device looks it up (cudaGetSymbolAddress); later calls reuse it.
+// on a device looks it up (cudaGetSymbolAddress); later calls in the same
+// context reuse it, and a new context of the device (after a device reset,
+// which reloads the library's module) looks it up again.
 int scratch_on_current_device(unsigned char** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PKM_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_setup_mutex);
-  if (!g_scratch_addr[dev]) {
+  // (a thread with no current context yet reads NULL here; the symbol
+  // lookup makes the device's primary context current, and it is read again)
+  const CUcontext ctx = current_context();
+  if (!g_scratch_addr[dev] || !ctx || ctx != g_scratch_ctx[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) {
       cudaGetLastError();
       return PKM_ERR_CUDA;
     }
     g_scratch_addr[dev] = static_cast<unsigned char*>(p);
+    g_scratch_ctx[dev] = current_context();
   }
   *out = g_scratch_addr[dev];
   return PKM_OK;

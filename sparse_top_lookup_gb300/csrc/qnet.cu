@@ -291,8 +291,10 @@ cudaError_t launch_qnet(const uint16_t* x, const uint16_t* w, int B, int dim, in
   }
   const int tm_count = (B + QM - 1) / QM, tn_count = (F + QN - 1) / QN;
   auto q16 = reinterpret_cast<__nv_bfloat16*>(q);
-  // pairs of row tiles share each W slab when there are at least two
-  if (tm_count >= 2) {
+  // pairs of row tiles share each W slab when there are at least two (and
+  // x and W are this device's memory: the slabs are multicast)
+  const void* const operands[2] = {x, w};
+  if (tm_count >= 2 && buffers_on_this_device(operands, 2)) {
     static bool attr_set = false;
     if (!attr_set) {
       cudaError_t e = cudaFuncSetAttribute(qnet_kernel<true>,

@@ -360,6 +360,27 @@ inline EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// True when every one of the `count` pointers is device memory of the
+// current device.  The cluster-multicast forms (a TMA load that lands in
+// both CTAs of a pair) read only such buffers; anything else (host, managed
+// or another GPU's memory) takes the one-CTA forms.
+inline bool buffers_on_this_device(const void* const* ptrs, int count) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  for (int i = 0; i < count; ++i) {
+    cudaPointerAttributes a;
+    if (!ptrs[i] || cudaPointerGetAttributes(&a, ptrs[i]) != cudaSuccess) {
+      cudaGetLastError();
+      return false;
+    }
+    if (a.type != cudaMemoryTypeDevice || a.device != dev) return false;
+  }
+  return true;
+}
+
 inline int sm_count() {
   int dev = 0, n = 0;
   cudaGetDevice(&dev);

@@ -150,3 +150,18 @@ def test_product_path_refuses_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(pk, "_lib", None)
     with pytest.raises(ImportError):
         pk.lib()
+
+
+def test_multicast_check_refuses_host_memory():
+    # the cluster-multicast tile loads read only this device's memory: host
+    # buffers (and, on a machine without a GPU, anything) are refused
+    pk = pytest.importorskip("sparse_top_lookup_gb300")
+    import ctypes
+    import numpy as np
+    L = pk.lib()
+    a, b = np.zeros(64, np.uint16), np.zeros(64, np.uint16)
+    ptrs = (ctypes.c_void_p * 2)(a.ctypes.data, b.ctypes.data)
+    assert L.pkm_multicast_ok(ptrs, 2) == 0
+    assert L.pkm_multicast_ok(None, 1) == 0
+    empty = (ctypes.c_void_p * 1)(None)
+    assert L.pkm_multicast_ok(empty, 1) == 0

@@ -1,6 +1,7 @@
-"""bench.py's multi-rank plumbing on CPU: two gloo ranks, each with its own
-batch (weak scaling), the step time reduced by max over ranks, and the
-reference arm printed by rank 0 only."""
+"""bench.py's multi-rank plumbing on CPU: two gloo ranks reduce a step time
+by max over ranks, the reference arm prints on rank 0 only, and this
+one-GPU build's own arm prints its "unavailable" line on rank 0 only and
+launches nothing."""
 import os
 import socket
 import sys
@@ -61,3 +62,18 @@ def test_reference_arm_runs_on_rank_zero_only(capsys):
     bench.run_reference(A, rank=0, world=1)
     line = capsys.readouterr().out.strip()
     assert '"impl": "reference"' in line and '"kind": "oracle"' in line
+
+
+def test_own_arm_with_several_ranks_prints_unavailable_on_rank_zero_only(capsys):
+    sys.path.insert(0, ROOT)
+    import json
+    import bench
+
+    class A:
+        workload, batch, n_keys = "tiny", None, None
+
+    bench.run_ours(A, rank=1, world=2, local=1)
+    assert capsys.readouterr().out == ""
+    bench.run_ours(A, rank=0, world=2, local=0)
+    line = json.loads(capsys.readouterr().out.strip())
+    assert line["impl"] == "ours" and line["n_gpus"] == 2 and "unavailable" in line

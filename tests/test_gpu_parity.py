@@ -118,26 +118,28 @@ def test_bf16_shapes(shape):
     (129, 1, 128, 2048, 64, 32),    # 8 chunks per half (the large workload's n_keys)
     (260, 2, 2048, 512, 128, 32),   # 16 k-slabs per chunk (the large workload's width)
 ])
-def test_two_sm_form_shapes(shape):
+@pytest.mark.parametrize("form", [2, 3])
+def test_two_sm_form_shapes(shape, form):
     c, q, C, V = random_case(sum(shape) + 5, *shape)
-    check_against_oracle(c, q, C, V, form=2)
+    check_against_oracle(c, q, C, V, form=form)
 
 
+@pytest.mark.parametrize("form", [2, 3])
 @pytest.mark.parametrize("z", [1e30, 1.53, -1e30])
-def test_two_sm_form_exact_for_any_threshold_hint(z):
+def test_two_sm_form_exact_for_any_threshold_hint(z, form):
     # every row retried (huge z: the lists are marked and the retry pass
     # selects their 128-row units with the one-SM kernel), about half of them,
     # or none with every score logged (repeated compactions from both log ends)
     c, q, C, V = random_case(99, 520, 2, 256, 1024, 128, 32)
     info = {}
-    check_against_oracle(c, q, C, V, hint_z=z, report=info, form=2)
+    check_against_oracle(c, q, C, V, hint_z=z, report=info, form=form)
     if z == 1e30:
         assert info["fallback"] == c["B"] * c["H"]
     if z < 0:
         assert info["fallback"] == 0
 
 
-@pytest.mark.parametrize("form", [1, 2])
+@pytest.mark.parametrize("form", [1, 2, 3])
 def test_forms_agree_bit_for_bit(form):
     # the mid workload through each selection form gives the same indices,
     # weights and outputs as the automatic choice
@@ -234,7 +236,7 @@ def test_exact_integer_ties_bit_exact(dtype, form):
     assert (np.abs(w - ref["w"]) <= 1e-6 * (1 + ref["w"])).all()
 
 
-@pytest.mark.parametrize("form", [1, 2])
+@pytest.mark.parametrize("form", [1, 2, 3])
 def test_exact_integer_ties_many_chunks(form):
     # exact ties across chunks and at the KL-th score of long rows: integer
     # scores over 520 subkeys (three 256-key chunks) with runs of duplicated
@@ -382,3 +384,16 @@ def test_forward_with_scratch_selection_matches():
         assert np.array_equal(out.cpu().numpy(), out_a)
     finally:
         pk.pkm_destroy(h)
+
+
+def test_multicast_check_on_device_and_host_buffers():
+    # device memory of this GPU passes; pinned host memory does not (the
+    # one-SM pair form and the query network then take their one-CTA forms)
+    import ctypes
+    L = pk.lib()
+    x = torch.zeros(64, device="cuda")
+    y = torch.zeros(64).pin_memory()
+    both = (ctypes.c_void_p * 2)(x.data_ptr(), x.data_ptr())
+    mixed = (ctypes.c_void_p * 2)(x.data_ptr(), y.data_ptr())
+    assert L.pkm_multicast_ok(both, 2) == 1
+    assert L.pkm_multicast_ok(mixed, 2) == 0

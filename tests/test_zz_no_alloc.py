@@ -28,10 +28,28 @@ def test_static_lookup_rejects_too_many_pairs_on_the_host():
         == pk.PKM_ERR_UNSUPPORTED
 
 
+def _static_call(pk, L, q, C, B, H, d_q, n, k):
+    """One pkm_lookup_static call through the C ABI; returns idx, w, status."""
+    import torch
+    idx = torch.full((B, H, k), -7, dtype=torch.int64, device="cuda")
+    w = torch.full((B, H, k), -7.0, device="cuda")
+    status = torch.full((1,), 12345, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    rc = L.pkm_lookup_static(ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(C.data_ptr()),
+                             B, H, d_q, n, k, ctypes.c_void_p(idx.data_ptr()),
+                             ctypes.c_void_p(w.data_ptr()), ctypes.c_void_p(status.data_ptr()),
+                             ctypes.c_void_p(stream))
+    assert rc == pk.PKM_OK, pk.pkm_strerror(rc)
+    torch.cuda.synchronize()
+    return idx, w, status.item()
+
+
 @pytest.mark.gpu
-def test_static_lookup_matches_handle_lookup_on_two_calls_in_a_row():
+def test_static_lookup_matches_oracle_and_handle_lookup_on_two_calls_in_a_row():
     torch = pytest.importorskip("torch")
     pk = pytest.importorskip("sparse_top_lookup_gb300")
+    import oracle
+    from helpers import compare_lookup
     L = pk.lib()
 
     def dev(a):
@@ -42,8 +60,9 @@ def test_static_lookup_matches_handle_lookup_on_two_calls_in_a_row():
         (130, 3, 128, 256, 16),
     ]
     for seed, (B, H, d_q, n, k) in enumerate(cases, start=41):
-        q = dev(synth.normal(seed, 1, B * H * d_q, 1.0, dtype="bf16"))
-        C = dev(synth.normal(seed, 2, H * 2 * n * (d_q // 2), 2.0 / d_q, dtype="bf16"))
+        q_np = synth.normal(seed, 1, B * H * d_q, 1.0, dtype="bf16")
+        C_np = synth.normal(seed, 2, H * 2 * n * (d_q // 2), 2.0 / d_q, dtype="bf16")
+        q, C = dev(q_np), dev(C_np)
 
         # the existing entry point, through a handle
         h = pk.pkm_create(pk.make_config(d_q, 64, B, H, n, k, q_dtype=pk.PKM_BF16))
@@ -56,20 +75,61 @@ def test_static_lookup_matches_handle_lookup_on_two_calls_in_a_row():
             pk.pkm_destroy(h)
 
         # the allocation-free entry point, called through the C ABI directly
-        idx = torch.full((B, H, k), -7, dtype=torch.int64, device="cuda")
-        w = torch.full((B, H, k), -7.0, device="cuda")
-        status = torch.full((1,), 12345, dtype=torch.int32, device="cuda")
-        stream = torch.cuda.current_stream().cuda_stream
-        rc = L.pkm_lookup_static(ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(C.data_ptr()),
-                                 B, H, d_q, n, k, ctypes.c_void_p(idx.data_ptr()),
-                                 ctypes.c_void_p(w.data_ptr()), ctypes.c_void_p(status.data_ptr()),
-                                 ctypes.c_void_p(stream))
-        assert rc == pk.PKM_OK, pk.pkm_strerror(rc)
-        torch.cuda.synchronize()
-        assert status.item() == pk.PKM_OK
+        idx, w, st = _static_call(pk, L, q, C, B, H, d_q, n, k)
+        assert st == pk.PKM_OK
         assert torch.equal(idx, idx_ref)
         ref = w_ref.double()
         assert ((w.double() - ref).abs() <= 2e-3 * (1 + ref.abs())).all()
+        # and against the fp64 oracle, as every other parity test
+        want = oracle.lookup(q_np, C_np, B, H, d_q, n, k)
+        rep = compare_lookup(idx.cpu().numpy(), w.cpu().numpy(), want, q_np, C_np, "bf16", H,
+                             d_q, n)
+        assert rep["failures"] == 0 and rep["w_ok"], rep
+
+
+@pytest.mark.gpu
+def test_static_lookup_retry_pass_and_no_allocation():
+    # Subkeys that are all equal but for a few make every row's scores a few
+    # distinct values above one value shared by all the others: the
+    # threshold hint (mean + z * spread) lands above the shared value, every
+    # list comes out short, and the retry pass (its counts, unit flags and
+    # unit list live in the static array) selects the rows again without the
+    # hint, breaking the exact ties by flat index.  Repeated calls leave the
+    # device's free memory unchanged.
+    torch = pytest.importorskip("torch")
+    pk = pytest.importorskip("sparse_top_lookup_gb300")
+    import oracle
+    L = pk.lib()
+    B, H, d_q, n, k = 260, 2, 64, 256, 32
+    rng = np.random.default_rng(5)
+    qf = rng.integers(-2, 3, (B, H, d_q)).astype(np.float32)
+    Cf = np.ones((H, 2, n, d_q // 2), np.float32)
+    Cf[:, :, :6] = rng.integers(-2, 3, (H, 2, 6, d_q // 2))
+    q_np, C_np = synth.f32_to_bf16(qf).ravel(), synth.f32_to_bf16(Cf).ravel()
+    q = torch.from_numpy(q_np.view(np.int16)).cuda().view(torch.bfloat16)
+    C = torch.from_numpy(C_np.view(np.int16)).cuda().view(torch.bfloat16)
+    want = oracle.lookup(q_np, C_np, B, H, d_q, n, k)
+    idx, w, st = _static_call(pk, L, q, C, B, H, d_q, n, k)  # warm-up (and first check)
+    assert st == pk.PKM_OK
+    assert np.array_equal(idx.cpu().numpy(), want["idx"])
+    free0 = torch.cuda.mem_get_info()[0]
+    for _ in range(3):
+        idx, w, st = _static_call(pk, L, q, C, B, H, d_q, n, k)
+        assert st == pk.PKM_OK
+        assert np.array_equal(idx.cpu().numpy(), want["idx"])
+        assert (np.abs(w.cpu().numpy() - want["w"]) <= 1e-6 * (1 + want["w"])).all()
+    assert torch.cuda.mem_get_info()[0] == free0
+    # the same input through a handle shows that the lists did go through
+    # the retry pass
+    h = pk.pkm_create(pk.make_config(d_q, 64, B, H, n, k, q_dtype=pk.PKM_BF16))
+    try:
+        i2 = torch.empty(B, H, k, dtype=torch.int64, device="cuda")
+        w2 = torch.empty(B, H, k, device="cuda")
+        pk.check(pk.pkm_lookup(h, q, C, B, H, n, k, i2, w2), "pkm_lookup")
+        assert pk.pkm_get_fallback_count(h) > 0
+        assert torch.equal(i2, idx)
+    finally:
+        pk.pkm_destroy(h)
 
 
 @pytest.mark.gpu
