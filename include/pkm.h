@@ -51,7 +51,7 @@
  * Ownership: the caller owns every tensor pointer; nothing is retained after a
  * call returns.  A handle owns only its scratch (device workspace for idx/w
  * when the caller passes NULL, a device status word, optional staging for
- * pkm_forward_host, and for pkm_backward a cuBLAS handle and gradient
+ * pkm_forward_host, and for pkm_backward the gradient
  * scratch).  pkm_create is the only call that allocates.
  *
  * Asynchrony: every call enqueues work on `stream` (a cudaStream_t; NULL is
@@ -93,7 +93,7 @@ enum {
                                n_keys^2 >= 2^31, d_q or d_v layout */
   PKM_ERR_ALIGN = -4,       /* a tensor pointer not 16-byte aligned */
   PKM_ERR_CUDA = -5,        /* a CUDA runtime call or launch failed */
-  PKM_ERR_NOMEM = -6,       /* pkm_create could not allocate its scratch (or cuBLAS handle) */
+  PKM_ERR_NOMEM = -6,       /* pkm_create could not allocate its scratch */
   PKM_ERR_TIMEOUT = -7,     /* device: a bounded wait inside a kernel gave up */
   PKM_ERR_BAD_INDEX = -8,   /* device: a row index outside [0, n_keys^2) reached the value read */
   PKM_ERR_NO_STAGING = -9,  /* pkm_forward_host on a handle created without host staging */
@@ -146,11 +146,10 @@ typedef struct pkm_handle *pkm_t;
  * n_keys and k any call will pass (sizes the scratch).  host_staging:
  * nonzero to also allocate device staging for pkm_forward_host (three slots of
  * max_B queries and outputs).  with_backward: nonzero to also allocate what
- * pkm_backward needs (bf16 queries and subkeys, bf16 or fp32 values): a
- * cuBLAS handle with a 32 MiB workspace and scratch for the gradients
- * (about 4 * max_B * max_H * (max_k + max_n_keys) bytes, or 24 * max_B *
- * max_H * max_k + max_n_keys^2 / 32 if larger); max_B * max_H * max_k and
- * max_B * d_v / 4 must stay below 2^31.
+ * pkm_backward needs (bf16 queries and subkeys with d_q <= 2048, bf16 or
+ * fp32 values): scratch for the gradients (about 44 * max_B * max_H * max_k
+ * bytes, or 28 * max_B * max_H * max_k + max_n_keys^2 / 32 if larger);
+ * max_B * max_H * max_k and max_B * d_v / 4 must stay below 2^31.
  */
 typedef struct {
   int d_q, d_v;
@@ -294,9 +293,10 @@ int pkm_lookup_static(const void *q, const void *subkeys, int B, int H, int d_q,
  *   dsubkeys  [H, 2, n_keys, d_q/2]    added to (zero it first, or accumulate);
  *   dvalues   [n_keys^2, d_v]          added to (only the selected rows change).
  * With dw = dout . V[idx] and ds = w * (dw - sum(w * dw)): dvalues[idx] +=
- * w * dout; dq and dsubkeys take ds through each winner's two subkeys.  The
- * per-subkey score gradients are rounded to bf16 for the two tensor-core
- * products (cuBLAS) that form dq and dsubkeys; dvalues and dw are fp32.
+ * w * dout; dq and dsubkeys take ds through each winner's two subkeys (the
+ * winners sharing a subkey summed first), gathering only the winning
+ * subkeys' rows and the queries' rows; all of it fp32 (the order in which a
+ * subkey's contributions are added to dsubkeys varies from call to call).
  * Requires a handle created with with_backward (else PKM_ERR_NO_BACKWARD).
  * Enqueued on `stream`; an index outside [0, n_keys^2) sets
  * PKM_ERR_BAD_INDEX in the status word and contributes nothing.

@@ -64,7 +64,7 @@ def build(force=False, verbose=False, ptxas_info=False):
                 sys.stderr.write(err)
     tmp = LIB + ".tmp%d" % os.getpid()
     cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + [o for o, _ in results] + [
-        "-cudart", "shared", "-lcublas", "-Xlinker", "-rpath," + _cuda_lib_dir()]
+        "-cudart", "shared", "-Xlinker", "-rpath," + _cuda_lib_dir()]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s\n%s" % (r.stdout, r.stderr))

@@ -10,7 +10,8 @@
 //   score = s1[a1] + s2[a2], a1 = idx / n, a2 = idx % n, s_i = q_i . C[h,i,a]:
 //   dq_i[b,h]  = sum_a DS_i[b,h][a] * C[h,i,a,:]
 //   dC[h,i,a] += sum_b DS_i[b,h][a] * q_i[b,h]
-// where DS_i[b,h] is the [n_keys] row of ds summed per subkey of half i.
+// where DS_i[b,h][a] is ds summed over the winners whose half-i subkey is a
+// (nonzero for at most k subkeys).
 //
 // Read part (dw and dV), grouped by value row so that each selected row of V
 // and of dV crosses HBM once however many selections hit it (the gradient
@@ -35,13 +36,16 @@
 //                          every dw of the piece, and the dV segment is
 //                          written back once: a plain store when the row has
 //                          one piece in one item, vector atomic adds otherwise.
-// Score part:
-//   ds_rows_kernel         one warp per (query, head, half): softmax backward
-//                          and the dense bf16 DS row (duplicates summed in
-//                          shared memory);
-//   two strided-batched cuBLAS GEMMs over the 2H (head, half) blocks (plain
-//   library GEMMs, bf16 in, fp32 out): dq = DS C (overwrites) and dC += DS^T q.
-#include <cublas_v2.h>
+// Score part, through the winning subkeys only (fp32 throughout):
+//   ds_gather_kernel       one warp per (query, head): ds, DS per distinct
+//                          winning subkey (winners sharing one summed in lane
+//                          order), dq from those subkeys' rows (L2 gathers),
+//                          and one (subkey, query, DS) contribution per
+//                          distinct subkey, counted per (head, half, subkey);
+//   key_scan_kernel        the counts' offsets (one CTA);
+//   key_scatter_kernel     the contributions grouped by subkey;
+//   dsub_kernel            one warp per (head, half, subkey): its dsubkeys row
+//                          += the sum of DS * q_half rows of its contributions.
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -596,44 +600,244 @@ row_grad_kernel(const void* __restrict__ values, int d_v, const float* __restric
   cp_async_wait<0>();
 }
 
-// One warp per (query, head, half): ds_j = w_j (dw_j - sum_l w_l dw_l), then
-// DS[(2h + half)][b][a] = sum of ds_j over the winners whose half-`half`
-// subkey is a, as a dense bf16 row of n entries.  k <= 32 (one lane per
-// winner); dynamic smem: n floats per warp.  A winner whose index is outside
-// [0, n^2) adds nothing (gather_bwd_kernel records it).
-__global__ void ds_rows_kernel(const int64_t* __restrict__ idx, const float* __restrict__ w,
-                               const float* __restrict__ dw, int B, int H, int n, int k,
-                               __nv_bfloat16* __restrict__ ds_rows) {
-  extern __shared__ __align__(16) float s_row[];
-  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
-  const int64_t item = (int64_t)blockIdx.x * (blockDim.x >> 5) + wib;  // (pair, half)
-  if (item >= (int64_t)B * H * 2) return;  // whole warp
-  const int64_t pair = item >> 1;
-  const int half = (int)(item & 1);
+// ------------------------------------------------------------ score part
+//
+// Through the selected pairs only: a winner j of (b, h) has flat index
+// a_j * n + c_j and score q1 . C1[a_j] + q2 . C2[c_j], so its score gradient
+// ds_j = w_j (dw_j - sum_l w_l dw_l) reaches dq1 through C1[a_j], dq2
+// through C2[c_j], and C1[a_j] (C2[c_j]) through q1 (q2).  Winners sharing a
+// subkey are summed first (DS, fp32).
+constexpr uint32_t kNoKey = 0xffffffffu;
+constexpr int kMaxChunks = 4;  // 256-wide chunks of a half-query: d_q / 2 <= 1024
+
+// One warp per (query, head).  Lane j holds winner j.  dq (overwritten) from
+// the distinct winning subkeys' rows; each (subkey, query, DS) contribution
+// to dsubkeys goes to slot ((pair * 2 + half) * k + lane) (kNoKey where lane
+// j is not the first winner of its subkey) and is counted per key
+// (h * 2 + half) * n + subkey.
+__global__ void __launch_bounds__(256)
+ds_gather_kernel(const uint16_t* __restrict__ subkeys, const int64_t* __restrict__ idx,
+                 const float* __restrict__ w, const float* __restrict__ dw, int B, int H, int hd,
+                 int n, int k, float* __restrict__ dq, uint32_t* __restrict__ ekey,
+                 uint32_t* __restrict__ eb, float* __restrict__ eds, int* __restrict__ kcount) {
+  const int lane = threadIdx.x & 31;
+  const int64_t pair = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (pair >= (int64_t)B * H) return;  // whole warp
   const int64_t b = pair / H;
   const int h = (int)(pair - b * H);
-  float* row = s_row + wib * n;
-  for (int a = lane; a < n; a += 32) row[a] = 0.0f;
-  const float wj = lane < k ? w[pair * k + lane] : 0.0f;
-  const float dwj = lane < k ? dw[pair * k + lane] : 0.0f;
+  const int64_t N = (int64_t)n * n;
+  int64_t f = -1;
+  float wj = 0.0f, dwj = 0.0f;
+  if (lane < k) {
+    f = idx[pair * k + lane];
+    wj = w[pair * k + lane];
+    dwj = dw[pair * k + lane];
+  }
+  const bool valid = f >= 0 && f < N;  // an index outside the table contributes nothing
   float sw = wj * dwj;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) sw += __shfl_xor_sync(0xffffffffu, sw, o);
-  __syncwarp();
-  if (lane < k) {
-    const int64_t f = idx[pair * k + lane];
-    if (f >= 0 && f < (int64_t)n * n) {
-      const int a = (int)(half == 0 ? f / n : f % n);
-      atomicAdd(&row[a], wj * (dwj - sw));
+  const float ds = valid ? wj * (dwj - sw) : 0.0f;
+  const int d_q = 2 * hd;
+  const int nchunks = (hd + 255) / 256;
+#pragma unroll 1
+  for (int half = 0; half < 2; ++half) {
+    // the winner's subkey in this half (lanes without one get distinct -1 - lane)
+    const int a = valid ? (int)(half == 0 ? f / n : f % n) : -1 - lane;
+    const unsigned same = __match_any_sync(0xffffffffu, a);
+    const bool first = (same & ((1u << lane) - 1u)) == 0u;
+    // DS: the sum over winners sharing the subkey, in lane order
+    float sum = 0.0f;
+#pragma unroll
+    for (int l = 0; l < 32; ++l) {
+      const float v = __shfl_sync(0xffffffffu, ds, l);
+      sum += ((same >> l) & 1u) ? v : 0.0f;
+    }
+    const bool lead = first && valid;
+    // dq of this half: the distinct subkeys' rows, 8 dimensions per lane and
+    // 256-wide chunk
+    float acc[kMaxChunks][8];
+#pragma unroll
+    for (int c = 0; c < kMaxChunks; ++c)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[c][e] = 0.0f;
+    const uint16_t* ctab = subkeys + (size_t)(h * 2 + half) * n * hd;
+    // four subkey rows per step, their loads issued together
+    unsigned m = __ballot_sync(0xffffffffu, lead);
+#pragma unroll 1
+    while (m) {
+      int aL[4];
+      float sL[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int L = m ? __ffs(m) - 1 : 0;
+        aL[r] = __shfl_sync(0xffffffffu, a, L);
+        sL[r] = m ? __shfl_sync(0xffffffffu, sum, L) : 0.0f;
+        if (!m) aL[r] = 0;  // a zero weight on row 0: in bounds, no effect
+        m &= m - 1u;
+      }
+#pragma unroll
+      for (int c = 0; c < kMaxChunks; ++c) {
+        const int d0 = c * 256 + lane * 8;
+        if (c < nchunks && d0 < hd) {
+          uint4 u[4];
+#pragma unroll
+          for (int r = 0; r < 4; ++r) u[r] = *reinterpret_cast<const uint4*>(ctab + (size_t)aL[r] * hd + d0);
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const uint32_t uw[4] = {u[r].x, u[r].y, u[r].z, u[r].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              acc[c][2 * e] = fmaf(sL[r], __uint_as_float(uw[e] << 16), acc[c][2 * e]);
+              acc[c][2 * e + 1] =
+                  fmaf(sL[r], __uint_as_float(uw[e] & 0xffff0000u), acc[c][2 * e + 1]);
+            }
+          }
+        }
+      }
+    }
+    float* out = dq + pair * d_q + half * hd;
+#pragma unroll
+    for (int c = 0; c < kMaxChunks; ++c) {
+      const int d0 = c * 256 + lane * 8;
+      if (c < nchunks && d0 < hd) {
+        reinterpret_cast<float4*>(out + d0)[0] =
+            make_float4(acc[c][0], acc[c][1], acc[c][2], acc[c][3]);
+        reinterpret_cast<float4*>(out + d0)[1] =
+            make_float4(acc[c][4], acc[c][5], acc[c][6], acc[c][7]);
+      }
+    }
+    // the dsubkeys contributions
+    if (lane < k) {
+      const int64_t slot = (pair * 2 + half) * k + lane;
+      const uint32_t key = (uint32_t)((h * 2 + half) * n + (lead ? a : 0));
+      ekey[slot] = lead ? key : kNoKey;
+      eb[slot] = (uint32_t)b;
+      eds[slot] = sum;
+      if (lead) atomicAdd(&kcount[key], 1);
     }
   }
-  __syncwarp();
-  __nv_bfloat16* out = ds_rows + ((int64_t)(2 * h + half) * B + b) * n;
-  if ((n & 1) == 0) {  // rows start 4-byte aligned: pairs of entries
-    for (int a = 2 * lane; a < n; a += 64)
-      *reinterpret_cast<__nv_bfloat162*>(out + a) = __floats2bfloat162_rn(row[a], row[a + 1]);
-  } else {
-    for (int a = lane; a < n; a += 32) out[a] = __float2bfloat16_rn(row[a]);
+}
+
+// Exclusive scan of the per-key counts into koff [K + 1] and the scatter
+// cursors (one CTA).
+__global__ void __launch_bounds__(1024)
+key_scan_kernel(const int* __restrict__ kcount, int K, int* __restrict__ koff,
+                int* __restrict__ kcursor) {
+  __shared__ int warp_sums[32];
+  const int t = threadIdx.x;
+  const int per = (K + 1023) / 1024;
+  const int k0 = t * per, k1 = min(K, k0 + per);
+  int local = 0;
+  for (int i = k0; i < k1; ++i) local += kcount[i];
+  // block-wide exclusive scan of the threads' sums
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if ((t & 31) >= o) incl += v;
+  }
+  if ((t & 31) == 31) warp_sums[t >> 5] = incl;
+  __syncthreads();
+  if (t < 32) {
+    int v = warp_sums[t];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, v, o);
+      if (t >= o) v += u;
+    }
+    warp_sums[t] = v;
+  }
+  __syncthreads();
+  int run = incl - local + ((t >> 5) ? warp_sums[(t >> 5) - 1] : 0);
+  for (int i = k0; i < k1; ++i) {
+    koff[i] = run;
+    kcursor[i] = run;
+    run += kcount[i];
+  }
+  if (t == 1023) koff[K] = run;
+}
+
+// The contributions grouped by key (order within a key: arrival).
+__global__ void key_scatter_kernel(const uint32_t* __restrict__ ekey, const uint32_t* __restrict__ eb,
+                                   const float* __restrict__ eds, int64_t S,
+                                   int* __restrict__ kcursor, uint32_t* __restrict__ sb,
+                                   float* __restrict__ sds) {
+  for (int64_t s = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; s < S;
+       s += (int64_t)gridDim.x * blockDim.x) {
+    const uint32_t key = ekey[s];
+    if (key == kNoKey) continue;
+    const int pos = atomicAdd(&kcursor[key], 1);
+    sb[pos] = eb[s];
+    sds[pos] = eds[s];
+  }
+}
+
+// One warp per key (h, half, subkey): dsubkeys row += sum over its
+// contributions of DS * q_half[b] (fp32 fma, one warp owns the row).
+__global__ void __launch_bounds__(256)
+dsub_kernel(const uint16_t* __restrict__ q, const int* __restrict__ koff,
+            const uint32_t* __restrict__ sb, const float* __restrict__ sds, int H, int hd, int n,
+            float* __restrict__ dsubkeys) {
+  const int lane = threadIdx.x & 31;
+  const int key = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (key >= 2 * H * n) return;  // whole warp
+  const int e0 = koff[key], e1 = koff[key + 1];
+  if (e0 == e1) return;
+  const int hh = key / n;  // h * 2 + half
+  const int h = hh >> 1, half = hh & 1;
+  const int d_q = 2 * hd;
+  const int nchunks = (hd + 255) / 256;
+  float acc[kMaxChunks][8];
+#pragma unroll
+  for (int c = 0; c < kMaxChunks; ++c)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[c][e] = 0.0f;
+  // four contributions per step, their query rows' loads issued together
+  // (past the end: weight 0 on the first row, in bounds)
+#pragma unroll 1
+  for (int e = e0; e < e1; e += 4) {
+    uint32_t b[4];
+    float s[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const bool in = e + r < e1;
+      b[r] = sb[in ? e + r : e0];
+      s[r] = in ? sds[e + r] : 0.0f;
+    }
+#pragma unroll
+    for (int c = 0; c < kMaxChunks; ++c) {
+      const int d0 = c * 256 + lane * 8;
+      if (c < nchunks && d0 < hd) {
+        uint4 u[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+          u[r] = *reinterpret_cast<const uint4*>(q + ((size_t)b[r] * H + h) * d_q + half * hd + d0);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const uint32_t uw[4] = {u[r].x, u[r].y, u[r].z, u[r].w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            acc[c][2 * i] = fmaf(s[r], __uint_as_float(uw[i] << 16), acc[c][2 * i]);
+            acc[c][2 * i + 1] =
+                fmaf(s[r], __uint_as_float(uw[i] & 0xffff0000u), acc[c][2 * i + 1]);
+          }
+        }
+      }
+    }
+  }
+  float* out = dsubkeys + (size_t)key * hd;
+#pragma unroll
+  for (int c = 0; c < kMaxChunks; ++c) {
+    const int d0 = c * 256 + lane * 8;
+    if (c < nchunks && d0 < hd) {
+      float4* o = reinterpret_cast<float4*>(out + d0);
+      float4 x = o[0], y = o[1];
+      x.x += acc[c][0]; x.y += acc[c][1]; x.z += acc[c][2]; x.w += acc[c][3];
+      y.x += acc[c][4]; y.y += acc[c][5]; y.z += acc[c][6]; y.w += acc[c][7];
+      o[0] = x;
+      o[1] = y;
+    }
   }
 }
 
@@ -673,15 +877,33 @@ size_t backward_read_workspace_bytes(int B, int H, int n_keys, int k) {
   return off[kOffEnd];
 }
 
-size_t backward_scores_workspace_bytes(int B, int H, int n_keys) {
-  return (size_t)2 * H * B * n_keys * 2;
+// The score part's scratch: per key (h, half, subkey) its count, offset
+// (K + 1) and scatter cursor; per slot (query, head, half, winner) a key,
+// query and DS; then the contributions grouped by key (query, DS).
+static void scores_layout(int B, int H, int n_keys, int k, size_t* off) {
+  const size_t K = (size_t)2 * H * n_keys, S = (size_t)B * H * 2 * k;
+  off[0] = 0;                                 // kcount [K]
+  off[1] = off[0] + align256(K * 4);          // koff [K + 1]
+  off[2] = off[1] + align256((K + 1) * 4);    // kcursor [K]
+  off[3] = off[2] + align256(K * 4);          // ekey [S]
+  off[4] = off[3] + align256(S * 4);          // eb [S]
+  off[5] = off[4] + align256(S * 4);          // eds [S]
+  off[6] = off[5] + align256(S * 4);          // sb [S]
+  off[7] = off[6] + align256(S * 4);          // sds [S]
+  off[8] = off[7] + align256(S * 4);
+}
+
+size_t backward_scores_workspace_bytes(int B, int H, int n_keys, int k) {
+  size_t off[9];
+  scores_layout(B, H, n_keys, k, off);
+  return off[8];
 }
 
 size_t backward_dw_bytes(int B, int H, int k) { return align256((size_t)B * H * k * 4); }
 
 size_t backward_workspace_bytes(int B, int H, int n_keys, int k) {
   return backward_dw_bytes(B, H, k) + std::max(backward_read_workspace_bytes(B, H, n_keys, k),
-                                               backward_scores_workspace_bytes(B, H, n_keys));
+                                               backward_scores_workspace_bytes(B, H, n_keys, k));
 }
 
 cudaError_t launch_backward_read(const void* values, int value_dtype, int B, int H, int n_keys,
@@ -755,52 +977,37 @@ cudaError_t launch_backward_read(const void* values, int value_dtype, int B, int
   return cudaGetLastError();
 }
 
-cudaError_t launch_backward_scores(cublasHandle_t blas, const uint16_t* q,
-                                   const uint16_t* subkeys, int B, int H, int d_q, int n_keys,
-                                   int k, const int64_t* idx, const float* w, const float* dw,
-                                   float* dq, float* dsubkeys, void* workspace,
-                                   void* blas_workspace, size_t blas_workspace_bytes,
+cudaError_t launch_backward_scores(const uint16_t* q, const uint16_t* subkeys, int B, int H,
+                                   int d_q, int n_keys, int k, const int64_t* idx, const float* w,
+                                   const float* dw, float* dq, float* dsubkeys, void* workspace,
                                    cudaStream_t stream) {
   if (B == 0) return cudaSuccess;
-  if (k > 32) return cudaErrorInvalidValue;
-  __nv_bfloat16* ds = static_cast<__nv_bfloat16*>(workspace);
-  // warps per block: up to 8 while their rows fit the default 48 KB; one
-  // warp (up to 181 KB for the largest n) past that
-  const size_t row_bytes = (size_t)n_keys * 4;
-  const int wpb = (int)std::max<size_t>(1, std::min<size_t>(8, (48u << 10) / row_bytes));
-  const size_t sm = wpb * row_bytes;
-  cudaError_t e;
-  if (sm > (48u << 10)) {
-    e = cudaFuncSetAttribute(ds_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)sm);
-    if (e != cudaSuccess) return e;
-  }
-  const int64_t items = (int64_t)B * H * 2;
-  ds_rows_kernel<<<(unsigned)((items + wpb - 1) / wpb), wpb * 32, sm, stream>>>(
-      idx, w, dw, B, H, n_keys, k, ds);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  // setting the stream puts cuBLAS back on its own workspace pool: hand it
-  // the preallocated one again, so no call allocates
-  if (cublasSetStream(blas, stream) != CUBLAS_STATUS_SUCCESS ||
-      cublasSetWorkspace(blas, blas_workspace, blas_workspace_bytes) != CUBLAS_STATUS_SUCCESS)
-    return cudaErrorUnknown;
   const int hd = d_q / 2;
-  const float one = 1.0f, zero = 0.0f;
-  // dq (row-major [B][H*d_q], block (h, half) at column offset (2h + half) * hd):
-  // column-major dq^T (hd x B) = C_half^T (hd x n) * DS^T (n x B)
-  cublasStatus_t st = cublasGemmStridedBatchedEx(
-      blas, CUBLAS_OP_N, CUBLAS_OP_N, hd, B, n_keys, &one, subkeys, CUDA_R_16BF, hd,
-      (long long)n_keys * hd, ds, CUDA_R_16BF, n_keys, (long long)B * n_keys, &zero, dq,
-      CUDA_R_32F, H * d_q, hd, 2 * H, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
-  if (st != CUBLAS_STATUS_SUCCESS) return cudaErrorUnknown;
-  // dsubkeys (row-major [n][hd] per block) += DS^T q_half:
-  // column-major dC^T (hd x n) += q_half^T (hd x B) * DS (B x n)
-  st = cublasGemmStridedBatchedEx(
-      blas, CUBLAS_OP_N, CUBLAS_OP_T, hd, n_keys, B, &one, q, CUDA_R_16BF, H * d_q, hd, ds,
-      CUDA_R_16BF, n_keys, (long long)B * n_keys, &one, dsubkeys, CUDA_R_32F, hd,
-      (long long)n_keys * hd, 2 * H, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
-  return st == CUBLAS_STATUS_SUCCESS ? cudaSuccess : cudaErrorUnknown;
+  if (k > 32 || hd > 256 * kMaxChunks || hd % 8) return cudaErrorInvalidValue;
+  size_t off[9];
+  scores_layout(B, H, n_keys, k, off);
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  int* kcount = reinterpret_cast<int*>(ws + off[0]);
+  int* koff = reinterpret_cast<int*>(ws + off[1]);
+  int* kcursor = reinterpret_cast<int*>(ws + off[2]);
+  uint32_t* ekey = reinterpret_cast<uint32_t*>(ws + off[3]);
+  uint32_t* eb = reinterpret_cast<uint32_t*>(ws + off[4]);
+  float* eds = reinterpret_cast<float*>(ws + off[5]);
+  uint32_t* sb = reinterpret_cast<uint32_t*>(ws + off[6]);
+  float* sds = reinterpret_cast<float*>(ws + off[7]);
+  const int K = 2 * H * n_keys;
+  const int64_t S = (int64_t)B * H * 2 * k;
+  cudaError_t e = cudaMemsetAsync(kcount, 0, (size_t)K * 4, stream);
+  if (e != cudaSuccess) return e;
+  const int64_t pairs = (int64_t)B * H;
+  ds_gather_kernel<<<(unsigned)((pairs + 7) / 8), 256, 0, stream>>>(
+      subkeys, idx, w, dw, B, H, hd, n_keys, k, dq, ekey, eb, eds, kcount);
+  key_scan_kernel<<<1, 1024, 0, stream>>>(kcount, K, koff, kcursor);
+  const int sms = tc::sm_count();
+  key_scatter_kernel<<<sms * 8, 256, 0, stream>>>(ekey, eb, eds, S, kcursor, sb, sds);
+  dsub_kernel<<<(unsigned)((K + 7) / 8), 256, 0, stream>>>(q, koff, sb, sds, H, hd, n_keys,
+                                                          dsubkeys);
+  return cudaGetLastError();
 }
 
 }  // namespace pkm

@@ -21,9 +21,7 @@ struct pkm_handle {
   int* retry_counts;  // [2 + units]: pairs of the last bf16 lookup that needed the retry,
                       // units retried, then the per-unit flags (units = retry_units(max_B, max_H))
   int* unit_list;     // [units]
-  cublasHandle_t blas;  // with_backward: dq / dsubkeys products
-  void* blas_ws;        // its workspace
-  void* bwd_ws;         // with_backward: dw and score-gradient rows
+  void* bwd_ws;         // with_backward: dw and the two parts' scratch
   float* list_v;     // [max_B * max_H * 2 * 32] per-half lists between the two bf16 kernels
   unsigned short* list_c;
   float hint_z;      // selection threshold hint override (NaN: automatic)
@@ -49,8 +47,6 @@ struct pkm_handle {
 
 namespace {
 
-constexpr size_t kBlasWorkspace = 32u << 20;  // cuBLAS workspace of a with_backward handle
-
 int elem_size(int dtype) { return dtype == PKM_FP8_E4M3 ? 1 : dtype == PKM_BF16 ? 2 : 4; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -65,6 +61,7 @@ int check_config(const pkm_config* c) {
     return PKM_ERR_UNSUPPORTED;
   if (c->q_dtype != c->key_dtype) return PKM_ERR_UNSUPPORTED;
   if (c->with_backward && (c->q_dtype != PKM_BF16 || c->value_dtype == PKM_FP8_E4M3 ||
+                           c->d_q > 2048 ||
                           (int64_t)c->max_B * c->max_H * c->max_k > INT32_MAX ||
                           (int64_t)c->max_B * c->d_v / 4 > INT32_MAX))
     return PKM_ERR_UNSUPPORTED;
@@ -168,8 +165,6 @@ void pkm_destroy(pkm_t h) {
   cudaFree(h->unit_list);
   cudaFree(h->list_v);
   cudaFree(h->list_c);
-  if (h->blas) cublasDestroy(h->blas);
-  cudaFree(h->blas_ws);
   cudaFree(h->bwd_ws);
   for (int s = 0; s < kHostSlots; ++s) {
     cudaFree(h->stage_q[s]);
@@ -240,10 +235,7 @@ int pkm_create(pkm_t* out, const pkm_config* cfg) {
   if (ok && cfg->with_backward) {
     const size_t ws = pkm::backward_workspace_bytes(cfg->max_B, cfg->max_H, cfg->max_n_keys,
                                                     cfg->max_k);
-    ok = cudaMalloc(&h->bwd_ws, ws ? ws : 256) == cudaSuccess &&
-         cudaMalloc(&h->blas_ws, kBlasWorkspace) == cudaSuccess &&
-         cublasCreate(&h->blas) == CUBLAS_STATUS_SUCCESS &&
-         cublasSetWorkspace(h->blas, h->blas_ws, kBlasWorkspace) == CUBLAS_STATUS_SUCCESS;
+    ok = cudaMalloc(&h->bwd_ws, ws ? ws : 256) == cudaSuccess;
   }
   if (!ok) {
     cudaGetLastError();
@@ -355,9 +347,8 @@ int pkm_backward_scores(pkm_t h, const void* q, const void* subkeys, int B, int 
                         (const void*)dq, (const void*)dsubkeys})
     if (!aligned16(p)) return PKM_ERR_ALIGN;
   return cuda_rc(pkm::launch_backward_scores(
-      h->blas, static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(subkeys), B, H,
-      h->cfg.d_q, n_keys, k, idx, w, dw, dq, dsubkeys, backward_region(h), h->blas_ws,
-      kBlasWorkspace,
+      static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(subkeys), B, H, h->cfg.d_q,
+      n_keys, k, idx, w, dw, dq, dsubkeys, backward_region(h),
       static_cast<cudaStream_t>(stream)));
 }
 

@@ -1,7 +1,6 @@
 // Internal interface between the C-ABI layer (pkm_api.cu) and the kernels.
 #pragma once
 
-#include <cublas_v2.h>
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -31,26 +30,23 @@ cudaError_t launch_qnet(const uint16_t* x, const uint16_t* w, int B, int dim, in
 // the distinct selected rows ascending in rows_out[0 .. *n_rows) and their
 // gradients in grad_rows [*n_rows, d_v]; bf16 or fp32 values; B*H*k < 2^31;
 // workspace: backward_read_workspace_bytes.  Score part: dq overwritten and
-// dsubkeys added to, from w, dw and the selection; bf16 queries/subkeys,
-// k <= 32; workspace: backward_scores_workspace_bytes (the dense bf16
-// per-subkey score-gradient rows [2H][B][n_keys]); blas_workspace: the
-// cuBLAS handle's workspace (re-attached after its stream is set).  A
-// handle's backward scratch is backward_workspace_bytes: dw
-// (backward_dw_bytes), then one region the two parts take in turn.
+// dsubkeys added to, from w, dw and the selection, through the winning
+// subkeys only (fp32); bf16 queries/subkeys, k <= 32, d_q <= 2048;
+// workspace: backward_scores_workspace_bytes.  A handle's backward scratch
+// is backward_workspace_bytes: dw (backward_dw_bytes), then one region the
+// two parts take in turn.
 size_t backward_workspace_bytes(int B, int H, int n_keys, int k);
 size_t backward_dw_bytes(int B, int H, int k);
 size_t backward_read_workspace_bytes(int B, int H, int n_keys, int k);
-size_t backward_scores_workspace_bytes(int B, int H, int n_keys);
+size_t backward_scores_workspace_bytes(int B, int H, int n_keys, int k);
 cudaError_t launch_backward_read(const void* values, int value_dtype, int B, int H, int n_keys,
                                  int d_v, int k, const int64_t* idx, const float* w,
                                  const float* dout, float* dw, float* dvalues, int64_t* rows_out,
                                  float* grad_rows, int* n_rows, void* workspace, int* status,
                                  cudaStream_t stream);
-cudaError_t launch_backward_scores(cublasHandle_t blas, const uint16_t* q,
-                                   const uint16_t* subkeys, int B, int H, int d_q, int n_keys,
-                                   int k, const int64_t* idx, const float* w, const float* dw,
-                                   float* dq, float* dsubkeys, void* workspace,
-                                   void* blas_workspace, size_t blas_workspace_bytes,
+cudaError_t launch_backward_scores(const uint16_t* q, const uint16_t* subkeys, int B, int H,
+                                   int d_q, int n_keys, int k, const int64_t* idx, const float* w,
+                                   const float* dw, float* dq, float* dsubkeys, void* workspace,
                                    cudaStream_t stream);
 
 // Step a6 (value read).  values: [N, d_v] of value_dtype; idx/w: [B, H*k];
