@@ -41,11 +41,18 @@
 //                          winning subkey (winners sharing one summed in lane
 //                          order), dq from those subkeys' rows (L2 gathers),
 //                          and one (subkey, query, DS) contribution per
-//                          distinct subkey, counted per (head, half, subkey);
+//                          distinct subkey, counted per (head, half, subkey)
+//                          by an atomic add whose return is the
+//                          contribution's place in its group; 8 row loads in
+//                          flight per lane;
 //   key_scan_kernel        the counts' offsets (one CTA);
-//   key_scatter_kernel     the contributions grouped by subkey;
-//   dsub_kernel            one warp per (head, half, subkey): its dsubkeys row
-//                          += the sum of DS * q_half rows of its contributions.
+//   key_scatter_kernel     the contributions grouped by subkey (offset +
+//                          place, no atomics);
+//   dsub_kernel            one warp per segment of 64 grouped contributions:
+//                          each key's run in it sums DS * q_half rows (16 row
+//                          loads in flight per lane, not kept in L1) and adds
+//                          the sum to the key's dsubkeys row (vector atomic
+//                          adds).
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -609,17 +616,64 @@ row_grad_kernel(const void* __restrict__ values, int d_v, const float* __restric
 // subkey are summed first (DS, fp32).
 constexpr uint32_t kNoKey = 0xffffffffu;
 constexpr int kMaxChunks = 4;  // 256-wide chunks of a half-query: d_q / 2 <= 1024
+constexpr int kGatherLoads = 8;  // 16-byte row loads a lane of ds_gather has in flight
+constexpr int kDsubLoads = 16;   // the same for dsub_kernel
+constexpr int kDsubSeg = 64;     // sorted contributions per dsub_kernel work item
+
+// A 16-byte load of read-only data that is not kept in L1 (each query row
+// serves one contribution of a group).
+__device__ __forceinline__ uint4 ld_nc_no_l1(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// acc[c][0..8) += s[r] * row[r][c * 256 + lane * 8 .. +8) summed over the R
+// bf16 rows (columns at or past hd skipped); every load is issued before the
+// first multiply-add.  kNoL1: the rows bypass L1 (subkey rows, re-read by the
+// queries an SM holds, are better kept there).
+template <int NC, int R, bool kNoL1>
+__device__ __forceinline__ void fma_rows(const uint16_t* const (&row)[R], const float (&s)[R],
+                                         int hd, int lane, float (&acc)[NC][8]) {
+  uint4 u[R][NC];
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+      const int d0 = c * 256 + lane * 8;
+      u[r][c] = d0 >= hd   ? make_uint4(0, 0, 0, 0)
+                : kNoL1    ? ld_nc_no_l1(row[r] + d0)
+                           : *reinterpret_cast<const uint4*>(row[r] + d0);
+    }
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+      const uint32_t uw[4] = {u[r][c].x, u[r][c].y, u[r][c].z, u[r][c].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        acc[c][2 * e] = fmaf(s[r], __uint_as_float(uw[e] << 16), acc[c][2 * e]);
+        acc[c][2 * e + 1] = fmaf(s[r], __uint_as_float(uw[e] & 0xffff0000u), acc[c][2 * e + 1]);
+      }
+    }
+}
 
 // One warp per (query, head).  Lane j holds winner j.  dq (overwritten) from
 // the distinct winning subkeys' rows; each (subkey, query, DS) contribution
 // to dsubkeys goes to slot ((pair * 2 + half) * k + lane) (kNoKey where lane
-// j is not the first winner of its subkey) and is counted per key
-// (h * 2 + half) * n + subkey.
+// j is not the first winner of its subkey), with its place among its key's
+// contributions (the count before it), key (h * 2 + half) * n + subkey.
+// NC: 256-wide chunks of a half-query (hd <= NC * 256).
+template <int NC>
 __global__ void __launch_bounds__(256)
 ds_gather_kernel(const uint16_t* __restrict__ subkeys, const int64_t* __restrict__ idx,
                  const float* __restrict__ w, const float* __restrict__ dw, int B, int H, int hd,
                  int n, int k, float* __restrict__ dq, uint32_t* __restrict__ ekey,
-                 uint32_t* __restrict__ eb, float* __restrict__ eds, int* __restrict__ kcount) {
+                 uint32_t* __restrict__ erank, float* __restrict__ eds,
+                 int* __restrict__ kcount) {
+  constexpr int R = kGatherLoads / NC;
   const int lane = threadIdx.x & 31;
   const int64_t pair = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (pair >= (int64_t)B * H) return;  // whole warp
@@ -639,7 +693,6 @@ ds_gather_kernel(const uint16_t* __restrict__ subkeys, const int64_t* __restrict
   for (int o = 16; o > 0; o >>= 1) sw += __shfl_xor_sync(0xffffffffu, sw, o);
   const float ds = valid ? wj * (dwj - sw) : 0.0f;
   const int d_q = 2 * hd;
-  const int nchunks = (hd + 255) / 256;
 #pragma unroll 1
   for (int half = 0; half < 2; ++half) {
     // the winner's subkey in this half (lanes without one get distinct -1 - lane)
@@ -654,189 +707,172 @@ ds_gather_kernel(const uint16_t* __restrict__ subkeys, const int64_t* __restrict
       sum += ((same >> l) & 1u) ? v : 0.0f;
     }
     const bool lead = first && valid;
+    // the dsubkeys contribution; its count's return is first needed after
+    // the row gathers below
+    const uint32_t key = (uint32_t)((h * 2 + half) * n + (lead ? a : 0));
+    int rank = 0;
+    if (lead) rank = atomicAdd(&kcount[key], 1);
     // dq of this half: the distinct subkeys' rows, 8 dimensions per lane and
-    // 256-wide chunk
-    float acc[kMaxChunks][8];
+    // 256-wide chunk, R rows per step (past the last: weight 0 on row 0)
+    float acc[NC][8];
 #pragma unroll
-    for (int c = 0; c < kMaxChunks; ++c)
+    for (int c = 0; c < NC; ++c)
 #pragma unroll
       for (int e = 0; e < 8; ++e) acc[c][e] = 0.0f;
     const uint16_t* ctab = subkeys + (size_t)(h * 2 + half) * n * hd;
-    // four subkey rows per step, their loads issued together
     unsigned m = __ballot_sync(0xffffffffu, lead);
 #pragma unroll 1
     while (m) {
-      int aL[4];
-      float sL[4];
+      const uint16_t* row[R];
+      float sL[R];
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
+      for (int r = 0; r < R; ++r) {
         const int L = m ? __ffs(m) - 1 : 0;
-        aL[r] = __shfl_sync(0xffffffffu, a, L);
-        sL[r] = m ? __shfl_sync(0xffffffffu, sum, L) : 0.0f;
-        if (!m) aL[r] = 0;  // a zero weight on row 0: in bounds, no effect
+        const int aL = __shfl_sync(0xffffffffu, a, L);
+        const float v = __shfl_sync(0xffffffffu, sum, L);
+        row[r] = ctab + (size_t)(m ? aL : 0) * hd;
+        sL[r] = m ? v : 0.0f;
         m &= m - 1u;
       }
-#pragma unroll
-      for (int c = 0; c < kMaxChunks; ++c) {
-        const int d0 = c * 256 + lane * 8;
-        if (c < nchunks && d0 < hd) {
-          uint4 u[4];
-#pragma unroll
-          for (int r = 0; r < 4; ++r) u[r] = *reinterpret_cast<const uint4*>(ctab + (size_t)aL[r] * hd + d0);
-#pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            const uint32_t uw[4] = {u[r].x, u[r].y, u[r].z, u[r].w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              acc[c][2 * e] = fmaf(sL[r], __uint_as_float(uw[e] << 16), acc[c][2 * e]);
-              acc[c][2 * e + 1] =
-                  fmaf(sL[r], __uint_as_float(uw[e] & 0xffff0000u), acc[c][2 * e + 1]);
-            }
-          }
-        }
-      }
+      fma_rows<NC, R, false>(row, sL, hd, lane, acc);
     }
     float* out = dq + pair * d_q + half * hd;
 #pragma unroll
-    for (int c = 0; c < kMaxChunks; ++c) {
+    for (int c = 0; c < NC; ++c) {
       const int d0 = c * 256 + lane * 8;
-      if (c < nchunks && d0 < hd) {
+      if (d0 < hd) {
         reinterpret_cast<float4*>(out + d0)[0] =
             make_float4(acc[c][0], acc[c][1], acc[c][2], acc[c][3]);
         reinterpret_cast<float4*>(out + d0)[1] =
             make_float4(acc[c][4], acc[c][5], acc[c][6], acc[c][7]);
       }
     }
-    // the dsubkeys contributions
     if (lane < k) {
       const int64_t slot = (pair * 2 + half) * k + lane;
-      const uint32_t key = (uint32_t)((h * 2 + half) * n + (lead ? a : 0));
       ekey[slot] = lead ? key : kNoKey;
-      eb[slot] = (uint32_t)b;
+      erank[slot] = (uint32_t)rank;
       eds[slot] = sum;
-      if (lead) atomicAdd(&kcount[key], 1);
     }
   }
 }
 
-// Exclusive scan of the per-key counts into koff [K + 1] and the scatter
-// cursors (one CTA).
+// Exclusive scan of the per-key counts into koff [K + 1] (one CTA of 1024
+// threads, 4096 counts per coalesced pass).
 __global__ void __launch_bounds__(1024)
-key_scan_kernel(const int* __restrict__ kcount, int K, int* __restrict__ koff,
-                int* __restrict__ kcursor) {
+key_scan_kernel(const int* __restrict__ kcount, int K, int* __restrict__ koff) {
   __shared__ int warp_sums[32];
+  __shared__ int s_carry;
   const int t = threadIdx.x;
-  const int per = (K + 1023) / 1024;
-  const int k0 = t * per, k1 = min(K, k0 + per);
-  int local = 0;
-  for (int i = k0; i < k1; ++i) local += kcount[i];
-  // block-wide exclusive scan of the threads' sums
-  int incl = local;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, o);
-    if ((t & 31) >= o) incl += v;
-  }
-  if ((t & 31) == 31) warp_sums[t >> 5] = incl;
+  if (t == 0) s_carry = 0;
   __syncthreads();
-  if (t < 32) {
-    int v = warp_sums[t];
+  for (int base = 0; base < K; base += 4096) {
+    const int i0 = base + t * 4;
+    int v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] = i0 + j < K ? kcount[i0 + j] : 0;
+    const int local = v[0] + v[1] + v[2] + v[3];
+    int incl = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int u = __shfl_up_sync(0xffffffffu, v, o);
-      if (t >= o) v += u;
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if ((t & 31) >= o) incl += y;
     }
-    warp_sums[t] = v;
+    if ((t & 31) == 31) warp_sums[t >> 5] = incl;
+    __syncthreads();
+    if (t < 32) {
+      int x = warp_sums[t];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (t >= o) x += y;
+      }
+      warp_sums[t] = x;
+    }
+    __syncthreads();
+    int run = s_carry + incl - local + ((t >> 5) ? warp_sums[(t >> 5) - 1] : 0);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (i0 + j < K) koff[i0 + j] = run;
+      run += v[j];
+    }
+    __syncthreads();
+    if (t == 1023) s_carry = run;
+    __syncthreads();
   }
-  __syncthreads();
-  int run = incl - local + ((t >> 5) ? warp_sums[(t >> 5) - 1] : 0);
-  for (int i = k0; i < k1; ++i) {
-    koff[i] = run;
-    kcursor[i] = run;
-    run += kcount[i];
-  }
-  if (t == 1023) koff[K] = run;
+  if (t == 0) koff[K] = s_carry;
 }
 
-// The contributions grouped by key (order within a key: arrival).
-__global__ void key_scatter_kernel(const uint32_t* __restrict__ ekey, const uint32_t* __restrict__ eb,
-                                   const float* __restrict__ eds, int64_t S,
-                                   int* __restrict__ kcursor, uint32_t* __restrict__ sb,
-                                   float* __restrict__ sds) {
+// The contributions grouped by key, each at its key's offset plus its place
+// (order within a key: the order of the count's atomic adds), as one record
+// (key, query, DS bits, 0); the query of slot s is s / (2 k H).
+__global__ void key_scatter_kernel(const uint32_t* __restrict__ ekey,
+                                   const uint32_t* __restrict__ erank,
+                                   const float* __restrict__ eds, int64_t S, int64_t per_query,
+                                   const int* __restrict__ koff, uint4* __restrict__ rec) {
   for (int64_t s = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; s < S;
        s += (int64_t)gridDim.x * blockDim.x) {
     const uint32_t key = ekey[s];
     if (key == kNoKey) continue;
-    const int pos = atomicAdd(&kcursor[key], 1);
-    sb[pos] = eb[s];
-    sds[pos] = eds[s];
+    const int pos = koff[key] + (int)erank[s];
+    rec[pos] = make_uint4(key, (uint32_t)(s / per_query), __float_as_uint(eds[s]), 0u);
   }
 }
 
-// One warp per key (h, half, subkey): dsubkeys row += sum over its
-// contributions of DS * q_half[b] (fp32 fma, one warp owns the row).
+// dsubkeys from the grouped contributions, one warp per segment of kDsubSeg
+// of them (grid-stride): each run of one key (h, half, subkey) in the
+// segment sums DS * q_half[b] over its contributions (fp32 fma) and adds the
+// sum to the key's dsubkeys row (vector atomic adds: a key's contributions
+// may span several segments).
+template <int NC>
 __global__ void __launch_bounds__(256)
-dsub_kernel(const uint16_t* __restrict__ q, const int* __restrict__ koff,
-            const uint32_t* __restrict__ sb, const float* __restrict__ sds, int H, int hd, int n,
-            float* __restrict__ dsubkeys) {
+dsub_kernel(const uint16_t* __restrict__ q, const int* __restrict__ koff, int K,
+            const uint4* __restrict__ rec, int H, int hd, int n, float* __restrict__ dsubkeys) {
+  constexpr int R = kDsubLoads / NC;
   const int lane = threadIdx.x & 31;
-  const int key = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (key >= 2 * H * n) return;  // whole warp
-  const int e0 = koff[key], e1 = koff[key + 1];
-  if (e0 == e1) return;
-  const int hh = key / n;  // h * 2 + half
-  const int h = hh >> 1, half = hh & 1;
+  const int total = koff[K];
   const int d_q = 2 * hd;
-  const int nchunks = (hd + 255) / 256;
-  float acc[kMaxChunks][8];
-#pragma unroll
-  for (int c = 0; c < kMaxChunks; ++c)
-#pragma unroll
-    for (int e = 0; e < 8; ++e) acc[c][e] = 0.0f;
-  // four contributions per step, their query rows' loads issued together
-  // (past the end: weight 0 on the first row, in bounds)
+  const int nwarps = gridDim.x * (blockDim.x >> 5);
 #pragma unroll 1
-  for (int e = e0; e < e1; e += 4) {
-    uint32_t b[4];
-    float s[4];
+  for (int seg = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); seg * kDsubSeg < total;
+       seg += nwarps) {
+    const int s1 = min(total, (seg + 1) * kDsubSeg);
+#pragma unroll 1
+    for (int e = seg * kDsubSeg; e < s1;) {
+      const uint32_t key = rec[e].x;
+      const int re = min(s1, koff[key + 1]);
+      const int hh = (int)key / n;  // h * 2 + half
+      const int h = hh >> 1, half = hh & 1;
+      float acc[NC][8];
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const bool in = e + r < e1;
-      b[r] = sb[in ? e + r : e0];
-      s[r] = in ? sds[e + r] : 0.0f;
-    }
+      for (int c = 0; c < NC; ++c)
 #pragma unroll
-    for (int c = 0; c < kMaxChunks; ++c) {
-      const int d0 = c * 256 + lane * 8;
-      if (c < nchunks && d0 < hd) {
-        uint4 u[4];
+        for (int i = 0; i < 8; ++i) acc[c][i] = 0.0f;
+      // R contributions per step (past the run's end: weight 0 on its first row)
+      const int rs = e;
+#pragma unroll 1
+      for (; e < re; e += R) {
+        const uint16_t* row[R];
+        float sv[R];
 #pragma unroll
-        for (int r = 0; r < 4; ++r)
-          u[r] = *reinterpret_cast<const uint4*>(q + ((size_t)b[r] * H + h) * d_q + half * hd + d0);
+        for (int r = 0; r < R; ++r) {
+          const bool in = e + r < re;
+          const uint4 c = rec[in ? e + r : rs];
+          const uint32_t b = c.y;
+          sv[r] = in ? __uint_as_float(c.z) : 0.0f;
+          row[r] = q + ((size_t)b * H + h) * d_q + half * hd;
+        }
+        fma_rows<NC, R, true>(row, sv, hd, lane, acc);
+      }
+      e = re;
+      float* out = dsubkeys + (size_t)key * hd;
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const uint32_t uw[4] = {u[r].x, u[r].y, u[r].z, u[r].w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            acc[c][2 * i] = fmaf(s[r], __uint_as_float(uw[i] << 16), acc[c][2 * i]);
-            acc[c][2 * i + 1] =
-                fmaf(s[r], __uint_as_float(uw[i] & 0xffff0000u), acc[c][2 * i + 1]);
-          }
+      for (int c = 0; c < NC; ++c) {
+        const int d0 = c * 256 + lane * 8;
+        if (d0 < hd) {
+          red_add4(out + d0, acc[c][0], acc[c][1], acc[c][2], acc[c][3]);
+          red_add4(out + d0 + 4, acc[c][4], acc[c][5], acc[c][6], acc[c][7]);
         }
       }
-    }
-  }
-  float* out = dsubkeys + (size_t)key * hd;
-#pragma unroll
-  for (int c = 0; c < kMaxChunks; ++c) {
-    const int d0 = c * 256 + lane * 8;
-    if (c < nchunks && d0 < hd) {
-      float4* o = reinterpret_cast<float4*>(out + d0);
-      float4 x = o[0], y = o[1];
-      x.x += acc[c][0]; x.y += acc[c][1]; x.z += acc[c][2]; x.w += acc[c][3];
-      y.x += acc[c][4]; y.y += acc[c][5]; y.z += acc[c][6]; y.w += acc[c][7];
-      o[0] = x;
-      o[1] = y;
     }
   }
 }
@@ -877,26 +913,25 @@ size_t backward_read_workspace_bytes(int B, int H, int n_keys, int k) {
   return off[kOffEnd];
 }
 
-// The score part's scratch: per key (h, half, subkey) its count, offset
-// (K + 1) and scatter cursor; per slot (query, head, half, winner) a key,
-// query and DS; then the contributions grouped by key (query, DS).
+// The score part's scratch: per key (h, half, subkey) its count and offset
+// (K + 1); per slot (query, head, half, winner) a key, the place among its
+// key's contributions and DS; then the contributions grouped by key (one
+// 16-byte record each).
 static void scores_layout(int B, int H, int n_keys, int k, size_t* off) {
   const size_t K = (size_t)2 * H * n_keys, S = (size_t)B * H * 2 * k;
   off[0] = 0;                                 // kcount [K]
   off[1] = off[0] + align256(K * 4);          // koff [K + 1]
-  off[2] = off[1] + align256((K + 1) * 4);    // kcursor [K]
-  off[3] = off[2] + align256(K * 4);          // ekey [S]
-  off[4] = off[3] + align256(S * 4);          // eb [S]
-  off[5] = off[4] + align256(S * 4);          // eds [S]
-  off[6] = off[5] + align256(S * 4);          // sb [S]
-  off[7] = off[6] + align256(S * 4);          // sds [S]
-  off[8] = off[7] + align256(S * 4);
+  off[2] = off[1] + align256((K + 1) * 4);    // ekey [S]
+  off[3] = off[2] + align256(S * 4);          // erank [S]
+  off[4] = off[3] + align256(S * 4);          // eds [S]
+  off[5] = off[4] + align256(S * 4);          // rec [S]
+  off[6] = off[5] + align256(S * 16);
 }
 
 size_t backward_scores_workspace_bytes(int B, int H, int n_keys, int k) {
-  size_t off[9];
+  size_t off[7];
   scores_layout(B, H, n_keys, k, off);
-  return off[8];
+  return off[6];
 }
 
 size_t backward_dw_bytes(int B, int H, int k) { return align256((size_t)B * H * k * 4); }
@@ -984,29 +1019,45 @@ cudaError_t launch_backward_scores(const uint16_t* q, const uint16_t* subkeys, i
   if (B == 0) return cudaSuccess;
   const int hd = d_q / 2;
   if (k > 32 || hd > 256 * kMaxChunks || hd % 8) return cudaErrorInvalidValue;
-  size_t off[9];
+  size_t off[7];
   scores_layout(B, H, n_keys, k, off);
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   int* kcount = reinterpret_cast<int*>(ws + off[0]);
   int* koff = reinterpret_cast<int*>(ws + off[1]);
-  int* kcursor = reinterpret_cast<int*>(ws + off[2]);
-  uint32_t* ekey = reinterpret_cast<uint32_t*>(ws + off[3]);
-  uint32_t* eb = reinterpret_cast<uint32_t*>(ws + off[4]);
-  float* eds = reinterpret_cast<float*>(ws + off[5]);
-  uint32_t* sb = reinterpret_cast<uint32_t*>(ws + off[6]);
-  float* sds = reinterpret_cast<float*>(ws + off[7]);
+  uint32_t* ekey = reinterpret_cast<uint32_t*>(ws + off[2]);
+  uint32_t* erank = reinterpret_cast<uint32_t*>(ws + off[3]);
+  float* eds = reinterpret_cast<float*>(ws + off[4]);
+  uint4* rec = reinterpret_cast<uint4*>(ws + off[5]);
   const int K = 2 * H * n_keys;
   const int64_t S = (int64_t)B * H * 2 * k;
   cudaError_t e = cudaMemsetAsync(kcount, 0, (size_t)K * 4, stream);
   if (e != cudaSuccess) return e;
   const int64_t pairs = (int64_t)B * H;
-  ds_gather_kernel<<<(unsigned)((pairs + 7) / 8), 256, 0, stream>>>(
-      subkeys, idx, w, dw, B, H, hd, n_keys, k, dq, ekey, eb, eds, kcount);
-  key_scan_kernel<<<1, 1024, 0, stream>>>(kcount, K, koff, kcursor);
+  const unsigned g_pairs = (unsigned)((pairs + 7) / 8);
   const int sms = tc::sm_count();
-  key_scatter_kernel<<<sms * 8, 256, 0, stream>>>(ekey, eb, eds, S, kcursor, sb, sds);
-  dsub_kernel<<<(unsigned)((K + 7) / 8), 256, 0, stream>>>(q, koff, sb, sds, H, hd, n_keys,
-                                                          dsubkeys);
+  const int nc = (hd + 255) / 256;
+  auto run = [&](auto nc_tag) {
+    constexpr int NC = decltype(nc_tag)::value;
+    ds_gather_kernel<NC><<<g_pairs, 256, 0, stream>>>(subkeys, idx, w, dw, B, H, hd, n_keys, k,
+                                                      dq, ekey, erank, eds, kcount);
+    key_scan_kernel<<<1, 1024, 0, stream>>>(kcount, K, koff);
+    // one thread per slot: each is a chain of two dependent loads
+    key_scatter_kernel<<<(unsigned)((S + 255) / 256), 256, 0, stream>>>(
+        ekey, erank, eds, S, (int64_t)2 * k * H, koff, rec);
+    int per_sm = 0;  // a persistent grid: the CTAs that fit at once
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dsub_kernel<NC>, 256, 0) !=
+            cudaSuccess ||
+        per_sm < 1)
+      per_sm = 1;
+    dsub_kernel<NC><<<sms * per_sm, 256, 0, stream>>>(q, koff, K, rec, H, hd, n_keys,
+                                                      dsubkeys);
+  };
+  if (nc <= 1)
+    run(std::integral_constant<int, 1>{});
+  else if (nc <= 2)
+    run(std::integral_constant<int, 2>{});
+  else
+    run(std::integral_constant<int, 4>{});
   return cudaGetLastError();
 }
 
