@@ -179,6 +179,33 @@ int pkm_lookup(pkm_t h, const void *q, const void *subkeys, int B, int H, int n_
                int64_t *idx, float *w, void *stream);
 
 /*
+ * The flat exact top-k: the search that product keys replace, for measuring
+ * what the factorisation saves on the same GPU ("Memory Retrieval
+ * Mechanisms: From Soft to Efficient", top-k retrieval and its cost walk-
+ * through: score all N keys, O(N d), keep the k best, softmax over them;
+ * "Product-Key Memory", "Factorising the key space": a full key is the
+ * concatenation of one subkey per half, 2 sqrt(N) subkey comparisons
+ * instead of N).
+ *
+ * pkm_full_keys: keys [H][n_keys^2][d_q] bf16 (caller-owned, device,
+ *   H * n_keys^2 * d_q * 2 bytes) from subkeys [H][2][n_keys][d_q/2] bf16:
+ *   keys[h][a * n_keys + b] = concat(subkeys[h][0][a], subkeys[h][1][b]).
+ * pkm_flat_lookup: per (query, head) every full key scored as one d_q-long
+ *   dot product (bf16 inputs, fp32 accumulation, tensor cores), the k best by
+ *   (score desc, flat index asc) in idx [B][H][k] int64 and their softmax in
+ *   w [B][H][k] fp32, as pkm_lookup returns them.  Needs bf16 queries and
+ *   keys and k <= 32; sizes are checked against the handle's configuration
+ *   like pkm_lookup's, k <= n_keys included (PKM_ERR_RANGE /
+ *   PKM_ERR_UNSUPPORTED).  A bounded wait
+ *   that runs out records PKM_ERR_TIMEOUT (pkm_get_status).
+ * Both are asynchronous on `stream`; device pointers, 16-byte aligned
+ * (PKM_ERR_ALIGN); NULL pointers give PKM_ERR_INVALID; B == 0 is a no-op.
+ */
+int pkm_full_keys(pkm_t h, const void *subkeys, int H, int n_keys, void *keys, void *stream);
+int pkm_flat_lookup(pkm_t h, const void *q, const void *keys, int B, int H, int n_keys, int k,
+                    int64_t *idx, float *w, void *stream);
+
+/*
  * The value read alone: out[b,:] = sum_{h,j} w[b,h,j] * values[idx[b,h,j], :]
  * (EmbeddingBag(mode="sum") with per-sample weights, bags of H*k rows).
  * Rows with an index outside [0, n_keys^2) contribute nothing and set

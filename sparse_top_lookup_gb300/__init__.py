@@ -28,7 +28,7 @@ EXPORTED = ["pkm_create", "pkm_destroy", "pkm_forward", "pkm_lookup", "pkm_gathe
             "pkm_abi_version", "pkm_set_option", "pkm_get_fallback_count", "pkm_lookup_static",
             "pkm_quantize_values_fp8", "pkm_bn_fold", "pkm_query_net", "pkm_backward", "pkm_backward_read",
             "pkm_backward_scores", "pkm_forward_host_async", "pkm_backward_sparse",
-            "pkm_backward_read_sparse", "pkm_multicast_ok"]
+            "pkm_backward_read_sparse", "pkm_multicast_ok", "pkm_full_keys", "pkm_flat_lookup"]
 PKM_STATIC_MAX_PAIRS = 1 << 16
 
 
@@ -87,6 +87,8 @@ def lib():
         L.pkm_backward_scores.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
         L.pkm_backward_sparse.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp,
                                           vp, vp, vp, vp]
+        L.pkm_full_keys.argtypes = [vp, vp, i32, i32, vp, vp]
+        L.pkm_flat_lookup.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp]
         L.pkm_backward_read_sparse.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp,
                                                vp, vp, vp]
         for f in ("pkm_create", "pkm_forward", "pkm_lookup", "pkm_gather", "pkm_forward_host",
@@ -94,7 +96,7 @@ def lib():
                   "pkm_get_fallback_count", "pkm_lookup_static", "pkm_quantize_values_fp8",
                   "pkm_bn_fold", "pkm_query_net", "pkm_backward", "pkm_backward_read",
                   "pkm_backward_scores", "pkm_forward_host_async", "pkm_backward_sparse",
-                  "pkm_backward_read_sparse"):
+                  "pkm_backward_read_sparse", "pkm_full_keys", "pkm_flat_lookup"):
             getattr(L, f).restype = i32
         _lib = L
     return _lib
@@ -162,6 +164,17 @@ def pkm_forward(h, q, subkeys, values, B, H, n_keys, k, out, idx=None, w=None, s
 def pkm_lookup(h, q, subkeys, B, H, n_keys, k, idx, w, stream=None):
     return lib().pkm_lookup(h, _addr(q), _addr(subkeys), B, H, n_keys, k, _addr(idx), _addr(w),
                             _stream(stream))
+
+
+def pkm_full_keys(h, subkeys, H, n_keys, keys, stream=None):
+    """The full key table [H][n_keys^2][d_q] from the subkeys (see include/pkm.h)."""
+    return lib().pkm_full_keys(h, _addr(subkeys), H, n_keys, _addr(keys), _stream(stream))
+
+
+def pkm_flat_lookup(h, q, keys, B, H, n_keys, k, idx, w, stream=None):
+    """Top-k over all n_keys^2 full keys and its softmax (see include/pkm.h)."""
+    return lib().pkm_flat_lookup(h, _addr(q), _addr(keys), B, H, n_keys, k, _addr(idx), _addr(w),
+                                 _stream(stream))
 
 
 def pkm_gather(h, values, B, H, n_keys, k, idx, w, out, stream=None):

@@ -14,7 +14,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpkm.so")
 SOURCES = ["pkm_api.cu", "gather.cu", "lookup_simt.cu", "lookup_tc.cu", "lookup_2sm.cu", "lookup_merge.cu",
-           "pkm_static.cu", "values_fp8.cu", "qnet.cu", "backward.cu"]
+           "pkm_static.cu", "values_fp8.cu", "qnet.cu", "backward.cu", "flat.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -191,12 +191,21 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 // Cluster c (CTAs 2c, 2c+1; rank 0 leads) takes pair units c + i * clusters.
 // Pair unit u: half u & 1, pair tile (u >> 1) / H, head (u >> 1) % H; CTA
 // rank r holds query rows 256 * tile + 128 * r + [0, 128).
-template <int KL, int kEpi>
+//
+// kFlat: the flat exact top-k that the factorisation replaces (Memory
+// Retrieval Mechanisms, top-k retrieval: score all keys, keep the k best).
+// The columns are the n = n_keys^2 full keys of a head (tmap_c over
+// [H][n][d_q]; the query map's half axis has one entry), unit u is pair tile
+// u / H, head u % H, and each row's best k (score desc, flat index asc) go
+// with their softmax to out_idx / out_w [B][H][k].  Run without a threshold
+// hint: the selection is exact with nothing to retry.
+template <int KL, int kEpi, bool kFlat>
 __global__ void __launch_bounds__(Shape2<kEpi>::kThreads, 1)
 select_2sm_kernel(const __grid_constant__ CUtensorMap tmap_q,
                   const __grid_constant__ CUtensorMap tmap_c, int B, int H, int n, int nch,
                   int kb_count, float hint_z, float* __restrict__ list_v,
-                  unsigned short* __restrict__ list_c, int* __restrict__ status, int stall) {
+                  unsigned short* __restrict__ list_c, int64_t* __restrict__ out_idx,
+                  float* __restrict__ out_w, int k, int* __restrict__ status, int stall) {
   constexpr int STAGES = Shape2<kEpi>::kStages, SETS = Shape2<kEpi>::kSets;
   constexpr int SMEM_TILES = Shape2<kEpi>::kTiles;
   extern __shared__ unsigned char smem_raw[];
@@ -208,7 +217,7 @@ select_2sm_kernel(const __grid_constant__ CUtensorMap tmap_q,
   const int slot = (int)(blockIdx.x >> 1);
   const int slots = (int)(gridDim.x >> 1);
   const int pair_tiles = (B + 2 * BM - 1) / (2 * BM);
-  const int units = pair_tiles * H * 2;
+  const int units = pair_tiles * H * (kFlat ? 1 : 2);
   const int mine = slot < units ? (units - 1 - slot) / slots + 1 : 0;
   if (mine == 0) return;  // both CTAs of the cluster alike
 
@@ -252,6 +261,13 @@ select_2sm_kernel(const __grid_constant__ CUtensorMap tmap_q,
   const Ctl ctl{&s_abort, status};
 
   auto unit_at = [&](int i) { return slot + i * slots; };
+  // unit u -> (half, pair tile, head)
+  auto decode = [&](int u, int& half, int& pt, int& h) {
+    half = kFlat ? 0 : (u & 1);
+    const int hu = kFlat ? u : (u >> 1);
+    pt = hu / H;
+    h = hu - pt * H;
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
@@ -263,8 +279,8 @@ select_2sm_kernel(const __grid_constant__ CUtensorMap tmap_q,
       for (int i0 = 0; ok && i0 < mine; i0 += SETS)
         for (int ch = 0; ok && ch < nch; ++ch)
           for (int st = 0; ok && st < SETS && i0 + st < mine; ++st) {
-            const int u = unit_at(i0 + st);
-            const int half = u & 1, pt = (u >> 1) / H, h = (u >> 1) - ((u >> 1) / H) * H;
+            int half, pt, h;
+            decode(unit_at(i0 + st), half, pt, h);
             const int row0 = pt * 2 * BM + (int)rank * BM;
             for (int kb = 0; kb < kb_count; ++kb, ++it) {
               const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
@@ -279,7 +295,7 @@ select_2sm_kernel(const __grid_constant__ CUtensorMap tmap_q,
               const uint32_t fb = mapa_shared(bar_full(s), 0);
               tma_load_4d_cg2(dst, &tmap_q, kb * BK, half, h, row0, fb);
               tma_load_3d_cg2(dst + A_BYTES, &tmap_c, kb * BK, ch * NP + (int)rank * NH,
-                              h * 2 + half, fb);
+                              kFlat ? h : h * 2 + half, fb);
             }
           }
       // the leader's last releases of this CTA's stages land before it exits
@@ -341,8 +357,8 @@ select_2sm_kernel(const __grid_constant__ CUtensorMap tmap_q,
     uint32_t cnt = 0;                          // chunks of this set consumed so far
     bool ok = true;
     for (int i = set; ok && i < mine; i += SETS) {
-      const int u = unit_at(i);
-      const int half = u & 1, pt = (u >> 1) / H, h = (u >> 1) - ((u >> 1) / H) * H;
+      int half, pt, h;
+      decode(unit_at(i), half, pt, h);
       float thr = -INFINITY;  // a score is logged when it is > thr
       float V[KL];
       uint32_t C[KL];
@@ -414,6 +430,24 @@ select_2sm_kernel(const __grid_constant__ CUtensorMap tmap_q,
       }
       if (!ok) break;
       const int b = pt * 2 * BM + (int)rank * BM + row;
+      if constexpr (kFlat) {
+        // the k best full keys and their softmax (V[0] is the largest)
+        if (b < B) {
+          const size_t off = ((size_t)b * H + h) * k;
+          float z = 0.0f;
+#pragma unroll
+          for (int r = 0; r < KL; ++r)
+            if (r < k) z += expf(V[r] - V[0]);
+          const float inv_z = 1.0f / z;
+#pragma unroll
+          for (int r = 0; r < KL; ++r)
+            if (r < k) {
+              out_idx[off + r] = (int64_t)C[r];
+              out_w[off + r] = expf(V[r] - V[0]) * inv_z;
+            }
+        }
+        continue;
+      }
       // the half's list by (score desc, subkey asc) to global memory.  A list
       // with fewer than `need` entries (the hint was above the row's KL-th
       // score) is marked by the subkey 0xffff in its first slot and selected
@@ -453,11 +487,12 @@ select_2sm_kernel(const __grid_constant__ CUtensorMap tmap_q,
 
 // ------------------------------------------------------------------ host
 
-template <int KL, int kEpi>
+template <int KL, int kEpi, bool kFlat = false>
 cudaError_t launch_kl(const CUtensorMap& mq, const CUtensorMap& mc, int B, int H, int n, int nch,
                       int kbc, float hint_z, float* list_v, unsigned short* list_c, int* status,
-                      int stall, cudaStream_t stream) {
-  auto kernel = select_2sm_kernel<KL, kEpi>;
+                      int stall, cudaStream_t stream, int64_t* out_idx = nullptr,
+                      float* out_w = nullptr, int k = 0) {
+  auto kernel = select_2sm_kernel<KL, kEpi, kFlat>;
   constexpr int SMEM_BYTES = Shape2<kEpi>::kSmem;
   static bool attr_set = false;
   if (!attr_set) {
@@ -484,10 +519,10 @@ cudaError_t launch_kl(const CUtensorMap& mq, const CUtensorMap& mc, int B, int H
     if (e != cudaSuccess) return e;
     if (max_clusters < 1) return cudaErrorInvalidConfiguration;
   }
-  const int units = (B + 2 * BM - 1) / (2 * BM) * H * 2;
+  const int units = (B + 2 * BM - 1) / (2 * BM) * H * (kFlat ? 1 : 2);
   cfg.gridDim = dim3(2 * (units < max_clusters ? units : max_clusters));
   return cudaLaunchKernelEx(&cfg, kernel, mq, mc, B, H, n, nch, kbc, hint_z, list_v, list_c,
-                            status, stall);
+                            out_idx, out_w, k, status, stall);
 }
 
 }  // namespace
@@ -506,6 +541,20 @@ cudaError_t launch_select_2sm(const CUtensorMap& tmap_q, const CUtensorMap& tmap
   if (epi == kEpiOneSet) return k <= 16 ? PKM_SEL2(16, kEpiOneSet) : PKM_SEL2(32, kEpiOneSet);
   return k <= 16 ? PKM_SEL2(16, kEpiTwoSets) : PKM_SEL2(32, kEpiTwoSets);
 #undef PKM_SEL2
+}
+
+cudaError_t launch_select_2sm_flat(const CUtensorMap& tmap_q, const CUtensorMap& tmap_keys, int B,
+                                   int H, int d_q, int N, int k, int64_t* idx, float* w,
+                                   int* status, cudaStream_t stream) {
+  if (B == 0) return cudaSuccess;
+  const int nch = (N + NP - 1) / NP;
+  const int kbc = (d_q + BK - 1) / BK;
+  return k <= 16 ? launch_kl<16, kEpiTwoSets, true>(tmap_q, tmap_keys, B, H, N, nch, kbc,
+                                                    -INFINITY, nullptr, nullptr, status, 0,
+                                                    stream, idx, w, k)
+                 : launch_kl<32, kEpiTwoSets, true>(tmap_q, tmap_keys, B, H, N, nch, kbc,
+                                                    -INFINITY, nullptr, nullptr, status, 0,
+                                                    stream, idx, w, k);
 }
 
 }  // namespace pkm

@@ -258,6 +258,34 @@ int pkm_lookup(pkm_t h, const void* q, const void* subkeys, int B, int H, int n_
   return run_lookup(h, q, subkeys, B, H, n_keys, k, idx, w, static_cast<cudaStream_t>(stream));
 }
 
+int pkm_full_keys(pkm_t h, const void* subkeys, int H, int n_keys, void* keys, void* stream) {
+  if (!h) return PKM_ERR_INVALID;
+  int rc = check_call(&h->cfg, 0, H, n_keys, 1);
+  if (rc) return rc;
+  if (h->cfg.key_dtype != PKM_BF16) return PKM_ERR_UNSUPPORTED;
+  if (!subkeys || !keys) return PKM_ERR_INVALID;
+  if (!aligned16(subkeys) || !aligned16(keys)) return PKM_ERR_ALIGN;
+  return cuda_rc(pkm::launch_full_keys(static_cast<const uint16_t*>(subkeys), H, n_keys,
+                                       h->cfg.d_q, static_cast<uint16_t*>(keys),
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+int pkm_flat_lookup(pkm_t h, const void* q, const void* keys, int B, int H, int n_keys, int k,
+                    int64_t* idx, float* w, void* stream) {
+  if (!h) return PKM_ERR_INVALID;
+  int rc = check_call(&h->cfg, B, H, n_keys, k);
+  if (rc) return rc;
+  if (h->cfg.q_dtype != PKM_BF16 || k > pkm::kTcMaxK) return PKM_ERR_UNSUPPORTED;
+  if (B == 0) return PKM_OK;
+  if (!q || !keys || !idx || !w) return PKM_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(keys) || !aligned16(idx) || !aligned16(w))
+    return PKM_ERR_ALIGN;
+  return cuda_rc(pkm::launch_flat_lookup(static_cast<const uint16_t*>(q),
+                                         static_cast<const uint16_t*>(keys), B, H, h->cfg.d_q,
+                                         n_keys * n_keys, k, idx, w, h->status,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
 int pkm_gather(pkm_t h, const void* values, int B, int H, int n_keys, int k, const int64_t* idx,
                const float* w, float* out, void* stream) {
   if (!h) return PKM_ERR_INVALID;

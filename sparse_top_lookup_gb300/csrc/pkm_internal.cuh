@@ -112,6 +112,22 @@ cudaError_t launch_select_2sm(const CUtensorMap& tmap_q, const CUtensorMap& tmap
                               unsigned short* list_c, int* status, bool stall,
                               cudaStream_t stream, int epi = 2);
 
+// The flat exact top-k (flat.cu), the baseline the factorisation replaces:
+// the full key table [H][n_keys^2][d_q] (bf16) from the subkeys, and per
+// (query, head) the top-k of all N full keys, each scored as one d_q-long
+// dot product, with its softmax: idx / w [B][H][k] (flat index a * n_keys +
+// b; ties to the lower index).  k <= kTcMaxK, d_q % 16 == 0.  The selection
+// is the flat form of the two-SM kernel (tmap_q: q as [B][H][1][d_q] in
+// 128x64 boxes; tmap_keys: the full keys in 128x64 boxes).
+cudaError_t launch_full_keys(const uint16_t* subkeys, int H, int n_keys, int d_q, uint16_t* keys,
+                             cudaStream_t stream);
+cudaError_t launch_flat_lookup(const uint16_t* q, const uint16_t* keys, int B, int H, int d_q,
+                               int N, int k, int64_t* idx, float* w, int* status,
+                               cudaStream_t stream);
+cudaError_t launch_select_2sm_flat(const CUtensorMap& tmap_q, const CUtensorMap& tmap_keys, int B,
+                                   int H, int d_q, int N, int k, int64_t* idx, float* w,
+                                   int* status, cudaStream_t stream);
+
 // Entries of one per-half list for a given k.
 int list_slots(int k);
 
