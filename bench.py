@@ -6,7 +6,13 @@ queries, H = 4 heads, d_q = 1024, n_keys = 1024 (N = 2^20), d_v = 1024,
 k = 32, bf16 inputs, all resident in HBM.  Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload page|mid|skew|large|tiny]
+                  [--workload page|mid|skew|large|tiny|page_fp8|page_layer|
+                              page_train|page_train_sparse|mid_flat]
+
+The training workloads add the backward pass to each step; the layer
+workload starts from the layer input (query network first); mid_flat
+searches all N full keys of the mid workload (the flat exact top-k) and
+times the factorised lookup of the same queries beside it.
 
 --impl reference times the fp64 CPU oracle on the host cores instead, on a
 bounded sample of the same workload.  This build runs on one GPU: under
@@ -155,6 +161,11 @@ def is_train(c):
     return bool(c.get("train"))
 
 
+def is_flat(c):
+    """A flat workload searches all n_keys^2 full keys instead of the two halves."""
+    return bool(c.get("flat"))
+
+
 def is_layer(c):
     """A layer workload starts from the layer input x and runs the query network."""
     return "qnet_dim" in c
@@ -189,6 +200,11 @@ def cpu_oracle_time(c, inputs, sample, nthreads):
     if is_fp8(c):
         ref = oracle.lookup(q, C, sample, H, d_q, n, k, nthreads=nthreads)
         oracle.gather_fp8(V[0], V[1], n * n, d_v, ref["idx"], ref["w"], nthreads=nthreads)
+    elif is_flat(c):
+        # brute force over every full key, then the value read
+        idx, score = oracle.brute_topk(q, C, sample, H, d_q, n, k, nthreads=nthreads)
+        z = np.exp(score - score[..., :1])
+        oracle.gather(V, n * n, d_v, idx, z / z.sum(-1, keepdims=True), nthreads=nthreads)
     elif is_train(c):
         # forward, then the backward pass for its selection (dvalues formed
         # for the selected rows only)
@@ -206,7 +222,7 @@ def run_reference(args, rank, world):
         return
     c = workload(args.workload, args.batch, args.n_keys)
     nthreads = os.cpu_count() or 1
-    sample = min(args.cpu_sample, c["B"])
+    sample = min(args.cpu_sample, c["B"], 64 if is_flat(c) else c["B"])
     inputs = cpu_inputs(c, sample)
     ts = []
     for i in range(args.warmup + args.steps):
@@ -218,7 +234,8 @@ def run_reference(args, rank, world):
     cpu = {"value": value, "unit": UNIT, "cores": nthreads, "kind": "oracle",
            "sample": "%d of %d queries of the %s workload per step (fp64 oracle %s)"
                      % (sample, c["B"], args.workload,
-                        "forward + backward" if is_train(c) else "forward")}
+                        "forward + backward" if is_train(c)
+                        else "brute-force forward" if is_flat(c) else "forward")}
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -246,6 +263,10 @@ def config_json(c, name):
                   "step = forward + backward (dq; dsubkeys accumulated in fp32; dvalues %s)"
                   % ("as distinct rows and their fp32 gradient rows" if c.get("sparse_grad")
                      else "accumulated into the dense fp32 table"))
+    if is_flat(c):
+        inputs = ("mid inputs, seeded synthetic; full key table [H, N, d_q] bf16 materialised "
+                  "from the subkeys once, outside the timed steps; step = flat top-k over all "
+                  "N full keys + value read")
     if is_layer(c):
         inputs = ("layer input x [B, %d] bf16 N(0,1); query network weight [H*d_q, %d] bf16 "
                   "N(0,1/%d) and BatchNorm running statistics; subkeys and values as page; "
@@ -271,6 +292,8 @@ def run_ours(args, rank, world, local):
 
     torch.cuda.set_device(local)
     c = workload(args.workload, args.batch, args.n_keys)
+    if is_flat(c):
+        return run_ours_flat(args, c, rank, world)
     B, H, d_q, n, d_v, k = (c[x] for x in ("B", "H", "d_q", "n_keys", "d_v", "k"))
     bf16 = c["dtype"] == "bf16"
     dt = pk.PKM_BF16 if bf16 else pk.PKM_F32
@@ -595,14 +618,15 @@ def run_ours(args, rank, world, local):
                 "calls_in_flight": 2 if (train or layer) else IN_FLIGHT,
                 "copy_gbs": {"h2d": h2d_gbs, "d2h": d2h_gbs},
                 "value_one_call_in_flight": world * B * H / e2e_sync_s},
-        # per step: select_tc_kernel and merge_kernel, their retry launches
+        # per step: select_2sm_kernel and merge_kernel, their retry launches
         # (return at once when no row missed its threshold hint) and the
         # value read (fp32 inputs: lookup_simt_kernel and the value read)
-        # (training: bucket_count, bucket_scan, bucket_scatter, bucket_sort,
-        # row_grad and ds_rows kernels too, and zero_rows for the sparse
-        # gradient, besides memsets and two cuBLAS GEMM launches)
+        # (training: bucket_count, bucket_scan, bucket_scatter, bucket_sort
+        # and row_grad kernels, zero_rows for the sparse gradient, and
+        # ds_gather, key_scan, key_scatter and dsub kernels too, besides
+        # memsets)
         "gpu_launches": ((5 if bf16 else 2) + (1 if layer else 0)
-                         + ((7 if sparse else 6) if train else 0)) * args.steps,
+                         + ((10 if sparse else 9) if train else 0)) * args.steps,
         "clocks": clk.summary(),
     }
     if train:
@@ -633,6 +657,138 @@ def run_ours(args, rank, world, local):
                       % (sample, B, H, args.workload,
                          "forward + backward" if train else "forward"),
             "value_1_thread": s1 * H / t1, "sample_1_thread": "the first %d of them" % s1}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_ours_flat(args, c, rank, world):
+    """The flat forward: per step the exact top-k over all N = n_keys^2 full
+    keys (pkm_flat_lookup) and the value read; the factorised lookup of the
+    same queries is timed in the same run for the comparison."""
+    import torch
+    import sparse_top_lookup_gb300 as pk
+
+    B, H, d_q, n, d_v, k = (c[x] for x in ("B", "H", "d_q", "n_keys", "d_v", "k"))
+    N = n * n
+
+    def dev(a):
+        return torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16)
+
+    q_np, C_np, V_np = synth.queries(c), synth.subkeys(c), synth.values(c)
+    dq, dC, dV = dev(q_np), dev(C_np), dev(V_np)
+    out = torch.empty(B, d_v, device="cuda")
+    idx = torch.empty(B, H, k, dtype=torch.int64, device="cuda")
+    w = torch.empty(B, H, k, device="cuda")
+    fidx, fw = torch.empty_like(idx), torch.empty_like(w)
+    keys = torch.empty(H, N, d_q, dtype=torch.bfloat16, device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    h = pk.pkm_create(pk.make_config(d_q, d_v, B, H, n, k))
+    stream = torch.cuda.current_stream()
+    # the full key table, once (as a value table is written once)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    pk.check(pk.pkm_full_keys(h, dC, H, n, keys, stream), "pkm_full_keys")
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_keys = e0.elapsed_time(e1)
+
+    def flat_step():
+        pk.check(pk.pkm_flat_lookup(h, dq, keys, B, H, n, k, idx, w, stream), "pkm_flat_lookup")
+        pk.check(pk.pkm_gather(h, dV, B, H, n, k, idx, w, out, stream), "pkm_gather")
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        flat_step()
+        pk.check(pk.pkm_lookup(h, dq, dC, B, H, n, k, fidx, fw, stream), "pkm_lookup")
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    fev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            pk.check(pk.pkm_flat_lookup(h, dq, keys, B, H, n, k, idx, w, stream),
+                     "pkm_flat_lookup")
+            ev[i][1].record(stream)
+            pk.check(pk.pkm_gather(h, dV, B, H, n, k, idx, w, out, stream), "pkm_gather")
+            ev[i][2].record(stream)
+        # the factorised search of the same queries, for the comparison
+        for i in range(args.steps):
+            flush.zero_()
+            fev[i][0].record(stream)
+            pk.check(pk.pkm_lookup(h, dq, dC, B, H, n, k, fidx, fw, stream), "pkm_lookup")
+            fev[i][1].record(stream)
+        torch.cuda.synchronize()
+        time.sleep(0.25)
+    dist_barrier(world)
+    st = pk.pkm_get_status(h)
+    if st != pk.PKM_OK:
+        raise RuntimeError("device status after timed steps: %s" % pk.pkm_strerror(st))
+    ms_flat = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
+    ms_gather = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
+    ms_step = dist_max(sum(e[0].elapsed_time(e[2]) for e in ev) / args.steps, world)
+    ms_fact = sum(e[0].elapsed_time(e[1]) for e in fev) / args.steps
+    same = float((idx == fidx).all(-1).float().mean())
+
+    # end to end: q in from pinned host memory, flat lookup and read, out back
+    q_host = torch.from_numpy(q_np.view(np.int16)).pin_memory()
+    out_host = torch.empty(B, d_v).pin_memory()
+
+    def e2e_call():
+        dq.view(torch.int16).view(-1).copy_(q_host.view(-1), non_blocking=True)
+        flat_step()
+        out_host.copy_(out, non_blocking=True)
+        stream.synchronize()
+    for _ in range(2):
+        e2e_call()
+    e2e_steps = max(3, min(args.steps, 20))
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_call()
+    e2e_s = dist_max((time.perf_counter() - t0) / e2e_steps, world)
+    pk.pkm_destroy(h)
+
+    pk_ = peaks()
+    flops = 2.0 * B * H * N * d_q
+    tflops = flops / (ms_flat * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": world * B * H / (ms_step * 1e-3), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": c["dtype"],
+        "data": "synthetic", "config": config_json(c, args.workload),
+        "queries_per_s": world * B / (ms_step * 1e-3),
+        "stages_ms": {"flat_lookup": ms_flat, "gather": ms_gather},
+        "roofline": {"kernel": "select_2sm_kernel, flat form (scoring of all N full keys and "
+                               "the exact top-k)", "bound": "tensor", "achieved": tflops,
+                     "peak": pk_["bf16"], "unit": "TFLOP/s", "frac": tflops / pk_["bf16"],
+                     "traffic": None, "peak_source": pk_["src"] + " bf16 burst"},
+        "flat_vs_factorised": {
+            "flat_lookup_ms": ms_flat, "factorised_lookup_ms": ms_fact,
+            "time_ratio": ms_flat / ms_fact,
+            "key_comparisons_per_query_head": {"flat": N, "factorised": 2 * n},
+            "comparison_ratio": N / (2 * n),
+            "page_counts": "the pages' worked example: 2048 subkey comparisons instead of "
+                           "10^6 at N = 10^6, k = 32",
+            "same_selection_frac": same,
+            "full_keys_ms": ms_keys, "full_keys_bytes": H * N * d_q * 2},
+        "e2e": {"value": world * B * H / e2e_s, "unit": UNIT,
+                "h2d_bytes_per_step": B * H * d_q * 2, "d2h_bytes_per_step": B * d_v * 4,
+                "calls_in_flight": 1},
+        # per step: select_2sm_kernel (flat form) and the value read
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        nthreads = os.cpu_count() or 1
+        sample = min(args.cpu_sample, 64, B)
+        inputs = cpu_inputs(c, sample, C=C_np, V=V_np)
+        t = cpu_oracle_time(c, inputs, sample, nthreads)
+        line["cpu_baseline"] = {
+            "value": sample * H / t, "unit": UNIT, "cores": nthreads, "kind": "oracle",
+            "sample": "%d of %d queries (all %d heads) of the %s workload, fp64 oracle brute "
+                      "force over all N full keys + value read" % (sample, B, H, args.workload)}
     if rank == 0:
         print(json.dumps(line), flush=True)
 

@@ -58,6 +58,12 @@ CONFIGS = {
     "page_train_sparse": dict(cfg_id=2, B=16384, H=4, d_q=1024, n_keys=1024, d_v=1024, k=32,
                               dtype="bf16", q_var=1.0, key_var=1.0 / 512, value_var=1.0 / 1024,
                               q_kind="normal", train=True, sparse_grad=True),
+    # the mid workload's inputs (same seed) searched flat: every query scored
+    # against all N = n_keys^2 materialised full keys (the search the
+    # factorisation replaces), then the same value read.
+    "mid_flat": dict(cfg_id=1, B=4096, H=4, d_q=512, n_keys=256, d_v=512, k=16, dtype="bf16",
+                     q_var=1.0, key_var=1.0 / 256, value_var=1.0 / 512, q_kind="normal",
+                     flat=True),
     # 16 GiB value table.
     "large": dict(cfg_id=4, B=32768, H=4, d_q=2048, n_keys=2048, d_v=2048, k=32, dtype="bf16",
                   q_var=1.0, key_var=1.0 / 1024, value_var=1.0 / 2048, q_kind="normal"),
