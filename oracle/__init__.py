@@ -49,6 +49,8 @@ def lib():
                                       vp, vp, vp, vp, vp, vp, vp, vp]
         L.oracle_query_net.argtypes = [vp, i32, vp, i32, i32, i32, i32, vp, vp, vp, vp,
                                        ctypes.c_double, vp, i32]
+        L.oracle_query_net_batch.argtypes = [vp, i32, vp, i32, i32, i32, i32, vp, vp,
+                                             ctypes.c_double, vp, vp, vp, i32]
         L.oracle_gather_fp8.argtypes = [vp, vp, i64, i32, i32, i32, i32, vp, vp, vp, i32]
         L.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
         L.oracle_e4m3_value.restype = ctypes.c_double
@@ -56,7 +58,7 @@ def lib():
         L.oracle_e4m3_encode.restype = ctypes.c_uint8
         for f in (L.oracle_lookup, L.oracle_gather, L.oracle_forward, L.oracle_brute_topk,
                   L.oracle_num_threads, L.oracle_quantize_fp8, L.oracle_gather_fp8,
-                  L.oracle_query_net, L.oracle_backward):
+                  L.oracle_query_net, L.oracle_query_net_batch, L.oracle_backward):
             f.restype = i32
         _lib = L
     return _lib
@@ -189,6 +191,21 @@ def query_net(x, weight, B, dim, F, gamma, beta, mean, var, eps, nthreads=0):
     if rc != 0:
         raise ValueError("oracle_query_net: bad shape")
     return q
+
+
+def query_net_batch(x, weight, B, dim, F, gamma, beta, eps, nthreads=0):
+    """q = BatchNorm1d(x W^T) normalised by the batch's own statistics (training
+    mode), in double.  Returns (q [B, F], batch mean [F], biased batch variance [F])."""
+    x, weight = _c(x), _c(weight)
+    g, bt = (np.ascontiguousarray(a, np.float32) for a in (gamma, beta))
+    q = np.empty((B, F), np.float64)
+    mean = np.empty(F, np.float64)
+    var = np.empty(F, np.float64)
+    rc = lib().oracle_query_net_batch(_p(x), _dt(x), _p(weight), _dt(weight), B, dim, F, _p(g),
+                                      _p(bt), float(eps), _p(q), _p(mean), _p(var), nthreads)
+    if rc != 0:
+        raise ValueError("oracle_query_net_batch: bad shape")
+    return q, mean, var
 
 
 def backward(q, subkeys, values, B, H, d_q, n_keys, d_v, k, idx, w, dout, dvalue_rows=None):

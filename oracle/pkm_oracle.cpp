@@ -406,6 +406,48 @@ int oracle_query_net(const void* x, int xdt, const void* w, int wdt, int B, int 
   return 0;
 }
 
+// The query network in training mode: q = BatchNorm1d(x W^T) normalised by
+// the statistics of the batch itself (Product-Key Memory, "Keeping the
+// memory in use": the BatchNorm over the queries, computed on the batch, is
+// a global constraint that spreads them over the key space; code listing:
+// Linear(dim, F, bias=False) then BatchNorm1d).  Per feature f: the batch
+// mean mu_f = sum_b z[b,f] / B and the biased variance var_f = sum_b (z[b,f]
+// - mu_f)^2 / B (two passes), then q = (z - mu_f) / sqrt(var_f + eps) *
+// gamma_f + beta_f.  mean_out / var_out (may be NULL) receive mu and var.
+int oracle_query_net_batch(const void* x, int xdt, const void* w, int wdt, int B, int dim, int F,
+                           const float* gamma, const float* beta, double eps, double* q,
+                           double* mean_out, double* var_out, int nthreads) {
+  if (B < 1 || dim < 1 || F < 1) return -1;
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(static)
+#endif
+  for (int64_t b = 0; b < B; ++b)
+    for (int f = 0; f < F; ++f) {
+      double z = 0.0;
+      for (int t = 0; t < dim; ++t)
+        z += widen(x, xdt, b * dim + t) * widen(w, wdt, (int64_t)f * dim + t);
+      q[b * F + f] = z;
+    }
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
+  for (int f = 0; f < F; ++f) {
+    double mu = 0.0;
+    for (int64_t b = 0; b < B; ++b) mu += q[b * F + f];
+    mu /= (double)B;
+    double var = 0.0;
+    for (int64_t b = 0; b < B; ++b) var += (q[b * F + f] - mu) * (q[b * F + f] - mu);
+    var /= (double)B;
+    const double inv = 1.0 / std::sqrt(var + eps);
+    for (int64_t b = 0; b < B; ++b)
+      q[b * F + f] = (q[b * F + f] - mu) * inv * (double)gamma[f] + (double)beta[f];
+    if (mean_out) mean_out[f] = mu;
+    if (var_out) var_out[f] = var;
+  }
+  return 0;
+}
+
 // Brute force over every full key: score(a, b') is ONE d_q-long dot product
 // of q[b,h] with concat(C[h,0,a], C[h,1,b']); all n^2 keys sorted by
 // (score desc, flat asc); first k kept.  Independent of the factorisation.

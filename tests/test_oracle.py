@@ -434,6 +434,61 @@ def test_query_net_closed_forms():
     assert (a == b).all()
 
 
+# The BatchNorm in training mode ("Product-Key Memory", "Keeping the memory in
+# use": the batch's own statistics normalise the queries).
+
+def test_query_net_batch_matches_torch_float64_train_mode():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(41)
+    B, dim, F, eps = 53, 40, 72, 1e-5
+    x = rng.standard_normal((B, dim)).astype(np.float32)
+    # features with a large common offset: the variance must not come from
+    # the difference of two large sums
+    x[:, 0] += 300.0
+    W = (rng.standard_normal((F, dim)) / np.sqrt(dim)).astype(np.float32)
+    gamma = (1 + 0.2 * rng.standard_normal(F)).astype(np.float32)
+    beta = (0.3 * rng.standard_normal(F)).astype(np.float32)
+    q, mean, var = oracle.query_net_batch(x, W, B, dim, F, gamma, beta, eps)
+    lin = torch.nn.Linear(dim, F, bias=False).double()
+    # momentum 1: the running statistics become the batch's (variance unbiased)
+    bn = torch.nn.BatchNorm1d(F, eps=eps, momentum=1.0).double().train()
+    with torch.no_grad():
+        lin.weight.copy_(torch.from_numpy(W.astype(np.float64)))
+        bn.weight.copy_(torch.from_numpy(gamma.astype(np.float64)))
+        bn.bias.copy_(torch.from_numpy(beta.astype(np.float64)))
+        ref = bn(lin(torch.from_numpy(x.astype(np.float64)))).numpy()
+    np.testing.assert_allclose(q, ref, rtol=1e-10, atol=1e-10)
+    np.testing.assert_allclose(mean, bn.running_mean.numpy(), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(var, bn.running_var.numpy() * (B - 1) / B, rtol=1e-10)
+
+
+def test_query_net_batch_invariants_and_special_cases():
+    rng = np.random.default_rng(42)
+    B, dim, F, eps = 31, 24, 40, 1e-3
+    x = rng.standard_normal((B, dim)).astype(np.float32)
+    W = rng.standard_normal((F, dim)).astype(np.float32)
+    W[5] = 0.0  # a constant (zero) feature
+    gamma = (rng.random(F) + 0.5).astype(np.float32)
+    beta = rng.standard_normal(F).astype(np.float32)
+    q, mean, var = oracle.query_net_batch(x, W, B, dim, F, gamma, beta, eps)
+    # every feature leaves with mean beta and biased variance
+    # gamma^2 var / (var + eps)
+    np.testing.assert_allclose(q.mean(0), beta.astype(np.float64), atol=1e-12)
+    want_var = gamma.astype(np.float64) ** 2 * var / (var + eps)
+    np.testing.assert_allclose(((q - q.mean(0)) ** 2).mean(0), want_var, rtol=1e-10, atol=1e-14)
+    # the constant feature: mean 0, variance 0, q = beta
+    assert mean[5] == 0.0 and var[5] == 0.0
+    assert (q[:, 5] == np.float64(beta[5])).all()
+    # B = 1: variance 0, every feature equals beta
+    q1, _, v1 = oracle.query_net_batch(x[:1], W, 1, dim, F, gamma, beta, eps)
+    assert (v1 == 0).all() and (q1[0] == beta.astype(np.float64)).all()
+    # two rows: mean and variance in closed form
+    z = x[:2].astype(np.float64) @ W.astype(np.float64).T
+    _, m2, v2 = oracle.query_net_batch(x[:2], W, 2, dim, F, gamma, beta, eps)
+    np.testing.assert_allclose(m2, (z[0] + z[1]) / 2, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(v2, ((z[0] - z[1]) / 2) ** 2, rtol=1e-12, atol=1e-13)
+
+
 # ------------------------------------------------------------------ backward
 #
 # The forward pass is differentiable for a fixed selection (the code listing's
