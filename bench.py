@@ -416,6 +416,30 @@ def run_ours(args, rank, world, local):
     # (query, head) pairs of the last timed lookup whose threshold hint missed
     # (their row tiles were selected again without it, inside the step)
     retried = pk.pkm_get_fallback_count(h) if bf16 else 0
+    ms_qbatch = None
+    if layer:
+        # the query network's other BatchNorm mode, timed on the same inputs:
+        # the batch's own statistics (two GEMM passes and the statistics)
+        qws = torch.empty(pk.pkm_query_net_batch_workspace_bytes(B, F), dtype=torch.uint8,
+                          device="cuda")
+        q_b = torch.empty_like(dq)
+
+        def qnet_batch():
+            pk.check(pk.pkm_query_net_batch(dx, dW, B, dim, F, bn_d[0], bn_d[1], c["bn_eps"],
+                                            qws, q_b, None, None, None, stream),
+                     "pkm_query_net_batch")
+        for _ in range(args.warmup):
+            qnet_batch()
+        qev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)]
+               for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.zero_()
+            qev[i][0].record(stream)
+            qnet_batch()
+            qev[i][1].record(stream)
+        torch.cuda.synchronize()
+        ms_qbatch = sum(e[0].elapsed_time(e[1]) for e in qev) / args.steps
+        del qws, q_b
     t_qnet = [e[0].elapsed_time(e[1]) for e in ev]
     t_lookup = [e[1].elapsed_time(e[2]) for e in ev]
     t_gather = [e[2].elapsed_time(e[3]) for e in ev]
@@ -638,6 +662,11 @@ def run_ours(args, rank, world, local):
             "achieved": qflops / (ms_qnet * 1e-3) / 1e12, "peak": pk_["bf16"], "unit": "TFLOP/s",
             "frac": qflops / (ms_qnet * 1e-3) / 1e12 / pk_["bf16"],
             "peak_source": pk_["src"] + " bf16 burst"}
+        line["query_net_modes_ms"] = {
+            "running_stats": ms_qnet, "batch_stats": ms_qbatch,
+            "batch_stats_note": "statistics pass (GEMM with column-statistics epilogue), fp64 "
+                                "combine, then the GEMM again with the folded scale and shift; "
+                                "timed after the steps, not part of them"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         nthreads = os.cpu_count() or 1
         sample = min(args.cpu_sample, B)

@@ -393,8 +393,11 @@ int pkm_quantize_values_fp8(const void *values, int value_dtype, int64_t N, int 
  * The query network ahead of the lookup (Product-Key Memory, code listing:
  * q = BatchNorm1d(Linear(dim, dim, bias=False)(x)); with H heads of width d_q
  * the Linear maps dim -> F = H * d_q features and q is the [B, H, d_q] query
- * of pkm_forward).  The BatchNorm is taken in its inference form, with
- * running statistics (the listing does not fix the mode).
+ * of pkm_forward).  The listing does not fix the BatchNorm's mode; both are
+ * provided: the inference form with running statistics (pkm_bn_fold +
+ * pkm_query_net) and the training form with the batch's own statistics
+ * (pkm_query_net_batch; Product-Key Memory, "Keeping the memory in use":
+ * the BatchNorm over the queries spreads them over the key space).
  *
  * pkm_bn_fold: scale[f] = gamma[f] / sqrt(var[f] + eps), shift[f] = beta[f] -
  * mean[f] * scale[f], fp32, f < F (device arrays; enqueued on `stream`).
@@ -413,6 +416,27 @@ int pkm_bn_fold(const float *gamma, const float *beta, const float *running_mean
                 void *stream);
 int pkm_query_net(const void *x, const void *weight, int B, int dim, int F, const float *scale,
                   const float *shift, void *q, int *status, void *stream);
+
+/*
+ * pkm_query_net_batch: the training form.  z = x W^T (bf16 in, fp32
+ * accumulation on the tensor cores); per feature f the batch mean mu[f] =
+ * sum_b z[b, f] / B and the biased variance var[f] = sum_b (z[b, f] -
+ * mu[f])^2 / B; q[b, f] = bf16_rn(z[b, f] * s[f] + t[f]) with s[f] =
+ * gamma[f] / sqrt(var[f] + eps) and t[f] = beta[f] - mu[f] * s[f].  The
+ * statistics come from 32-row blocks (each block's mean and sum of squared
+ * deviations, fp32) combined in fp64; z is computed twice (statistics, then
+ * q) and never stored.  batch_mean / batch_var: NULL, or device [F] fp32
+ * receiving mu and var (a running-statistics update would take the unbiased
+ * var * B / (B - 1)).  workspace: device scratch of
+ * pkm_query_net_batch_workspace_bytes(B, F) bytes (about 8 * F * B / 32),
+ * caller-owned, 16-byte aligned.  Shapes, alignment, status and errors as
+ * pkm_query_net's, and PKM_ERR_INVALID for eps < 0 or NaN, PKM_ERR_RANGE
+ * when (B + 31) / 32 * F exceeds 2^31 - 1.  B == 1 gives var = 0 (q = beta).
+ */
+size_t pkm_query_net_batch_workspace_bytes(int B, int F);
+int pkm_query_net_batch(const void *x, const void *weight, int B, int dim, int F,
+                        const float *gamma, const float *beta, float eps, void *workspace, void *q,
+                        float *batch_mean, float *batch_var, int *status, void *stream);
 
 #ifdef __cplusplus
 }

@@ -28,7 +28,8 @@ EXPORTED = ["pkm_create", "pkm_destroy", "pkm_forward", "pkm_lookup", "pkm_gathe
             "pkm_abi_version", "pkm_set_option", "pkm_get_fallback_count", "pkm_lookup_static",
             "pkm_quantize_values_fp8", "pkm_bn_fold", "pkm_query_net", "pkm_backward", "pkm_backward_read",
             "pkm_backward_scores", "pkm_forward_host_async", "pkm_backward_sparse",
-            "pkm_backward_read_sparse", "pkm_multicast_ok", "pkm_full_keys", "pkm_flat_lookup"]
+            "pkm_backward_read_sparse", "pkm_multicast_ok", "pkm_full_keys", "pkm_flat_lookup",
+            "pkm_query_net_batch", "pkm_query_net_batch_workspace_bytes"]
 PKM_STATIC_MAX_PAIRS = 1 << 16
 
 
@@ -88,6 +89,10 @@ def lib():
         L.pkm_backward_sparse.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp,
                                           vp, vp, vp, vp]
         L.pkm_full_keys.argtypes = [vp, vp, i32, i32, vp, vp]
+        L.pkm_query_net_batch.argtypes = [vp, vp, i32, i32, i32, vp, vp, ctypes.c_float, vp, vp,
+                                          vp, vp, vp, vp]
+        L.pkm_query_net_batch_workspace_bytes.argtypes = [i32, i32]
+        L.pkm_query_net_batch_workspace_bytes.restype = ctypes.c_size_t
         L.pkm_flat_lookup.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp]
         L.pkm_backward_read_sparse.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp,
                                                vp, vp, vp]
@@ -96,7 +101,8 @@ def lib():
                   "pkm_get_fallback_count", "pkm_lookup_static", "pkm_quantize_values_fp8",
                   "pkm_bn_fold", "pkm_query_net", "pkm_backward", "pkm_backward_read",
                   "pkm_backward_scores", "pkm_forward_host_async", "pkm_backward_sparse",
-                  "pkm_backward_read_sparse", "pkm_full_keys", "pkm_flat_lookup"):
+                  "pkm_backward_read_sparse", "pkm_full_keys", "pkm_flat_lookup",
+                  "pkm_query_net_batch"):
             getattr(L, f).restype = i32
         _lib = L
     return _lib
@@ -260,6 +266,19 @@ def pkm_lookup_static(q, subkeys, B, H, d_q, n_keys, k, idx, w, status=None, str
     """The bf16 lookup without a handle or any device allocation (see include/pkm.h)."""
     return lib().pkm_lookup_static(_addr(q), _addr(subkeys), B, H, d_q, n_keys, k, _addr(idx),
                                    _addr(w), _addr(status), _stream(stream))
+
+
+def pkm_query_net_batch_workspace_bytes(B, F):
+    return int(lib().pkm_query_net_batch_workspace_bytes(B, F))
+
+
+def pkm_query_net_batch(x, weight, B, dim, F, gamma, beta, eps, workspace, q, batch_mean=None,
+                        batch_var=None, status=None, stream=None):
+    """The query network with the batch's own BatchNorm statistics (see include/pkm.h)."""
+    return lib().pkm_query_net_batch(_addr(x), _addr(weight), B, dim, F, _addr(gamma),
+                                     _addr(beta), float(eps), _addr(workspace), _addr(q),
+                                     _addr(batch_mean), _addr(batch_var), _addr(status),
+                                     _stream(stream))
 
 
 def pkm_quantize_values_fp8(values, value_dtype, N, d_v, out, stream=None):

@@ -23,6 +23,14 @@ cudaError_t launch_bn_fold(const float* gamma, const float* beta, const float* m
 cudaError_t launch_qnet(const uint16_t* x, const uint16_t* w, int B, int dim, int F,
                         const float* scale, const float* shift, uint16_t* q, int* status,
                         cudaStream_t stream);
+// The training form: q normalised by the batch's own per-feature mean and
+// biased variance (two GEMM passes, see qnet.cu); workspace of
+// qnet_batch_workspace_bytes(B, F); batch_mean / batch_var may be NULL.
+size_t qnet_batch_workspace_bytes(int B, int F);
+cudaError_t launch_qnet_batch(const uint16_t* x, const uint16_t* w, int B, int dim, int F,
+                              const float* gamma, const float* beta, float eps, void* workspace,
+                              uint16_t* q, float* batch_mean, float* batch_var, int* status,
+                              cudaStream_t stream);
 
 // Backward pass for a fixed selection (backward.cu), in two parts.
 // Read part: dw = dout . V[idx] (overwritten) and the value-table gradient,

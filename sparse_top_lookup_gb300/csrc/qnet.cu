@@ -1,13 +1,21 @@
-// The query network ahead of the lookup: q = BatchNorm1d(x W^T), eval mode.
+// The query network ahead of the lookup: q = BatchNorm1d(x W^T).
 //
 // Product-Key Memory, code listing (module setup and forward): the query is
 // an nn.Linear(dim, dim, bias=False) of the layer input followed by an
-// nn.BatchNorm1d, a global constraint on the query distribution.  With H
-// heads of width d_q the Linear maps dim -> F = H * d_q features (one head
-// in the listing).  The listing leaves the BatchNorm mode open; this is the
-// inference form: per feature f, q = (z - mean[f]) / sqrt(var[f] + eps) *
-// gamma[f] + beta[f] with the running statistics, folded into
-// q = z * scale[f] + shift[f] (bn_fold_kernel).
+// nn.BatchNorm1d, a global constraint on the query distribution ("Keeping
+// the memory in use").  With H heads of width d_q the Linear maps dim -> F =
+// H * d_q features (one head in the listing).  The listing leaves the
+// BatchNorm mode open; both are built:
+//   inference form: per feature f, q = (z - mean[f]) / sqrt(var[f] + eps) *
+//     gamma[f] + beta[f] with the running statistics, folded into
+//     q = z * scale[f] + shift[f] (bn_fold_kernel);
+//   training form: mean[f] and the biased variance var[f] of z over the
+//     batch itself.  A first GEMM pass (kStats) writes, per 32-row block and
+//     feature, the block's mean and its sum of squared deviations from it
+//     (warp transpose-reduce in the epilogue; z is not stored); the blocks
+//     are combined by the parallel-variance formula in fp64
+//     (bn_batch_finalize_kernel) into scale / shift; the GEMM runs again with
+//     them (the same tiles and MMA order: identical z).
 //
 // GEMM z = x W^T on the tcgen05 tensor cores, bf16 in, fp32 accumulate, one
 // persistent CTA per SM over 128 x 256 output tiles:
@@ -42,6 +50,59 @@ constexpr int QSTAGE_BYTES = QA_BYTES + QB_BYTES;
 constexpr int QSMEM = QSTAGES * QSTAGE_BYTES + 1024;  // + alignment slack
 constexpr int QTHREADS = 192;
 
+// One warp per feature: the 32-row blocks' (mean, squared-deviation sum)
+// combined in fp64 (lane l takes blocks l, l + 32, ..., then a shuffle tree),
+// by the parallel form of the variance: joining (n_a, m_a, M_a) and (n_b,
+// m_b, M_b) gives n = n_a + n_b, m = m_a + (m_b - m_a) n_b / n and M = M_a +
+// M_b + (m_b - m_a)^2 n_a n_b / n.  var = M / B (biased); scale / shift fold
+// gamma and beta as in bn_fold_kernel; batch_mean / batch_var may be NULL.
+__global__ void bn_batch_finalize_kernel(const float* __restrict__ part_mean,
+                                         const float* __restrict__ part_m2, int B, int F,
+                                         const float* __restrict__ gamma,
+                                         const float* __restrict__ beta, float eps,
+                                         float* __restrict__ scale, float* __restrict__ shift,
+                                         float* __restrict__ batch_mean,
+                                         float* __restrict__ batch_var) {
+  const int lane = threadIdx.x & 31;
+  const int f = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (f >= F) return;  // whole warp
+  const int blocks = (B + 31) / 32;
+  double n = 0.0, m = 0.0, M = 0.0;
+  for (int k = lane; k < blocks; k += 32) {
+    const double nb = (double)min(32, B - 32 * k);
+    const double mb = part_mean[(size_t)k * F + f], Mb = part_m2[(size_t)k * F + f];
+    const double nn = n + nb, d = mb - m;
+    m += d * nb / nn;
+    M += Mb + d * d * n * nb / nn;
+    n = nn;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const double n2 = __shfl_xor_sync(0xffffffffu, n, o);
+    const double m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const double M2 = __shfl_xor_sync(0xffffffffu, M, o);
+    const double nn = n + n2;
+    if (nn > 0.0) {
+      const double d = m2 - m;
+      // the same expression in both lanes of a pair (operands in lane order)
+      const bool lo = (lane & o) == 0;
+      const double na = lo ? n : n2, nbb = lo ? n2 : n, ma = lo ? m : m2;
+      const double Ma = lo ? M : M2, Mb = lo ? M2 : M, dd = lo ? d : -d;
+      m = ma + dd * nbb / nn;
+      M = Ma + Mb + dd * dd * na * nbb / nn;
+      n = nn;
+    }
+  }
+  if (lane == 0) {
+    const double var = M / (double)B;
+    const double s = (double)gamma[f] / sqrt(var + (double)eps);
+    scale[f] = (float)s;
+    shift[f] = (float)((double)beta[f] - m * s);
+    if (batch_mean) batch_mean[f] = (float)m;
+    if (batch_var) batch_var[f] = (float)var;
+  }
+}
+
 __global__ void bn_fold_kernel(const float* __restrict__ gamma, const float* __restrict__ beta,
                                const float* __restrict__ mean, const float* __restrict__ var,
                                float eps, int F, float* __restrict__ scale,
@@ -60,12 +121,34 @@ __global__ void bn_fold_kernel(const float* __restrict__ gamma, const float* __r
 // once both CTAs' MMAs have read it (each MMA's release commit arrives on
 // both CTAs' empty barriers).  A CTA whose row tile is past the batch loads
 // zero-filled x rows for its partner's sake and stores nothing.
-template <bool kPair>
+// Sum over the warp's 32 lanes of each of 32 values: on return lane j holds
+// the sum of every lane's a[j] (31 shuffles: each step halves the values a
+// lane holds, the pair of lanes keeping complementary halves).
+__device__ __forceinline__ float transpose_sum32(float (&a)[32], int lane) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    const bool up = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < off; ++i) {
+      const float send = up ? a[i] : a[i + off];
+      const float keep = up ? a[i + off] : a[i];
+      a[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+  }
+  return a[0];
+}
+
+// kStats: the epilogue writes column statistics instead of q: for the 32
+// rows of each epilogue warp (block tm * 4 + quad) and each feature f, the
+// mean of the block's rows inside the batch and the sum of their squared
+// deviations from it, at part_mean / part_m2 [block][F].
+template <bool kPair, bool kStats>
 __global__ void __launch_bounds__(QTHREADS, 1)
 qnet_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
             const __grid_constant__ CUtensorMap tmap_w_half, int B, int F, int dim,
             const float* __restrict__ scale, const float* __restrict__ shift,
-            __nv_bfloat16* __restrict__ q, int* __restrict__ status) {
+            __nv_bfloat16* __restrict__ q, float* __restrict__ part_mean,
+            float* __restrict__ part_m2, int* __restrict__ status) {
   extern __shared__ unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t bars[2 * QSTAGES + 4 + 1];
   __shared__ uint32_t s_tmem_base;
@@ -207,6 +290,27 @@ qnet_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         if (c0 >= F) break;  // F is a multiple of 32: a group is all in or all out
         float v[32];
         tmem_ld32(lane_addr + buf * QN + g, v);
+        if constexpr (kStats) {
+          const bool in = b < B;
+          const int nb = __popc(__ballot_sync(0xffffffffu, in));  // the block's rows in the batch
+          if (nb == 0) continue;  // warp-uniform: a block past the batch writes nothing
+          float a[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) a[j] = in ? v[j] : 0.0f;
+          const float mean = transpose_sum32(a, lane) / (float)nb;  // column c0 + lane
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            // every lane takes part in the broadcast, in the block or not
+            const float mj = __shfl_sync(0xffffffffu, mean, j);
+            const float d = in ? v[j] - mj : 0.0f;
+            a[j] = d * d;
+          }
+          const float m2 = transpose_sum32(a, lane);
+          const size_t o = (size_t)(tm * 4 + quad) * F + c0 + lane;
+          part_mean[o] = mean;
+          part_m2[o] = m2;
+          continue;
+        }
         const float4* sc4 = reinterpret_cast<const float4*>(scale + c0);
         const float4* sh4 = reinterpret_cast<const float4*>(shift + c0);
         uint32_t packed[16];
@@ -255,10 +359,14 @@ cudaError_t launch_bn_fold(const float* gamma, const float* beta, const float* m
   return cudaGetLastError();
 }
 
-cudaError_t launch_qnet(const uint16_t* x, const uint16_t* w, int B, int dim, int F,
-                        const float* scale, const float* shift, uint16_t* q, int* status,
-                        cudaStream_t stream) {
-  if (B == 0) return cudaSuccess;
+namespace {
+
+// The GEMM z = x W^T with either epilogue: q = z * scale + shift (bf16), or
+// (kStats) the per-block column statistics.
+template <bool kStats>
+cudaError_t launch_qnet_gemm(const uint16_t* x, const uint16_t* w, int B, int dim, int F,
+                             const float* scale, const float* shift, uint16_t* q,
+                             float* part_mean, float* part_m2, int* status, cudaStream_t stream) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   CUtensorMap mx, mw, mwh;
@@ -295,10 +403,11 @@ cudaError_t launch_qnet(const uint16_t* x, const uint16_t* w, int B, int dim, in
   // x and W are this device's memory: the slabs are multicast)
   const void* const operands[2] = {x, w};
   if (tm_count >= 2 && buffers_on_this_device(operands, 2)) {
+    auto kernel = qnet_kernel<true, kStats>;
     static bool attr_set = false;
     if (!attr_set) {
-      cudaError_t e = cudaFuncSetAttribute(qnet_kernel<true>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, QSMEM);
+      cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           QSMEM);
       if (e != cudaSuccess) return e;
       attr_set = true;
     }
@@ -316,27 +425,68 @@ cudaError_t launch_qnet(const uint16_t* x, const uint16_t* w, int B, int dim, in
     static int max_clusters = 0;
     if (!max_clusters) {
       cfg.gridDim = dim3(2 * (sm_count() / 2));
-      cudaError_t e = cudaOccupancyMaxActiveClusters(&max_clusters, qnet_kernel<true>, &cfg);
+      cudaError_t e = cudaOccupancyMaxActiveClusters(&max_clusters, kernel, &cfg);
       if (e != cudaSuccess) return e;
       if (max_clusters < 1) return cudaErrorInvalidConfiguration;
     }
     const int pair_tiles = (tm_count + 1) / 2 * tn_count;
     cfg.gridDim = dim3(2 * (pair_tiles < max_clusters ? pair_tiles : max_clusters));
-    return cudaLaunchKernelEx(&cfg, qnet_kernel<true>, mx, mw, mwh, B, F, dim, scale, shift, q16,
-                              status);
+    return cudaLaunchKernelEx(&cfg, kernel, mx, mw, mwh, B, F, dim, scale, shift, q16, part_mean,
+                              part_m2, status);
   }
+  auto kernel = qnet_kernel<false, kStats>;
   static bool attr_set1 = false;
   if (!attr_set1) {
     cudaError_t e =
-        cudaFuncSetAttribute(qnet_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, QSMEM);
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, QSMEM);
     if (e != cudaSuccess) return e;
     attr_set1 = true;
   }
   const int tiles = tm_count * tn_count;
   const int grid = tiles < sm_count() ? tiles : sm_count();
-  qnet_kernel<false><<<grid, QTHREADS, QSMEM, stream>>>(mx, mw, mwh, B, F, dim, scale, shift, q16,
-                                                        status);
+  kernel<<<grid, QTHREADS, QSMEM, stream>>>(mx, mw, mwh, B, F, dim, scale, shift, q16, part_mean,
+                                           part_m2, status);
   return cudaGetLastError();
+}
+
+size_t align256(size_t v) { return (v + 255) / 256 * 256; }
+
+}  // namespace
+
+cudaError_t launch_qnet(const uint16_t* x, const uint16_t* w, int B, int dim, int F,
+                        const float* scale, const float* shift, uint16_t* q, int* status,
+                        cudaStream_t stream) {
+  if (B == 0) return cudaSuccess;
+  return launch_qnet_gemm<false>(x, w, B, dim, F, scale, shift, q, nullptr, nullptr, status,
+                                 stream);
+}
+
+size_t qnet_batch_workspace_bytes(int B, int F) {
+  const size_t blocks = ((size_t)B + 31) / 32;
+  return 2 * align256(blocks * F * 4) + 2 * align256((size_t)F * 4);
+}
+
+cudaError_t launch_qnet_batch(const uint16_t* x, const uint16_t* w, int B, int dim, int F,
+                              const float* gamma, const float* beta, float eps, void* workspace,
+                              uint16_t* q, float* batch_mean, float* batch_var, int* status,
+                              cudaStream_t stream) {
+  if (B == 0) return cudaSuccess;
+  const size_t blocks = ((size_t)B + 31) / 32;
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  float* part_mean = reinterpret_cast<float*>(ws);
+  float* part_m2 = reinterpret_cast<float*>(ws + align256(blocks * F * 4));
+  float* scale = reinterpret_cast<float*>(ws + 2 * align256(blocks * F * 4));
+  float* shift = scale + align256((size_t)F * 4) / 4;
+  cudaError_t e = launch_qnet_gemm<true>(x, w, B, dim, F, nullptr, nullptr, nullptr, part_mean,
+                                         part_m2, status, stream);
+  if (e != cudaSuccess) return e;
+  bn_batch_finalize_kernel<<<(F + 7) / 8, 256, 0, stream>>>(part_mean, part_m2, B, F, gamma, beta,
+                                                            eps, scale, shift, batch_mean,
+                                                            batch_var);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_qnet_gemm<false>(x, w, B, dim, F, scale, shift, q, nullptr, nullptr, status,
+                                 stream);
 }
 
 }  // namespace pkm
@@ -355,6 +505,37 @@ extern "C" int pkm_bn_fold(const float* gamma, const float* beta, const float* r
     return PKM_ERR_INVALID;
   return pkm::launch_bn_fold(gamma, beta, running_mean, running_var, eps, F, scale, shift,
                              static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PKM_OK
+             : PKM_ERR_CUDA;
+}
+
+extern "C" size_t pkm_query_net_batch_workspace_bytes(int B, int F) {
+  if (B < 0 || F < 1) return 0;
+  return pkm::qnet_batch_workspace_bytes(B, F);
+}
+
+extern "C" int pkm_query_net_batch(const void* x, const void* weight, int B, int dim, int F,
+                                   const float* gamma, const float* beta, float eps,
+                                   void* workspace, void* q, float* batch_mean, float* batch_var,
+                                   int* status, void* stream) {
+  if (B < 0 || dim < 1 || F < 1 || !(eps >= 0.0f)) return PKM_ERR_INVALID;
+  if (dim % 16 || F % 32) return PKM_ERR_UNSUPPORTED;
+  if ((int64_t)(B + 31) / 32 * F > INT32_MAX) return PKM_ERR_RANGE;
+  if (B == 0) return PKM_OK;
+  if (!x || !weight || !gamma || !beta || !workspace || !q) return PKM_ERR_INVALID;
+  if (!qnet_aligned16(x) || !qnet_aligned16(weight) || !qnet_aligned16(workspace) ||
+      !qnet_aligned16(q))
+    return PKM_ERR_ALIGN;
+  int* st = status;
+  if (!st) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_qnet_status) != cudaSuccess) return PKM_ERR_CUDA;
+    st = static_cast<int*>(p);
+  }
+  return pkm::launch_qnet_batch(static_cast<const uint16_t*>(x),
+                                static_cast<const uint16_t*>(weight), B, dim, F, gamma, beta, eps,
+                                workspace, static_cast<uint16_t*>(q), batch_mean, batch_var, st,
+                                static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? PKM_OK
              : PKM_ERR_CUDA;
 }
