@@ -45,8 +45,14 @@ struct MergeLayout {
   // (slots [0, KL)) and pair codes (slots [KL, 2KL)).  Every use keeps a
   // thread inside its own column, so warps in different phases never touch
   // each other's slots.
-  static constexpr int kRegionA = (kRest > 2 * KL ? kRest : 2 * KL) * 4 * kThreads;
-  static constexpr int kRegionC = kRegionA + 2 * KL * 2 * kThreads;  // after the lists' subkeys
+  // First, in the first pass, it holds the CTA's lists as loaded, [pair][2KL
+  // + 4] floats (rows 16-byte aligned; the +4 spreads rows over banks).
+  static constexpr int kSlotsA = kRest > 2 * KL + 4 ? kRest : 2 * KL + 4;
+  static constexpr int kRegionA = kSlotsA * 4 * kThreads;
+  // the lists' subkeys, [pair][2KL + 2] 16-bit (odd word stride: a thread's
+  // own row and the cooperative fill are both free of bank conflicts)
+  static constexpr int kCodeRow = 2 * KL + 2;
+  static constexpr int kRegionC = kRegionA + (kCodeRow * 2 * kThreads + 15) / 16 * 16;
   // region C, [place][thread]: the survivors' pair codes by output place
   static constexpr int kBytes = kRegionC + KL * 4 * kThreads;
 };
@@ -65,7 +71,7 @@ __device__ __forceinline__ void merge_cta(const float* __restrict__ list_v,
   float* stg = reinterpret_cast<float*>(smem);                                  // [kRest][T]
   float* sv = reinterpret_cast<float*>(smem);                                   // [KL][T]
   uint32_t* sp = reinterpret_cast<uint32_t*>(sv + KL * kThreads);               // [KL][T]
-  unsigned short* sc = reinterpret_cast<unsigned short*>(smem + Lay::kRegionA); // [2KL][T]
+  unsigned short* sc = reinterpret_cast<unsigned short*>(smem + Lay::kRegionA); // [T][2KL+2]
   uint32_t* so = reinterpret_cast<uint32_t*>(smem + Lay::kRegionC);             // [KL][T]
   const int t = threadIdx.x;
   int pair;
@@ -84,9 +90,42 @@ __device__ __forceinline__ void merge_cta(const float* __restrict__ list_v,
   }
 
   const float* v1 = list_v + (size_t)(valid ? pair : 0) * 2 * KL;
-  const unsigned short* c1 = list_c + (size_t)(valid ? pair : 0) * 2 * KL;
+  unsigned short* my_sc = sc + t * Lay::kCodeRow;
   float s1v[KL], s2v[KL];
-  {
+  if (!retry_pass) {
+    // the CTA's pairs are consecutive, so are their lists: coalesced 16-byte
+    // loads by the whole CTA into shared memory, then each thread takes its
+    // own row (a thread's own lists are 256 + 128 scattered bytes apart from
+    // its neighbours')
+    constexpr int kRowV = 2 * KL + 4;
+    const int pair0 = cta * kThreads;
+    const int np = min(kThreads, B * H - pair0);
+    const float4* gv = reinterpret_cast<const float4*>(list_v + (size_t)pair0 * 2 * KL);
+    for (int q = t; q < np * (KL / 2); q += kThreads) {
+      const int p = q / (KL / 2), s4 = q - p * (KL / 2);
+      *reinterpret_cast<float4*>(stg + p * kRowV + 4 * s4) = gv[q];
+    }
+    const uint4* gc = reinterpret_cast<const uint4*>(list_c + (size_t)pair0 * 2 * KL);
+    uint32_t* sc32 = reinterpret_cast<uint32_t*>(sc);
+    for (int q = t; q < np * (KL / 4); q += kThreads) {
+      const int p = q / (KL / 4), m = q - p * (KL / 4);
+      const uint4 u = gc[q];
+      uint32_t* d = sc32 + p * (Lay::kCodeRow / 2) + 4 * m;
+      d[0] = u.x;
+      d[1] = u.y;
+      d[2] = u.z;
+      d[3] = u.w;
+    }
+    __syncthreads();
+    const float4* r4 = reinterpret_cast<const float4*>(stg + t * kRowV);
+#pragma unroll
+    for (int i = 0; i < KL / 4; ++i) {
+      const float4 a = r4[i], b = r4[KL / 4 + i];
+      s1v[4 * i] = a.x; s1v[4 * i + 1] = a.y; s1v[4 * i + 2] = a.z; s1v[4 * i + 3] = a.w;
+      s2v[4 * i] = b.x; s2v[4 * i + 1] = b.y; s2v[4 * i + 2] = b.z; s2v[4 * i + 3] = b.w;
+    }
+    __syncthreads();  // region A is reused below
+  } else {
     const float4* g = reinterpret_cast<const float4*>(v1);
 #pragma unroll
     for (int i = 0; i < KL / 4; ++i) {
@@ -94,19 +133,18 @@ __device__ __forceinline__ void merge_cta(const float* __restrict__ list_v,
       s1v[4 * i] = a.x; s1v[4 * i + 1] = a.y; s1v[4 * i + 2] = a.z; s1v[4 * i + 3] = a.w;
       s2v[4 * i] = b.x; s2v[4 * i + 1] = b.y; s2v[4 * i + 2] = b.z; s2v[4 * i + 3] = b.w;
     }
-    const uint4* gc = reinterpret_cast<const uint4*>(c1);
+    const uint4* gc = reinterpret_cast<const uint4*>(list_c + (size_t)(valid ? pair : 0) * 2 * KL);
+    uint32_t* my32 = reinterpret_cast<uint32_t*>(my_sc);
 #pragma unroll
-    for (int i = 0; i < 2 * KL / 8; ++i) {
+    for (int i = 0; i < KL / 4; ++i) {
       const uint4 u = gc[i];
-      const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        sc[(8 * i + 2 * q) * kThreads + t] = (unsigned short)(wv[q] & 0xffffu);
-        sc[(8 * i + 2 * q + 1) * kThreads + t] = (unsigned short)(wv[q] >> 16);
-      }
+      my32[4 * i] = u.x;
+      my32[4 * i + 1] = u.y;
+      my32[4 * i + 2] = u.z;
+      my32[4 * i + 3] = u.w;
     }
   }
-  const bool bad1 = sc[t] == 0xffffu, bad2 = sc[KL * kThreads + t] == 0xffffu;
+  const bool bad1 = my_sc[0] == 0xffffu, bad2 = my_sc[KL] == 0xffffu;
   if (valid && (bad1 || bad2) && !retry_pass) {  // without the hint every list is complete
     atomicAdd(&retry.counts[0], 1);
     const int b = pair / H, h = pair - (pair / H) * H;
@@ -120,8 +158,8 @@ __device__ __forceinline__ void merge_cta(const float* __restrict__ list_v,
 #pragma unroll
     for (int i = 0; i < KL; ++i) s1v[i] = s2v[i] = 0.0f;
   }
-  auto col1 = [&](int i) { return (int)sc[i * kThreads + t]; };
-  auto col2 = [&](int j) { return (int)sc[(KL + j) * kThreads + t]; };
+  auto col1 = [&](int i) { return (int)my_sc[i]; };
+  auto col2 = [&](int j) { return (int)my_sc[KL + j]; };
 
   // V: the sorted KL best sums.  Row 0 of the candidate grid is already in
   // descending order; row 1 is too, and one bitonic merge takes it in.
