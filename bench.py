@@ -664,9 +664,10 @@ def run_ours(args, rank, world, local):
             "peak_source": pk_["src"] + " bf16 burst"}
         line["query_net_modes_ms"] = {
             "running_stats": ms_qnet, "batch_stats": ms_qbatch,
-            "batch_stats_note": "statistics pass (GEMM with column-statistics epilogue), fp64 "
-                                "combine, then the GEMM again with the folded scale and shift; "
-                                "timed after the steps, not part of them"}
+            "batch_stats_note": "statistics pass (GEMM with column-statistics epilogue), the "
+                                "blocks joined by the law of total variance, then the GEMM "
+                                "again with the folded scale and shift; timed after the steps, "
+                                "not part of them"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         nthreads = os.cpu_count() or 1
         sample = min(args.cpu_sample, B)

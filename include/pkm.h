@@ -424,7 +424,7 @@ int pkm_query_net(const void *x, const void *weight, int B, int dim, int F, cons
  * mu[f])^2 / B; q[b, f] = bf16_rn(z[b, f] * s[f] + t[f]) with s[f] =
  * gamma[f] / sqrt(var[f] + eps) and t[f] = beta[f] - mu[f] * s[f].  The
  * statistics come from 32-row blocks (each block's mean and sum of squared
- * deviations, fp32) combined in fp64; z is computed twice (statistics, then
+ * deviations, fp32) joined in fp32 by the law of total variance; z is computed twice (statistics, then
  * q) and never stored.  batch_mean / batch_var: NULL, or device [F] fp32
  * receiving mu and var (a running-statistics update would take the unbiased
  * var * B / (B - 1)).  workspace: device scratch of

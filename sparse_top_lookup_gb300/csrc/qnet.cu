@@ -13,8 +13,8 @@
 //     batch itself.  A first GEMM pass (kStats) writes, per 32-row block and
 //     feature, the block's mean and its sum of squared deviations from it
 //     (warp transpose-reduce in the epilogue; z is not stored); the blocks
-//     are combined by the parallel-variance formula in fp64
-//     (bn_batch_finalize_kernel) into scale / shift; the GEMM runs again with
+//     are joined by the law of total variance (bn_batch_finalize_kernel)
+//     into scale / shift; the GEMM runs again with
 //     them (the same tiles and MMA order: identical z).
 //
 // GEMM z = x W^T on the tcgen05 tensor cores, bf16 in, fp32 accumulate, one
@@ -50,56 +50,98 @@ constexpr int QSTAGE_BYTES = QA_BYTES + QB_BYTES;
 constexpr int QSMEM = QSTAGES * QSTAGE_BYTES + 1024;  // + alignment slack
 constexpr int QTHREADS = 192;
 
-// One warp per feature: the 32-row blocks' (mean, squared-deviation sum)
-// combined in fp64 (lane l takes blocks l, l + 32, ..., then a shuffle tree),
-// by the parallel form of the variance: joining (n_a, m_a, M_a) and (n_b,
-// m_b, M_b) gives n = n_a + n_b, m = m_a + (m_b - m_a) n_b / n and M = M_a +
-// M_b + (m_b - m_a)^2 n_a n_b / n.  var = M / B (biased); scale / shift fold
-// gamma and beta as in bn_fold_kernel; batch_mean / batch_var may be NULL.
-__global__ void bn_batch_finalize_kernel(const float* __restrict__ part_mean,
-                                         const float* __restrict__ part_m2, int B, int F,
-                                         const float* __restrict__ gamma,
-                                         const float* __restrict__ beta, float eps,
-                                         float* __restrict__ scale, float* __restrict__ shift,
-                                         float* __restrict__ batch_mean,
-                                         float* __restrict__ batch_var) {
-  const int lane = threadIdx.x & 31;
-  const int f = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (f >= F) return;  // whole warp
+// The 32-row blocks' (mean m_b, squared-deviation sum M_b, row count n_b)
+// joined by the law of total variance, in two passes over the blocks: mu =
+// sum_b n_b m_b / B, then M = sum_b (M_b + n_b (m_b - mu)^2) and var = M / B
+// (biased; every term of the second sum is >= 0, so nothing cancels).  A CTA
+// takes 32 consecutive features (one per lane: coalesced reads) and its 32
+// warps split the blocks, four independent loads in flight per thread; fp32
+// with four accumulators per thread, joined in shared memory.  scale / shift fold gamma and beta as in bn_fold_kernel;
+// batch_mean / batch_var may be NULL.
+constexpr int kFinWarps = 32;
+
+__global__ void __launch_bounds__(kFinWarps * 32)
+bn_batch_finalize_kernel(const float* __restrict__ part_mean, const float* __restrict__ part_m2,
+                         int B, int F, const float* __restrict__ gamma,
+                         const float* __restrict__ beta, float eps, float* __restrict__ scale,
+                         float* __restrict__ shift, float* __restrict__ batch_mean,
+                         float* __restrict__ batch_var) {
+  __shared__ float s_part[kFinWarps][4][32];
+  __shared__ float s_mu[32];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int f = blockIdx.x * 32 + lane;
+  const bool in = f < F;
   const int blocks = (B + 31) / 32;
-  double n = 0.0, m = 0.0, M = 0.0;
-  for (int k = lane; k < blocks; k += 32) {
-    const double nb = (double)min(32, B - 32 * k);
-    const double mb = part_mean[(size_t)k * F + f], Mb = part_m2[(size_t)k * F + f];
-    const double nn = n + nb, d = mb - m;
-    m += d * nb / nn;
-    M += Mb + d * d * n * nb / nn;
-    n = nn;
-  }
+  auto count = [&](int k) { return (float)min(32, B - 32 * k); };
+  // pass 1: sum_b n_b m_b (blocks wid + kFinWarps * (4 i + r) to accumulator r)
+  float a[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  for (int k0 = wid; k0 < blocks; k0 += 4 * kFinWarps) {
+    float m[4];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const double n2 = __shfl_xor_sync(0xffffffffu, n, o);
-    const double m2 = __shfl_xor_sync(0xffffffffu, m, o);
-    const double M2 = __shfl_xor_sync(0xffffffffu, M, o);
-    const double nn = n + n2;
-    if (nn > 0.0) {
-      const double d = m2 - m;
-      // the same expression in both lanes of a pair (operands in lane order)
-      const bool lo = (lane & o) == 0;
-      const double na = lo ? n : n2, nbb = lo ? n2 : n, ma = lo ? m : m2;
-      const double Ma = lo ? M : M2, Mb = lo ? M2 : M, dd = lo ? d : -d;
-      m = ma + dd * nbb / nn;
-      M = Ma + Mb + dd * dd * na * nbb / nn;
-      n = nn;
+    for (int r = 0; r < 4; ++r) {
+      const int k = k0 + r * kFinWarps;
+      m[r] = in && k < blocks ? part_mean[(size_t)k * F + f] : 0.0f;
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int k = k0 + r * kFinWarps;
+      if (k < blocks) a[r] = fmaf(count(k), m[r], a[r]);
     }
   }
-  if (lane == 0) {
-    const double var = M / (double)B;
-    const double s = (double)gamma[f] / sqrt(var + (double)eps);
-    scale[f] = (float)s;
-    shift[f] = (float)((double)beta[f] - m * s);
-    if (batch_mean) batch_mean[f] = (float)m;
-    if (batch_var) batch_var[f] = (float)var;
+#pragma unroll
+  for (int r = 0; r < 4; ++r) s_part[wid][r][lane] = a[r];
+  __syncthreads();
+  if (wid == 0) {
+    float t = 0.0f;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      float u = 0.0f;
+#pragma unroll
+      for (int w = 0; w < kFinWarps; ++w) u += s_part[w][r][lane];
+      t += u;
+    }
+    s_mu[lane] = t / (float)B;
+  }
+  __syncthreads();
+  const float mu = s_mu[lane];
+  // pass 2: sum_b (M_b + n_b (m_b - mu)^2)
+#pragma unroll
+  for (int r = 0; r < 4; ++r) a[r] = 0.0f;
+  for (int k0 = wid; k0 < blocks; k0 += 4 * kFinWarps) {
+    float m[4], q[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int k = k0 + r * kFinWarps;
+      const bool ok = in && k < blocks;
+      m[r] = ok ? part_mean[(size_t)k * F + f] : mu;
+      q[r] = ok ? part_m2[(size_t)k * F + f] : 0.0f;
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int k = k0 + r * kFinWarps;
+      const float d = m[r] - mu;
+      if (k < blocks) a[r] += fmaf(count(k) * d, d, q[r]);
+    }
+  }
+  __syncthreads();  // pass 1's partial sums have been read
+#pragma unroll
+  for (int r = 0; r < 4; ++r) s_part[wid][r][lane] = a[r];
+  __syncthreads();
+  if (wid == 0 && in) {
+    float M = 0.0f;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      float u = 0.0f;
+#pragma unroll
+      for (int w = 0; w < kFinWarps; ++w) u += s_part[w][r][lane];
+      M += u;
+    }
+    const float var = M / (float)B;
+    const float sc = gamma[f] / sqrtf(var + eps);
+    scale[f] = sc;
+    shift[f] = fmaf(-mu, sc, beta[f]);
+    if (batch_mean) batch_mean[f] = mu;
+    if (batch_var) batch_var[f] = var;
   }
 }
 
@@ -480,9 +522,8 @@ cudaError_t launch_qnet_batch(const uint16_t* x, const uint16_t* w, int B, int d
   cudaError_t e = launch_qnet_gemm<true>(x, w, B, dim, F, nullptr, nullptr, nullptr, part_mean,
                                          part_m2, status, stream);
   if (e != cudaSuccess) return e;
-  bn_batch_finalize_kernel<<<(F + 7) / 8, 256, 0, stream>>>(part_mean, part_m2, B, F, gamma, beta,
-                                                            eps, scale, shift, batch_mean,
-                                                            batch_var);
+  bn_batch_finalize_kernel<<<(F + 31) / 32, kFinWarps * 32, 0, stream>>>(
+      part_mean, part_m2, B, F, gamma, beta, eps, scale, shift, batch_mean, batch_var);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_qnet_gemm<false>(x, w, B, dim, F, scale, shift, q, nullptr, nullptr, status,
