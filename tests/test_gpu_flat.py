@@ -26,8 +26,9 @@ def case(seed, B, H, d_q, n, k):
     return c, q, C
 
 
-def run_flat(c, q, C, also_factorised=False):
-    """Full keys and flat top-k on the GPU; returns (keys bits, idx, w[, f_idx, f_w])."""
+def run_flat(c, q, C, also_factorised=False, keys_back=True):
+    """Full keys and flat top-k on the GPU; returns (keys bits or None, idx, w[, f_idx,
+    f_w])."""
     B, H, d_q, n, k = (c[x] for x in ("B", "H", "d_q", "n_keys", "k"))
     h, _ = make_handle(dict(c, B=max(B, 1)))
     try:
@@ -37,8 +38,8 @@ def run_flat(c, q, C, also_factorised=False):
         idx = torch.empty(B, H, k, dtype=torch.int64, device="cuda")
         w = torch.empty(B, H, k, device="cuda")
         pk.check(pk.pkm_flat_lookup(h, dq, keys, B, H, n, k, idx, w), "flat_lookup")
-        res = [keys.view(torch.int16).cpu().numpy().view(np.uint16), idx.cpu().numpy(),
-               w.cpu().numpy()]
+        res = [keys.view(torch.int16).cpu().numpy().view(np.uint16) if keys_back else None,
+               idx.cpu().numpy(), w.cpu().numpy()]
         if also_factorised:
             fi = torch.empty_like(idx)
             fw = torch.empty_like(w)
@@ -115,7 +116,7 @@ def test_flat_mid_sampled_against_brute_force_and_factorised():
     c = synth.CONFIGS["mid"]
     q, C = synth.queries(c), synth.subkeys(c)
     B, H, d_q, n, k = (c[x] for x in ("B", "H", "d_q", "n_keys", "k"))
-    _, idx, w, fidx, fw = run_flat(dict(c), q, C, also_factorised=True)
+    _, idx, w, fidx, fw = run_flat(dict(c), q, C, also_factorised=True, keys_back=False)
     rows = np.random.default_rng(7).choice(B, 12, replace=False)
     ref, qs, Bs = brute_ref(c, q, C, rows)
     rep = compare_lookup(idx[rows], w[rows], ref, qs, C, "bf16", H, d_q, n)
@@ -144,3 +145,25 @@ def test_flat_argument_errors():
         assert pk.pkm_get_status(h) == pk.PKM_OK
     finally:
         pk.pkm_destroy(h)
+
+
+def test_flat_page_shapes_small_batch():
+    # the page workload's tables at a small batch: N = 2^20 full keys per head
+    # (an 8 GiB full key table), d_q = 1024, k = 32; every (query, head) against
+    # the factorised GPU search, sampled queries against the oracle (whose
+    # factorised search is pinned to its brute force)
+    c = dict(synth.CONFIGS["page"], B=256)
+    q, C = synth.queries(c), synth.subkeys(c)
+    B, H, d_q, n, k = (c[x] for x in ("B", "H", "d_q", "n_keys", "k"))
+    _, idx, w, fidx, fw = run_flat(c, q, C, also_factorised=True, keys_back=False)
+    fsc = exact_scores(q, C, "bf16", H, d_q, n, fidx)
+    rep = compare_lookup(idx, w, dict(idx=fidx, w=fw.astype(np.float64), score=fsc), q, C, "bf16",
+                         H, d_q, n)
+    assert rep["failures"] == 0, rep
+    assert rep["near_ties"] <= 0.01 * B * H, rep
+    assert rep["w_ok"], rep
+    rows = np.random.default_rng(9).choice(B, 16, replace=False)
+    qs = q.reshape(B, H * d_q)[rows].ravel()
+    ref = oracle.lookup(qs, C, len(rows), H, d_q, n, k)
+    rep = compare_lookup(idx[rows], w[rows], ref, qs, C, "bf16", H, d_q, n)
+    assert rep["failures"] == 0 and rep["w_ok"], rep
