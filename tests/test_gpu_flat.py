@@ -80,6 +80,7 @@ def test_full_keys_are_the_concatenated_subkeys():
     (257, 3, 96, 40, 32),      # d_q = 96 (a partial k-slab), N = 1600, k = 32
     (40, 1, 32, 20, 1),        # k = 1: the argmax
     (33, 2, 64, 12, 12),       # k = n_keys (the largest k a handle takes), N = 144 < one chunk
+    (70, 8, 128, 48, 32),      # eight heads (the skewed workload's H), N = 2304
 ])
 def test_flat_matches_brute_force(shape):
     c, q, C = case(sum(shape), *shape)

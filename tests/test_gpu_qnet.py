@@ -132,7 +132,8 @@ def check_batch(x, W, B, dim, F, gamma, beta, eps):
 
 
 @pytest.mark.parametrize("B,dim,F", [(300, 1024, 4096), (129, 48, 96), (64, 256, 288),
-                                     (1000, 512, 512), (33, 64, 96), (2, 32, 64)])
+                                     (1000, 512, 512), (33, 64, 96), (2, 32, 64),
+                                     (4096, 512, 1024)])
 def test_query_net_batch_matches_oracle(B, dim, F):
     rng = np.random.default_rng(B * 7 + dim + F)
     x = synth.normal(B + 1, 6, B * dim, 1.0, dtype="bf16").reshape(B, dim)
