@@ -670,7 +670,11 @@ cudaError_t launch_lookup_tc(const uint16_t* q, const uint16_t* subkeys, int B, 
   // own memory
   const void* const operands[2] = {q, subkeys};
   const bool pair = !two_sm && pair_shape && tc::buffers_on_this_device(operands, 2);
-  const int epi = form == 3 ? 1 : 2;  // the two-SM kernel's epilogue form
+  // the two-SM kernel's epilogue form: one set with deeper tile stages for
+  // the pipeline-bound wide half-queries (measured on GB300, large workload's
+  // lookup call: 1.003 -> 0.885 ms), two sets otherwise (page 0.287 against
+  // 0.306 ms with one set, skewed 1.678 against 1.938)
+  const int epi = form == 3 || (form == 0 && deep) ? 1 : 2;
   auto select = [&](float z, const int* list, const int* count, int st) {
     if (two_sm && !list)
       return launch_select_2sm(mq, m2, B, H, d_q, n_keys, k, z, list_v, list_c, status, st != 0,
