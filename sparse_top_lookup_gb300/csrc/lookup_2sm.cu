@@ -549,10 +549,13 @@ cudaError_t launch_select_2sm_flat(const CUtensorMap& tmap_q, const CUtensorMap&
   if (B == 0) return cudaSuccess;
   const int nch = (N + NP - 1) / NP;
   const int kbc = (d_q + BK - 1) / BK;
-  return k <= 16 ? launch_kl<16, kEpiTwoSets, true>(tmap_q, tmap_keys, B, H, N, nch, kbc,
+  // one epilogue set with 5 tile stages: once a row's threshold has risen,
+  // the flat search mostly compares and drops, so the tile pipeline bounds it
+  // (mid_flat on GB300: 1.91 ms with two sets, 1.21 ms with one)
+  return k <= 16 ? launch_kl<16, kEpiOneSet, true>(tmap_q, tmap_keys, B, H, N, nch, kbc,
                                                     -INFINITY, nullptr, nullptr, status, 0,
                                                     stream, idx, w, k)
-                 : launch_kl<32, kEpiTwoSets, true>(tmap_q, tmap_keys, B, H, N, nch, kbc,
+                 : launch_kl<32, kEpiOneSet, true>(tmap_q, tmap_keys, B, H, N, nch, kbc,
                                                     -INFINITY, nullptr, nullptr, status, 0,
                                                     stream, idx, w, k);
 }
