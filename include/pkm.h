@@ -271,8 +271,8 @@ int pkm_abi_version(void);
 /*
  * 1 if every one of the `count` pointers is device memory of the current
  * device, else 0 (also on any CUDA error, or with no device).  The lookup's
- * one-SM selection form and the query network load tiles once for two CTAs
- * of a cluster (TMA multicast) only when their operands pass this test;
+ * one-SM selection form loads tiles once for two CTAs of a cluster (TMA
+ * multicast) only when its operands pass this test;
  * other operands (host, managed or another GPU's memory) take the one-CTA
  * forms.  Host-side only; nothing is launched.
  */

@@ -48,6 +48,11 @@ constexpr int QA_BYTES = QM * QK * 2;  // 16 KiB
 constexpr int QB_BYTES = QN * QK * 2;  // 32 KiB
 constexpr int QSTAGE_BYTES = QA_BYTES + QB_BYTES;
 constexpr int QSMEM = QSTAGES * QSTAGE_BYTES + 1024;  // + alignment slack
+// the two-SM form: per CTA an x slab and half (128 rows) of the W slab
+constexpr int Q2STAGES = 6;
+constexpr int Q2STAGE_BYTES = QA_BYTES + QB_BYTES / 2;  // 32 KiB
+constexpr int Q2SMEM = Q2STAGES * Q2STAGE_BYTES + 1024;
+static_assert(Q2SMEM <= 227 * 1024, "two-SM query network shared memory");
 constexpr int QTHREADS = 192;
 
 // The 32-row blocks' (mean m_b, squared-deviation sum M_b, row count n_b)
@@ -156,13 +161,6 @@ __global__ void bn_fold_kernel(const float* __restrict__ gamma, const float* __r
   shift[f] = fmaf(-mean[f], s, beta[f]);
 }
 
-// kPair: clusters of two CTAs on row tiles 2p and 2p+1 of the same feature
-// tile, in lockstep: each CTA loads its own x slab and half (128 rows) of the
-// W slab, multicast to both, so a W slab crosses from L2 once for the pair
-// (32 KB of L2 reads per stage and CTA instead of 48 KB).  A stage is free
-// once both CTAs' MMAs have read it (each MMA's release commit arrives on
-// both CTAs' empty barriers).  A CTA whose row tile is past the batch loads
-// zero-filled x rows for its partner's sake and stores nothing.
 // Sum over the warp's 32 lanes of each of 32 values: on return lane j holds
 // the sum of every lane's a[j] (31 shuffles: each step halves the values a
 // lane holds, the pair of lanes keeping complementary halves).
@@ -180,31 +178,88 @@ __device__ __forceinline__ float transpose_sum32(float (&a)[32], int lane) {
   return a[0];
 }
 
-// kStats: the epilogue writes column statistics instead of q: for the 32
-// rows of each epilogue warp (block tm * 4 + quad) and each feature f, the
+// The epilogue of one 128 x 256 output tile (row tile tm, feature tile tn),
+// whose accumulators are at TMEM address taddr (this thread's lane, column
+// 0): q = z * scale + shift in bf16, or (kStats) column statistics instead of
+// q: for the 32 rows of the warp (block tm * 4 + quad) and each feature f, the
 // mean of the block's rows inside the batch and the sum of their squared
 // deviations from it, at part_mean / part_m2 [block][F].
-template <bool kPair, bool kStats>
+template <bool kStats>
+__device__ __forceinline__ void qnet_tile_out(uint32_t taddr, int tm, int tn, int quad, int row,
+                                              int lane, int B, int F,
+                                              const float* __restrict__ scale,
+                                              const float* __restrict__ shift,
+                                              __nv_bfloat16* __restrict__ q,
+                                              float* __restrict__ part_mean,
+                                              float* __restrict__ part_m2) {
+  const int b = tm * QM + row;
+  for (int g = 0; g < QN; g += 32) {
+    const int c0 = tn * QN + g;
+    if (c0 >= F) break;  // F is a multiple of 32: a group is all in or all out
+    float v[32];
+    tmem_ld32(taddr + g, v);
+    if constexpr (kStats) {
+      const bool in = b < B;
+      const int nb = __popc(__ballot_sync(0xffffffffu, in));  // the block's rows in the batch
+      if (nb == 0) continue;  // warp-uniform: a block past the batch writes nothing
+      float a[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) a[j] = in ? v[j] : 0.0f;
+      const float mean = transpose_sum32(a, lane) / (float)nb;  // column c0 + lane
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        // every lane takes part in the broadcast, in the block or not
+        const float mj = __shfl_sync(0xffffffffu, mean, j);
+        const float d = in ? v[j] - mj : 0.0f;
+        a[j] = d * d;
+      }
+      const float m2 = transpose_sum32(a, lane);
+      const size_t o = (size_t)(tm * 4 + quad) * F + c0 + lane;
+      part_mean[o] = mean;
+      part_m2[o] = m2;
+      continue;
+    }
+    const float4* sc4 = reinterpret_cast<const float4*>(scale + c0);
+    const float4* sh4 = reinterpret_cast<const float4*>(shift + c0);
+    uint32_t packed[16];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float4 a = sc4[j], t = sh4[j];
+      const __nv_bfloat162 lo =
+          __floats2bfloat162_rn(fmaf(v[4 * j], a.x, t.x), fmaf(v[4 * j + 1], a.y, t.y));
+      const __nv_bfloat162 hi =
+          __floats2bfloat162_rn(fmaf(v[4 * j + 2], a.z, t.z), fmaf(v[4 * j + 3], a.w, t.w));
+      packed[2 * j] = *reinterpret_cast<const uint32_t*>(&lo);
+      packed[2 * j + 1] = *reinterpret_cast<const uint32_t*>(&hi);
+    }
+    if (b < B) {
+      uint4* dst = reinterpret_cast<uint4*>(q + (size_t)b * F + c0);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        dst[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+    }
+  }
+}
+
+// One CTA per tile (a batch of at most one 128-row tile, or the pair form
+// unavailable): persistent over 128 x 256 output tiles.
+template <bool kStats>
 __global__ void __launch_bounds__(QTHREADS, 1)
 qnet_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
-            const __grid_constant__ CUtensorMap tmap_w_half, int B, int F, int dim,
-            const float* __restrict__ scale, const float* __restrict__ shift,
-            __nv_bfloat16* __restrict__ q, float* __restrict__ part_mean,
-            float* __restrict__ part_m2, int* __restrict__ status) {
+            int B, int F, int dim, const float* __restrict__ scale,
+            const float* __restrict__ shift, __nv_bfloat16* __restrict__ q,
+            float* __restrict__ part_mean, float* __restrict__ part_m2,
+            int* __restrict__ status) {
   extern __shared__ unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t bars[2 * QSTAGES + 4 + 1];
   __shared__ uint32_t s_tmem_base;
   __shared__ int s_abort;
 
   const int tm_count = (B + QM - 1) / QM, tn_count = (F + QN - 1) / QN;
-  // pair mode: the cluster's work items (pair tiles: two row tiles, one
-  // feature tile) and this CTA's rank in it; otherwise the CTA's own tiles
-  const uint32_t rank = kPair ? cluster_ctarank() : 0u;
-  const int slot = kPair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
-  const int slots = kPair ? (int)(gridDim.x >> 1) : (int)gridDim.x;
-  const int tiles = (kPair ? (tm_count + 1) / 2 : tm_count) * tn_count;
+  const int slot = (int)blockIdx.x, slots = (int)gridDim.x;
+  const int tiles = tm_count * tn_count;
   const int mine = slot < tiles ? (tiles - 1 - slot) / slots + 1 : 0;
-  if (mine == 0) return;  // (pair mode: both CTAs of the cluster alike)
+  if (mine == 0) return;
   const int kb_count = (dim + QK - 1) / QK;
 
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -221,7 +276,7 @@ qnet_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
   if (threadIdx.x == 0) {
     for (int s = 0; s < QSTAGES; ++s) {
       mbar_init(bar_full(s), 1);
-      mbar_init(bar_empty(s), kPair ? 2 : 1);  // pair: both CTAs' MMAs release it
+      mbar_init(bar_empty(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar_tfull(b), 1);
@@ -242,14 +297,12 @@ qnet_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (kPair) cluster_sync();  // the peer's barriers exist before any multicast reaches them
   const uint32_t tmem = s_tmem_base;
   const Ctl ctl{&s_abort, status};
   auto tile_of = [&](int i, int& tm, int& tn) {
     const int t = slot + i * slots;
     tm = t / tn_count;
     tn = t - tm * tn_count;
-    if (kPair) tm = 2 * tm + (int)rank;
   };
 
   if (warp == 0) {
@@ -269,11 +322,7 @@ qnet_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
           mbar_expect_tx(bar_full(s), QSTAGE_BYTES);
           const uint32_t dst = tiles_u32 + s * QSTAGE_BYTES;
           tma_load_2d(dst, &tmap_x, kb * QK, tm * QM, bar_full(s));
-          if (kPair)  // this CTA's half of the W slab, to both CTAs
-            tma_load_2d_mc(dst + QA_BYTES + rank * (QN / 2) * 128, &tmap_w_half, kb * QK,
-                           tn * QN + (int)rank * (QN / 2), bar_full(s), 3);
-          else
-            tma_load_2d(dst + QA_BYTES, &tmap_w, kb * QK, tn * QN, bar_full(s));
+          tma_load_2d(dst + QA_BYTES, &tmap_w, kb * QK, tn * QN, bar_full(s));
         }
       }
       if (!ok) {  // let the copies already issued land before the CTA exits
@@ -304,10 +353,7 @@ qnet_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
 #pragma unroll
           for (int kk = 0; kk < QK / 16; ++kk)
             tc_mma(d_tmem, a_desc + 2u * kk, b_desc + 2u * kk, idesc, (kb | kk) != 0);
-          if (kPair)
-            tc_commit_mc(bar_empty(s), 3);
-          else
-            tc_commit(bar_empty(s));
+          tc_commit(bar_empty(s));
         }
         if (!ok) break;
         tc_commit(bar_tfull(buf));
@@ -326,53 +372,8 @@ qnet_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
       const uint32_t buf = i & 1u, use = i >> 1;
       if (!__all_sync(0xffffffffu, wait_phase(bar_tfull(buf), use & 1u, ctl))) break;
       tc_fence_after();
-      const int b = tm * QM + row;
-      for (int g = 0; g < QN; g += 32) {
-        const int c0 = tn * QN + g;
-        if (c0 >= F) break;  // F is a multiple of 32: a group is all in or all out
-        float v[32];
-        tmem_ld32(lane_addr + buf * QN + g, v);
-        if constexpr (kStats) {
-          const bool in = b < B;
-          const int nb = __popc(__ballot_sync(0xffffffffu, in));  // the block's rows in the batch
-          if (nb == 0) continue;  // warp-uniform: a block past the batch writes nothing
-          float a[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) a[j] = in ? v[j] : 0.0f;
-          const float mean = transpose_sum32(a, lane) / (float)nb;  // column c0 + lane
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            // every lane takes part in the broadcast, in the block or not
-            const float mj = __shfl_sync(0xffffffffu, mean, j);
-            const float d = in ? v[j] - mj : 0.0f;
-            a[j] = d * d;
-          }
-          const float m2 = transpose_sum32(a, lane);
-          const size_t o = (size_t)(tm * 4 + quad) * F + c0 + lane;
-          part_mean[o] = mean;
-          part_m2[o] = m2;
-          continue;
-        }
-        const float4* sc4 = reinterpret_cast<const float4*>(scale + c0);
-        const float4* sh4 = reinterpret_cast<const float4*>(shift + c0);
-        uint32_t packed[16];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float4 a = sc4[j], t = sh4[j];
-          const __nv_bfloat162 lo =
-              __floats2bfloat162_rn(fmaf(v[4 * j], a.x, t.x), fmaf(v[4 * j + 1], a.y, t.y));
-          const __nv_bfloat162 hi =
-              __floats2bfloat162_rn(fmaf(v[4 * j + 2], a.z, t.z), fmaf(v[4 * j + 3], a.w, t.w));
-          packed[2 * j] = *reinterpret_cast<const uint32_t*>(&lo);
-          packed[2 * j + 1] = *reinterpret_cast<const uint32_t*>(&hi);
-        }
-        if (b < B) {
-          uint4* dst = reinterpret_cast<uint4*>(q + (size_t)b * F + c0);
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            dst[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
-        }
-      }
+      qnet_tile_out<kStats>(lane_addr + buf * QN, tm, tn, quad, row, lane, B, F, scale, shift, q,
+                            part_mean, part_m2);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_tempty(buf));
@@ -386,9 +387,176 @@ qnet_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512)
                  : "memory");
   }
-  // pair: neither CTA leaves while the other may still load into its shared
-  // memory or arrive on its barriers
-  if (kPair) cluster_sync();
+}
+
+// The two-SM form (batches of at least two row tiles): clusters of two CTAs
+// on row tiles 2p and 2p + 1 of one feature tile issue one MMA of M = 256
+// rows (128 in each CTA) and N = 256 features, each CTA loading its own x
+// slab and half (128 rows) of the W slab, so for the same MMA work an SM
+// receives 32 KB per k-slab instead of 48 KB.  As in the two-SM selection
+// kernel: both CTAs' copies complete on the leader CTA's full barrier, whose
+// producer expects both CTAs' bytes; the leader's MMA warp issues
+// tcgen05.mma.cta_group::2 and commits to both CTAs' barriers; the epilogue
+// warps of both CTAs hand a TMEM buffer back on the leader's barrier; TMEM is
+// allocated and freed jointly.  A CTA whose row tile is past the batch loads
+// zero-filled x rows for its partner's sake and stores nothing.
+template <bool kStats>
+__global__ void __launch_bounds__(QTHREADS, 1)
+qnet2_kernel(const __grid_constant__ CUtensorMap tmap_x,
+             const __grid_constant__ CUtensorMap tmap_w_half, int B, int F, int dim,
+             const float* __restrict__ scale, const float* __restrict__ shift,
+             __nv_bfloat16* __restrict__ q, float* __restrict__ part_mean,
+             float* __restrict__ part_m2, int* __restrict__ status) {
+  extern __shared__ unsigned char smem_raw[];
+  __shared__ __align__(8) uint64_t bars[2 * Q2STAGES + 4 + 1];
+  __shared__ uint32_t s_tmem_base;
+  __shared__ int s_abort;
+
+  const int tm_count = (B + QM - 1) / QM, tn_count = (F + QN - 1) / QN;
+  const uint32_t rank = cluster_ctarank();
+  const int slot = (int)(blockIdx.x >> 1), slots = (int)(gridDim.x >> 1);
+  const int tiles = (tm_count + 1) / 2 * tn_count;
+  const int mine = slot < tiles ? (tiles - 1 - slot) / slots + 1 : 0;
+  if (mine == 0) return;  // both CTAs of the cluster alike
+  const int kb_count = (dim + QK - 1) / QK;
+
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t tiles_u32 = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t bar0 = smem_u32(&bars[0]);
+  auto bar_full = [&](uint32_t s) { return bar0 + 8u * s; };
+  auto bar_empty = [&](uint32_t s) { return bar0 + 8u * (Q2STAGES + s); };
+  auto bar_tfull = [&](uint32_t b) { return bar0 + 8u * (2 * Q2STAGES + b); };
+  auto bar_tempty = [&](uint32_t b) { return bar0 + 8u * (2 * Q2STAGES + 2 + b); };
+  const uint32_t bar_done = bar0 + 8u * (2 * Q2STAGES + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < Q2STAGES; ++s) {
+      mbar_init(bar_full(s), 1);   // leader: its producer's expect_tx (both CTAs' bytes)
+      mbar_init(bar_empty(s), 1);  // the leader's MMA commit, multicast to both CTAs
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_tfull(b), 1);   // the leader's MMA commit, multicast
+      mbar_init(bar_tempty(b), 8);  // leader: four epilogue warps of each CTA
+    }
+    mbar_init(bar_done, 1);
+    s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {  // one warp of each CTA allocates, jointly for the pair
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&s_tmem_base)),
+                 "r"(512)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  cluster_sync();  // both CTAs' barriers exist before any remote arrival
+  const uint32_t tmem = s_tmem_base;
+  const Ctl ctl{&s_abort, status};
+  // the cluster's tile i: pair tile (row tiles 2p, 2p + 1) and feature tile
+  auto tile_of = [&](int i, int& tp, int& tn) {
+    const int t = slot + i * slots;
+    tp = t / tn_count;
+    tn = t - tp * tn_count;
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int i = 0; ok && i < mine; ++i) {
+        int tp, tn;
+        tile_of(i, tp, tn);
+        const int row0 = (2 * tp + (int)rank) * QM;
+        for (int kb = 0; kb < kb_count; ++kb, ++it) {
+          const uint32_t s = it % Q2STAGES, ph = (it / Q2STAGES) & 1u;
+          if (!wait_phase_cluster(bar_empty(s), ph ^ 1u, ctl)) {
+            ok = false;
+            break;
+          }
+          if (rank == 0) mbar_expect_tx(bar_full(s), 2u * Q2STAGE_BYTES);
+          const uint32_t dst = tiles_u32 + s * Q2STAGE_BYTES;
+          const uint32_t fb = mapa_shared(bar_full(s), 0);
+          tma_load_2d_cg2(dst, &tmap_x, kb * QK, row0, fb);
+          tma_load_2d_cg2(dst + QA_BYTES, &tmap_w_half, kb * QK, tn * QN + (int)rank * (QN / 2),
+                          fb);
+        }
+      }
+      // the leader's last releases of this CTA's stages land before it exits
+      if (ok) {
+        const uint32_t first = it > (uint32_t)Q2STAGES ? it - Q2STAGES : 0u;
+        for (uint32_t j = first; j < it; ++j)
+          wait_phase_drain(bar_empty(j % Q2STAGES), (j / Q2STAGES) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer (leader)
+    if (rank == 0 && lane == 0) {
+      const uint32_t idesc = idesc_bf16(2 * QM, QN);
+      uint32_t it = 0;
+      bool ok = true;
+      for (int i = 0; ok && i < mine; ++i) {
+        const uint32_t buf = i & 1u, use = i >> 1;
+        if (!wait_phase_cluster(bar_tempty(buf), (use & 1u) ^ 1u, ctl)) break;
+        tc_fence_after();
+        for (int kb = 0; kb < kb_count; ++kb, ++it) {
+          const uint32_t s = it % Q2STAGES, ph = (it / Q2STAGES) & 1u;
+          if (!wait_phase_cluster(bar_full(s), ph, ctl)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t a_desc = sw128_desc(tiles_u32 + s * Q2STAGE_BYTES);
+          const uint64_t b_desc = sw128_desc(tiles_u32 + s * Q2STAGE_BYTES + QA_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < QK / 16; ++kk)
+            tc_mma_cg2(tmem + buf * QN, a_desc + 2u * kk, b_desc + 2u * kk, idesc,
+                       (kb | kk) != 0);
+          tc_commit_cg2_mc(bar_empty(s), 3);  // the stage is free again in both CTAs
+        }
+        if (!ok) break;
+        tc_commit_cg2_mc(bar_tfull(buf), 3);  // the tile's sums are in both TMEMs
+      }
+      // every issued MMA completes before TMEM is released
+      tc_commit_cg2_mc(bar_done, 1);
+      wait_phase_drain(bar_done, 0);
+    }
+  } else {
+    // ------------------------------------------------ epilogue (both CTAs)
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16);
+    for (int i = 0; i < mine; ++i) {
+      int tp, tn;
+      tile_of(i, tp, tn);
+      const uint32_t buf = i & 1u, use = i >> 1;
+      if (!__all_sync(0xffffffffu, wait_phase_cluster(bar_tfull(buf), use & 1u, ctl))) break;
+      tc_fence_after();
+      qnet_tile_out<kStats>(lane_addr + buf * QN, 2 * tp + (int)rank, tn, quad, row, lane, B, F,
+                            scale, shift, q, part_mean, part_m2);
+      // tile written: hand the TMEM buffer back to the leader's MMA warp
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(bar_tempty(buf), 0));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  // the leader's MMAs (which write both CTAs' TMEM and read both CTAs'
+  // stages) are complete, and no CTA still arrives on the other's barriers
+  cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512)
+                 : "memory");
+  }
 }
 
 }  // namespace
@@ -431,8 +599,8 @@ cudaError_t launch_qnet_gemm(const uint16_t* x, const uint16_t* w, int B, int di
             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
-    // the same view in half-slab boxes (128 rows): each CTA of a pair loads
-    // one half and multicasts it
+    // the same view in half-slab boxes (128 rows): each CTA of the two-SM
+    // form loads its half of each W slab
     const cuuint32_t hbox[2] = {QK, QN / 2};
     if (enc(&mwh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(w), dims, strides,
             hbox, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -441,15 +609,13 @@ cudaError_t launch_qnet_gemm(const uint16_t* x, const uint16_t* w, int B, int di
   }
   const int tm_count = (B + QM - 1) / QM, tn_count = (F + QN - 1) / QN;
   auto q16 = reinterpret_cast<__nv_bfloat16*>(q);
-  // pairs of row tiles share each W slab when there are at least two (and
-  // x and W are this device's memory: the slabs are multicast)
-  const void* const operands[2] = {x, w};
-  if (tm_count >= 2 && buffers_on_this_device(operands, 2)) {
-    auto kernel = qnet_kernel<true, kStats>;
+  // the two-SM form when there are at least two row tiles
+  if (tm_count >= 2) {
+    auto kernel = qnet2_kernel<kStats>;
     static bool attr_set = false;
     if (!attr_set) {
       cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           QSMEM);
+                                           Q2SMEM);
       if (e != cudaSuccess) return e;
       attr_set = true;
     }
@@ -460,7 +626,7 @@ cudaError_t launch_qnet_gemm(const uint16_t* x, const uint16_t* w, int B, int di
     attr[0].val.clusterDim.z = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(QTHREADS);
-    cfg.dynamicSmemBytes = QSMEM;
+    cfg.dynamicSmemBytes = Q2SMEM;
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
@@ -473,10 +639,10 @@ cudaError_t launch_qnet_gemm(const uint16_t* x, const uint16_t* w, int B, int di
     }
     const int pair_tiles = (tm_count + 1) / 2 * tn_count;
     cfg.gridDim = dim3(2 * (pair_tiles < max_clusters ? pair_tiles : max_clusters));
-    return cudaLaunchKernelEx(&cfg, kernel, mx, mw, mwh, B, F, dim, scale, shift, q16, part_mean,
+    return cudaLaunchKernelEx(&cfg, kernel, mx, mwh, B, F, dim, scale, shift, q16, part_mean,
                               part_m2, status);
   }
-  auto kernel = qnet_kernel<false, kStats>;
+  auto kernel = qnet_kernel<kStats>;
   static bool attr_set1 = false;
   if (!attr_set1) {
     cudaError_t e =
@@ -486,7 +652,7 @@ cudaError_t launch_qnet_gemm(const uint16_t* x, const uint16_t* w, int B, int di
   }
   const int tiles = tm_count * tn_count;
   const int grid = tiles < sm_count() ? tiles : sm_count();
-  kernel<<<grid, QTHREADS, QSMEM, stream>>>(mx, mw, mwh, B, F, dim, scale, shift, q16, part_mean,
+  kernel<<<grid, QTHREADS, QSMEM, stream>>>(mx, mw, B, F, dim, scale, shift, q16, part_mean,
                                            part_m2, status);
   return cudaGetLastError();
 }

@@ -161,6 +161,14 @@ __device__ __forceinline__ void tma_load_4d_cg2(uint32_t dst, const CUtensorMap*
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
       : "memory");
 }
+__device__ __forceinline__ void tma_load_2d_cg2(uint32_t dst, const CUtensorMap* map, int c0,
+                                                int c1, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
 __device__ __forceinline__ void tma_load_3d_cg2(uint32_t dst, const CUtensorMap* map, int c0,
                                                 int c1, int c2, uint32_t bar) {
   asm volatile(
