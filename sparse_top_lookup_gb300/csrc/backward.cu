@@ -16,10 +16,13 @@
 // Read part (dw and dV), grouped by value row so that each selected row of V
 // and of dV crosses HBM once however many selections hit it (the gradient
 // rows dout, B * d_v * 4 bytes, are re-read from L2 instead):
-//   bucket_count_kernel    selections per bucket of 256 consecutive rows;
+//   bucket_count_kernel    selections per bucket of 256 consecutive rows
+//                          (each selection's place in its bucket from the
+//                          counting atomic);
 //   bucket_scan_kernel     bucket offsets, and the work items: each bucket's
 //                          list cut into chunks of at most kChunk selections;
-//   bucket_scatter_kernel  selection numbers into their bucket's list;
+//   bucket_scatter_kernel  selection numbers into their bucket's list (first
+//                          slot + place, no atomics);
 //   bucket_sort_kernel     one CTA per item: a counting sort of the chunk by
 //                          row in shared memory, cut into pieces (up to
 //                          kPiece selections of one row), each appended to a
@@ -107,22 +110,23 @@ __device__ __forceinline__ void red_add4(float* p, float a, float b, float c, fl
                : "memory");
 }
 
-// Selections per bucket; with `bitmap` (the sparse output) also one bit per
-// selected row.
+// Selections per bucket, one thread per selection, whose place in its
+// bucket's list is the count before it (the atomic add's return, kept in
+// erank); with `bitmap` (the sparse output) also one bit per selected row.
 __global__ void bucket_count_kernel(const int64_t* __restrict__ idx, int E, int64_t N,
-                                    int* __restrict__ bcount, uint32_t* __restrict__ bitmap,
-                                    float* __restrict__ dw, int* __restrict__ status) {
-  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < E;
-       e += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = idx[e];
-    if (r < 0 || r >= N) {  // recorded; the selection contributes nothing
-      atomicExch(status, PKM_ERR_BAD_INDEX);
-      dw[e] = 0.0f;
-      continue;
-    }
-    atomicAdd(&bcount[r / kRowsPerBucket], 1);
-    if (bitmap) atomicOr(&bitmap[r >> 5], 1u << (r & 31));
+                                    int* __restrict__ bcount, int* __restrict__ erank,
+                                    uint32_t* __restrict__ bitmap, float* __restrict__ dw,
+                                    int* __restrict__ status) {
+  const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= E) return;
+  const int64_t r = idx[e];
+  if (r < 0 || r >= N) {  // recorded; the selection contributes nothing
+    atomicExch(status, PKM_ERR_BAD_INDEX);
+    dw[e] = 0.0f;
+    return;
   }
+  erank[e] = atomicAdd(&bcount[r / kRowsPerBucket], 1);
+  if (bitmap) atomicOr(&bitmap[r >> 5], 1u << (r & 31));
 }
 
 // One CTA of 1024 threads: exclusive scans of the bucket sizes (list
@@ -201,14 +205,15 @@ bucket_scan_kernel(const int* __restrict__ bcount, int nb, int* __restrict__ cur
   }
 }
 
+// Each selection to its bucket's first slot plus its place (no atomics).
 __global__ void bucket_scatter_kernel(const int64_t* __restrict__ idx, int E, int64_t N,
-                                      int* __restrict__ cursor, int* __restrict__ list) {
-  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < E;
-       e += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = idx[e];
-    if (r < 0 || r >= N) continue;
-    list[atomicAdd(&cursor[r / kRowsPerBucket], 1)] = (int)e;
-  }
+                                      const int* __restrict__ cursor,
+                                      const int* __restrict__ erank, int* __restrict__ list) {
+  const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= E) return;
+  const int64_t r = idx[e];
+  if (r < 0 || r >= N) return;
+  list[cursor[r / kRowsPerBucket] + erank[e]] = (int)e;
 }
 
 // One CTA per item: the item's selections sorted by row (counting sort in
@@ -974,11 +979,15 @@ cudaError_t launch_backward_read(const void* values, int value_dtype, int B, int
   }
   if (B == 0) return cudaSuccess;
   const int sms = tc::sm_count();
-  const int grid = (int)std::min<int64_t>((E + 255) / 256, (int64_t)sms * 8);
-  bucket_count_kernel<<<grid, 256, 0, stream>>>(idx, (int)E, N, bcount, bitmap, dw, status);
+  // the places of the selections in their buckets, between the count and the
+  // scatter, in the piece records' region (written only by the sort after)
+  int* erank = reinterpret_cast<int*>(ws + off[kOffPieces]);
+  const unsigned eblocks = (unsigned)((E + 255) / 256);
+  bucket_count_kernel<<<eblocks, 256, 0, stream>>>(idx, (int)E, N, bcount, erank, bitmap, dw,
+                                                   status);
   bucket_scan_kernel<<<1, 1024, 0, stream>>>(bcount, (int)nb, cursor, items, n_items, bitmap,
                                              rowoff, n_rows);
-  bucket_scatter_kernel<<<grid, 256, 0, stream>>>(idx, (int)E, N, cursor, list);
+  bucket_scatter_kernel<<<eblocks, 256, 0, stream>>>(idx, (int)E, N, cursor, erank, list);
   bucket_sort_kernel<<<(unsigned)max_items, kReadWarps * 32, 0, stream>>>(
       idx, w, H * k, items, n_items, list, pieces, n_pieces, bitmap, rowoff, rows_out, zero_list,
       n_zero);
