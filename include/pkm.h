@@ -128,7 +128,7 @@ enum {
      whatever this option says. */
   PKM_OPT_READ_SMS = 4,
   /* bf16 lookups with k <= 32: the form of the selection kernel's main pass.
-     0 (default): automatic (the two-SM form from 256 queries, with one
+     0 (default): automatic (the two-SM form above 128 queries, with one
      epilogue set for half-queries wider than 512, two otherwise); 1: one-SM
      forms (tcgen05 MMAs of 128 query rows per SM); 2: the two-SM form (MMAs of 256 query rows spanning the two
      CTAs of a cluster, each loading half of every subkey slab) with two

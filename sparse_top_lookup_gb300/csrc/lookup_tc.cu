@@ -664,8 +664,9 @@ cudaError_t launch_lookup_tc(const uint16_t* q, const uint16_t* subkeys, int B, 
   // CTA with 5 tile stages in flight
   const bool deep = kbc > 8;
   // the two-SM form (MMAs of 256 query rows over a CTA pair, each CTA
-  // receiving half of every subkey slab) for the main pass
-  const bool two_sm = form >= 2 || (form == 0 && B >= 2 * BM);
+  // receiving half of every subkey slab) for the main pass of any batch of
+  // more than one row tile (a lone 128-row tile runs on one SM)
+  const bool two_sm = form >= 2 || (form == 0 && B > BM);
   // the one-SM pair form multicasts subkey slabs: only with this device's
   // own memory
   const void* const operands[2] = {q, subkeys};
