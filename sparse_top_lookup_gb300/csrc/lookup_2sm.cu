@@ -205,7 +205,8 @@ select_2sm_kernel(const __grid_constant__ CUtensorMap tmap_q,
                   const __grid_constant__ CUtensorMap tmap_c, int B, int H, int n, int nch,
                   int kb_count, float hint_z, float* __restrict__ list_v,
                   unsigned short* __restrict__ list_c, int64_t* __restrict__ out_idx,
-                  float* __restrict__ out_w, int k, int* __restrict__ status, int stall) {
+                  float* __restrict__ out_w, int k, int* __restrict__ status, int stall,
+                  int* __restrict__ clear_words, int clear_count) {
   constexpr int STAGES = Shape2<kEpi>::kStages, SETS = Shape2<kEpi>::kSets;
   constexpr int SMEM_TILES = Shape2<kEpi>::kTiles;
   extern __shared__ unsigned char smem_raw[];
@@ -213,6 +214,12 @@ select_2sm_kernel(const __grid_constant__ CUtensorMap tmap_q,
   __shared__ uint32_t s_tmem_base;
   __shared__ int s_abort;
 
+  // the call's retry bookkeeping starts clear: the merge after this kernel
+  // counts into it (every CTA helps, also one without units)
+  if (clear_words)
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < clear_count;
+         i += gridDim.x * blockDim.x)
+      clear_words[i] = 0;
   const uint32_t rank = cluster_ctarank();
   const int slot = (int)(blockIdx.x >> 1);
   const int slots = (int)(gridDim.x >> 1);
@@ -491,7 +498,8 @@ template <int KL, int kEpi, bool kFlat = false>
 cudaError_t launch_kl(const CUtensorMap& mq, const CUtensorMap& mc, int B, int H, int n, int nch,
                       int kbc, float hint_z, float* list_v, unsigned short* list_c, int* status,
                       int stall, cudaStream_t stream, int64_t* out_idx = nullptr,
-                      float* out_w = nullptr, int k = 0) {
+                      float* out_w = nullptr, int k = 0, int* clear_words = nullptr,
+                      int clear_count = 0) {
   auto kernel = select_2sm_kernel<KL, kEpi, kFlat>;
   constexpr int SMEM_BYTES = Shape2<kEpi>::kSmem;
   static bool attr_set = false;
@@ -522,7 +530,7 @@ cudaError_t launch_kl(const CUtensorMap& mq, const CUtensorMap& mc, int B, int H
   const int units = (B + 2 * BM - 1) / (2 * BM) * H * (kFlat ? 1 : 2);
   cfg.gridDim = dim3(2 * (units < max_clusters ? units : max_clusters));
   return cudaLaunchKernelEx(&cfg, kernel, mq, mc, B, H, n, nch, kbc, hint_z, list_v, list_c,
-                            out_idx, out_w, k, status, stall);
+                            out_idx, out_w, k, status, stall, clear_words, clear_count);
 }
 
 }  // namespace
@@ -530,14 +538,14 @@ cudaError_t launch_kl(const CUtensorMap& mq, const CUtensorMap& mc, int B, int H
 cudaError_t launch_select_2sm(const CUtensorMap& tmap_q, const CUtensorMap& tmap_c_half, int B,
                               int H, int d_q, int n_keys, int k, float hint_z, float* list_v,
                               unsigned short* list_c, int* status, bool stall,
-                              cudaStream_t stream, int epi) {
+                              cudaStream_t stream, int epi, int* clear_words, int clear_count) {
   if (B == 0) return cudaSuccess;
   const int nch = (n_keys + NP - 1) / NP;
   const int kbc = (d_q / 2 + BK - 1) / BK;
   const int st = stall ? 1 : 0;
 #define PKM_SEL2(KLv, EPIv)                                                                   \
   launch_kl<KLv, EPIv>(tmap_q, tmap_c_half, B, H, n_keys, nch, kbc, hint_z, list_v, list_c, \
-                       status, st, stream)
+                       status, st, stream, nullptr, nullptr, 0, clear_words, clear_count)
   if (epi == kEpiOneSet) return k <= 16 ? PKM_SEL2(16, kEpiOneSet) : PKM_SEL2(32, kEpiOneSet);
   return k <= 16 ? PKM_SEL2(16, kEpiTwoSets) : PKM_SEL2(32, kEpiTwoSets);
 #undef PKM_SEL2

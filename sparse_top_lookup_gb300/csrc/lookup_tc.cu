@@ -222,7 +222,8 @@ select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
                  int B, int H, int n, int NC, int nch, int kb_count, float hint_z,
                  float* __restrict__ list_v, unsigned short* __restrict__ list_c,
                  int* __restrict__ status, const int* __restrict__ unit_list,
-                 const int* __restrict__ unit_count, int stall) {
+                 const int* __restrict__ unit_count, int stall, int* __restrict__ clear_words,
+                 int clear_count) {
   using Shape = SelShape<kSets>;
   constexpr int STAGES = Shape::kStages, SETS = kSets, BUFS = Shape::kBufs, CPS = Shape::kCps;
   constexpr int SMEM_TILES = Shape::kTiles, STAGE_BYTES = Shape::kStageBytes;
@@ -232,6 +233,12 @@ select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
   __shared__ uint32_t s_tmem_base;
   __shared__ int s_abort;
 
+  // the main pass clears the call's retry bookkeeping first: the merge after
+  // this kernel counts into it (every CTA helps, also one without units)
+  if (clear_words)
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < clear_count;
+         i += gridDim.x * blockDim.x)
+      clear_words[i] = 0;
   // work unit u: tile u / 2 (row tile, head), half u % 2.  The CTA's i-th
   // unit is entry blockIdx.x + i * gridDim.x of all units, or of unit_list
   // when one is given (a retry launch).  A CTA without units returns at once.
@@ -536,7 +543,8 @@ template <int KL, bool kPair, int kSets>
 cudaError_t launch_kl(const CUtensorMap& mq, const CUtensorMap& mc, const CUtensorMap& mch,
                       int B, int H, int n, int NC, int nch, int kbc, float hint_z,
                       float* list_v, unsigned short* list_c, int* status, const int* unit_list,
-                      const int* unit_count, int stall, cudaStream_t stream) {
+                      const int* unit_count, int stall, cudaStream_t stream,
+                      int* clear_words = nullptr, int clear_count = 0) {
   using Shape = SelShape<kSets>;
   auto kernel = select_tc_kernel<KL, kPair, kSets>;
   static bool attr_set = false;
@@ -572,7 +580,8 @@ cudaError_t launch_kl(const CUtensorMap& mq, const CUtensorMap& mc, const CUtens
     cfg.gridDim = dim3(units < sm_count() ? units : sm_count());  // one CTA per SM
   }
   return cudaLaunchKernelEx(&cfg, kernel, mq, mc, mch, B, H, n, NC, nch, kbc, hint_z, list_v,
-                            list_c, status, unit_list, unit_count, stall);
+                            list_c, status, unit_list, unit_count, stall, clear_words,
+                            clear_count);
 }
 
 // z with P(N(0,1) > z) = p, by bisection on the normal tail (host, once per call).
@@ -676,22 +685,23 @@ cudaError_t launch_lookup_tc(const uint16_t* q, const uint16_t* subkeys, int B, 
   // lookup call: 1.003 -> 0.885 ms), two sets otherwise (page 0.287 against
   // 0.306 ms with one set, skewed 1.678 against 1.938)
   const int epi = form == 3 || (form == 0 && deep) ? 1 : 2;
+  // the main pass also clears the retry bookkeeping (counts and the per-unit
+  // flags, one buffer) before anything else, in place of a memset
+  const int clear_count = 2 + (int)retry_units(B, H);
   auto select = [&](float z, const int* list, const int* count, int st) {
+    int* clear = list ? nullptr : retry.counts;
     if (two_sm && !list)
       return launch_select_2sm(mq, m2, B, H, d_q, n_keys, k, z, list_v, list_c, status, st != 0,
-                               stream, epi);
+                               stream, epi, clear, clear_count);
 #define PKM_SELECT(KLv, PAIRv, SETSv)                                                          \
   launch_kl<KLv, PAIRv, SETSv>(mq, mc, mch, B, H, n_keys, NC, nch, kbc, z, list_v, list_c, \
-                               status, list, count, st, stream)
+                               status, list, count, st, stream, clear, clear_count)
     if (pair && !list) return k <= 16 ? PKM_SELECT(16, true, 2) : PKM_SELECT(32, true, 2);
     if (deep && !list) return k <= 16 ? PKM_SELECT(16, false, 1) : PKM_SELECT(32, false, 1);
     return k <= 16 ? PKM_SELECT(16, false, 2) : PKM_SELECT(32, false, 2);
 #undef PKM_SELECT
   };
-  // the retry bookkeeping starts clear: counts and the per-unit flags (one buffer)
-  cudaError_t e =
-      cudaMemsetAsync(retry.counts, 0, (2 + (size_t)retry_units(B, H)) * sizeof(int), stream);
-  if (e == cudaSuccess) e = select(hint_z, nullptr, nullptr, stall ? 1 : 0);
+  cudaError_t e = select(hint_z, nullptr, nullptr, stall ? 1 : 0);
   // a4, a5: the k^2 merge and softmax, one thread per (query, head); lists
   // the units whose threshold hint was above a row's KL-th score
   if (e == cudaSuccess)

@@ -83,8 +83,8 @@ cudaError_t launch_lookup_simt_bf16(const uint16_t* q, const uint16_t* subkeys, 
 // one head x one half; unit index ((row tile * H + head) << 1) | half), and
 // the listed units are scored and selected again without the hint, which is
 // exact by construction, and their pairs merged again.
-// counts and unit_flag are one buffer (unit_flag == counts + 2), cleared by
-// one memset per call.
+// counts and unit_flag are one buffer (unit_flag == counts + 2), cleared at
+// the start of each call by the main pass's selection kernel.
 struct RetryScratch {
   int* counts;     // [0] pairs that had a marked list, [1] units listed for the retry
   int* unit_flag;  // [retry_units(B, H)]: nonzero once a unit is listed
@@ -114,11 +114,14 @@ cudaError_t launch_lookup_tc(const uint16_t* q, const uint16_t* subkeys, int B, 
 // tmap_q: q viewed as [B][H][2][d_q/2] in 128x64 boxes; tmap_c_half: the
 // subkeys viewed as [2H][n_keys][d_q/2] in 128x64 boxes; both 128-byte
 // swizzled.  epi: the epilogue form (1: one set of epilogue warps, 2: two
-// sets on alternate work units).
+// sets on alternate work units).  clear_words (may be NULL): clear_count
+// ints the kernel zeroes before anything else (the call's retry
+// bookkeeping, which the merge after it counts into).
 cudaError_t launch_select_2sm(const CUtensorMap& tmap_q, const CUtensorMap& tmap_c_half, int B,
                               int H, int d_q, int n_keys, int k, float hint_z, float* list_v,
                               unsigned short* list_c, int* status, bool stall,
-                              cudaStream_t stream, int epi = 2);
+                              cudaStream_t stream, int epi = 2, int* clear_words = nullptr,
+                              int clear_count = 0);
 
 // The flat exact top-k (flat.cu), the baseline the factorisation replaces:
 // the full key table [H][n_keys^2][d_q] (bf16) from the subkeys, and per
