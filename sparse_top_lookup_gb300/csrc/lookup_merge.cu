@@ -10,13 +10,14 @@
 // subkey asc).  Only pairs (i, j) with (i + 1)(j + 1) <= KL can reach the top
 // KL (every (i', j') with i' <= i, j' <= j scores at least as much).  Their
 // sums go through value-only sorting networks to the sorted KL best sums V;
-// when those are all distinct and no left-out pair ties the KL-th, each
-// surviving pair's output slot is the number of larger sums and its softmax
-// weight follows from V.  Exact ties take a frontier walk that orders equal
-// sums by flat index.  A list marked failed (subkey 0xffff in its first
-// slot: the selection threshold hint was above the row's KL-th score) lists
-// its work unit for the retry pass, which selects that unit again without
-// the hint and then merges the unit's pairs in this kernel's retry mode.
+// each surviving pair's output slot is the number of larger sums (equal sums
+// in flat index order) and its softmax weight follows from V.  When more
+// than KL pairs reach the KL-th sum x (a tie at the cut), the pairs above x
+// are placed that way and those at x fill the places left in flat index
+// order.  A list marked failed (subkey 0xffff in its first slot: the
+// selection threshold hint was above the row's KL-th score) lists its work
+// unit for the retry pass, which selects that unit again without the hint
+// and then merges the unit's pairs in this kernel's retry mode.
 #include <math.h>
 #include <stdint.h>
 
@@ -38,10 +39,18 @@ int tc_sms() {
 template <int KL>
 struct MergeLayout {
   static constexpr MergePairs<KL> P{};
-  static constexpr int kRow01 = KL + KL / 2;         // candidates of rows 0 and 1 (table is row-major)
-  static constexpr int kRest = P.kCount - kRow01;    // candidates of rows >= 2
-  // region A, 4-byte slots in [slot][thread] order: the rows >= 2 scores
-  // staged for folding (slots [0, kRest)), later the survivors' scores
+  // the pairs outside the sorted runs (i, j >= 3), staged and folded in one
+  // block of kRestBlock (a power of two)
+  static constexpr int rest() {
+    int c = 0;
+    for (int q = 0; q < P.kCount; ++q) c += P.i[q] >= 3 && P.j[q] >= 3;
+    return c;
+  }
+  static constexpr int kRest = rest();
+  static constexpr int kRestBlock = kRest <= 2 ? 2 : kRest <= 4 ? 4 : kRest <= 8 ? 8 : 16;
+  static_assert(kRest >= 1 && kRest <= 16, "merge: pairs outside the sorted runs");
+  // region A, 4-byte slots in [slot][thread] order: the scores of the pairs
+  // outside the runs staged for folding (slots [0, kRest)), later the survivors' scores
   // (slots [0, KL)) and pair codes (slots [KL, 2KL)).  Every use keeps a
   // thread inside its own column, so warps in different phases never touch
   // each other's slots.
@@ -101,12 +110,14 @@ __device__ __forceinline__ void merge_cta(const float* __restrict__ list_v,
     const int pair0 = cta * kThreads;
     const int np = min(kThreads, B * H - pair0);
     const float4* gv = reinterpret_cast<const float4*>(list_v + (size_t)pair0 * 2 * KL);
+#pragma unroll 4
     for (int q = t; q < np * (KL / 2); q += kThreads) {
       const int p = q / (KL / 2), s4 = q - p * (KL / 2);
       *reinterpret_cast<float4*>(stg + p * kRowV + 4 * s4) = gv[q];
     }
     const uint4* gc = reinterpret_cast<const uint4*>(list_c + (size_t)pair0 * 2 * KL);
     uint32_t* sc32 = reinterpret_cast<uint32_t*>(sc);
+#pragma unroll 4
     for (int q = t; q < np * (KL / 4); q += kThreads) {
       const int p = q / (KL / 4), m = q - p * (KL / 4);
       const uint4 u = gc[q];
@@ -161,56 +172,69 @@ __device__ __forceinline__ void merge_cta(const float* __restrict__ list_v,
   auto col1 = [&](int i) { return (int)my_sc[i]; };
   auto col2 = [&](int j) { return (int)my_sc[KL + j]; };
 
-  // V: the sorted KL best sums.  Row 0 of the candidate grid is already in
-  // descending order; row 1 is too, and one bitonic merge takes it in.
+  // V: the sorted KL best sums.  Rows and columns of the candidate grid are
+  // sorted runs: row 0 starts V, and row 1, column 0, column 1 and the rest
+  // of row 2 and of column 2 are merged in, one bitonic merge each.  The
+  // pairs left (i, j >= 3: twelve at KL = 32) are staged when above V's
+  // KL-th sum and folded in one block.
   float V[KL];
 #pragma unroll
   for (int j = 0; j < KL; ++j) V[j] = s1v[0] + s2v[j];
   {
-    float R[KL / 2];
+    float R[KL / 2];  // row 1
 #pragma unroll
     for (int j = 0; j < KL / 2; ++j) R[j] = s1v[1] + s2v[j];
     merge_top<KL, KL / 2>(V, R);
   }
-  // rows >= 2: only sums above V's KL-th can change V; they are staged in
-  // shared memory and folded in blocks
+  {
+    float R[KL - 2];  // column 0, rows 2 ..
+#pragma unroll
+    for (int u = 0; u < KL - 2; ++u) R[u] = s1v[2 + u] + s2v[0];
+    merge_top<KL, KL - 2>(V, R);
+  }
+  {
+    float R[KL / 2 - 2];  // column 1, rows 2 ..
+#pragma unroll
+    for (int u = 0; u < KL / 2 - 2; ++u) R[u] = s1v[2 + u] + s2v[1];
+    merge_top<KL, KL / 2 - 2>(V, R);
+  }
+  {
+    float R[KL / 3 - 2];  // row 2, columns 2 ..
+#pragma unroll
+    for (int u = 0; u < KL / 3 - 2; ++u) R[u] = s1v[2] + s2v[2 + u];
+    merge_top<KL, KL / 3 - 2>(V, R);
+  }
+  {
+    float R[KL / 3 - 3];  // column 2, rows 3 ..
+#pragma unroll
+    for (int u = 0; u < KL / 3 - 3; ++u) R[u] = s1v[3 + u] + s2v[2];
+    merge_top<KL, KL / 3 - 3>(V, R);
+  }
   {
     const float x1 = V[KL - 1];
     const uint32_t a0 = static_cast<uint32_t>(__cvta_generic_to_shared(stg + t));
     uint32_t a = a0;
 #pragma unroll
-    for (int c = Lay::kRow01; c < P.kCount; ++c)
-      stage_push<kThreads * 4>(a, s1v[P.i[c]] + s2v[P.j[c]], x1);
+    for (int c = 0; c < P.kCount; ++c)
+      if (P.i[c] >= 3 && P.j[c] >= 3) stage_push<kThreads * 4>(a, s1v[P.i[c]] + s2v[P.j[c]], x1);
     const int m = (int)((a - a0) / (kThreads * 4));
-#pragma unroll 1
-    for (int b0 = 0; __any_sync(0xffffffffu, m > b0); b0 += 32) {
-      if (__any_sync(0xffffffffu, m > b0 + 16)) {
-        float Bv[32];
+    if (__any_sync(0xffffffffu, m > 0)) {
+      constexpr int NR = Lay::kRestBlock;
+      float Bv[NR];
 #pragma unroll
-        for (int u = 0; u < 32; ++u) {
-          const int e = b0 + u < Lay::kRest ? b0 + u : Lay::kRest - 1;
-          const float x = stg[e * kThreads + t];
-          Bv[u] = b0 + u < m ? x : -INFINITY;
-        }
-        sort_desc<32>(Bv);
-        merge_top<KL, 32>(V, Bv);
-      } else {
-        float Bv[16];
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          const int e = b0 + u < Lay::kRest ? b0 + u : Lay::kRest - 1;
-          const float x = stg[e * kThreads + t];
-          Bv[u] = b0 + u < m ? x : -INFINITY;
-        }
-        sort_desc<16>(Bv);
-        merge_top<KL, 16>(V, Bv);
+      for (int u = 0; u < NR; ++u) {
+        const float v = stg[(u < Lay::kRest ? u : 0) * kThreads + t];
+        Bv[u] = u < m ? v : -INFINITY;
       }
+      sort_desc<NR>(Bv);
+      merge_top<KL, NR>(V, Bv);
     }
   }
   const float x = V[KL - 1];
-  bool tie = false;
+  // bit i: V[i] == V[i + 1] (a sum that occurs more than once in the best KL)
+  uint32_t dup = 0;
 #pragma unroll
-  for (int i = 0; i + 1 < KL; ++i) tie |= V[i] == V[i + 1];
+  for (int i = 0; i + 1 < KL; ++i) dup |= (V[i] == V[i + 1] ? 1u : 0u) << i;
   // survivors: pairs scoring >= x; more than KL of them means a tie at x
   // (region A is free again: the staged scores were all folded)
   const uint32_t va0 = static_cast<uint32_t>(__cvta_generic_to_shared(sv + t));
@@ -230,78 +254,89 @@ __device__ __forceinline__ void merge_cta(const float* __restrict__ list_v,
     if (r < k) z += expf(V[r] - V[0]);
   int64_t* ip = idx + (size_t)pair * k;
   float* wp = w + (size_t)pair * k;
-  if (!tie && nsurv == (uint32_t)KL) {
-    // each survivor's output place is the number of larger sums; its pair
-    // code goes to that place's slot of this thread's column
-#pragma unroll 2
-    for (int e = 0; e < KL; ++e) {
-      const float s = sv[e * kThreads + t];
-      so[count_greater<KL>(V, s) * kThreads + t] = sp[e * kThreads + t];
+  auto flat_of = [&](uint32_t pc) { return (int64_t)col1((int)(pc >> 5)) * n + col2((int)(pc & 31)); };
+  uint32_t placed = nsurv;  // survivors placed by value
+  if (nsurv != (uint32_t)KL) {
+    // a tie at the KL-th sum x: more than KL pairs reach it.  The pairs above
+    // x (fewer than KL) are placed by value below; those at x take the
+    // remaining places in flat index order after them.  Rare: plain loops
+    // over the lists in global memory keep this code small.
+    uint32_t va2 = va0;
+    placed = 0;
+#pragma unroll 1
+    for (int i = 0; i < KL; ++i) {
+      const float xi = v1[i];
+#pragma unroll 1
+      for (int j = 0; (i + 1) * (j + 1) <= KL; ++j)
+        surv_push<kThreads * 4, KL * kThreads * 4>(va2, placed, va_end, xi + v1[KL + j], x,
+                                                   (uint32_t)(i * 32 + j));
     }
-    // then the places in order: flat index and softmax weight (the place's
-    // sum is V[r]), written as whole vectors when the row holds KL
-    const float inv_z = 1.0f / z;
-    auto flat = [&](int r) {
-      const int pc = (int)so[r * kThreads + t];
-      return (int64_t)(col1(pc >> 5) * n + col2(pc & 31));
-    };
-    if (k == KL) {
-#pragma unroll
-      for (int r = 0; r < KL; r += 4) {
-        reinterpret_cast<longlong2*>(ip + r)[0] = make_longlong2(flat(r), flat(r + 1));
-        reinterpret_cast<longlong2*>(ip + r)[1] = make_longlong2(flat(r + 2), flat(r + 3));
-        reinterpret_cast<float4*>(wp + r)[0] =
-            make_float4(expf(V[r] - V[0]) * inv_z, expf(V[r + 1] - V[0]) * inv_z,
-                        expf(V[r + 2] - V[0]) * inv_z, expf(V[r + 3] - V[0]) * inv_z);
+  }
+  // Each survivor's output place is the number of larger sums, plus, for a
+  // sum that occurs more than once (dup bit set at that place), the number
+  // of equal survivors with a lower flat index; its pair code goes to that
+  // place's slot of this thread's column.
+#pragma unroll 2
+  for (int e = 0; e < KL; ++e) {
+    if (e < (int)placed) {
+      const float s = sv[e * kThreads + t];
+      const uint32_t pc = sp[e * kThreads + t];
+      int place = count_greater<KL>(V, s);
+      if ((dup >> place) & 1u) {
+        const int64_t f = flat_of(pc);
+#pragma unroll 1
+        for (int e2 = 0; e2 < (int)placed; ++e2)
+          place += sv[e2 * kThreads + t] == s && flat_of(sp[e2 * kThreads + t]) < f;
       }
-    } else {
-#pragma unroll
-      for (int r = 0; r < KL; ++r) {
-        if (r < k) {
-          ip[r] = flat(r);
-          wp[r] = expf(V[r] - V[0]) * inv_z;
+      so[place * kThreads + t] = pc;
+    }
+  }
+  if ((int)placed < k) {
+    // the places left (sum x each) in flat index order: per place, a scan for
+    // the lowest flat index above the previous place's among the pairs at x
+    int64_t last = -1;
+#pragma unroll 1
+    for (int r = (int)placed; r < k; ++r) {
+      int64_t best = INT64_MAX;
+      uint32_t bc = 0;
+#pragma unroll 1
+      for (int i = 0; i < KL; ++i) {
+        const float xi = v1[i];
+#pragma unroll 1
+        for (int j = 0; (i + 1) * (j + 1) <= KL; ++j) {
+          if (xi + v1[KL + j] == x) {
+            const uint32_t pc = (uint32_t)(i * 32 + j);
+            const int64_t f = flat_of(pc);
+            if (f > last && f < best) {
+              best = f;
+              bc = pc;
+            }
+          }
         }
       }
+      so[r * kThreads + t] = bc;
+      last = best;
     }
-    return;
   }
-  // frontier walk (exact ties): row i of the candidate grid is sorted, the
-  // next winner is the best of the rows' heads, (score desc, flat asc)
-  float fv[KL];
-  int ff[KL], fp[KL];
+  // then the places in order: flat index and softmax weight (the place's sum
+  // is V[r]), written as whole vectors when the row holds KL
+  const float inv_z = 1.0f / z;
+  auto flat = [&](int r) { return flat_of(so[r * kThreads + t]); };
+  if (k == KL) {
 #pragma unroll
-  for (int i = 0; i < KL; ++i) {
-    fv[i] = s1v[i] + s2v[0];
-    ff[i] = col1(i) * n + col2(0);
-    fp[i] = 0;
-  }
-#pragma unroll 1
-  for (int r = 0; r < k; ++r) {
-    float bv = fv[0];
-    int bf = ff[0], bi = 0, bp = fp[0];
-#pragma unroll
-    for (int i = 1; i < KL; ++i) {
-      const bool better = fv[i] > bv || (fv[i] == bv && ff[i] < bf);
-      bv = better ? fv[i] : bv;
-      bf = better ? ff[i] : bf;
-      bi = better ? i : bi;
-      bp = better ? fp[i] : bp;
+    for (int r = 0; r < KL; r += 4) {
+      reinterpret_cast<longlong2*>(ip + r)[0] = make_longlong2(flat(r), flat(r + 1));
+      reinterpret_cast<longlong2*>(ip + r)[1] = make_longlong2(flat(r + 2), flat(r + 3));
+      reinterpret_cast<float4*>(wp + r)[0] =
+          make_float4(expf(V[r] - V[0]) * inv_z, expf(V[r + 1] - V[0]) * inv_z,
+                      expf(V[r + 2] - V[0]) * inv_z, expf(V[r + 3] - V[0]) * inv_z);
     }
-    ip[r] = (int64_t)bf;
-    wp[r] = expf(bv - V[0]) / z;
-    const int np = bp + 1;
-    float nv = -INFINITY;
-    int nf = 0;
-    if (np < KL) {
-      nv = v1[bi] + v1[KL + np];
-      nf = col1(bi) * n + col2(np);
-    }
+  } else {
 #pragma unroll
-    for (int i = 0; i < KL; ++i) {
-      if (i == bi) {
-        fv[i] = nv;
-        ff[i] = nf;
-        fp[i] = np;
+    for (int r = 0; r < KL; ++r) {
+      if (r < k) {
+        ip[r] = flat(r);
+        wp[r] = expf(V[r] - V[0]) * inv_z;
       }
     }
   }
@@ -311,17 +346,16 @@ __device__ __forceinline__ void merge_cta(const float* __restrict__ list_v,
 // persistent grid walks the listed units (none listed: every CTA returns at
 // once).
 template <int KL>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 3)
 merge_kernel(const float* __restrict__ list_v, const unsigned short* __restrict__ list_c, int B,
              int H, int n, int k, int64_t* __restrict__ idx, float* __restrict__ w,
              RetryScratch retry, bool retry_pass) {
-  if (!retry_pass) {
-    merge_cta<KL>(list_v, list_c, B, H, n, k, idx, w, retry, false, (int)blockIdx.x);
-    return;
-  }
-  const int listed = retry.counts[1];
-  for (int u = (int)blockIdx.x; u < listed; u += (int)gridDim.x) {
-    merge_cta<KL>(list_v, list_c, B, H, n, k, idx, w, retry, true, u);
+  // one call site: a single inlined copy of the per-pair code serves both
+  // passes (the code is long and runs once per warp, so its size is fetch
+  // time)
+  const int end = retry_pass ? retry.counts[1] : (int)blockIdx.x + 1;
+  for (int u = (int)blockIdx.x; u < end; u += (int)gridDim.x) {
+    merge_cta<KL>(list_v, list_c, B, H, n, k, idx, w, retry, retry_pass, u);
     __syncthreads();  // the CTA's shared-memory columns are reused by its next unit
   }
 }
