@@ -50,13 +50,17 @@ struct MergeLayout {
   static constexpr int kRestBlock = kRest <= 2 ? 2 : kRest <= 4 ? 4 : kRest <= 8 ? 8 : 16;
   static_assert(kRest >= 1 && kRest <= 16, "merge: pairs outside the sorted runs");
   // region A, 4-byte slots in [slot][thread] order: the scores of the pairs
-  // outside the runs staged for folding (slots [0, kRest)), later the survivors' scores
-  // (slots [0, KL)) and pair codes (slots [KL, 2KL)).  Every use keeps a
-  // thread inside its own column, so warps in different phases never touch
-  // each other's slots.
+  // outside the runs staged for folding (slots [0, kRest)), later the
+  // survivors' scores (slots [0, kSurvCap)) and pair codes (slots
+  // [kSurvCap, 2 kSurvCap)).  Every use keeps a thread inside its own
+  // column, so warps in different phases never touch each other's slots.
   // First, in the first pass, it holds the CTA's lists as loaded, [pair][2KL
   // + 4] floats (rows 16-byte aligned; the +4 spreads rows over banks).
   static constexpr int kSlotsA = kRest > 2 * KL + 4 ? kRest : 2 * KL + 4;
+  // survivors held (scores and codes): KL and two more, so a tie at the KL-th
+  // sum that brings one or two more pairs is resolved from the store
+  static constexpr int kSurvCap = KL + 2;
+  static_assert(2 * kSurvCap <= kSlotsA, "merge: survivor store");
   static constexpr int kRegionA = kSlotsA * 4 * kThreads;
   // the lists' subkeys, [pair][2KL + 2] 16-bit (odd word stride: a thread's
   // own row and the cooperative fill are both free of bank conflicts)
@@ -78,8 +82,9 @@ __device__ __forceinline__ void merge_cta(const float* __restrict__ list_v,
   constexpr MergePairs<KL> P{};
   extern __shared__ __align__(16) unsigned char smem[];
   float* stg = reinterpret_cast<float*>(smem);                                  // [kRest][T]
-  float* sv = reinterpret_cast<float*>(smem);                                   // [KL][T]
-  uint32_t* sp = reinterpret_cast<uint32_t*>(sv + KL * kThreads);               // [KL][T]
+  constexpr int kCap = Lay::kSurvCap;
+  float* sv = reinterpret_cast<float*>(smem);                                   // [kCap][T]
+  uint32_t* sp = reinterpret_cast<uint32_t*>(sv + kCap * kThreads);             // [kCap][T]
   unsigned short* sc = reinterpret_cast<unsigned short*>(smem + Lay::kRegionA); // [T][2KL+2]
   uint32_t* so = reinterpret_cast<uint32_t*>(smem + Lay::kRegionC);             // [KL][T]
   const int t = threadIdx.x;
@@ -235,17 +240,18 @@ __device__ __forceinline__ void merge_cta(const float* __restrict__ list_v,
   uint32_t dup = 0;
 #pragma unroll
   for (int i = 0; i + 1 < KL; ++i) dup |= (V[i] == V[i + 1] ? 1u : 0u) << i;
-  // survivors: pairs scoring >= x; more than KL of them means a tie at x
-  // (region A is free again: the staged scores were all folded)
+  // survivors: pairs scoring >= x, the first kCap of them held; more than KL
+  // of them means a tie at x (region A is free again: the staged scores were
+  // all folded)
   const uint32_t va0 = static_cast<uint32_t>(__cvta_generic_to_shared(sv + t));
-  const uint32_t va_end = va0 + KL * (kThreads * 4);
+  const uint32_t va_end = va0 + kCap * (kThreads * 4);
   uint32_t va = va0, nsurv = 0;
   const float below_x = nextafterf(x, -INFINITY);  // >= x  <=>  > below_x
 #pragma unroll
   for (int c = 0; c < P.kCount; ++c) {
     const float s = s1v[P.i[c]] + s2v[P.j[c]];
-    surv_push<kThreads * 4, KL * kThreads * 4>(va, nsurv, va_end, s, below_x,
-                                               (uint32_t)(P.i[c] * 32 + P.j[c]));
+    surv_push<kThreads * 4, kCap * kThreads * 4>(va, nsurv, va_end, s, below_x,
+                                                 (uint32_t)(P.i[c] * 32 + P.j[c]));
   }
   if (!valid) return;
   float z = 0.0f;
@@ -255,48 +261,52 @@ __device__ __forceinline__ void merge_cta(const float* __restrict__ list_v,
   int64_t* ip = idx + (size_t)pair * k;
   float* wp = w + (size_t)pair * k;
   auto flat_of = [&](uint32_t pc) { return (int64_t)col1((int)(pc >> 5)) * n + col2((int)(pc & 31)); };
-  uint32_t placed = nsurv;  // survivors placed by value
-  if (nsurv != (uint32_t)KL) {
-    // a tie at the KL-th sum x: more than KL pairs reach it.  The pairs above
-    // x (fewer than KL) are placed by value below; those at x take the
-    // remaining places in flat index order after them.  Rare: plain loops
-    // over the lists in global memory keep this code small.
+  uint32_t held = nsurv < (uint32_t)kCap ? nsurv : (uint32_t)kCap;
+  // a tie at x (more than KL pairs reach it): the pairs at x are ranked by
+  // flat index after the larger sums, and those ranked KL or later dropped
+  bool cut = nsurv > (uint32_t)KL;
+  if (nsurv > (uint32_t)kCap) {
+    // more pairs at x than the store holds: hold the pairs above x only
+    // (fewer than KL) and fill the places left after them below.  Rare:
+    // plain loops over the lists in global memory keep this code small.
     uint32_t va2 = va0;
-    placed = 0;
+    held = 0;
+    cut = false;
 #pragma unroll 1
     for (int i = 0; i < KL; ++i) {
       const float xi = v1[i];
 #pragma unroll 1
       for (int j = 0; (i + 1) * (j + 1) <= KL; ++j)
-        surv_push<kThreads * 4, KL * kThreads * 4>(va2, placed, va_end, xi + v1[KL + j], x,
-                                                   (uint32_t)(i * 32 + j));
+        surv_push<kThreads * 4, kCap * kThreads * 4>(va2, held, va_end, xi + v1[KL + j], x,
+                                                     (uint32_t)(i * 32 + j));
     }
   }
-  // Each survivor's output place is the number of larger sums, plus, for a
-  // sum that occurs more than once (dup bit set at that place), the number
-  // of equal survivors with a lower flat index; its pair code goes to that
-  // place's slot of this thread's column.
+  // Each held survivor's output place is the number of larger sums, plus,
+  // for a sum that occurs more than once (dup bit set at that place, or a
+  // sum at x cut by the tie), the number of equal held survivors with a
+  // lower flat index; its pair code goes to that place's slot of this
+  // thread's column.
 #pragma unroll 2
-  for (int e = 0; e < KL; ++e) {
-    if (e < (int)placed) {
+  for (int e = 0; e < kCap; ++e) {
+    if (e < (int)held) {
       const float s = sv[e * kThreads + t];
       const uint32_t pc = sp[e * kThreads + t];
       int place = count_greater<KL>(V, s);
-      if ((dup >> place) & 1u) {
+      if (((dup >> place) & 1u) || (cut && s == x)) {
         const int64_t f = flat_of(pc);
 #pragma unroll 1
-        for (int e2 = 0; e2 < (int)placed; ++e2)
+        for (int e2 = 0; e2 < (int)held; ++e2)
           place += sv[e2 * kThreads + t] == s && flat_of(sp[e2 * kThreads + t]) < f;
       }
-      so[place * kThreads + t] = pc;
+      if (place < KL) so[place * kThreads + t] = pc;
     }
   }
-  if ((int)placed < k) {
+  if (nsurv > (uint32_t)kCap && (int)held < k) {
     // the places left (sum x each) in flat index order: per place, a scan for
     // the lowest flat index above the previous place's among the pairs at x
     int64_t last = -1;
 #pragma unroll 1
-    for (int r = (int)placed; r < k; ++r) {
+    for (int r = (int)held; r < k; ++r) {
       int64_t best = INT64_MAX;
       uint32_t bc = 0;
 #pragma unroll 1

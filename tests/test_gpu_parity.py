@@ -258,6 +258,52 @@ def test_exact_integer_ties_many_chunks(form):
         assert (np.abs(w - ref["w"]) <= 1e-6 * (1 + ref["w"])).all(), z
 
 
+def test_merge_ties_inside_and_at_the_cut_bit_exact():
+    # Equal pair sums inside the best k, and at the k-th sum with one or two
+    # and with many more pairs reaching it.  Each query's half scores are an
+    # integer column pair of the subkeys, 16 c[2m] + c[2m+1] (exact in bf16
+    # and fp32), and the 1024 queries take every pair of columns of the two
+    # halves.  The order of equal sums (lower flat index first) and the pairs
+    # kept at the cut must match the oracle bit for bit.
+    rng = np.random.default_rng(21)
+    B, H, n, hd, d_v, k = 1024, 1, 64, 64, 32, 32
+    d_q = 2 * hd
+    Cf = np.zeros((H, 2, n, hd), np.float32)
+    for hf in range(2):
+        for m in range(hd // 2):
+            spread = (2, 8, 40, 127)[m % 4]  # narrow spreads tie often
+            Cf[0, hf, :, 2 * m] = rng.integers(-spread, spread + 1, n)
+            Cf[0, hf, :, 2 * m + 1] = rng.integers(-127, 128, n)
+    qf = np.zeros((B, H, d_q), np.float32)
+    for b in range(B):
+        m1, m2 = divmod(b, hd // 2)
+        qf[b, 0, 2 * m1], qf[b, 0, 2 * m1 + 1] = 16, 1
+        qf[b, 0, hd + 2 * m2], qf[b, 0, hd + 2 * m2 + 1] = 16, 1
+    # coverage: how many pairs reach the k-th sum of the pruned candidate grid
+    kinds = {"distinct": 0, "equal inside": 0, "cut by one or two": 0, "cut by more": 0}
+    cand = [(i, j) for i in range(k) for j in range(k) if (i + 1) * (j + 1) <= k]
+    ci, cj = np.array(cand).T
+    for b in range(B):
+        m1, m2 = divmod(b, hd // 2)
+        s1 = 16 * Cf[0, 0, :, 2 * m1] + Cf[0, 0, :, 2 * m1 + 1]
+        s2 = 16 * Cf[0, 1, :, 2 * m2] + Cf[0, 1, :, 2 * m2 + 1]
+        X = s1[np.lexsort((np.arange(n), -s1))[:k]]
+        Y = s2[np.lexsort((np.arange(n), -s2))[:k]]
+        S = X[ci] + Y[cj]
+        top = -np.sort(-S)[:k]
+        reach = int((S >= top[-1]).sum())
+        kinds["cut by more" if reach > k + 2 else "cut by one or two" if reach > k else
+              "equal inside" if (top[1:] == top[:-1]).any() else "distinct"] += 1
+    assert min(kinds.values()) >= 10, kinds
+    Vf = rng.standard_normal((n * n, d_v)).astype(np.float32)
+    q, C, V = synth.f32_to_bf16(qf), synth.f32_to_bf16(Cf), synth.f32_to_bf16(Vf)
+    c = dict(B=B, H=H, d_q=d_q, n_keys=n, d_v=d_v, k=k, dtype="bf16")
+    _, idx, w = run_forward(c, q.ravel(), C.ravel(), V.ravel())
+    ref = oracle.lookup(q.ravel(), C.ravel(), B, H, d_q, n, k)
+    assert np.array_equal(idx, ref["idx"])
+    assert (np.abs(w - ref["w"]) <= 1e-6 * (1 + ref["w"])).all()
+
+
 def test_gather_alone_fed_oracle_selection():
     # Step a6 in isolation: oracle indices and weights in, fp64 read out.
     for name in ("tiny", "mid"):
