@@ -114,24 +114,28 @@ __device__ __forceinline__ void merge_cta(const float* __restrict__ list_v,
     constexpr int kRowV = 2 * KL + 4;
     const int pair0 = cta * kThreads;
     const int np = min(kThreads, B * H - pair0);
+    // asynchronous copies (no registers held), all in flight before the wait
+    const uint32_t st0 = static_cast<uint32_t>(__cvta_generic_to_shared(stg));
+    const uint32_t sc0 = static_cast<uint32_t>(__cvta_generic_to_shared(sc));
     const float4* gv = reinterpret_cast<const float4*>(list_v + (size_t)pair0 * 2 * KL);
 #pragma unroll 4
     for (int q = t; q < np * (KL / 2); q += kThreads) {
       const int p = q / (KL / 2), s4 = q - p * (KL / 2);
-      *reinterpret_cast<float4*>(stg + p * kRowV + 4 * s4) = gv[q];
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                       st0 + (uint32_t)(p * kRowV + 4 * s4) * 4u),
+                   "l"(gv + q)
+                   : "memory");
     }
-    const uint4* gc = reinterpret_cast<const uint4*>(list_c + (size_t)pair0 * 2 * KL);
-    uint32_t* sc32 = reinterpret_cast<uint32_t*>(sc);
+    const uint32_t* gc = reinterpret_cast<const uint32_t*>(list_c + (size_t)pair0 * 2 * KL);
 #pragma unroll 4
-    for (int q = t; q < np * (KL / 4); q += kThreads) {
-      const int p = q / (KL / 4), m = q - p * (KL / 4);
-      const uint4 u = gc[q];
-      uint32_t* d = sc32 + p * (Lay::kCodeRow / 2) + 4 * m;
-      d[0] = u.x;
-      d[1] = u.y;
-      d[2] = u.z;
-      d[3] = u.w;
+    for (int q = t; q < np * KL; q += kThreads) {  // KL words (2 KL codes) per pair
+      const int p = q / KL, m = q - p * KL;
+      asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
+                       sc0 + (uint32_t)(p * (Lay::kCodeRow / 2) + m) * 4u),
+                   "l"(gc + q)
+                   : "memory");
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
     const float4* r4 = reinterpret_cast<const float4*>(stg + t * kRowV);
 #pragma unroll
@@ -253,11 +257,11 @@ __device__ __forceinline__ void merge_cta(const float* __restrict__ list_v,
     surv_push<kThreads * 4, kCap * kThreads * 4>(va, nsurv, va_end, s, below_x,
                                                  (uint32_t)(P.i[c] * 32 + P.j[c]));
   }
+  // the warp's vote for the equal-sum pass below, taken while every lane is
+  // still here (lanes without a pair leave at the next line and wait at the
+  // caller's barrier)
+  const bool any_equal = __any_sync(0xffffffffu, valid && (dup != 0u || nsurv > (uint32_t)KL));
   if (!valid) return;
-  float z = 0.0f;
-#pragma unroll
-  for (int r = 0; r < KL; ++r)
-    if (r < k) z += expf(V[r] - V[0]);
   int64_t* ip = idx + (size_t)pair * k;
   float* wp = w + (size_t)pair * k;
   auto flat_of = [&](uint32_t pc) { return (int64_t)col1((int)(pc >> 5)) * n + col2((int)(pc & 31)); };
@@ -281,24 +285,35 @@ __device__ __forceinline__ void merge_cta(const float* __restrict__ list_v,
                                                      (uint32_t)(i * 32 + j));
     }
   }
-  // Each held survivor's output place is the number of larger sums, plus,
-  // for a sum that occurs more than once (dup bit set at that place, or a
-  // sum at x cut by the tie), the number of equal held survivors with a
-  // lower flat index; its pair code goes to that place's slot of this
-  // thread's column.
-#pragma unroll 2
+  // Each held survivor's output place is the number of larger sums (its
+  // pair code goes to that place's slot of this thread's column); branch
+  // free, several survivors in flight.
+#pragma unroll 4
   for (int e = 0; e < kCap; ++e) {
-    if (e < (int)held) {
+    const float s = sv[e * kThreads + t];
+    const uint32_t pc = sp[e * kThreads + t];
+    const int place = count_greater<KL>(V, s);
+    if (e < (int)held && place < KL) so[place * kThreads + t] = pc;
+    // kept beside the code (bits 16 and up) for the equal-sum pass
+    if (any_equal && e < (int)held) sp[e * kThreads + t] = pc | ((uint32_t)place << 16);
+  }
+  // A sum that occurs more than once (dup bit set at its place, or a sum at
+  // x cut by the tie) moves up by the number of equal held survivors with a
+  // lower flat index (the lowest keeps its place).  Rare: warps enter only
+  // when one of their rows has equal sums.
+  if (any_equal) {
+#pragma unroll 1
+    for (int e = 0; e < (int)held; ++e) {
       const float s = sv[e * kThreads + t];
-      const uint32_t pc = sp[e * kThreads + t];
-      int place = count_greater<KL>(V, s);
+      const uint32_t pc = sp[e * kThreads + t] & 0xffffu;
+      int place = (int)(sp[e * kThreads + t] >> 16);
       if (((dup >> place) & 1u) || (cut && s == x)) {
         const int64_t f = flat_of(pc);
 #pragma unroll 1
         for (int e2 = 0; e2 < (int)held; ++e2)
-          place += sv[e2 * kThreads + t] == s && flat_of(sp[e2 * kThreads + t]) < f;
+          place += sv[e2 * kThreads + t] == s && flat_of(sp[e2 * kThreads + t] & 0xffffu) < f;
+        if (place < KL) so[place * kThreads + t] = pc;
       }
-      if (place < KL) so[place * kThreads + t] = pc;
     }
   }
   if (nsurv > (uint32_t)kCap && (int)held < k) {
@@ -329,24 +344,31 @@ __device__ __forceinline__ void merge_cta(const float* __restrict__ list_v,
     }
   }
   // then the places in order: flat index and softmax weight (the place's sum
-  // is V[r]), written as whole vectors when the row holds KL
-  const float inv_z = 1.0f / z;
+  // is V[r]; the softmax over the first k, V[0] the largest), written as
+  // whole vectors when the row holds KL
+  float ex[KL];
+  float z4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+  for (int r = 0; r < KL; ++r) {
+    ex[r] = r < k ? expf(V[r] - V[0]) : 0.0f;
+    z4[r & 3] += ex[r];
+  }
+  const float inv_z = 1.0f / ((z4[0] + z4[1]) + (z4[2] + z4[3]));
   auto flat = [&](int r) { return flat_of(so[r * kThreads + t]); };
   if (k == KL) {
 #pragma unroll
     for (int r = 0; r < KL; r += 4) {
       reinterpret_cast<longlong2*>(ip + r)[0] = make_longlong2(flat(r), flat(r + 1));
       reinterpret_cast<longlong2*>(ip + r)[1] = make_longlong2(flat(r + 2), flat(r + 3));
-      reinterpret_cast<float4*>(wp + r)[0] =
-          make_float4(expf(V[r] - V[0]) * inv_z, expf(V[r + 1] - V[0]) * inv_z,
-                      expf(V[r + 2] - V[0]) * inv_z, expf(V[r + 3] - V[0]) * inv_z);
+      reinterpret_cast<float4*>(wp + r)[0] = make_float4(ex[r] * inv_z, ex[r + 1] * inv_z,
+                                                         ex[r + 2] * inv_z, ex[r + 3] * inv_z);
     }
   } else {
 #pragma unroll
     for (int r = 0; r < KL; ++r) {
       if (r < k) {
         ip[r] = flat(r);
-        wp[r] = expf(V[r] - V[0]) * inv_z;
+        wp[r] = ex[r] * inv_z;
       }
     }
   }
@@ -362,7 +384,8 @@ merge_kernel(const float* __restrict__ list_v, const unsigned short* __restrict_
              RetryScratch retry, bool retry_pass) {
   // one call site: a single inlined copy of the per-pair code serves both
   // passes (the code is long and runs once per warp, so its size is fetch
-  // time)
+  // time).  Lanes without a pair return from merge_cta early and wait at the
+  // barrier below, so merge_cta takes no warp vote after they leave.
   const int end = retry_pass ? retry.counts[1] : (int)blockIdx.x + 1;
   for (int u = (int)blockIdx.x; u < end; u += (int)gridDim.x) {
     merge_cta<KL>(list_v, list_c, B, H, n, k, idx, w, retry, retry_pass, u);
