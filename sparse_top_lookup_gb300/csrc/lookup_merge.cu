@@ -89,8 +89,8 @@ __device__ __forceinline__ void merge_cta(const float* __restrict__ list_v,
   uint32_t* so = reinterpret_cast<uint32_t*>(smem + Lay::kRegionC);             // [KL][T]
   const int t = threadIdx.x;
   int pair;
-  // every lane stays to the end (warp votes below); lanes without a pair of
-  // their own work on zeros and store nothing
+  // every lane stays until the last warp vote (below); lanes without a pair
+  // of their own work on zeros until then and store nothing
   bool valid;
   if (retry_pass) {
     const int tile = retry.unit_list[cta] >> 1;
@@ -107,10 +107,10 @@ __device__ __forceinline__ void merge_cta(const float* __restrict__ list_v,
   unsigned short* my_sc = sc + t * Lay::kCodeRow;
   float s1v[KL], s2v[KL];
   if (!retry_pass) {
-    // the CTA's pairs are consecutive, so are their lists: coalesced 16-byte
-    // loads by the whole CTA into shared memory, then each thread takes its
-    // own row (a thread's own lists are 256 + 128 scattered bytes apart from
-    // its neighbours')
+    // the CTA's pairs are consecutive, so are their lists: coalesced copies
+    // by the whole CTA into shared memory, then each thread takes its own row
+    // (a thread's own lists are 256 + 128 scattered bytes apart from its
+    // neighbours')
     constexpr int kRowV = 2 * KL + 4;
     const int pair0 = cta * kThreads;
     const int np = min(kThreads, B * H - pair0);
