@@ -27,7 +27,9 @@
 namespace pkm {
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 64;    // pairs (threads) per CTA
+constexpr int kTileRows = 128;  // queries per selection row tile (a retry unit's rows)
+constexpr int kSplit = kTileRows / kThreads;  // CTAs per retry unit
 
 int tc_sms() {
   int dev = 0, n = 0;
@@ -66,12 +68,13 @@ struct MergeLayout {
   // own row and the cooperative fill are both free of bank conflicts)
   static constexpr int kCodeRow = 2 * KL + 2;
   static constexpr int kRegionC = kRegionA + (kCodeRow * 2 * kThreads + 15) / 16 * 16;
-  // region C, [place][thread]: the survivors' pair codes by output place
-  static constexpr int kBytes = kRegionC + KL * 4 * kThreads;
+  // region C, [place][thread]: the survivors' pair codes (16-bit) by output
+  // place
+  static constexpr int kBytes = kRegionC + (KL * 2 * kThreads + 15) / 16 * 16;
 };
 
-// One CTA's pairs: first pass, pair = cta * 128 + thread; retry pass, listed
-// unit `cta` and thread t its row tile's query t.
+// One CTA's pairs: first pass, pair = cta * 64 + thread; retry pass, listed
+// unit cta / 2 and thread t its row tile's query 64 (cta % 2) + t.
 template <int KL>
 __device__ __forceinline__ void merge_cta(const float* __restrict__ list_v,
                                           const unsigned short* __restrict__ list_c, int B, int H,
@@ -86,16 +89,16 @@ __device__ __forceinline__ void merge_cta(const float* __restrict__ list_v,
   float* sv = reinterpret_cast<float*>(smem);                                   // [kCap][T]
   uint32_t* sp = reinterpret_cast<uint32_t*>(sv + kCap * kThreads);             // [kCap][T]
   unsigned short* sc = reinterpret_cast<unsigned short*>(smem + Lay::kRegionA); // [T][2KL+2]
-  uint32_t* so = reinterpret_cast<uint32_t*>(smem + Lay::kRegionC);             // [KL][T]
+  unsigned short* so = reinterpret_cast<unsigned short*>(smem + Lay::kRegionC); // [KL][T]
   const int t = threadIdx.x;
   int pair;
   // every lane stays until the last warp vote (below); lanes without a pair
   // of their own work on zeros until then and store nothing
   bool valid;
   if (retry_pass) {
-    const int tile = retry.unit_list[cta] >> 1;
+    const int tile = retry.unit_list[cta / kSplit] >> 1;
     const int rt = tile / H, h = tile - (tile / H) * H;
-    const int b = rt * kThreads + t;  // row tiles hold 128 queries, one per thread
+    const int b = rt * kTileRows + (cta % kSplit) * kThreads + t;
     valid = b < B;
     pair = valid ? b * H + h : 0;
   } else {
@@ -168,7 +171,7 @@ __device__ __forceinline__ void merge_cta(const float* __restrict__ list_v,
   if (valid && (bad1 || bad2) && !retry_pass) {  // without the hint every list is complete
     atomicAdd(&retry.counts[0], 1);
     const int b = pair / H, h = pair - (pair / H) * H;
-    const int unit0 = ((b / kThreads) * H + h) << 1;
+    const int unit0 = ((b / kTileRows) * H + h) << 1;
     for (int hf = 0; hf < 2; ++hf)
       if ((hf ? bad2 : bad1) && atomicExch(&retry.unit_flag[unit0 | hf], 1) == 0)
         retry.unit_list[atomicAdd(&retry.counts[1], 1)] = unit0 | hf;
@@ -293,7 +296,7 @@ __device__ __forceinline__ void merge_cta(const float* __restrict__ list_v,
     const float s = sv[e * kThreads + t];
     const uint32_t pc = sp[e * kThreads + t];
     const int place = count_greater<KL>(V, s);
-    if (e < (int)held && place < KL) so[place * kThreads + t] = pc;
+    if (e < (int)held && place < KL) so[place * kThreads + t] = (unsigned short)pc;
     // kept beside the code (bits 16 and up) for the equal-sum pass
     if (any_equal && e < (int)held) sp[e * kThreads + t] = pc | ((uint32_t)place << 16);
   }
@@ -312,7 +315,7 @@ __device__ __forceinline__ void merge_cta(const float* __restrict__ list_v,
 #pragma unroll 1
         for (int e2 = 0; e2 < (int)held; ++e2)
           place += sv[e2 * kThreads + t] == s && flat_of(sp[e2 * kThreads + t] & 0xffffu) < f;
-        if (place < KL) so[place * kThreads + t] = pc;
+        if (place < KL) so[place * kThreads + t] = (unsigned short)pc;
       }
     }
   }
@@ -339,7 +342,7 @@ __device__ __forceinline__ void merge_cta(const float* __restrict__ list_v,
           }
         }
       }
-      so[r * kThreads + t] = bc;
+      so[r * kThreads + t] = (unsigned short)bc;
       last = best;
     }
   }
@@ -374,11 +377,17 @@ __device__ __forceinline__ void merge_cta(const float* __restrict__ list_v,
   }
 }
 
-// First pass: CTA c merges pairs [128c, 128c + 128).  Retry pass: a
-// persistent grid walks the listed units (none listed: every CTA returns at
-// once).
+// First pass: CTA c merges pairs [64c, 64c + 64).  Retry pass: a persistent
+// grid walks the listed units, two CTA-sized halves each (none listed: every
+// CTA returns at once).
 template <int KL>
-__global__ void __launch_bounds__(kThreads, 3)
+// 128 registers: seven 64-thread CTAs per SM (14 warps; the register file is
+// split over the SM's four schedulers, 16,384 registers each, and a scheduler
+// holding four warps leaves 128 to each), so the page-size batch's 1024 CTAs
+// run in one wave; shared memory allows seven as well.  The cap spills a few
+// hundred bytes per thread; 144 registers would fit only three warps per
+// scheduler (two waves, slower).
+__global__ void __maxnreg__(128)
 merge_kernel(const float* __restrict__ list_v, const unsigned short* __restrict__ list_c, int B,
              int H, int n, int k, int64_t* __restrict__ idx, float* __restrict__ w,
              RetryScratch retry, bool retry_pass) {
@@ -386,7 +395,7 @@ merge_kernel(const float* __restrict__ list_v, const unsigned short* __restrict_
   // passes (the code is long and runs once per warp, so its size is fetch
   // time).  Lanes without a pair return from merge_cta early and wait at the
   // barrier below, so merge_cta takes no warp vote after they leave.
-  const int end = retry_pass ? retry.counts[1] : (int)blockIdx.x + 1;
+  const int end = retry_pass ? retry.counts[1] * kSplit : (int)blockIdx.x + 1;
   for (int u = (int)blockIdx.x; u < end; u += (int)gridDim.x) {
     merge_cta<KL>(list_v, list_c, B, H, n, k, idx, w, retry, retry_pass, u);
     __syncthreads();  // the CTA's shared-memory columns are reused by its next unit
@@ -403,10 +412,14 @@ cudaError_t launch_merge_kl(const float* list_v, const unsigned short* list_c, i
     cudaError_t e = cudaFuncSetAttribute(merge_kernel<KL>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
+    // seven CTAs per SM need the whole shared-memory carveout
+    e = cudaFuncSetAttribute(merge_kernel<KL>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
     attr_set = true;
   }
   const int64_t units = retry_units(B, H);
-  const int64_t grid = retry_pass ? (units < 2 * tc_sms() ? units : 2 * tc_sms())
+  const int64_t grid = retry_pass ? (units * kSplit < 7 * tc_sms() ? units * kSplit : 7 * tc_sms())
                                   : ((int64_t)B * H + kThreads - 1) / kThreads;
   merge_kernel<KL><<<(unsigned)grid, kThreads, smem, stream>>>(list_v, list_c, B, H, n, k, idx, w,
                                                                 retry, retry_pass);
@@ -415,7 +428,7 @@ cudaError_t launch_merge_kl(const float* list_v, const unsigned short* list_c, i
 
 }  // namespace
 
-int64_t retry_units(int64_t B, int64_t H) { return (B + kThreads - 1) / kThreads * H * 2; }
+int64_t retry_units(int64_t B, int64_t H) { return (B + kTileRows - 1) / kTileRows * H * 2; }
 
 cudaError_t launch_merge(const float* list_v, const unsigned short* list_c, int B, int H,
                          int n_keys, int k, int64_t* idx, float* w, const RetryScratch& retry,
