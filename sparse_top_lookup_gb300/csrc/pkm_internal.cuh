@@ -145,7 +145,8 @@ int list_slots(int k);
 // Steps a4-a5 from the per-half lists (lookup_merge.cu).  First pass: every
 // pair; pairs with a marked list are counted in retry.counts[0] and their
 // units listed.  Retry pass: the pairs of the units in
-// retry.unit_list[0 .. retry.counts[1]), one CTA per listed unit.
+// retry.unit_list[0 .. retry.counts[1]), two CTAs per listed unit (64
+// queries each).
 cudaError_t launch_merge(const float* list_v, const unsigned short* list_c, int B, int H,
                          int n_keys, int k, int64_t* idx, float* w, const RetryScratch& retry,
                          bool retry_pass, cudaStream_t stream);
