@@ -9,7 +9,8 @@
 // The lists come from the selection kernel, each ordered by (score desc,
 // subkey asc).  Only pairs (i, j) with (i + 1)(j + 1) <= KL can reach the top
 // KL (every (i', j') with i' <= i, j' <= j scores at least as much).  Their
-// sums go through value-only sorting networks to the sorted KL best sums V;
+// sums reach the sorted KL best sums V through value-only bitonic merges of
+// the grid's sorted runs (its first rows and columns) and one small fold;
 // each surviving pair's output slot is the number of larger sums (equal sums
 // in flat index order) and its softmax weight follows from V.  When more
 // than KL pairs reach the KL-th sum x (a tie at the cut), the pairs above x
