@@ -144,6 +144,35 @@ def test_query_net_rejects_bad_arguments_before_any_cuda_call(L):
     assert L.pkm_bn_fold(16, 16, 16, 16, 1e-5, 0, 16, 16, None) == pk.PKM_ERR_INVALID
 
 
+def test_query_net_batch_rejects_bad_arguments_before_any_cuda_call(L):
+    Q = L.pkm_query_net_batch
+    args = lambda x=16, w=16, B=4, dim=64, F=64, eps=1e-5, ws=16, q=16: \
+        Q(x, w, B, dim, F, 16, 16, eps, ws, q, None, None, None, None)
+    assert args(B=-1) == pk.PKM_ERR_INVALID
+    assert args(dim=0) == pk.PKM_ERR_INVALID
+    assert args(eps=-1.0) == pk.PKM_ERR_INVALID
+    assert args(eps=float("nan")) == pk.PKM_ERR_INVALID
+    assert args(dim=72) == pk.PKM_ERR_UNSUPPORTED  # dim % 16
+    assert args(F=48) == pk.PKM_ERR_UNSUPPORTED    # F % 32
+    assert args(B=0) == pk.PKM_OK
+    assert args(x=None) == pk.PKM_ERR_INVALID
+    assert args(ws=None) == pk.PKM_ERR_INVALID
+    assert args(x=8) == pk.PKM_ERR_ALIGN
+    assert args(ws=8) == pk.PKM_ERR_ALIGN
+    # workspace: per-32-row-block sums and squares of every feature, then the
+    # joined mean and variance, each region 256-byte aligned
+    W = L.pkm_query_net_batch_workspace_bytes
+    assert W(-1, 64) == 0 and W(4, 0) == 0
+    assert W(32, 64) == 2 * 256 + 2 * 256
+    assert W(33, 1024) == 2 * (2 * 1024 * 4) + 2 * (1024 * 4)
+    assert W(4096, 1024) >= 2 * 128 * 1024 * 4
+
+
+def test_flat_entry_points_reject_null_handle_before_any_cuda_call(L):
+    assert L.pkm_full_keys(None, 16, 1, 16, 16, None) == pk.PKM_ERR_INVALID
+    assert L.pkm_flat_lookup(None, 16, 16, 1, 1, 16, 1, 16, 16, None) == pk.PKM_ERR_INVALID
+
+
 def test_product_path_refuses_without_library(monkeypatch, tmp_path):
     # No CPU fallback: a missing libpkm.so is an import-time error.
     monkeypatch.setattr(pk, "LIB_PATH", str(tmp_path / "missing.so"))
