@@ -208,6 +208,20 @@ def test_one_set_selection_exact_for_any_threshold_hint(z):
         assert info["fallback"] == 0
 
 
+@pytest.mark.parametrize("z", [1e30, 1.86])
+def test_short_lists_exact_for_any_threshold_hint(z):
+    # k <= 16 (16-entry per-half lists, the merge's KL = 16 form) with every
+    # row retried (huge z) or about half of them (z = 1.86 puts about 16 of
+    # the 512 scores above the hint), on a batch that ends inside a row tile
+    # (200 = 128 + 72: the retry pass's two CTAs of the last unit, one partly
+    # and one wholly past the batch)
+    c, q, C, V = random_case(123, 200, 3, 256, 512, 64, 12)
+    info = {}
+    check_against_oracle(c, q, C, V, hint_z=z, report=info)
+    if z == 1e30:
+        assert info["fallback"] == c["B"] * c["H"]
+
+
 def test_fp32_shapes():
     c, q, C, V = random_case(7, 33, 3, 48, 40, 32, 12, dtype="f32", kvar=1.0)
     check_against_oracle(c, q, C, V)
